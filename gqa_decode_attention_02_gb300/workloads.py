@@ -1,0 +1,231 @@
+"""Seeded synthetic inputs for paged GQA decode / verify attention.
+
+This module is shared by the tests, the bench and the CPU oracle's callers.  It
+holds no arithmetic of the method itself (no scores, softmax, argmax or slot
+arithmetic beyond laying out the block pool): it draws random numbers, lays out
+a paged block pool and fills unused cache slots with NaN sentinels, so that any
+read of a slot outside a sequence's context poisons the result.
+
+Value recipe: every element is drawn as fp32 N(0,1) from a torch.Generator seeded
+per workload and rounded (round-to-nearest-even) to the workload dtype.  Unused
+cache slots hold NaN; unused block-table entries hold INT32_MAX.
+
+The five named workloads follow the shapes of the pages' own running examples:
+the 24-layer, 14-query-head, 2-KV-head, H=64 fp16 model measured on page "جعل
+inference رخيصًا: KV cache وbatching والتكميم", a Llama-style N=32/K=8/H=128
+bf16 geometry, and a 4-draft speculative-verify batch (page "Болжау арқылы Sonar
+модельдерін жылдамдату").
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+INT32_MAX = 2**31 - 1
+BLOCK_SIZE = 16
+
+_TORCH_DT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    B: int
+    T: int
+    N: int
+    K: int
+    H: int
+    dtype: str  # "f16" | "bf16"
+    layers: int
+    block_size: int
+    num_blocks: int
+    max_blocks: int
+    context_lens: torch.Tensor  # int32 [B]
+    block_tables: torch.Tensor  # int32 [B, max_blocks]
+    q: list  # per layer [B,T,N,H]
+    k_cache: list  # per layer [NB,bs,K,H]
+    v_cache: list
+    k_new: list  # per layer [B,T,K,H] (the T tokens the append writes)
+    v_new: list
+    appended: bool  # True: the caches do NOT yet hold the T new tokens (NaN there)
+    logits: Optional[torch.Tensor] = None  # fp32 [B,T,V] (verify workloads)
+    draft: Optional[torch.Tensor] = None  # int32 [B,T-1]
+    draft_k: Optional[np.ndarray] = None  # planted accepted-prefix length per b
+    desc: str = ""
+
+    @property
+    def G(self) -> int:
+        return self.N // self.K
+
+    @property
+    def torch_dtype(self):
+        return _TORCH_DT[self.dtype]
+
+
+def _randn_into(out: torch.Tensor, gen: torch.Generator, chunk_elems: int = 1 << 26):
+    """Fill `out` (fp16/bf16, any device) with N(0,1) rounded to its dtype,
+    drawing fp32 in chunks so big caches never need an fp32 copy."""
+    flat = out.view(-1)
+    n = flat.numel()
+    for s in range(0, n, chunk_elems):
+        e = min(n, s + chunk_elems)
+        flat[s:e] = torch.randn(e - s, generator=gen, dtype=torch.float32,
+                                device=out.device).to(out.dtype)
+
+
+def context_lengths(kind: str, B: int, rng: np.random.Generator, *args) -> np.ndarray:
+    """Context-length mixes of the workloads (tokens held per sequence, including
+    the new ones).  fixed(c); uniform(lo, hi) inclusive; lognormal(median, sigma,
+    lo, hi): ln c ~ N(ln median, sigma^2), rounded to nearest, clipped."""
+    if kind == "fixed":
+        return np.full(B, int(args[0]), np.int64)
+    if kind == "uniform":
+        lo, hi = args
+        return rng.integers(lo, hi + 1, size=B)
+    if kind == "lognormal":
+        median, sigma, lo, hi = args
+        x = np.rint(np.exp(rng.normal(math.log(median), sigma, size=B)))
+        return np.clip(x, lo, hi).astype(np.int64)
+    raise ValueError(kind)
+
+
+def build(name: str, B: int, T: int, N: int, K: int, H: int, dtype: str,
+          ctx: np.ndarray, *, seed: int, layers: int = 1, shuffle: bool = True,
+          append: bool = True, spare_blocks: int = 1, block_size: int = BLOCK_SIZE,
+          max_blocks: Optional[int] = None, device="cpu", vocab: int = 0,
+          desc: str = "") -> Workload:
+    """Lay out a paged block pool for the given context lengths and fill it.
+
+    Physical blocks: sum_b ceil(ctx_b / bs) in use plus `spare_blocks` never
+    referenced; ids are a random permutation of the pool when `shuffle`, else
+    0,1,2,... in sequence order.  When `append` is set, the T newest positions
+    of each sequence are left as NaN in the cache (the append fills them)."""
+    assert N % K == 0
+    gen = torch.Generator(device=device).manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    ctx = np.asarray(ctx, np.int64)
+    nblk = (ctx + block_size - 1) // block_size
+    used = int(nblk.sum())
+    NB = used + spare_blocks
+    if max_blocks is None:
+        max_blocks = max(1, int(nblk.max()) if B else 1)
+    ids = rng.permutation(NB) if shuffle else np.arange(NB)
+    tables = np.full((B, max_blocks), INT32_MAX, np.int64)
+    off = 0
+    for b in range(B):
+        tables[b, : nblk[b]] = ids[off: off + nblk[b]]
+        off += nblk[b]
+    tdt = _TORCH_DT[dtype]
+    nan_slots = []  # (block, row) pairs that must hold NaN
+    for b in range(B):
+        first_nan = ctx[b] - T if append else ctx[b]
+        first_nan = max(first_nan, 0)
+        for pos in range(first_nan, nblk[b] * block_size):
+            nan_slots.append((tables[b, pos // block_size], pos % block_size))
+    spare = ids[used:]
+
+    qs, kcs, vcs, kns, vns = [], [], [], [], []
+    for _ in range(layers):
+        q = torch.empty((B, T, N, H), dtype=tdt, device=device)
+        kc = torch.empty((NB, block_size, K, H), dtype=tdt, device=device)
+        vc = torch.empty_like(kc)
+        kn = torch.empty((B, T, K, H), dtype=tdt, device=device)
+        vn = torch.empty_like(kn)
+        for t_ in (q, kc, vc, kn, vn):
+            _randn_into(t_, gen)
+        if nan_slots:
+            sl = torch.as_tensor(np.array(nan_slots, np.int64), device=device)
+            kc[sl[:, 0], sl[:, 1]] = float("nan")
+            vc[sl[:, 0], sl[:, 1]] = float("nan")
+        if len(spare):
+            sp = torch.as_tensor(spare, device=device)
+            kc[sp] = float("nan")
+            vc[sp] = float("nan")
+        qs.append(q)
+        kcs.append(kc)
+        vcs.append(vc)
+        kns.append(kn)
+        vns.append(vn)
+
+    w = Workload(name=name, B=B, T=T, N=N, K=K, H=H, dtype=dtype, layers=layers,
+                 block_size=block_size, num_blocks=NB, max_blocks=max_blocks,
+                 context_lens=torch.as_tensor(ctx.astype(np.int32), device=device),
+                 block_tables=torch.as_tensor(tables.astype(np.int32), device=device),
+                 q=qs, k_cache=kcs, v_cache=vcs, k_new=kns, v_new=vns,
+                 appended=append, desc=desc)
+    if vocab:
+        logits = torch.randn((B, T, vocab), generator=gen, dtype=torch.float32,
+                             device=device)
+        # Drafts: the first k_b positions carry the target's choice by construction
+        # (a planted logit of 10.0, far above any N(0,1) draw of this size), the
+        # rest are uniform random ids.  The oracle, not this recipe, decides the
+        # accepted length.
+        kb = rng.integers(0, T, size=B)  # k uniform in 0..T-1
+        draft = rng.integers(0, vocab, size=(B, max(T - 1, 0)))
+        li = logits.cpu() if device != "cpu" else logits
+        for b in range(B):
+            for t in range(int(kb[b])):
+                li[b, t, int(draft[b, t])] = 10.0
+        if device != "cpu":
+            logits.copy_(li)
+        w.logits = logits
+        w.draft = torch.as_tensor(draft.astype(np.int32), device=device)
+        w.draft_k = kb
+    return w
+
+
+# The five workloads: (description, builder kwargs, context-length recipe, seed)
+SPECS = {
+    "cfg1": dict(
+        desc="single layer, B=1, T=1, N=14, K=2, H=64, fp16, context 295, "
+             "contiguous block table",
+        B=1, T=1, N=14, K=2, H=64, dtype="f16", layers=1, shuffle=False,
+        append=False, ctx=("fixed", 295), seed=101),
+    "cfg2": dict(
+        desc="24 layers back-to-back, B=64, T=1, N=14, K=2, H=64, fp16, context "
+             "U[16,1024], block tables a random permutation of a shared pool",
+        B=64, T=1, N=14, K=2, H=64, dtype="f16", layers=24, shuffle=True,
+        append=True, ctx=("uniform", 16, 1024), seed=102),
+    "cfg3": dict(
+        desc="single layer, B=32, T=1, N=32, K=8, H=128, bf16, context 8192 "
+             "(8191 cached + 1 appended), shuffled blocks",
+        B=32, T=1, N=32, K=8, H=128, dtype="bf16", layers=1, shuffle=True,
+        append=True, ctx=("fixed", 8192), seed=103),
+    "cfg4": dict(
+        desc="ragged batch, B=256, T=1, N=32, K=8, H=128, bf16, context "
+             "log-normal (median 2048, sigma 1.0) clipped to [1,32768], shuffled, "
+             "append 1 then decode",
+        B=256, T=1, N=32, K=8, H=128, dtype="bf16", layers=1, shuffle=True,
+        append=True, ctx=("lognormal", 2048, 1.0, 1, 32768), seed=104),
+    "cfg5": dict(
+        desc="speculative verify, B=16, T=5, N=64, K=8, H=128, bf16, context "
+             "U[512,4096], causal among the 5 new tokens; greedy acceptance over "
+             "fp32 logits [16,5,32000]",
+        B=16, T=5, N=64, K=8, H=128, dtype="bf16", layers=1, shuffle=True,
+        append=True, ctx=("uniform", 512, 4096), seed=105, vocab=32000),
+}
+
+
+def make(name: str, *, device="cpu", seed: Optional[int] = None,
+         B: Optional[int] = None, layers: Optional[int] = None,
+         append: Optional[bool] = None) -> Workload:
+    """One of the five named workloads (optionally with fewer sequences or
+    layers, for the oracle's bounded samples)."""
+    s = dict(SPECS[name])
+    seed = s.pop("seed") if seed is None else seed
+    s.pop("seed", None)
+    kind, *args = s.pop("ctx")
+    desc = s.pop("desc")
+    if B is not None:
+        s["B"] = B
+    if layers is not None:
+        s["layers"] = layers
+    if append is not None:
+        s["append"] = append
+    rng = np.random.default_rng(seed + 7919)
+    ctx = context_lengths(kind, s["B"], rng, *args)
+    return build(name, ctx=ctx, seed=seed, device=device, desc=desc, **s)

@@ -1,0 +1,18 @@
+"""fp64 CPU oracle for paged GQA decode/verify attention, KV append and greedy
+prefix acceptance.
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the bench's CPU
+baseline leg may import this package; the product path never does.  It shares no
+code with the CUDA library and does not import it.
+"""
+from .oracle import (  # noqa: F401
+    build,
+    f16_to_f64,
+    bf16_to_f64,
+    kv_append,
+    attention,
+    accept_prefix,
+    argmax,
+    num_threads,
+)
+from .recompute import causal_attention_full  # noqa: F401

@@ -1,0 +1,253 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for paged grouped-query decode / verify
+ * attention, the KV append that precedes it, and greedy prefix acceptance.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file: only the tests, the package's smoke check and the bench's CPU
+ * baseline leg do.  It shares no code, header or table with the CUDA kernels.
+ *
+ * Sources (web pages; cited by page title and section):
+ *   [CS336-RU]  "CS336, лекции 10 и 12: инференс и оценка моделей"
+ *   [KV-AR]     "جعل inference رخيصًا: KV cache وbatching والتكميم"
+ *   [SONAR-KK]  "Болжау арқылы Sonar модельдерін жылдамдату"
+ *
+ * Everything is written from the plain definitions, in fp64, one output element
+ * at a time; there is no tiling, no online softmax and no split of the context.
+ * Input elements (IEEE binary16 or bfloat16) are widened to double exactly.
+ *
+ * Notation follows [CS336-RU] §"Напоминание: трансформер": B sequences, T new
+ * query tokens per sequence, N query heads, K key/value heads, G = N/K, head
+ * size H.  Paged layout follows [CS336-RU] §"PagedAttention" (fixed-size blocks
+ * of tokens plus a per-sequence block table):
+ *   q            [B][T][N][H]
+ *   k/v cache    [num_blocks][block_size][K][H]
+ *   block_tables [B][max_blocks]   logical block i of sequence b -> physical id
+ *   context_lens [B]               tokens held for b, INCLUDING the T new ones
+ * (the last reading is ours: the pages define no such array.)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Per-sequence error codes written to seq_err (0 = fine).  Same meaning as the
+ * library's status codes of the same names, restated here on purpose. */
+#define ORACLE_ERR_CONTEXT 7  /* context length < T, <= 0 or beyond the table */
+#define ORACLE_ERR_BLOCK_ID 8 /* a needed block-table entry is not a valid block */
+
+/* ---- element widening (IEEE 754 binary16; bfloat16 = top half of binary32) ---- */
+
+double oracle_f16_to_f64(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24); /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m | 0x400), e - 25); /* (1.m) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+double oracle_bf16_to_f64(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double widen(uint16_t x, int dtype) {
+    return dtype == 0 ? oracle_f16_to_f64(x) : oracle_bf16_to_f64(x);
+}
+
+/* ---- KV append ------------------------------------------------------------
+ * [KV-AR], KV-cache section: each new token's key and value vectors are stored
+ * once and reused by every later step.  [CS336-RU] §"PagedAttention": logical
+ * position j of sequence b lives in physical block block_tables[b][j / bs] at
+ * row j % bs.  Token t of the T new ones sits at position ctx_b - T + t.
+ * A byte copy: the result must be bit-identical. */
+int oracle_kv_append(int B, int T, int K, int H, int block_size, int num_blocks,
+                     int max_blocks, const uint16_t *k_new, const uint16_t *v_new,
+                     uint16_t *k_cache, uint16_t *v_cache,
+                     const int32_t *block_tables, const int32_t *context_lens,
+                     int32_t *seq_err) {
+    int any = 0;
+    size_t row = (size_t)K * H; /* one token's K heads x H elements */
+    for (int b = 0; b < B; ++b) {
+        int ctx = context_lens[b];
+        if (seq_err) seq_err[b] = 0;
+        if (ctx < T || ctx > (long long)max_blocks * block_size) {
+            if (seq_err) seq_err[b] = ORACLE_ERR_CONTEXT;
+            any = 1;
+            continue;
+        }
+        for (int t = 0; t < T; ++t) {
+            int pos = ctx - T + t;
+            int blk = block_tables[(size_t)b * max_blocks + pos / block_size];
+            if (blk < 0 || blk >= num_blocks) {
+                if (seq_err && !seq_err[b]) seq_err[b] = ORACLE_ERR_BLOCK_ID;
+                any = 1;
+                continue;
+            }
+            size_t dst = ((size_t)blk * block_size + pos % block_size) * row;
+            size_t src = ((size_t)b * T + t) * row;
+            memcpy(k_cache + dst, k_new + src, row * sizeof(uint16_t));
+            memcpy(v_cache + dst, v_new + src, row * sizeof(uint16_t));
+        }
+    }
+    return any;
+}
+
+/* ---- attention -------------------------------------------------------------
+ * [CS336-RU] §"Арифметическая интенсивность инференса" (attention layer: scores
+ * A = Q K^T, Y = softmax(A) V) and §"Уменьшаем KV-кэш" (GQA: N query heads, K
+ * key/value heads, each KV head serves N/K query heads).  Readings: query head
+ * n uses KV head n / G (contiguous groups); scores are multiplied by `scale`
+ * (1/sqrt(H) unless given); query token t of the T new ones sees every cached
+ * position j <= ctx - T + t (full prefix, causal among the new tokens).
+ *
+ * For each listed sequence b = b_list[i] (all b when b_list is NULL) writes
+ * out[i][t][n][h] in fp64.  A sequence with a bad context length or a bad
+ * block id gets an all-zero output and a nonzero seq_err[i]. */
+int oracle_attention(int B, int T, int N, int K, int H, int block_size,
+                     int num_blocks, int max_blocks, int dtype, double scale,
+                     const uint16_t *q, const uint16_t *k_cache,
+                     const uint16_t *v_cache, const int32_t *block_tables,
+                     const int32_t *context_lens, const int32_t *b_list, int nb,
+                     double *out, int32_t *seq_err, int nthreads) {
+    if (K <= 0 || N % K != 0) return -1;
+    int G = N / K;
+    if (!b_list) nb = B;
+    if (scale <= 0) scale = 1.0 / sqrt((double)H);
+    int any = 0;
+
+    /* validate each listed sequence first (plain loop) */
+    int32_t *bad = (int32_t *)calloc((size_t)(nb > 0 ? nb : 1), sizeof(int32_t));
+    for (int i = 0; i < nb; ++i) {
+        int b = b_list ? b_list[i] : i;
+        int ctx = context_lens[b];
+        if (ctx < T || ctx <= 0 || ctx > (long long)max_blocks * block_size) {
+            bad[i] = ORACLE_ERR_CONTEXT;
+        } else {
+            int nblk = (ctx + block_size - 1) / block_size;
+            for (int j = 0; j < nblk; ++j) {
+                int blk = block_tables[(size_t)b * max_blocks + j];
+                if (blk < 0 || blk >= num_blocks) {
+                    bad[i] = ORACLE_ERR_BLOCK_ID;
+                    break;
+                }
+            }
+        }
+        if (seq_err) seq_err[i] = bad[i];
+        if (bad[i]) any = 1;
+    }
+
+    long long work = (long long)nb * T * N;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (long long w = 0; w < work; ++w) {
+        int i = (int)(w / ((long long)T * N));
+        int t = (int)((w / N) % T);
+        int n = (int)(w % N);
+        int b = b_list ? b_list[i] : i;
+        double *o = out + (((size_t)i * T + t) * N + n) * H;
+        if (bad[i]) {
+            for (int h = 0; h < H; ++h) o[h] = 0.0;
+            continue;
+        }
+        int ctx = context_lens[b];
+        int last = ctx - T + t; /* last visible position for query token t */
+        int kh = n / G;
+        const uint16_t *qv = q + (((size_t)b * T + t) * N + n) * H;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(last + 1));
+        double *qd = (double *)malloc(sizeof(double) * (size_t)H);
+        for (int h = 0; h < H; ++h) qd[h] = widen(qv[h], dtype);
+        /* scores s_j = scale * <q, k_j> */
+        double smax = -INFINITY;
+        for (int j = 0; j <= last; ++j) {
+            int blk = block_tables[(size_t)b * max_blocks + j / block_size];
+            const uint16_t *kr =
+                k_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h) acc += qd[h] * widen(kr[h], dtype);
+            s[j] = scale * acc;
+            if (s[j] > smax) smax = s[j];
+        }
+        /* softmax weights p_j = exp(s_j - max) / sum, then out = sum_j p_j v_j */
+        double denom = 0.0;
+        for (int j = 0; j <= last; ++j) {
+            s[j] = exp(s[j] - smax);
+            denom += s[j];
+        }
+        for (int h = 0; h < H; ++h) o[h] = 0.0;
+        for (int j = 0; j <= last; ++j) {
+            int blk = block_tables[(size_t)b * max_blocks + j / block_size];
+            const uint16_t *vr =
+                v_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;
+            double p = s[j] / denom;
+            for (int h = 0; h < H; ++h) o[h] += p * widen(vr[h], dtype);
+        }
+        free(qd);
+        free(s);
+    }
+    free(bad);
+    return any;
+}
+
+/* ---- greedy prefix acceptance ----------------------------------------------
+ * [KV-AR], speculative-decoding section: with greedy decoding a drafted token is
+ * kept only if the target model would have produced it.  [SONAR-KK]
+ * §"Спекулятивті кодтан шығару": the longest accepted prefix is found, and the
+ * target's logits at the first mismatch (or after the last draft) give one more
+ * token, so n drafts yield between 1 and n+1 tokens.
+ *
+ * logits [B][T][V] fp32; draft [B][T-1]: draft[b][i] is the token fed at input
+ * position i+1, checked against the target's choice g_i = argmax logits[b][i].
+ * accepted[b] = a, the largest i <= T-1 with draft[b][j] == g_j for all j < i;
+ * next_token[b] = g_a.  If ctx_inout is given, ctx_inout[b] -= (T-1-a): the
+ * KV entries of the rejected drafts are dropped.
+ *
+ * argmax reading: the first index of the largest value wins ties; a NaN counts
+ * as larger than every number and the first NaN wins (torch/numpy behaviour). */
+static int argmax_row(const float *x, int V) {
+    int best = 0;
+    for (int v = 1; v < V; ++v) {
+        if (isnan(x[best])) break; /* nothing beats the first NaN */
+        if (isnan(x[v]) || x[v] > x[best]) best = v;
+    }
+    return best;
+}
+
+void oracle_accept_prefix(int B, int T, int V, const float *logits,
+                          const int32_t *draft, int32_t *accepted,
+                          int32_t *next_token, int32_t *ctx_inout) {
+    for (int b = 0; b < B; ++b) {
+        int a = 0;
+        while (a < T - 1) {
+            int g = argmax_row(logits + ((size_t)b * T + a) * V, V);
+            if (draft[(size_t)b * (T - 1) + a] != g) break;
+            ++a;
+        }
+        accepted[b] = a;
+        next_token[b] = argmax_row(logits + ((size_t)b * T + a) * V, V);
+        if (ctx_inout) ctx_inout[b] -= (T - 1 - a);
+    }
+}
+
+/* argmax of one row, exposed so tests can pin the tie / NaN reading directly. */
+int oracle_argmax(const float *x, int V) { return argmax_row(x, V); }
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,155 @@
+"""ctypes front end of oracle.c (fp64 CPU oracle).
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).  Arrays are numpy; 16-bit
+elements travel as their raw uint16 bit patterns, so the C side widens them to
+double itself.  `dtype` is "f16" or "bf16".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_DT = {"f16": 0, "bf16": 1}
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (OpenMP when the compiler has it)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-std=c99", "-shared", "-fPIC", _SRC, "-o", _LIB + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True, text=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True, text=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _get():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i = ctypes.c_int
+            lib.oracle_f16_to_f64.restype = ctypes.c_double
+            lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_f64.restype = ctypes.c_double
+            lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.oracle_kv_append.restype = i
+            lib.oracle_kv_append.argtypes = [i] * 7 + [P] * 7
+            lib.oracle_attention.restype = i
+            lib.oracle_attention.argtypes = [i] * 9 + [ctypes.c_double] + [P] * 6 + [i, P, P, i]
+            lib.oracle_accept_prefix.restype = None
+            lib.oracle_accept_prefix.argtypes = [i, i, i, P, P, P, P, P]
+            lib.oracle_argmax.restype = i
+            lib.oracle_argmax.argtypes = [P, i]
+            lib.oracle_num_threads.restype = i
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _bits(a) -> np.ndarray:
+    """Raw 16-bit patterns of an fp16/bf16 array (numpy uint16 or float16, or a
+    torch CPU tensor)."""
+    if hasattr(a, "detach"):  # torch tensor
+        import torch
+
+        t = a.detach().cpu().contiguous()
+        if t.dtype in (torch.float16, torch.bfloat16):
+            t = t.view(torch.int16)
+        return t.numpy().view(np.uint16)
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        return a.view(np.uint16)
+    assert a.dtype in (np.uint16, np.int16), a.dtype
+    return a.view(np.uint16)
+
+
+def _i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def f16_to_f64(bits: int) -> float:
+    return _get().oracle_f16_to_f64(int(bits))
+
+
+def bf16_to_f64(bits: int) -> float:
+    return _get().oracle_bf16_to_f64(int(bits))
+
+
+def num_threads() -> int:
+    return _get().oracle_num_threads()
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens):
+    """Writes k_new/v_new [B,T,K,H] into copies of the caches [NB,bs,K,H].
+    Returns (k_cache', v_cache', seq_err[B]) as uint16 bit arrays."""
+    kn, vn = _bits(k_new), _bits(v_new)
+    kc, vc = _bits(k_cache).copy(), _bits(v_cache).copy()
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    B, T, K, H = kn.shape
+    NB, bs = kc.shape[0], kc.shape[1]
+    err = np.zeros(B, np.int32)
+    _get().oracle_kv_append(B, T, K, H, bs, NB, bt.shape[1], _p(kn), _p(vn), _p(kc),
+                            _p(vc), _p(bt), _p(cl), _p(err))
+    return kc, vc, err
+
+
+def attention(q, k_cache, v_cache, block_tables, context_lens, dtype, scale=0.0,
+              b_list=None, nthreads=0):
+    """fp64 paged GQA attention.  q [B,T,N,H]; caches [NB,bs,K,H].
+    Returns (out [nb,T,N,H] float64, seq_err [nb]) for the listed sequences."""
+    qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    B, T, N, H = qb.shape
+    NB, bs, K, H2 = kc.shape
+    assert H2 == H
+    bl = None if b_list is None else _i32(b_list)
+    nb = B if bl is None else len(bl)
+    out = np.zeros((nb, T, N, H), np.float64)
+    err = np.zeros(max(nb, 1), np.int32)
+    rc = _get().oracle_attention(B, T, N, K, H, bs, NB, bt.shape[1], _DT[dtype],
+                                 float(scale), _p(qb), _p(kc), _p(vc), _p(bt), _p(cl),
+                                 _p(bl), nb, _p(out), _p(err), int(nthreads))
+    if rc < 0:
+        raise ValueError("oracle_attention: N must be a multiple of K")
+    return out, err[:nb]
+
+
+def accept_prefix(logits, draft, context_lens=None):
+    """Greedy acceptance.  logits [B,T,V] float32, draft [B,T-1] int32.
+    Returns (accepted [B], next_token [B], context_lens' or None)."""
+    if hasattr(logits, "detach"):
+        logits = logits.detach().cpu().numpy()
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    B, T, V = lg.shape
+    dr = _i32(draft).reshape(B, max(T - 1, 0))
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    cl = None if context_lens is None else _i32(context_lens).copy()
+    _get().oracle_accept_prefix(B, T, V, _p(lg), _p(dr), _p(acc), _p(nxt), _p(cl))
+    return acc, nxt, cl
+
+
+def argmax(row) -> int:
+    r = np.ascontiguousarray(row, dtype=np.float32)
+    return _get().oracle_argmax(_p(r), r.shape[0])

@@ -1,0 +1,94 @@
+"""The byte / flop accounting (the bench's roofline numerator) reproduces the
+figures the pages print (tests/golden/page_figures.json)."""
+import json
+import os
+
+import pytest
+
+from gqa_decode_attention_02_gb300 import analytic as A
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_figures.json")))
+
+
+def g(name):
+    return GOLD[name]["value"], GOLD[name]["inputs"]
+
+
+def test_kv_bytes_per_token_formula():
+    v, i = g("kv_bytes_per_token_24L_2kv_h64_fp16")
+    assert A.kv_bytes_per_token(i["layers"], i["kv_heads"], i["head_dim"], i["elem_bytes"]) == v
+
+
+def test_allocator_bytes_for_295_tokens():
+    v, i = g("allocator_bytes_295_tokens")
+    assert i["tokens"] * A.kv_bytes_per_token(i["layers"], i["kv_heads"], i["head_dim"],
+                                              i["elem_bytes"]) == v
+    # the paged reservation: 19 blocks of 16 = 304 slots, 9 slots of fragmentation
+    assert A.paged_kv_bytes(295, 24, 2, 64, 2) == 304 * 12288 == 3735552
+
+
+def test_cache_depends_only_on_total_tokens():
+    v, i = g("cache_bytes_65536_tokens_MB")
+    per = A.kv_bytes_per_token(i["layers"], i["kv_heads"], i["head_dim"], i["elem_bytes"])
+    for users, tokens in ((32, 2048), (64, 1024), (128, 512)):
+        assert users * tokens * per == v * 2**20
+
+
+def test_mha_and_7b_figures():
+    v, i = g("mha_bytes_per_token_14_heads")
+    assert A.kv_bytes_per_token(i["layers"], i["kv_heads"], i["head_dim"], i["elem_bytes"]) == v
+    assert v // 12288 == 7  # exactly the 14 / 2 head ratio
+    v, i = g("kv_bytes_per_token_7b_KB")
+    assert A.kv_bytes_per_token(i["layers"], i["kv_heads"], i["head_dim"],
+                                i["elem_bytes"]) == v * 1024
+
+
+def test_score_buffer_sizes():
+    v, i = g("score_bytes_4096_recompute_MB")
+    assert round(A.score_matrix_bytes(i["n"], cached=False) / 1e6) == v
+    v, i = g("score_bytes_4096_cached_KB")
+    assert A.score_matrix_bytes(i["n"], cached=True) == v * 1024
+
+
+def test_accelerator_intensities():
+    for name in ("h100_intensity", "rtx4080_intensity"):
+        v, i = g(name)
+        assert round(A.accelerator_intensity(i["flops"], i["bytes"])) == v
+    assert A.decode_attention_intensity(1024) < 1.0
+    assert A.decode_attention_intensity(1024, T=1024) == 512
+
+
+def test_llama2_13b_tables():
+    v, i = g("llama2_13b_num_params")
+    assert A.transformer_params(i["V"], i["D"], i["F"], i["L"], i["N"], i["K"], i["H"]) == v
+    v, i = g("llama2_13b_kv_per_seq_1024")
+    assert i["S"] * i["K"] * i["H"] * i["L"] * 2 * 2 == v
+    t = GOLD["llama2_13b_table"]
+    c = t["inputs"]
+    for row in t["rows"]:
+        mem, lat, tput = A.decode_step_model(row["B"], c["S"], c["V"], c["D"], c["F"], c["L"],
+                                             c["N"], row["K"], c["H"], c["bandwidth"])
+        assert A.round_half_up(mem / 1e9, 1) == pytest.approx(row["memory_GB"])
+        assert A.round_half_up(lat * 1e3, 1) == pytest.approx(row["latency_ms"])
+        assert A.round_half_up(tput) == row["tokens_per_s"]
+
+
+@pytest.mark.parametrize("name", ["spec_tokens_alpha_0p3_gamma_4", "spec_speedup_alpha_0p9_gamma_8",
+                                  "spec_speedup_alpha_0p3_gamma_8",
+                                  "spec_speedup_alpha_0p3_gamma_4_c_fifth"])
+def test_speculative_calculator(name):
+    v, i = g(name)
+    d = GOLD[name]["digits"]
+    if "c" in i:
+        got = A.spec_speedup(i["alpha"], i["gamma"], i["c"])
+    else:
+        got = A.spec_expected_tokens(i["alpha"], i["gamma"])
+    assert A.round_half_up(got, d) == pytest.approx(v)
+
+
+def test_algorithmic_bytes_config_1():
+    # one sequence of 295 tokens, N=14/K=2/H=64 fp16: 75,520 bytes of keys and
+    # as many of values, plus q in / out back, 19 block ids and one length
+    b = A.attention_algorithmic_bytes([295], T=1, N=14, K=2, H=64, elem_bytes=2)
+    assert 295 * 2 * 64 * 2 == 75520
+    assert b == 2 * 75520 + 2 * 14 * 64 * 2 + 4 * 19 + 4
