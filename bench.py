@@ -1,0 +1,505 @@
+#!/usr/bin/env python3
+"""Bench: paged GQA decode attention on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg2]
+                    [--impl ours|reference]
+
+A step is one pass of the hot path over one batch: for every layer, the append
+of the new token's key/value (kv_append) and the decode attention over the
+paged cache (plus verify and greedy acceptance for the speculative workload).
+The default workload is the 24-layer one (B=64, N=14, K=2, H=64, fp16, context
+U[16,1024], block tables a random permutation of a shared pool).  The step's
+library calls are captured once into CUDA graphs (appends, then attentions) and
+replayed, so launch overhead does not hide the kernels; the attention graph is
+bracketed by its own events, which gives the attention kernel's average launch
+duration live inside the timed region.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the path
+has no exchange step); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention achieved HBM GB/s (% of GB300 peak) and attention tokens/sec"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="cfg2", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the oracle CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---- accounting ------------------------------------------------------------------
+def step_bytes(w):
+    from gqa_decode_attention_02_gb300 import analytic as A
+
+    e = 2
+    ctx = w.context_lens.cpu().numpy()
+    attn = A.attention_algorithmic_bytes(ctx, w.T, w.N, w.K, w.H, e)
+    app = A.kv_append_bytes(w.B, w.T, w.K, w.H, e) if w.appended else 0
+    acc = A.accept_bytes(w.B, w.T, w.logits.shape[-1]) if w.logits is not None else 0
+    return attn, app, acc
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("attention.cu", "ptx.cuh"):
+        h.update(open(os.path.join(ROOT, "gqa_decode_attention_02_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """dram bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"attention_{workload}_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---- clocks ------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", index, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        import statistics
+
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_index_for_smi(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[local_rank].strip()
+    return str(local_rank)
+
+
+# ---- CPU oracle timing --------------------------------------------------------------
+def oracle_sample(w, budget_s):
+    """Time the oracle (as it stands, all host threads) on a bounded sample of the
+    workload: (layer, 8-sequence chunk) units in order until the budget is
+    spent.  Returns (GB/s of algorithmic bytes, seconds, description, threads)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from gqa_decode_attention_02_gb300 import analytic as A
+
+    oracle.build()
+    ctx = w.context_lens.cpu().numpy()
+    tables = w.block_tables.cpu()
+    lens = w.context_lens.cpu()
+    done_bytes, spent, units, seqs = 0, 0.0, 0, 0
+    for layer in range(w.layers):
+        q = w.q[layer].cpu()
+        kc, vc = w.k_cache[layer].cpu(), w.v_cache[layer].cpu()
+        kn, vn = w.k_new[layer].cpu(), w.v_new[layer].cpu()
+        for s0 in range(0, w.B, 8):
+            bl = np.arange(s0, min(w.B, s0 + 8), dtype=np.int32)
+            t0 = time.perf_counter()
+            if w.appended:
+                kb, vb, _ = oracle.kv_append(kn, vn, kc, vc, tables, lens)
+                kcx = torch.from_numpy(kb.view(np.int16)).view(w.torch_dtype)
+                vcx = torch.from_numpy(vb.view(np.int16)).view(w.torch_dtype)
+            else:
+                kcx, vcx = kc, vc
+            oracle.attention(q, kcx, vcx, tables, lens, w.dtype, b_list=bl)
+            spent += time.perf_counter() - t0
+            done_bytes += A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2)
+            units += 1
+            seqs += len(bl)
+            if spent >= budget_s:
+                break
+        if spent >= budget_s:
+            break
+    desc = (f"oracle over {seqs} (layer, sequence) pairs of {w.layers * w.B} "
+            f"({units} chunks of <=8 sequences, appends included), fp64 C + OpenMP")
+    return done_bytes / spent / 1e9, spent, desc, oracle.num_threads()
+
+
+# ---- our arm -----------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gqa_decode_attention_02_gb300 as gq
+    from gqa_decode_attention_02_gb300 import workloads
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    w = workloads.make(args.workload, device=dev)
+    L = w.layers
+    attn_fn = gq.decode_attention if w.T == 1 else gq.verify_attention
+    ws_bytes = gq.attention_workspace_size(w.q[0], w.k_cache[0], w.block_tables)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    outs = [torch.empty_like(q) for q in w.q]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    has_acc = w.logits is not None
+    if has_acc:
+        ctx_scratch = w.context_lens.clone()
+        acc_out = torch.empty(w.B, dtype=torch.int32, device=dev)
+        nxt_out = torch.empty(w.B, dtype=torch.int32, device=dev)
+
+    def do_append():
+        if w.appended:
+            for l in range(L):
+                gq.kv_append(w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
+                             w.block_tables, w.context_lens, status=st)
+
+    def do_attn():
+        for l in range(L):
+            attn_fn(w.q[l], w.k_cache[l], w.v_cache[l], w.block_tables, w.context_lens,
+                    out=outs[l], workspace=ws, status=st)
+
+    def do_acc():
+        if has_acc:
+            gq.accept_prefix(w.logits, w.draft, ctx_scratch, accepted=acc_out,
+                             next_token=nxt_out, status=st)
+
+    # eager warm-up (also builds the launch plans), then capture
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        do_append(), do_attn(), do_acc()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graphs = {}
+    for name, fn in (("append", do_append), ("attn", do_attn), ("acc", do_acc)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[name] = g
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def refresh():
+        flush.zero_()  # evict L2 (126 MB) between steps
+        if has_acc:
+            ctx_scratch.copy_(w.context_lens)
+
+    for _ in range(args.warmup):
+        refresh()
+        graphs["append"].replay()
+        graphs["attn"].replay()
+        graphs["acc"].replay()
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())} during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(gpu_index_for_smi(local)) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        refresh()
+        e = evs[i]
+        e[0].record()
+        graphs["append"].replay()
+        e[1].record()
+        graphs["attn"].replay()
+        e[2].record()
+        graphs["acc"].replay()
+        e[3].record()
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop() if clocks else None
+    step_ms = sum(e[0].elapsed_time(e[3]) for e in evs) / K
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / K
+    app_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    acc_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())} in the timed region")
+
+    attn_b, app_b, acc_b = step_bytes(w)
+    bytes_step = L * (attn_b + app_b) + acc_b
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms_max = float(t.item())
+    else:
+        step_ms_max = step_ms
+    value = world * bytes_step / (step_ms_max * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+    attn_launch_ms = attn_ms / L
+    achieved = attn_b / (attn_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.workload)
+
+    # e2e: host buffers -> device, the captured API calls, results -> host
+    e2e = None
+    e2e_eager = None
+    if not args.no_e2e:
+        h_in = [t.cpu().pin_memory() for t in (w.q + (w.k_new + w.v_new if w.appended else []))]
+        d_in = w.q + (w.k_new + w.v_new if w.appended else [])
+        h_meta = [w.block_tables.cpu().pin_memory(), w.context_lens.cpu().pin_memory()]
+        d_meta = [w.block_tables, w.context_lens]
+        h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+        if has_acc:
+            h_in.append(w.logits.cpu().pin_memory())
+            d_in.append(w.logits)
+            h_acc = [torch.empty(w.B, dtype=torch.int32).pin_memory() for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in h_in + h_meta)
+        d2h = sum(t.numel() * t.element_size() for t in h_out) + (8 * w.B if has_acc else 0)
+
+        def e2e_step(use_graph):
+            for d, h in zip(d_in + d_meta, h_in + h_meta):
+                d.copy_(h, non_blocking=True)
+            if use_graph:
+                graphs["append"].replay()
+                graphs["attn"].replay()
+                graphs["acc"].replay()
+            else:
+                do_append(), do_attn(), do_acc()
+            for h, o in zip(h_out, outs):
+                h.copy_(o, non_blocking=True)
+            if has_acc:
+                h_acc[0].copy_(acc_out, non_blocking=True)
+                h_acc[1].copy_(nxt_out, non_blocking=True)
+
+        for use_graph in (True, False):
+            for _ in range(2):
+                refresh()
+                e2e_step(use_graph)
+            torch.cuda.synchronize()
+            tot = 0.0
+            for _ in range(K):
+                refresh()
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                e2e_step(use_graph)
+                torch.cuda.synchronize()
+                tot += time.perf_counter() - t0
+            ms = tot / K * 1e3
+            rec = {"value": world * bytes_step / (ms * 1e-3) / 1e9, "unit": "GB/s",
+                   "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            if use_graph:
+                rec["how"] = ("pinned host inputs copied in, the step's library calls "
+                              "replayed from their CUDA-graph capture, outputs copied out; "
+                              "host wall clock around each step")
+                e2e = rec
+            else:
+                rec["how"] = "as e2e but every library call made from Python each step"
+                e2e_eager = rec
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, spent, desc, thr = oracle_sample(w, args.cpu_seconds)
+        cpu = {"value": v, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
+               "seconds": round(spent, 2)}
+
+    ctx = w.context_lens.cpu().numpy()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic: seeded N(0,1) values rounded to the dtype, paged cache with "
+                "NaN sentinels in unused slots, shuffled block tables",
+        "config": {
+            "workload": f"{w.name}: {w.desc}",
+            "B": w.B, "T": w.T, "N": w.N, "K": w.K, "H": w.H, "layers": L,
+            "block_size": w.block_size, "sum_context_tokens": int(ctx.sum()),
+            "l2": "flushed between steps (256 MiB write outside the step events)",
+            "parallelism": f"replicas x{world}",
+        },
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "attention_tokens_per_s": round(world * w.B * w.T * L / (step_ms_max * 1e-3), 1),
+        "context_tokens_per_s": round(world * int(ctx.sum()) * L / (step_ms_max * 1e-3), 1),
+        "breakdown_ms": {"append": round(app_ms, 5), "attention": round(attn_ms, 5),
+                         "accept": round(acc_ms, 5)},
+        "roofline": {"bound": "hbm", "kernel": "attention_kernel (decode/verify)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": attn_b,
+                     "avg_launch_us": round(attn_launch_ms * 1e3, 3)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "e2e_eager": e2e_eager,
+        "gpu_launches": K * ((L if w.appended else 0) + L + (1 if has_acc else 0)),
+        "clocks": clk,
+        "wall_s_timed": round(wall, 4),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ---- reference arm: the oracle on the host cores ----------------------------------------
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from gqa_decode_attention_02_gb300 import analytic as A
+    from gqa_decode_attention_02_gb300 import workloads
+
+    oracle.build()
+    w = workloads.make(args.workload)  # CPU tensors
+    ctx = w.context_lens.numpy()
+    chunk = 8
+    units = [(l, s) for l in range(w.layers) for s in range(0, w.B, chunk)]
+    # one step = the oracle on one (layer, 8-sequence) unit, cycling through the batch
+    times, nbytes = [], []
+    K, W = args.steps, args.warmup
+    for i in range(W + K):
+        l, s0 = units[i % len(units)]
+        bl = np.arange(s0, min(w.B, s0 + chunk), dtype=np.int32)
+        t0 = time.perf_counter()
+        if w.appended:
+            kb, vb, _ = oracle.kv_append(w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
+                                         w.block_tables, w.context_lens)
+            kc = torch.from_numpy(kb.view(np.int16)).view(w.torch_dtype)
+            vc = torch.from_numpy(vb.view(np.int16)).view(w.torch_dtype)
+        else:
+            kc, vc = w.k_cache[l], w.v_cache[l]
+        oracle.attention(w.q[l], kc, vc, w.block_tables, w.context_lens, w.dtype, b_list=bl)
+        dt = time.perf_counter() - t0
+        if i >= W:
+            times.append(dt)
+            nbytes.append(A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2))
+    value = sum(nbytes) / sum(times) / 1e9
+    ms = 1e3 * sum(times) / K
+    desc = (f"each step: the fp64 oracle on one layer x {chunk} sequences of {w.name} "
+            f"(append included), cycling through {w.layers} layers x {w.B} sequences")
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "impl": "reference",
+        "data": "synthetic (same seeded recipe as our arm)",
+        "config": {"workload": f"{w.name}: {w.desc}", "B": w.B, "T": w.T, "N": w.N,
+                   "K": w.K, "H": w.H, "layers": w.layers, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

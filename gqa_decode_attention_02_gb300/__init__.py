@@ -1,0 +1,113 @@
+"""Paged grouped-query decode attention for GB300 (sm_103a).
+
+Python face of the C ABI in include/gqa_decode.h: same operation names, torch
+tensors in, argument marshalling only.  All computation runs in the library's
+CUDA kernels; calling any op without the built library raises.
+
+    kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens)
+    decode_attention(q, k_cache, v_cache, block_tables, context_lens) -> out
+    verify_attention(q, k_cache, v_cache, block_tables, context_lens) -> out
+    accept_prefix(target_logits, draft_ids, context_lens=None) -> (accepted, next)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import GqaError, Shape, Status, status_string  # noqa: F401
+
+__all__ = ["kv_append", "decode_attention", "verify_attention", "accept_prefix",
+           "attention_workspace_size", "GqaError", "Status", "Shape"]
+
+
+def _status_arg(status):
+    if status is None:
+        return None
+    _lib._need(status, "status", torch.int32)
+    return _lib._ptr(status)
+
+
+def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens, *, status=None,
+              stream=None):
+    """gqa_kv_append: k_new/v_new [B,T,K,H] -> caches [NB,16,K,H] at positions
+    context_lens[b]-T+t.  Asynchronous on `stream` (default: current)."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _lib._need(t, n, ndim=4)
+    _lib._need(block_tables, "block_tables", torch.int32, 2)
+    _lib._need(context_lens, "context_lens", torch.int32, 1)
+    shape = _lib.make_shape(k_new, k_cache, block_tables, None, heads_dim=3)
+    rc = _lib.lib().gqa_kv_append(ctypes.byref(shape), _lib._ptr(k_new), _lib._ptr(v_new),
+                                  _lib._ptr(k_cache), _lib._ptr(v_cache),
+                                  _lib._ptr(block_tables), _lib._ptr(context_lens),
+                                  _status_arg(status), _lib._stream(stream))
+    _lib._check("gqa_kv_append", rc)
+
+
+def attention_workspace_size(q, k_cache, block_tables, scale=None) -> int:
+    return _lib.workspace_size(_lib.make_shape(q, k_cache, block_tables, scale))
+
+
+def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, scale,
+               workspace, status, stream):
+    _lib._need(q, "q", ndim=4)
+    _lib._need(k_cache, "k_cache", q.dtype, 4)
+    _lib._need(v_cache, "v_cache", q.dtype, 4)
+    _lib._need(block_tables, "block_tables", torch.int32, 2)
+    _lib._need(context_lens, "context_lens", torch.int32, 1)
+    shape = _lib.make_shape(q, k_cache, block_tables, scale)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _lib._need(out, "out", q.dtype, 4)
+    nbytes = _lib.workspace_size(shape)
+    if workspace is None:
+        workspace = _lib.get_workspace(nbytes, q.device)
+    else:
+        _lib._need(workspace, "workspace", torch.uint8)
+    L = _lib.lib()
+    rc = getattr(L, fn_name)(ctypes.byref(shape), _lib._ptr(q), _lib._ptr(k_cache),
+                             _lib._ptr(v_cache), _lib._ptr(block_tables),
+                             _lib._ptr(context_lens), _lib._ptr(out), _lib._ptr(workspace),
+                             workspace.numel(), _status_arg(status), _lib._stream(stream))
+    _lib._check(fn_name, rc)
+    return out
+
+
+def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
+                     workspace=None, status=None, stream=None):
+    """gqa_decode_attention (T == 1).  q [B,1,N,H] -> out [B,1,N,H]."""
+    return _attention("gqa_decode_attention", q, k_cache, v_cache, block_tables, context_lens,
+                      out, scale, workspace, status, stream)
+
+
+def verify_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
+                     workspace=None, status=None, stream=None):
+    """gqa_verify_attention (T >= 1, causal among the T new tokens)."""
+    return _attention("gqa_verify_attention", q, k_cache, v_cache, block_tables, context_lens,
+                      out, scale, workspace, status, stream)
+
+
+def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,
+                  next_token=None, status=None, stream=None):
+    """gqa_accept_prefix.  target_logits fp32 [B,T,V], draft_ids int32 [B,T-1].
+    Returns (accepted [B], next_token [B]); updates context_lens in place if given."""
+    _lib._need(target_logits, "target_logits", torch.float32, 3)
+    B, T, V = target_logits.shape
+    if T > 1:
+        _lib._need(draft_ids, "draft_ids", torch.int32, 2)
+    if context_lens is not None:
+        _lib._need(context_lens, "context_lens", torch.int32, 1)
+    dev = target_logits.device
+    if accepted is None:
+        accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = _lib.lib().gqa_accept_prefix(B, T, V, _lib._ptr(target_logits),
+                                      _lib._ptr(draft_ids) if T > 1 else None,
+                                      _lib._ptr(accepted), _lib._ptr(next_token),
+                                      _lib._ptr(context_lens), _status_arg(status),
+                                      _lib._stream(stream))
+    _lib._check("gqa_accept_prefix", rc)
+    return accepted, next_token

@@ -1,0 +1,154 @@
+"""Thin ctypes binding over libgqa_decode.so (include/gqa_decode.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  torch supplies device memory and the current
+stream.  If the library is missing the calls raise: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgqa_decode.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_NULL = 1
+    ERR_SHAPE = 2
+    ERR_DTYPE = 3
+    ERR_ALIGN = 4
+    ERR_WORKSPACE = 5
+    ERR_CUDA = 6
+    ERR_CONTEXT = 7
+    ERR_BLOCK_ID = 8
+    ERR_TIMEOUT = 9
+
+
+class GqaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{fn}: {status_string(status)} (status {int(status)})")
+
+
+class Shape(ctypes.Structure):
+    """gqa_shape of include/gqa_decode.h."""
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("N", ctypes.c_int),
+                ("K", ctypes.c_int), ("H", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("scale", ctypes.c_float)]
+
+
+EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
+           "gqa_attention_workspace_size", "gqa_workspace_clear", "gqa_decode_attention",
+           "gqa_verify_attention", "gqa_accept_prefix")
+
+
+def lib() -> ctypes.CDLL:
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m gqa_decode_attention_02_gb300.build` (no CPU fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(Shape)
+        L.gqa_version.restype = I
+        L.gqa_version.argtypes = []
+        L.gqa_status_string.restype = ctypes.c_char_p
+        L.gqa_status_string.argtypes = [I]
+        L.gqa_kv_append.restype = I
+        L.gqa_kv_append.argtypes = [S, P, P, P, P, P, P, P, P]
+        L.gqa_attention_workspace_size.restype = ctypes.c_size_t
+        L.gqa_attention_workspace_size.argtypes = [S]
+        L.gqa_workspace_clear.restype = I
+        L.gqa_workspace_clear.argtypes = [P, ctypes.c_size_t, P]
+        for name in ("gqa_decode_attention", "gqa_verify_attention"):
+            f = getattr(L, name)
+            f.restype = I
+            f.argtypes = [S, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+        L.gqa_accept_prefix.restype = I
+        L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, P]
+        _lib = L
+        return L
+
+
+def status_string(code: int) -> str:
+    return lib().gqa_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+_DTYPES = {torch.float16: 0, torch.bfloat16: 1}
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise GqaError(fn, rc)
+
+
+def _need(t, name, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def make_shape(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
+               scale: float | None, heads_dim: int = 2) -> Shape:
+    B, T, X, H = q_or_new.shape
+    NB, bs, K, H2 = k_cache.shape
+    if H2 != H:
+        raise ValueError(f"head size mismatch: {H} vs {H2}")
+    if q_or_new.dtype not in _DTYPES:
+        raise ValueError(f"dtype {q_or_new.dtype} unsupported (fp16 / bf16)")
+    return Shape(B=B, T=T, N=X if heads_dim == 2 else K, K=K, H=H, block_size=bs,
+                 num_blocks=NB, max_blocks_per_seq=block_tables.shape[1],
+                 dtype=_DTYPES[q_or_new.dtype], scale=float(scale or 0.0))
+
+
+_ws_cache: dict = {}
+
+
+def workspace_size(shape: Shape) -> int:
+    n = lib().gqa_attention_workspace_size(ctypes.byref(shape))
+    if n == 0:
+        raise GqaError("gqa_attention_workspace_size", Status.ERR_SHAPE)
+    return n
+
+
+def get_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled workspace of at least nbytes, kept per device and reused
+    (the library returns it zero-filled after every call)."""
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
+        _ws_cache[key] = ws
+    return ws

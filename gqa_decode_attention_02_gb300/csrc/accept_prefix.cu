@@ -1,0 +1,155 @@
+// accept_prefix.cu -- greedy longest-prefix acceptance of drafted tokens.
+//
+// Speculative-decoding section of "جعل inference رخيصًا: KV cache وbatching
+// والتكميم": with greedy decoding a drafted token is accepted only if the target
+// model would have produced it.  "Болжау арқылы Sonar модельдерін жылдамдату"
+// §"Спекулятивті кодтан шығару": the longest accepted run is found, and the
+// target's logits at the first mismatch (or after the last draft) supply one
+// more token; §"Спекулятивті кодтан шығару арқылы инференс": doing this
+// bookkeeping on the GPU avoids a GPU->CPU synchronisation, so the sequence
+// length is updated here, on the device.
+//
+// One thread-block cluster per sequence.  The cluster's CS blocks split the
+// sequence's T*V logits into CS contiguous ranges; each block reduces the
+// argmax of every row its range touches to a 64-bit key
+//     (order-preserving image of the value) << 32 | (~index)
+// so that a plain max over keys picks the largest value and, among equal
+// values, the smallest index; NaN maps above +inf (first NaN wins) and -0 is
+// folded into +0.  Block r writes its key for row t into block 0's shared
+// memory (distributed shared memory); after one cluster barrier block 0 takes
+// the max over ranks, walks the drafts and writes the results.
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kMaxT = 64;
+constexpr int kMaxCluster = 8;
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ unsigned long long argmax_key(float x, uint32_t idx) {
+    uint32_t u = __float_as_uint(x);
+    uint32_t o;
+    if (x != x) {
+        o = 0xffffffffu;
+    } else {
+        if (u == 0x80000000u) u = 0u;  // -0 == +0
+        o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    return ((unsigned long long)o << 32) | (unsigned long long)(0xffffffffu - idx);
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void st_remote_u64(const void* local, uint32_t rank,
+                                              unsigned long long v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads)
+    accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ draft,
+                  int32_t* accepted, int32_t* next_token, int32_t* ctx_io, int32_t* status,
+                  int T, int V, int cs) {
+    __shared__ unsigned long long table[kMaxT * kMaxCluster];  // used in rank 0
+    __shared__ unsigned long long red[kThreads / 32];
+    const uint32_t rank = cluster_rank();
+    const int b = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long TV = (long long)T * V;
+    const long long chunk = (TV + cs - 1) / cs;
+    const long long lo = (long long)rank * chunk;
+    const long long hi = lo + chunk < TV ? lo + chunk : TV;
+    const float* row0 = logits + (size_t)b * TV;
+
+    for (int t = 0; t < T; ++t) {
+        const long long rs = (long long)t * V, re = rs + V;
+        const long long s = lo > rs ? lo : rs;
+        const long long e = hi < re ? hi : re;
+        unsigned long long key = 0ull;  // below every real key
+        if (s < e) {
+            const float* row = row0 + rs;
+            const int vs = (int)(s - rs), ve = (int)(e - rs);
+#pragma unroll 8
+            for (int v = vs + tid; v < ve; v += kThreads)
+                key = umax64(key, argmax_key(__ldg(row + v), (uint32_t)v));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
+            if (lane == 0) red[warp] = key;
+            __syncthreads();
+            if (tid == 0) {
+                for (int i = 1; i < kThreads / 32; ++i) key = umax64(key, red[i]);
+            }
+            __syncthreads();
+        }
+        if (tid == 0) st_remote_u64(&table[t * kMaxCluster + rank], 0, key);
+    }
+    cluster_sync_all();
+    if (rank != 0 || tid != 0) return;
+    int g[kMaxT];
+    for (int t = 0; t < T; ++t) {
+        unsigned long long k = 0ull;
+        for (int r = 0; r < cs; ++r) k = umax64(k, table[t * kMaxCluster + r]);
+        g[t] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+    }
+    int a = 0;
+    while (a < T - 1 && draft[(size_t)b * (T - 1) + a] == g[a]) ++a;
+    accepted[b] = a;
+    next_token[b] = g[a];
+    if (ctx_io) {
+        const int nc = ctx_io[b] - (T - 1 - a);
+        if (nc < 0)
+            report(status, GQA_ERR_CONTEXT);
+        else
+            ctx_io[b] = nc;
+    }
+}
+
+}  // namespace
+
+gqa_status launch_accept_prefix(int B, int T, int V, const float* logits, const int32_t* draft,
+                                int32_t* accepted, int32_t* next_token, int32_t* ctx_io,
+                                int32_t* dev_status, cudaStream_t stream) {
+    if (B == 0) return GQA_OK;
+    const long long TV = (long long)T * V;
+    int cs = (int)((TV + 4095) / 4096);
+    if (cs > kMaxCluster) cs = kMaxCluster;
+    if (cs < 1) cs = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, B, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, accept_kernel, logits, draft, accepted,
+                                             next_token, ctx_io, dev_status, T, V, cs);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace gqa

@@ -1,0 +1,128 @@
+// api.cu -- the extern "C" entry points declared in include/gqa_decode.h:
+// host-side argument validation, then one launch per operation.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+gqa_status check_common(const gqa_shape* s) {
+    if (!s) return GQA_ERR_NULL;
+    if (s->dtype != GQA_F16 && s->dtype != GQA_BF16) return GQA_ERR_DTYPE;
+    if (s->B < 0 || s->T < 1 || s->N < 1 || s->K < 1 || s->N % s->K != 0) return GQA_ERR_SHAPE;
+    if (s->H != 64 && s->H != 128) return GQA_ERR_SHAPE;
+    if (s->block_size != 16 || s->num_blocks < 1 || s->max_blocks_per_seq < 1)
+        return GQA_ERR_SHAPE;
+    if ((long long)s->num_blocks * 16 > (1ll << 31) - 1) return GQA_ERR_SHAPE;
+    if ((long long)s->max_blocks_per_seq * 16 > (1ll << 30)) return GQA_ERR_SHAPE;
+    if ((long long)s->B * s->K * s->max_blocks_per_seq > (1ll << 31) - 1) return GQA_ERR_SHAPE;
+    return GQA_OK;
+}
+
+gqa_status attention_entry(const gqa_shape* s, bool decode_only, const void* q,
+                           const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, const int32_t* context_lens, void* out,
+                           void* workspace, size_t ws_bytes, int32_t* dev_status,
+                           void* stream) {
+    gqa_status st = check_common(s);
+    if (st != GQA_OK) return st;
+    if (decode_only && s->T != 1) return GQA_ERR_SHAPE;
+    if (s->B == 0) return GQA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return GQA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return GQA_ERR_ALIGN;
+    gqa::AttnPlan plan;
+    st = gqa::attention_plan(*s, &plan);
+    if (st != GQA_OK) return st;
+    if (!workspace || ws_bytes < plan.workspace) return GQA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GQA_ERR_ALIGN;
+    return gqa::launch_attention(*s, plan, q, k_cache, v_cache, block_tables, context_lens, out,
+                                 workspace, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqa_version(void) { return 100; }
+
+const char* gqa_status_string(int status) {
+    switch (status) {
+        case GQA_OK: return "ok";
+        case GQA_ERR_NULL: return "a required pointer is NULL";
+        case GQA_ERR_SHAPE: return "unsupported or inconsistent sizes";
+        case GQA_ERR_DTYPE: return "unsupported dtype";
+        case GQA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case GQA_ERR_WORKSPACE: return "workspace missing or too small";
+        case GQA_ERR_CUDA: return "CUDA call failed";
+        case GQA_ERR_CONTEXT: return "context length out of range";
+        case GQA_ERR_BLOCK_ID: return "block id out of range";
+        case GQA_ERR_TIMEOUT: return "bounded wait inside a kernel timed out";
+        default: return "unknown status";
+    }
+}
+
+gqa_status gqa_kv_append(const gqa_shape* shape, const void* k_new, const void* v_new,
+                         void* k_cache, void* v_cache, const int32_t* block_tables,
+                         const int32_t* context_lens, int32_t* dev_status, void* stream) {
+    gqa_status st = check_common(shape);
+    if (st != GQA_OK) return st;
+    if (shape->B == 0) return GQA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens)
+        return GQA_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return GQA_ERR_ALIGN;
+    return gqa::launch_kv_append(*shape, k_new, v_new, k_cache, v_cache, block_tables,
+                                 context_lens, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+size_t gqa_attention_workspace_size(const gqa_shape* shape) {
+    if (check_common(shape) != GQA_OK) return 0;
+    gqa::AttnPlan plan;
+    if (gqa::attention_plan(*shape, &plan) != GQA_OK) return 0;
+    return plan.workspace;
+}
+
+gqa_status gqa_workspace_clear(void* workspace, size_t bytes, void* stream) {
+    if (bytes == 0) return GQA_OK;
+    if (!workspace) return GQA_ERR_NULL;
+    return cudaMemsetAsync(workspace, 0, bytes, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GQA_OK
+               : GQA_ERR_CUDA;
+}
+
+gqa_status gqa_decode_attention(const gqa_shape* shape, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, void* out, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    return attention_entry(shape, true, q, k_cache, v_cache, block_tables, context_lens, out,
+                           workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_verify_attention(const gqa_shape* shape, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                const int32_t* context_lens, void* out, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    return attention_entry(shape, false, q, k_cache, v_cache, block_tables, context_lens, out,
+                           workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_accept_prefix(int B, int T, int V, const float* target_logits,
+                             const int32_t* draft_ids, int32_t* accepted, int32_t* next_token,
+                             int32_t* context_lens_inout, int32_t* dev_status, void* stream) {
+    if (B < 0 || T < 1 || T > 64 || V < 1 || B > 65535) return GQA_ERR_SHAPE;
+    if (B == 0) return GQA_OK;
+    if (!target_logits || !accepted || !next_token || (T > 1 && !draft_ids))
+        return GQA_ERR_NULL;
+    if (!aligned16(target_logits)) return GQA_ERR_ALIGN;
+    if ((long long)T * V > (1ll << 31) - 1) return GQA_ERR_SHAPE;
+    return gqa::launch_accept_prefix(B, T, V, target_logits, draft_ids, accepted, next_token,
+                                     context_lens_inout, dev_status,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

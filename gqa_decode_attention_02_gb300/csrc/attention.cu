@@ -1,0 +1,741 @@
+// attention.cu -- paged grouped-query decode / verify attention for sm_103a.
+//
+// What it computes (CS336 lecture 10, Russian translation, §"Арифметическая
+// интенсивность инференса" and §"Уменьшаем KV-кэш"; paged reads from
+// §"PagedAttention"): for sequence b, new token t < T and query head n, with KV
+// head k = n / G,
+//     s_j = scale * <q[b,t,n,:], K_b[j,k,:]>   for j <= ctx_b - T + t
+//     out[b,t,n,:] = sum_j softmax(s)_j V_b[j,k,:]
+// where K_b[j] / V_b[j] is row j % 16 of physical block block_tables[b][j/16].
+//
+// Why it is shaped this way.  The same section derives that decode attention
+// reads every cached key and value once and does only ~1 flop per byte per
+// query row, so HBM bandwidth bounds it whatever the batch; with GQA the G
+// query heads of one KV head (times the T new tokens) share each K/V byte, so
+// all T*G rows of a KV head are processed together and every KV byte crosses
+// HBM once.
+//
+// Structure of one CTA (persistent; grid = SMs x resident CTAs):
+//  * Work order.  The tiles of the whole batch are laid out as segments
+//    (b, k) in b-major order, each segment being ceil(ctx_b/16) tiles of 16
+//    tokens (one cache block of one KV head).  CTA c takes the contiguous
+//    range [c*quota, (c+1)*quota) of that order, so every CTA streams the same
+//    number of bytes however ragged the context lengths are.  A segment cut by
+//    a range boundary is finished by merging its pieces with log-sum-exp
+//    weights -- the context split of FlashDecoding (named in §"PagedAttention"),
+//    balanced over the whole batch.  Every CTA derives the plan from
+//    context_lens itself (one warp scan), so the host never reads device data.
+//  * One producer warp walks the range, reads block ids 32 at a time and issues
+//    TMA tiled loads (3-D view [blocks*16 rows][K][H], box 16 rows x 64
+//    elements, 128-byte swizzle) of the K and V tile into a ring of stages,
+//    each completing on an mbarrier with a transaction count.
+//  * Consumer warp w owns query rows 8w..8w+7 (rows r = t*G + g).  Per tile it
+//    computes S^T[16 tokens x 8 rows] = K_tile . Q^T with mma.sync m16n8k16
+//    (tokens on M, so no tensor-core rows are wasted on a small G), keeps a
+//    running max / sum in the log2 domain (rescaling the accumulator only when
+//    the max grows by more than 2^8, which leaves the result unchanged up to
+//    rounding), transposes P in registers with movmatrix and accumulates
+//    O^T[H x 8 rows] += V_tile^T . P^T, again on mma.sync.
+//  * A finished segment is written directly when the CTA owns all of it;
+//    otherwise the warp stores its (max, sum, accumulator) piece in the
+//    workspace, takes a ticket from an atomic counter, and the last piece to
+//    arrive merges all pieces and writes the output (nothing ever waits for
+//    another CTA; the counter is reset by the merger).
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kMaxConsumerWarps = 6;  // rows T*G <= 48
+constexpr int kEnd = 1, kBad = 2;
+constexpr int kQuotaMin = 4;  // at least this many tiles per CTA
+constexpr float kRescaleGap = 8.0f;  // log2-domain slack before rescaling
+constexpr long long kMaxCounters = 65536;  // B * K * consumer warps per call
+
+struct AttnParams {
+    const void* q;
+    void* out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    float* partials;
+    int32_t* counters;
+    int32_t* status;
+    int B, T, N, K, G, R, nt;
+    int max_blocks, num_blocks;
+    float scale_log2;
+};
+
+struct StageMeta {
+    int b, k, blk_i, ctx;
+    int seg_start, nblk, quota, cta_start;
+    int flags, pad0, pad1, pad2;
+};
+
+template <int H>
+struct Cfg {
+    static constexpr int kTileBytes = 16 * H * 2;  // 16 tokens x H elements
+    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
+    static constexpr int kStages = (H == 128) ? 4 : 8;
+    static constexpr int kHalves = H / 64;  // 64-element (128-byte) swizzle spans
+    static constexpr int kSteps = H / 16;  // k16 steps of QK^T == m16 tiles of PV
+    static constexpr int kAccFloats = H / 4;  // accumulator floats per lane
+    static constexpr int kHeaderFloats = 32;  // m[8], l[8], flag, pad
+    static constexpr int kSectionFloats = kHeaderFloats + 32 * kAccFloats;
+    static constexpr size_t kSmem =
+        1024 + kStages * kStageBytes + kStages * 16 + kStages * sizeof(StageMeta) + 64;
+};
+
+__device__ __forceinline__ int seq_blocks(int ctx, int T, int max_blocks) {
+    return (ctx >= T && ctx >= 1 && ctx <= max_blocks * 16) ? (ctx + 15) >> 4 : 0;
+}
+
+// Zero the outputs of one sequence (T x N x H elements of 2 bytes).
+template <int H>
+__device__ void zero_sequence(const AttnParams& p, int b) {
+    const size_t n16 = (size_t)p.T * p.N * H * 2 / 16;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (size_t)b * n16 * 16);
+    for (size_t i = 0; i < n16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------------------
+template <int H>
+__device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
+                         uint8_t* stages, uint64_t* full, uint64_t* empty, StageMeta* meta,
+                         volatile int* abort_flag) {
+    using C = Cfg<H>;
+    constexpr unsigned FULL = 0xffffffffu;
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        tma_prefetch_desc(tmk);
+        tma_prefetch_desc(tmv);
+    }
+    // 1. Blocks per sequence and their prefix sum (lane l owns a run of b).
+    const int per = (p.B + 31) / 32;
+    const int lo = min(p.B, lane * per), hi = min(p.B, lo + per);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) {
+        const int n = seq_blocks(p.context_lens[b], p.T, p.max_blocks);
+        local += n;
+        if (n == 0 && blockIdx.x == 0) {
+            report(p.status, GQA_ERR_CONTEXT);
+            zero_sequence<H>(p, b);
+        }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int excl = incl - local;
+    const long long total = (long long)p.K * __shfl_sync(FULL, incl, 31);
+    const int quota = max((int)((total + gridDim.x - 1) / gridDim.x), kQuotaMin);
+    const long long c0 = (long long)blockIdx.x * quota;
+    const long long c1 = min(total, c0 + quota);
+    const uint64_t pol = policy_evict_first();
+
+    int it = 0;
+    bool aborted = false;
+    if (c0 < c1) {
+        // 2. Locate tile c0: the lane whose run of sequences contains it.
+        const bool mine = (long long)p.K * excl <= c0 && c0 < (long long)p.K * incl;
+        const unsigned owners = __ballot_sync(FULL, mine);
+        const int owner = __ffs(owners) - 1;
+        int fb = 0;
+        long long fbase = 0;
+        if (lane == owner) {
+            long long acc = (long long)p.K * excl;
+            for (int b = lo; b < hi; ++b) {
+                const long long n =
+                    (long long)p.K * seq_blocks(p.context_lens[b], p.T, p.max_blocks);
+                if (c0 < acc + n) {
+                    fb = b;
+                    fbase = acc;
+                    break;
+                }
+                acc += n;
+            }
+        }
+        int b = __shfl_sync(FULL, fb, owner);
+        long long base = __shfl_sync(FULL, fbase, owner);  // first tile of segment (b, 0)
+        int ctx = p.context_lens[b];
+        int nblk = seq_blocks(ctx, p.T, p.max_blocks);
+        const int rel = (int)(c0 - base);
+        int k = rel / nblk, i = rel % nblk;
+        int ids = 0, ids_base = -(1 << 30);
+
+        // 3. Stream the range.
+        for (long long x = c0; x < c1; ++x, ++it) {
+            if (i < ids_base || i >= ids_base + 32) {  // warp-uniform refill
+                ids_base = i;
+                ids = (i + lane < nblk) ? __ldg(p.block_tables + (size_t)b * p.max_blocks + i + lane)
+                                        : 0;
+            }
+            const int blk = __shfl_sync(FULL, ids, i - ids_base);
+            if (lane == 0) {
+                const int s = it % C::kStages;
+                bool ok = true;
+                if (it >= C::kStages)
+                    ok = mbar_wait(smem_addr(&empty[s]), ((it / C::kStages) - 1) & 1);
+                if (!ok) report(p.status, GQA_ERR_TIMEOUT);
+                if (!ok || *abort_flag) {
+                    *abort_flag = 1;
+                    aborted = true;
+                } else {
+                    StageMeta& m = meta[s];
+                    m.b = b;
+                    m.k = k;
+                    m.blk_i = i;
+                    m.ctx = ctx;
+                    m.seg_start = (int)(base + (long long)k * nblk);
+                    m.nblk = nblk;
+                    m.quota = quota;
+                    m.cta_start = (int)c0;
+                    const uint32_t fb_ = smem_addr(&full[s]);
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        report(p.status, GQA_ERR_BLOCK_ID);
+                        m.flags = kBad;
+                        mbar_arrive(fb_);
+                    } else {
+                        m.flags = 0;
+                        mbar_arrive_expect_tx(fb_, C::kStageBytes);
+                        const uint32_t dst = smem_addr(stages + (size_t)s * C::kStageBytes);
+#pragma unroll
+                        for (int hh = 0; hh < C::kHalves; ++hh)
+                            tma_load_3d(dst + hh * 2048, tmk, fb_, hh * 64, k, blk * 16, pol);
+#pragma unroll
+                        for (int hh = 0; hh < C::kHalves; ++hh)
+                            tma_load_3d(dst + C::kTileBytes + hh * 2048, tmv, fb_, hh * 64, k,
+                                        blk * 16, pol);
+                    }
+                }
+            }
+            aborted = __shfl_sync(FULL, aborted, 0);
+            if (aborted) break;
+            if (++i == nblk) {
+                i = 0;
+                if (++k == p.K) {
+                    k = 0;
+                    base += (long long)p.K * nblk;
+                    if (x + 1 < c1) {
+                        do {
+                            ++b;
+                            ctx = p.context_lens[b];
+                            nblk = seq_blocks(ctx, p.T, p.max_blocks);
+                        } while (nblk == 0);
+                    }
+                    ids_base = -(1 << 30);
+                }
+            }
+        }
+    }
+    // 4. End marker (a stage with no data), then, after an abort, let every
+    //    copy already issued land before the CTA exits.
+    if (lane == 0) {
+        if (!aborted) {
+            const int s = it % C::kStages;
+            const bool ok =
+                it < C::kStages || mbar_wait(smem_addr(&empty[s]), ((it / C::kStages) - 1) & 1);
+            if (ok) {
+                meta[s].flags = kEnd;
+                mbar_arrive(smem_addr(&full[s]));
+            } else {
+                report(p.status, GQA_ERR_TIMEOUT);
+                *abort_flag = 1;
+                aborted = true;
+            }
+        }
+        if (aborted) {
+            for (int j = max(0, it - C::kStages); j < it; ++j)
+                mbar_wait(smem_addr(&full[j % C::kStages]), (j / C::kStages) & 1);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+template <int H, bool BF16>
+struct Consumer {
+    using C = Cfg<H>;
+    using E = Elt<BF16>;
+    static constexpr unsigned FULL = 0xffffffffu;
+
+    const AttnParams& p;
+    const int w, lane, g, q4;
+    int t0, t1;  // new-token index of this lane's two C-fragment rows
+    uint32_t qf[C::kSteps][2];
+    float acc[C::kSteps][4];
+    float m0, m1, l0, l1;
+    bool bad;
+    int cb, ck, cctx, cstart, cnblk, cquota, ccta0;
+
+    __device__ Consumer(const AttnParams& p_, int w_)
+        : p(p_), w(w_), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), q4(threadIdx.x & 3) {
+        const int r0 = 8 * w + 2 * q4;
+        t0 = min(r0 / p.G, p.T - 1);
+        t1 = min((r0 + 1) / p.G, p.T - 1);
+    }
+
+    __device__ void begin(const StageMeta& md) {
+        cb = md.b;
+        ck = md.k;
+        cctx = md.ctx;
+        cstart = md.seg_start;
+        cnblk = md.nblk;
+        cquota = md.quota;
+        ccta0 = md.cta_start;
+        bad = false;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+        // B fragments of Q^T (k = head dim, n = query row): row 8w+g, dims
+        // kk*16 + 2*q4 + {0,1} and the same + 8.
+        const int r = 8 * w + g;
+        if (r < p.R) {
+            const int t = r / p.G, gg = r % p.G;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                static_cast<const uint16_t*>(p.q) +
+                (((size_t)cb * p.T + t) * p.N + (size_t)ck * p.G + gg) * H);
+#pragma unroll
+            for (int kk = 0; kk < C::kSteps; ++kk) {
+                qf[kk][0] = __ldg(qrow + kk * 8 + q4);
+                qf[kk][1] = __ldg(qrow + kk * 8 + 4 + q4);
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < C::kSteps; ++kk) qf[kk][0] = qf[kk][1] = 0u;
+        }
+    }
+
+    __device__ void tile(uint32_t kbase, const StageMeta& md) {
+        const uint32_t vbase = kbase + C::kTileBytes;
+        // ---- S^T = K_tile . Q^T --------------------------------------------
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int chk = lane >> 4;
+#pragma unroll
+            for (int kk = 0; kk < C::kSteps; ++kk) {
+                const int hh = kk >> 2;
+                const int chunk = ((kk & 3) << 1) + chk;
+                uint32_t a[4];
+                ldsm_x4(kbase + hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4), a);
+                E::mma(c, a, qf[kk][0], qf[kk][1]);
+            }
+        }
+        float s0 = c[0] * p.scale_log2, s1 = c[1] * p.scale_log2;
+        float s2 = c[2] * p.scale_log2, s3 = c[3] * p.scale_log2;
+        const int pos0 = md.blk_i * 16 + g, pos8 = pos0 + 8;
+        if (md.blk_i * 16 + 15 > md.ctx - p.T) {  // some position hidden from some row
+            const int lim0 = md.ctx - p.T + t0, lim1 = md.ctx - p.T + t1;
+            if (pos0 > lim0) s0 = -INFINITY;
+            if (pos0 > lim1) s1 = -INFINITY;
+            if (pos8 > lim0) s2 = -INFINITY;
+            if (pos8 > lim1) s3 = -INFINITY;
+        }
+        // ---- running max (log2 domain), lazy rescale ----------------------------
+        float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, o));
+            x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, o));
+        }
+        const bool need0 = x0 > m0 + kRescaleGap, need1 = x1 > m1 + kRescaleGap;
+        if (__any_sync(FULL, need0 || need1)) {
+            const float n0 = need0 ? x0 : m0, n1 = need1 ? x1 : m1;
+            const float f0 = need0 ? fast_exp2(m0 - n0) : 1.f;
+            const float f1 = need1 ? fast_exp2(m1 - n1) : 1.f;
+            l0 *= f0;
+            l1 *= f1;
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt) {
+                acc[mt][0] *= f0;
+                acc[mt][1] *= f1;
+                acc[mt][2] *= f0;
+                acc[mt][3] *= f1;
+            }
+            m0 = n0;
+            m1 = n1;
+        }
+        const float ref0 = (m0 == -INFINITY) ? 0.f : m0;
+        const float ref1 = (m1 == -INFINITY) ? 0.f : m1;
+        const uint32_t pt0 = E::pack(fast_exp2(s0 - ref0), fast_exp2(s1 - ref1));  // token g
+        const uint32_t pt1 = E::pack(fast_exp2(s2 - ref0), fast_exp2(s3 - ref1));  // token g+8
+        l0 += E::lo(pt0) + E::lo(pt1);
+        l1 += E::hi(pt0) + E::hi(pt1);
+        // P^T as the B operand: tokens 2*q4+{0,1} (+8) of query row g.
+        const uint32_t pb0 = movm_t(pt0), pb1 = movm_t(pt1);
+        // ---- O^T += V_tile^T . P^T --------------------------------------------
+        uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
+        const bool tail = md.blk_i * 16 + 16 > md.ctx;
+        if (tail) {  // NaN-safe: zero V elements of slots past the context
+            const int pb = md.blk_i * 16 + 2 * q4;
+            v01 = (pb < md.ctx ? 0x0000ffffu : 0u) | (pb + 1 < md.ctx ? 0xffff0000u : 0u);
+            v89 = (pb + 8 < md.ctx ? 0x0000ffffu : 0u) | (pb + 9 < md.ctx ? 0xffff0000u : 0u);
+        }
+        const int tok = (lane & 7) + (lane >> 4) * 8;
+        const int dof = ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt) {
+            const int d0 = mt * 16 + dof;
+            const int hh = d0 >> 6;
+            const int chunk = (d0 & 63) >> 3;
+            uint32_t a[4];
+            ldsm_x4_t(vbase + hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4), a);
+            if (tail) {
+                a[0] &= v01;
+                a[1] &= v01;
+                a[2] &= v89;
+                a[3] &= v89;
+            }
+            E::mma(acc[mt], a, pb0, pb1);
+        }
+    }
+
+    // Normalise and store rows 8w..8w+7 of segment (cb, ck).
+    __device__ void store(float L0, float L1, bool is_bad) {
+        const float i0 = (!is_bad && L0 > 0.f) ? 1.f / L0 : 0.f;
+        const float i1 = (!is_bad && L1 > 0.f) ? 1.f / L1 : 0.f;
+        const int r = 8 * w + g;
+        uint32_t* dst = nullptr;
+        if (r < p.R) {
+            const int t = r / p.G, gg = r % p.G;
+            dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) +
+                                              (((size_t)cb * p.T + t) * p.N +
+                                               (size_t)ck * p.G + gg) * H);
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt) {
+            uint32_t x = is_bad ? 0u : E::pack(acc[mt][0] * i0, acc[mt][1] * i1);
+            uint32_t y = is_bad ? 0u : E::pack(acc[mt][2] * i0, acc[mt][3] * i1);
+            x = movm_t(x);  // -> row g, dims mt*16 + 2*q4 + {0,1}
+            y = movm_t(y);  // -> row g, dims mt*16 + 8 + 2*q4 + {0,1}
+            if (dst) {
+                dst[mt * 8 + q4] = x;
+                dst[mt * 8 + 4 + q4] = y;
+            }
+        }
+    }
+
+    __device__ float* section(int cta, int slot) const {
+        return p.partials + ((size_t)(cta * 2 + slot) * p.nt + w) * C::kSectionFloats;
+    }
+
+    __device__ void finalize() {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l0 += __shfl_xor_sync(FULL, l0, o);
+            l1 += __shfl_xor_sync(FULL, l1, o);
+        }
+        const int first = cstart / cquota;
+        const int last = (cstart + cnblk - 1) / cquota;
+        if (first == last) {
+            store(l0, l1, bad);
+            return;
+        }
+        const int me = blockIdx.x;
+        const int slot = (me == first && ccta0 < cstart) ? 1 : 0;
+        float* sec = section(me, slot);
+        if (g == 0) {
+            sec[2 * q4] = m0;
+            sec[2 * q4 + 1] = m1;
+            sec[8 + 2 * q4] = l0;
+            sec[8 + 2 * q4 + 1] = l1;
+        }
+        if (lane == 0) sec[16] = bad ? 1.f : 0.f;
+        float4* a4 = reinterpret_cast<float4*>(sec + C::kHeaderFloats) + lane * C::kSteps;
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt)
+            a4[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+        __threadfence();
+        __syncwarp();
+        int is_last = 0;
+        if (lane == 0) {
+            int32_t* ctr = p.counters + ((size_t)cb * p.K + ck) * p.nt + w;
+            const int old = atomicAdd(ctr, 1);
+            is_last = (old == last - first);
+            if (is_last) *ctr = 0;  // every piece has arrived: ready for the next call
+        }
+        is_last = __shfl_sync(FULL, is_last, 0);
+        if (!is_last) return;
+        __threadfence();
+        // ---- merge the pieces (log-sum-exp weights) ---------------------------
+        float M0 = -INFINITY, M1 = -INFINITY;
+        bool any_bad = false;
+        for (int c = first; c <= last; ++c) {
+            const int sl = (c == first && (long long)c * cquota < cstart) ? 1 : 0;
+            const float* sc = section(c, sl);
+            M0 = fmaxf(M0, __ldcg(sc + 2 * q4));
+            M1 = fmaxf(M1, __ldcg(sc + 2 * q4 + 1));
+            any_bad |= __ldcg(sc + 16) != 0.f;
+        }
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+        float L0 = 0.f, L1 = 0.f;
+        for (int c = first; c <= last; ++c) {
+            const int sl = (c == first && (long long)c * cquota < cstart) ? 1 : 0;
+            const float* sc = section(c, sl);
+            const float mc0 = __ldcg(sc + 2 * q4), mc1 = __ldcg(sc + 2 * q4 + 1);
+            const float w0 = (mc0 == -INFINITY) ? 0.f : fast_exp2(mc0 - M0);
+            const float w1 = (mc1 == -INFINITY) ? 0.f : fast_exp2(mc1 - M1);
+            L0 += w0 * __ldcg(sc + 8 + 2 * q4);
+            L1 += w1 * __ldcg(sc + 8 + 2 * q4 + 1);
+            const float4* b4 = reinterpret_cast<const float4*>(sc + C::kHeaderFloats) +
+                               lane * C::kSteps;
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt) {
+                const float4 v = __ldcg(b4 + mt);
+                acc[mt][0] += w0 * v.x;
+                acc[mt][1] += w1 * v.y;
+                acc[mt][2] += w0 * v.z;
+                acc[mt][3] += w1 * v.w;
+            }
+        }
+        store(L0, L1, any_bad);
+    }
+};
+
+template <int H, bool BF16>
+__device__ void consumer(const AttnParams& p, uint8_t* stages, uint64_t* full, uint64_t* empty,
+                         const StageMeta* meta, volatile int* abort_flag, int w) {
+    using C = Cfg<H>;
+    Consumer<H, BF16> cs(p, w);
+    const int lane = threadIdx.x & 31;
+    int cur = -1;
+    for (int it = 0;; ++it) {
+        const int s = it % C::kStages;
+        if (!mbar_wait(smem_addr(&full[s]), (it / C::kStages) & 1)) {
+            if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return;
+        }
+        const StageMeta md = meta[s];
+        if (md.flags & kEnd) {
+            if (cur >= 0) cs.finalize();
+            return;
+        }
+        const int seg = md.b * p.K + md.k;
+        if (seg != cur) {
+            if (cur >= 0) cs.finalize();
+            cs.begin(md);
+            cur = seg;
+        }
+        if (md.flags & kBad)
+            cs.bad = true;
+        else
+            cs.tile(smem_addr(stages + (size_t)s * C::kStageBytes), md);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+    }
+}
+
+template <int H, bool BF16>
+__global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
+    attention_kernel(const __grid_constant__ CUtensorMap tmk,
+                     const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+    using C = Cfg<H>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+    uint64_t* empty = full + C::kStages;
+    StageMeta* meta = reinterpret_cast<StageMeta*>(empty + C::kStages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + C::kStages);
+
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), p.nt);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == p.nt)
+        producer<H>(&tmk, &tmv, p, stages, full, empty, meta, abort_flag);
+    else
+        consumer<H, BF16>(p, stages, full, empty, meta, abort_flag, warp);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+template <int H, bool BF16>
+const void* kernel_ptr() {
+    return reinterpret_cast<const void*>(&attention_kernel<H, BF16>);
+}
+
+const void* pick_kernel(int H, bool bf16) {
+    if (H == 64) return bf16 ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
+    return bf16 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+}
+
+size_t smem_for(int H) { return H == 64 ? Cfg<64>::kSmem : Cfg<128>::kSmem; }
+size_t section_floats(int H) {
+    return H == 64 ? Cfg<64>::kSectionFloats : Cfg<128>::kSectionFloats;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
+    return fn;
+}
+
+// 3-D view of a cache [num_blocks][16][K][H]: (h, kv head, block*16 + row);
+// one box = 16 rows x 64 elements of one KV head, 128-byte swizzled.
+bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)s.H, (cuuint64_t)s.K,
+                                (cuuint64_t)s.num_blocks * 16};
+    const cuuint64_t strides[2] = {(cuuint64_t)s.H * 2, (cuuint64_t)s.K * s.H * 2};
+    const cuuint32_t box[3] = {64, 1, 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, s.dtype == GQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// CTAs of one variant resident per SM, queried once per (device, variant) so
+// that later calls -- including calls being captured into a CUDA graph -- make
+// no attribute or occupancy API calls.
+int resident_ctas(int H, bool bf16, int nt, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const auto key = std::make_tuple(dev, H, (int)bf16, nt);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const void* kern = pick_kernel(H, bf16);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return 0;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * (nt + 1), smem) !=
+        cudaSuccess)
+        return 0;
+    cache[key] = occ;
+    return occ;
+}
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    static int cache[64] = {0};
+    if (dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
+    if (s.B < 0 || s.T < 1 || s.N < 1 || s.K < 1 || s.N % s.K != 0) return GQA_ERR_SHAPE;
+    if (s.H != 64 && s.H != 128) return GQA_ERR_SHAPE;
+    if (s.block_size != 16 || s.num_blocks < 1 || s.max_blocks_per_seq < 1) return GQA_ERR_SHAPE;
+    if ((long long)s.num_blocks * 16 > (1ll << 31) - 1) return GQA_ERR_SHAPE;
+    if ((long long)s.max_blocks_per_seq * 16 > (1ll << 30)) return GQA_ERR_SHAPE;
+    if (s.dtype != GQA_F16 && s.dtype != GQA_BF16) return GQA_ERR_DTYPE;
+    const int G = s.N / s.K;
+    const long long R = (long long)s.T * G;
+    if (R > 8 * kMaxConsumerWarps) return GQA_ERR_SHAPE;
+    const int nt = (int)((R + 7) / 8);
+    const int threads = 32 * (nt + 1);
+    const size_t smem = smem_for(s.H);
+    const int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, smem);
+    if (occ < 1) return GQA_ERR_CUDA;
+    const int sms = device_sm_count();
+    if (sms < 1) return GQA_ERR_CUDA;
+    long long grid = (long long)sms * occ;
+    const long long tiles_max = (long long)s.B * s.K * s.max_blocks_per_seq;
+    grid = std::min<long long>(grid, std::max<long long>(1, (tiles_max + kQuotaMin - 1) / kQuotaMin));
+    plan->grid = (int)grid;
+    plan->consumer_warps = nt;
+    plan->threads = threads;
+    plan->smem = smem;
+    // The ticket counters live in a fixed region at the start of every
+    // workspace, whatever the shape, and partial results always start after
+    // it: partial data of one call can then never sit where a later call of
+    // another shape expects zeroed counters.
+    if ((long long)s.B * s.K * nt > kMaxCounters) return GQA_ERR_SHAPE;
+    plan->counters_bytes = (size_t)kMaxCounters * 4;
+    plan->partial_floats_per_slot = section_floats(s.H) * nt;
+    plan->workspace = plan->counters_bytes + (size_t)grid * 2 * plan->partial_floats_per_slot * 4;
+    return GQA_OK;
+}
+
+gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
+                            const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            void* out, void* workspace, int32_t* dev_status,
+                            cudaStream_t stream) {
+    if (s.B == 0) return GQA_OK;
+    CUtensorMap tmk, tmv;
+    if (!encode_cache_map(&tmk, k_cache, s) || !encode_cache_map(&tmv, v_cache, s))
+        return GQA_ERR_CUDA;
+    AttnParams p;
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.counters = static_cast<int32_t*>(workspace);
+    p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes);
+    p.status = dev_status;
+    p.B = s.B;
+    p.T = s.T;
+    p.N = s.N;
+    p.K = s.K;
+    p.G = s.N / s.K;
+    p.R = s.T * p.G;
+    p.nt = plan.consumer_warps;
+    p.max_blocks = s.max_blocks_per_seq;
+    p.num_blocks = s.num_blocks;
+    const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
+    p.scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
+    const bool bf16 = s.dtype == GQA_BF16;
+    const dim3 grid(plan.grid), block(plan.threads);
+    if (s.H == 64) {
+        if (bf16)
+            attention_kernel<64, true><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
+        else
+            attention_kernel<64, false><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
+    } else {
+        if (bf16)
+            attention_kernel<128, true><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
+        else
+            attention_kernel<128, false><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
+    }
+    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace gqa

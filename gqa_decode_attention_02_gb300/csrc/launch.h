@@ -1,0 +1,45 @@
+// launch.h -- host-side launchers shared between the kernel files and api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gqa_decode.h"
+
+namespace gqa {
+
+// Launch plan of the attention kernel for one shape on the current device.
+struct AttnPlan {
+    int grid;            // persistent CTAs
+    int consumer_warps;  // one per 8 query rows (rows = T * G)
+    int threads;
+    size_t smem;         // dynamic shared memory per CTA
+    size_t counters_bytes;
+    size_t partial_floats_per_slot;
+    size_t workspace;    // total bytes
+};
+
+// Fills `plan`; returns GQA_OK or a validation error.
+gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan);
+
+gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
+                            const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* context_lens,
+                            void* out, void* workspace, int32_t* dev_status,
+                            cudaStream_t stream);
+
+gqa_status launch_kv_append(const gqa_shape& s, const void* k_new, const void* v_new,
+                            void* k_cache, void* v_cache, const int32_t* block_tables,
+                            const int32_t* context_lens, int32_t* dev_status,
+                            cudaStream_t stream);
+
+gqa_status launch_accept_prefix(int B, int T, int V, const float* logits,
+                                const int32_t* draft, int32_t* accepted,
+                                int32_t* next_token, int32_t* ctx_io, int32_t* dev_status,
+                                cudaStream_t stream);
+
+// Cached per-device SM count (0 on failure).
+int device_sm_count();
+
+}  // namespace gqa

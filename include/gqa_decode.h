@@ -1,0 +1,187 @@
+/*
+ * gqa_decode.h -- C ABI of the paged grouped-query decode-attention library
+ * (hand-written CUDA for sm_103a / GB300).
+ *
+ * Four operations on a paged KV cache, all asynchronous on the caller's stream:
+ *   gqa_kv_append        write the T newest tokens' keys and values into the cache
+ *   gqa_decode_attention attention of one new query token per sequence (T == 1)
+ *   gqa_verify_attention the same for T >= 1 new tokens, causal among them
+ *   gqa_accept_prefix    greedy longest-prefix acceptance of draft tokens
+ *
+ * Sources (web pages, cited by title and section):
+ *   "CS336, лекции 10 и 12: инференс и оценка моделей" (CS336 lectures 10/12,
+ *     Russian translation): §"Напоминание: трансформер" (notation B,T,N,K,G,H),
+ *     §"Арифметическая интенсивность инференса" (KV cache; attention of the new
+ *     token over the cache; decode is memory-bound), §"Уменьшаем KV-кэш" (GQA),
+ *     §"Спекулятивное сэмплирование" (verify several drafted tokens in one pass),
+ *     §"PagedAttention" (fixed-size blocks + per-sequence block table; fused
+ *     block-read + attention kernel; FlashDecoding).
+ *   "جعل inference رخيصًا: KV cache وbatching والتكميم" (KV cache, batching and
+ *     quantization): the KV-cache section (cache == recompute; bytes per token)
+ *     and the speculative-decoding section (greedy acceptance).
+ *   "Болжау арқылы Sonar модельдерін жылдамдату" (Accelerating Sonar through
+ *     speculation): §"Спекулятивті кодтан шығару" (longest accepted prefix plus
+ *     one target token) and §"Спекулятивті кодтан шығару арқылы инференс"
+ *     (appending accepted tokens on the GPU, avoiding a GPU->CPU sync).
+ *
+ * Conventions for every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, except the
+ *     `const gqa_shape*`, which is a host pointer read during the call only.
+ *     The library allocates no device memory and keeps no pointer after return.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work is
+ *     enqueued on it; the call returns without synchronising.
+ *   - The return value reports host-side validation only (arguments, shapes,
+ *     alignment, launch errors).  Problems found in device data (a context
+ *     length out of range, a bad block id) are reported through the optional
+ *     device int32 `dev_status`: the first nonzero gqa_status code written
+ *     wins, later ones are dropped; the library never clears it.  The affected
+ *     sequence's outputs are written as zeros (attention) or left untouched
+ *     (append).  No kernel ever traps or waits without a time limit.
+ *   - Layouts are dense row-major with the last dimension contiguous:
+ *       q, out        [B][T][N][H]      (dtype of the shape)
+ *       k_new, v_new  [B][T][K][H]
+ *       k/v cache     [num_blocks][block_size][K][H]
+ *       block_tables  int32 [B][max_blocks_per_seq]: logical block i of
+ *                     sequence b -> physical block id
+ *       context_lens  int32 [B]: tokens held for sequence b INCLUDING the T new
+ *                     ones; new token t sits at position context_lens[b]-T+t.
+ *     q, out, k/v caches, k_new, v_new must be 16-byte aligned.
+ *   - Query head n reads KV head n / G, G = N / K (contiguous groups).
+ */
+#ifndef GQA_DECODE_H
+#define GQA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_NULL = 1,      /* a required pointer is NULL */
+    GQA_ERR_SHAPE = 2,     /* unsupported or inconsistent sizes (see each call) */
+    GQA_ERR_DTYPE = 3,     /* dtype not GQA_F16 / GQA_BF16 */
+    GQA_ERR_ALIGN = 4,     /* a tensor pointer is not 16-byte aligned */
+    GQA_ERR_WORKSPACE = 5, /* workspace NULL or smaller than the size query */
+    GQA_ERR_CUDA = 6,      /* a CUDA runtime / driver call failed */
+    GQA_ERR_CONTEXT = 7,   /* device: context_lens[b] < T, < 1 or > capacity */
+    GQA_ERR_BLOCK_ID = 8,  /* device: a block-table entry in use not in [0,num_blocks) */
+    GQA_ERR_TIMEOUT = 9    /* device: a bounded wait inside a kernel gave up */
+} gqa_status;
+
+typedef enum { GQA_F16 = 0, GQA_BF16 = 1 } gqa_dtype;
+
+/* Problem sizes, in the pages' notation (CS336 lecture 10, §"Напоминание:
+ * трансформер"): B sequences, T new query tokens per sequence, N query heads,
+ * K key/value heads (G = N/K), head size H. */
+typedef struct {
+    int B;
+    int T;
+    int N;
+    int K;
+    int H;                  /* 64 or 128 */
+    int block_size;         /* tokens per cache block; must be 16 */
+    int num_blocks;         /* physical blocks in each cache tensor */
+    int max_blocks_per_seq; /* columns of block_tables */
+    gqa_dtype dtype;        /* element type of q, out, caches, k_new, v_new */
+    float scale;            /* score scale; <= 0 selects 1/sqrt(H) */
+} gqa_shape;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int gqa_version(void);
+
+/* Static description of a status code (never NULL). */
+const char *gqa_status_string(int status);
+
+/* KV append.  KV-cache section of "جعل inference رخيصًا: KV cache وbatching
+ * والتكميم" (each new token's key/value vectors are stored once) with the block
+ * addressing of CS336 lecture 10 §"PagedAttention": for b < B, t < T, position
+ * pos = context_lens[b] - T + t goes to block block_tables[b][pos / 16], row
+ * pos % 16.  k_new[b][t] (K*H elements) is copied there bit for bit; same for
+ * v_new.  Requires T >= 1, K >= 1, H in {64,128}.  Device errors: a sequence
+ * with context_lens[b] < T or > 16*max_blocks_per_seq is skipped
+ * (GQA_ERR_CONTEXT); a token whose block id is out of range is skipped
+ * (GQA_ERR_BLOCK_ID). */
+gqa_status gqa_kv_append(const gqa_shape *shape, const void *k_new, const void *v_new,
+                         void *k_cache, void *v_cache, const int32_t *block_tables,
+                         const int32_t *context_lens, int32_t *dev_status,
+                         void *stream);
+
+/* Bytes of device workspace gqa_decode_attention / gqa_verify_attention need
+ * for this shape on the CURRENT device: a fixed 256 KiB region of int32
+ * ticket counters (one per sequence, KV head and group of 8 query rows; at
+ * most 65536, else the shape is rejected) followed by the split-context
+ * partial results.  Returns 0 if the shape is invalid.  The workspace must be
+ * zero-filled before its first use (for example with gqa_workspace_clear);
+ * every call whose kernels finish without GQA_ERR_TIMEOUT leaves the counter
+ * region zero-filled again (the partial-result region is scratch and never
+ * needs clearing), so one buffer can be reused by later calls of any shape
+ * that fits.  Calls that share a workspace must not overlap on the GPU (use
+ * one stream, or one workspace per stream).  After GQA_ERR_TIMEOUT, clear the
+ * workspace again before reusing it. */
+size_t gqa_attention_workspace_size(const gqa_shape *shape);
+
+/* Zero-fill `bytes` of workspace on `stream` (a cudaMemsetAsync). */
+gqa_status gqa_workspace_clear(void *workspace, size_t bytes, void *stream);
+
+/* Decode attention, T == 1.  CS336 lecture 10 §"Арифметическая интенсивность
+ * инференса" (Y = softmax(Q K^T) V of the new token over the cached keys and
+ * values) with GQA from §"Уменьшаем KV-кэш" and paged reads from
+ * §"PagedAttention".  For each b, query head n (KV head k = n / G):
+ *   s_j = scale * <q[b][0][n], K_b[j][k]>,   j = 0 .. context_lens[b]-1
+ *   out[b][0][n] = sum_j softmax(s)_j * V_b[j][k]
+ * where K_b[j] is row j % 16 of block block_tables[b][j / 16].  fp32
+ * accumulation; `out` gets q's dtype (round to nearest even).  The context is
+ * split across thread blocks and the pieces merged with their log-sum-exp
+ * weights (FlashDecoding, named in §"PagedAttention"); the result equals the
+ * unsplit softmax up to rounding.  Requires: T == 1, N % K == 0, H in {64,128},
+ * block_size == 16, N/K <= 48, a workspace of at least
+ * gqa_attention_workspace_size(shape) bytes (zeroed, see above).  Device
+ * errors: a sequence whose context length is < 1, < T or above
+ * 16*max_blocks_per_seq (GQA_ERR_CONTEXT) or whose table holds a block id
+ * outside [0, num_blocks) among its first ceil(len/16) entries
+ * (GQA_ERR_BLOCK_ID) gets an all-zero output. */
+gqa_status gqa_decode_attention(const gqa_shape *shape, const void *q,
+                                const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables,
+                                const int32_t *context_lens, void *out,
+                                void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, void *stream);
+
+/* Verify attention, T >= 1 new tokens per sequence (speculative verification:
+ * CS336 lecture 10 §"Спекулятивное сэмплирование" -- the target model scores
+ * several drafted tokens in one pass).  As gqa_decode_attention, except that
+ * new token t (t < T) sees cached positions j <= context_lens[b] - T + t: the
+ * whole prefix plus the new tokens up to itself.  Requires T * (N/K) <= 48. */
+gqa_status gqa_verify_attention(const gqa_shape *shape, const void *q,
+                                const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables,
+                                const int32_t *context_lens, void *out,
+                                void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, void *stream);
+
+/* Greedy prefix acceptance.  Speculative-decoding section of "جعل inference
+ * رخيصًا" (a drafted token is kept only if the target would produce it) and
+ * "Болжау арқылы Sonar модельдерін жылдамдату" §"Спекулятивті кодтан шығару"
+ * (longest accepted prefix, then one token from the target's logits).
+ *   target_logits fp32 [B][T][V]; draft_ids int32 [B][T-1]
+ *   g_t = argmax_v target_logits[b][t][v]   (first index wins ties; NaN is
+ *         larger than any number and the first NaN wins)
+ *   accepted[b]   = largest a <= T-1 with draft_ids[b][j] == g_j for all j < a
+ *   next_token[b] = g_a
+ *   context_lens_inout[b] -= T-1-a  (if not NULL: drops the KV entries of the
+ *                                    rejected drafts, on the device)
+ * Requires B >= 0, 1 <= T <= 64, V >= 1.  target_logits must be 16-byte
+ * aligned.  Device errors: a context length that would drop below zero is
+ * left unchanged (GQA_ERR_CONTEXT). */
+gqa_status gqa_accept_prefix(int B, int T, int V, const float *target_logits,
+                             const int32_t *draft_ids, int32_t *accepted,
+                             int32_t *next_token, int32_t *context_lens_inout,
+                             int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQA_DECODE_H */

@@ -1,0 +1,91 @@
+"""CPU checks of the C ABI: the library loads, exports every symbol the header
+declares, and its host-side validation rejects bad arguments without touching
+a GPU (these calls fail before any launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gqa_decode_attention_02_gb300 import _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "gqa_decode.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for op in ("gqa_kv_append", "gqa_decode_attention", "gqa_verify_attention",
+               "gqa_accept_prefix"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    for name in declared_functions():
+        assert hasattr(cuda_lib, name), name
+    assert set(_lib.EXPORTS) <= set(declared_functions())
+
+
+def test_version_and_status_strings(cuda_lib):
+    assert cuda_lib.gqa_version() >= 100
+    assert _lib.status_string(0) == "ok"
+    assert "aligned" in _lib.status_string(4)
+    assert _lib.status_string(12345) == "unknown status"
+
+
+def _shape(**kw):
+    d = dict(B=2, T=1, N=8, K=2, H=128, block_size=16, num_blocks=10, max_blocks_per_seq=4,
+             dtype=1, scale=0.0)
+    d.update(kw)
+    return _lib.Shape(**d)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=7), 2),            # N % K != 0
+    (dict(H=96), 2),           # unsupported head size
+    (dict(block_size=32), 2),  # only 16-token blocks
+    (dict(T=0), 2),
+    (dict(dtype=5), 3),
+    (dict(N=98, K=2), 2),      # 49 rows per KV head > 48
+])
+def test_validation_rejects_bad_shapes(cuda_lib, kw, code):
+    s = _shape(**kw)
+    fake = ctypes.c_void_p(16)
+    rc = cuda_lib.gqa_verify_attention(ctypes.byref(s), fake, fake, fake, fake, fake, fake,
+                                       fake, 1 << 30, None, None)
+    assert rc == code
+
+
+def test_validation_rejects_null_and_misaligned(cuda_lib):
+    s = _shape()
+    fake = ctypes.c_void_p(16)
+    rc = cuda_lib.gqa_decode_attention(ctypes.byref(s), None, fake, fake, fake, fake, fake,
+                                       fake, 1 << 30, None, None)
+    assert rc == 1
+    odd = ctypes.c_void_p(18)
+    rc = cuda_lib.gqa_decode_attention(ctypes.byref(s), odd, fake, fake, fake, fake, fake,
+                                       fake, 1 << 30, None, None)
+    assert rc == 4
+    rc = cuda_lib.gqa_decode_attention(ctypes.byref(_shape(T=2)), fake, fake, fake, fake, fake,
+                                       fake, fake, 1 << 30, None, None)
+    assert rc == 2  # decode is T == 1 only
+    rc = cuda_lib.gqa_kv_append(ctypes.byref(s), None, fake, fake, fake, fake, fake, None, None)
+    assert rc == 1
+    rc = cuda_lib.gqa_accept_prefix(2, 0, 10, fake, fake, fake, fake, None, None, None)
+    assert rc == 2
+    rc = cuda_lib.gqa_accept_prefix(2, 3, 10, odd, fake, fake, fake, None, None, None)
+    assert rc == 4
+
+
+def test_empty_batch_is_a_no_op(cuda_lib):
+    s = _shape(B=0)
+    rc = cuda_lib.gqa_kv_append(ctypes.byref(s), None, None, None, None, None, None, None,
+                                None)
+    assert rc == 0
+    rc = cuda_lib.gqa_accept_prefix(0, 3, 10, None, None, None, None, None, None, None)
+    assert rc == 0

@@ -1,0 +1,61 @@
+"""GPU accept_prefix: bit-exact against the oracle (integers), ties, NaN, -0."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_attention_02_gb300 as gq
+import oracle
+from helpers import small
+
+pytestmark = pytest.mark.gpu
+
+
+def run(lg, draft, ctx, dev):
+    lg_d = torch.as_tensor(lg).to(dev).contiguous()
+    dr_d = torch.as_tensor(draft, dtype=torch.int32).to(dev).contiguous()
+    ctx_d = None if ctx is None else torch.as_tensor(ctx, dtype=torch.int32).to(dev)
+    acc, nxt = gq.accept_prefix(lg_d, dr_d, ctx_d)
+    torch.cuda.synchronize()
+    return acc.cpu().numpy(), nxt.cpu().numpy(), None if ctx_d is None else ctx_d.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,T,V", [(16, 5, 32000), (3, 1, 7), (4, 8, 50257), (2, 64, 999),
+                                   (300, 2, 100)])
+def test_accept_matches_oracle(gpu, B, T, V):
+    w = small(B=B, T=T, N=1, K=1, H=64, ctx=(70,) * B, seed=B + T, vocab=V)
+    ctx = np.full(B, 70, np.int32)
+    ra, rn, rc = oracle.accept_prefix(w.logits, w.draft, ctx)
+    ga, gn, gc = run(w.logits, w.draft, ctx, gpu)
+    np.testing.assert_array_equal(ga, ra)
+    np.testing.assert_array_equal(gn, rn)
+    np.testing.assert_array_equal(gc, rc)
+
+
+def test_accept_ties_nan_negative_zero(gpu):
+    rng = np.random.default_rng(3)
+    B, T, V = 64, 4, 37
+    lg = rng.integers(-2, 3, size=(B, T, V)).astype(np.float32)  # heavy ties
+    lg[::3, :, 5] = np.nan
+    lg[1::4, :, :] = 0.0
+    lg[1::4, :, 7] = -0.0
+    lg[2::5] = -np.inf
+    draft = rng.integers(0, V, size=(B, T - 1)).astype(np.int32)
+    for b in range(0, B, 2):  # make some drafts right
+        for t in range(T - 1):
+            draft[b, t] = oracle.argmax(lg[b, t])
+    ra, rn, _ = oracle.accept_prefix(lg, draft)
+    ga, gn, _ = run(lg, draft, None, gpu)
+    np.testing.assert_array_equal(ga, ra)
+    np.testing.assert_array_equal(gn, rn)
+
+
+def test_context_length_update_underflow_is_reported(gpu):
+    lg = np.zeros((2, 3, 4), np.float32)
+    draft = np.full((2, 2), 3, np.int32)  # argmax is 0 everywhere -> reject all
+    ctx = torch.tensor([5, 1], dtype=torch.int32, device=gpu)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    gq.accept_prefix(torch.as_tensor(lg).to(gpu), torch.as_tensor(draft).to(gpu), ctx,
+                     status=st)
+    torch.cuda.synchronize()
+    assert ctx.cpu().tolist() == [3, 1]
+    assert int(st.item()) == 7

@@ -1,0 +1,183 @@
+"""GPU parity of kv_append, decode_attention and verify_attention against the
+fp64 oracle, element by element, at sizes the oracle finishes in seconds that
+still span many 16-token tiles, several split pieces and ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_attention_02_gb300 as gq
+import oracle
+from helpers import assert_close, small, to
+
+pytestmark = pytest.mark.gpu
+
+
+def run_attention(w, dev, fn=None, status=None):
+    wd = to(w, dev)
+    fn = fn or (gq.decode_attention if w.T == 1 else gq.verify_attention)
+    out = fn(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables, wd.context_lens,
+             status=status)
+    torch.cuda.synchronize()
+    return out.float().cpu().double().numpy()
+
+
+def oracle_out(w):
+    out, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                                w.context_lens, w.dtype)
+    return out, err
+
+
+CTX_MIX = (1, 2, 15, 16, 17, 31, 295, 4097)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("N,K", [(1, 1), (8, 8), (14, 2), (32, 8), (64, 8), (8, 1)])
+def test_decode_matches_oracle(gpu, dtype, H, N, K):
+    w = small(B=len(CTX_MIX), T=1, N=N, K=K, H=H, dtype=dtype, ctx=CTX_MIX,
+              seed=H + 7 * N + 131 * K + (dtype == "bf16"))
+    ref, err = oracle_out(w)
+    assert (err == 0).all()
+    got = run_attention(w, gpu)
+    assert_close(got, ref, dtype, f"decode {dtype} H={H} N={N} K={K}")
+
+
+@pytest.mark.parametrize("T,N,K", [(2, 8, 2), (5, 64, 8), (3, 16, 1), (4, 12, 4), (6, 8, 1)])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_verify_matches_oracle(gpu, T, N, K, dtype):
+    ctx = (T, T + 1, 16, 17, 33, 300, 1029)
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype=dtype, ctx=ctx, seed=T * 100 + N)
+    ref, err = oracle_out(w)
+    assert (err == 0).all()
+    got = run_attention(w, gpu)
+    assert_close(got, ref, dtype, f"verify T={T} N={N} K={K}")
+
+
+def test_decode_entry_point_rejects_t_above_one(gpu):
+    w = small(B=2, T=2, N=8, K=2, H=64, ctx=(4, 9), seed=1)
+    with pytest.raises(gq.GqaError):
+        run_attention(w, gpu, fn=gq.decode_attention)
+
+
+@pytest.mark.parametrize("dtype,H", [("f16", 64), ("bf16", 128)])
+def test_kv_append_bit_exact(gpu, dtype, H):
+    ctx = (1, 3, 16, 17, 31, 32, 33, 500)
+    for T in (1, 3):
+        ctx_t = tuple(max(c, T) for c in ctx)  # at least the T new tokens
+        w = small(B=len(ctx), T=T, N=8, K=4, H=H, dtype=dtype, ctx=ctx_t, seed=T, append=True)
+        kc, vc, err = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                       w.block_tables, w.context_lens)
+        assert (err == 0).all()
+        wd = to(w, gpu)
+        gq.kv_append(wd.k_new[0], wd.v_new[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                     wd.context_lens)
+        torch.cuda.synchronize()
+        gk = wd.k_cache[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        gv = wd.v_cache[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(gk, kc)  # every byte, sentinels included
+        np.testing.assert_array_equal(gv, vc)
+
+
+def test_append_then_attend_equals_oracle(gpu):
+    w = small(B=5, T=3, N=32, K=8, H=128, dtype="bf16", ctx=(3, 16, 17, 250, 1000),
+              seed=21, append=True)
+    kc, vc, _ = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                 w.block_tables, w.context_lens)
+    kc_t = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16)
+    vc_t = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16)
+    ref, _ = oracle.attention(w.q[0], kc_t, vc_t, w.block_tables, w.context_lens, "bf16")
+    wd = to(w, gpu)
+    gq.kv_append(wd.k_new[0], wd.v_new[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                 wd.context_lens)
+    out = gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                              wd.context_lens)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", "append+verify")
+
+
+def test_shared_prefix_blocks(gpu):
+    # copy-on-write prefix sharing: several tables point at the same blocks.
+    w = small(B=4, T=1, N=8, K=2, H=64, ctx=(64, 64, 64, 64), seed=5)
+    w.block_tables[1, :2] = w.block_tables[0, :2]
+    w.block_tables[2, :3] = w.block_tables[0, :3]
+    w.block_tables[3, :] = w.block_tables[0, :]
+    ref, _ = oracle_out(w)
+    got = run_attention(w, gpu)
+    assert_close(got, ref, "f16", "shared blocks")
+
+
+def test_block_permutation_and_repeat_are_bit_identical(gpu):
+    w = small(B=6, T=1, N=32, K=8, H=128, dtype="bf16", ctx=(5, 700, 1500, 33, 16, 2000),
+              seed=6, spare=4)
+    a = run_attention(w, gpu)
+    b = run_attention(w, gpu)
+    np.testing.assert_array_equal(a, b)  # deterministic merge order
+    perm = torch.randperm(w.num_blocks, generator=torch.Generator().manual_seed(1))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(w.num_blocks)
+    w.k_cache[0] = w.k_cache[0][perm].contiguous()
+    w.v_cache[0] = w.v_cache[0][perm].contiguous()
+    used = w.block_tables != 2**31 - 1
+    w.block_tables[used] = inv[w.block_tables[used].long()].int()
+    c = run_attention(w, gpu)
+    np.testing.assert_array_equal(a, c)
+
+
+def test_device_errors_zero_the_sequence_and_set_status(gpu):
+    w = small(B=4, T=2, N=8, K=2, H=64, ctx=(1, 40, 40, 40), seed=7)
+    w.block_tables[2, 1] = w.num_blocks + 3  # bad id inside sequence 2's context
+    w.block_tables[3, 0] = -1                # bad id in sequence 3
+    ref, err = oracle_out(w)
+    assert list(err) == [7, 0, 8, 8]
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    got = run_attention(w, gpu, status=st)
+    assert int(st.item()) in (7, 8)
+    assert (got[0] == 0).all() and (got[2] == 0).all() and (got[3] == 0).all()
+    assert_close(got[1], ref[1], "f16", "healthy sequence next to bad ones")
+
+
+def test_workspace_counters_return_to_zero(gpu):
+    w = small(B=3, T=1, N=32, K=8, H=128, dtype="bf16", ctx=(3000, 5000, 40), seed=8)
+    wd = to(w, gpu)
+    n = gq.attention_workspace_size(wd.q[0], wd.k_cache[0], wd.block_tables)
+    ws = torch.zeros(n, dtype=torch.uint8, device=gpu)
+    for _ in range(3):
+        gq.decode_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                            wd.context_lens, workspace=ws)
+    torch.cuda.synchronize()
+    counters = ws[: 65536 * 4].view(torch.int32)  # the fixed ticket-counter region
+    assert int(counters.abs().sum().item()) == 0
+
+
+def test_workspace_shared_by_shapes_of_different_sizes(gpu):
+    # one buffer, a small-batch call (leaves partial results behind) and then
+    # a large-batch call: the second must still find its counters at zero.
+    ws = None
+    for B, ctx, seed in ((2, (3000, 2500), 1), (40, tuple(range(700, 700 + 40 * 37, 37)), 2)):
+        w = small(B=B, T=1, N=8, K=2, H=64, ctx=ctx, seed=seed)
+        wd = to(w, gpu)
+        n = gq.attention_workspace_size(wd.q[0], wd.k_cache[0], wd.block_tables)
+        if ws is None:
+            ws = torch.zeros(4 * n, dtype=torch.uint8, device=gpu)
+        out = gq.decode_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                                  wd.context_lens, workspace=ws)
+        torch.cuda.synchronize()
+        ref, _ = oracle_out(w)
+        assert_close(out.cpu().double().numpy(), ref, "f16", f"B={B}")
+
+
+def test_empty_batch(gpu):
+    q = torch.empty(0, 1, 8, 64, dtype=torch.float16, device=gpu)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.float16, device=gpu)
+    bt = torch.zeros(0, 2, dtype=torch.int32, device=gpu)
+    cl = torch.zeros(0, dtype=torch.int32, device=gpu)
+    out = gq.decode_attention(q, kc, kc, bt, cl)
+    assert out.shape == (0, 1, 8, 64)
+
+
+def test_long_single_sequence_many_pieces(gpu):
+    # one sequence, 32k tokens: the whole grid splits one segment per KV head.
+    w = small(B=1, T=1, N=8, K=1, H=128, dtype="bf16", ctx=(32768,), seed=9)
+    ref, _ = oracle_out(w)
+    got = run_attention(w, gpu)
+    assert_close(got, ref, "bf16", "32k context")
