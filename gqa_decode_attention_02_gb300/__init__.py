@@ -30,14 +30,16 @@ def _status_arg(status):
 
 
 def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens, *, status=None,
-              stream=None):
+              stream=None, pdl=False):
     """gqa_kv_append: k_new/v_new [B,T,K,H] -> caches [NB,16,K,H] at positions
-    context_lens[b]-T+t.  Asynchronous on `stream` (default: current)."""
+    context_lens[b]-T+t.  Asynchronous on `stream` (default: current).
+    pdl: launch with programmatic dependent launch (GQA_FLAG_PDL)."""
     for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
         _lib._need(t, n, ndim=4)
     _lib._need(block_tables, "block_tables", torch.int32, 2)
     _lib._need(context_lens, "context_lens", torch.int32, 1)
-    shape = _lib.make_shape(k_new, k_cache, block_tables, None, heads_dim=3)
+    shape = _lib.make_shape(k_new, k_cache, block_tables, None, heads_dim=3,
+                            flags=_lib.FLAG_PDL if pdl else 0)
     rc = _lib.lib().gqa_kv_append(ctypes.byref(shape), _lib._ptr(k_new), _lib._ptr(v_new),
                                   _lib._ptr(k_cache), _lib._ptr(v_cache),
                                   _lib._ptr(block_tables), _lib._ptr(context_lens),
@@ -50,13 +52,14 @@ def attention_workspace_size(q, k_cache, block_tables, scale=None) -> int:
 
 
 def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, scale,
-               workspace, status, stream):
+               workspace, status, stream, pdl, early_kv):
     _lib._need(q, "q", ndim=4)
     _lib._need(k_cache, "k_cache", q.dtype, 4)
     _lib._need(v_cache, "v_cache", q.dtype, 4)
     _lib._need(block_tables, "block_tables", torch.int32, 2)
     _lib._need(context_lens, "context_lens", torch.int32, 1)
-    shape = _lib.make_shape(q, k_cache, block_tables, scale)
+    flags = (_lib.FLAG_PDL if pdl else 0) | (_lib.FLAG_EARLY_KV if early_kv else 0)
+    shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -76,17 +79,18 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
 
 
 def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
-                     workspace=None, status=None, stream=None):
-    """gqa_decode_attention (T == 1).  q [B,1,N,H] -> out [B,1,N,H]."""
+                     workspace=None, status=None, stream=None, pdl=False, early_kv=False):
+    """gqa_decode_attention (T == 1).  q [B,1,N,H] -> out [B,1,N,H].
+    pdl / early_kv select GQA_FLAG_PDL / GQA_FLAG_EARLY_KV (see the C header)."""
     return _attention("gqa_decode_attention", q, k_cache, v_cache, block_tables, context_lens,
-                      out, scale, workspace, status, stream)
+                      out, scale, workspace, status, stream, pdl, early_kv)
 
 
 def verify_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
-                     workspace=None, status=None, stream=None):
+                     workspace=None, status=None, stream=None, pdl=False, early_kv=False):
     """gqa_verify_attention (T >= 1, causal among the T new tokens)."""
     return _attention("gqa_verify_attention", q, k_cache, v_cache, block_tables, context_lens,
-                      out, scale, workspace, status, stream)
+                      out, scale, workspace, status, stream, pdl, early_kv)
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,

@@ -73,6 +73,8 @@ __global__ void __launch_bounds__(kThreads)
                   int T, int V, int cs) {
     __shared__ unsigned long long table[kMaxT * kMaxCluster];  // used in rank 0
     __shared__ unsigned long long red[kThreads / 32];
+    griddep_launch_dependents();
+    griddep_wait();  // logits and lengths follow the previous kernels
     const uint32_t rank = cluster_rank();
     const int b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

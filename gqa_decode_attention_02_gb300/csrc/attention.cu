@@ -73,6 +73,7 @@ struct AttnParams {
     int B, T, N, K, G, R, nt;
     int max_blocks, num_blocks;
     float scale_log2;
+    int early_kv;  // GQA_FLAG_EARLY_KV: stream old cache blocks before the wait
 };
 
 struct StageMeta {
@@ -119,16 +120,36 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         tma_prefetch_desc(tmk);
         tma_prefetch_desc(tmv);
     }
+    // Without the early-KV promise every global access waits for the grids
+    // this launch depends on; with it, context_lens, block_tables and the
+    // cache below position ctx - T may be read first, and the wait happens
+    // before the first tile that holds one of the T newest positions and
+    // before any write.
+    bool waited = false;
+    if (!p.early_kv) {
+        griddep_wait();
+        waited = true;
+    }
     // 1. Blocks per sequence and their prefix sum (lane l owns a run of b).
     const int per = (p.B + 31) / 32;
     const int lo = min(p.B, lane * per), hi = min(p.B, lo + per);
     int local = 0;
+    bool invalid = false;
     for (int b = lo; b < hi; ++b) {
         const int n = seq_blocks(p.context_lens[b], p.T, p.max_blocks);
         local += n;
-        if (n == 0 && blockIdx.x == 0) {
-            report(p.status, GQA_ERR_CONTEXT);
-            zero_sequence<H>(p, b);
+        invalid |= (n == 0);
+    }
+    if (blockIdx.x == 0 && __any_sync(FULL, invalid)) {
+        if (!waited) {
+            griddep_wait();
+            waited = true;
+        }
+        for (int b = lo; b < hi; ++b) {
+            if (seq_blocks(p.context_lens[b], p.T, p.max_blocks) == 0) {
+                report(p.status, GQA_ERR_CONTEXT);
+                zero_sequence<H>(p, b);
+            }
         }
     }
     int incl = local;
@@ -182,6 +203,10 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                                         : 0;
             }
             const int blk = __shfl_sync(FULL, ids, i - ids_base);
+            if (!waited && (i * 16 + 15 >= ctx - p.T || blk < 0 || blk >= p.num_blocks)) {
+                griddep_wait();  // this tile holds new positions (or reports an error)
+                waited = true;
+            }
             if (lane == 0) {
                 const int s = it % C::kStages;
                 bool ok = true;
@@ -322,7 +347,8 @@ struct Consumer {
     __device__ void tile(uint32_t kbase, const StageMeta& md) {
         const uint32_t vbase = kbase + C::kTileBytes;
         // ---- S^T = K_tile . Q^T --------------------------------------------
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        // two accumulators (even / odd k-steps) halve the dependent mma chain
+        float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
         {
             const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int chk = lane >> 4;
@@ -332,8 +358,13 @@ struct Consumer {
                 const int chunk = ((kk & 3) << 1) + chk;
                 uint32_t a[4];
                 ldsm_x4(kbase + hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4), a);
-                E::mma(c, a, qf[kk][0], qf[kk][1]);
+                if (kk & 1)
+                    E::mma(c2, a, qf[kk][0], qf[kk][1]);
+                else
+                    E::mma(c, a, qf[kk][0], qf[kk][1]);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[e] += c2[e];
         }
         float s0 = c[0] * p.scale_log2, s1 = c[1] * p.scale_log2;
         float s2 = c[2] * p.scale_log2, s3 = c[3] * p.scale_log2;
@@ -471,38 +502,60 @@ struct Consumer {
         is_last = __shfl_sync(FULL, is_last, 0);
         if (!is_last) return;
         __threadfence();
-        // ---- merge the pieces (log-sum-exp weights) ---------------------------
-        float M0 = -INFINITY, M1 = -INFINITY;
+        // ---- merge the pieces: running log-sum-exp over batches of pieces whose
+        //      loads are all issued before any of them is used ------------------
+        constexpr int kBatch = (H == 64) ? 4 : 2;
+        float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
         bool any_bad = false;
-        for (int c = first; c <= last; ++c) {
-            const int sl = (c == first && (long long)c * cquota < cstart) ? 1 : 0;
-            const float* sc = section(c, sl);
-            M0 = fmaxf(M0, __ldcg(sc + 2 * q4));
-            M1 = fmaxf(M1, __ldcg(sc + 2 * q4 + 1));
-            any_bad |= __ldcg(sc + 16) != 0.f;
-        }
 #pragma unroll
         for (int mt = 0; mt < C::kSteps; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-        float L0 = 0.f, L1 = 0.f;
-        for (int c = first; c <= last; ++c) {
-            const int sl = (c == first && (long long)c * cquota < cstart) ? 1 : 0;
-            const float* sc = section(c, sl);
-            const float mc0 = __ldcg(sc + 2 * q4), mc1 = __ldcg(sc + 2 * q4 + 1);
-            const float w0 = (mc0 == -INFINITY) ? 0.f : fast_exp2(mc0 - M0);
-            const float w1 = (mc1 == -INFINITY) ? 0.f : fast_exp2(mc1 - M1);
-            L0 += w0 * __ldcg(sc + 8 + 2 * q4);
-            L1 += w1 * __ldcg(sc + 8 + 2 * q4 + 1);
-            const float4* b4 = reinterpret_cast<const float4*>(sc + C::kHeaderFloats) +
-                               lane * C::kSteps;
+        for (int c0 = first; c0 <= last; c0 += kBatch) {
+            float mc[kBatch][2], lc[kBatch][2], fl[kBatch];
+            float4 v[kBatch][C::kSteps];
 #pragma unroll
-            for (int mt = 0; mt < C::kSteps; ++mt) {
-                const float4 v = __ldcg(b4 + mt);
-                acc[mt][0] += w0 * v.x;
-                acc[mt][1] += w1 * v.y;
-                acc[mt][2] += w0 * v.z;
-                acc[mt][3] += w1 * v.w;
+            for (int j = 0; j < kBatch; ++j) {
+                const int c = c0 + j;
+                if (c <= last) {
+                    const int sl = (c == first && (long long)c * cquota < cstart) ? 1 : 0;
+                    const float* sc = section(c, sl);
+                    mc[j][0] = __ldcg(sc + 2 * q4);
+                    mc[j][1] = __ldcg(sc + 2 * q4 + 1);
+                    lc[j][0] = __ldcg(sc + 8 + 2 * q4);
+                    lc[j][1] = __ldcg(sc + 8 + 2 * q4 + 1);
+                    fl[j] = __ldcg(sc + 16);
+                    const float4* b4 = reinterpret_cast<const float4*>(sc + C::kHeaderFloats) +
+                                       lane * C::kSteps;
+#pragma unroll
+                    for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = __ldcg(b4 + mt);
+                } else {
+                    mc[j][0] = mc[j][1] = -INFINITY;
+                    lc[j][0] = lc[j][1] = 0.f;
+                    fl[j] = 0.f;
+#pragma unroll
+                    for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = make_float4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                any_bad |= fl[j] != 0.f;
+                const float n0 = fmaxf(M0, mc[j][0]), n1 = fmaxf(M1, mc[j][1]);
+                const float a0 = (M0 == -INFINITY) ? 0.f : fast_exp2(M0 - n0);
+                const float a1 = (M1 == -INFINITY) ? 0.f : fast_exp2(M1 - n1);
+                const float b0 = (mc[j][0] == -INFINITY) ? 0.f : fast_exp2(mc[j][0] - n0);
+                const float b1 = (mc[j][1] == -INFINITY) ? 0.f : fast_exp2(mc[j][1] - n1);
+                L0 = L0 * a0 + lc[j][0] * b0;
+                L1 = L1 * a1 + lc[j][1] * b1;
+#pragma unroll
+                for (int mt = 0; mt < C::kSteps; ++mt) {
+                    acc[mt][0] = acc[mt][0] * a0 + v[j][mt].x * b0;
+                    acc[mt][1] = acc[mt][1] * a1 + v[j][mt].y * b1;
+                    acc[mt][2] = acc[mt][2] * a0 + v[j][mt].z * b0;
+                    acc[mt][3] = acc[mt][3] * a1 + v[j][mt].w * b1;
+                }
+                M0 = n0;
+                M1 = n1;
             }
         }
         store(L0, L1, any_bad);
@@ -515,6 +568,7 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, uint64_t* full, u
     using C = Cfg<H>;
     Consumer<H, BF16> cs(p, w);
     const int lane = threadIdx.x & 31;
+    griddep_wait();  // q, the workspace and out follow the previous kernels
     int cur = -1;
     for (int it = 0;; ++it) {
         const int s = it % C::kStages;
@@ -558,6 +612,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
     volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + C::kStages);
 
     const int warp = threadIdx.x >> 5;
+    griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -722,20 +777,27 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     p.num_blocks = s.num_blocks;
     const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
     p.scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
+    p.early_kv = (s.flags & GQA_FLAG_EARLY_KV) ? 1 : 0;
+    const bool pdl = (s.flags & (GQA_FLAG_PDL | GQA_FLAG_EARLY_KV)) != 0;
     const bool bf16 = s.dtype == GQA_BF16;
-    const dim3 grid(plan.grid), block(plan.threads);
-    if (s.H == 64) {
-        if (bf16)
-            attention_kernel<64, true><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
-        else
-            attention_kernel<64, false><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
-    } else {
-        if (bf16)
-            attention_kernel<128, true><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
-        else
-            attention_kernel<128, false><<<grid, block, plan.smem, stream>>>(tmk, tmv, p);
-    }
-    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(plan.threads);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e;
+    if (s.H == 64)
+        e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<64, true>, tmk, tmv, p)
+                 : cudaLaunchKernelEx(&cfg, attention_kernel<64, false>, tmk, tmv, p);
+    else
+        e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<128, true>, tmk, tmv, p)
+                 : cudaLaunchKernelEx(&cfg, attention_kernel<128, false>, tmk, tmv, p);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 
 }  // namespace gqa

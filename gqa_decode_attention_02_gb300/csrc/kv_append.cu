@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(128)
                      const int32_t* __restrict__ block_tables,
                      const int32_t* __restrict__ context_lens, int32_t* status, int B, int T,
                      int row_vec, int max_blocks, int num_blocks) {
+    griddep_launch_dependents();
+    griddep_wait();  // k_new / v_new and the cache follow the previous kernels
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const long long pairs = (long long)B * T;
@@ -62,11 +64,21 @@ gqa_status launch_kv_append(const gqa_shape& s, const void* k_new, const void* v
     const int sms = device_sm_count();
     const long long cap = (long long)(sms > 0 ? sms : 148) * 16;
     if (blocks > cap) blocks = cap;
-    kv_append_kernel<<<(unsigned)blocks, 32 * wpb, 0, stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), block_tables, context_lens,
-        dev_status, s.B, s.T, row_vec, s.max_blocks_per_seq, s.num_blocks);
-    return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(32 * wpb);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (s.flags & (GQA_FLAG_PDL | GQA_FLAG_EARLY_KV)) ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, kv_append_kernel, static_cast<const uint4*>(k_new),
+        static_cast<const uint4*>(v_new), static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), block_tables, context_lens, dev_status, s.B, s.T, row_vec,
+        s.max_blocks_per_seq, s.num_blocks);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 
 }  // namespace gqa

@@ -5,7 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/gqa_decode.h"
+#include "gqa_decode.h"
 
 namespace gqa {
 

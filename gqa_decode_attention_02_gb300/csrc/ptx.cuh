@@ -7,7 +7,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
-#include "../../include/gqa_decode.h"
+#include "gqa_decode.h"
 
 namespace gqa {
 
@@ -27,6 +27,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// ---- programmatic dependent launch ----------------------------------------------
+// Lets the next kernel on the stream be scheduled once every CTA of this one
+// has issued it (no-op when nothing depends programmatically on this grid).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory
+// operations are visible (returns at once for a plain launch).
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---- mbarrier ---------------------------------------------------------------

@@ -87,7 +87,22 @@ typedef struct {
     int max_blocks_per_seq; /* columns of block_tables */
     gqa_dtype dtype;        /* element type of q, out, caches, k_new, v_new */
     float scale;            /* score scale; <= 0 selects 1/sqrt(H) */
+    unsigned int flags;     /* GQA_FLAG_* bits, 0 for plain stream order */
 } gqa_shape;
+
+/* Launch with programmatic dependent launch: the kernel may be scheduled while
+ * the previous kernel on the stream is still finishing, and waits for it (with
+ * griddepcontrol.wait) before its first access to device memory, so the
+ * results are exactly those of plain stream order; only launch latency and
+ * set-up are overlapped. */
+#define GQA_FLAG_PDL 1u
+/* Attention only, implies GQA_FLAG_PDL.  The caller promises that the work
+ * still running from earlier on the stream writes neither block_tables,
+ * context_lens nor any cache position below context_lens[b] - T.  The kernel
+ * then starts streaming those cache blocks before the previous kernel has
+ * finished; q, the T newest positions, the workspace and `out` are still
+ * touched only after it has. */
+#define GQA_FLAG_EARLY_KV 2u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int gqa_version(void);

@@ -181,3 +181,58 @@ def test_long_single_sequence_many_pieces(gpu):
     ref, _ = oracle_out(w)
     got = run_attention(w, gpu)
     assert_close(got, ref, "bf16", "32k context")
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_pdl_and_early_kv_launches_match_plain_ones(gpu, T):
+    # The same append + attention sequence over three layers, launched plainly
+    # and with programmatic dependent launch / early KV reads, eagerly and from
+    # a CUDA graph: identical bits.
+    ctx = (T, 17, 300, 2000, 64)
+    layers = 3
+    w = small(B=5, T=T, N=32, K=8, H=128, dtype="bf16", ctx=ctx, seed=40 + T, append=True,
+              layers=layers)
+    fn = gq.decode_attention if T == 1 else gq.verify_attention
+
+    def run(flags, graph):
+        wd = to(w, gpu)
+        outs = [torch.empty_like(q) for q in wd.q]
+        ws = torch.zeros(gq.attention_workspace_size(wd.q[0], wd.k_cache[0], wd.block_tables),
+                         dtype=torch.uint8, device=gpu)
+
+        def step():
+            for l in range(layers):
+                gq.kv_append(wd.k_new[l], wd.v_new[l], wd.k_cache[l], wd.v_cache[l],
+                             wd.block_tables, wd.context_lens, pdl=flags["pdl"])
+                fn(wd.q[l], wd.k_cache[l], wd.v_cache[l], wd.block_tables, wd.context_lens,
+                   out=outs[l], workspace=ws, **flags)
+
+        if graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                step()  # warm-up (plans)
+            torch.cuda.current_stream().wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        return [o.cpu() for o in outs]
+
+    ref = run(dict(pdl=False, early_kv=False), graph=False)
+    for flags in (dict(pdl=True, early_kv=False), dict(pdl=True, early_kv=True)):
+        for graph in (False, True):
+            got = run(flags, graph)
+            for l in range(layers):
+                assert torch.equal(got[l].view(torch.int16), ref[l].view(torch.int16)), (
+                    flags, graph, l)
+    # and the plain result matches the oracle
+    kc, vc, _ = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                 w.block_tables, w.context_lens)
+    kc = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16)
+    vc = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16)
+    o, _ = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, "bf16")
+    assert_close(ref[0].double().numpy(), o, "bf16", "layer 0")
