@@ -25,22 +25,30 @@
 //    weights -- the context split of FlashDecoding (named in §"PagedAttention"),
 //    balanced over the whole batch.  Every CTA derives the plan from
 //    context_lens itself (one warp scan), so the host never reads device data.
-//  * One producer warp walks the range, reads block ids 32 at a time and issues
-//    TMA tiled loads (3-D view [blocks*16 rows][K][H], box 16 rows x 64
-//    elements, 128-byte swizzle) of the K and V tile into a ring of stages,
-//    each completing on an mbarrier with a transaction count.
-//  * Consumer warp w owns query rows 8w..8w+7 (rows r = t*G + g).  Per tile it
-//    computes S^T[16 tokens x 8 rows] = K_tile . Q^T with mma.sync m16n8k16
-//    (tokens on M, so no tensor-core rows are wasted on a small G), keeps a
-//    running max / sum in the log2 domain (rescaling the accumulator only when
-//    the max grows by more than 2^8, which leaves the result unchanged up to
-//    rounding), transposes P in registers with movmatrix and accumulates
+//  * One producer warp walks the range in stages of up to four consecutive
+//    tiles of one segment, reads block ids 32 at a time and issues TMA tiled
+//    loads (3-D view [blocks*16 rows][K][H], box 16 rows x 64 elements,
+//    128-byte swizzle) of the K and V tiles into a ring of stages.  Each stage
+//    has a metadata barrier, armed as soon as the stage's description is
+//    written (so consumers can fetch q for a new segment while the tiles are
+//    in flight), and a data barrier completed by the TMA transaction count.
+//  * Consumer warp w owns query rows 8w..8w+7 (rows r = t*G + g).  Per stage
+//    it computes S^T[16 tokens x 8 rows] = K_tile . Q^T for every tile with
+//    mma.sync m16n8k16 (tokens on M, so no tensor-core rows are wasted on a
+//    small G; the tiles give independent mma chains), keeps a running max /
+//    sum in the log2 domain (rescaling the accumulator only when the max grows
+//    by more than 2^8, which leaves the result unchanged up to rounding),
+//    transposes P in registers with movmatrix and accumulates
 //    O^T[H x 8 rows] += V_tile^T . P^T, again on mma.sync.
-//  * A finished segment is written directly when the CTA owns all of it;
-//    otherwise the warp stores its (max, sum, accumulator) piece in the
-//    workspace, takes a ticket from an atomic counter, and the last piece to
-//    arrive merges all pieces and writes the output (nothing ever waits for
-//    another CTA; the counter is reset by the merger).
+//  * Stage-parallel consumer groups: group g computes the stages whose index
+//    is g modulo the group count; at a segment boundary the groups' states
+//    meet in shared memory and group 0 finishes the segment.
+//  * A finished segment is written directly when the CTA owns all of it.  Of
+//    a split segment, the CTA holding the first piece meets it last in its
+//    range and merges; every other piece is the first segment of its CTA,
+//    which publishes it (partial result, then a release flag) early and goes
+//    on, so no merge ever stalls the middle of a range and no CTA waits for a
+//    piece that is still being computed behind it.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -56,11 +64,13 @@
 namespace gqa {
 namespace {
 
-constexpr int kMaxConsumerWarps = 6;  // rows T*G <= 48
+constexpr int kMaxRowWarps = 6;            // rows T*G <= 48
+constexpr int kGroups = 2;                 // stage-parallel consumer groups per CTA
 constexpr int kEnd = 1, kBad = 2;
-constexpr int kQuotaMin = 4;  // at least this many tiles per CTA
-constexpr float kRescaleGap = 8.0f;  // log2-domain slack before rescaling
-constexpr long long kMaxCounters = 65536;  // B * K * consumer warps per call
+constexpr int kTilesPerStage = 4;          // cache blocks per pipeline stage
+constexpr int kQuotaMin = 4 * kTilesPerStage;  // tiles per CTA at least: fewer split pieces
+constexpr float kRescaleGap = 8.0f;        // log2-domain slack before rescaling
+constexpr long long kMaxFlags = 65536;     // CTAs * row warps per launch
 
 struct AttnParams {
     const void* q;
@@ -68,32 +78,37 @@ struct AttnParams {
     const int32_t* block_tables;
     const int32_t* context_lens;
     float* partials;
-    int32_t* counters;
+    int32_t* flags;  // one per (CTA, row warp): piece published
     int32_t* status;
-    int B, T, N, K, G, R, nt;
+    int B, T, N, K, G, R, nt;  // nt: row warps per consumer group
     int max_blocks, num_blocks;
     float scale_log2;
     int early_kv;  // GQA_FLAG_EARLY_KV: stream old cache blocks before the wait
 };
 
+// Description of one pipeline stage, written by the producer.
 struct StageMeta {
-    int b, k, blk_i, ctx;
-    int seg_start, nblk, quota, cta_start;
-    int flags, pad0, pad1, pad2;
+    int b, k, blk_i, ntiles;  // segment (b, k); its tiles blk_i .. blk_i+ntiles-1
+    int ctx, seg_start, nblk, quota;
+    int cta_start, flags, pad0, pad1;
 };
 
 template <int H>
 struct Cfg {
     static constexpr int kTileBytes = 16 * H * 2;  // 16 tokens x H elements
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
-    static constexpr int kStages = (H == 128) ? 4 : 8;
+    static constexpr int kStageBytes = 2 * kTilesPerStage * kTileBytes;  // K tiles, V tiles
+    static constexpr int kStages = (H == 128) ? 3 : 6;
     static constexpr int kHalves = H / 64;  // 64-element (128-byte) swizzle spans
     static constexpr int kSteps = H / 16;  // k16 steps of QK^T == m16 tiles of PV
     static constexpr int kAccFloats = H / 4;  // accumulator floats per lane
     static constexpr int kHeaderFloats = 32;  // m[8], l[8], flag, pad
     static constexpr int kSectionFloats = kHeaderFloats + 32 * kAccFloats;
-    static constexpr size_t kSmem =
-        1024 + kStages * kStageBytes + kStages * 16 + kStages * sizeof(StageMeta) + 64;
+    // stages, barriers (full/meta/empty per stage + combine), stage
+    // descriptions, abort flag; the combine scratch is added per launch
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStages * 24 + 8 +
+                                    kStages * sizeof(StageMeta) + 64;
+    static constexpr size_t kScratchBytesPerRowWarp =
+        2 * (kGroups - 1) * 32 * (4 + kAccFloats) * sizeof(float);
 };
 
 __device__ __forceinline__ int seq_blocks(int ctx, int T, int max_blocks) {
@@ -108,10 +123,42 @@ __device__ void zero_sequence(const AttnParams& p, int b) {
     for (size_t i = 0; i < n16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
+// Publication flags of split pieces (GPU scope): the publisher's release
+// store follows its partial-result stores (made visible to it by __syncwarp);
+// the merger's acquire load precedes its reads of them.
+__device__ __forceinline__ void st_release_gpu(int32_t* f, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+// Bounded wait for a flag.  Every CTA of the grid is resident (the grid is
+// sized to one wave) and a publisher never waits for its merger, so the flag
+// is set in bounded time; the limit only guards against an aborted CTA.
+__device__ __forceinline__ bool wait_flag(const int32_t* f) {
+    if (ld_acquire_gpu(f)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        __nanosleep(100);
+        if (ld_acquire_gpu(f)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Barriers of one CTA.
+struct Bars {
+    uint64_t* full;   // data landed (TMA transaction count)
+    uint64_t* meta;   // stage description written
+    uint64_t* empty;  // every consumer warp is done with the stage
+    uint64_t* cbar;   // consumer groups' states written to the combine scratch
+};
+
 // ---------------------------------------------------------------------------
 template <int H>
 __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
-                         uint8_t* stages, uint64_t* full, uint64_t* empty, StageMeta* meta,
+                         uint8_t* stages, const Bars& bar, StageMeta* meta,
                          volatile int* abort_flag) {
     using C = Cfg<H>;
     constexpr unsigned FULL = 0xffffffffu;
@@ -123,7 +170,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     // Without the early-KV promise every global access waits for the grids
     // this launch depends on; with it, context_lens, block_tables and the
     // cache below position ctx - T may be read first, and the wait happens
-    // before the first tile that holds one of the T newest positions and
+    // before the first stage that holds one of the T newest positions and
     // before any write.
     bool waited = false;
     if (!p.early_kv) {
@@ -165,7 +212,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     const long long c1 = min(total, c0 + quota);
     const uint64_t pol = policy_evict_first();
 
-    int it = 0;
+    int it = 0;  // stages issued
     bool aborted = false;
     if (c0 < c1) {
         // 2. Locate tile c0: the lane whose run of sequences contains it.
@@ -189,29 +236,50 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         }
         int b = __shfl_sync(FULL, fb, owner);
         long long base = __shfl_sync(FULL, fbase, owner);  // first tile of segment (b, 0)
-        int ctx = p.context_lens[b];
+        // Lane-distributed look-ahead windows: context lengths of sequences
+        // b .. b+31, and the first 32 block ids of sequence b+1, fetched before
+        // they are needed so that moving to the next sequence costs no
+        // dependent global load.
+        int cbase = b;
+        int ctxw = (b + lane < p.B) ? __ldg(p.context_lens + b + lane) : 0;
+        int ctx = __shfl_sync(FULL, ctxw, 0);
         int nblk = seq_blocks(ctx, p.T, p.max_blocks);
         const int rel = (int)(c0 - base);
         int k = rel / nblk, i = rel % nblk;
         int ids = 0, ids_base = -(1 << 30);
+        auto next_ids = [&](int bn) {
+            const int cn = (bn < p.B) ? __shfl_sync(FULL, ctxw, min(bn - cbase, 31)) : 0;
+            const int nn = (bn < p.B && bn - cbase < 32) ? seq_blocks(cn, p.T, p.max_blocks) : 0;
+            return (lane < nn) ? __ldg(p.block_tables + (size_t)bn * p.max_blocks + lane) : 0;
+        };
+        int ids_next = next_ids(b + 1);
+        bool next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);  // ids_next is b+1's
 
-        // 3. Stream the range.
-        for (long long x = c0; x < c1; ++x, ++it) {
-            if (i < ids_base || i >= ids_base + 32) {  // warp-uniform refill
+        // 3. Stream the range, one stage (up to four tiles of a segment) at a time.
+        long long x = c0;
+        while (x < c1) {
+            const int run = (int)min((long long)min(kTilesPerStage, nblk - i), c1 - x);
+            if (i < ids_base || i + run > ids_base + 32) {  // warp-uniform refill
                 ids_base = i;
                 ids = (i + lane < nblk) ? __ldg(p.block_tables + (size_t)b * p.max_blocks + i + lane)
                                         : 0;
             }
-            const int blk = __shfl_sync(FULL, ids, i - ids_base);
-            if (!waited && (i * 16 + 15 >= ctx - p.T || blk < 0 || blk >= p.num_blocks)) {
-                griddep_wait();  // this tile holds new positions (or reports an error)
+            int blk[kTilesPerStage];
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < kTilesPerStage; ++j) {
+                blk[j] = __shfl_sync(FULL, ids, min(i - ids_base + j, 31));
+                if (j < run) bad |= (blk[j] < 0 || blk[j] >= p.num_blocks);
+            }
+            if (!waited && ((i + run - 1) * 16 + 15 >= ctx - p.T || bad)) {
+                griddep_wait();  // the stage holds new positions (or reports an error)
                 waited = true;
             }
             if (lane == 0) {
                 const int s = it % C::kStages;
                 bool ok = true;
                 if (it >= C::kStages)
-                    ok = mbar_wait(smem_addr(&empty[s]), ((it / C::kStages) - 1) & 1);
+                    ok = mbar_wait(smem_addr(&bar.empty[s]), ((it / C::kStages) - 1) & 1);
                 if (!ok) report(p.status, GQA_ERR_TIMEOUT);
                 if (!ok || *abort_flag) {
                     *abort_flag = 1;
@@ -221,45 +289,66 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                     m.b = b;
                     m.k = k;
                     m.blk_i = i;
+                    m.ntiles = run;
                     m.ctx = ctx;
                     m.seg_start = (int)(base + (long long)k * nblk);
                     m.nblk = nblk;
                     m.quota = quota;
                     m.cta_start = (int)c0;
-                    const uint32_t fb_ = smem_addr(&full[s]);
-                    if (blk < 0 || blk >= p.num_blocks) {
+                    m.flags = bad ? kBad : 0;
+                    mbar_arrive(smem_addr(&bar.meta[s]));
+                    const uint32_t fb_ = smem_addr(&bar.full[s]);
+                    if (bad) {
                         report(p.status, GQA_ERR_BLOCK_ID);
-                        m.flags = kBad;
                         mbar_arrive(fb_);
                     } else {
-                        m.flags = 0;
-                        mbar_arrive_expect_tx(fb_, C::kStageBytes);
+                        mbar_arrive_expect_tx(fb_, (uint32_t)(run * 2 * C::kTileBytes));
                         const uint32_t dst = smem_addr(stages + (size_t)s * C::kStageBytes);
 #pragma unroll
-                        for (int hh = 0; hh < C::kHalves; ++hh)
-                            tma_load_3d(dst + hh * 2048, tmk, fb_, hh * 64, k, blk * 16, pol);
+                        for (int j = 0; j < kTilesPerStage; ++j) {
+                            if (j < run) {
 #pragma unroll
-                        for (int hh = 0; hh < C::kHalves; ++hh)
-                            tma_load_3d(dst + C::kTileBytes + hh * 2048, tmv, fb_, hh * 64, k,
-                                        blk * 16, pol);
+                                for (int hh = 0; hh < C::kHalves; ++hh) {
+                                    tma_load_3d(dst + j * C::kTileBytes + hh * 2048, tmk, fb_,
+                                                hh * 64, k, blk[j] * 16, pol);
+                                    tma_load_3d(dst + (kTilesPerStage + j) * C::kTileBytes +
+                                                    hh * 2048,
+                                                tmv, fb_, hh * 64, k, blk[j] * 16, pol);
+                                }
+                            }
+                        }
                     }
                 }
             }
             aborted = __shfl_sync(FULL, aborted, 0);
             if (aborted) break;
-            if (++i == nblk) {
+            ++it;
+            x += run;
+            i += run;
+            if (i == nblk) {
                 i = 0;
                 if (++k == p.K) {
                     k = 0;
                     base += (long long)p.K * nblk;
-                    if (x + 1 < c1) {
+                    ids_base = -(1 << 30);
+                    if (x < c1) {
+                        const int b_prev = b;
                         do {
                             ++b;
-                            ctx = p.context_lens[b];
+                            if (b >= cbase + 32) {  // warp-uniform window refill
+                                cbase = b;
+                                ctxw = (b + lane < p.B) ? __ldg(p.context_lens + b + lane) : 0;
+                            }
+                            ctx = __shfl_sync(FULL, ctxw, b - cbase);
                             nblk = seq_blocks(ctx, p.T, p.max_blocks);
                         } while (nblk == 0);
+                        if (b == b_prev + 1 && next_ok) {  // prefetched ids are b's
+                            ids = ids_next;
+                            ids_base = 0;
+                        }
+                        ids_next = next_ids(b + 1);
+                        next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);
                     }
-                    ids_base = -(1 << 30);
                 }
             }
         }
@@ -269,11 +358,12 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     if (lane == 0) {
         if (!aborted) {
             const int s = it % C::kStages;
-            const bool ok =
-                it < C::kStages || mbar_wait(smem_addr(&empty[s]), ((it / C::kStages) - 1) & 1);
+            const bool ok = it < C::kStages ||
+                            mbar_wait(smem_addr(&bar.empty[s]), ((it / C::kStages) - 1) & 1);
             if (ok) {
                 meta[s].flags = kEnd;
-                mbar_arrive(smem_addr(&full[s]));
+                mbar_arrive(smem_addr(&bar.meta[s]));
+                mbar_arrive(smem_addr(&bar.full[s]));
             } else {
                 report(p.status, GQA_ERR_TIMEOUT);
                 *abort_flag = 1;
@@ -282,7 +372,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         }
         if (aborted) {
             for (int j = max(0, it - C::kStages); j < it; ++j)
-                mbar_wait(smem_addr(&full[j % C::kStages]), (j / C::kStages) & 1);
+                mbar_wait(smem_addr(&bar.full[j % C::kStages]), (j / C::kStages) & 1);
         }
     }
 }
@@ -301,7 +391,7 @@ struct Consumer {
     float acc[C::kSteps][4];
     float m0, m1, l0, l1;
     bool bad;
-    int cb, ck, cctx, cstart, cnblk, cquota, ccta0;
+    int cb, ck, cstart, cnblk, cquota, ccta0;
 
     __device__ Consumer(const AttnParams& p_, int w_)
         : p(p_), w(w_), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), q4(threadIdx.x & 3) {
@@ -310,10 +400,12 @@ struct Consumer {
         t1 = min((r0 + 1) / p.G, p.T - 1);
     }
 
+    // Start segment (b, k): reset the running state and fetch the B fragments
+    // of Q^T (k = head dim, n = query row): row 8w+g, dims kk*16 + 2*q4 + {0,1}
+    // and the same + 8.  The loads complete while the stage's tiles land.
     __device__ void begin(const StageMeta& md) {
         cb = md.b;
         ck = md.k;
-        cctx = md.ctx;
         cstart = md.seg_start;
         cnblk = md.nblk;
         cquota = md.quota;
@@ -325,8 +417,6 @@ struct Consumer {
         for (int mt = 0; mt < C::kSteps; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-        // B fragments of Q^T (k = head dim, n = query row): row 8w+g, dims
-        // kk*16 + 2*q4 + {0,1} and the same + 8.
         const int r = 8 * w + g;
         if (r < p.R) {
             const int t = r / p.G, gg = r % p.G;
@@ -344,40 +434,55 @@ struct Consumer {
         }
     }
 
-    __device__ void tile(uint32_t kbase, const StageMeta& md) {
-        const uint32_t vbase = kbase + C::kTileBytes;
-        // ---- S^T = K_tile . Q^T --------------------------------------------
-        // two accumulators (even / odd k-steps) halve the dependent mma chain
-        float c[4] = {0.f, 0.f, 0.f, 0.f}, c2[4] = {0.f, 0.f, 0.f, 0.f};
+    // One stage: md.ntiles tiles of 16 tokens starting at tile md.blk_i.
+    __device__ void stage(uint32_t kbase, const StageMeta& md) {
+        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
+        const int ntl = md.ntiles;
+        // ---- S^T = K_tile . Q^T for every tile (independent mma chains) ------
+        float sc[kTilesPerStage][4];
         {
             const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int chk = lane >> 4;
 #pragma unroll
+            for (int j = 0; j < kTilesPerStage; ++j) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
+            }
+#pragma unroll
             for (int kk = 0; kk < C::kSteps; ++kk) {
                 const int hh = kk >> 2;
                 const int chunk = ((kk & 3) << 1) + chk;
-                uint32_t a[4];
-                ldsm_x4(kbase + hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4), a);
-                if (kk & 1)
-                    E::mma(c2, a, qf[kk][0], qf[kk][1]);
-                else
-                    E::mma(c, a, qf[kk][0], qf[kk][1]);
-            }
+                const uint32_t off = hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) c[e] += c2[e];
+                for (int j = 0; j < kTilesPerStage; ++j) {
+                    uint32_t a[4];
+                    ldsm_x4(kbase + j * C::kTileBytes + off, a);
+                    E::mma(sc[j], a, qf[kk][0], qf[kk][1]);
+                }
+            }
         }
-        float s0 = c[0] * p.scale_log2, s1 = c[1] * p.scale_log2;
-        float s2 = c[2] * p.scale_log2, s3 = c[3] * p.scale_log2;
-        const int pos0 = md.blk_i * 16 + g, pos8 = pos0 + 8;
-        if (md.blk_i * 16 + 15 > md.ctx - p.T) {  // some position hidden from some row
-            const int lim0 = md.ctx - p.T + t0, lim1 = md.ctx - p.T + t1;
-            if (pos0 > lim0) s0 = -INFINITY;
-            if (pos0 > lim1) s1 = -INFINITY;
-            if (pos8 > lim0) s2 = -INFINITY;
-            if (pos8 > lim1) s3 = -INFINITY;
+        // ---- scale, mask (unused tiles, causal bound, slots past the context) --
+        float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kTilesPerStage; ++j) {
+            const int tb = (md.blk_i + j) * 16;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[j][e] *= p.scale_log2;
+            if (j >= ntl) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[j][e] = -INFINITY;
+            } else if (tb + 15 > md.ctx - p.T) {  // some position hidden from some row
+                const int lim0 = md.ctx - p.T + t0, lim1 = md.ctx - p.T + t1;
+                const int pos0 = tb + g, pos8 = pos0 + 8;
+                if (pos0 > lim0) sc[j][0] = -INFINITY;
+                if (pos0 > lim1) sc[j][1] = -INFINITY;
+                if (pos8 > lim0) sc[j][2] = -INFINITY;
+                if (pos8 > lim1) sc[j][3] = -INFINITY;
+            }
+            x0 = fmaxf(x0, fmaxf(sc[j][0], sc[j][2]));
+            x1 = fmaxf(x1, fmaxf(sc[j][1], sc[j][3]));
         }
         // ---- running max (log2 domain), lazy rescale ----------------------------
-        float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, o));
@@ -402,36 +507,44 @@ struct Consumer {
         }
         const float ref0 = (m0 == -INFINITY) ? 0.f : m0;
         const float ref1 = (m1 == -INFINITY) ? 0.f : m1;
-        const uint32_t pt0 = E::pack(fast_exp2(s0 - ref0), fast_exp2(s1 - ref1));  // token g
-        const uint32_t pt1 = E::pack(fast_exp2(s2 - ref0), fast_exp2(s3 - ref1));  // token g+8
-        l0 += E::lo(pt0) + E::lo(pt1);
-        l1 += E::hi(pt0) + E::hi(pt1);
-        // P^T as the B operand: tokens 2*q4+{0,1} (+8) of query row g.
-        const uint32_t pb0 = movm_t(pt0), pb1 = movm_t(pt1);
-        // ---- O^T += V_tile^T . P^T --------------------------------------------
-        uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
-        const bool tail = md.blk_i * 16 + 16 > md.ctx;
-        if (tail) {  // NaN-safe: zero V elements of slots past the context
-            const int pb = md.blk_i * 16 + 2 * q4;
-            v01 = (pb < md.ctx ? 0x0000ffffu : 0u) | (pb + 1 < md.ctx ? 0xffff0000u : 0u);
-            v89 = (pb + 8 < md.ctx ? 0x0000ffffu : 0u) | (pb + 9 < md.ctx ? 0xffff0000u : 0u);
-        }
+        // ---- O^T += V_tile^T . P^T, tile by tile ------------------------------------
         const int tok = (lane & 7) + (lane >> 4) * 8;
         const int dof = ((lane >> 3) & 1) * 8;
 #pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt) {
-            const int d0 = mt * 16 + dof;
-            const int hh = d0 >> 6;
-            const int chunk = (d0 & 63) >> 3;
-            uint32_t a[4];
-            ldsm_x4_t(vbase + hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4), a);
-            if (tail) {
-                a[0] &= v01;
-                a[1] &= v01;
-                a[2] &= v89;
-                a[3] &= v89;
+        for (int j = 0; j < kTilesPerStage; ++j) {
+            if (j >= ntl) break;  // warp-uniform
+            const uint32_t pt0 =
+                E::pack(fast_exp2(sc[j][0] - ref0), fast_exp2(sc[j][1] - ref1));  // token g
+            const uint32_t pt1 =
+                E::pack(fast_exp2(sc[j][2] - ref0), fast_exp2(sc[j][3] - ref1));  // token g+8
+            l0 += E::lo(pt0) + E::lo(pt1);
+            l1 += E::hi(pt0) + E::hi(pt1);
+            // P^T as the B operand: tokens 2*q4+{0,1} (+8) of query row g.
+            const uint32_t pb0 = movm_t(pt0), pb1 = movm_t(pt1);
+            const int tb = (md.blk_i + j) * 16;
+            const bool tail = tb + 16 > md.ctx;
+            uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
+            if (tail) {  // NaN-safe: zero V elements of slots past the context
+                const int pb = tb + 2 * q4;
+                v01 = (pb < md.ctx ? 0x0000ffffu : 0u) | (pb + 1 < md.ctx ? 0xffff0000u : 0u);
+                v89 = (pb + 8 < md.ctx ? 0x0000ffffu : 0u) | (pb + 9 < md.ctx ? 0xffff0000u : 0u);
             }
-            E::mma(acc[mt], a, pb0, pb1);
+            const uint32_t vt = vbase + j * C::kTileBytes;
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt) {
+                const int d0 = mt * 16 + dof;
+                const int hh = d0 >> 6;
+                const int chunk = (d0 & 63) >> 3;
+                uint32_t a[4];
+                ldsm_x4_t(vt + hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4), a);
+                if (tail) {
+                    a[0] &= v01;
+                    a[1] &= v01;
+                    a[2] &= v89;
+                    a[3] &= v89;
+                }
+                E::mma(acc[mt], a, pb0, pb1);
+            }
         }
     }
 
@@ -460,93 +573,133 @@ struct Consumer {
         }
     }
 
-    __device__ float* section(int cta, int slot) const {
-        return p.partials + ((size_t)(cta * 2 + slot) * p.nt + w) * C::kSectionFloats;
+    // Partial-result section of CTA `cta` for this row warp.  One per CTA is
+    // enough: the only segment a CTA hands to another for merging is its first.
+    __device__ float* section(int cta) const {
+        return p.partials + ((size_t)cta * p.nt + w) * C::kSectionFloats;
     }
+    __device__ int32_t* flag(int cta) const { return p.flags + (size_t)cta * p.nt + w; }
 
-    __device__ void finalize() {
+    // Row sums: each lane holds the sum over its own tokens; add up the 8 lanes
+    // that share a row pair.
+    __device__ void reduce_l() {
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
             l0 += __shfl_xor_sync(FULL, l0, o);
             l1 += __shfl_xor_sync(FULL, l1, o);
         }
+    }
+
+    // Per-lane layout of a group's state in the combine scratch.
+    static constexpr int kScratchFloats = 4 + C::kAccFloats;
+
+    __device__ void save_state(float* slot) const {
+        float4* d = reinterpret_cast<float4*>(slot);
+        d[0] = make_float4(m0, m1, l0, l1);
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt)
+            d[1 + mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+    }
+
+    // Fold another group's state (same segment, same rows) into this one.
+    __device__ void absorb(const float* slot) {
+        const float4* d = reinterpret_cast<const float4*>(slot);
+        const float4 h = d[0];
+        const float n0 = fmaxf(m0, h.x), n1 = fmaxf(m1, h.y);
+        const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - n0);
+        const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - n1);
+        const float b0 = (h.x == -INFINITY) ? 0.f : fast_exp2(h.x - n0);
+        const float b1 = (h.y == -INFINITY) ? 0.f : fast_exp2(h.y - n1);
+        l0 = l0 * a0 + h.z * b0;
+        l1 = l1 * a1 + h.w * b1;
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt) {
+            const float4 v = d[1 + mt];
+            acc[mt][0] = acc[mt][0] * a0 + v.x * b0;
+            acc[mt][1] = acc[mt][1] * a1 + v.y * b1;
+            acc[mt][2] = acc[mt][2] * a0 + v.z * b0;
+            acc[mt][3] = acc[mt][3] * a1 + v.w * b1;
+        }
+        m0 = n0;
+        m1 = n1;
+    }
+
+    // Finish the segment (row sums already reduced).  A split segment's pieces
+    // sit in CTAs first..last.  CTA `first` meets the segment last in its own
+    // range, so it is the merger; every other piece is the first segment of
+    // its CTA, which publishes it (partial result, then a release flag) and
+    // goes on.  The merger folds the published pieces into its own in CTA
+    // order (deterministic) and clears their flags for the next call.
+    __device__ void finalize() {
         const int first = cstart / cquota;
         const int last = (cstart + cnblk - 1) / cquota;
+        const int me = blockIdx.x;
         if (first == last) {
             store(l0, l1, bad);
             return;
         }
-        const int me = blockIdx.x;
-        const int slot = (me == first && ccta0 < cstart) ? 1 : 0;
-        float* sec = section(me, slot);
-        if (g == 0) {
-            sec[2 * q4] = m0;
-            sec[2 * q4 + 1] = m1;
-            sec[8 + 2 * q4] = l0;
-            sec[8 + 2 * q4 + 1] = l1;
-        }
-        if (lane == 0) sec[16] = bad ? 1.f : 0.f;
-        float4* a4 = reinterpret_cast<float4*>(sec + C::kHeaderFloats) + lane * C::kSteps;
+        if (me != first) {
+            float* sec = section(me);
+            if (g == 0) {
+                sec[2 * q4] = m0;
+                sec[2 * q4 + 1] = m1;
+                sec[8 + 2 * q4] = l0;
+                sec[8 + 2 * q4 + 1] = l1;
+            }
+            if (lane == 0) sec[16] = bad ? 1.f : 0.f;
+            float4* a4 = reinterpret_cast<float4*>(sec + C::kHeaderFloats) + lane * C::kSteps;
 #pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt)
-            a4[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
-        __threadfence();
-        __syncwarp();
-        int is_last = 0;
-        if (lane == 0) {
-            int32_t* ctr = p.counters + ((size_t)cb * p.K + ck) * p.nt + w;
-            const int old = atomicAdd(ctr, 1);
-            is_last = (old == last - first);
-            if (is_last) *ctr = 0;  // every piece has arrived: ready for the next call
+            for (int mt = 0; mt < C::kSteps; ++mt)
+                a4[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+            __syncwarp();  // orders the lanes' stores before lane 0's release
+            if (lane == 0) st_release_gpu(flag(me), 1);
+            return;
         }
-        is_last = __shfl_sync(FULL, is_last, 0);
-        if (!is_last) return;
-        __threadfence();
-        // ---- merge the pieces: running log-sum-exp over batches of pieces whose
-        //      loads are all issued before any of them is used ------------------
+        // ---- merger: batches of published pieces, loads issued before use ----
         constexpr int kBatch = (H == 64) ? 4 : 2;
-        float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-        bool any_bad = false;
+        bool any_bad = bad;
+        for (int c0 = first + 1; c0 <= last; c0 += kBatch) {
+            int ok = 1;
+            if (lane == 0) {
 #pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-        for (int c0 = first; c0 <= last; c0 += kBatch) {
+                for (int j = 0; j < kBatch; ++j)
+                    if (c0 + j <= last) ok &= wait_flag(flag(c0 + j)) ? 1 : 0;
+            }
+            ok = __shfl_sync(FULL, ok, 0);
+            if (!ok) {  // a piece never arrived (cannot happen unless a CTA aborted)
+                if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
+                store(0.f, 0.f, true);
+                return;
+            }
+            __syncwarp();  // orders lane 0's acquires before every lane's loads
             float mc[kBatch][2], lc[kBatch][2], fl[kBatch];
             float4 v[kBatch][C::kSteps];
+            // Unconditional loads (past the last piece the batch re-reads it and
+            // then gives it no weight): every load is in flight before any use.
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
-                const int c = c0 + j;
-                if (c <= last) {
-                    const int sl = (c == first && (long long)c * cquota < cstart) ? 1 : 0;
-                    const float* sc = section(c, sl);
-                    mc[j][0] = __ldcg(sc + 2 * q4);
-                    mc[j][1] = __ldcg(sc + 2 * q4 + 1);
-                    lc[j][0] = __ldcg(sc + 8 + 2 * q4);
-                    lc[j][1] = __ldcg(sc + 8 + 2 * q4 + 1);
-                    fl[j] = __ldcg(sc + 16);
-                    const float4* b4 = reinterpret_cast<const float4*>(sc + C::kHeaderFloats) +
-                                       lane * C::kSteps;
+                const float* sc = section(min(c0 + j, last));
+                mc[j][0] = __ldcg(sc + 2 * q4);
+                mc[j][1] = __ldcg(sc + 2 * q4 + 1);
+                lc[j][0] = __ldcg(sc + 8 + 2 * q4);
+                lc[j][1] = __ldcg(sc + 8 + 2 * q4 + 1);
+                fl[j] = __ldcg(sc + 16);
+                const float4* b4 =
+                    reinterpret_cast<const float4*>(sc + C::kHeaderFloats) + lane * C::kSteps;
 #pragma unroll
-                    for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = __ldcg(b4 + mt);
-                } else {
-                    mc[j][0] = mc[j][1] = -INFINITY;
-                    lc[j][0] = lc[j][1] = 0.f;
-                    fl[j] = 0.f;
-#pragma unroll
-                    for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = make_float4(0, 0, 0, 0);
-                }
+                for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = __ldcg(b4 + mt);
             }
 #pragma unroll
             for (int j = 0; j < kBatch; ++j) {
+                if (c0 + j > last) continue;
                 any_bad |= fl[j] != 0.f;
-                const float n0 = fmaxf(M0, mc[j][0]), n1 = fmaxf(M1, mc[j][1]);
-                const float a0 = (M0 == -INFINITY) ? 0.f : fast_exp2(M0 - n0);
-                const float a1 = (M1 == -INFINITY) ? 0.f : fast_exp2(M1 - n1);
+                const float n0 = fmaxf(m0, mc[j][0]), n1 = fmaxf(m1, mc[j][1]);
+                const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - n0);
+                const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - n1);
                 const float b0 = (mc[j][0] == -INFINITY) ? 0.f : fast_exp2(mc[j][0] - n0);
                 const float b1 = (mc[j][1] == -INFINITY) ? 0.f : fast_exp2(mc[j][1] - n1);
-                L0 = L0 * a0 + lc[j][0] * b0;
-                L1 = L1 * a1 + lc[j][1] * b1;
+                l0 = l0 * a0 + lc[j][0] * b0;
+                l1 = l1 * a1 + lc[j][1] * b1;
 #pragma unroll
                 for (int mt = 0; mt < C::kSteps; ++mt) {
                     acc[mt][0] = acc[mt][0] * a0 + v[j][mt].x * b0;
@@ -554,51 +707,93 @@ struct Consumer {
                     acc[mt][2] = acc[mt][2] * a0 + v[j][mt].z * b0;
                     acc[mt][3] = acc[mt][3] * a1 + v[j][mt].w * b1;
                 }
-                M0 = n0;
-                M1 = n1;
+                m0 = n0;
+                m1 = n1;
             }
         }
-        store(L0, L1, any_bad);
+        if (lane == 0)
+            for (int c = first + 1; c <= last; ++c) *flag(c) = 0;  // ready for the next call
+        store(l0, l1, any_bad);
     }
 };
 
+// Consumer warp w belongs to group w / nt (stage-parallel: group g computes
+// the stages whose index is g modulo the group count) and owns query rows
+// 8*(w % nt) .. +7.  Every warp reads every stage's description, so all groups
+// agree on segment boundaries; at each boundary the groups' partial states
+// meet in shared memory and group 0 finishes the segment.
 template <int H, bool BF16>
-__device__ void consumer(const AttnParams& p, uint8_t* stages, uint64_t* full, uint64_t* empty,
-                         const StageMeta* meta, volatile int* abort_flag, int w) {
+__device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
+                         const StageMeta* meta, float* scratch, volatile int* abort_flag,
+                         int w) {
     using C = Cfg<H>;
-    Consumer<H, BF16> cs(p, w);
+    using CS = Consumer<H, BF16>;
+    const int gi = w / p.nt, wr = w % p.nt;
+    CS cs(p, wr);
     const int lane = threadIdx.x & 31;
     griddep_wait();  // q, the workspace and out follow the previous kernels
+    auto slot = [&](int buf, int gg) {
+        return scratch +
+               ((((size_t)buf * (kGroups - 1) + (gg - 1)) * p.nt + wr) * 32 + lane) *
+                   CS::kScratchFloats;
+    };
+    int nseg = 0;  // segments closed so far (phase of the combine barrier)
+    auto close = [&]() -> bool {
+        cs.reduce_l();
+        const int buf = nseg & 1;  // double buffer: group 0 may still read the other
+        if (gi != 0) cs.save_state(slot(buf, gi));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(bar.cbar));
+        if (!mbar_wait(smem_addr(bar.cbar), nseg & 1)) {
+            if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+        if (gi == 0) {
+#pragma unroll
+            for (int gg = 1; gg < kGroups; ++gg) cs.absorb(slot(buf, gg));
+            cs.finalize();
+        }
+        ++nseg;
+        return true;
+    };
     int cur = -1;
     for (int it = 0;; ++it) {
         const int s = it % C::kStages;
-        if (!mbar_wait(smem_addr(&full[s]), (it / C::kStages) & 1)) {
+        const uint32_t par = (it / C::kStages) & 1;
+        if (!mbar_wait(smem_addr(&bar.meta[s]), par)) {
             if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
             *abort_flag = 1;
             return;
         }
         const StageMeta md = meta[s];
         if (md.flags & kEnd) {
-            if (cur >= 0) cs.finalize();
+            if (cur >= 0) close();
             return;
         }
         const int seg = md.b * p.K + md.k;
         if (seg != cur) {
-            if (cur >= 0) cs.finalize();
+            if (cur >= 0 && !close()) return;
             cs.begin(md);
             cur = seg;
         }
-        if (md.flags & kBad)
+        if (md.flags & kBad) {
             cs.bad = true;
-        else
-            cs.tile(smem_addr(stages + (size_t)s * C::kStageBytes), md);
+        } else if (it % kGroups == gi) {
+            if (!mbar_wait(smem_addr(&bar.full[s]), par)) {
+                if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
+                *abort_flag = 1;
+                return;
+            }
+            cs.stage(smem_addr(stages + (size_t)s * C::kStageBytes), md);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
+        if (lane == 0) mbar_arrive(smem_addr(&bar.empty[s]));
     }
 }
 
 template <int H, bool BF16>
-__global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
+__global__ void __launch_bounds__(32 * (kGroups * kMaxRowWarps + 1))
     attention_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
     using C = Cfg<H>;
@@ -606,26 +801,34 @@ __global__ void __launch_bounds__(32 * (kMaxConsumerWarps + 1))
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-    uint64_t* empty = full + C::kStages;
-    StageMeta* meta = reinterpret_cast<StageMeta*>(empty + C::kStages);
+    Bars bar;
+    bar.full = reinterpret_cast<uint64_t*>(smem + (size_t)C::kStages * C::kStageBytes);
+    bar.meta = bar.full + C::kStages;
+    bar.empty = bar.meta + C::kStages;
+    bar.cbar = bar.empty + C::kStages;
+    StageMeta* meta = reinterpret_cast<StageMeta*>(bar.cbar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + C::kStages);
+    float* scratch = reinterpret_cast<float*>(
+        (reinterpret_cast<uintptr_t>(abort_flag + 1) + 15) & ~uintptr_t(15));
+    const int consumers = kGroups * p.nt;
 
     const int warp = threadIdx.x >> 5;
     griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), p.nt);
+            mbar_init(smem_addr(&bar.full[s]), 1);
+            mbar_init(smem_addr(&bar.meta[s]), 1);
+            mbar_init(smem_addr(&bar.empty[s]), consumers);
         }
+        mbar_init(smem_addr(bar.cbar), consumers);
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp == p.nt)
-        producer<H>(&tmk, &tmv, p, stages, full, empty, meta, abort_flag);
+    if (warp == consumers)
+        producer<H>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
     else
-        consumer<H, BF16>(p, stages, full, empty, meta, abort_flag, warp);
+        consumer<H, BF16>(p, stages, bar, meta, scratch, abort_flag, warp);
 }
 
 // ---------------------------------------------------------------------------
@@ -640,7 +843,11 @@ const void* pick_kernel(int H, bool bf16) {
     return bf16 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
 }
 
-size_t smem_for(int H) { return H == 64 ? Cfg<64>::kSmem : Cfg<128>::kSmem; }
+// Dynamic shared memory of one CTA with nt row warps per consumer group.
+size_t smem_for(int H, int nt) {
+    return H == 64 ? Cfg<64>::kSmem + nt * Cfg<64>::kScratchBytesPerRowWarp
+                   : Cfg<128>::kSmem + nt * Cfg<128>::kScratchBytesPerRowWarp;
+}
 size_t section_floats(int H) {
     return H == 64 ? Cfg<64>::kSectionFloats : Cfg<128>::kSectionFloats;
 }
@@ -690,11 +897,14 @@ int resident_ctas(int H, bool bf16, int nt, size_t smem) {
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     const void* kern = pick_kernel(H, bf16);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    // The attribute belongs to the kernel, whatever the row-warp count: set it
+    // to the largest launch any shape can make.
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_for(H, kMaxRowWarps)) != cudaSuccess)
         return 0;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * (nt + 1), smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * (kGroups * nt + 1),
+                                                      smem) !=
         cudaSuccess)
         return 0;
     cache[key] = occ;
@@ -723,29 +933,34 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     if (s.dtype != GQA_F16 && s.dtype != GQA_BF16) return GQA_ERR_DTYPE;
     const int G = s.N / s.K;
     const long long R = (long long)s.T * G;
-    if (R > 8 * kMaxConsumerWarps) return GQA_ERR_SHAPE;
+    if (R > 8 * kMaxRowWarps) return GQA_ERR_SHAPE;
     const int nt = (int)((R + 7) / 8);
-    const int threads = 32 * (nt + 1);
-    const size_t smem = smem_for(s.H);
-    const int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, smem);
+    const int threads = 32 * (kGroups * nt + 1);
+    const size_t smem = smem_for(s.H, nt);
+    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, smem);
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
-    long long grid = (long long)sms * occ;
+    // Small problems (at most ~256 tiles per SM even if every sequence were
+    // full) run one CTA per SM: fewer CTAs split fewer sequences, and the SM
+    // keeps room for the next launch on the stream, whose producer can then
+    // start streaming (programmatic dependent launch) while this one finishes.
     const long long tiles_max = (long long)s.B * s.K * s.max_blocks_per_seq;
+    if (tiles_max <= 256ll * sms) occ = 1;
+    long long grid = (long long)sms * occ;
     grid = std::min<long long>(grid, std::max<long long>(1, (tiles_max + kQuotaMin - 1) / kQuotaMin));
     plan->grid = (int)grid;
     plan->consumer_warps = nt;
     plan->threads = threads;
     plan->smem = smem;
-    // The ticket counters live in a fixed region at the start of every
+    // The publication flags live in a fixed region at the start of every
     // workspace, whatever the shape, and partial results always start after
     // it: partial data of one call can then never sit where a later call of
-    // another shape expects zeroed counters.
-    if ((long long)s.B * s.K * nt > kMaxCounters) return GQA_ERR_SHAPE;
-    plan->counters_bytes = (size_t)kMaxCounters * 4;
-    plan->partial_floats_per_slot = section_floats(s.H) * nt;
-    plan->workspace = plan->counters_bytes + (size_t)grid * 2 * plan->partial_floats_per_slot * 4;
+    // another shape expects zeroed flags.
+    if (grid * nt > kMaxFlags) return GQA_ERR_SHAPE;
+    plan->flags_bytes = (size_t)kMaxFlags * 4;
+    plan->partial_floats_per_cta = section_floats(s.H) * nt;
+    plan->workspace = plan->flags_bytes + (size_t)grid * plan->partial_floats_per_cta * 4;
     return GQA_OK;
 }
 
@@ -763,8 +978,8 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     p.out = out;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
-    p.counters = static_cast<int32_t*>(workspace);
-    p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.counters_bytes);
+    p.flags = static_cast<int32_t*>(workspace);
+    p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan.flags_bytes);
     p.status = dev_status;
     p.B = s.B;
     p.T = s.T;

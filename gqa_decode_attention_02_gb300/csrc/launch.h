@@ -15,8 +15,8 @@ struct AttnPlan {
     int consumer_warps;  // one per 8 query rows (rows = T * G)
     int threads;
     size_t smem;         // dynamic shared memory per CTA
-    size_t counters_bytes;
-    size_t partial_floats_per_slot;
+    size_t flags_bytes;             // fixed region of publication flags
+    size_t partial_floats_per_cta;
     size_t workspace;    // total bytes
 };
 

@@ -126,16 +126,16 @@ gqa_status gqa_kv_append(const gqa_shape *shape, const void *k_new, const void *
 
 /* Bytes of device workspace gqa_decode_attention / gqa_verify_attention need
  * for this shape on the CURRENT device: a fixed 256 KiB region of int32
- * ticket counters (one per sequence, KV head and group of 8 query rows; at
- * most 65536, else the shape is rejected) followed by the split-context
- * partial results.  Returns 0 if the shape is invalid.  The workspace must be
- * zero-filled before its first use (for example with gqa_workspace_clear);
- * every call whose kernels finish without GQA_ERR_TIMEOUT leaves the counter
- * region zero-filled again (the partial-result region is scratch and never
- * needs clearing), so one buffer can be reused by later calls of any shape
- * that fits.  Calls that share a workspace must not overlap on the GPU (use
- * one stream, or one workspace per stream).  After GQA_ERR_TIMEOUT, clear the
- * workspace again before reusing it. */
+ * publication flags (one per thread block and group of 8 query rows) followed
+ * by the split-context partial results.  Returns 0 if the shape is invalid.
+ * The workspace must be zero-filled before its first use (for example with
+ * gqa_workspace_clear); every call whose kernels finish without
+ * GQA_ERR_TIMEOUT leaves the flag region zero-filled again (the
+ * partial-result region is scratch and never needs clearing), so one buffer
+ * can be reused by later calls of any shape that fits.  Calls that share a
+ * workspace must not overlap on the GPU (use one stream, or one workspace per
+ * stream).  After GQA_ERR_TIMEOUT, clear the workspace again before reusing
+ * it. */
 size_t gqa_attention_workspace_size(const gqa_shape *shape);
 
 /* Zero-fill `bytes` of workspace on `stream` (a cudaMemsetAsync). */

@@ -136,7 +136,7 @@ def test_device_errors_zero_the_sequence_and_set_status(gpu):
     assert_close(got[1], ref[1], "f16", "healthy sequence next to bad ones")
 
 
-def test_workspace_counters_return_to_zero(gpu):
+def test_workspace_flags_return_to_zero(gpu):
     w = small(B=3, T=1, N=32, K=8, H=128, dtype="bf16", ctx=(3000, 5000, 40), seed=8)
     wd = to(w, gpu)
     n = gq.attention_workspace_size(wd.q[0], wd.k_cache[0], wd.block_tables)
@@ -145,25 +145,27 @@ def test_workspace_counters_return_to_zero(gpu):
         gq.decode_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
                             wd.context_lens, workspace=ws)
     torch.cuda.synchronize()
-    counters = ws[: 65536 * 4].view(torch.int32)  # the fixed ticket-counter region
-    assert int(counters.abs().sum().item()) == 0
+    flags = ws[: 65536 * 4].view(torch.int32)  # the fixed publication-flag region
+    assert int(flags.abs().sum().item()) == 0
 
 
 def test_workspace_shared_by_shapes_of_different_sizes(gpu):
     # one buffer, a small-batch call (leaves partial results behind) and then
-    # a large-batch call: the second must still find its counters at zero.
+    # a large-batch call: the second must still find its flags at zero.
+    cases = [small(B=B, T=1, N=8, K=2, H=64, ctx=ctx, seed=seed) for B, ctx, seed in
+             ((2, (3000, 2500), 1), (40, tuple(range(700, 700 + 40 * 37, 37)), 2))]
     ws = None
-    for B, ctx, seed in ((2, (3000, 2500), 1), (40, tuple(range(700, 700 + 40 * 37, 37)), 2)):
-        w = small(B=B, T=1, N=8, K=2, H=64, ctx=ctx, seed=seed)
+    for w in cases:
         wd = to(w, gpu)
-        n = gq.attention_workspace_size(wd.q[0], wd.k_cache[0], wd.block_tables)
         if ws is None:
-            ws = torch.zeros(4 * n, dtype=torch.uint8, device=gpu)
+            n = max(gq.attention_workspace_size(c.q[0].to(gpu), c.k_cache[0].to(gpu),
+                                                c.block_tables.to(gpu)) for c in cases)
+            ws = torch.zeros(n, dtype=torch.uint8, device=gpu)
         out = gq.decode_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
                                   wd.context_lens, workspace=ws)
         torch.cuda.synchronize()
         ref, _ = oracle_out(w)
-        assert_close(out.cpu().double().numpy(), ref, "f16", f"B={B}")
+        assert_close(out.cpu().double().numpy(), ref, "f16", f"B={w.B}")
 
 
 def test_empty_batch(gpu):
@@ -236,3 +238,22 @@ def test_pdl_and_early_kv_launches_match_plain_ones(gpu, T):
     vc = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16)
     o, _ = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, "bf16")
     assert_close(ref[0].double().numpy(), o, "bf16", "layer 0")
+
+
+def test_many_tiny_sequences_with_gaps(gpu):
+    # 20000 one-block sequences (so each CTA range spans dozens of sequences and
+    # the look-ahead windows of lengths and block ids roll over), some of them
+    # empty (skipped, zeroed, reported).
+    rng = np.random.default_rng(11)
+    B = 20000
+    ctx = rng.integers(1, 17, size=B)
+    ctx[rng.choice(B, size=200, replace=False)] = 0
+    w = small(B=B, T=1, N=2, K=1, H=64, ctx=np.maximum(ctx, 1), seed=12)
+    w.context_lens[torch.as_tensor(ctx == 0)] = 0
+    ref, err = oracle_out(w)
+    assert (err[ctx == 0] == 7).all() and (err[ctx > 0] == 0).all()
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    got = run_attention(w, gpu, status=st)
+    assert int(st.item()) == 7
+    assert (got[ctx == 0] == 0).all()
+    assert_close(got[ctx > 0], ref[ctx > 0], "f16", "tiny sequences")
