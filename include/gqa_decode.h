@@ -165,6 +165,28 @@ gqa_status gqa_decode_attention(const gqa_shape *shape, const void *q,
                                 void *workspace, size_t workspace_bytes,
                                 int32_t *dev_status, void *stream);
 
+/* Decode attention that allocates nothing (no counterpart on the pages: it is
+ * a convenience of this library).  For callers that cannot call cudaMalloc --
+ * a host program that keeps all device memory in its own pool, a decode loop
+ * that must not let cudaMalloc / cudaFree synchronise the device, a plain C
+ * caller without an allocator -- this computes exactly what
+ * gqa_decode_attention computes, with the same requirements, but takes no
+ * workspace: its scratch is a static 8 MiB device array inside the library,
+ * held on every GPU that loads the library until the process exits.
+ *  - Shapes whose gqa_attention_workspace_size exceeds 8 MiB are rejected
+ *    with GQA_ERR_WORKSPACE.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - Each call first clears, on `stream`, the part of the array that must
+ *    start at zero (one cudaMemsetAsync; nothing is allocated or freed).
+ *  - All calls share the one array: calls whose work overlaps on the GPU (on
+ *    different streams or from different host threads) race on it. */
+gqa_status gqa_decode_attention_noalloc(const gqa_shape *shape, const void *q,
+                                        const void *k_cache, const void *v_cache,
+                                        const int32_t *block_tables,
+                                        const int32_t *context_lens, void *out,
+                                        int32_t *dev_status, void *stream);
+
 /* Verify attention, T >= 1 new tokens per sequence (speculative verification:
  * CS336 lecture 10 §"Спекулятивное сэмплирование" -- the target model scores
  * several drafted tokens in one pass).  As gqa_decode_attention, except that
