@@ -7,6 +7,8 @@ CUDA kernels; calling any op without the built library raises.
     kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens)
     decode_attention(q, k_cache, v_cache, block_tables, context_lens) -> out
     verify_attention(q, k_cache, v_cache, block_tables, context_lens) -> out
+    append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)
+    append_verify_attention(...)  (kv_append fused into the attention launch)
     accept_prefix(target_logits, draft_ids, context_lens=None) -> (accepted, next)
 """
 from __future__ import annotations
@@ -18,7 +20,8 @@ import torch
 from . import _lib
 from ._lib import GqaError, Shape, Status, status_string  # noqa: F401
 
-__all__ = ["kv_append", "decode_attention", "verify_attention", "accept_prefix",
+__all__ = ["kv_append", "decode_attention", "verify_attention", "append_decode_attention",
+           "append_verify_attention", "accept_prefix",
            "attention_workspace_size", "GqaError", "Status", "Shape"]
 
 
@@ -52,8 +55,11 @@ def attention_workspace_size(q, k_cache, block_tables, scale=None) -> int:
 
 
 def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, scale,
-               workspace, status, stream, pdl, early_kv):
+               workspace, status, stream, pdl, early_kv, k_new=None, v_new=None):
     _lib._need(q, "q", ndim=4)
+    if k_new is not None:
+        _lib._need(k_new, "k_new", q.dtype, 4)
+        _lib._need(v_new, "v_new", q.dtype, 4)
     _lib._need(k_cache, "k_cache", q.dtype, 4)
     _lib._need(v_cache, "v_cache", q.dtype, 4)
     _lib._need(block_tables, "block_tables", torch.int32, 2)
@@ -70,7 +76,8 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
     else:
         _lib._need(workspace, "workspace", torch.uint8)
     L = _lib.lib()
-    rc = getattr(L, fn_name)(ctypes.byref(shape), _lib._ptr(q), _lib._ptr(k_cache),
+    new = () if k_new is None else (_lib._ptr(k_new), _lib._ptr(v_new))
+    rc = getattr(L, fn_name)(ctypes.byref(shape), _lib._ptr(q), *new, _lib._ptr(k_cache),
                              _lib._ptr(v_cache), _lib._ptr(block_tables),
                              _lib._ptr(context_lens), _lib._ptr(out), _lib._ptr(workspace),
                              workspace.numel(), _status_arg(status), _lib._stream(stream))
@@ -91,6 +98,25 @@ def verify_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=Non
     """gqa_verify_attention (T >= 1, causal among the T new tokens)."""
     return _attention("gqa_verify_attention", q, k_cache, v_cache, block_tables, context_lens,
                       out, scale, workspace, status, stream, pdl, early_kv)
+
+
+def append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
+                            out=None, scale=None, workspace=None, status=None, stream=None,
+                            pdl=False, early_kv=False):
+    """gqa_append_decode_attention: kv_append + decode_attention in one launch
+    (T == 1).  Writes k_new/v_new into the caches and returns out."""
+    return _attention("gqa_append_decode_attention", q, k_cache, v_cache, block_tables,
+                      context_lens, out, scale, workspace, status, stream, pdl, early_kv,
+                      k_new=k_new, v_new=v_new)
+
+
+def append_verify_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
+                            out=None, scale=None, workspace=None, status=None, stream=None,
+                            pdl=False, early_kv=False):
+    """gqa_append_verify_attention: kv_append + verify_attention in one launch."""
+    return _attention("gqa_append_verify_attention", q, k_cache, v_cache, block_tables,
+                      context_lens, out, scale, workspace, status, stream, pdl, early_kv,
+                      k_new=k_new, v_new=v_new)
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,

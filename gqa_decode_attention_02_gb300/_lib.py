@@ -54,7 +54,8 @@ FLAG_EARLY_KV = 2
 
 EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_attention_workspace_size", "gqa_workspace_clear", "gqa_decode_attention",
-           "gqa_verify_attention", "gqa_accept_prefix")
+           "gqa_verify_attention", "gqa_append_decode_attention", "gqa_append_verify_attention",
+           "gqa_accept_prefix")
 
 
 def lib() -> ctypes.CDLL:
@@ -83,6 +84,10 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = I
             f.argtypes = [S, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+        for name in ("gqa_append_decode_attention", "gqa_append_verify_attention"):
+            f = getattr(L, name)
+            f.restype = I
+            f.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
         L.gqa_accept_prefix.restype = I
         L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, P]
         _lib = L

@@ -22,26 +22,29 @@ gqa_status check_common(const gqa_shape* s) {
     return GQA_OK;
 }
 
-gqa_status attention_entry(const gqa_shape* s, bool decode_only, const void* q,
-                           const void* k_cache, const void* v_cache,
-                           const int32_t* block_tables, const int32_t* context_lens, void* out,
-                           void* workspace, size_t ws_bytes, int32_t* dev_status,
-                           void* stream) {
+gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, const void* q,
+                           const void* k_new, const void* v_new, const void* k_cache,
+                           const void* v_cache, const int32_t* block_tables,
+                           const int32_t* context_lens, void* out, void* workspace,
+                           size_t ws_bytes, int32_t* dev_status, void* stream) {
     gqa_status st = check_common(s);
     if (st != GQA_OK) return st;
     if (decode_only && s->T != 1) return GQA_ERR_SHAPE;
     if (s->B == 0) return GQA_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return GQA_ERR_NULL;
+    if (fused && (!k_new || !v_new)) return GQA_ERR_NULL;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return GQA_ERR_ALIGN;
+    if (fused && (!aligned16(k_new) || !aligned16(v_new))) return GQA_ERR_ALIGN;
     gqa::AttnPlan plan;
     st = gqa::attention_plan(*s, &plan);
     if (st != GQA_OK) return st;
     if (!workspace || ws_bytes < plan.workspace) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_ALIGN;
-    return gqa::launch_attention(*s, plan, q, k_cache, v_cache, block_tables, context_lens, out,
-                                 workspace, dev_status, static_cast<cudaStream_t>(stream));
+    return gqa::launch_attention(*s, plan, q, fused ? k_new : nullptr, fused ? v_new : nullptr,
+                                 k_cache, v_cache, block_tables, context_lens, out, workspace,
+                                 dev_status, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -99,16 +102,38 @@ gqa_status gqa_decode_attention(const gqa_shape* shape, const void* q, const voi
                                 const void* v_cache, const int32_t* block_tables,
                                 const int32_t* context_lens, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
-    return attention_entry(shape, true, q, k_cache, v_cache, block_tables, context_lens, out,
-                           workspace, workspace_bytes, dev_status, stream);
+    return attention_entry(shape, true, false, q, nullptr, nullptr, k_cache, v_cache,
+                           block_tables, context_lens, out, workspace, workspace_bytes,
+                           dev_status, stream);
 }
 
 gqa_status gqa_verify_attention(const gqa_shape* shape, const void* q, const void* k_cache,
                                 const void* v_cache, const int32_t* block_tables,
                                 const int32_t* context_lens, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
-    return attention_entry(shape, false, q, k_cache, v_cache, block_tables, context_lens, out,
-                           workspace, workspace_bytes, dev_status, stream);
+    return attention_entry(shape, false, false, q, nullptr, nullptr, k_cache, v_cache,
+                           block_tables, context_lens, out, workspace, workspace_bytes,
+                           dev_status, stream);
+}
+
+gqa_status gqa_append_decode_attention(const gqa_shape* shape, const void* q,
+                                       const void* k_new, const void* v_new, void* k_cache,
+                                       void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, void* out, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status,
+                                       void* stream) {
+    return attention_entry(shape, true, true, q, k_new, v_new, k_cache, v_cache, block_tables,
+                           context_lens, out, workspace, workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_append_verify_attention(const gqa_shape* shape, const void* q,
+                                       const void* k_new, const void* v_new, void* k_cache,
+                                       void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, void* out, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status,
+                                       void* stream) {
+    return attention_entry(shape, false, true, q, k_new, v_new, k_cache, v_cache, block_tables,
+                           context_lens, out, workspace, workspace_bytes, dev_status, stream);
 }
 
 gqa_status gqa_accept_prefix(int B, int T, int V, const float* target_logits,

@@ -84,6 +84,12 @@ struct AttnParams {
     int max_blocks, num_blocks;
     float scale_log2;
     int early_kv;  // GQA_FLAG_EARLY_KV: stream old cache blocks before the wait
+    // Fused append (k_new != nullptr): the T newest positions are taken from
+    // k_new / v_new [B][T][K][H] and written into the caches by this kernel.
+    const void* k_new;
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
 };
 
 // Description of one pipeline stage, written by the producer.
@@ -91,6 +97,7 @@ struct StageMeta {
     int b, k, blk_i, ntiles;  // segment (b, k); its tiles blk_i .. blk_i+ntiles-1
     int ctx, seg_start, nblk, quota;
     int cta_start, flags, pad0, pad1;
+    int blk[kTilesPerStage];  // physical block of each tile
 };
 
 template <int H>
@@ -154,6 +161,16 @@ struct Bars {
     uint64_t* empty;  // every consumer warp is done with the stage
     uint64_t* cbar;   // consumer groups' states written to the combine scratch
 };
+
+// L2 prefetch of the q rows segment (b, k) will read: for each new token t,
+// the G query heads of KV head k are contiguous (G*H elements).
+template <int H>
+__device__ __forceinline__ void prefetch_q(const AttnParams& p, int b, int k) {
+    const uint16_t* base = static_cast<const uint16_t*>(p.q);
+    for (int t = 0; t < p.T; ++t)
+        prefetch_l2(base + (((size_t)b * p.T + t) * p.N + (size_t)k * p.G) * H,
+                    (uint32_t)(p.G * H * 2));
+}
 
 // ---------------------------------------------------------------------------
 template <int H>
@@ -253,6 +270,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             return (lane < nn) ? __ldg(p.block_tables + (size_t)bn * p.max_blocks + lane) : 0;
         };
         int ids_next = next_ids(b + 1);
+        if (lane == 0) prefetch_q<H>(p, b, k);
         bool next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);  // ids_next is b+1's
 
         // 3. Stream the range, one stage (up to four tiles of a segment) at a time.
@@ -271,7 +289,9 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                 blk[j] = __shfl_sync(FULL, ids, min(i - ids_base + j, 31));
                 if (j < run) bad |= (blk[j] < 0 || blk[j] >= p.num_blocks);
             }
-            if (!waited && ((i + run - 1) * 16 + 15 >= ctx - p.T || bad)) {
+            // (with the append fused in, the new positions come from k_new /
+            // v_new after the consumers' wait, so only an error waits here)
+            if (!waited && ((!p.k_new && (i + run - 1) * 16 + 15 >= ctx - p.T) || bad)) {
                 griddep_wait();  // the stage holds new positions (or reports an error)
                 waited = true;
             }
@@ -296,6 +316,8 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                     m.quota = quota;
                     m.cta_start = (int)c0;
                     m.flags = bad ? kBad : 0;
+#pragma unroll
+                    for (int j = 0; j < kTilesPerStage; ++j) m.blk[j] = blk[j];
                     mbar_arrive(smem_addr(&bar.meta[s]));
                     const uint32_t fb_ = smem_addr(&bar.full[s]);
                     if (bad) {
@@ -327,6 +349,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             i += run;
             if (i == nblk) {
                 i = 0;
+                const bool more = x < c1;
                 if (++k == p.K) {
                     k = 0;
                     base += (long long)p.K * nblk;
@@ -350,6 +373,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                         next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);
                     }
                 }
+                if (more && lane == 0) prefetch_q<H>(p, b, k);  // the next segment's q
             }
         }
     }
@@ -434,8 +458,51 @@ struct Consumer {
         }
     }
 
+    // Fused append: the tiles holding the T newest positions may carry stale
+    // rows there (TMA read the cache before this call writes it).  Overwrite
+    // those rows of the staged K and V tiles with k_new / v_new, and let row
+    // warp 0 write them into the caches (each new position of KV head k lies in
+    // exactly one tile, handled by exactly one CTA).  Every row warp of the
+    // group patches its own copy of the same bytes before reading them.
+    __device__ bool patch_new_rows(uint32_t kbase, const StageMeta& md) {
+        constexpr int kChunks = H / 8;  // 16-byte chunks per row
+        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
+        const int first_new = md.ctx - p.T;
+        bool any = false;
+        for (int j = 0; j < md.ntiles; ++j) {  // warp-uniform
+            const int tb = (md.blk_i + j) * 16;
+            const int lo = max(first_new, tb), hi = min(md.ctx, tb + 16);
+            for (int pos = lo; pos < hi; ++pos) {
+                any = true;
+                const int r = pos - tb, t = pos - first_new;
+                if (lane < 2 * kChunks) {
+                    const bool is_v = lane >= kChunks;
+                    const int c = is_v ? lane - kChunks : lane;
+                    const size_t row = (((size_t)cb * p.T + t) * p.K + ck) * kChunks;
+                    const uint4 val =
+                        __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row + c);
+                    const uint32_t dst = (is_v ? vbase : kbase) + j * C::kTileBytes +
+                                         (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+                    st_shared_v4(dst, val);
+                    if (w == 0) {
+                        uint4* cache = static_cast<uint4*>(is_v ? p.v_cache : p.k_cache);
+                        cache[(((size_t)md.blk[j] * 16 + r) * p.K + ck) * kChunks + c] = val;
+                    }
+                }
+            }
+        }
+        if (any) {
+            // the generic-proxy writes must precede the next TMA write into this
+            // stage buffer (issued after every consumer released it)
+            fence_proxy_async_shared();
+            __syncwarp();
+        }
+        return any;
+    }
+
     // One stage: md.ntiles tiles of 16 tokens starting at tile md.blk_i.
     __device__ void stage(uint32_t kbase, const StageMeta& md) {
+        if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
         const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
         const int ntl = md.ntiles;
         // ---- S^T = K_tile . Q^T for every tile (independent mma chains) ------
@@ -965,10 +1032,10 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
 }
 
 gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
-                            const void* k_cache, const void* v_cache,
-                            const int32_t* block_tables, const int32_t* context_lens,
-                            void* out, void* workspace, int32_t* dev_status,
-                            cudaStream_t stream) {
+                            const void* k_new, const void* v_new, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables,
+                            const int32_t* context_lens, void* out, void* workspace,
+                            int32_t* dev_status, cudaStream_t stream) {
     if (s.B == 0) return GQA_OK;
     CUtensorMap tmk, tmv;
     if (!encode_cache_map(&tmk, k_cache, s) || !encode_cache_map(&tmv, v_cache, s))
@@ -993,6 +1060,10 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
     p.scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
     p.early_kv = (s.flags & GQA_FLAG_EARLY_KV) ? 1 : 0;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = const_cast<void*>(k_cache);
+    p.v_cache = const_cast<void*>(v_cache);
     const bool pdl = (s.flags & (GQA_FLAG_PDL | GQA_FLAG_EARLY_KV)) != 0;
     const bool bf16 = s.dtype == GQA_BF16;
     cudaLaunchConfig_t cfg = {};

@@ -23,11 +23,14 @@ struct AttnPlan {
 // Fills `plan`; returns GQA_OK or a validation error.
 gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan);
 
+// k_new / v_new == nullptr: attention over the cache as it is; otherwise the
+// T newest tokens are appended from them by the same launch (the caches are
+// then written).
 gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
-                            const void* k_cache, const void* v_cache,
-                            const int32_t* block_tables, const int32_t* context_lens,
-                            void* out, void* workspace, int32_t* dev_status,
-                            cudaStream_t stream);
+                            const void* k_new, const void* v_new, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables,
+                            const int32_t* context_lens, void* out, void* workspace,
+                            int32_t* dev_status, cudaStream_t stream);
 
 gqa_status launch_kv_append(const gqa_shape& s, const void* k_new, const void* v_new,
                             void* k_cache, void* v_cache, const int32_t* block_tables,

@@ -199,6 +199,31 @@ gqa_status gqa_verify_attention(const gqa_shape *shape, const void *q,
                                 void *workspace, size_t workspace_bytes,
                                 int32_t *dev_status, void *stream);
 
+/* KV append fused into attention: the same results (cache bytes and
+ * attention output) as gqa_kv_append followed by gqa_decode_attention /
+ * gqa_verify_attention on the same stream, in one launch.  The kernel takes the
+ * T newest positions' keys and values from k_new / v_new [B][T][K][H] (16-byte
+ * aligned) instead of the cache and writes them into the caches, as the
+ * pages' speculative-decoding blog does on the GPU ("Болжау арқылы Sonar
+ * модельдерін жылдамдату" §"Спекулятивті кодтан шығару арқылы инференс").
+ * With GQA_FLAG_EARLY_KV the kernel can then stream every older cache block
+ * before the previous kernel on the stream finishes (q, k_new, v_new, the
+ * workspace and out stay ordered after it).  Requirements and device errors as
+ * for the unfused calls; a sequence whose blocks include an invalid id gets a
+ * zero output and its new tokens may not be written. */
+gqa_status gqa_append_decode_attention(const gqa_shape *shape, const void *q,
+                                       const void *k_new, const void *v_new, void *k_cache,
+                                       void *v_cache, const int32_t *block_tables,
+                                       const int32_t *context_lens, void *out, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status,
+                                       void *stream);
+gqa_status gqa_append_verify_attention(const gqa_shape *shape, const void *q,
+                                       const void *k_new, const void *v_new, void *k_cache,
+                                       void *v_cache, const int32_t *block_tables,
+                                       const int32_t *context_lens, void *out, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status,
+                                       void *stream);
+
 /* Greedy prefix acceptance.  Speculative-decoding section of "جعل inference
  * رخيصًا" (a drafted token is kept only if the target would produce it) and
  * "Болжау арқылы Sonar модельдерін жылдамдату" §"Спекулятивті кодтан шығару"

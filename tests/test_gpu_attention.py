@@ -257,3 +257,82 @@ def test_many_tiny_sequences_with_gaps(gpu):
     assert int(st.item()) == 7
     assert (got[ctx == 0] == 0).all()
     assert_close(got[ctx > 0], ref[ctx > 0], "f16", "tiny sequences")
+
+
+@pytest.mark.parametrize("T,N,K,H,dtype,ctx", [
+    (1, 32, 8, 128, "bf16", (1, 2, 16, 17, 33, 300, 4097)),
+    (1, 14, 2, 64, "f16", (1, 15, 16, 17, 295, 1024)),
+    (5, 64, 8, 128, "bf16", (5, 6, 16, 19, 20, 33, 512, 4096)),  # new tokens straddle blocks
+    (3, 16, 1, 64, "f16", (3, 17, 18, 100)),
+])
+def test_fused_append_equals_append_then_attention(gpu, T, N, K, H, dtype, ctx):
+    w = small(B=len(ctx), T=T, N=N, K=K, H=H, dtype=dtype, ctx=ctx, seed=T * 7 + H, append=True)
+    # oracle: append, then attention
+    kc, vc, err = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                   w.block_tables, w.context_lens)
+    assert (err == 0).all()
+    tdt = w.torch_dtype
+    ref, _ = oracle.attention(w.q[0], torch.from_numpy(kc.view(np.int16)).view(tdt),
+                              torch.from_numpy(vc.view(np.int16)).view(tdt), w.block_tables,
+                              w.context_lens, dtype)
+    # GPU: unfused pair, then the fused call on a fresh copy of the caches
+    a = to(w, gpu)
+    gq.kv_append(a.k_new[0], a.v_new[0], a.k_cache[0], a.v_cache[0], a.block_tables,
+                 a.context_lens)
+    fn = gq.decode_attention if T == 1 else gq.verify_attention
+    out_pair = fn(a.q[0], a.k_cache[0], a.v_cache[0], a.block_tables, a.context_lens)
+    b = to(w, gpu)
+    ffn = gq.append_decode_attention if T == 1 else gq.append_verify_attention
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    out_fused = ffn(b.q[0], b.k_new[0], b.v_new[0], b.k_cache[0], b.v_cache[0], b.block_tables,
+                    b.context_lens, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for mine, theirs in ((b.k_cache[0], kc), (b.v_cache[0], vc)):  # every cache byte
+        np.testing.assert_array_equal(mine.cpu().view(torch.int16).numpy().view(np.uint16),
+                                      theirs)
+    assert torch.equal(out_fused.view(torch.int16), out_pair.view(torch.int16))
+    assert_close(out_fused.float().cpu().double().numpy(), ref, dtype, "fused append")
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_fused_append_pdl_early_graph_matches_plain(gpu, T):
+    ctx = (T, 17, 300, 2000, 64)
+    layers = 3
+    w = small(B=5, T=T, N=32, K=8, H=128, dtype="bf16", ctx=ctx, seed=50 + T, append=True,
+              layers=layers)
+    ffn = gq.append_decode_attention if T == 1 else gq.append_verify_attention
+
+    def run(flags, graph):
+        wd = to(w, gpu)
+        outs = [torch.empty_like(q) for q in wd.q]
+        ws = torch.zeros(gq.attention_workspace_size(wd.q[0], wd.k_cache[0], wd.block_tables),
+                         dtype=torch.uint8, device=gpu)
+
+        def step():
+            for l in range(layers):
+                ffn(wd.q[l], wd.k_new[l], wd.v_new[l], wd.k_cache[l], wd.v_cache[l],
+                    wd.block_tables, wd.context_lens, out=outs[l], workspace=ws, **flags)
+
+        if graph:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                step()
+            torch.cuda.current_stream().wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        return [o.cpu() for o in outs], [c.cpu() for c in wd.k_cache]
+
+    ref, ref_k = run(dict(pdl=False, early_kv=False), graph=False)
+    for flags in (dict(pdl=True, early_kv=False), dict(pdl=True, early_kv=True)):
+        for graph in (False, True):
+            got, got_k = run(flags, graph)
+            for l in range(layers):
+                assert torch.equal(got[l].view(torch.int16), ref[l].view(torch.int16))
+                assert torch.equal(got_k[l].view(torch.int16), ref_k[l].view(torch.int16))

@@ -24,7 +24,7 @@ def sample_sequences(ctx: np.ndarray, n: int, seed: int) -> np.ndarray:
     return np.array(sorted(pick), np.int32)
 
 
-def check_workload(name, dev, sample=None, layers=None):
+def check_workload(name, dev, sample=None, layers=None, fused=False):
     w = workloads.make(name, layers=layers)
     ctx = w.context_lens.numpy()
     bl = sample_sequences(ctx, sample, 1) if sample else np.arange(w.B, dtype=np.int32)
@@ -45,9 +45,15 @@ def check_workload(name, dev, sample=None, layers=None):
         kd, vd = kc.to(dev), vc.to(dev)
         bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
         st = torch.zeros(1, dtype=torch.int32, device=dev)
-        if w.appended:
+        out = None
+        if w.appended and fused:  # the append inside the attention launch (the bench's call)
+            ffn = gq.append_decode_attention if w.T == 1 else gq.append_verify_attention
+            out = ffn(w.q[layer].to(dev), w.k_new[layer].to(dev), w.v_new[layer].to(dev), kd, vd,
+                      bt, cl, status=st, pdl=True, early_kv=True)
+        elif w.appended:
             gq.kv_append(w.k_new[layer].to(dev), w.v_new[layer].to(dev), kd, vd, bt, cl,
                          status=st)
+        if w.appended:
             # the append itself, bit for bit, on the blocks of the checked sequences
             tb = w.block_tables[torch.as_tensor(bl).long()]
             blocks = torch.unique(tb[tb != workloads.INT32_MAX]).long()
@@ -55,8 +61,9 @@ def check_workload(name, dev, sample=None, layers=None):
                                           okc[blocks].view(torch.int16).numpy())
             np.testing.assert_array_equal(vd[blocks.to(dev)].cpu().view(torch.int16).numpy(),
                                           ovc[blocks].view(torch.int16).numpy())
-        fn = gq.decode_attention if w.T == 1 else gq.verify_attention
-        out = fn(w.q[layer].to(dev), kd, vd, bt, cl, status=st)
+        if out is None:
+            fn = gq.decode_attention if w.T == 1 else gq.verify_attention
+            out = fn(w.q[layer].to(dev), kd, vd, bt, cl, status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         got = out.cpu()[torch.as_tensor(bl).long()].double().numpy()
@@ -93,3 +100,8 @@ def test_cfg5_verify_and_accept(gpu):
     np.testing.assert_array_equal(nxt.cpu().numpy(), rn)
     np.testing.assert_array_equal(cl.cpu().numpy(), rc)
     assert (ra >= w.draft_k).all()
+
+
+@pytest.mark.parametrize("name,sample", [("cfg2", None), ("cfg3", 8), ("cfg4", 16), ("cfg5", None)])
+def test_fused_append_at_full_size(gpu, name, sample):
+    check_workload(name, gpu, sample=sample, fused=True)
