@@ -113,6 +113,20 @@ def profiled_traffic(workload):
         return None
 
 
+def combine_ranks(step_ms: float, bytes_step: int, world: int, device):
+    """Whole-job figure over replicas: every rank processed `bytes_step` per
+    step; the job's step time is the slowest rank's.  Returns (max step ms,
+    GB/s of all ranks' bytes).  Uses the default process group when world > 1."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([step_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    return step_ms, world * bytes_step / (step_ms * 1e-3) / 1e9
+
+
 # ---- clocks ------------------------------------------------------------------------
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -352,15 +366,7 @@ def run_ours(args, world, rank, local):
 
     attn_b, app_b, acc_b = step_bytes(w)
     bytes_step = L * (attn_b + app_b) + acc_b
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms_max = float(t.item())
-    else:
-        step_ms_max = step_ms
-    value = world * bytes_step / (step_ms_max * 1e-3) / 1e9
+    step_ms_max, value = combine_ranks(step_ms, bytes_step, world, dev)
     peak, peak_src = measured_peak()
     attn_launch_ms = attn_ms / L
     kernel_b = attn_b + (app_b if fused else 0)  # the fused launch also does the append

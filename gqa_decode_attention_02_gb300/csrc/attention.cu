@@ -65,7 +65,8 @@ namespace gqa {
 namespace {
 
 constexpr int kMaxRowWarps = 6;            // rows T*G <= 48
-constexpr int kGroups = 2;                 // stage-parallel consumer groups per CTA
+constexpr int kGroups = 2;                 // stage-parallel consumer groups (default)
+constexpr int kMaxThreads = 32 * (kGroups * kMaxRowWarps + 1);
 constexpr int kEnd = 1, kBad = 2;
 constexpr int kTilesPerStage = 4;          // cache blocks per pipeline stage
 constexpr int kQuotaMin = 4 * kTilesPerStage;  // tiles per CTA at least: fewer split pieces
@@ -83,6 +84,8 @@ struct AttnParams {
     int B, T, N, K, G, R, nt;  // nt: row warps per consumer group
     int max_blocks, num_blocks;
     float scale_log2;
+    int stages;    // depth of the shared-memory ring
+    int groups;    // stage-parallel consumer groups
     int early_kv;  // GQA_FLAG_EARLY_KV: stream old cache blocks before the wait
     // Fused append (k_new != nullptr): the T newest positions are taken from
     // k_new / v_new [B][T][K][H] and written into the caches by this kernel.
@@ -104,6 +107,8 @@ template <int H>
 struct Cfg {
     static constexpr int kTileBytes = 16 * H * 2;  // 16 tokens x H elements
     static constexpr int kStageBytes = 2 * kTilesPerStage * kTileBytes;  // K tiles, V tiles
+    // Default ring depth (two CTAs per SM fit); a CTA alone on its SM (the
+    // host decides) gets as many stages as the opt-in shared memory holds.
     static constexpr int kStages = (H == 128) ? 3 : 6;
     static constexpr int kHalves = H / 64;  // 64-element (128-byte) swizzle spans
     static constexpr int kSteps = H / 16;  // k16 steps of QK^T == m16 tiles of PV
@@ -112,10 +117,10 @@ struct Cfg {
     static constexpr int kSectionFloats = kHeaderFloats + 32 * kAccFloats;
     // stages, barriers (full/meta/empty per stage + combine), stage
     // descriptions, abort flag; the combine scratch is added per launch
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kStages * 24 + 8 +
-                                    kStages * sizeof(StageMeta) + 64;
+    static constexpr size_t kStageOverhead = 24 + sizeof(StageMeta);  // barriers + meta
+    static constexpr size_t kFixed = 1024 + 8 + 64;  // alignment, combine barrier, flag
     static constexpr size_t kScratchBytesPerRowWarp =
-        2 * (kGroups - 1) * 32 * (4 + kAccFloats) * sizeof(float);
+        2 * 32 * (4 + kAccFloats) * sizeof(float);  // per row warp of each extra group
 };
 
 __device__ __forceinline__ int seq_blocks(int ctx, int T, int max_blocks) {
@@ -296,10 +301,10 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                 waited = true;
             }
             if (lane == 0) {
-                const int s = it % C::kStages;
+                const int s = it % p.stages;
                 bool ok = true;
-                if (it >= C::kStages)
-                    ok = mbar_wait(smem_addr(&bar.empty[s]), ((it / C::kStages) - 1) & 1);
+                if (it >= p.stages)
+                    ok = mbar_wait(smem_addr(&bar.empty[s]), ((it / p.stages) - 1) & 1);
                 if (!ok) report(p.status, GQA_ERR_TIMEOUT);
                 if (!ok || *abort_flag) {
                     *abort_flag = 1;
@@ -381,9 +386,9 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     //    copy already issued land before the CTA exits.
     if (lane == 0) {
         if (!aborted) {
-            const int s = it % C::kStages;
-            const bool ok = it < C::kStages ||
-                            mbar_wait(smem_addr(&bar.empty[s]), ((it / C::kStages) - 1) & 1);
+            const int s = it % p.stages;
+            const bool ok = it < p.stages ||
+                            mbar_wait(smem_addr(&bar.empty[s]), ((it / p.stages) - 1) & 1);
             if (ok) {
                 meta[s].flags = kEnd;
                 mbar_arrive(smem_addr(&bar.meta[s]));
@@ -395,14 +400,18 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             }
         }
         if (aborted) {
-            for (int j = max(0, it - C::kStages); j < it; ++j)
-                mbar_wait(smem_addr(&bar.full[j % C::kStages]), (j / C::kStages) & 1);
+            for (int j = max(0, it - p.stages); j < it; ++j)
+                mbar_wait(smem_addr(&bar.full[j % p.stages]), (j / p.stages) & 1);
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-template <int H, bool BF16>
+// Consumer warp state.  The warp owns NW tiles of 8 query rows: tile u holds
+// rows 8*(w*NW + u) .. +7 (rows r = t*G + g).  Every K / V fragment it reads
+// from shared memory feeds NW mma, so more rows per warp means fewer warps
+// re-reading the same stage.
+template <int H, bool BF16, int NW>
 struct Consumer {
     using C = Cfg<H>;
     using E = Elt<BF16>;
@@ -410,23 +419,28 @@ struct Consumer {
 
     const AttnParams& p;
     const int w, lane, g, q4;
-    int t0, t1;  // new-token index of this lane's two C-fragment rows
-    uint32_t qf[C::kSteps][2];
-    float acc[C::kSteps][4];
-    float m0, m1, l0, l1;
+    int t0[NW], t1[NW];  // new-token index of this lane's two C-fragment rows, per tile
+    uint32_t qf[NW][C::kSteps][2];
+    float acc[NW][C::kSteps][4];
+    float m0[NW], m1[NW], l0[NW], l1[NW];
     bool bad;
     int cb, ck, cstart, cnblk, cquota, ccta0;
 
+    __device__ int row0(int u) const { return 8 * (w * NW + u); }
+
     __device__ Consumer(const AttnParams& p_, int w_)
         : p(p_), w(w_), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), q4(threadIdx.x & 3) {
-        const int r0 = 8 * w + 2 * q4;
-        t0 = min(r0 / p.G, p.T - 1);
-        t1 = min((r0 + 1) / p.G, p.T - 1);
+#pragma unroll
+        for (int u = 0; u < NW; ++u) {
+            const int r0 = row0(u) + 2 * q4;
+            t0[u] = min(r0 / p.G, p.T - 1);
+            t1[u] = min((r0 + 1) / p.G, p.T - 1);
+        }
     }
 
     // Start segment (b, k): reset the running state and fetch the B fragments
-    // of Q^T (k = head dim, n = query row): row 8w+g, dims kk*16 + 2*q4 + {0,1}
-    // and the same + 8.  The loads complete while the stage's tiles land.
+    // of Q^T (k = head dim, n = query row): row row0(u)+g, dims kk*16 + 2*q4 +
+    // {0,1} and the same + 8.  The loads complete while the stage's tiles land.
     __device__ void begin(const StageMeta& md) {
         cb = md.b;
         ck = md.k;
@@ -435,26 +449,29 @@ struct Consumer {
         cquota = md.quota;
         ccta0 = md.cta_start;
         bad = false;
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt)
+        for (int u = 0; u < NW; ++u) {
+            m0[u] = m1[u] = -INFINITY;
+            l0[u] = l1[u] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
-        const int r = 8 * w + g;
-        if (r < p.R) {
-            const int t = r / p.G, gg = r % p.G;
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                static_cast<const uint16_t*>(p.q) +
-                (((size_t)cb * p.T + t) * p.N + (size_t)ck * p.G + gg) * H);
+            for (int mt = 0; mt < C::kSteps; ++mt)
 #pragma unroll
-            for (int kk = 0; kk < C::kSteps; ++kk) {
-                qf[kk][0] = __ldg(qrow + kk * 8 + q4);
-                qf[kk][1] = __ldg(qrow + kk * 8 + 4 + q4);
+                for (int e = 0; e < 4; ++e) acc[u][mt][e] = 0.f;
+            const int r = row0(u) + g;
+            if (r < p.R) {
+                const int t = r / p.G, gg = r % p.G;
+                const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                    static_cast<const uint16_t*>(p.q) +
+                    (((size_t)cb * p.T + t) * p.N + (size_t)ck * p.G + gg) * H);
+#pragma unroll
+                for (int kk = 0; kk < C::kSteps; ++kk) {
+                    qf[u][kk][0] = __ldg(qrow + kk * 8 + q4);
+                    qf[u][kk][1] = __ldg(qrow + kk * 8 + 4 + q4);
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < C::kSteps; ++kk) qf[u][kk][0] = qf[u][kk][1] = 0u;
             }
-        } else {
-#pragma unroll
-            for (int kk = 0; kk < C::kSteps; ++kk) qf[kk][0] = qf[kk][1] = 0u;
         }
     }
 
@@ -505,16 +522,17 @@ struct Consumer {
         if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
         const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
         const int ntl = md.ntiles;
-        // ---- S^T = K_tile . Q^T for every tile (independent mma chains) ------
-        float sc[kTilesPerStage][4];
+        // ---- S^T = K_tile . Q^T for every tile and row tile (independent chains)
+        float sc[NW][kTilesPerStage][4];
+#pragma unroll
+        for (int u = 0; u < NW; ++u)
+#pragma unroll
+            for (int j = 0; j < kTilesPerStage; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[u][j][e] = 0.f;
         {
             const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
             const int chk = lane >> 4;
-#pragma unroll
-            for (int j = 0; j < kTilesPerStage; ++j) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sc[j][e] = 0.f;
-            }
 #pragma unroll
             for (int kk = 0; kk < C::kSteps; ++kk) {
                 const int hh = kk >> 2;
@@ -524,70 +542,80 @@ struct Consumer {
                 for (int j = 0; j < kTilesPerStage; ++j) {
                     uint32_t a[4];
                     ldsm_x4(kbase + j * C::kTileBytes + off, a);
-                    E::mma(sc[j], a, qf[kk][0], qf[kk][1]);
+#pragma unroll
+                    for (int u = 0; u < NW; ++u) E::mma(sc[u][j], a, qf[u][kk][0], qf[u][kk][1]);
                 }
             }
         }
-        // ---- scale, mask (unused tiles, causal bound, slots past the context) --
-        float x0 = -INFINITY, x1 = -INFINITY;
+        // ---- scale, mask (unused tiles, causal bound, slots past the context),
+        //      running max in the log2 domain, lazy rescale ----------------------
+        float ref0[NW], ref1[NW];
 #pragma unroll
-        for (int j = 0; j < kTilesPerStage; ++j) {
-            const int tb = (md.blk_i + j) * 16;
+        for (int u = 0; u < NW; ++u) {
+            float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[j][e] *= p.scale_log2;
-            if (j >= ntl) {
+            for (int j = 0; j < kTilesPerStage; ++j) {
+                const int tb = (md.blk_i + j) * 16;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[j][e] = -INFINITY;
-            } else if (tb + 15 > md.ctx - p.T) {  // some position hidden from some row
-                const int lim0 = md.ctx - p.T + t0, lim1 = md.ctx - p.T + t1;
-                const int pos0 = tb + g, pos8 = pos0 + 8;
-                if (pos0 > lim0) sc[j][0] = -INFINITY;
-                if (pos0 > lim1) sc[j][1] = -INFINITY;
-                if (pos8 > lim0) sc[j][2] = -INFINITY;
-                if (pos8 > lim1) sc[j][3] = -INFINITY;
+                for (int e = 0; e < 4; ++e) sc[u][j][e] *= p.scale_log2;
+                if (j >= ntl) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sc[u][j][e] = -INFINITY;
+                } else if (tb + 15 > md.ctx - p.T) {  // some position hidden from some row
+                    const int lim0 = md.ctx - p.T + t0[u], lim1 = md.ctx - p.T + t1[u];
+                    const int pos0 = tb + g, pos8 = pos0 + 8;
+                    if (pos0 > lim0) sc[u][j][0] = -INFINITY;
+                    if (pos0 > lim1) sc[u][j][1] = -INFINITY;
+                    if (pos8 > lim0) sc[u][j][2] = -INFINITY;
+                    if (pos8 > lim1) sc[u][j][3] = -INFINITY;
+                }
+                x0 = fmaxf(x0, fmaxf(sc[u][j][0], sc[u][j][2]));
+                x1 = fmaxf(x1, fmaxf(sc[u][j][1], sc[u][j][3]));
             }
-            x0 = fmaxf(x0, fmaxf(sc[j][0], sc[j][2]));
-            x1 = fmaxf(x1, fmaxf(sc[j][1], sc[j][3]));
-        }
-        // ---- running max (log2 domain), lazy rescale ----------------------------
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, o));
-            x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, o));
-        }
-        const bool need0 = x0 > m0 + kRescaleGap, need1 = x1 > m1 + kRescaleGap;
-        if (__any_sync(FULL, need0 || need1)) {
-            const float n0 = need0 ? x0 : m0, n1 = need1 ? x1 : m1;
-            const float f0 = need0 ? fast_exp2(m0 - n0) : 1.f;
-            const float f1 = need1 ? fast_exp2(m1 - n1) : 1.f;
-            l0 *= f0;
-            l1 *= f1;
-#pragma unroll
-            for (int mt = 0; mt < C::kSteps; ++mt) {
-                acc[mt][0] *= f0;
-                acc[mt][1] *= f1;
-                acc[mt][2] *= f0;
-                acc[mt][3] *= f1;
+            for (int o = 4; o < 32; o <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(FULL, x0, o));
+                x1 = fmaxf(x1, __shfl_xor_sync(FULL, x1, o));
             }
-            m0 = n0;
-            m1 = n1;
+            const bool need0 = x0 > m0[u] + kRescaleGap, need1 = x1 > m1[u] + kRescaleGap;
+            if (__any_sync(FULL, need0 || need1)) {
+                const float n0 = need0 ? x0 : m0[u], n1 = need1 ? x1 : m1[u];
+                const float f0 = need0 ? fast_exp2(m0[u] - n0) : 1.f;
+                const float f1 = need1 ? fast_exp2(m1[u] - n1) : 1.f;
+                l0[u] *= f0;
+                l1[u] *= f1;
+#pragma unroll
+                for (int mt = 0; mt < C::kSteps; ++mt) {
+                    acc[u][mt][0] *= f0;
+                    acc[u][mt][1] *= f1;
+                    acc[u][mt][2] *= f0;
+                    acc[u][mt][3] *= f1;
+                }
+                m0[u] = n0;
+                m1[u] = n1;
+            }
+            ref0[u] = (m0[u] == -INFINITY) ? 0.f : m0[u];
+            ref1[u] = (m1[u] == -INFINITY) ? 0.f : m1[u];
         }
-        const float ref0 = (m0 == -INFINITY) ? 0.f : m0;
-        const float ref1 = (m1 == -INFINITY) ? 0.f : m1;
         // ---- O^T += V_tile^T . P^T, tile by tile ------------------------------------
         const int tok = (lane & 7) + (lane >> 4) * 8;
         const int dof = ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int j = 0; j < kTilesPerStage; ++j) {
             if (j >= ntl) break;  // warp-uniform
-            const uint32_t pt0 =
-                E::pack(fast_exp2(sc[j][0] - ref0), fast_exp2(sc[j][1] - ref1));  // token g
-            const uint32_t pt1 =
-                E::pack(fast_exp2(sc[j][2] - ref0), fast_exp2(sc[j][3] - ref1));  // token g+8
-            l0 += E::lo(pt0) + E::lo(pt1);
-            l1 += E::hi(pt0) + E::hi(pt1);
-            // P^T as the B operand: tokens 2*q4+{0,1} (+8) of query row g.
-            const uint32_t pb0 = movm_t(pt0), pb1 = movm_t(pt1);
+            uint32_t pb0[NW], pb1[NW];
+#pragma unroll
+            for (int u = 0; u < NW; ++u) {
+                const uint32_t pt0 = E::pack(fast_exp2(sc[u][j][0] - ref0[u]),
+                                             fast_exp2(sc[u][j][1] - ref1[u]));  // token g
+                const uint32_t pt1 = E::pack(fast_exp2(sc[u][j][2] - ref0[u]),
+                                             fast_exp2(sc[u][j][3] - ref1[u]));  // token g+8
+                l0[u] += E::lo(pt0) + E::lo(pt1);
+                l1[u] += E::hi(pt0) + E::hi(pt1);
+                // P^T as the B operand: tokens 2*q4+{0,1} (+8) of query row g.
+                pb0[u] = movm_t(pt0);
+                pb1[u] = movm_t(pt1);
+            }
             const int tb = (md.blk_i + j) * 16;
             const bool tail = tb + 16 > md.ctx;
             uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
@@ -610,16 +638,17 @@ struct Consumer {
                     a[2] &= v89;
                     a[3] &= v89;
                 }
-                E::mma(acc[mt], a, pb0, pb1);
+#pragma unroll
+                for (int u = 0; u < NW; ++u) E::mma(acc[u][mt], a, pb0[u], pb1[u]);
             }
         }
     }
 
-    // Normalise and store rows 8w..8w+7 of segment (cb, ck).
-    __device__ void store(float L0, float L1, bool is_bad) {
+    // Normalise and store the rows of tile u of segment (cb, ck).
+    __device__ void store(int u, float L0, float L1, bool is_bad) {
         const float i0 = (!is_bad && L0 > 0.f) ? 1.f / L0 : 0.f;
         const float i1 = (!is_bad && L1 > 0.f) ? 1.f / L1 : 0.f;
-        const int r = 8 * w + g;
+        const int r = row0(u) + g;
         uint32_t* dst = nullptr;
         if (r < p.R) {
             const int t = r / p.G, gg = r % p.G;
@@ -629,8 +658,8 @@ struct Consumer {
         }
 #pragma unroll
         for (int mt = 0; mt < C::kSteps; ++mt) {
-            uint32_t x = is_bad ? 0u : E::pack(acc[mt][0] * i0, acc[mt][1] * i1);
-            uint32_t y = is_bad ? 0u : E::pack(acc[mt][2] * i0, acc[mt][3] * i1);
+            uint32_t x = is_bad ? 0u : E::pack(acc[u][mt][0] * i0, acc[u][mt][1] * i1);
+            uint32_t y = is_bad ? 0u : E::pack(acc[u][mt][2] * i0, acc[u][mt][3] * i1);
             x = movm_t(x);  // -> row g, dims mt*16 + 2*q4 + {0,1}
             y = movm_t(y);  // -> row g, dims mt*16 + 8 + 2*q4 + {0,1}
             if (dst) {
@@ -640,10 +669,10 @@ struct Consumer {
         }
     }
 
-    // Partial-result section of CTA `cta` for this row warp.  One per CTA is
-    // enough: the only segment a CTA hands to another for merging is its first.
-    __device__ float* section(int cta) const {
-        return p.partials + ((size_t)cta * p.nt + w) * C::kSectionFloats;
+    // Partial-result section of tile u in CTA `cta`.  One per CTA is enough:
+    // the only segment a CTA hands to another for merging is its first.
+    __device__ float* section(int cta, int u) const {
+        return p.partials + (((size_t)cta * p.nt + w) * NW + u) * C::kSectionFloats;
     }
     __device__ int32_t* flag(int cta) const { return p.flags + (size_t)cta * p.nt + w; }
 
@@ -651,44 +680,60 @@ struct Consumer {
     // that share a row pair.
     __device__ void reduce_l() {
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            l0 += __shfl_xor_sync(FULL, l0, o);
-            l1 += __shfl_xor_sync(FULL, l1, o);
+        for (int u = 0; u < NW; ++u) {
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                l0[u] += __shfl_xor_sync(FULL, l0[u], o);
+                l1[u] += __shfl_xor_sync(FULL, l1[u], o);
+            }
         }
     }
 
     // Per-lane layout of a group's state in the combine scratch.
-    static constexpr int kScratchFloats = 4 + C::kAccFloats;
+    static constexpr int kScratchFloats = NW * (4 + C::kAccFloats);
 
     __device__ void save_state(float* slot) const {
         float4* d = reinterpret_cast<float4*>(slot);
-        d[0] = make_float4(m0, m1, l0, l1);
 #pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt)
-            d[1 + mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+        for (int u = 0; u < NW; ++u) {
+            float4* du = d + u * (1 + C::kSteps);
+            du[0] = make_float4(m0[u], m1[u], l0[u], l1[u]);
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt)
+                du[1 + mt] = make_float4(acc[u][mt][0], acc[u][mt][1], acc[u][mt][2],
+                                         acc[u][mt][3]);
+        }
+    }
+
+    // Fold a (max, sum, accumulator) state of tile u into this one.
+    __device__ void fold(int u, float mc0, float mc1, float lc0, float lc1, const float4* v) {
+        const float n0 = fmaxf(m0[u], mc0), n1 = fmaxf(m1[u], mc1);
+        const float a0 = (m0[u] == -INFINITY) ? 0.f : fast_exp2(m0[u] - n0);
+        const float a1 = (m1[u] == -INFINITY) ? 0.f : fast_exp2(m1[u] - n1);
+        const float b0 = (mc0 == -INFINITY) ? 0.f : fast_exp2(mc0 - n0);
+        const float b1 = (mc1 == -INFINITY) ? 0.f : fast_exp2(mc1 - n1);
+        l0[u] = l0[u] * a0 + lc0 * b0;
+        l1[u] = l1[u] * a1 + lc1 * b1;
+#pragma unroll
+        for (int mt = 0; mt < C::kSteps; ++mt) {
+            acc[u][mt][0] = acc[u][mt][0] * a0 + v[mt].x * b0;
+            acc[u][mt][1] = acc[u][mt][1] * a1 + v[mt].y * b1;
+            acc[u][mt][2] = acc[u][mt][2] * a0 + v[mt].z * b0;
+            acc[u][mt][3] = acc[u][mt][3] * a1 + v[mt].w * b1;
+        }
+        m0[u] = n0;
+        m1[u] = n1;
     }
 
     // Fold another group's state (same segment, same rows) into this one.
     __device__ void absorb(const float* slot) {
         const float4* d = reinterpret_cast<const float4*>(slot);
-        const float4 h = d[0];
-        const float n0 = fmaxf(m0, h.x), n1 = fmaxf(m1, h.y);
-        const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - n0);
-        const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - n1);
-        const float b0 = (h.x == -INFINITY) ? 0.f : fast_exp2(h.x - n0);
-        const float b1 = (h.y == -INFINITY) ? 0.f : fast_exp2(h.y - n1);
-        l0 = l0 * a0 + h.z * b0;
-        l1 = l1 * a1 + h.w * b1;
 #pragma unroll
-        for (int mt = 0; mt < C::kSteps; ++mt) {
-            const float4 v = d[1 + mt];
-            acc[mt][0] = acc[mt][0] * a0 + v.x * b0;
-            acc[mt][1] = acc[mt][1] * a1 + v.y * b1;
-            acc[mt][2] = acc[mt][2] * a0 + v.z * b0;
-            acc[mt][3] = acc[mt][3] * a1 + v.w * b1;
+        for (int u = 0; u < NW; ++u) {
+            const float4* du = d + u * (1 + C::kSteps);
+            const float4 h = du[0];
+            fold(u, h.x, h.y, h.z, h.w, du + 1);
         }
-        m0 = n0;
-        m1 = n1;
     }
 
     // Finish the segment (row sums already reduced).  A split segment's pieces
@@ -702,85 +747,78 @@ struct Consumer {
         const int last = (cstart + cnblk - 1) / cquota;
         const int me = blockIdx.x;
         if (first == last) {
-            store(l0, l1, bad);
+#pragma unroll
+            for (int u = 0; u < NW; ++u) store(u, l0[u], l1[u], bad);
             return;
         }
         if (me != first) {
-            float* sec = section(me);
-            if (g == 0) {
-                sec[2 * q4] = m0;
-                sec[2 * q4 + 1] = m1;
-                sec[8 + 2 * q4] = l0;
-                sec[8 + 2 * q4 + 1] = l1;
-            }
-            if (lane == 0) sec[16] = bad ? 1.f : 0.f;
-            float4* a4 = reinterpret_cast<float4*>(sec + C::kHeaderFloats) + lane * C::kSteps;
 #pragma unroll
-            for (int mt = 0; mt < C::kSteps; ++mt)
-                a4[mt] = make_float4(acc[mt][0], acc[mt][1], acc[mt][2], acc[mt][3]);
+            for (int u = 0; u < NW; ++u) {
+                float* sec = section(me, u);
+                if (g == 0) {
+                    sec[2 * q4] = m0[u];
+                    sec[2 * q4 + 1] = m1[u];
+                    sec[8 + 2 * q4] = l0[u];
+                    sec[8 + 2 * q4 + 1] = l1[u];
+                }
+                if (lane == 0) sec[16] = bad ? 1.f : 0.f;
+                float4* a4 = reinterpret_cast<float4*>(sec + C::kHeaderFloats) + lane * C::kSteps;
+#pragma unroll
+                for (int mt = 0; mt < C::kSteps; ++mt)
+                    a4[mt] = make_float4(acc[u][mt][0], acc[u][mt][1], acc[u][mt][2],
+                                         acc[u][mt][3]);
+            }
             __syncwarp();  // orders the lanes' stores before lane 0's release
             if (lane == 0) st_release_gpu(flag(me), 1);
             return;
         }
-        // ---- merger: batches of published pieces, loads issued before use ----
+        // ---- merger: wait for every published piece, then fold them in, in
+        //      batches whose loads are all in flight before any is used -----
+        int ok = 1;
+        if (lane == 0)
+            for (int c = first + 1; c <= last; ++c) ok &= wait_flag(flag(c)) ? 1 : 0;
+        ok = __shfl_sync(FULL, ok, 0);
+        if (!ok) {  // a piece never arrived (cannot happen unless a CTA aborted)
+            if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
+#pragma unroll
+            for (int u = 0; u < NW; ++u) store(u, 0.f, 0.f, true);
+            return;
+        }
+        __syncwarp();  // orders lane 0's acquires before every lane's loads
         constexpr int kBatch = (H == 64) ? 4 : 2;
         bool any_bad = bad;
-        for (int c0 = first + 1; c0 <= last; c0 += kBatch) {
-            int ok = 1;
-            if (lane == 0) {
 #pragma unroll
-                for (int j = 0; j < kBatch; ++j)
-                    if (c0 + j <= last) ok &= wait_flag(flag(c0 + j)) ? 1 : 0;
-            }
-            ok = __shfl_sync(FULL, ok, 0);
-            if (!ok) {  // a piece never arrived (cannot happen unless a CTA aborted)
-                if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
-                store(0.f, 0.f, true);
-                return;
-            }
-            __syncwarp();  // orders lane 0's acquires before every lane's loads
-            float mc[kBatch][2], lc[kBatch][2], fl[kBatch];
-            float4 v[kBatch][C::kSteps];
-            // Unconditional loads (past the last piece the batch re-reads it and
-            // then gives it no weight): every load is in flight before any use.
+        for (int u = 0; u < NW; ++u) {
+            for (int c0 = first + 1; c0 <= last; c0 += kBatch) {
+                float mc[kBatch][2], lc[kBatch][2], fl[kBatch];
+                float4 v[kBatch][C::kSteps];
+                // Unconditional loads (past the last piece the batch re-reads it
+                // and then gives it no weight).
 #pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                const float* sc = section(min(c0 + j, last));
-                mc[j][0] = __ldcg(sc + 2 * q4);
-                mc[j][1] = __ldcg(sc + 2 * q4 + 1);
-                lc[j][0] = __ldcg(sc + 8 + 2 * q4);
-                lc[j][1] = __ldcg(sc + 8 + 2 * q4 + 1);
-                fl[j] = __ldcg(sc + 16);
-                const float4* b4 =
-                    reinterpret_cast<const float4*>(sc + C::kHeaderFloats) + lane * C::kSteps;
+                for (int j = 0; j < kBatch; ++j) {
+                    const float* sc = section(min(c0 + j, last), u);
+                    mc[j][0] = __ldcg(sc + 2 * q4);
+                    mc[j][1] = __ldcg(sc + 2 * q4 + 1);
+                    lc[j][0] = __ldcg(sc + 8 + 2 * q4);
+                    lc[j][1] = __ldcg(sc + 8 + 2 * q4 + 1);
+                    fl[j] = __ldcg(sc + 16);
+                    const float4* b4 =
+                        reinterpret_cast<const float4*>(sc + C::kHeaderFloats) + lane * C::kSteps;
 #pragma unroll
-                for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = __ldcg(b4 + mt);
-            }
-#pragma unroll
-            for (int j = 0; j < kBatch; ++j) {
-                if (c0 + j > last) continue;
-                any_bad |= fl[j] != 0.f;
-                const float n0 = fmaxf(m0, mc[j][0]), n1 = fmaxf(m1, mc[j][1]);
-                const float a0 = (m0 == -INFINITY) ? 0.f : fast_exp2(m0 - n0);
-                const float a1 = (m1 == -INFINITY) ? 0.f : fast_exp2(m1 - n1);
-                const float b0 = (mc[j][0] == -INFINITY) ? 0.f : fast_exp2(mc[j][0] - n0);
-                const float b1 = (mc[j][1] == -INFINITY) ? 0.f : fast_exp2(mc[j][1] - n1);
-                l0 = l0 * a0 + lc[j][0] * b0;
-                l1 = l1 * a1 + lc[j][1] * b1;
-#pragma unroll
-                for (int mt = 0; mt < C::kSteps; ++mt) {
-                    acc[mt][0] = acc[mt][0] * a0 + v[j][mt].x * b0;
-                    acc[mt][1] = acc[mt][1] * a1 + v[j][mt].y * b1;
-                    acc[mt][2] = acc[mt][2] * a0 + v[j][mt].z * b0;
-                    acc[mt][3] = acc[mt][3] * a1 + v[j][mt].w * b1;
+                    for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = __ldcg(b4 + mt);
                 }
-                m0 = n0;
-                m1 = n1;
+#pragma unroll
+                for (int j = 0; j < kBatch; ++j) {
+                    if (c0 + j > last) continue;
+                    any_bad |= fl[j] != 0.f;
+                    fold(u, mc[j][0], mc[j][1], lc[j][0], lc[j][1], v[j]);
+                }
             }
         }
         if (lane == 0)
             for (int c = first + 1; c <= last; ++c) *flag(c) = 0;  // ready for the next call
-        store(l0, l1, any_bad);
+#pragma unroll
+        for (int u = 0; u < NW; ++u) store(u, l0[u], l1[u], any_bad);
     }
 };
 
@@ -789,19 +827,19 @@ struct Consumer {
 // 8*(w % nt) .. +7.  Every warp reads every stage's description, so all groups
 // agree on segment boundaries; at each boundary the groups' partial states
 // meet in shared memory and group 0 finishes the segment.
-template <int H, bool BF16>
+template <int H, bool BF16, int NW>
 __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
                          const StageMeta* meta, float* scratch, volatile int* abort_flag,
                          int w) {
     using C = Cfg<H>;
-    using CS = Consumer<H, BF16>;
+    using CS = Consumer<H, BF16, NW>;
     const int gi = w / p.nt, wr = w % p.nt;
     CS cs(p, wr);
     const int lane = threadIdx.x & 31;
     griddep_wait();  // q, the workspace and out follow the previous kernels
     auto slot = [&](int buf, int gg) {
         return scratch +
-               ((((size_t)buf * (kGroups - 1) + (gg - 1)) * p.nt + wr) * 32 + lane) *
+               ((((size_t)buf * (p.groups - 1) + (gg - 1)) * p.nt + wr) * 32 + lane) *
                    CS::kScratchFloats;
     };
     int nseg = 0;  // segments closed so far (phase of the combine barrier)
@@ -818,7 +856,7 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
         }
         if (gi == 0) {
 #pragma unroll
-            for (int gg = 1; gg < kGroups; ++gg) cs.absorb(slot(buf, gg));
+            for (int gg = 1; gg < p.groups; ++gg) cs.absorb(slot(buf, gg));
             cs.finalize();
         }
         ++nseg;
@@ -826,8 +864,8 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
     };
     int cur = -1;
     for (int it = 0;; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t par = (it / C::kStages) & 1;
+        const int s = it % p.stages;
+        const uint32_t par = (it / p.stages) & 1;
         if (!mbar_wait(smem_addr(&bar.meta[s]), par)) {
             if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
             *abort_flag = 1;
@@ -846,7 +884,7 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
         }
         if (md.flags & kBad) {
             cs.bad = true;
-        } else if (it % kGroups == gi) {
+        } else if (it % p.groups == gi) {
             if (!mbar_wait(smem_addr(&bar.full[s]), par)) {
                 if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
                 *abort_flag = 1;
@@ -859,8 +897,10 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
     }
 }
 
-template <int H, bool BF16>
-__global__ void __launch_bounds__(32 * (kGroups * kMaxRowWarps + 1))
+// NW = 1: up to 6 row warps per group; NW = 2 (two 8-row tiles per warp, for
+// many query rows) up to 3, with the register budget of the smaller CTA.
+template <int H, bool BF16, int NW>
+__global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRowWarps / 2 + 1))
     attention_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
     using C = Cfg<H>;
@@ -869,20 +909,20 @@ __global__ void __launch_bounds__(32 * (kGroups * kMaxRowWarps + 1))
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = smem;
     Bars bar;
-    bar.full = reinterpret_cast<uint64_t*>(smem + (size_t)C::kStages * C::kStageBytes);
-    bar.meta = bar.full + C::kStages;
-    bar.empty = bar.meta + C::kStages;
-    bar.cbar = bar.empty + C::kStages;
+    bar.full = reinterpret_cast<uint64_t*>(smem + (size_t)p.stages * C::kStageBytes);
+    bar.meta = bar.full + p.stages;
+    bar.empty = bar.meta + p.stages;
+    bar.cbar = bar.empty + p.stages;
     StageMeta* meta = reinterpret_cast<StageMeta*>(bar.cbar + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + C::kStages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + p.stages);
     float* scratch = reinterpret_cast<float*>(
         (reinterpret_cast<uintptr_t>(abort_flag + 1) + 15) & ~uintptr_t(15));
-    const int consumers = kGroups * p.nt;
+    const int consumers = p.groups * p.nt;
 
     const int warp = threadIdx.x >> 5;
     griddep_launch_dependents();
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < p.stages; ++s) {
             mbar_init(smem_addr(&bar.full[s]), 1);
             mbar_init(smem_addr(&bar.meta[s]), 1);
             mbar_init(smem_addr(&bar.empty[s]), consumers);
@@ -895,26 +935,45 @@ __global__ void __launch_bounds__(32 * (kGroups * kMaxRowWarps + 1))
     if (warp == consumers)
         producer<H>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
     else
-        consumer<H, BF16>(p, stages, bar, meta, scratch, abort_flag, warp);
+        consumer<H, BF16, NW>(p, stages, bar, meta, scratch, abort_flag, warp);
 }
 
 // ---------------------------------------------------------------------------
 // Host side
-template <int H, bool BF16>
+template <int H, bool BF16, int NW>
 const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(&attention_kernel<H, BF16>);
+    return reinterpret_cast<const void*>(&attention_kernel<H, BF16, NW>);
 }
 
-const void* pick_kernel(int H, bool bf16) {
-    if (H == 64) return bf16 ? kernel_ptr<64, true>() : kernel_ptr<64, false>();
-    return bf16 ? kernel_ptr<128, true>() : kernel_ptr<128, false>();
+const void* pick_kernel(int H, bool bf16, int nw) {
+    if (H == 64) {
+        if (nw == 1) return bf16 ? kernel_ptr<64, true, 1>() : kernel_ptr<64, false, 1>();
+        return bf16 ? kernel_ptr<64, true, 2>() : kernel_ptr<64, false, 2>();
+    }
+    if (nw == 1) return bf16 ? kernel_ptr<128, true, 1>() : kernel_ptr<128, false, 1>();
+    return bf16 ? kernel_ptr<128, true, 2>() : kernel_ptr<128, false, 2>();
 }
 
-// Dynamic shared memory of one CTA with nt row warps per consumer group.
-size_t smem_for(int H, int nt) {
-    return H == 64 ? Cfg<64>::kSmem + nt * Cfg<64>::kScratchBytesPerRowWarp
-                   : Cfg<128>::kSmem + nt * Cfg<128>::kScratchBytesPerRowWarp;
+// Consumer groups for nt row warps.  (A third group was measured slower on
+// the 40-row verify workload: stages then contend for shared memory.)
+int groups_for(int /*nt*/) { return kGroups; }
+
+// Row warps a group may have with nw 8-row tiles per warp (48 rows at most).
+int max_row_warps(int nw) { return nw == 1 ? kMaxRowWarps : kMaxRowWarps / 2; }
+
+// Dynamic shared memory of one CTA: nt row warps (nw tiles each) per consumer
+// group and a ring of `stages` stages.
+template <int H>
+size_t smem_of(int nt, int nw, int stages) {
+    using C = Cfg<H>;
+    return C::kFixed + (size_t)stages * (C::kStageBytes + C::kStageOverhead) +
+           (size_t)(groups_for(nt) - 1) * nt * nw * C::kScratchBytesPerRowWarp;
 }
+size_t smem_for(int H, int nt, int nw, int stages) {
+    return H == 64 ? smem_of<64>(nt, nw, stages) : smem_of<128>(nt, nw, stages);
+}
+int default_stages(int H) { return H == 64 ? Cfg<64>::kStages : Cfg<128>::kStages; }
+
 size_t section_floats(int H) {
     return H == 64 ? Cfg<64>::kSectionFloats : Cfg<128>::kSectionFloats;
 }
@@ -954,23 +1013,24 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
 // CTAs of one variant resident per SM, queried once per (device, variant) so
 // that later calls -- including calls being captured into a CUDA graph -- make
 // no attribute or occupancy API calls.
-int resident_ctas(int H, bool bf16, int nt, size_t smem) {
+int resident_ctas(int H, bool bf16, int nt, int nw, size_t smem) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int>, int> cache;
+    static std::map<std::tuple<int, int, int, int, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key = std::make_tuple(dev, H, (int)bf16, nt);
+    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void* kern = pick_kernel(H, bf16);
+    const void* kern = pick_kernel(H, bf16, nw);
     // The attribute belongs to the kernel, whatever the row-warp count: set it
-    // to the largest launch any shape can make.
+    // to the largest launch any shape makes.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_for(H, kMaxRowWarps)) != cudaSuccess)
+                             (int)smem_for(H, max_row_warps(nw), nw, default_stages(H))) !=
+        cudaSuccess)
         return 0;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * (kGroups * nt + 1),
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * (groups_for(nt) * nt + 1),
                                                       smem) !=
         cudaSuccess)
         return 0;
@@ -1001,10 +1061,16 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     const int G = s.N / s.K;
     const long long R = (long long)s.T * G;
     if (R > 8 * kMaxRowWarps) return GQA_ERR_SHAPE;
-    const int nt = (int)((R + 7) / 8);
-    const int threads = 32 * (kGroups * nt + 1);
-    const size_t smem = smem_for(s.H, nt);
-    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, smem);
+    // One 8-row tile per warp.  (Two tiles per warp -- each K/V fragment read
+    // from shared memory serving 16 rows -- measured slower on the 40-row verify
+    // workload: fewer warps hide less latency.  The kernel keeps both forms.)
+    const int nw = 1;
+    const int nt = (int)((R + 8 * nw - 1) / (8 * nw));
+    const int groups = groups_for(nt);
+    const int threads = 32 * (groups * nt + 1);
+    int stages = default_stages(s.H);
+    size_t smem = smem_for(s.H, nt, nw, stages);
+    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, smem);
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
@@ -1020,13 +1086,16 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     plan->consumer_warps = nt;
     plan->threads = threads;
     plan->smem = smem;
+    plan->stages = stages;
+    plan->groups = groups;
+    plan->tiles_per_warp = nw;
     // The publication flags live in a fixed region at the start of every
     // workspace, whatever the shape, and partial results always start after
     // it: partial data of one call can then never sit where a later call of
     // another shape expects zeroed flags.
     if (grid * nt > kMaxFlags) return GQA_ERR_SHAPE;
     plan->flags_bytes = (size_t)kMaxFlags * 4;
-    plan->partial_floats_per_cta = section_floats(s.H) * nt;
+    plan->partial_floats_per_cta = section_floats(s.H) * nt * nw;
     plan->workspace = plan->flags_bytes + (size_t)grid * plan->partial_floats_per_cta * 4;
     return GQA_OK;
 }
@@ -1055,6 +1124,8 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     p.G = s.N / s.K;
     p.R = s.T * p.G;
     p.nt = plan.consumer_warps;
+    p.stages = plan.stages;
+    p.groups = plan.groups;
     p.max_blocks = s.max_blocks_per_seq;
     p.num_blocks = s.num_blocks;
     const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
@@ -1077,12 +1148,22 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cudaError_t e;
-    if (s.H == 64)
-        e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<64, true>, tmk, tmv, p)
-                 : cudaLaunchKernelEx(&cfg, attention_kernel<64, false>, tmk, tmv, p);
-    else
-        e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<128, true>, tmk, tmv, p)
-                 : cudaLaunchKernelEx(&cfg, attention_kernel<128, false>, tmk, tmv, p);
+    const int nw = plan.tiles_per_warp;
+    if (s.H == 64) {
+        if (nw == 1)
+            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<64, true, 1>, tmk, tmv, p)
+                     : cudaLaunchKernelEx(&cfg, attention_kernel<64, false, 1>, tmk, tmv, p);
+        else
+            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<64, true, 2>, tmk, tmv, p)
+                     : cudaLaunchKernelEx(&cfg, attention_kernel<64, false, 2>, tmk, tmv, p);
+    } else {
+        if (nw == 1)
+            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<128, true, 1>, tmk, tmv, p)
+                     : cudaLaunchKernelEx(&cfg, attention_kernel<128, false, 1>, tmk, tmv, p);
+        else
+            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<128, true, 2>, tmk, tmv, p)
+                     : cudaLaunchKernelEx(&cfg, attention_kernel<128, false, 2>, tmk, tmv, p);
+    }
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 

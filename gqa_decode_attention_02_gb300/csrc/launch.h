@@ -12,9 +12,12 @@ namespace gqa {
 // Launch plan of the attention kernel for one shape on the current device.
 struct AttnPlan {
     int grid;            // persistent CTAs
-    int consumer_warps;  // one per 8 query rows (rows = T * G)
+    int consumer_warps;  // row warps per group (8 * tiles_per_warp query rows each)
     int threads;
     size_t smem;         // dynamic shared memory per CTA
+    int stages;          // depth of the shared-memory ring
+    int groups;          // stage-parallel consumer groups
+    int tiles_per_warp;  // 8-row query tiles per consumer warp (1 or 2)
     size_t flags_bytes;             // fixed region of publication flags
     size_t partial_floats_per_cta;
     size_t workspace;    // total bytes
