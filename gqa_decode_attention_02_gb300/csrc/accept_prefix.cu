@@ -10,8 +10,8 @@
 // length is updated here, on the device.
 //
 // One thread-block cluster per sequence.  The cluster's CS blocks split the
-// sequence's T*V logits into CS contiguous ranges; each block reduces the
-// argmax of every row its range touches to a 64-bit key
+// vocabulary into CS column slices; each block reduces its slice of every row
+// (several rows' 16-byte loads in flight at once) to a 64-bit argmax key
 //     (order-preserving image of the value) << 32 | (~index)
 // so that a plain max over keys picks the largest value and, among equal
 // values, the smallest index; NaN maps above +inf (first NaN wins) and -0 is
@@ -28,7 +28,8 @@ namespace {
 
 constexpr int kMaxT = 64;
 constexpr int kMaxCluster = 8;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kRowsPerPass = 8;  // rows whose loads are in flight together
 
 __device__ __forceinline__ unsigned long long argmax_key(float x, uint32_t idx) {
     uint32_t u = __float_as_uint(x);
@@ -67,44 +68,78 @@ __device__ __forceinline__ void cluster_sync_all() {
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Cluster rank r reduces columns [r*S, min(V, (r+1)*S)) of every row of its
+// sequence (S a multiple of 4): the T slices are loaded a few rows at a time
+// with 16-byte loads (vec) or scalar loads, all of a pass in flight together.
+template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
     accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ draft,
                   int32_t* accepted, int32_t* next_token, int32_t* ctx_io, int32_t* status,
                   int T, int V, int cs) {
     __shared__ unsigned long long table[kMaxT * kMaxCluster];  // used in rank 0
-    __shared__ unsigned long long red[kThreads / 32];
+    __shared__ unsigned long long red[kThreads / 32][kRowsPerPass];
     griddep_launch_dependents();
     griddep_wait();  // logits and lengths follow the previous kernels
     const uint32_t rank = cluster_rank();
     const int b = blockIdx.y;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long TV = (long long)T * V;
-    const long long chunk = (TV + cs - 1) / cs;
-    const long long lo = (long long)rank * chunk;
-    const long long hi = lo + chunk < TV ? lo + chunk : TV;
-    const float* row0 = logits + (size_t)b * TV;
+    const int S = (((V + cs - 1) / cs) + 3) & ~3;
+    const int c_lo = min(V, (int)rank * S), c_hi = min(V, c_lo + S);
+    const float* row0 = logits + (size_t)b * T * V;
+    // Block 0's shared memory may be written only once block 0 is running:
+    // arrive now, wait before the first remote store.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-    for (int t = 0; t < T; ++t) {
-        const long long rs = (long long)t * V, re = rs + V;
-        const long long s = lo > rs ? lo : rs;
-        const long long e = hi < re ? hi : re;
-        unsigned long long key = 0ull;  // below every real key
-        if (s < e) {
-            const float* row = row0 + rs;
-            const int vs = (int)(s - rs), ve = (int)(e - rs);
-#pragma unroll 8
-            for (int v = vs + tid; v < ve; v += kThreads)
-                key = umax64(key, argmax_key(__ldg(row + v), (uint32_t)v));
+    for (int t0 = 0; t0 < T; t0 += kRowsPerPass) {
+        unsigned long long key[kRowsPerPass];
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
-            if (lane == 0) red[warp] = key;
-            __syncthreads();
-            if (tid == 0) {
-                for (int i = 1; i < kThreads / 32; ++i) key = umax64(key, red[i]);
+        for (int i = 0; i < kRowsPerPass; ++i) key[i] = 0ull;  // below every real key
+        if (kVec) {
+            // columns c_lo + 4*(tid + k*kThreads), all rows of the pass
+            for (int c = c_lo + 4 * tid; c < c_hi; c += 4 * kThreads) {
+                float4 v[kRowsPerPass];
+#pragma unroll
+                for (int i = 0; i < kRowsPerPass; ++i)
+                    if (t0 + i < T)
+                        v[i] = __ldg(reinterpret_cast<const float4*>(row0 + (size_t)(t0 + i) * V + c));
+#pragma unroll
+                for (int i = 0; i < kRowsPerPass; ++i) {
+                    if (t0 + i < T) {
+                        key[i] = umax64(key[i], argmax_key(v[i].x, (uint32_t)c));
+                        key[i] = umax64(key[i], argmax_key(v[i].y, (uint32_t)c + 1));
+                        key[i] = umax64(key[i], argmax_key(v[i].z, (uint32_t)c + 2));
+                        key[i] = umax64(key[i], argmax_key(v[i].w, (uint32_t)c + 3));
+                    }
+                }
             }
-            __syncthreads();
+        } else {
+            for (int c = c_lo + tid; c < c_hi; c += kThreads) {
+#pragma unroll
+                for (int i = 0; i < kRowsPerPass; ++i)
+                    if (t0 + i < T)
+                        key[i] = umax64(key[i],
+                                        argmax_key(__ldg(row0 + (size_t)(t0 + i) * V + c),
+                                                   (uint32_t)c));
+            }
         }
-        if (tid == 0) st_remote_u64(&table[t * kMaxCluster + rank], 0, key);
+#pragma unroll
+        for (int i = 0; i < kRowsPerPass; ++i) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                key[i] = umax64(key[i], __shfl_xor_sync(0xffffffffu, key[i], o));
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < kRowsPerPass; ++i) red[warp][i] = key[i];
+        }
+        if (t0 == 0) asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+        __syncthreads();
+        if (tid < kRowsPerPass && t0 + tid < T) {
+            unsigned long long k = 0ull;
+            for (int wi = 0; wi < kThreads / 32; ++wi) k = umax64(k, red[wi][tid]);
+            st_remote_u64(&table[(t0 + tid) * kMaxCluster + rank], 0, k);
+        }
+        __syncthreads();
     }
     cluster_sync_all();
     if (rank != 0 || tid != 0) return;
@@ -133,8 +168,8 @@ gqa_status launch_accept_prefix(int B, int T, int V, const float* logits, const 
                                 int32_t* accepted, int32_t* next_token, int32_t* ctx_io,
                                 int32_t* dev_status, cudaStream_t stream) {
     if (B == 0) return GQA_OK;
-    const long long TV = (long long)T * V;
-    int cs = (int)((TV + 4095) / 4096);
+    // one cluster of up to 8 blocks per sequence; each block takes V/cs columns
+    int cs = (int)((V + 1023) / 1024);
     if (cs > kMaxCluster) cs = kMaxCluster;
     if (cs < 1) cs = 1;
     cudaLaunchConfig_t cfg = {};
@@ -149,8 +184,13 @@ gqa_status launch_accept_prefix(int B, int T, int V, const float* logits, const 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, accept_kernel, logits, draft, accepted,
-                                             next_token, ctx_io, dev_status, T, V, cs);
+    // 16-byte loads need every row to start on a 16-byte boundary
+    const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+    const cudaError_t e =
+        vec ? cudaLaunchKernelEx(&cfg, accept_kernel<true>, logits, draft, accepted, next_token,
+                                 ctx_io, dev_status, T, V, cs)
+            : cudaLaunchKernelEx(&cfg, accept_kernel<false>, logits, draft, accepted, next_token,
+                                 ctx_io, dev_status, T, V, cs);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -59,3 +59,25 @@ def test_context_length_update_underflow_is_reported(gpu):
     torch.cuda.synchronize()
     assert ctx.cpu().tolist() == [3, 1]
     assert int(st.item()) == 7
+
+
+@pytest.mark.parametrize("V", [32768, 32001])  # 16-byte loads; scalar loads
+def test_accept_ties_across_cluster_slices(gpu, V):
+    """Equal maxima and NaNs in several blocks' column slices: the smallest
+    index still wins, over more rows than one pass holds."""
+    rng = np.random.default_rng(V)
+    B, T = 6, 13
+    lg = rng.integers(-3, 2, size=(B, T, V)).astype(np.float32)  # max 1, ties everywhere
+    lg[0, :, V - 5] = np.nan  # a NaN only in the last slice
+    lg[1, :, ::4097] = np.nan  # NaNs in every slice: the first one wins
+    lg[2, :, :] = -0.0
+    lg[2, :, V // 2] = 0.0  # +0 ties with -0: index 0 wins
+    lg[3, :, V - 1] = 2.0  # a unique maximum at the very end
+    draft = np.zeros((B, T - 1), np.int32)
+    for b in range(B):
+        for t in range(T - 1):
+            draft[b, t] = oracle.argmax(lg[b, t]) if (b + t) % 5 else 1
+    ra, rn, _ = oracle.accept_prefix(lg, draft)
+    ga, gn, _ = run(lg, draft, None, gpu)
+    np.testing.assert_array_equal(ga, ra)
+    np.testing.assert_array_equal(gn, rn)
