@@ -1,5 +1,5 @@
-"""fp64 CPU oracle for paged GQA decode/verify attention, KV append and greedy
-prefix acceptance.
+"""fp64 CPU oracle for paged GQA decode/verify attention, KV append, greedy
+prefix acceptance and speculative sampling.
 
 TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the bench's CPU
 baseline leg may import this package; the product path never does.  It shares no
@@ -12,6 +12,7 @@ from .oracle import (  # noqa: F401
     kv_append,
     attention,
     accept_prefix,
+    accept_sampled,
     argmax,
     num_threads,
 )

@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain fp64 CPU oracle for paged grouped-query decode / verify
- * attention, the KV append that precedes it, and greedy prefix acceptance.
+ * attention, the KV append that precedes it, greedy prefix acceptance and
+ * stochastic acceptance (speculative sampling).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
  * this file: only the tests, the package's smoke check and the bench's CPU
@@ -243,6 +244,118 @@ void oracle_accept_prefix(int B, int T, int V, const float *logits,
 
 /* argmax of one row, exposed so tests can pin the tie / NaN reading directly. */
 int oracle_argmax(const float *x, int V) { return argmax_row(x, V); }
+
+/* ---- speculative sampling: stochastic acceptance ---------------------------
+ * [CS336-RU] §"Спекулятивное сэмплирование": the draft model p proposes tokens,
+ * the target model q scores them in one pass, and a modified rejection sampler
+ * decides.  Draft token x (drawn from p) is kept with probability
+ * min(1, q(x)/p(x)); at the first rejection one token is drawn from the
+ * residual max(q - p, 0), renormalised, and the run stops; if every draft is
+ * kept, one more token is drawn from the target's next distribution.  The
+ * page's two-token example shows the emitted token is an exact sample of q.
+ *
+ * q [B][T][V] fp32 (q[b][t] is the target's distribution after the prefix and
+ * drafts 0..t-1); p [B][T-1][V] fp32 (the draft's distribution that draft[b][t]
+ * was drawn from); u [B][T] fp64 uniforms in [0,1): u[b][t], t < T-1, decides
+ * draft t, u[b][T-1] draws the final token.
+ *
+ * Our readings where the page leaves the arithmetic open:
+ *   - "kept with probability min(1, q/p)" is the test u * p(x) < q(x) with u,
+ *     p(x), q(x) widened to double (the product is then exact; p(x) = 0 keeps x
+ *     iff q(x) > 0).  A draft id outside [0, V) is rejected.
+ *   - A categorical draw from weights w_v is the inverse CDF on the weights
+ *     rounded down to multiples of 2^-40: W_v = floor(w_v * 2^40), S = sum W_v
+ *     (exact integers), r = floor(u * S) (double product, clamped to S-1), and
+ *     the token is the least v with W_0 + ... + W_v > r.  The rounding moves at
+ *     most V * 2^-40 of probability mass.
+ *   - The residual weight is max(q(v) - p(v), 0) with the difference rounded
+ *     once to fp32.  A residual of total weight zero (q == p up to rounding)
+ *     falls back to q itself.
+ *   - An entry that is not a probability (NaN, < 0, > 1) is taken as 0, and a
+ *     uniform outside [0, 1) as 0; either sets seq_err[b] = ORACLE_ERR_PROBS.
+ *     A row with no weight at all gives token 0 and ORACLE_ERR_PROBS.
+ *   - ctx_inout[b] -= (T-1-a) as in greedy acceptance; a result below zero
+ *     leaves it unchanged and sets ORACLE_ERR_CONTEXT.
+ * Requires 1 <= T <= 64. */
+#define ORACLE_ERR_PROBS 10 /* an input is not a probability or a uniform in [0,1) */
+
+static float clean_prob(float x, int *bad) {
+    if (x >= 0.0f && x <= 1.0f) return x;
+    *bad = 1;
+    return 0.0f;
+}
+
+/* floor(w * 2^40) for w in [0, 1] */
+static uint64_t fixed40(float w) { return (uint64_t)((double)w * 1099511627776.0); }
+
+/* weight of token v: residual max(q - p, 0) when p is given, else q */
+static uint64_t draw_weight(const float *qrow, const float *prow, int v, int *bad) {
+    float w = clean_prob(qrow[v], bad);
+    if (prow) {
+        float d = w - clean_prob(prow[v], bad);
+        w = d > 0.0f ? d : 0.0f;
+    }
+    return fixed40(w);
+}
+
+static int draw_token(const float *qrow, const float *prow, int V, double u, int *bad) {
+    uint64_t S = 0;
+    for (int v = 0; v < V; ++v) S += draw_weight(qrow, prow, v, bad);
+    if (S == 0) return -1;
+    uint64_t r = (uint64_t)(u * (double)S);
+    if (r > S - 1) r = S - 1;
+    uint64_t c = 0;
+    for (int v = 0; v < V; ++v) {
+        c += draw_weight(qrow, prow, v, bad);
+        if (c > r) return v;
+    }
+    return V - 1; /* not reached: c ends at S > r */
+}
+
+void oracle_accept_sampled(int B, int T, int V, const float *q, const float *p,
+                           const int32_t *draft, const double *u, int32_t *accepted,
+                           int32_t *next_token, int32_t *ctx_inout, int32_t *seq_err) {
+    for (int b = 0; b < B; ++b) {
+        int bad = 0;
+        const double *ub = u + (size_t)b * T;
+        double uu[64];
+        for (int t = 0; t < T && t < 64; ++t) {
+            uu[t] = ub[t];
+            if (!(uu[t] >= 0.0 && uu[t] < 1.0)) {
+                uu[t] = 0.0;
+                bad = 1;
+            }
+        }
+        int a = 0;
+        while (a < T - 1) {
+            const int x = draft[(size_t)b * (T - 1) + a];
+            if (x < 0 || x >= V) break;
+            const double qx = clean_prob(q[((size_t)b * T + a) * V + x], &bad);
+            const double px = clean_prob(p[((size_t)b * (T - 1) + a) * V + x], &bad);
+            if (!(uu[a] * px < qx)) break;
+            ++a;
+        }
+        const float *qrow = q + ((size_t)b * T + a) * V;
+        const float *prow = (a < T - 1) ? p + ((size_t)b * (T - 1) + a) * V : NULL;
+        int tok = draw_token(qrow, prow, V, uu[T - 1], &bad);
+        if (tok < 0 && prow) tok = draw_token(qrow, NULL, V, uu[T - 1], &bad);
+        if (tok < 0) {
+            tok = 0;
+            bad = 1;
+        }
+        accepted[b] = a;
+        next_token[b] = tok;
+        seq_err[b] = bad ? ORACLE_ERR_PROBS : 0;
+        if (ctx_inout) {
+            const int nc = ctx_inout[b] - (T - 1 - a);
+            if (nc < 0) {
+                if (!seq_err[b]) seq_err[b] = ORACLE_ERR_CONTEXT;
+            } else {
+                ctx_inout[b] = nc;
+            }
+        }
+    }
+}
 
 int oracle_num_threads(void) {
 #ifdef _OPENMP

@@ -54,6 +54,8 @@ def _get():
             lib.oracle_attention.argtypes = [i] * 9 + [ctypes.c_double] + [P] * 6 + [i, P, P, i]
             lib.oracle_accept_prefix.restype = None
             lib.oracle_accept_prefix.argtypes = [i, i, i, P, P, P, P, P]
+            lib.oracle_accept_sampled.restype = None
+            lib.oracle_accept_sampled.argtypes = [i, i, i] + [P] * 8
             lib.oracle_argmax.restype = i
             lib.oracle_argmax.argtypes = [P, i]
             lib.oracle_num_threads.restype = i
@@ -148,6 +150,27 @@ def accept_prefix(logits, draft, context_lens=None):
     cl = None if context_lens is None else _i32(context_lens).copy()
     _get().oracle_accept_prefix(B, T, V, _p(lg), _p(dr), _p(acc), _p(nxt), _p(cl))
     return acc, nxt, cl
+
+
+def accept_sampled(q, p, draft, u, context_lens=None):
+    """Speculative sampling (stochastic acceptance).  q [B,T,V] float32 target
+    probabilities, p [B,T-1,V] float32 draft probabilities, draft [B,T-1]
+    int32, u [B,T] float64 uniforms in [0,1).  Returns (accepted [B],
+    next_token [B], context_lens' or None, seq_err [B])."""
+    qa = np.ascontiguousarray(q, dtype=np.float32)
+    B, T, V = qa.shape
+    if not 1 <= T <= 64:
+        raise ValueError("accept_sampled: T must be in [1, 64]")
+    pa = np.ascontiguousarray(p, dtype=np.float32).reshape(B, T - 1, V)
+    dr = _i32(draft).reshape(B, T - 1)
+    ua = np.ascontiguousarray(u, dtype=np.float64).reshape(B, T)
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    err = np.zeros(max(B, 1), np.int32)
+    cl = None if context_lens is None else _i32(context_lens).copy()
+    _get().oracle_accept_sampled(B, T, V, _p(qa), _p(pa), _p(dr), _p(ua), _p(acc), _p(nxt),
+                                 _p(cl), _p(err))
+    return acc, nxt, cl, err[:B]
 
 
 def argmax(row) -> int:
