@@ -10,6 +10,8 @@ CUDA kernels; calling any op without the built library raises.
     append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)
     append_verify_attention(...)  (kv_append fused into the attention launch)
     accept_prefix(target_logits, draft_ids, context_lens=None) -> (accepted, next)
+    accept_sampled(target_probs, draft_probs, draft_ids, uniforms,
+                   context_lens=None) -> (accepted, next)
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ from . import _lib
 from ._lib import GqaError, Shape, Status, status_string  # noqa: F401
 
 __all__ = ["kv_append", "decode_attention", "verify_attention", "append_decode_attention",
-           "append_verify_attention", "accept_prefix",
+           "append_verify_attention", "accept_prefix", "accept_sampled",
            "attention_workspace_size", "GqaError", "Status", "Shape"]
 
 
@@ -140,4 +142,36 @@ def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,
                                       _lib._ptr(context_lens), _status_arg(status),
                                       _lib._stream(stream))
     _lib._check("gqa_accept_prefix", rc)
+    return accepted, next_token
+
+
+def accept_sampled(target_probs, draft_probs, draft_ids, uniforms, context_lens=None, *,
+                   accepted=None, next_token=None, status=None, stream=None):
+    """gqa_accept_sampled.  target_probs fp32 [B,T,V], draft_probs fp32
+    [B,T-1,V], draft_ids int32 [B,T-1], uniforms fp64 [B,T] in [0,1).
+    Returns (accepted [B], next_token [B]); updates context_lens in place if given."""
+    _lib._need(target_probs, "target_probs", torch.float32, 3)
+    B, T, V = target_probs.shape
+    _lib._need(uniforms, "uniforms", torch.float64, 2)
+    if tuple(uniforms.shape) != (B, T):
+        raise ValueError(f"uniforms must be [{B},{T}], got {tuple(uniforms.shape)}")
+    if T > 1:
+        _lib._need(draft_probs, "draft_probs", torch.float32, 3)
+        _lib._need(draft_ids, "draft_ids", torch.int32, 2)
+        if tuple(draft_probs.shape) != (B, T - 1, V) or tuple(draft_ids.shape) != (B, T - 1):
+            raise ValueError("draft_probs must be [B,T-1,V] and draft_ids [B,T-1]")
+    if context_lens is not None:
+        _lib._need(context_lens, "context_lens", torch.int32, 1)
+    dev = target_probs.device
+    if accepted is None:
+        accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=dev)
+    rc = _lib.lib().gqa_accept_sampled(B, T, V, _lib._ptr(target_probs),
+                                       _lib._ptr(draft_probs) if T > 1 else None,
+                                       _lib._ptr(draft_ids) if T > 1 else None,
+                                       _lib._ptr(uniforms), _lib._ptr(accepted),
+                                       _lib._ptr(next_token), _lib._ptr(context_lens),
+                                       _status_arg(status), _lib._stream(stream))
+    _lib._check("gqa_accept_sampled", rc)
     return accepted, next_token

@@ -31,6 +31,7 @@ class Status(enum.IntEnum):
     ERR_CONTEXT = 7
     ERR_BLOCK_ID = 8
     ERR_TIMEOUT = 9
+    ERR_PROBS = 10
 
 
 class GqaError(RuntimeError):
@@ -55,7 +56,7 @@ FLAG_EARLY_KV = 2
 EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_attention_workspace_size", "gqa_workspace_clear", "gqa_decode_attention",
            "gqa_verify_attention", "gqa_append_decode_attention", "gqa_append_verify_attention",
-           "gqa_accept_prefix")
+           "gqa_accept_prefix", "gqa_accept_sampled")
 
 
 def lib() -> ctypes.CDLL:
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
             f.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
         L.gqa_accept_prefix.restype = I
         L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, P]
+        L.gqa_accept_sampled.restype = I
+        L.gqa_accept_sampled.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P]
         _lib = L
         return L
 

@@ -65,6 +65,7 @@ const char* gqa_status_string(int status) {
         case GQA_ERR_CONTEXT: return "context length out of range";
         case GQA_ERR_BLOCK_ID: return "block id out of range";
         case GQA_ERR_TIMEOUT: return "bounded wait inside a kernel timed out";
+        case GQA_ERR_PROBS: return "invalid probability, uniform or empty distribution";
         default: return "unknown status";
     }
 }
@@ -148,6 +149,20 @@ gqa_status gqa_accept_prefix(int B, int T, int V, const float* target_logits,
     return gqa::launch_accept_prefix(B, T, V, target_logits, draft_ids, accepted, next_token,
                                      context_lens_inout, dev_status,
                                      static_cast<cudaStream_t>(stream));
+}
+
+gqa_status gqa_accept_sampled(int B, int T, int V, const float* target_probs,
+                              const float* draft_probs, const int32_t* draft_ids,
+                              const double* uniforms, int32_t* accepted, int32_t* next_token,
+                              int32_t* context_lens_inout, int32_t* dev_status, void* stream) {
+    if (B < 0 || T < 1 || T > 64 || V < 1) return GQA_ERR_SHAPE;
+    if (B == 0) return GQA_OK;
+    if (!target_probs || !uniforms || !accepted || !next_token) return GQA_ERR_NULL;
+    if (T > 1 && (!draft_probs || !draft_ids)) return GQA_ERR_NULL;
+    return gqa::launch_accept_sampled(B, T, V, target_probs, T > 1 ? draft_probs : nullptr,
+                                      T > 1 ? draft_ids : nullptr, uniforms, accepted,
+                                      next_token, context_lens_inout, dev_status,
+                                      static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

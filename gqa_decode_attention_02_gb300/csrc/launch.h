@@ -45,6 +45,11 @@ gqa_status launch_accept_prefix(int B, int T, int V, const float* logits,
                                 int32_t* next_token, int32_t* ctx_io, int32_t* dev_status,
                                 cudaStream_t stream);
 
+gqa_status launch_accept_sampled(int B, int T, int V, const float* q, const float* p,
+                                 const int32_t* draft, const double* u, int32_t* accepted,
+                                 int32_t* next_token, int32_t* ctx_io, int32_t* dev_status,
+                                 cudaStream_t stream);
+
 // Cached per-device SM count (0 on failure).
 int device_sm_count();
 

@@ -10,6 +10,12 @@ Value recipe: every element is drawn as fp32 N(0,1) from a torch.Generator seede
 per workload and rounded (round-to-nearest-even) to the workload dtype.  Unused
 cache slots hold NaN; unused block-table entries hold INT32_MAX.
 
+Inputs of stochastic acceptance (speculative sampling) are probability rows
+drawn from Dirichlet distributions: the target's rows q ~ Dir(alpha) (alpha < 1
+gives the peaked rows of a language model), the draft's rows a mixture of q and
+an independent Dirichlet row, so that drafts and target mostly agree; each draft
+id is drawn from its draft row, and the acceptance uniforms are U[0,1) doubles.
+
 The five named workloads follow the shapes of the pages' own running examples:
 the 24-layer, 14-query-head, 2-KV-head, H=64 fp16 model measured on page "جعل
 inference رخيصًا: KV cache وbatching والتكميم", a Llama-style N=32/K=8/H=128
@@ -229,3 +235,34 @@ def make(name: str, *, device="cpu", seed: Optional[int] = None,
     rng = np.random.default_rng(seed + 7919)
     ctx = context_lengths(kind, s["B"], rng, *args)
     return build(name, ctx=ctx, seed=seed, device=device, desc=desc, **s)
+
+
+@dataclasses.dataclass
+class SamplingInputs:
+    q: torch.Tensor         # fp32 [B,T,V] target probabilities
+    p: torch.Tensor         # fp32 [B,T-1,V] draft probabilities
+    draft: torch.Tensor     # int32 [B,T-1], draft[b,t] drawn from p[b,t]
+    uniforms: torch.Tensor  # fp64 [B,T] in [0,1)
+
+
+def sampling_inputs(B: int, T: int, V: int, seed: int, device="cpu", alpha: float = 0.1,
+                    mix: float = 0.7) -> SamplingInputs:
+    """Seeded inputs for stochastic acceptance: q ~ Dir(alpha) per row, p =
+    mix * q + (1 - mix) * Dir(alpha) per row, both rounded to fp32; drafts
+    drawn from p (in fp64); uniforms U[0,1)."""
+    rng = np.random.default_rng(seed)
+    q64 = rng.dirichlet(np.full(V, alpha), size=(B, T))
+    d64 = rng.dirichlet(np.full(V, alpha), size=(B, max(T - 1, 0)))
+    p64 = mix * q64[:, : T - 1] + (1.0 - mix) * d64
+    draft = np.zeros((B, max(T - 1, 0)), np.int32)
+    for b in range(B):
+        for t in range(T - 1):
+            c = np.cumsum(p64[b, t])
+            draft[b, t] = min(int(np.searchsorted(c, rng.random() * c[-1], side="right")),
+                              V - 1)
+    u = rng.random((B, T))
+    return SamplingInputs(
+        q=torch.as_tensor(q64.astype(np.float32), device=device),
+        p=torch.as_tensor(p64.astype(np.float32).reshape(B, max(T - 1, 0), V), device=device),
+        draft=torch.as_tensor(draft, device=device),
+        uniforms=torch.as_tensor(u, dtype=torch.float64, device=device))

@@ -7,6 +7,8 @@
  *   gqa_decode_attention attention of one new query token per sequence (T == 1)
  *   gqa_verify_attention the same for T >= 1 new tokens, causal among them
  *   gqa_accept_prefix    greedy longest-prefix acceptance of draft tokens
+ *   gqa_accept_sampled   stochastic acceptance of draft tokens (speculative
+ *                        sampling: modified rejection sampling)
  *
  * Sources (web pages, cited by title and section):
  *   "CS336, лекции 10 и 12: инференс и оценка моделей" (CS336 lectures 10/12,
@@ -68,7 +70,9 @@ typedef enum {
     GQA_ERR_CUDA = 6,      /* a CUDA runtime / driver call failed */
     GQA_ERR_CONTEXT = 7,   /* device: context_lens[b] < T, < 1 or > capacity */
     GQA_ERR_BLOCK_ID = 8,  /* device: a block-table entry in use not in [0,num_blocks) */
-    GQA_ERR_TIMEOUT = 9    /* device: a bounded wait inside a kernel gave up */
+    GQA_ERR_TIMEOUT = 9,   /* device: a bounded wait inside a kernel gave up */
+    GQA_ERR_PROBS = 10     /* device: an entry read is not a probability in [0,1], a
+                              uniform is not in [0,1), or a row has no weight */
 } gqa_status;
 
 typedef enum { GQA_F16 = 0, GQA_BF16 = 1 } gqa_dtype;
@@ -242,6 +246,44 @@ gqa_status gqa_accept_prefix(int B, int T, int V, const float *target_logits,
                              const int32_t *draft_ids, int32_t *accepted,
                              int32_t *next_token, int32_t *context_lens_inout,
                              int32_t *dev_status, void *stream);
+
+/* Stochastic acceptance (speculative sampling).  CS336 lecture 10
+ * §"Спекулятивное сэмплирование": modified rejection sampling with the draft
+ * model p as proposal and the target model q as target; draft token x is kept
+ * with probability min(1, q(x)/p(x)), the first rejection is replaced by a draw
+ * from max(q - p, 0) renormalised, and when every draft is kept one more token
+ * is drawn from the target's last distribution.  The emitted tokens are then
+ * exact samples of q (the page's two-token proof).
+ *   target_probs  fp32 [B][T][V]   q_t: target's distribution for the token
+ *                                  after the prefix and drafts 0..t-1
+ *   draft_probs   fp32 [B][T-1][V] p_t: the distribution draft_ids[b][t] was
+ *                                  drawn from (NULL allowed when T == 1)
+ *   draft_ids     int32 [B][T-1]   (NULL allowed when T == 1)
+ *   uniforms      fp64 [B][T] in [0,1): uniforms[b][t], t < T-1, decides draft
+ *                 t; uniforms[b][T-1] draws the final token.  The caller draws
+ *                 them (any generator); the call itself is deterministic.
+ *   accepted[b]   = a, the number of drafts kept (a run from the start)
+ *   next_token[b] = the token drawn at position a
+ *   context_lens_inout[b] -= T-1-a  (if not NULL, as in gqa_accept_prefix)
+ * Arithmetic, identical on every device and in any thread order:
+ *   - draft t is kept iff u * p_t(x) < q_t(x), u and both probabilities widened
+ *     to double (the product is exact); an id outside [0, V) is rejected;
+ *   - a draw from weights w_v is the inverse CDF on W_v = floor(w_v * 2^40)
+ *     (integers): S = sum_v W_v, r = min(floor(u * S), S-1) in double, token =
+ *     least v with W_0 + ... + W_v > r; the residual weight is max(q - p, 0)
+ *     with the difference rounded once to fp32; a residual with S == 0 falls
+ *     back to q itself.
+ * Requires B >= 0, 1 <= T <= 64, V >= 1; no alignment (16-byte aligned rows
+ * with V % 4 == 0 are read with 16-byte loads).  Device errors: an entry read
+ * that is NaN, < 0 or > 1 counts as 0, and a uniform outside [0,1) as 0
+ * (GQA_ERR_PROBS); a row with no weight gives token 0 (GQA_ERR_PROBS); a
+ * context length that would drop below zero is left unchanged
+ * (GQA_ERR_CONTEXT). */
+gqa_status gqa_accept_sampled(int B, int T, int V, const float *target_probs,
+                              const float *draft_probs, const int32_t *draft_ids,
+                              const double *uniforms, int32_t *accepted,
+                              int32_t *next_token, int32_t *context_lens_inout,
+                              int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }
