@@ -53,6 +53,10 @@ def parse_args():
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--accept", default="greedy", choices=["greedy", "sampled"],
+                    help="acceptance step of a verify workload: greedy longest prefix over "
+                         "logits, or stochastic acceptance (speculative sampling) over "
+                         "probabilities")
     ap.add_argument("--unfused", action="store_true",
                     help="separate kv_append launches instead of the append fused into "
                          "the attention launch")
@@ -269,10 +273,15 @@ def run_ours(args, world, rank, local):
     outs = [torch.empty_like(q) for q in w.q]
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     has_acc = w.logits is not None
+    sampled = has_acc and args.accept == "sampled"
     if has_acc:
         ctx_scratch = w.context_lens.clone()
         acc_out = torch.empty(w.B, dtype=torch.int32, device=dev)
         nxt_out = torch.empty(w.B, dtype=torch.int32, device=dev)
+        V = w.logits.shape[-1]
+    if sampled:
+        sin = workloads.sampling_inputs(w.B, w.T, V, seed=workloads.SPECS[args.workload]["seed"]
+                                        + 1000, device=dev)
 
     def do_append():
         if w.appended and not fused:
@@ -294,7 +303,10 @@ def run_ours(args, world, rank, local):
                         out=outs[l], workspace=ws, status=st, pdl=True, early_kv=True)
 
     def do_acc():
-        if has_acc:
+        if sampled:
+            gq.accept_sampled(sin.q, sin.p, sin.draft, sin.uniforms, ctx_scratch,
+                              accepted=acc_out, next_token=nxt_out, status=st)
+        elif has_acc:
             gq.accept_prefix(w.logits, w.draft, ctx_scratch, accepted=acc_out,
                              next_token=nxt_out, status=st)
 
@@ -365,6 +377,10 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {int(st.item())} in the timed region")
 
     attn_b, app_b, acc_b = step_bytes(w)
+    if sampled:
+        from gqa_decode_attention_02_gb300 import analytic as A
+
+        acc_b = A.accept_sampled_bytes(acc_out.cpu().numpy(), w.T, V)
     bytes_step = L * (attn_b + app_b) + acc_b
     step_ms_max, value = combine_ranks(step_ms, bytes_step, world, dev)
     peak, peak_src = measured_peak()
@@ -382,9 +398,15 @@ def run_ours(args, world, rank, local):
         h_meta = [w.block_tables.cpu().pin_memory(), w.context_lens.cpu().pin_memory()]
         d_meta = [w.block_tables, w.context_lens]
         h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+        if sampled:
+            for t in (sin.q, sin.p, sin.draft, sin.uniforms):
+                h_in.append(t.cpu().pin_memory())
+                d_in.append(t)
+        elif has_acc:
+            for t in (w.logits, w.draft):
+                h_in.append(t.cpu().pin_memory())
+                d_in.append(t)
         if has_acc:
-            h_in.append(w.logits.cpu().pin_memory())
-            d_in.append(w.logits)
             h_acc = [torch.empty(w.B, dtype=torch.int32).pin_memory() for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in h_in + h_meta)
         d2h = sum(t.numel() * t.element_size() for t in h_out) + (8 * w.B if has_acc else 0)
@@ -455,6 +477,10 @@ def run_ours(args, world, rank, local):
             "B": w.B, "T": w.T, "N": w.N, "K": w.K, "H": w.H, "layers": L,
             "block_size": w.block_size, "sum_context_tokens": int(ctx.sum()),
             "l2": "flushed between steps (256 MiB read outside the step events)",
+            "accept": ("none" if not has_acc else
+                       "stochastic (speculative sampling) over fp32 probabilities [B,T,V] and "
+                       "[B,T-1,V], seeded Dirichlet rows" if sampled else
+                       "greedy longest prefix over fp32 logits [B,T,V]"),
             "append": ("fused into the attention launch" if fused else
                        "separate kv_append launches" if w.appended else "none"),
             "parallelism": f"replicas x{world}",

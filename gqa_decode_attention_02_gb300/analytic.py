@@ -89,6 +89,21 @@ def accept_bytes(B: int, T: int, V: int) -> int:
     return B * T * V * 4 + B * max(T - 1, 0) * 4 + 3 * 4 * B
 
 
+def accept_sampled_bytes(accepted, T: int, V: int) -> int:
+    """Bytes stochastic acceptance must move, given the accepted counts: per
+    sequence the T fp64 uniforms and T-1 draft ids, q(x) and p(x) of every draft
+    test reached (min(a+1, T-1) of them), the row(s) of the final draw (q and p
+    after a rejection, q alone after a full run), and accepted / next token /
+    length (read and written)."""
+    tot = 0
+    for a in accepted:
+        a = int(a)
+        tests = min(a + 1, T - 1)
+        rows = 2 if a < T - 1 else 1
+        tot += 8 * T + 4 * (T - 1) + 8 * tests + rows * V * 4 + 4 * 4
+    return tot
+
+
 def spec_expected_tokens(alpha: float, gamma: int) -> float:
     """Expected tokens kept per verify pass with per-token acceptance alpha and
     gamma drafts (geometric run plus the target's own token).  The formula is

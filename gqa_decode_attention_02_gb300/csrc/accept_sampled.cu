@@ -9,15 +9,17 @@
 // drawn from the target's last distribution.  The emitted tokens are exact
 // samples of q.
 //
-// One block of 1024 threads per sequence:
-//   1. threads t < T evaluate every draft test at once (u * p(x) < q(x) in
-//      double, an exact product) and the block takes the first rejection a;
-//   2. each warp sums the integer weights W_v = floor(w_v * 2^40) of its
-//      contiguous column segment of the row to draw from (16-byte loads when
-//      rows are 16-byte aligned);
-//   3. warp 0 scans the 32 segment sums, picks r = floor(u * S) and the
-//      segment that holds the crossing; that warp re-reads its segment (now in
-//      cache) and finds the least v with W_0 + ... + W_v > r.
+// One thread-block cluster of CS <= 8 blocks per sequence; block k owns column
+// slice k of the vocabulary and each of its threads a contiguous run of it:
+//   1. every block evaluates the draft tests (u * p(x) < q(x) in double, an
+//      exact product; a handful of loads) and takes the first rejection a;
+//   2. each thread sums the integer weights W_v = floor(w_v * 2^40) of its run
+//      of the row to draw from; the block reduces them to its slice total and
+//      writes it into every block of the cluster (distributed shared memory);
+//   3. after one cluster barrier every block knows S = sum of the slice totals,
+//      r = floor(u * S) and the slice holding the crossing; that block scans
+//      its thread sums and the thread whose run holds it finds the least v
+//      with W_0 + ... + W_v > r.
 // The weights are exact integers, so the sums do not depend on their order and
 // the drawn index is the same whatever the thread layout.
 #include <cuda_runtime.h>
@@ -28,10 +30,11 @@
 namespace gqa {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxT = 64;
-constexpr int kGroup = 4;  // chunks of one warp whose loads are in flight together
+constexpr int kMaxCluster = 8;
+constexpr int kVecInFlight = 4;  // 16-byte loads of a run issued together
 
 // floor(w * 2^40) for w in [0, 1], from the bits (exact; w <= 0 gives 0)
 __device__ __forceinline__ unsigned long long fixed40(float w) {
@@ -53,21 +56,14 @@ __device__ __forceinline__ float clean_prob(float x, bool& bad) {
 }
 
 // Weight of one column: the residual max(q - p, 0) (difference rounded once
-// to fp32) when the draft row is given, else q itself.
-template <bool kResid>
-__device__ __forceinline__ unsigned long long weight(float qv, float pv, bool& bad) {
+// to fp32) when the draft row is used, else q itself.
+__device__ __forceinline__ unsigned long long weight(float qv, float pv, bool resid, bool& bad) {
     float w = clean_prob(qv, bad);
-    if (kResid) {
+    if (resid) {
         const float d = __fsub_rn(w, clean_prob(pv, bad));
         w = d > 0.f ? d : 0.f;
     }
     return fixed40(w);
-}
-
-__device__ __forceinline__ unsigned long long warp_sum(unsigned long long x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
 }
 
 __device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long x, int lane) {
@@ -79,106 +75,84 @@ __device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long 
     return x;
 }
 
-// Column layout of one warp's segment [lo, hi): chunk k covers kW*32 columns
-// starting at lo + k*kW*32; lane l takes kW consecutive columns of the chunk.
-// kW = 4 with 16-byte loads, 1 with scalar loads.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_u64(const void* local, uint32_t rank,
+                                               unsigned long long v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Sum of the weights of columns [c, e) (e - c <= run length).  With kVec, c
+// and e are multiples of 4 and the rows 16-byte aligned.
 template <bool kVec>
-struct Seg {
-    static constexpr int kW = kVec ? 4 : 1;
-    static constexpr int kChunk = 32 * kW;
-
-    // lane's kW values of chunk starting at c (columns >= hi read as 0 weight)
-    template <bool kResid>
-    __device__ static void weights(const float* qrow, const float* prow, int c, int hi,
-                                   unsigned long long (&w)[kW], bool& bad) {
-        if (kVec) {
-            float4 qv = make_float4(0.f, 0.f, 0.f, 0.f), pv = qv;
-            if (c < hi) {  // hi is a multiple of 4 here
-                qv = __ldg(reinterpret_cast<const float4*>(qrow + c));
-                if (kResid) pv = __ldg(reinterpret_cast<const float4*>(prow + c));
-            }
-            const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
-            const float pa[4] = {pv.x, pv.y, pv.z, pv.w};
+__device__ __forceinline__ unsigned long long run_sum(const float* qrow, const float* prow,
+                                                      bool resid, int c, int e, bool& bad) {
+    unsigned long long s = 0ull;
+    if (kVec) {
+        for (; c < e; c += 4 * kVecInFlight) {
+            float4 qv[kVecInFlight], pv[kVecInFlight];
 #pragma unroll
-            for (int e = 0; e < kW; ++e)
-                w[e] = (c < hi) ? weight<kResid>(qa[e], pa[e], bad) : 0ull;
-        } else {
-            w[0] = 0ull;
-            if (c < hi) w[0] = weight<kResid>(__ldg(qrow + c), kResid ? __ldg(prow + c) : 0.f, bad);
-        }
-    }
-
-    // Sum of the segment's weights (every lane gets it).
-    template <bool kResid>
-    __device__ static unsigned long long sum(const float* qrow, const float* prow, int lo,
-                                             int hi, int lane, bool& bad) {
-        unsigned long long s = 0ull;
-        for (int c0 = lo; c0 < hi; c0 += kGroup * kChunk) {
-            unsigned long long w[kGroup][kW];
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g)
-                weights<kResid>(qrow, prow, c0 + g * kChunk + lane * kW, hi, w[g], bad);
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g)
-#pragma unroll
-                for (int e = 0; e < kW; ++e) s += w[g][e];
-        }
-        return warp_sum(s);
-    }
-
-    // Least column v of the segment with base + W_lo + ... + W_v > r (the
-    // caller guarantees that the segment holds it).  Returns -1 if not found.
-    template <bool kResid>
-    __device__ static int find(const float* qrow, const float* prow, int lo, int hi, int lane,
-                               unsigned long long base, unsigned long long r) {
-        bool bad = false;  // already recorded by the sum pass
-        for (int c = lo; c < hi; c += kChunk) {
-            unsigned long long w[kW];
-            weights<kResid>(qrow, prow, c + lane * kW, hi, w, bad);
-            unsigned long long ls = 0ull;
-#pragma unroll
-            for (int e = 0; e < kW; ++e) ls += w[e];
-            const unsigned long long incl = warp_incl_scan(ls, lane);
-            const unsigned long long tot = __shfl_sync(0xffffffffu, incl, 31);
-            const unsigned hit = __ballot_sync(0xffffffffu, base + incl > r);
-            if (hit) {
-                const int l = __ffs(hit) - 1;
-                int v = -1;
-                if (lane == l) {
-                    unsigned long long cum = base + incl - ls;
-#pragma unroll
-                    for (int e = 0; e < kW; ++e) {
-                        cum += w[e];
-                        if (v < 0 && cum > r) v = c + lane * kW + e;
-                    }
+            for (int i = 0; i < kVecInFlight; ++i) {
+                qv[i] = pv[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c + 4 * i < e) {
+                    qv[i] = __ldg(reinterpret_cast<const float4*>(qrow + c + 4 * i));
+                    if (resid) pv[i] = __ldg(reinterpret_cast<const float4*>(prow + c + 4 * i));
                 }
-                return __shfl_sync(0xffffffffu, v, l);
             }
-            base += tot;
+#pragma unroll
+            for (int i = 0; i < kVecInFlight; ++i) {
+                if (c + 4 * i < e) {
+                    s += weight(qv[i].x, pv[i].x, resid, bad);
+                    s += weight(qv[i].y, pv[i].y, resid, bad);
+                    s += weight(qv[i].z, pv[i].z, resid, bad);
+                    s += weight(qv[i].w, pv[i].w, resid, bad);
+                }
+            }
         }
-        return -1;
+    } else {
+        for (; c < e; ++c)
+            s += weight(__ldg(qrow + c), resid ? __ldg(prow + c) : 0.f, resid, bad);
     }
-};
+    return s;
+}
 
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
     accept_sampled_kernel(const float* __restrict__ q, const float* __restrict__ p,
                           const int32_t* __restrict__ draft, const double* __restrict__ u,
                           int32_t* accepted, int32_t* next_token, int32_t* ctx_io,
-                          int32_t* status, int T, int V) {
-    using S = Seg<kVec>;
+                          int32_t* status, int T, int V, int cs) {
+    // slice totals of every block of the cluster, one table per draw attempt
+    __shared__ unsigned long long s_tot[2][kMaxCluster];
+    __shared__ unsigned long long s_warp[kWarps];
     __shared__ int s_first;
     __shared__ int s_bad;
     __shared__ unsigned char s_tbad[kMaxT];
     __shared__ double s_ufin;
-    __shared__ unsigned long long s_wsum[kWarps];
-    __shared__ int s_wstar, s_resid, s_tok;
-    __shared__ unsigned long long s_base, s_r;
 
     griddep_launch_dependents();
     griddep_wait();  // the probabilities come from the previous kernels
-    const int b = blockIdx.x;
+    const uint32_t rank = cluster_rank();
+    const int b = blockIdx.x / cs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // Remote stores into a block may start only once it runs: arrive now, wait
+    // before the first one.
+    cluster_arrive();
     if (tid == 0) {
         s_first = T - 1;
         s_bad = 0;
@@ -206,88 +180,103 @@ __global__ void __launch_bounds__(kThreads)
             s_ufin = ut;
         }
         s_tbad[tid] = bad_t ? 1 : 0;  // counts only if this test was reached
-        if (bad_u) s_bad = 1;
+        if (bad_u && rank == 0) s_bad = 1;
     }
     __syncthreads();
     const int a = s_first;
-    if (tid == 0) {
+    if (tid == 0 && rank == 0)
         for (int t = 0; t <= a && t < T - 1; ++t)
             if (s_tbad[t]) s_bad = 1;
-        s_resid = (a < T - 1) ? 1 : 0;
-    }
-    __syncthreads();
 
     // ---- 2./3. draw from the residual (or q), falling back to q once -----
     const float* qrow = q + ((size_t)b * T + a) * V;
     const float* prow = (a < T - 1) ? p + ((size_t)b * (T - 1) + a) * V : nullptr;
-    const int seg = ((((V + kWarps - 1) / kWarps) + 3) / 4) * 4;
-    const int lo = min(V, warp * seg), hi = min(V, lo + seg);
-    int tok = -1;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        const bool resid = s_resid != 0;  // block-uniform
+    const int slice = ((((V + cs - 1) / cs) + 3) / 4) * 4;
+    const int c_lo = min(V, (int)rank * slice), c_hi = min(V, c_lo + slice);
+    int run = (c_hi - c_lo + kThreads - 1) / kThreads;
+    if (kVec) run = ((run + 3) / 4) * 4;
+    const int r_lo = min(c_hi, c_lo + tid * run), r_hi = min(c_hi, r_lo + run);
+    bool resid = prow != nullptr;
+    bool empty = false;
+    for (int attempt = 0; attempt < 2; ++attempt) {  // block- and cluster-uniform
         bool bad = false;
-        const unsigned long long ws = resid ? S::template sum<true>(qrow, prow, lo, hi, lane, bad)
-                                            : S::template sum<false>(qrow, prow, lo, hi, lane, bad);
-        if (lane == 0) s_wsum[warp] = ws;
+        const unsigned long long mine = run_sum<kVec>(qrow, prow, resid, r_lo, r_hi, bad);
         if (bad) s_bad = 1;
+        // block scan of the thread sums (thread order is column order)
+        const unsigned long long incl = warp_incl_scan(mine, lane);
+        if (lane == 31) s_warp[warp] = incl;
         __syncthreads();
+        unsigned long long slice_tot = 0ull;
         if (warp == 0) {
-            const unsigned long long x = s_wsum[lane];
-            const unsigned long long incl = warp_incl_scan(x, lane);
-            const unsigned long long tot = __shfl_sync(0xffffffffu, incl, 31);
-            if (tot == 0ull) {
-                if (lane == 0) {
-                    s_wstar = -1;
-                    if (resid)
-                        s_resid = 0;  // vanishing residual: draw from q instead
-                    else
-                        s_bad = 1;    // nothing to draw from at all
-                }
-            } else {
-                unsigned long long r = (unsigned long long)__double2ull_rz(
-                    __dmul_rn(s_ufin, __ull2double_rn(tot)));
-                if (r > tot - 1ull) r = tot - 1ull;
-                const unsigned hit = __ballot_sync(0xffffffffu, incl > r);
-                const int l = __ffs(hit) - 1;
-                if (lane == l) {
-                    s_wstar = l;
-                    s_base = incl - x;
-                    s_r = r;
-                }
-            }
+            const unsigned long long x = lane < kWarps ? s_warp[lane] : 0ull;
+            const unsigned long long wi = warp_incl_scan(x, lane);
+            slice_tot = __shfl_sync(0xffffffffu, wi, kWarps - 1);
+            if (lane < kWarps) s_warp[lane] = wi - x;  // exclusive prefix of each warp
         }
-        __syncthreads();
-        const int wstar = s_wstar;
-        if (wstar >= 0) {
-            if (warp == wstar) {
-                const int v = resid ? S::template find<true>(qrow, prow, lo, hi, lane, s_base, s_r)
-                                    : S::template find<false>(qrow, prow, lo, hi, lane, s_base, s_r);
-                if (lane == 0) s_tok = v;
+        if (attempt == 0) cluster_wait();  // every block of the cluster is running
+        if (warp == 0 && lane < cs) st_cluster_u64(&s_tot[attempt][rank], lane, slice_tot);
+        cluster_arrive();
+        cluster_wait();  // every slice total is in every block
+        unsigned long long S = 0ull;
+        for (int k = 0; k < cs; ++k) S += s_tot[attempt][k];
+        if (S == 0ull) {
+            if (resid) {  // vanishing residual: draw from q instead
+                resid = false;
+                continue;
             }
-            __syncthreads();
-            tok = s_tok;
+            empty = true;  // nothing to draw from at all
             break;
         }
-        if (!resid || s_resid != 0) break;  // nothing left to try
-        __syncthreads();  // every thread has read s_resid before the next round
+        unsigned long long r = __double2ull_rz(__dmul_rn(s_ufin, __ull2double_rn(S)));
+        if (r > S - 1ull) r = S - 1ull;
+        unsigned long long base = 0ull;
+        int kstar = cs - 1;
+        for (int k = 0; k < cs; ++k) {
+            const unsigned long long t = s_tot[attempt][k];
+            if (base + t > r) {
+                kstar = k;
+                break;
+            }
+            base += t;
+        }
+        if ((int)rank == kstar) {
+            const unsigned long long rr = r - base;  // offset inside this slice
+            const unsigned long long ex = s_warp[warp] + (incl - mine);
+            if (mine > 0ull && ex <= rr && rr < ex + mine) {  // exactly one thread
+                unsigned long long cum = ex;
+                int tok = r_hi - 1;
+                bool dummy = false;
+                for (int c = r_lo; c < r_hi; ++c) {
+                    cum += weight(__ldg(qrow + c), resid ? __ldg(prow + c) : 0.f, resid, dummy);
+                    if (cum > rr) {
+                        tok = c;
+                        break;
+                    }
+                }
+                next_token[b] = tok;
+            }
+        }
+        break;
     }
 
+    __syncthreads();
     if (tid == 0) {
-        int bad = s_bad;
-        if (tok < 0) {
-            tok = 0;
-            bad = 1;
+        bool bad = s_bad != 0;
+        if (rank == 0) {
+            if (empty) {
+                next_token[b] = 0;
+                bad = true;
+            }
+            accepted[b] = a;
+            if (ctx_io) {
+                const int nc = ctx_io[b] - (T - 1 - a);
+                if (nc < 0)
+                    report(status, GQA_ERR_CONTEXT);
+                else
+                    ctx_io[b] = nc;
+            }
         }
-        accepted[b] = a;
-        next_token[b] = tok;
         if (bad) report(status, GQA_ERR_PROBS);
-        if (ctx_io) {
-            const int nc = ctx_io[b] - (T - 1 - a);
-            if (nc < 0)
-                report(status, GQA_ERR_CONTEXT);
-            else
-                ctx_io[b] = nc;
-        }
     }
 }
 
@@ -300,21 +289,29 @@ gqa_status launch_accept_sampled(int B, int T, int V, const float* q, const floa
     // 16-byte loads need every row of q and p to start on a 16-byte boundary
     const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(q) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+    // one cluster of up to 8 blocks per sequence, about 8 columns per thread
+    int cs = (int)((V + kThreads * 8 - 1) / (kThreads * 8));
+    if (cs > kMaxCluster) cs = kMaxCluster;
+    if (cs < 1) cs = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(B, 1, 1);
+    cfg.gridDim = dim3((unsigned)(cs * B), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e =
         vec ? cudaLaunchKernelEx(&cfg, accept_sampled_kernel<true>, q, p, draft, u, accepted,
-                                 next_token, ctx_io, dev_status, T, V)
+                                 next_token, ctx_io, dev_status, T, V, cs)
             : cudaLaunchKernelEx(&cfg, accept_sampled_kernel<false>, q, p, draft, u, accepted,
-                                 next_token, ctx_io, dev_status, T, V);
+                                 next_token, ctx_io, dev_status, T, V, cs);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -155,7 +155,7 @@ gqa_status gqa_accept_sampled(int B, int T, int V, const float* target_probs,
                               const float* draft_probs, const int32_t* draft_ids,
                               const double* uniforms, int32_t* accepted, int32_t* next_token,
                               int32_t* context_lens_inout, int32_t* dev_status, void* stream) {
-    if (B < 0 || T < 1 || T > 64 || V < 1) return GQA_ERR_SHAPE;
+    if (B < 0 || T < 1 || T > 64 || V < 1 || B > (1 << 28)) return GQA_ERR_SHAPE;
     if (B == 0) return GQA_OK;
     if (!target_probs || !uniforms || !accepted || !next_token) return GQA_ERR_NULL;
     if (T > 1 && (!draft_probs || !draft_ids)) return GQA_ERR_NULL;

@@ -273,8 +273,8 @@ gqa_status gqa_accept_prefix(int B, int T, int V, const float *target_logits,
  *     least v with W_0 + ... + W_v > r; the residual weight is max(q - p, 0)
  *     with the difference rounded once to fp32; a residual with S == 0 falls
  *     back to q itself.
- * Requires B >= 0, 1 <= T <= 64, V >= 1; no alignment (16-byte aligned rows
- * with V % 4 == 0 are read with 16-byte loads).  Device errors: an entry read
+ * Requires 0 <= B <= 2^28, 1 <= T <= 64, V >= 1; no alignment (16-byte aligned
+ * rows with V % 4 == 0 are read with 16-byte loads).  Device errors: an entry read
  * that is NaN, < 0 or > 1 counts as 0, and a uniform outside [0,1) as 0
  * (GQA_ERR_PROBS); a row with no weight gives token 0 (GQA_ERR_PROBS); a
  * context length that would drop below zero is left unchanged

@@ -92,3 +92,16 @@ def test_algorithmic_bytes_config_1():
     b = A.attention_algorithmic_bytes([295], T=1, N=14, K=2, H=64, elem_bytes=2)
     assert 295 * 2 * 64 * 2 == 75520
     assert b == 2 * 75520 + 2 * 14 * 64 * 2 + 4 * 19 + 4
+
+
+def test_accept_sampled_bytes_by_hand():
+    # T=5 (4 drafts), V=1000.  a=0: one test, a residual draw over q and p;
+    # a=4: four tests, a draw over q alone.
+    T, V = 5, 1000
+    per_seq_fixed = 8 * 5 + 4 * 4 + 16
+    assert A.accept_sampled_bytes([0], T, V) == per_seq_fixed + 8 * 1 + 2 * 4000
+    assert A.accept_sampled_bytes([4], T, V) == per_seq_fixed + 8 * 4 + 1 * 4000
+    assert A.accept_sampled_bytes([0, 4], T, V) == (A.accept_sampled_bytes([0], T, V)
+                                                    + A.accept_sampled_bytes([4], T, V))
+    # T=1: no drafts, one uniform, a draw over q
+    assert A.accept_sampled_bytes([0], 1, V) == 8 + 16 + 4000
