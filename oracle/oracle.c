@@ -11,6 +11,7 @@
  *   [CS336-RU]  "CS336, лекции 10 и 12: инференс и оценка моделей"
  *   [KV-AR]     "جعل inference رخيصًا: KV cache وbatching والتكميم"
  *   [SONAR-KK]  "Болжау арқылы Sonar модельдерін жылдамдату"
+ *   [CS336-ZH]  "Stanford CS336 Day 13 - Inference"
  *
  * Everything is written from the plain definitions, in fp64, one output element
  * at a time; there is no tiling, no online softmax and no split of the context.
@@ -112,16 +113,26 @@ int oracle_kv_append(int B, int T, int K, int H, int block_size, int num_blocks,
  * (1/sqrt(H) unless given); query token t of the T new ones sees every cached
  * position j <= ctx - T + t (full prefix, causal among the new tokens).
  *
+ * Local (sliding-window) attention, [CS336-RU] §"Уменьшаем KV-кэш" (local
+ * attention: attend only to a recent stretch of the context, the KV cache no
+ * longer grows with the sequence) and [CS336-ZH] §"Local Attention" (only
+ * the last k tokens are attended; tokens that leave the window can be dropped
+ * from the cache): with window > 0, query token t sees only positions
+ * last-window < j <= last, last = ctx - T + t --
+ * our reading of "the last k tokens" is the window tokens ending at the query
+ * itself.  window == 0 is full attention.  Only the blocks holding a visible
+ * position are looked up (blocks wholly below every window may be freed).
+ *
  * For each listed sequence b = b_list[i] (all b when b_list is NULL) writes
  * out[i][t][n][h] in fp64.  A sequence with a bad context length or a bad
  * block id gets an all-zero output and a nonzero seq_err[i]. */
 int oracle_attention(int B, int T, int N, int K, int H, int block_size,
                      int num_blocks, int max_blocks, int dtype, double scale,
-                     const uint16_t *q, const uint16_t *k_cache,
+                     int window, const uint16_t *q, const uint16_t *k_cache,
                      const uint16_t *v_cache, const int32_t *block_tables,
                      const int32_t *context_lens, const int32_t *b_list, int nb,
                      double *out, int32_t *seq_err, int nthreads) {
-    if (K <= 0 || N % K != 0) return -1;
+    if (K <= 0 || N % K != 0 || window < 0) return -1;
     int G = N / K;
     if (!b_list) nb = B;
     if (scale <= 0) scale = 1.0 / sqrt((double)H);
@@ -136,7 +147,9 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
             bad[i] = ORACLE_ERR_CONTEXT;
         } else {
             int nblk = (ctx + block_size - 1) / block_size;
-            for (int j = 0; j < nblk; ++j) {
+            int lo = window > 0 ? ctx - T - window + 1 : 0; /* first visible position */
+            if (lo < 0) lo = 0;
+            for (int j = lo / block_size; j < nblk; ++j) {
                 int blk = block_tables[(size_t)b * max_blocks + j];
                 if (blk < 0 || blk >= num_blocks) {
                     bad[i] = ORACLE_ERR_BLOCK_ID;
@@ -165,6 +178,8 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
         }
         int ctx = context_lens[b];
         int last = ctx - T + t; /* last visible position for query token t */
+        int first = 0;          /* first visible position */
+        if (window > 0 && last - window + 1 > 0) first = last - window + 1;
         int kh = n / G;
         const uint16_t *qv = q + (((size_t)b * T + t) * N + n) * H;
         double *s = (double *)malloc(sizeof(double) * (size_t)(last + 1));
@@ -172,7 +187,7 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
         for (int h = 0; h < H; ++h) qd[h] = widen(qv[h], dtype);
         /* scores s_j = scale * <q, k_j> */
         double smax = -INFINITY;
-        for (int j = 0; j <= last; ++j) {
+        for (int j = first; j <= last; ++j) {
             int blk = block_tables[(size_t)b * max_blocks + j / block_size];
             const uint16_t *kr =
                 k_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;
@@ -183,12 +198,12 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
         }
         /* softmax weights p_j = exp(s_j - max) / sum, then out = sum_j p_j v_j */
         double denom = 0.0;
-        for (int j = 0; j <= last; ++j) {
+        for (int j = first; j <= last; ++j) {
             s[j] = exp(s[j] - smax);
             denom += s[j];
         }
         for (int h = 0; h < H; ++h) o[h] = 0.0;
-        for (int j = 0; j <= last; ++j) {
+        for (int j = first; j <= last; ++j) {
             int blk = block_tables[(size_t)b * max_blocks + j / block_size];
             const uint16_t *vr =
                 v_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;

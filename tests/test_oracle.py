@@ -296,3 +296,105 @@ def test_accept_prefix_single_token_and_planted_drafts():
                                         np.zeros((6, 0), np.int32))
     assert (one == 0).all()
     assert list(nxt1) == [int(np.argmax(lg[b, 0])) for b in range(6)]
+
+
+# ---- local (sliding-window) attention ------------------------------------------
+@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("W", [1, 5, 16, 23])
+def test_window_equal_keys_average_the_window(T, W):
+    # Equal keys -> uniform weights over the visible band; v_j = j makes query
+    # token t (position last = ctx - T + t) return the mean of
+    # max(0, last - W + 1) .. last.  Pins both ends of the band.
+    ctx = (T, 16 + T, 37, 64)
+    w = small(B=4, T=T, N=4, K=2, H=64, ctx=ctx, seed=31)
+    key = torch.randn(2, 64, generator=torch.Generator().manual_seed(9))
+    for b, c in enumerate(ctx):
+        for pos in range(c):
+            set_token(w, b, pos, k=key, v=torch.full((2, 64), float(pos)))
+    out, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                                w.context_lens, "f16", window=W)
+    assert (err == 0).all()
+    for b, c in enumerate(ctx):
+        for t in range(T):
+            last = c - T + t
+            first = max(0, last - W + 1)
+            np.testing.assert_allclose(out[b, t], (first + last) / 2.0, rtol=1e-12, atol=1e-12)
+
+
+def test_window_of_one_returns_the_own_v_row():
+    ctx = (9, 40)
+    w = small(B=2, T=3, N=4, K=2, H=64, ctx=ctx, seed=32)
+    out, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "f16", window=1)
+    for b, c in enumerate(ctx):
+        for t in range(3):
+            blk, r = slot(w, b, c - 3 + t)
+            for n in range(4):
+                np.testing.assert_array_equal(out[b, t, n], w.v_cache[0][blk, r, n // 2].double())
+
+
+def test_window_wider_than_context_is_full_attention():
+    ctx = (5, 17, 40)
+    w = small(B=3, T=2, N=4, K=2, H=64, ctx=ctx, seed=33)
+    full, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                               w.context_lens, "f16")
+    win, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "f16", window=41)
+    np.testing.assert_array_equal(win, full)
+
+
+@pytest.mark.parametrize("W,T", [(7, 1), (16, 2), (33, 4)])
+def test_window_paged_equals_banded_recompute(W, T):
+    ctx = (T, 30, 77)
+    w = small(B=3, T=T, N=6, K=2, H=64, dtype="bf16", ctx=ctx, seed=34)
+    out, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "bf16", window=W)
+    gen = torch.Generator().manual_seed(12)
+    for b, c in enumerate(ctx):
+        kk, vv = unpage(w, b, c)
+        q_all = torch.randn(c, 6, 64, generator=gen).to(w.torch_dtype).double().numpy()
+        q_all[c - T:] = w.q[0][b].double().numpy()
+        full = oracle.causal_attention_full(q_all, kk, vv, 1.0 / 8.0, window=W)
+        np.testing.assert_allclose(out[b], full[c - T:], rtol=0, atol=1e-12)
+
+
+def test_tokens_outside_the_window_do_not_matter_and_freed_blocks_are_not_read():
+    # Poison every position below the first window (NaN K and V) and free the
+    # blocks that hold no visible position (INT32_MAX in the table): the output
+    # stays finite and equal.  A band one token too wide would read a NaN.
+    T, W = 2, 20
+    ctx = (50, 64, 21)
+    w = small(B=3, T=T, N=4, K=2, H=64, ctx=ctx, seed=35)
+    ref, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "f16", window=W)
+    nan = torch.full((2, 64), float("nan"))
+    tables = w.block_tables.clone()
+    for b, c in enumerate(ctx):
+        first = max(0, c - T - W + 1)
+        for pos in range(first):
+            set_token(w, b, pos, k=nan, v=nan)
+        tables[b, : first // 16] = 2**31 - 1
+    out, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], tables, w.context_lens,
+                                "f16", window=W)
+    assert (err == 0).all()
+    np.testing.assert_array_equal(out, ref)
+    # the first visible position does matter
+    b, c = 0, ctx[0]
+    set_token(w, b, c - T - W + 1, v=nan)
+    out2, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], tables, w.context_lens,
+                               "f16", window=W)
+    assert np.isnan(out2[0, 0]).all() and np.isfinite(out2[0, 1]).all()
+
+
+def test_window_block_check_covers_the_earliest_query_of_the_run():
+    # T = 3, W = 20, ctx = 36: query 0 sees positions 14..33, query 2 sees
+    # 16..35.  Block 0 holds position 14 and 15, so a bad id there is an error;
+    # with ctx = 38 no query sees block 0 and the same bad id is never read.
+    T, W = 3, 20
+    w = small(B=2, T=T, N=4, K=2, H=64, ctx=(36, 38), seed=36)
+    tables = w.block_tables.clone()
+    tables[:, 0] = -1
+    out, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], tables, w.context_lens,
+                                "f16", window=W)
+    assert err.tolist() == [8, 0]
+    assert (out[0] == 0).all() and np.isfinite(out[1]).all()
