@@ -47,7 +47,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     # Default: the workload the metric's bandwidth target is quoted on -- the
     # long-context ragged batch (B=256, log-normal contexts, 3.5 GB per step).
-    ap.add_argument("--workload", default="cfg4", choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5"])
+    ap.add_argument("--workload", default="cfg4",
+                    choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "hybrid"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
@@ -76,7 +77,9 @@ def step_bytes(w):
 
     e = 2
     ctx = w.context_lens.cpu().numpy()
-    attn = A.attention_algorithmic_bytes(ctx, w.T, w.N, w.K, w.H, e)
+    # mean over the layers (they differ only in their local-attention window)
+    attn = sum(A.attention_algorithmic_bytes(ctx, w.T, w.N, w.K, w.H, e, window=w.window(l))
+               for l in range(w.layers)) // w.layers
     app = A.kv_append_bytes(w.B, w.T, w.K, w.H, e) if w.appended else 0
     acc = A.accept_bytes(w.B, w.T, w.logits.shape[-1]) if w.logits is not None else 0
     return attn, app, acc
@@ -226,9 +229,10 @@ def oracle_sample(w, budget_s):
         for s0 in range(0, w.B, 8):
             bl = np.arange(s0, min(w.B, s0 + 8), dtype=np.int32)
             t0 = time.perf_counter()
-            oracle.attention(q, kc, vc, tables, lens, w.dtype, b_list=bl)
+            oracle.attention(q, kc, vc, tables, lens, w.dtype, b_list=bl, window=w.window(layer))
             spent += time.perf_counter() - t0
-            done_bytes += A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2)
+            done_bytes += A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2,
+                                                        window=w.window(layer))
             units += 1
             seqs += len(bl)
             if spent >= budget_s:
@@ -297,10 +301,11 @@ def run_ours(args, world, rank, local):
             if fused:
                 fused_fn(w.q[l], w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
                          w.block_tables, w.context_lens, out=outs[l], workspace=ws, status=st,
-                         pdl=True, early_kv=True)
+                         pdl=True, early_kv=True, window=w.window(l))
             else:
                 attn_fn(w.q[l], w.k_cache[l], w.v_cache[l], w.block_tables, w.context_lens,
-                        out=outs[l], workspace=ws, status=st, pdl=True, early_kv=True)
+                        out=outs[l], workspace=ws, status=st, pdl=True, early_kv=True,
+                        window=w.window(l))
 
     def do_acc():
         if sampled:
@@ -484,6 +489,7 @@ def run_ours(args, world, rank, local):
             "append": ("fused into the attention launch" if fused else
                        "separate kv_append launches" if w.appended else "none"),
             "parallelism": f"replicas x{world}",
+            "windows": list(w.windows) if w.windows else None,
         },
         "pct_of_peak": round(100 * value / world / peak, 2),
         "attention_tokens_per_s": round(world * w.B * w.T * L / (step_ms_max * 1e-3), 1),
@@ -540,11 +546,13 @@ def run_reference(args, world, rank, local):
         q, kc, vc = cache[l]
         bl = np.arange(s0, min(w.B, s0 + chunk), dtype=np.int32)
         t0 = time.perf_counter()
-        oracle.attention(q, kc, vc, w.block_tables, w.context_lens, w.dtype, b_list=bl)
+        oracle.attention(q, kc, vc, w.block_tables, w.context_lens, w.dtype, b_list=bl,
+                         window=w.window(l))
         dt = time.perf_counter() - t0
         if i >= W:
             times.append(dt)
-            nbytes.append(A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2))
+            nbytes.append(A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2,
+                                                        window=w.window(l)))
     value = sum(nbytes) / sum(times) / 1e9
     ms = 1e3 * sum(times) / K
     desc = (f"each step: the fp64 oracle's attention over one layer x {chunk} sequences of "

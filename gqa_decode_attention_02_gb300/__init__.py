@@ -9,6 +9,7 @@ CUDA kernels; calling any op without the built library raises.
     verify_attention(q, k_cache, v_cache, block_tables, context_lens) -> out
     append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)
     append_verify_attention(...)  (kv_append fused into the attention launch)
+    (every attention call takes window=W > 0 for local attention)
     accept_prefix(target_logits, draft_ids, context_lens=None) -> (accepted, next)
     accept_sampled(target_probs, draft_probs, draft_ids, uniforms,
                    context_lens=None) -> (accepted, next)
@@ -52,12 +53,14 @@ def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens, *, sta
     _lib._check("gqa_kv_append", rc)
 
 
-def attention_workspace_size(q, k_cache, block_tables, scale=None) -> int:
-    return _lib.workspace_size(_lib.make_shape(q, k_cache, block_tables, scale))
+def attention_workspace_size(q, k_cache, block_tables, scale=None, window=0) -> int:
+    """Workspace bytes of one attention call (a window never needs more than
+    full attention of the same shape)."""
+    return _lib.workspace_size(_lib.make_shape(q, k_cache, block_tables, scale, window=window))
 
 
 def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, scale,
-               workspace, status, stream, pdl, early_kv, k_new=None, v_new=None):
+               workspace, status, stream, pdl, early_kv, k_new=None, v_new=None, window=0):
     _lib._need(q, "q", ndim=4)
     if k_new is not None:
         _lib._need(k_new, "k_new", q.dtype, 4)
@@ -67,7 +70,7 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
     _lib._need(block_tables, "block_tables", torch.int32, 2)
     _lib._need(context_lens, "context_lens", torch.int32, 1)
     flags = (_lib.FLAG_PDL if pdl else 0) | (_lib.FLAG_EARLY_KV if early_kv else 0)
-    shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags)
+    shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags, window=window)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -88,37 +91,40 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
 
 
 def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
-                     workspace=None, status=None, stream=None, pdl=False, early_kv=False):
+                     workspace=None, status=None, stream=None, pdl=False, early_kv=False,
+                     window=0):
     """gqa_decode_attention (T == 1).  q [B,1,N,H] -> out [B,1,N,H].
-    pdl / early_kv select GQA_FLAG_PDL / GQA_FLAG_EARLY_KV (see the C header)."""
+    pdl / early_kv select GQA_FLAG_PDL / GQA_FLAG_EARLY_KV (see the C header);
+    window > 0 is local attention over each query's last `window` positions."""
     return _attention("gqa_decode_attention", q, k_cache, v_cache, block_tables, context_lens,
-                      out, scale, workspace, status, stream, pdl, early_kv)
+                      out, scale, workspace, status, stream, pdl, early_kv, window=window)
 
 
 def verify_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
-                     workspace=None, status=None, stream=None, pdl=False, early_kv=False):
+                     workspace=None, status=None, stream=None, pdl=False, early_kv=False,
+                     window=0):
     """gqa_verify_attention (T >= 1, causal among the T new tokens)."""
     return _attention("gqa_verify_attention", q, k_cache, v_cache, block_tables, context_lens,
-                      out, scale, workspace, status, stream, pdl, early_kv)
+                      out, scale, workspace, status, stream, pdl, early_kv, window=window)
 
 
 def append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
                             out=None, scale=None, workspace=None, status=None, stream=None,
-                            pdl=False, early_kv=False):
+                            pdl=False, early_kv=False, window=0):
     """gqa_append_decode_attention: kv_append + decode_attention in one launch
     (T == 1).  Writes k_new/v_new into the caches and returns out."""
     return _attention("gqa_append_decode_attention", q, k_cache, v_cache, block_tables,
                       context_lens, out, scale, workspace, status, stream, pdl, early_kv,
-                      k_new=k_new, v_new=v_new)
+                      k_new=k_new, v_new=v_new, window=window)
 
 
 def append_verify_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
                             out=None, scale=None, workspace=None, status=None, stream=None,
-                            pdl=False, early_kv=False):
+                            pdl=False, early_kv=False, window=0):
     """gqa_append_verify_attention: kv_append + verify_attention in one launch."""
     return _attention("gqa_append_verify_attention", q, k_cache, v_cache, block_tables,
                       context_lens, out, scale, workspace, status, stream, pdl, early_kv,
-                      k_new=k_new, v_new=v_new)
+                      k_new=k_new, v_new=v_new, window=window)
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,

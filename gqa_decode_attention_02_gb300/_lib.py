@@ -46,7 +46,7 @@ class Shape(ctypes.Structure):
                 ("K", ctypes.c_int), ("H", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("num_blocks", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("scale", ctypes.c_float),
-                ("flags", ctypes.c_uint)]
+                ("flags", ctypes.c_uint), ("window", ctypes.c_int)]
 
 
 FLAG_PDL = 1
@@ -133,7 +133,8 @@ def _need(t, name, dtype=None, ndim=None):
 
 
 def make_shape(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
-               scale: float | None, heads_dim: int = 2, flags: int = 0) -> Shape:
+               scale: float | None, heads_dim: int = 2, flags: int = 0,
+               window: int = 0) -> Shape:
     B, T, X, H = q_or_new.shape
     NB, bs, K, H2 = k_cache.shape
     if H2 != H:
@@ -142,7 +143,8 @@ def make_shape(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: torc
         raise ValueError(f"dtype {q_or_new.dtype} unsupported (fp16 / bf16)")
     return Shape(B=B, T=T, N=X if heads_dim == 2 else K, K=K, H=H, block_size=bs,
                  num_blocks=NB, max_blocks_per_seq=block_tables.shape[1],
-                 dtype=_DTYPES[q_or_new.dtype], scale=float(scale or 0.0), flags=int(flags))
+                 dtype=_DTYPES[q_or_new.dtype], scale=float(scale or 0.0), flags=int(flags),
+                 window=int(window))
 
 
 _ws_cache: dict = {}

@@ -62,21 +62,27 @@ def score_matrix_bytes(n: int, cached: bool, elem_bytes: int = 4) -> int:
 
 
 def attention_algorithmic_bytes(ctx_lens: Iterable[int], T: int, N: int, K: int, H: int,
-                                elem_bytes: int, block_size: int = 16) -> int:
+                                elem_bytes: int, block_size: int = 16, window: int = 0) -> int:
     """Bytes one decode/verify attention launch must move at minimum: every
-    valid cached key and value once, q in and out back, the block ids in use
-    and the context lengths."""
+    visible cached key and value once, q in and out back, the block ids in use
+    and the context lengths.  With a window W > 0 the visible positions of a
+    sequence are ctx - T - W + 1 .. ctx - 1 (clipped at 0): min(ctx, W + T - 1)
+    tokens, in the blocks from the one holding the first of them."""
     ctx = np.asarray(list(ctx_lens), np.int64)
     B = ctx.size
-    kv = int(ctx.sum()) * 2 * K * H * elem_bytes
+    first = np.maximum(0, ctx - T - window + 1) if window > 0 else np.zeros_like(ctx)
+    kv = int((ctx - first).sum()) * 2 * K * H * elem_bytes
     qo = 2 * B * T * N * H * elem_bytes
-    ids = 4 * int(((ctx + block_size - 1) // block_size).sum())
+    ids = 4 * int(((ctx + block_size - 1) // block_size - first // block_size).sum())
     return kv + qo + ids + 4 * B
 
 
-def attention_flops(ctx_lens: Iterable[int], T: int, N: int, H: int) -> int:
-    """4 * sum(ctx) * T * N * H (QK^T and PV; an upper bound when T > 1)."""
-    return 4 * int(np.asarray(list(ctx_lens), np.int64).sum()) * T * N * H
+def attention_flops(ctx_lens: Iterable[int], T: int, N: int, H: int, window: int = 0) -> int:
+    """4 * (visible tokens) * T * N * H (QK^T and PV; an upper bound when T > 1)."""
+    ctx = np.asarray(list(ctx_lens), np.int64)
+    if window > 0:
+        ctx = np.minimum(ctx, window + T - 1)
+    return 4 * int(ctx.sum()) * T * N * H
 
 
 def kv_append_bytes(B: int, T: int, K: int, H: int, elem_bytes: int) -> int:

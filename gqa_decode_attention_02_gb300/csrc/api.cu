@@ -19,6 +19,7 @@ gqa_status check_common(const gqa_shape* s) {
     if ((long long)s->num_blocks * 16 > (1ll << 31) - 1) return GQA_ERR_SHAPE;
     if ((long long)s->max_blocks_per_seq * 16 > (1ll << 30)) return GQA_ERR_SHAPE;
     if ((long long)s->B * s->K * s->max_blocks_per_seq > (1ll << 31) - 1) return GQA_ERR_SHAPE;
+    if (s->window < 0) return GQA_ERR_SHAPE;
     return GQA_OK;
 }
 

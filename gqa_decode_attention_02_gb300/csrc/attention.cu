@@ -87,6 +87,7 @@ struct AttnParams {
     int stages;    // depth of the shared-memory ring
     int groups;    // stage-parallel consumer groups
     int early_kv;  // GQA_FLAG_EARLY_KV: stream old cache blocks before the wait
+    int window;    // local attention: each query sees its last `window` positions (0: all)
     // Fused append (k_new != nullptr): the T newest positions are taken from
     // k_new / v_new [B][T][K][H] and written into the caches by this kernel.
     const void* k_new;
@@ -123,8 +124,17 @@ struct Cfg {
         2 * 32 * (4 + kAccFloats) * sizeof(float);  // per row warp of each extra group
 };
 
-__device__ __forceinline__ int seq_blocks(int ctx, int T, int max_blocks) {
-    return (ctx >= T && ctx >= 1 && ctx <= max_blocks * 16) ? (ctx + 15) >> 4 : 0;
+// First logical block a segment reads: the one holding the earliest position
+// any of the T new tokens sees (0 without a window).
+__device__ __forceinline__ int first_block(int ctx, int T, int window) {
+    return window > 0 ? max(0, ctx - T - window + 1) >> 4 : 0;
+}
+
+// Tiles (cache blocks) of one (b, k) segment; 0 for an invalid context length.
+__device__ __forceinline__ int seq_blocks(int ctx, int T, int max_blocks, int window) {
+    return (ctx >= T && ctx >= 1 && ctx <= max_blocks * 16)
+               ? ((ctx + 15) >> 4) - first_block(ctx, T, window)
+               : 0;
 }
 
 // Zero the outputs of one sequence (T x N x H elements of 2 bytes).
@@ -178,11 +188,12 @@ __device__ __forceinline__ void prefetch_q(const AttnParams& p, int b, int k) {
 }
 
 // ---------------------------------------------------------------------------
-template <int H>
+template <int H, bool WIN>
 __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
                          uint8_t* stages, const Bars& bar, StageMeta* meta,
                          volatile int* abort_flag) {
     using C = Cfg<H>;
+    const int win = WIN ? p.window : 0;  // compile-time 0 for full attention
     constexpr unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
@@ -205,7 +216,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     int local = 0;
     bool invalid = false;
     for (int b = lo; b < hi; ++b) {
-        const int n = seq_blocks(p.context_lens[b], p.T, p.max_blocks);
+        const int n = seq_blocks(p.context_lens[b], p.T, p.max_blocks, win);
         local += n;
         invalid |= (n == 0);
     }
@@ -215,7 +226,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             waited = true;
         }
         for (int b = lo; b < hi; ++b) {
-            if (seq_blocks(p.context_lens[b], p.T, p.max_blocks) == 0) {
+            if (seq_blocks(p.context_lens[b], p.T, p.max_blocks, win) == 0) {
                 report(p.status, GQA_ERR_CONTEXT);
                 zero_sequence<H>(p, b);
             }
@@ -247,7 +258,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             long long acc = (long long)p.K * excl;
             for (int b = lo; b < hi; ++b) {
                 const long long n =
-                    (long long)p.K * seq_blocks(p.context_lens[b], p.T, p.max_blocks);
+                    (long long)p.K * seq_blocks(p.context_lens[b], p.T, p.max_blocks, win);
                 if (c0 < acc + n) {
                     fb = b;
                     fbase = acc;
@@ -265,14 +276,17 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         int cbase = b;
         int ctxw = (b + lane < p.B) ? __ldg(p.context_lens + b + lane) : 0;
         int ctx = __shfl_sync(FULL, ctxw, 0);
-        int nblk = seq_blocks(ctx, p.T, p.max_blocks);
+        int nblk = seq_blocks(ctx, p.T, p.max_blocks, win);
+        int f0 = first_block(ctx, p.T, win);  // tile i is logical block f0 + i
         const int rel = (int)(c0 - base);
         int k = rel / nblk, i = rel % nblk;
         int ids = 0, ids_base = -(1 << 30);
         auto next_ids = [&](int bn) {
             const int cn = (bn < p.B) ? __shfl_sync(FULL, ctxw, min(bn - cbase, 31)) : 0;
-            const int nn = (bn < p.B && bn - cbase < 32) ? seq_blocks(cn, p.T, p.max_blocks) : 0;
-            return (lane < nn) ? __ldg(p.block_tables + (size_t)bn * p.max_blocks + lane) : 0;
+            const int nn =
+                (bn < p.B && bn - cbase < 32) ? seq_blocks(cn, p.T, p.max_blocks, win) : 0;
+            const int fn = first_block(cn, p.T, win);
+            return (lane < nn) ? __ldg(p.block_tables + (size_t)bn * p.max_blocks + fn + lane) : 0;
         };
         int ids_next = next_ids(b + 1);
         if (lane == 0) prefetch_q<H>(p, b, k);
@@ -284,8 +298,9 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             const int run = (int)min((long long)min(kTilesPerStage, nblk - i), c1 - x);
             if (i < ids_base || i + run > ids_base + 32) {  // warp-uniform refill
                 ids_base = i;
-                ids = (i + lane < nblk) ? __ldg(p.block_tables + (size_t)b * p.max_blocks + i + lane)
-                                        : 0;
+                ids = (i + lane < nblk)
+                          ? __ldg(p.block_tables + (size_t)b * p.max_blocks + f0 + i + lane)
+                          : 0;
             }
             int blk[kTilesPerStage];
             bool bad = false;
@@ -296,7 +311,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             }
             // (with the append fused in, the new positions come from k_new /
             // v_new after the consumers' wait, so only an error waits here)
-            if (!waited && ((!p.k_new && (i + run - 1) * 16 + 15 >= ctx - p.T) || bad)) {
+            if (!waited && ((!p.k_new && (f0 + i + run - 1) * 16 + 15 >= ctx - p.T) || bad)) {
                 griddep_wait();  // the stage holds new positions (or reports an error)
                 waited = true;
             }
@@ -313,7 +328,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                     StageMeta& m = meta[s];
                     m.b = b;
                     m.k = k;
-                    m.blk_i = i;
+                    m.blk_i = f0 + i;  // logical block index
                     m.ntiles = run;
                     m.ctx = ctx;
                     m.seg_start = (int)(base + (long long)k * nblk);
@@ -368,8 +383,9 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                                 ctxw = (b + lane < p.B) ? __ldg(p.context_lens + b + lane) : 0;
                             }
                             ctx = __shfl_sync(FULL, ctxw, b - cbase);
-                            nblk = seq_blocks(ctx, p.T, p.max_blocks);
+                            nblk = seq_blocks(ctx, p.T, p.max_blocks, win);
                         } while (nblk == 0);
+                        f0 = first_block(ctx, p.T, win);
                         if (b == b_prev + 1 && next_ok) {  // prefetched ids are b's
                             ids = ids_next;
                             ids_base = 0;
@@ -411,7 +427,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
 // rows 8*(w*NW + u) .. +7 (rows r = t*G + g).  Every K / V fragment it reads
 // from shared memory feeds NW mma, so more rows per warp means fewer warps
 // re-reading the same stage.
-template <int H, bool BF16, int NW>
+template <int H, bool BF16, int NW, bool WIN>
 struct Consumer {
     using C = Cfg<H>;
     using E = Elt<BF16>;
@@ -519,6 +535,7 @@ struct Consumer {
 
     // One stage: md.ntiles tiles of 16 tokens starting at tile md.blk_i.
     __device__ void stage(uint32_t kbase, const StageMeta& md) {
+        const int win = WIN ? p.window : 0;  // compile-time 0 for full attention
         if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
         const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
         const int ntl = md.ntiles;
@@ -561,13 +578,17 @@ struct Consumer {
                 if (j >= ntl) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[u][j][e] = -INFINITY;
-                } else if (tb + 15 > md.ctx - p.T) {  // some position hidden from some row
+                } else if (tb + 15 > md.ctx - p.T ||
+                           (win > 0 && tb < md.ctx - win)) {
+                    // some position hidden from some row: above its causal
+                    // bound lim, or (local attention) at or below lim - window
                     const int lim0 = md.ctx - p.T + t0[u], lim1 = md.ctx - p.T + t1[u];
                     const int pos0 = tb + g, pos8 = pos0 + 8;
-                    if (pos0 > lim0) sc[u][j][0] = -INFINITY;
-                    if (pos0 > lim1) sc[u][j][1] = -INFINITY;
-                    if (pos8 > lim0) sc[u][j][2] = -INFINITY;
-                    if (pos8 > lim1) sc[u][j][3] = -INFINITY;
+                    const int wl = win > 0 ? win : (1 << 30);
+                    if (pos0 > lim0 || pos0 <= lim0 - wl) sc[u][j][0] = -INFINITY;
+                    if (pos0 > lim1 || pos0 <= lim1 - wl) sc[u][j][1] = -INFINITY;
+                    if (pos8 > lim0 || pos8 <= lim0 - wl) sc[u][j][2] = -INFINITY;
+                    if (pos8 > lim1 || pos8 <= lim1 - wl) sc[u][j][3] = -INFINITY;
                 }
                 x0 = fmaxf(x0, fmaxf(sc[u][j][0], sc[u][j][2]));
                 x1 = fmaxf(x1, fmaxf(sc[u][j][1], sc[u][j][3]));
@@ -617,12 +638,17 @@ struct Consumer {
                 pb1[u] = movm_t(pt1);
             }
             const int tb = (md.blk_i + j) * 16;
-            const bool tail = tb + 16 > md.ctx;
+            // NaN-safe: zero V elements of slots past the context and, with a
+            // window, of positions below every new token's window (a block
+            // only partly inside the window may hold anything there)
+            const int lo_min = win > 0 ? md.ctx - p.T - win + 1 : 0;
+            const bool tail = tb + 16 > md.ctx || tb < lo_min;
             uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
-            if (tail) {  // NaN-safe: zero V elements of slots past the context
+            if (tail) {
                 const int pb = tb + 2 * q4;
-                v01 = (pb < md.ctx ? 0x0000ffffu : 0u) | (pb + 1 < md.ctx ? 0xffff0000u : 0u);
-                v89 = (pb + 8 < md.ctx ? 0x0000ffffu : 0u) | (pb + 9 < md.ctx ? 0xffff0000u : 0u);
+                auto ok = [&](int x) { return x < md.ctx && x >= lo_min; };
+                v01 = (ok(pb) ? 0x0000ffffu : 0u) | (ok(pb + 1) ? 0xffff0000u : 0u);
+                v89 = (ok(pb + 8) ? 0x0000ffffu : 0u) | (ok(pb + 9) ? 0xffff0000u : 0u);
             }
             const uint32_t vt = vbase + j * C::kTileBytes;
 #pragma unroll
@@ -827,12 +853,12 @@ struct Consumer {
 // 8*(w % nt) .. +7.  Every warp reads every stage's description, so all groups
 // agree on segment boundaries; at each boundary the groups' partial states
 // meet in shared memory and group 0 finishes the segment.
-template <int H, bool BF16, int NW>
+template <int H, bool BF16, int NW, bool WIN>
 __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
                          const StageMeta* meta, float* scratch, volatile int* abort_flag,
                          int w) {
     using C = Cfg<H>;
-    using CS = Consumer<H, BF16, NW>;
+    using CS = Consumer<H, BF16, NW, WIN>;
     const int gi = w / p.nt, wr = w % p.nt;
     CS cs(p, wr);
     const int lane = threadIdx.x & 31;
@@ -899,7 +925,8 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
 
 // NW = 1: up to 6 row warps per group; NW = 2 (two 8-row tiles per warp, for
 // many query rows) up to 3, with the register budget of the smaller CTA.
-template <int H, bool BF16, int NW>
+// WIN: local attention (the window arithmetic is compiled out without it).
+template <int H, bool BF16, int NW, bool WIN>
 __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRowWarps / 2 + 1))
     attention_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -933,25 +960,25 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
     }
     __syncthreads();
     if (warp == consumers)
-        producer<H>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
+        producer<H, WIN>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
     else
-        consumer<H, BF16, NW>(p, stages, bar, meta, scratch, abort_flag, warp);
+        consumer<H, BF16, NW, WIN>(p, stages, bar, meta, scratch, abort_flag, warp);
 }
 
 // ---------------------------------------------------------------------------
 // Host side
-template <int H, bool BF16, int NW>
-const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(&attention_kernel<H, BF16, NW>);
+// The instantiated variants: (nw, window) in {(1, no), (1, yes), (2, no)} for
+// each head size and dtype.
+template <int H, bool BF16>
+const void* kernel_ptr(int nw, bool win) {
+    if (nw == 2) return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 2, false>);
+    return win ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true>)
+               : reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false>);
 }
 
-const void* pick_kernel(int H, bool bf16, int nw) {
-    if (H == 64) {
-        if (nw == 1) return bf16 ? kernel_ptr<64, true, 1>() : kernel_ptr<64, false, 1>();
-        return bf16 ? kernel_ptr<64, true, 2>() : kernel_ptr<64, false, 2>();
-    }
-    if (nw == 1) return bf16 ? kernel_ptr<128, true, 1>() : kernel_ptr<128, false, 1>();
-    return bf16 ? kernel_ptr<128, true, 2>() : kernel_ptr<128, false, 2>();
+const void* pick_kernel(int H, bool bf16, int nw, bool win) {
+    if (H == 64) return bf16 ? kernel_ptr<64, true>(nw, win) : kernel_ptr<64, false>(nw, win);
+    return bf16 ? kernel_ptr<128, true>(nw, win) : kernel_ptr<128, false>(nw, win);
 }
 
 // Consumer groups for nt row warps.  (A third group was measured slower on
@@ -1013,16 +1040,16 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
 // CTAs of one variant resident per SM, queried once per (device, variant) so
 // that later calls -- including calls being captured into a CUDA graph -- make
 // no attribute or occupancy API calls.
-int resident_ctas(int H, bool bf16, int nt, int nw, size_t smem) {
+int resident_ctas(int H, bool bf16, int nt, int nw, bool win, size_t smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw);
+    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw * 2 + (int)win);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void* kern = pick_kernel(H, bf16, nw);
+    const void* kern = pick_kernel(H, bf16, nw, win);
     // The attribute belongs to the kernel, whatever the row-warp count: set it
     // to the largest launch any shape makes.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1058,6 +1085,7 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     if ((long long)s.num_blocks * 16 > (1ll << 31) - 1) return GQA_ERR_SHAPE;
     if ((long long)s.max_blocks_per_seq * 16 > (1ll << 30)) return GQA_ERR_SHAPE;
     if (s.dtype != GQA_F16 && s.dtype != GQA_BF16) return GQA_ERR_DTYPE;
+    if (s.window < 0) return GQA_ERR_SHAPE;
     const int G = s.N / s.K;
     const long long R = (long long)s.T * G;
     if (R > 8 * kMaxRowWarps) return GQA_ERR_SHAPE;
@@ -1070,7 +1098,7 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     const int threads = 32 * (groups * nt + 1);
     int stages = default_stages(s.H);
     size_t smem = smem_for(s.H, nt, nw, stages);
-    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, smem);
+    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, s.window > 0, smem);
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
@@ -1078,7 +1106,10 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     // full) run one CTA per SM: fewer CTAs split fewer sequences, and the SM
     // keeps room for the next launch on the stream, whose producer can then
     // start streaming (programmatic dependent launch) while this one finishes.
-    const long long tiles_max = (long long)s.B * s.K * s.max_blocks_per_seq;
+    long long blocks_max = s.max_blocks_per_seq;  // per sequence, window included
+    if (s.window > 0)
+        blocks_max = std::min<long long>(blocks_max, ((long long)s.window + s.T + 14) / 16 + 1);
+    const long long tiles_max = (long long)s.B * s.K * blocks_max;
     if (tiles_max <= 256ll * sms) occ = 1;
     long long grid = (long long)sms * occ;
     grid = std::min<long long>(grid, std::max<long long>(1, (tiles_max + kQuotaMin - 1) / kQuotaMin));
@@ -1131,6 +1162,7 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
     p.scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
     p.early_kv = (s.flags & GQA_FLAG_EARLY_KV) ? 1 : 0;
+    p.window = s.window;
     p.k_new = k_new;
     p.v_new = v_new;
     p.k_cache = const_cast<void*>(k_cache);
@@ -1147,23 +1179,10 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t e;
     const int nw = plan.tiles_per_warp;
-    if (s.H == 64) {
-        if (nw == 1)
-            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<64, true, 1>, tmk, tmv, p)
-                     : cudaLaunchKernelEx(&cfg, attention_kernel<64, false, 1>, tmk, tmv, p);
-        else
-            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<64, true, 2>, tmk, tmv, p)
-                     : cudaLaunchKernelEx(&cfg, attention_kernel<64, false, 2>, tmk, tmv, p);
-    } else {
-        if (nw == 1)
-            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<128, true, 1>, tmk, tmv, p)
-                     : cudaLaunchKernelEx(&cfg, attention_kernel<128, false, 1>, tmk, tmv, p);
-        else
-            e = bf16 ? cudaLaunchKernelEx(&cfg, attention_kernel<128, true, 2>, tmk, tmv, p)
-                     : cudaLaunchKernelEx(&cfg, attention_kernel<128, false, 2>, tmk, tmv, p);
-    }
+    const void* kern = pick_kernel(s.H, bf16, nw, s.window > 0);
+    void* args[] = {&tmk, &tmv, &p};
+    const cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -62,6 +62,10 @@ class Workload:
     draft: Optional[torch.Tensor] = None  # int32 [B,T-1]
     draft_k: Optional[np.ndarray] = None  # planted accepted-prefix length per b
     desc: str = ""
+    windows: tuple = ()  # per layer: local-attention window, 0 = global (all 0 if empty)
+
+    def window(self, layer: int) -> int:
+        return self.windows[layer] if self.windows else 0
 
     @property
     def G(self) -> int:
@@ -103,7 +107,7 @@ def build(name: str, B: int, T: int, N: int, K: int, H: int, dtype: str,
           ctx: np.ndarray, *, seed: int, layers: int = 1, shuffle: bool = True,
           append: bool = True, spare_blocks: int = 1, block_size: int = BLOCK_SIZE,
           max_blocks: Optional[int] = None, device="cpu", vocab: int = 0,
-          desc: str = "") -> Workload:
+          desc: str = "", windows: tuple = ()) -> Workload:
     """Lay out a paged block pool for the given context lengths and fill it.
 
     Physical blocks: sum_b ceil(ctx_b / bs) in use plus `spare_blocks` never
@@ -162,7 +166,7 @@ def build(name: str, B: int, T: int, N: int, K: int, H: int, dtype: str,
                  context_lens=torch.as_tensor(ctx.astype(np.int32), device=device),
                  block_tables=torch.as_tensor(tables.astype(np.int32), device=device),
                  q=qs, k_cache=kcs, v_cache=vcs, k_new=kns, v_new=vns,
-                 appended=append, desc=desc)
+                 appended=append, desc=desc, windows=tuple(windows))
     if vocab:
         logits = torch.randn((B, T, vocab), generator=gen, dtype=torch.float32,
                              device=device)
@@ -213,6 +217,14 @@ SPECS = {
              "fp32 logits [16,5,32000]",
         B=16, T=5, N=64, K=8, H=128, dtype="bf16", layers=1, shuffle=True,
         append=True, ctx=("uniform", 512, 4096), seed=105, vocab=32000),
+    # Not one of the five: local attention in a hybrid-layer schedule (one
+    # global layer in every six, the rest local), on the long-context geometry.
+    "hybrid": dict(
+        desc="hybrid local/global layers: 6 layers, layers 0-4 local attention with a "
+             "1024-token window, layer 5 global; B=32, T=1, N=32, K=8, H=128, bf16, "
+             "context 8192 (8191 cached + 1 appended), shuffled blocks",
+        B=32, T=1, N=32, K=8, H=128, dtype="bf16", layers=6, shuffle=True,
+        append=True, ctx=("fixed", 8192), seed=106, windows=(1024,) * 5 + (0,)),
 }
 
 

@@ -92,7 +92,19 @@ typedef struct {
     gqa_dtype dtype;        /* element type of q, out, caches, k_new, v_new */
     float scale;            /* score scale; <= 0 selects 1/sqrt(H) */
     unsigned int flags;     /* GQA_FLAG_* bits, 0 for plain stream order */
+    int window;             /* local attention: > 0 limits each query to the last
+                               `window` positions up to itself; 0 = all */
 } gqa_shape;
+
+/* Local (sliding-window) attention, for the attention calls: CS336 lecture 10
+ * §"Уменьшаем KV-кэш" (attend only to a recent stretch of context; the cache no
+ * longer grows with the sequence; hybrid schedules interleave local and global
+ * layers) and "Stanford CS336 Day 13 - Inference" §"Local Attention" (only the
+ * last k tokens are attended; older tokens may be dropped from the cache).
+ * With window = W > 0, new token t (position i = context_lens[b] - T + t) sees
+ * positions i-W+1 .. i only.  Blocks wholly below position
+ * context_lens[b] - T - W + 1 are never read, so their table entries may hold
+ * anything (freed blocks); only the blocks of the window are checked. */
 
 /* Launch with programmatic dependent launch: the kernel may be scheduled while
  * the previous kernel on the stream is still finishing, and waits for it (with

@@ -105,3 +105,16 @@ def test_accept_sampled_bytes_by_hand():
                                                     + A.accept_sampled_bytes([4], T, V))
     # T=1: no drafts, one uniform, a draw over q
     assert A.accept_sampled_bytes([0], 1, V) == 8 + 16 + 4000
+
+
+def test_windowed_bytes_by_hand():
+    # ctx 100, T=1, W=20: positions 80..99 (20 tokens) in blocks 5 and 6;
+    # ctx 10: all 10 tokens in block 0.  K=2, H=64, fp16.
+    b = A.attention_algorithmic_bytes([100, 10], T=1, N=4, K=2, H=64, elem_bytes=2, window=20)
+    assert b == (20 + 10) * 2 * 2 * 64 * 2 + 2 * 2 * 1 * 4 * 64 * 2 + 4 * (2 + 1) + 4 * 2
+    # a window wider than every context is full attention
+    assert (A.attention_algorithmic_bytes([100, 10], 3, 4, 2, 64, 2, window=500)
+            == A.attention_algorithmic_bytes([100, 10], 3, 4, 2, 64, 2))
+    # T=3, W=20, ctx 100: positions 78..99 (22 tokens) from block 4
+    b3 = A.attention_algorithmic_bytes([100], T=3, N=4, K=2, H=64, elem_bytes=2, window=20)
+    assert b3 == 22 * 2 * 2 * 64 * 2 + 2 * 3 * 4 * 64 * 2 + 4 * (7 - 4) + 4

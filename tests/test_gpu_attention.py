@@ -7,7 +7,7 @@ import torch
 
 import gqa_decode_attention_02_gb300 as gq
 import oracle
-from helpers import assert_close, small, to
+from helpers import assert_close, set_token, small, to
 
 pytestmark = pytest.mark.gpu
 
@@ -336,3 +336,106 @@ def test_fused_append_pdl_early_graph_matches_plain(gpu, T):
             for l in range(layers):
                 assert torch.equal(got[l].view(torch.int16), ref[l].view(torch.int16))
                 assert torch.equal(got_k[l].view(torch.int16), ref_k[l].view(torch.int16))
+
+
+# ---- local (sliding-window) attention --------------------------------------------
+def oracle_window(w, W, tables=None):
+    return oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0],
+                            w.block_tables if tables is None else tables, w.context_lens,
+                            w.dtype, window=W)
+
+
+@pytest.mark.parametrize("T,N,K,H,dtype", [(1, 32, 8, 128, "bf16"), (1, 14, 2, 64, "f16"),
+                                           (5, 64, 8, 128, "bf16"), (3, 16, 1, 64, "f16")])
+@pytest.mark.parametrize("W", [1, 15, 16, 17, 100, 1024])
+def test_window_matches_oracle(gpu, T, N, K, H, dtype, W):
+    ctx = tuple(max(c, T) for c in (1, 2, 15, 16, 17, 31, 295, 1029, 4097))
+    w = small(B=len(ctx), T=T, N=N, K=K, H=H, dtype=dtype, ctx=ctx, seed=W + 13 * T + N)
+    ref, err = oracle_window(w, W)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    fn = gq.decode_attention if T == 1 else gq.verify_attention
+    out = fn(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables, wd.context_lens, window=W)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, dtype, f"window {W} T={T}")
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_window_ignores_poisoned_and_freed_blocks(gpu, T):
+    """NaN in every position below the earliest window and INT32_MAX in the
+    table entries of blocks no query sees: same result, no error."""
+    W = 40
+    ctx = (T, 45, 64, 300, 1000)
+    w = small(B=len(ctx), T=T, N=8, K=2, H=128, dtype="bf16", ctx=ctx, seed=77 + T)
+    ref, _ = oracle_window(w, W)
+    tables = w.block_tables.clone()
+    for b, c in enumerate(ctx):
+        first = max(0, c - T - W + 1)
+        for pos in range(first):
+            set_token(w, b, pos, k=torch.full((2, 128), float("nan")),
+                      v=torch.full((2, 128), float("nan")))
+        tables[b, : first // 16] = 2**31 - 1
+    ref2, err = oracle_window(w, W, tables)
+    assert (err == 0).all()
+    np.testing.assert_array_equal(ref2, ref)
+    wd = to(w, gpu)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    fn = gq.decode_attention if T == 1 else gq.verify_attention
+    out = fn(wd.q[0], wd.k_cache[0], wd.v_cache[0], tables.to(gpu), wd.context_lens, window=W,
+             status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.float().cpu().double().numpy()
+    assert np.isfinite(got).all()
+    assert_close(got, ref, "bf16", "poisoned window")
+
+
+def test_window_bad_block_inside_window_is_reported(gpu):
+    T, W = 3, 20
+    w = small(B=2, T=T, N=4, K=2, H=64, ctx=(36, 38), seed=36)
+    tables = w.block_tables.clone()
+    tables[:, 0] = -1  # seen by query 0 of sequence 0 only
+    ref, err = oracle_window(w, W, tables)
+    assert err.tolist() == [8, 0]
+    wd = to(w, gpu)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    out = gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], tables.to(gpu),
+                              wd.context_lens, window=W, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 8
+    got = out.float().cpu().double().numpy()
+    assert (got[0] == 0).all()
+    assert_close(got[1:], ref[1:], "f16", "bad block in window")
+
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_window_fused_append_matches_oracle(gpu, T):
+    W = 64
+    ctx = (T, 70, 333, 2000)
+    w = small(B=len(ctx), T=T, N=64 if T == 5 else 32, K=8, H=128, dtype="bf16", ctx=ctx,
+              seed=91 + T, append=True)
+    kc, vc, _ = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                 w.block_tables, w.context_lens)
+    kt = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16)
+    vt = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16)
+    ref, err = oracle.attention(w.q[0], kt, vt, w.block_tables, w.context_lens, "bf16",
+                                window=W)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    fn = gq.append_decode_attention if T == 1 else gq.append_verify_attention
+    out = fn(wd.q[0], wd.k_new[0], wd.v_new[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+             wd.context_lens, window=W)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", f"fused window T={T}")
+    np.testing.assert_array_equal(wd.k_cache[0].cpu().view(torch.int16).numpy().view(np.uint16),
+                                  kc)
+
+
+def test_window_of_int_max_is_full_attention(gpu):
+    w = small(B=3, T=2, N=8, K=2, H=64, dtype="f16", ctx=(2, 40, 1000), seed=5)
+    ref, _ = oracle_out(w)
+    wd = to(w, gpu)
+    out = gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                              wd.context_lens, window=2**31 - 1)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, "f16", "window INT_MAX")

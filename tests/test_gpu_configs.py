@@ -1,4 +1,4 @@
-"""Parity at the five named workloads' full sizes, through the same calls the
+"""Parity at the named workloads' full sizes, through the same calls the
 bench times (kv_append then decode/verify attention; accept_prefix).  Where the
 oracle would take too long on the whole batch, it checks a seeded sample of
 sequences that always includes the shortest and the longest."""
@@ -39,8 +39,9 @@ def check_workload(name, dev, sample=None, layers=None, fused=False):
             ovc = torch.from_numpy(ovc.view(np.int16)).view(w.torch_dtype)
         else:
             okc, ovc = kc, vc
+        win = w.window(layer)
         ref, err = oracle.attention(w.q[layer], okc, ovc, w.block_tables, w.context_lens,
-                                    w.dtype, b_list=bl)
+                                    w.dtype, b_list=bl, window=win)
         assert (err == 0).all()
         kd, vd = kc.to(dev), vc.to(dev)
         bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
@@ -49,7 +50,7 @@ def check_workload(name, dev, sample=None, layers=None, fused=False):
         if w.appended and fused:  # the append inside the attention launch (the bench's call)
             ffn = gq.append_decode_attention if w.T == 1 else gq.append_verify_attention
             out = ffn(w.q[layer].to(dev), w.k_new[layer].to(dev), w.v_new[layer].to(dev), kd, vd,
-                      bt, cl, status=st, pdl=True, early_kv=True)
+                      bt, cl, status=st, pdl=True, early_kv=True, window=win)
         elif w.appended:
             gq.kv_append(w.k_new[layer].to(dev), w.v_new[layer].to(dev), kd, vd, bt, cl,
                          status=st)
@@ -63,7 +64,7 @@ def check_workload(name, dev, sample=None, layers=None, fused=False):
                                           ovc[blocks].view(torch.int16).numpy())
         if out is None:
             fn = gq.decode_attention if w.T == 1 else gq.verify_attention
-            out = fn(w.q[layer].to(dev), kd, vd, bt, cl, status=st)
+            out = fn(w.q[layer].to(dev), kd, vd, bt, cl, status=st, window=win)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         got = out.cpu()[torch.as_tensor(bl).long()].double().numpy()
@@ -105,3 +106,11 @@ def test_cfg5_verify_and_accept(gpu):
 @pytest.mark.parametrize("name,sample", [("cfg2", None), ("cfg3", 8), ("cfg4", 16), ("cfg5", None)])
 def test_fused_append_at_full_size(gpu, name, sample):
     check_workload(name, gpu, sample=sample, fused=True)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_hybrid_local_global_layers(gpu, fused):
+    """Six layers, five of local attention (1024-token window) and one global,
+    on the long-context geometry, through the bench's calls."""
+    w, _ = check_workload("hybrid", gpu, sample=8, fused=fused)
+    assert w.windows == (1024,) * 5 + (0,)
