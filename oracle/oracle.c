@@ -123,16 +123,26 @@ int oracle_kv_append(int B, int T, int K, int H, int block_size, int num_blocks,
  * itself.  window == 0 is full attention.  Only the blocks holding a visible
  * position are looked up (blocks wholly below every window may be freed).
  *
+ * Tree verification, [SONAR-KK] §"EAGLE": drafts form a tree (Top-K candidates
+ * at each node), and verifying the tree in the target model needs a custom
+ * attention mask.  With tree_mask != NULL, new token t (t < T) sees the whole
+ * prefix (positions < ctx - T), itself, and new token j < t iff bit j of
+ * tree_mask[b][t] is set: for a tree laid out in topological order (every
+ * node after its parent), its ancestors.  Bits j >= t are ignored.
+ * tree_mask == NULL is the chain (token t sees new tokens 0..t).  Window and
+ * tree mask are not combined (the call rejects both at once).
+ *
  * For each listed sequence b = b_list[i] (all b when b_list is NULL) writes
  * out[i][t][n][h] in fp64.  A sequence with a bad context length or a bad
  * block id gets an all-zero output and a nonzero seq_err[i]. */
 int oracle_attention(int B, int T, int N, int K, int H, int block_size,
                      int num_blocks, int max_blocks, int dtype, double scale,
-                     int window, const uint16_t *q, const uint16_t *k_cache,
+                     int window, const uint64_t *tree_mask, const uint16_t *q, const uint16_t *k_cache,
                      const uint16_t *v_cache, const int32_t *block_tables,
                      const int32_t *context_lens, const int32_t *b_list, int nb,
                      double *out, int32_t *seq_err, int nthreads) {
-    if (K <= 0 || N % K != 0 || window < 0) return -1;
+    if (K <= 0 || N % K != 0 || window < 0 || (window > 0 && tree_mask)) return -1;
+    if (tree_mask && T > 64) return -1;
     int G = N / K;
     if (!b_list) nb = B;
     if (scale <= 0) scale = 1.0 / sqrt((double)H);
@@ -186,8 +196,16 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
         double *qd = (double *)malloc(sizeof(double) * (size_t)H);
         for (int h = 0; h < H; ++h) qd[h] = widen(qv[h], dtype);
         /* scores s_j = scale * <q, k_j> */
+        /* visible(j): in the band first..last and, with a tree, a prefix
+         * position, the token itself or a new token its mask row selects */
+        const int first_new = ctx - T;
+        const uint64_t mrow = tree_mask ? tree_mask[(size_t)b * T + t] : 0;
+#define VISIBLE(j)                                                                   \
+    (!tree_mask || (j) < first_new || (j) - first_new == t ||                       \
+     (((j) - first_new) < 64 && ((mrow >> ((j) - first_new)) & 1u)))
         double smax = -INFINITY;
         for (int j = first; j <= last; ++j) {
+            if (!VISIBLE(j)) continue;
             int blk = block_tables[(size_t)b * max_blocks + j / block_size];
             const uint16_t *kr =
                 k_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;
@@ -199,11 +217,13 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
         /* softmax weights p_j = exp(s_j - max) / sum, then out = sum_j p_j v_j */
         double denom = 0.0;
         for (int j = first; j <= last; ++j) {
+            if (!VISIBLE(j)) continue;
             s[j] = exp(s[j] - smax);
             denom += s[j];
         }
         for (int h = 0; h < H; ++h) o[h] = 0.0;
         for (int j = first; j <= last; ++j) {
+            if (!VISIBLE(j)) continue;
             int blk = block_tables[(size_t)b * max_blocks + j / block_size];
             const uint16_t *vr =
                 v_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;

@@ -51,7 +51,7 @@ def _get():
             lib.oracle_kv_append.restype = i
             lib.oracle_kv_append.argtypes = [i] * 7 + [P] * 7
             lib.oracle_attention.restype = i
-            lib.oracle_attention.argtypes = [i] * 9 + [ctypes.c_double, i] + [P] * 6 + [i, P, P, i]
+            lib.oracle_attention.argtypes = [i] * 9 + [ctypes.c_double, i] + [P] * 7 + [i, P, P, i]
             lib.oracle_accept_prefix.restype = None
             lib.oracle_accept_prefix.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_accept_sampled.restype = None
@@ -117,9 +117,10 @@ def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens):
 
 
 def attention(q, k_cache, v_cache, block_tables, context_lens, dtype, scale=0.0,
-              b_list=None, nthreads=0, window=0):
+              b_list=None, nthreads=0, window=0, tree_mask=None):
     """fp64 paged GQA attention.  q [B,T,N,H]; caches [NB,bs,K,H]; window > 0
-    limits query position i to positions i-window+1 .. i.
+    limits query position i to positions i-window+1 .. i; tree_mask [B,T]
+    (uint64) lets new token t see new token j < t only if bit j is set.
     Returns (out [nb,T,N,H] float64, seq_err [nb]) for the listed sequences."""
     qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
     bt, cl = _i32(block_tables), _i32(context_lens)
@@ -130,12 +131,16 @@ def attention(q, k_cache, v_cache, block_tables, context_lens, dtype, scale=0.0,
     nb = B if bl is None else len(bl)
     out = np.zeros((nb, T, N, H), np.float64)
     err = np.zeros(max(nb, 1), np.int32)
+    tm = None
+    if tree_mask is not None:
+        tm = np.ascontiguousarray(np.asarray(tree_mask).astype(np.uint64)).reshape(B, T)
     rc = _get().oracle_attention(B, T, N, K, H, bs, NB, bt.shape[1], _DT[dtype],
-                                 float(scale), int(window), _p(qb), _p(kc), _p(vc), _p(bt),
-                                 _p(cl),
+                                 float(scale), int(window), _p(tm), _p(qb), _p(kc), _p(vc),
+                                 _p(bt), _p(cl),
                                  _p(bl), nb, _p(out), _p(err), int(nthreads))
     if rc < 0:
-        raise ValueError("oracle_attention: N must be a multiple of K and window >= 0")
+        raise ValueError("oracle_attention: N must be a multiple of K, window >= 0, and a "
+                         "tree mask needs window == 0 and T <= 64")
     return out, err[:nb]
 
 

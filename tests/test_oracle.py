@@ -398,3 +398,85 @@ def test_window_block_check_covers_the_earliest_query_of_the_run():
                                 "f16", window=W)
     assert err.tolist() == [8, 0]
     assert (out[0] == 0).all() and np.isfinite(out[1]).all()
+
+
+# ---- tree verification (custom mask among the new tokens) -------------------------
+def tree_masks(parents):
+    """uint64 mask rows of a tree given as parent indices (-1: child of the
+    prefix), nodes in topological order: bit j of row t set for every ancestor."""
+    T = len(parents)
+    m = np.zeros(T, np.uint64)
+    for t in range(T):
+        a = parents[t]
+        while a >= 0:
+            m[t] |= np.uint64(1) << np.uint64(a)
+            a = parents[a]
+    return m
+
+
+TREE = [-1, 0, 0, 1, 1, 2, 3, -1]  # two roots, depth 4
+
+
+def test_tree_chain_mask_equals_verify():
+    T = 6
+    ctx = (T, 30, 77)
+    w = small(B=3, T=T, N=4, K=2, H=64, ctx=ctx, seed=41)
+    chain = np.array([(1 << t) - 1 for t in range(T)], np.uint64)
+    ref, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "f16")
+    got, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "f16", tree_mask=np.tile(chain, (3, 1)))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_tree_equal_keys_average_prefix_and_ancestors():
+    T = len(TREE)
+    ctx = (T, 21, 50)
+    w = small(B=3, T=T, N=4, K=2, H=64, ctx=ctx, seed=42)
+    key = torch.randn(2, 64, generator=torch.Generator().manual_seed(9))
+    for b, c in enumerate(ctx):
+        for pos in range(c):
+            set_token(w, b, pos, k=key, v=torch.full((2, 64), float(pos)))
+    m = tree_masks(TREE)
+    out, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                                w.context_lens, "f16", tree_mask=np.tile(m, (3, 1)))
+    assert (err == 0).all()
+    for b, c in enumerate(ctx):
+        P = c - T
+        for t in range(T):
+            vis = list(range(P)) + [P + j for j in range(T) if j == t or (int(m[t]) >> j) & 1]
+            np.testing.assert_allclose(out[b, t], np.mean(vis), rtol=1e-12, atol=1e-12)
+
+
+def test_tree_rows_equal_causal_attention_down_their_path():
+    """EAGLE's tree attention is causal attention of the prefix followed by the
+    node's root-to-node path: recompute each path as a linear sequence."""
+    T = len(TREE)
+    ctx = (T + 3, 40, 100)
+    w = small(B=3, T=T, N=6, K=2, H=64, dtype="bf16", ctx=ctx, seed=43)
+    m = tree_masks(TREE)
+    out, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "bf16", tree_mask=np.tile(m, (3, 1)))
+    for b, c in enumerate(ctx):
+        P = c - T
+        kk, vv = unpage(w, b, c)
+        qn = w.q[0][b].double().numpy()  # [T, N, H]
+        for t in range(T):
+            path = [j for j in range(T) if (int(m[t]) >> j) & 1] + [t]
+            seq = list(range(P)) + [P + j for j in path]
+            q_all = np.zeros((len(seq), 6, 64))
+            q_all[-1] = qn[t]
+            full = oracle.causal_attention_full(q_all, kk[seq], vv[seq], 1.0 / 8.0)
+            np.testing.assert_allclose(out[b, t], full[-1], rtol=0, atol=1e-12)
+
+
+def test_tree_bits_at_or_after_the_row_are_ignored():
+    T = len(TREE)
+    w = small(B=2, T=T, N=4, K=2, H=64, ctx=(T, 60), seed=44)
+    m = tree_masks(TREE)
+    junk = m | np.array([~np.uint64(0) << np.uint64(t) for t in range(T)], np.uint64)
+    a, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables, w.context_lens,
+                            "f16", tree_mask=np.tile(m, (2, 1)))
+    b_, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables, w.context_lens,
+                             "f16", tree_mask=np.tile(junk, (2, 1)))
+    np.testing.assert_array_equal(a, b_)
