@@ -60,8 +60,14 @@ def attention_workspace_size(q, k_cache, block_tables, scale=None, window=0) -> 
 
 
 def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, scale,
-               workspace, status, stream, pdl, early_kv, k_new=None, v_new=None, window=0):
+               workspace, status, stream, pdl, early_kv, k_new=None, v_new=None, window=0,
+               tree_mask=None):
     _lib._need(q, "q", ndim=4)
+    if tree_mask is not None:
+        _lib._need(tree_mask, "tree_mask", torch.int64, 2)  # uint64 bits, held as int64
+        if tuple(tree_mask.shape) != tuple(q.shape[:2]):
+            raise ValueError(f"tree_mask must be [B,T] = {tuple(q.shape[:2])}")
+        fn_name = fn_name.replace("verify_attention", "tree_verify_attention")
     if k_new is not None:
         _lib._need(k_new, "k_new", q.dtype, 4)
         _lib._need(v_new, "v_new", q.dtype, 4)
@@ -82,10 +88,12 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
         _lib._need(workspace, "workspace", torch.uint8)
     L = _lib.lib()
     new = () if k_new is None else (_lib._ptr(k_new), _lib._ptr(v_new))
+    mask = () if tree_mask is None else (_lib._ptr(tree_mask),)
     rc = getattr(L, fn_name)(ctypes.byref(shape), _lib._ptr(q), *new, _lib._ptr(k_cache),
                              _lib._ptr(v_cache), _lib._ptr(block_tables),
-                             _lib._ptr(context_lens), _lib._ptr(out), _lib._ptr(workspace),
-                             workspace.numel(), _status_arg(status), _lib._stream(stream))
+                             _lib._ptr(context_lens), *mask, _lib._ptr(out),
+                             _lib._ptr(workspace), workspace.numel(), _status_arg(status),
+                             _lib._stream(stream))
     _lib._check(fn_name, rc)
     return out
 
@@ -102,10 +110,13 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=Non
 
 def verify_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
                      workspace=None, status=None, stream=None, pdl=False, early_kv=False,
-                     window=0):
-    """gqa_verify_attention (T >= 1, causal among the T new tokens)."""
+                     window=0, tree_mask=None):
+    """gqa_verify_attention (T >= 1, causal among the T new tokens), or with
+    tree_mask (int64 [B,T] holding the uint64 mask rows)
+    gqa_tree_verify_attention."""
     return _attention("gqa_verify_attention", q, k_cache, v_cache, block_tables, context_lens,
-                      out, scale, workspace, status, stream, pdl, early_kv, window=window)
+                      out, scale, workspace, status, stream, pdl, early_kv, window=window,
+                      tree_mask=tree_mask)
 
 
 def append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
@@ -120,11 +131,12 @@ def append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, con
 
 def append_verify_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
                             out=None, scale=None, workspace=None, status=None, stream=None,
-                            pdl=False, early_kv=False, window=0):
-    """gqa_append_verify_attention: kv_append + verify_attention in one launch."""
+                            pdl=False, early_kv=False, window=0, tree_mask=None):
+    """gqa_append_verify_attention: kv_append + verify_attention in one launch
+    (gqa_append_tree_verify_attention with tree_mask)."""
     return _attention("gqa_append_verify_attention", q, k_cache, v_cache, block_tables,
                       context_lens, out, scale, workspace, status, stream, pdl, early_kv,
-                      k_new=k_new, v_new=v_new, window=window)
+                      k_new=k_new, v_new=v_new, window=window, tree_mask=tree_mask)
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,

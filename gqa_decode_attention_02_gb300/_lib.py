@@ -56,7 +56,8 @@ FLAG_EARLY_KV = 2
 EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_attention_workspace_size", "gqa_workspace_clear", "gqa_decode_attention",
            "gqa_verify_attention", "gqa_append_decode_attention", "gqa_append_verify_attention",
-           "gqa_accept_prefix", "gqa_accept_sampled")
+           "gqa_accept_prefix", "gqa_accept_sampled", "gqa_tree_verify_attention",
+           "gqa_append_tree_verify_attention")
 
 
 def lib() -> ctypes.CDLL:
@@ -89,6 +90,10 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = I
             f.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+        L.gqa_tree_verify_attention.restype = I
+        L.gqa_tree_verify_attention.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+        L.gqa_append_tree_verify_attention.restype = I
+        L.gqa_append_tree_verify_attention.argtypes = [S] + [P] * 10 + [ctypes.c_size_t, P, P]
         L.gqa_accept_prefix.restype = I
         L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, P]
         L.gqa_accept_sampled.restype = I

@@ -26,8 +26,9 @@ gqa_status check_common(const gqa_shape* s) {
 gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, const void* q,
                            const void* k_new, const void* v_new, const void* k_cache,
                            const void* v_cache, const int32_t* block_tables,
-                           const int32_t* context_lens, void* out, void* workspace,
-                           size_t ws_bytes, int32_t* dev_status, void* stream) {
+                           const int32_t* context_lens, const uint64_t* tree_mask, void* out,
+                           void* workspace, size_t ws_bytes, int32_t* dev_status,
+                           void* stream) {
     gqa_status st = check_common(s);
     if (st != GQA_OK) return st;
     if (decode_only && s->T != 1) return GQA_ERR_SHAPE;
@@ -38,14 +39,16 @@ gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, con
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return GQA_ERR_ALIGN;
     if (fused && (!aligned16(k_new) || !aligned16(v_new))) return GQA_ERR_ALIGN;
+    if (tree_mask && s->window > 0) return GQA_ERR_SHAPE;  // not combined
+    if (tree_mask && (reinterpret_cast<uintptr_t>(tree_mask) & 7u) != 0) return GQA_ERR_ALIGN;
     gqa::AttnPlan plan;
-    st = gqa::attention_plan(*s, &plan);
+    st = gqa::attention_plan(*s, tree_mask != nullptr, &plan);
     if (st != GQA_OK) return st;
     if (!workspace || ws_bytes < plan.workspace) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_ALIGN;
     return gqa::launch_attention(*s, plan, q, fused ? k_new : nullptr, fused ? v_new : nullptr,
-                                 k_cache, v_cache, block_tables, context_lens, out, workspace,
-                                 dev_status, static_cast<cudaStream_t>(stream));
+                                 k_cache, v_cache, block_tables, context_lens, tree_mask, out,
+                                 workspace, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -87,9 +90,11 @@ gqa_status gqa_kv_append(const gqa_shape* shape, const void* k_new, const void* 
 
 size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     if (check_common(shape) != GQA_OK) return 0;
-    gqa::AttnPlan plan;
-    if (gqa::attention_plan(*shape, &plan) != GQA_OK) return 0;
-    return plan.workspace;
+    // the larger of the two kernel variants' needs (they normally agree)
+    gqa::AttnPlan plain, masked;
+    if (gqa::attention_plan(*shape, false, &plain) != GQA_OK) return 0;
+    if (gqa::attention_plan(*shape, true, &masked) != GQA_OK) return 0;
+    return plain.workspace > masked.workspace ? plain.workspace : masked.workspace;
 }
 
 gqa_status gqa_workspace_clear(void* workspace, size_t bytes, void* stream) {
@@ -105,8 +110,8 @@ gqa_status gqa_decode_attention(const gqa_shape* shape, const void* q, const voi
                                 const int32_t* context_lens, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
     return attention_entry(shape, true, false, q, nullptr, nullptr, k_cache, v_cache,
-                           block_tables, context_lens, out, workspace, workspace_bytes,
-                           dev_status, stream);
+                           block_tables, context_lens, nullptr, out, workspace,
+                           workspace_bytes, dev_status, stream);
 }
 
 gqa_status gqa_verify_attention(const gqa_shape* shape, const void* q, const void* k_cache,
@@ -114,8 +119,8 @@ gqa_status gqa_verify_attention(const gqa_shape* shape, const void* q, const voi
                                 const int32_t* context_lens, void* out, void* workspace,
                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
     return attention_entry(shape, false, false, q, nullptr, nullptr, k_cache, v_cache,
-                           block_tables, context_lens, out, workspace, workspace_bytes,
-                           dev_status, stream);
+                           block_tables, context_lens, nullptr, out, workspace,
+                           workspace_bytes, dev_status, stream);
 }
 
 gqa_status gqa_append_decode_attention(const gqa_shape* shape, const void* q,
@@ -125,7 +130,8 @@ gqa_status gqa_append_decode_attention(const gqa_shape* shape, const void* q,
                                        size_t workspace_bytes, int32_t* dev_status,
                                        void* stream) {
     return attention_entry(shape, true, true, q, k_new, v_new, k_cache, v_cache, block_tables,
-                           context_lens, out, workspace, workspace_bytes, dev_status, stream);
+                           context_lens, nullptr, out, workspace, workspace_bytes, dev_status,
+                           stream);
 }
 
 gqa_status gqa_append_verify_attention(const gqa_shape* shape, const void* q,
@@ -135,7 +141,33 @@ gqa_status gqa_append_verify_attention(const gqa_shape* shape, const void* q,
                                        size_t workspace_bytes, int32_t* dev_status,
                                        void* stream) {
     return attention_entry(shape, false, true, q, k_new, v_new, k_cache, v_cache, block_tables,
-                           context_lens, out, workspace, workspace_bytes, dev_status, stream);
+                           context_lens, nullptr, out, workspace, workspace_bytes, dev_status,
+                           stream);
+}
+
+gqa_status gqa_tree_verify_attention(const gqa_shape* shape, const void* q,
+                                     const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     const uint64_t* tree_mask, void* out, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (!tree_mask) return GQA_ERR_NULL;
+    return attention_entry(shape, false, false, q, nullptr, nullptr, k_cache, v_cache,
+                           block_tables, context_lens, tree_mask, out, workspace,
+                           workspace_bytes, dev_status, stream);
+}
+
+gqa_status gqa_append_tree_verify_attention(const gqa_shape* shape, const void* q,
+                                            const void* k_new, const void* v_new,
+                                            void* k_cache, void* v_cache,
+                                            const int32_t* block_tables,
+                                            const int32_t* context_lens,
+                                            const uint64_t* tree_mask, void* out,
+                                            void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_status, void* stream) {
+    if (!tree_mask) return GQA_ERR_NULL;
+    return attention_entry(shape, false, true, q, k_new, v_new, k_cache, v_cache, block_tables,
+                           context_lens, tree_mask, out, workspace, workspace_bytes, dev_status,
+                           stream);
 }
 
 gqa_status gqa_accept_prefix(int B, int T, int V, const float* target_logits,

@@ -88,6 +88,9 @@ struct AttnParams {
     int groups;    // stage-parallel consumer groups
     int early_kv;  // GQA_FLAG_EARLY_KV: stream old cache blocks before the wait
     int window;    // local attention: each query sees its last `window` positions (0: all)
+    // Tree verification: new token t sees new token j < t only if bit j of
+    // tree_mask[b * T + t] is set (nullptr: the chain, all j < t).
+    const uint64_t* tree_mask;
     // Fused append (k_new != nullptr): the T newest positions are taken from
     // k_new / v_new [B][T][K][H] and written into the caches by this kernel.
     const void* k_new;
@@ -188,12 +191,12 @@ __device__ __forceinline__ void prefetch_q(const AttnParams& p, int b, int k) {
 }
 
 // ---------------------------------------------------------------------------
-template <int H, bool WIN>
+template <int H, bool MASKED>
 __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
                          uint8_t* stages, const Bars& bar, StageMeta* meta,
                          volatile int* abort_flag) {
     using C = Cfg<H>;
-    const int win = WIN ? p.window : 0;  // compile-time 0 for full attention
+    const int win = MASKED ? p.window : 0;  // compile-time 0 for the plain kernel
     constexpr unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
@@ -427,7 +430,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
 // rows 8*(w*NW + u) .. +7 (rows r = t*G + g).  Every K / V fragment it reads
 // from shared memory feeds NW mma, so more rows per warp means fewer warps
 // re-reading the same stage.
-template <int H, bool BF16, int NW, bool WIN>
+template <int H, bool BF16, int NW, bool MASKED>
 struct Consumer {
     using C = Cfg<H>;
     using E = Elt<BF16>;
@@ -535,7 +538,7 @@ struct Consumer {
 
     // One stage: md.ntiles tiles of 16 tokens starting at tile md.blk_i.
     __device__ void stage(uint32_t kbase, const StageMeta& md) {
-        const int win = WIN ? p.window : 0;  // compile-time 0 for full attention
+        const int win = MASKED ? p.window : 0;  // compile-time 0 for the plain kernel
         if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
         const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
         const int ntl = md.ntiles;
@@ -578,17 +581,36 @@ struct Consumer {
                 if (j >= ntl) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[u][j][e] = -INFINITY;
-                } else if (tb + 15 > md.ctx - p.T ||
+                } else if (tb + 15 > md.ctx - p.T - (MASKED && p.tree_mask ? 1 : 0) ||
                            (win > 0 && tb < md.ctx - win)) {
                     // some position hidden from some row: above its causal
-                    // bound lim, or (local attention) at or below lim - window
+                    // bound lim, or (local attention) at or below lim - window,
+                    // or (tree) a new position -- the first new token too
                     const int lim0 = md.ctx - p.T + t0[u], lim1 = md.ctx - p.T + t1[u];
                     const int pos0 = tb + g, pos8 = pos0 + 8;
                     const int wl = win > 0 ? win : (1 << 30);
-                    if (pos0 > lim0 || pos0 <= lim0 - wl) sc[u][j][0] = -INFINITY;
-                    if (pos0 > lim1 || pos0 <= lim1 - wl) sc[u][j][1] = -INFINITY;
-                    if (pos8 > lim0 || pos8 <= lim0 - wl) sc[u][j][2] = -INFINITY;
-                    if (pos8 > lim1 || pos8 <= lim1 - wl) sc[u][j][3] = -INFINITY;
+                    bool h00 = pos0 > lim0 || pos0 <= lim0 - wl;
+                    bool h01 = pos0 > lim1 || pos0 <= lim1 - wl;
+                    bool h80 = pos8 > lim0 || pos8 <= lim0 - wl;
+                    bool h81 = pos8 > lim1 || pos8 <= lim1 - wl;
+                    if (MASKED && p.tree_mask) {
+                        // tree: a new position other than the row's own is
+                        // visible only if the row's mask selects it
+                        const int fn = md.ctx - p.T;
+                        const uint64_t mk0 = __ldg(p.tree_mask + (size_t)cb * p.T + t0[u]);
+                        const uint64_t mk1 = __ldg(p.tree_mask + (size_t)cb * p.T + t1[u]);
+                        auto off = [&](int pos, int lim, uint64_t mk) {
+                            return pos >= fn && pos < lim && !((mk >> (pos - fn)) & 1ull);
+                        };
+                        h00 |= off(pos0, lim0, mk0);
+                        h01 |= off(pos0, lim1, mk1);
+                        h80 |= off(pos8, lim0, mk0);
+                        h81 |= off(pos8, lim1, mk1);
+                    }
+                    if (h00) sc[u][j][0] = -INFINITY;
+                    if (h01) sc[u][j][1] = -INFINITY;
+                    if (h80) sc[u][j][2] = -INFINITY;
+                    if (h81) sc[u][j][3] = -INFINITY;
                 }
                 x0 = fmaxf(x0, fmaxf(sc[u][j][0], sc[u][j][2]));
                 x1 = fmaxf(x1, fmaxf(sc[u][j][1], sc[u][j][3]));
@@ -853,12 +875,12 @@ struct Consumer {
 // 8*(w % nt) .. +7.  Every warp reads every stage's description, so all groups
 // agree on segment boundaries; at each boundary the groups' partial states
 // meet in shared memory and group 0 finishes the segment.
-template <int H, bool BF16, int NW, bool WIN>
+template <int H, bool BF16, int NW, bool MASKED>
 __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
                          const StageMeta* meta, float* scratch, volatile int* abort_flag,
                          int w) {
     using C = Cfg<H>;
-    using CS = Consumer<H, BF16, NW, WIN>;
+    using CS = Consumer<H, BF16, NW, MASKED>;
     const int gi = w / p.nt, wr = w % p.nt;
     CS cs(p, wr);
     const int lane = threadIdx.x & 31;
@@ -925,8 +947,9 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
 
 // NW = 1: up to 6 row warps per group; NW = 2 (two 8-row tiles per warp, for
 // many query rows) up to 3, with the register budget of the smaller CTA.
-// WIN: local attention (the window arithmetic is compiled out without it).
-template <int H, bool BF16, int NW, bool WIN>
+// MASKED: local attention or a tree mask (the extra masking is compiled out of
+// the plain kernel).
+template <int H, bool BF16, int NW, bool MASKED>
 __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRowWarps / 2 + 1))
     attention_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -960,25 +983,25 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
     }
     __syncthreads();
     if (warp == consumers)
-        producer<H, WIN>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
+        producer<H, MASKED>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
     else
-        consumer<H, BF16, NW, WIN>(p, stages, bar, meta, scratch, abort_flag, warp);
+        consumer<H, BF16, NW, MASKED>(p, stages, bar, meta, scratch, abort_flag, warp);
 }
 
 // ---------------------------------------------------------------------------
 // Host side
-// The instantiated variants: (nw, window) in {(1, no), (1, yes), (2, no)} for
+// The instantiated variants: (nw, masked) in {(1, no), (1, yes), (2, no)} for
 // each head size and dtype.
 template <int H, bool BF16>
-const void* kernel_ptr(int nw, bool win) {
+const void* kernel_ptr(int nw, bool masked) {
     if (nw == 2) return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 2, false>);
-    return win ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true>)
+    return masked ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true>)
                : reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false>);
 }
 
-const void* pick_kernel(int H, bool bf16, int nw, bool win) {
-    if (H == 64) return bf16 ? kernel_ptr<64, true>(nw, win) : kernel_ptr<64, false>(nw, win);
-    return bf16 ? kernel_ptr<128, true>(nw, win) : kernel_ptr<128, false>(nw, win);
+const void* pick_kernel(int H, bool bf16, int nw, bool masked) {
+    if (H == 64) return bf16 ? kernel_ptr<64, true>(nw, masked) : kernel_ptr<64, false>(nw, masked);
+    return bf16 ? kernel_ptr<128, true>(nw, masked) : kernel_ptr<128, false>(nw, masked);
 }
 
 // Consumer groups for nt row warps.  (A third group was measured slower on
@@ -1040,16 +1063,16 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
 // CTAs of one variant resident per SM, queried once per (device, variant) so
 // that later calls -- including calls being captured into a CUDA graph -- make
 // no attribute or occupancy API calls.
-int resident_ctas(int H, bool bf16, int nt, int nw, bool win, size_t smem) {
+int resident_ctas(int H, bool bf16, int nt, int nw, bool masked, size_t smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw * 2 + (int)win);
+    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw * 2 + (int)masked);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void* kern = pick_kernel(H, bf16, nw, win);
+    const void* kern = pick_kernel(H, bf16, nw, masked);
     // The attribute belongs to the kernel, whatever the row-warp count: set it
     // to the largest launch any shape makes.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1078,7 +1101,7 @@ int device_sm_count() {
     return n;
 }
 
-gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
+gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     if (s.B < 0 || s.T < 1 || s.N < 1 || s.K < 1 || s.N % s.K != 0) return GQA_ERR_SHAPE;
     if (s.H != 64 && s.H != 128) return GQA_ERR_SHAPE;
     if (s.block_size != 16 || s.num_blocks < 1 || s.max_blocks_per_seq < 1) return GQA_ERR_SHAPE;
@@ -1098,7 +1121,8 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     const int threads = 32 * (groups * nt + 1);
     int stages = default_stages(s.H);
     size_t smem = smem_for(s.H, nt, nw, stages);
-    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, s.window > 0, smem);
+    masked = masked || s.window > 0;
+    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, masked, smem);
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
@@ -1120,6 +1144,7 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
     plan->stages = stages;
     plan->groups = groups;
     plan->tiles_per_warp = nw;
+    plan->masked = masked;
     // The publication flags live in a fixed region at the start of every
     // workspace, whatever the shape, and partial results always start after
     // it: partial data of one call can then never sit where a later call of
@@ -1134,8 +1159,8 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan) {
 gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
                             const void* k_new, const void* v_new, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables,
-                            const int32_t* context_lens, void* out, void* workspace,
-                            int32_t* dev_status, cudaStream_t stream) {
+                            const int32_t* context_lens, const uint64_t* tree_mask, void* out,
+                            void* workspace, int32_t* dev_status, cudaStream_t stream) {
     if (s.B == 0) return GQA_OK;
     CUtensorMap tmk, tmv;
     if (!encode_cache_map(&tmk, k_cache, s) || !encode_cache_map(&tmv, v_cache, s))
@@ -1163,6 +1188,7 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     p.scale_log2 = (float)(scale * 1.4426950408889634);  // log2(e)
     p.early_kv = (s.flags & GQA_FLAG_EARLY_KV) ? 1 : 0;
     p.window = s.window;
+    p.tree_mask = tree_mask;
     p.k_new = k_new;
     p.v_new = v_new;
     p.k_cache = const_cast<void*>(k_cache);
@@ -1180,7 +1206,8 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     const int nw = plan.tiles_per_warp;
-    const void* kern = pick_kernel(s.H, bf16, nw, s.window > 0);
+    if ((tree_mask || s.window > 0) && !plan.masked) return GQA_ERR_SHAPE;  // plan mismatch
+    const void* kern = pick_kernel(s.H, bf16, nw, plan.masked);
     void* args[] = {&tmk, &tmv, &p};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;

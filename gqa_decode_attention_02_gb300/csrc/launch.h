@@ -18,13 +18,15 @@ struct AttnPlan {
     int stages;          // depth of the shared-memory ring
     int groups;          // stage-parallel consumer groups
     int tiles_per_warp;  // 8-row query tiles per consumer warp (1 or 2)
+    bool masked;         // the kernel variant with window / tree masking
     size_t flags_bytes;             // fixed region of publication flags
     size_t partial_floats_per_cta;
     size_t workspace;    // total bytes
 };
 
-// Fills `plan`; returns GQA_OK or a validation error.
-gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan);
+// Fills `plan` for the plain kernel or (masked) the one that also handles a
+// window or a tree mask; returns GQA_OK or a validation error.
+gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan);
 
 // k_new / v_new == nullptr: attention over the cache as it is; otherwise the
 // T newest tokens are appended from them by the same launch (the caches are
@@ -32,8 +34,8 @@ gqa_status attention_plan(const gqa_shape& s, AttnPlan* plan);
 gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
                             const void* k_new, const void* v_new, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables,
-                            const int32_t* context_lens, void* out, void* workspace,
-                            int32_t* dev_status, cudaStream_t stream);
+                            const int32_t* context_lens, const uint64_t* tree_mask, void* out,
+                            void* workspace, int32_t* dev_status, cudaStream_t stream);
 
 gqa_status launch_kv_append(const gqa_shape& s, const void* k_new, const void* v_new,
                             void* k_cache, void* v_cache, const int32_t* block_tables,

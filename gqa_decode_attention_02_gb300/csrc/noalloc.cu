@@ -62,7 +62,7 @@ extern "C" gqa_status gqa_decode_attention_noalloc(const gqa_shape* shape, const
     if (need == 0) return GQA_ERR_SHAPE;
     if (need > kScratchBytes) return GQA_ERR_WORKSPACE;  // beyond the fixed 8 MiB
     gqa::AttnPlan plan;
-    const gqa_status st = gqa::attention_plan(*shape, &plan);
+    const gqa_status st = gqa::attention_plan(*shape, false, &plan);
     if (st != GQA_OK) return st;
     void* scratch = nullptr;
     const gqa_status ss = scratch_on_current_device(&scratch);

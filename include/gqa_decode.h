@@ -6,6 +6,7 @@
  *   gqa_kv_append        write the T newest tokens' keys and values into the cache
  *   gqa_decode_attention attention of one new query token per sequence (T == 1)
  *   gqa_verify_attention the same for T >= 1 new tokens, causal among them
+ *   gqa_tree_verify_attention  the same with a tree mask among the new tokens
  *   gqa_accept_prefix    greedy longest-prefix acceptance of draft tokens
  *   gqa_accept_sampled   stochastic acceptance of draft tokens (speculative
  *                        sampling: modified rejection sampling)
@@ -239,6 +240,35 @@ gqa_status gqa_append_verify_attention(const gqa_shape *shape, const void *q,
                                        const int32_t *context_lens, void *out, void *workspace,
                                        size_t workspace_bytes, int32_t *dev_status,
                                        void *stream);
+
+/* Tree verification: verify_attention with a custom mask among the T new
+ * tokens.  "Болжау арқылы Sonar модельдерін жылдамдату" §"EAGLE": drafts form a
+ * tree (Top-K candidates at each node) and the target model verifies the
+ * tree's sequences with a custom attention mask (which, applied to the whole
+ * sequence, the page reports slowing attention by up to 50 %).  Here the mask
+ * only concerns the new tokens:
+ *   tree_mask  uint64 [B][T], 8-byte aligned: new token t sees the whole
+ *              prefix (positions < context_lens[b] - T), itself, and new token
+ *              j < t iff bit j of tree_mask[b][t] is set -- for a tree laid out
+ *              in topological order, its ancestors.  Bits j >= t are ignored;
+ *              the chain mask (bits 0..t-1 set) gives gqa_verify_attention.
+ * Requirements, layouts, workspace and device errors as gqa_verify_attention;
+ * shape->window must be 0.  The _append_ form fuses gqa_kv_append as
+ * gqa_append_verify_attention does. */
+gqa_status gqa_tree_verify_attention(const gqa_shape *shape, const void *q,
+                                     const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables,
+                                     const int32_t *context_lens, const uint64_t *tree_mask,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     int32_t *dev_status, void *stream);
+gqa_status gqa_append_tree_verify_attention(const gqa_shape *shape, const void *q,
+                                            const void *k_new, const void *v_new,
+                                            void *k_cache, void *v_cache,
+                                            const int32_t *block_tables,
+                                            const int32_t *context_lens,
+                                            const uint64_t *tree_mask, void *out,
+                                            void *workspace, size_t workspace_bytes,
+                                            int32_t *dev_status, void *stream);
 
 /* Greedy prefix acceptance.  Speculative-decoding section of "جعل inference
  * رخيصًا" (a drafted token is kept only if the target would produce it) and

@@ -439,3 +439,113 @@ def test_window_of_int_max_is_full_attention(gpu):
                               wd.context_lens, window=2**31 - 1)
     torch.cuda.synchronize()
     assert_close(out.float().cpu().double().numpy(), ref, "f16", "window INT_MAX")
+
+
+# ---- tree verification ---------------------------------------------------------------
+def tree_mask_rows(parents):
+    T = len(parents)
+    m = np.zeros(T, np.uint64)
+    for t in range(T):
+        a = parents[t]
+        while a >= 0:
+            m[t] |= np.uint64(1) << np.uint64(a)
+            a = parents[a]
+    return m
+
+
+def random_trees(B, T, seed):
+    """Per sequence a random tree in topological order (parent < child, -1 =
+    child of the prefix)."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for _ in range(B):
+        parents = [-1] + [int(rng.integers(-1, t)) for t in range(1, T)]
+        rows.append(tree_mask_rows(parents))
+    return np.stack(rows)
+
+
+def as_i64(mask):
+    return torch.from_numpy(mask.view(np.int64).copy())
+
+
+@pytest.mark.parametrize("T,N,K,H,dtype", [(6, 64, 8, 128, "bf16"), (5, 16, 2, 64, "f16"),
+                                           (4, 14, 2, 64, "f16"), (2, 8, 8, 128, "bf16")])
+def test_tree_verify_matches_oracle(gpu, T, N, K, H, dtype):
+    ctx = (T, T + 1, 16, 17, 33, 300, 1029, 4100)
+    w = small(B=len(ctx), T=T, N=N, K=K, H=H, dtype=dtype, ctx=ctx, seed=7 * T + N)
+    m = random_trees(len(ctx), T, seed=T)
+    ref, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                                w.context_lens, dtype, tree_mask=m)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    out = gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                              wd.context_lens, tree_mask=as_i64(m).to(gpu))
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, dtype, f"tree T={T} N={N} K={K}")
+
+
+def test_tree_chain_mask_is_bit_identical_to_verify(gpu):
+    T = 5
+    ctx = (T, 40, 700, 3000)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=51)
+    chain = np.tile(np.array([(1 << t) - 1 for t in range(T)], np.uint64), (len(ctx), 1))
+    junk = chain | np.tile(np.array([~np.uint64(0) << np.uint64(t) for t in range(T)],
+                                    np.uint64), (len(ctx), 1))
+    wd = to(w, gpu)
+    args = (wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables, wd.context_lens)
+    plain = gq.verify_attention(*args)
+    tree = gq.verify_attention(*args, tree_mask=as_i64(chain).to(gpu))
+    tree_junk = gq.verify_attention(*args, tree_mask=as_i64(junk).to(gpu))
+    torch.cuda.synchronize()
+    assert torch.equal(plain, tree)
+    assert torch.equal(plain, tree_junk)  # bits at or after the row are ignored
+
+
+def test_tree_fused_append_matches_oracle(gpu):
+    T = 6
+    ctx = (T, 70, 333, 2000)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=52, append=True)
+    m = random_trees(len(ctx), T, seed=9)
+    kc, vc, _ = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                 w.block_tables, w.context_lens)
+    kt = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16)
+    vt = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16)
+    ref, err = oracle.attention(w.q[0], kt, vt, w.block_tables, w.context_lens, "bf16",
+                                tree_mask=m)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    out = gq.append_verify_attention(wd.q[0], wd.k_new[0], wd.v_new[0], wd.k_cache[0],
+                                     wd.v_cache[0], wd.block_tables, wd.context_lens,
+                                     tree_mask=as_i64(m).to(gpu))
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", "fused tree")
+    np.testing.assert_array_equal(wd.v_cache[0].cpu().view(torch.int16).numpy().view(np.uint16),
+                                  vc)
+
+
+def test_tree_mask_with_window_is_rejected(gpu):
+    w = small(B=2, T=3, N=8, K=2, H=64, ctx=(5, 40), seed=53)
+    wd = to(w, gpu)
+    m = as_i64(random_trees(2, 3, 1)).to(gpu)
+    with pytest.raises(gq.GqaError):
+        gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                            wd.context_lens, tree_mask=m, window=16)
+
+
+@pytest.mark.parametrize("first_new", [15, 16, 31, 1023])
+def test_tree_first_new_token_at_a_tile_edge(gpu, first_new):
+    """Rows that do not descend from new token 0 must not see it, also when
+    it is the last position of a tile."""
+    T = 4
+    ctx = (first_new + T,) * 3
+    w = small(B=3, T=T, N=16, K=2, H=64, dtype="f16", ctx=ctx, seed=first_new)
+    m = np.zeros((3, T), np.uint64)  # every node a root: prefix + itself only
+    m[1] = tree_mask_rows([-1, -1, 1, 2])
+    m[2] = tree_mask_rows([-1, 0, 0, 0])
+    ref, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "f16", tree_mask=m)
+    wd = to(w, gpu)
+    out = gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                              wd.context_lens, tree_mask=as_i64(m).to(gpu))
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, "f16", f"tree edge {first_new}")
