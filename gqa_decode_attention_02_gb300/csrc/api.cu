@@ -91,10 +91,10 @@ gqa_status gqa_kv_append(const gqa_shape* shape, const void* k_new, const void* 
 size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     if (check_common(shape) != GQA_OK) return 0;
     // the larger of the two kernel variants' needs (they normally agree)
-    gqa::AttnPlan plain, masked;
+    gqa::AttnPlan plain, general;
     if (gqa::attention_plan(*shape, false, &plain) != GQA_OK) return 0;
-    if (gqa::attention_plan(*shape, true, &masked) != GQA_OK) return 0;
-    return plain.workspace > masked.workspace ? plain.workspace : masked.workspace;
+    if (gqa::attention_plan(*shape, true, &general) != GQA_OK) return 0;
+    return plain.workspace > general.workspace ? plain.workspace : general.workspace;
 }
 
 gqa_status gqa_workspace_clear(void* workspace, size_t bytes, void* stream) {

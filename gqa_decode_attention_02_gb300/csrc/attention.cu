@@ -64,7 +64,8 @@
 namespace gqa {
 namespace {
 
-constexpr int kMaxRowWarps = 6;            // rows T*G <= 48
+constexpr int kMaxRowWarps = 6;            // query rows per chunk <= 48
+constexpr long long kMaxRows = 8192;       // T*G: above 48 the rows go in chunks
 constexpr int kGroups = 2;                 // stage-parallel consumer groups (default)
 constexpr int kMaxThreads = 32 * (kGroups * kMaxRowWarps + 1);
 constexpr int kEnd = 1, kBad = 2;
@@ -82,6 +83,10 @@ struct AttnParams {
     int32_t* flags;  // one per (CTA, row warp): piece published
     int32_t* status;
     int B, T, N, K, G, R, nt;  // nt: row warps per consumer group
+    // Row chunks: the R = T*G query rows of a KV head are split into C chunks
+    // of Rc rows; the pair (KV head k, chunk c) is the virtual head k*C + c,
+    // KC = K*C of them, each its own segment over the same cache blocks.
+    int C, Rc, KC;
     int max_blocks, num_blocks;
     float scale_log2;
     int stages;    // depth of the shared-memory ring
@@ -191,12 +196,14 @@ __device__ __forceinline__ void prefetch_q(const AttnParams& p, int b, int k) {
 }
 
 // ---------------------------------------------------------------------------
-template <int H, bool MASKED>
+template <int H, bool GENERAL>
 __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
                          uint8_t* stages, const Bars& bar, StageMeta* meta,
                          volatile int* abort_flag) {
     using C = Cfg<H>;
-    const int win = MASKED ? p.window : 0;  // compile-time 0 for the plain kernel
+    const int win = GENERAL ? p.window : 0;  // compile-time 0 for the plain kernel
+    const int nC = GENERAL ? p.C : 1;        // row chunks (1 in the plain kernel)
+    const int nKC = GENERAL ? p.KC : p.K;    // virtual heads
     constexpr unsigned FULL = 0xffffffffu;
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
@@ -242,26 +249,27 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         if (lane >= o) incl += v;
     }
     const int excl = incl - local;
-    const long long total = (long long)p.K * __shfl_sync(FULL, incl, 31);
+    const long long total = (long long)nKC * __shfl_sync(FULL, incl, 31);
     const int quota = max((int)((total + gridDim.x - 1) / gridDim.x), kQuotaMin);
     const long long c0 = (long long)blockIdx.x * quota;
     const long long c1 = min(total, c0 + quota);
-    const uint64_t pol = policy_evict_first();
+    // Chunked rows read every block once per chunk: keep them in L2 then.
+    const uint64_t pol = nC > 1 ? policy_evict_normal() : policy_evict_first();
 
     int it = 0;  // stages issued
     bool aborted = false;
     if (c0 < c1) {
         // 2. Locate tile c0: the lane whose run of sequences contains it.
-        const bool mine = (long long)p.K * excl <= c0 && c0 < (long long)p.K * incl;
+        const bool mine = (long long)nKC * excl <= c0 && c0 < (long long)nKC * incl;
         const unsigned owners = __ballot_sync(FULL, mine);
         const int owner = __ffs(owners) - 1;
         int fb = 0;
         long long fbase = 0;
         if (lane == owner) {
-            long long acc = (long long)p.K * excl;
+            long long acc = (long long)nKC * excl;
             for (int b = lo; b < hi; ++b) {
                 const long long n =
-                    (long long)p.K * seq_blocks(p.context_lens[b], p.T, p.max_blocks, win);
+                    (long long)nKC * seq_blocks(p.context_lens[b], p.T, p.max_blocks, win);
                 if (c0 < acc + n) {
                     fb = b;
                     fbase = acc;
@@ -283,6 +291,9 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         int f0 = first_block(ctx, p.T, win);  // tile i is logical block f0 + i
         const int rel = (int)(c0 - base);
         int k = rel / nblk, i = rel % nblk;
+        // KV head of virtual head k, kept incrementally (the issue path of
+        // this warp is on the critical path: no division per stage)
+        int kv = k / nC, kc = k - kv * nC;
         int ids = 0, ids_base = -(1 << 30);
         auto next_ids = [&](int bn) {
             const int cn = (bn < p.B) ? __shfl_sync(FULL, ctxw, min(bn - cbase, 31)) : 0;
@@ -292,7 +303,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             return (lane < nn) ? __ldg(p.block_tables + (size_t)bn * p.max_blocks + fn + lane) : 0;
         };
         int ids_next = next_ids(b + 1);
-        if (lane == 0) prefetch_q<H>(p, b, k);
+        if (lane == 0) prefetch_q<H>(p, b, GENERAL ? kv : k);
         bool next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);  // ids_next is b+1's
 
         // 3. Stream the range, one stage (up to four tiles of a segment) at a time.
@@ -355,10 +366,11 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
 #pragma unroll
                                 for (int hh = 0; hh < C::kHalves; ++hh) {
                                     tma_load_3d(dst + j * C::kTileBytes + hh * 2048, tmk, fb_,
-                                                hh * 64, k, blk[j] * 16, pol);
+                                                hh * 64, GENERAL ? kv : k, blk[j] * 16, pol);
                                     tma_load_3d(dst + (kTilesPerStage + j) * C::kTileBytes +
                                                     hh * 2048,
-                                                tmv, fb_, hh * 64, k, blk[j] * 16, pol);
+                                                tmv, fb_, hh * 64, GENERAL ? kv : k, blk[j] * 16,
+                                                pol);
                                 }
                             }
                         }
@@ -373,9 +385,14 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             if (i == nblk) {
                 i = 0;
                 const bool more = x < c1;
-                if (++k == p.K) {
+                if (GENERAL && ++kc == nC) {
+                    kc = 0;
+                    ++kv;
+                }
+                if (++k == nKC) {
                     k = 0;
-                    base += (long long)p.K * nblk;
+                    kv = 0;
+                    base += (long long)nKC * nblk;
                     ids_base = -(1 << 30);
                     if (x < c1) {
                         const int b_prev = b;
@@ -397,7 +414,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                         next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);
                     }
                 }
-                if (more && lane == 0) prefetch_q<H>(p, b, k);  // the next segment's q
+                if (more && lane == 0) prefetch_q<H>(p, b, GENERAL ? kv : k);  // next segment's q
             }
         }
     }
@@ -430,7 +447,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
 // rows 8*(w*NW + u) .. +7 (rows r = t*G + g).  Every K / V fragment it reads
 // from shared memory feeds NW mma, so more rows per warp means fewer warps
 // re-reading the same stage.
-template <int H, bool BF16, int NW, bool MASKED>
+template <int H, bool BF16, int NW, bool GENERAL>
 struct Consumer {
     using C = Cfg<H>;
     using E = Elt<BF16>;
@@ -444,11 +461,12 @@ struct Consumer {
     float m0[NW], m1[NW], l0[NW], l1[NW];
     bool bad;
     int cb, ck, cstart, cnblk, cquota, ccta0;
+    int rbase, rend;  // query rows [rbase, rend) of the current chunk
 
-    __device__ int row0(int u) const { return 8 * (w * NW + u); }
+    __device__ int row0(int u) const { return (GENERAL ? rbase : 0) + 8 * (w * NW + u); }
+    __device__ int row_end() const { return GENERAL ? rend : p.R; }
 
-    __device__ Consumer(const AttnParams& p_, int w_)
-        : p(p_), w(w_), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), q4(threadIdx.x & 3) {
+    __device__ void set_row_tokens() {
 #pragma unroll
         for (int u = 0; u < NW; ++u) {
             const int r0 = row0(u) + 2 * q4;
@@ -457,12 +475,25 @@ struct Consumer {
         }
     }
 
+    __device__ Consumer(const AttnParams& p_, int w_)
+        : p(p_), w(w_), lane(threadIdx.x & 31), g((threadIdx.x & 31) >> 2), q4(threadIdx.x & 3),
+          rbase(0), rend(0) {
+        if (!GENERAL) set_row_tokens();  // one chunk: the rows never change
+    }
+
     // Start segment (b, k): reset the running state and fetch the B fragments
     // of Q^T (k = head dim, n = query row): row row0(u)+g, dims kk*16 + 2*q4 +
     // {0,1} and the same + 8.  The loads complete while the stage's tiles land.
     __device__ void begin(const StageMeta& md) {
         cb = md.b;
-        ck = md.k;
+        if (GENERAL) {  // md.k is the virtual head (KV head, row chunk)
+            ck = md.k / p.C;
+            rbase = (md.k - ck * p.C) * p.Rc;
+            rend = min(p.R, rbase + p.Rc);
+            set_row_tokens();
+        } else {
+            ck = md.k;
+        }
         cstart = md.seg_start;
         cnblk = md.nblk;
         cquota = md.quota;
@@ -477,7 +508,7 @@ struct Consumer {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[u][mt][e] = 0.f;
             const int r = row0(u) + g;
-            if (r < p.R) {
+            if (r < row_end()) {
                 const int t = r / p.G, gg = r % p.G;
                 const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                     static_cast<const uint16_t*>(p.q) +
@@ -520,7 +551,7 @@ struct Consumer {
                     const uint32_t dst = (is_v ? vbase : kbase) + j * C::kTileBytes +
                                          (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
                     st_shared_v4(dst, val);
-                    if (w == 0) {
+                    if (w == 0 && (!GENERAL || rbase == 0)) {  // one writer: row chunk 0
                         uint4* cache = static_cast<uint4*>(is_v ? p.v_cache : p.k_cache);
                         cache[(((size_t)md.blk[j] * 16 + r) * p.K + ck) * kChunks + c] = val;
                     }
@@ -538,7 +569,7 @@ struct Consumer {
 
     // One stage: md.ntiles tiles of 16 tokens starting at tile md.blk_i.
     __device__ void stage(uint32_t kbase, const StageMeta& md) {
-        const int win = MASKED ? p.window : 0;  // compile-time 0 for the plain kernel
+        const int win = GENERAL ? p.window : 0;  // compile-time 0 for the plain kernel
         if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
         const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
         const int ntl = md.ntiles;
@@ -581,7 +612,7 @@ struct Consumer {
                 if (j >= ntl) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[u][j][e] = -INFINITY;
-                } else if (tb + 15 > md.ctx - p.T - (MASKED && p.tree_mask ? 1 : 0) ||
+                } else if (tb + 15 > md.ctx - p.T - (GENERAL && p.tree_mask ? 1 : 0) ||
                            (win > 0 && tb < md.ctx - win)) {
                     // some position hidden from some row: above its causal
                     // bound lim, or (local attention) at or below lim - window,
@@ -593,7 +624,7 @@ struct Consumer {
                     bool h01 = pos0 > lim1 || pos0 <= lim1 - wl;
                     bool h80 = pos8 > lim0 || pos8 <= lim0 - wl;
                     bool h81 = pos8 > lim1 || pos8 <= lim1 - wl;
-                    if (MASKED && p.tree_mask) {
+                    if (GENERAL && p.tree_mask) {
                         // tree: a new position other than the row's own is
                         // visible only if the row's mask selects it
                         const int fn = md.ctx - p.T;
@@ -698,7 +729,7 @@ struct Consumer {
         const float i1 = (!is_bad && L1 > 0.f) ? 1.f / L1 : 0.f;
         const int r = row0(u) + g;
         uint32_t* dst = nullptr;
-        if (r < p.R) {
+        if (r < row_end()) {
             const int t = r / p.G, gg = r % p.G;
             dst = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) +
                                               (((size_t)cb * p.T + t) * p.N +
@@ -875,12 +906,12 @@ struct Consumer {
 // 8*(w % nt) .. +7.  Every warp reads every stage's description, so all groups
 // agree on segment boundaries; at each boundary the groups' partial states
 // meet in shared memory and group 0 finishes the segment.
-template <int H, bool BF16, int NW, bool MASKED>
+template <int H, bool BF16, int NW, bool GENERAL>
 __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
                          const StageMeta* meta, float* scratch, volatile int* abort_flag,
                          int w) {
     using C = Cfg<H>;
-    using CS = Consumer<H, BF16, NW, MASKED>;
+    using CS = Consumer<H, BF16, NW, GENERAL>;
     const int gi = w / p.nt, wr = w % p.nt;
     CS cs(p, wr);
     const int lane = threadIdx.x & 31;
@@ -924,7 +955,7 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
             if (cur >= 0) close();
             return;
         }
-        const int seg = md.b * p.K + md.k;
+        const int seg = md.b * (GENERAL ? p.KC : p.K) + md.k;
         if (seg != cur) {
             if (cur >= 0 && !close()) return;
             cs.begin(md);
@@ -947,9 +978,9 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
 
 // NW = 1: up to 6 row warps per group; NW = 2 (two 8-row tiles per warp, for
 // many query rows) up to 3, with the register budget of the smaller CTA.
-// MASKED: local attention or a tree mask (the extra masking is compiled out of
-// the plain kernel).
-template <int H, bool BF16, int NW, bool MASKED>
+// GENERAL: local attention, a tree mask or row chunks (all compiled out of the
+// plain kernel, which then runs with no window, the chain mask and one chunk).
+template <int H, bool BF16, int NW, bool GENERAL>
 __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRowWarps / 2 + 1))
     attention_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -983,25 +1014,25 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
     }
     __syncthreads();
     if (warp == consumers)
-        producer<H, MASKED>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
+        producer<H, GENERAL>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
     else
-        consumer<H, BF16, NW, MASKED>(p, stages, bar, meta, scratch, abort_flag, warp);
+        consumer<H, BF16, NW, GENERAL>(p, stages, bar, meta, scratch, abort_flag, warp);
 }
 
 // ---------------------------------------------------------------------------
 // Host side
-// The instantiated variants: (nw, masked) in {(1, no), (1, yes), (2, no)} for
+// The instantiated variants: (nw, general) in {(1, no), (1, yes), (2, no)} for
 // each head size and dtype.
 template <int H, bool BF16>
-const void* kernel_ptr(int nw, bool masked) {
+const void* kernel_ptr(int nw, bool general) {
     if (nw == 2) return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 2, false>);
-    return masked ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true>)
+    return general ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true>)
                : reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false>);
 }
 
-const void* pick_kernel(int H, bool bf16, int nw, bool masked) {
-    if (H == 64) return bf16 ? kernel_ptr<64, true>(nw, masked) : kernel_ptr<64, false>(nw, masked);
-    return bf16 ? kernel_ptr<128, true>(nw, masked) : kernel_ptr<128, false>(nw, masked);
+const void* pick_kernel(int H, bool bf16, int nw, bool general) {
+    if (H == 64) return bf16 ? kernel_ptr<64, true>(nw, general) : kernel_ptr<64, false>(nw, general);
+    return bf16 ? kernel_ptr<128, true>(nw, general) : kernel_ptr<128, false>(nw, general);
 }
 
 // Consumer groups for nt row warps.  (A third group was measured slower on
@@ -1063,16 +1094,16 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
 // CTAs of one variant resident per SM, queried once per (device, variant) so
 // that later calls -- including calls being captured into a CUDA graph -- make
 // no attribute or occupancy API calls.
-int resident_ctas(int H, bool bf16, int nt, int nw, bool masked, size_t smem) {
+int resident_ctas(int H, bool bf16, int nt, int nw, bool general, size_t smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw * 2 + (int)masked);
+    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw * 2 + (int)general);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void* kern = pick_kernel(H, bf16, nw, masked);
+    const void* kern = pick_kernel(H, bf16, nw, general);
     // The attribute belongs to the kernel, whatever the row-warp count: set it
     // to the largest launch any shape makes.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1102,6 +1133,7 @@ int device_sm_count() {
 }
 
 gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
+    // masked: a tree mask will be passed (the general kernel variant)
     if (s.B < 0 || s.T < 1 || s.N < 1 || s.K < 1 || s.N % s.K != 0) return GQA_ERR_SHAPE;
     if (s.H != 64 && s.H != 128) return GQA_ERR_SHAPE;
     if (s.block_size != 16 || s.num_blocks < 1 || s.max_blocks_per_seq < 1) return GQA_ERR_SHAPE;
@@ -1111,18 +1143,21 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     if (s.window < 0) return GQA_ERR_SHAPE;
     const int G = s.N / s.K;
     const long long R = (long long)s.T * G;
-    if (R > 8 * kMaxRowWarps) return GQA_ERR_SHAPE;
+    if (R > kMaxRows) return GQA_ERR_SHAPE;
+    // Row chunks of at most 48 rows, as even as multiples of 8 allow.
+    const int chunks = (int)((R + 8 * kMaxRowWarps - 1) / (8 * kMaxRowWarps));
+    const int rows_per_chunk = (int)(((R + chunks - 1) / chunks + 7) / 8 * 8);
     // One 8-row tile per warp.  (Two tiles per warp -- each K/V fragment read
     // from shared memory serving 16 rows -- measured slower on the 40-row verify
     // workload: fewer warps hide less latency.  The kernel keeps both forms.)
     const int nw = 1;
-    const int nt = (int)((R + 8 * nw - 1) / (8 * nw));
+    const int nt = (rows_per_chunk + 8 * nw - 1) / (8 * nw);
     const int groups = groups_for(nt);
     const int threads = 32 * (groups * nt + 1);
     int stages = default_stages(s.H);
     size_t smem = smem_for(s.H, nt, nw, stages);
-    masked = masked || s.window > 0;
-    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, masked, smem);
+    const bool general = masked || s.window > 0 || chunks > 1;
+    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, general, smem);
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
@@ -1133,7 +1168,7 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     long long blocks_max = s.max_blocks_per_seq;  // per sequence, window included
     if (s.window > 0)
         blocks_max = std::min<long long>(blocks_max, ((long long)s.window + s.T + 14) / 16 + 1);
-    const long long tiles_max = (long long)s.B * s.K * blocks_max;
+    const long long tiles_max = (long long)s.B * s.K * chunks * blocks_max;
     if (tiles_max <= 256ll * sms) occ = 1;
     long long grid = (long long)sms * occ;
     grid = std::min<long long>(grid, std::max<long long>(1, (tiles_max + kQuotaMin - 1) / kQuotaMin));
@@ -1144,7 +1179,9 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     plan->stages = stages;
     plan->groups = groups;
     plan->tiles_per_warp = nw;
-    plan->masked = masked;
+    plan->general = general;
+    plan->chunks = chunks;
+    plan->rows_per_chunk = rows_per_chunk;
     // The publication flags live in a fixed region at the start of every
     // workspace, whatever the shape, and partial results always start after
     // it: partial data of one call can then never sit where a later call of
@@ -1179,6 +1216,9 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     p.K = s.K;
     p.G = s.N / s.K;
     p.R = s.T * p.G;
+    p.C = plan.chunks;
+    p.Rc = plan.rows_per_chunk;
+    p.KC = s.K * plan.chunks;
     p.nt = plan.consumer_warps;
     p.stages = plan.stages;
     p.groups = plan.groups;
@@ -1206,8 +1246,9 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     const int nw = plan.tiles_per_warp;
-    if ((tree_mask || s.window > 0) && !plan.masked) return GQA_ERR_SHAPE;  // plan mismatch
-    const void* kern = pick_kernel(s.H, bf16, nw, plan.masked);
+    if ((tree_mask || s.window > 0 || plan.chunks > 1) && !plan.general)
+        return GQA_ERR_SHAPE;  // plan made for another call
+    const void* kern = pick_kernel(s.H, bf16, nw, plan.general);
     void* args[] = {&tmk, &tmv, &p};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;

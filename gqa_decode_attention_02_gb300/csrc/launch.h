@@ -18,14 +18,17 @@ struct AttnPlan {
     int stages;          // depth of the shared-memory ring
     int groups;          // stage-parallel consumer groups
     int tiles_per_warp;  // 8-row query tiles per consumer warp (1 or 2)
-    bool masked;         // the kernel variant with window / tree masking
+    bool general;        // the kernel variant with window, tree mask and row chunks
+    int chunks;          // row chunks per KV head (T*G rows, at most 48 per chunk)
+    int rows_per_chunk;
     size_t flags_bytes;             // fixed region of publication flags
     size_t partial_floats_per_cta;
     size_t workspace;    // total bytes
 };
 
-// Fills `plan` for the plain kernel or (masked) the one that also handles a
-// window or a tree mask; returns GQA_OK or a validation error.
+// Fills `plan`; `masked`: a tree mask will be passed.  The plan picks the plain
+// kernel or the general one (window, tree mask, row chunks).  Returns GQA_OK
+// or a validation error.
 gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan);
 
 // k_new / v_new == nullptr: attention over the cache as it is; otherwise the

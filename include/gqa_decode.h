@@ -169,7 +169,7 @@ gqa_status gqa_workspace_clear(void *workspace, size_t bytes, void *stream);
  * split across thread blocks and the pieces merged with their log-sum-exp
  * weights (FlashDecoding, named in §"PagedAttention"); the result equals the
  * unsplit softmax up to rounding.  Requires: T == 1, N % K == 0, H in {64,128},
- * block_size == 16, N/K <= 48, a workspace of at least
+ * block_size == 16, N/K <= 8192, a workspace of at least
  * gqa_attention_workspace_size(shape) bytes (zeroed, see above).  Device
  * errors: a sequence whose context length is < 1, < T or above
  * 16*max_blocks_per_seq (GQA_ERR_CONTEXT) or whose table holds a block id
@@ -208,7 +208,10 @@ gqa_status gqa_decode_attention_noalloc(const gqa_shape *shape, const void *q,
  * CS336 lecture 10 §"Спекулятивное сэмплирование" -- the target model scores
  * several drafted tokens in one pass).  As gqa_decode_attention, except that
  * new token t (t < T) sees cached positions j <= context_lens[b] - T + t: the
- * whole prefix plus the new tokens up to itself.  Requires T * (N/K) <= 48. */
+ * whole prefix plus the new tokens up to itself.  Requires T * (N/K) <= 8192.
+ * The T*(N/K) query rows of a KV head are processed in chunks of at most 48
+ * rows (one per consumer warp and 8 rows); beyond 48 rows every chunk reads
+ * the KV head's blocks again, from L2 when they are still there. */
 gqa_status gqa_verify_attention(const gqa_shape *shape, const void *q,
                                 const void *k_cache, const void *v_cache,
                                 const int32_t *block_tables,

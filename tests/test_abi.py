@@ -51,7 +51,7 @@ def _shape(**kw):
     (dict(block_size=32), 2),  # only 16-token blocks
     (dict(T=0), 2),
     (dict(dtype=5), 3),
-    (dict(N=98, K=2), 2),      # 49 rows per KV head > 48
+    (dict(N=2 * 8193, K=2), 2),  # 8193 query rows per KV head > 8192
 ])
 def test_validation_rejects_bad_shapes(cuda_lib, kw, code):
     s = _shape(**kw)

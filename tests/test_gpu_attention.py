@@ -549,3 +549,63 @@ def test_tree_first_new_token_at_a_tile_edge(gpu, first_new):
                               wd.context_lens, tree_mask=as_i64(m).to(gpu))
     torch.cuda.synchronize()
     assert_close(out.float().cpu().double().numpy(), ref, "f16", f"tree edge {first_new}")
+
+
+# ---- more than 48 query rows per KV head: row chunks ---------------------------------
+@pytest.mark.parametrize("N,K,H,dtype", [(64, 1, 128, "bf16"), (56, 1, 64, "f16"),
+                                         (128, 2, 128, "bf16"), (49, 1, 64, "f16")])
+def test_decode_many_query_heads_per_kv_head(gpu, N, K, H, dtype):
+    ctx = (1, 15, 16, 17, 300, 2049)
+    w = small(B=len(ctx), T=1, N=N, K=K, H=H, dtype=dtype, ctx=ctx, seed=N + K)
+    ref, err = oracle_out(w)
+    assert (err == 0).all()
+    assert_close(run_attention(w, gpu), ref, dtype, f"decode G={N // K}")
+
+
+@pytest.mark.parametrize("T,N,K", [(8, 64, 8), (26, 64, 8), (64, 4, 4), (7, 56, 8)])
+def test_verify_more_than_48_rows(gpu, T, N, K):
+    ctx = (T, T + 3, 100, 1500)
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype="bf16", ctx=ctx, seed=T * N)
+    ref, err = oracle_out(w)
+    assert (err == 0).all()
+    assert_close(run_attention(w, gpu), ref, "bf16", f"verify T={T} G={N // K}")
+
+
+def test_tree_verify_26_node_tree(gpu):
+    """An EAGLE-sized tree (26 nodes: a root, then 3, 6, 8, 8 nodes per level)
+    with 8 query heads per KV head: 208 rows in five chunks."""
+    parents = [-1, 0, 0, 0, 1, 1, 2, 2, 3, 3] + [4 + i // 2 for i in range(8)] + \
+              [10 + i for i in range(8)]
+    T = len(parents)
+    assert T == 26
+    ctx = (T, 40, 1000, 3000)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=26)
+    m = np.tile(tree_mask_rows(parents), (len(ctx), 1))
+    ref, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                                w.context_lens, "bf16", tree_mask=m)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    out = gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables,
+                              wd.context_lens, tree_mask=as_i64(m).to(gpu))
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", "26-node tree")
+
+
+def test_fused_append_with_row_chunks_writes_the_cache_once(gpu):
+    T = 8
+    ctx = (T, 70, 900)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=88, append=True)
+    kc, vc, _ = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                 w.block_tables, w.context_lens)
+    kt = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16)
+    vt = torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16)
+    ref, _ = oracle.attention(w.q[0], kt, vt, w.block_tables, w.context_lens, "bf16")
+    wd = to(w, gpu)
+    out = gq.append_verify_attention(wd.q[0], wd.k_new[0], wd.v_new[0], wd.k_cache[0],
+                                     wd.v_cache[0], wd.block_tables, wd.context_lens)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", "fused, 64 rows")
+    np.testing.assert_array_equal(wd.k_cache[0].cpu().view(torch.int16).numpy().view(np.uint16),
+                                  kc)
+    np.testing.assert_array_equal(wd.v_cache[0].cpu().view(torch.int16).numpy().view(np.uint16),
+                                  vc)
