@@ -48,7 +48,7 @@ def parse_args():
     # Default: the workload the metric's bandwidth target is quoted on -- the
     # long-context ragged batch (B=256, log-normal contexts, 3.5 GB per step).
     ap.add_argument("--workload", default="cfg4",
-                    choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "hybrid"])
+                    choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "hybrid", "tree"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
@@ -229,7 +229,8 @@ def oracle_sample(w, budget_s):
         for s0 in range(0, w.B, 8):
             bl = np.arange(s0, min(w.B, s0 + 8), dtype=np.int32)
             t0 = time.perf_counter()
-            oracle.attention(q, kc, vc, tables, lens, w.dtype, b_list=bl, window=w.window(layer))
+            oracle.attention(q, kc, vc, tables, lens, w.dtype, b_list=bl, window=w.window(layer),
+                             tree_mask=w.tree_mask())
             spent += time.perf_counter() - t0
             done_bytes += A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2,
                                                         window=w.window(layer))
@@ -246,6 +247,7 @@ def oracle_sample(w, budget_s):
 
 # ---- our arm -----------------------------------------------------------------------------
 def run_ours(args, world, rank, local):
+    import numpy as np
     import torch
 
     import __graft_entry__
@@ -287,6 +289,10 @@ def run_ours(args, world, rank, local):
         sin = workloads.sampling_inputs(w.B, w.T, V, seed=workloads.SPECS[args.workload]["seed"]
                                         + 1000, device=dev)
 
+    tm = w.tree_mask()
+    tree_t = None if tm is None else torch.from_numpy(tm.view(np.int64)).to(dev)
+    extra = {} if tree_t is None else {"tree_mask": tree_t}
+
     def do_append():
         if w.appended and not fused:
             for l in range(L):
@@ -301,11 +307,11 @@ def run_ours(args, world, rank, local):
             if fused:
                 fused_fn(w.q[l], w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
                          w.block_tables, w.context_lens, out=outs[l], workspace=ws, status=st,
-                         pdl=True, early_kv=True, window=w.window(l))
+                         pdl=True, early_kv=True, window=w.window(l), **extra)
             else:
                 attn_fn(w.q[l], w.k_cache[l], w.v_cache[l], w.block_tables, w.context_lens,
                         out=outs[l], workspace=ws, status=st, pdl=True, early_kv=True,
-                        window=w.window(l))
+                        window=w.window(l), **extra)
 
     def do_acc():
         if sampled:
@@ -380,6 +386,33 @@ def run_ours(args, world, rank, local):
     acc_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / K
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())} in the timed region")
+
+    # Tree verification: the same launches with the plain chain mask, for the
+    # cost of the custom mask (the speculation blog reports up to 50 % for a
+    # mask over the whole sequence).
+    tree_rec = None
+    if tree_t is not None:
+        g_chain = torch.cuda.CUDAGraph()
+        saved = dict(extra)
+        extra.clear()
+        with torch.cuda.graph(g_chain):
+            do_attn()
+        extra.update(saved)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for _ in range(args.warmup):
+            refresh()
+            g_chain.replay()
+        for i in range(K):
+            refresh()
+            ev[i][0].record()
+            g_chain.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        chain_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+        tree_rec = {"nodes": w.T, "parents": list(w.tree), "tree_attention_us": round(
+            attn_ms * 1e3 / L, 3), "chain_attention_us": round(chain_ms * 1e3 / L, 3),
+            "tree_over_chain": round(attn_ms / chain_ms, 4)}
 
     attn_b, app_b, acc_b = step_bytes(w)
     if sampled:
@@ -503,6 +536,7 @@ def run_ours(args, world, rank, local):
                      "traffic": traffic,
                      "algorithmic_bytes_per_launch": kernel_b,
                      "avg_launch_us": round(attn_launch_ms * 1e3, 3)},
+        "tree_verify": tree_rec,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "e2e_eager": e2e_eager,
@@ -547,7 +581,7 @@ def run_reference(args, world, rank, local):
         bl = np.arange(s0, min(w.B, s0 + chunk), dtype=np.int32)
         t0 = time.perf_counter()
         oracle.attention(q, kc, vc, w.block_tables, w.context_lens, w.dtype, b_list=bl,
-                         window=w.window(l))
+                         window=w.window(l), tree_mask=w.tree_mask())
         dt = time.perf_counter() - t0
         if i >= W:
             times.append(dt)

@@ -63,9 +63,22 @@ class Workload:
     draft_k: Optional[np.ndarray] = None  # planted accepted-prefix length per b
     desc: str = ""
     windows: tuple = ()  # per layer: local-attention window, 0 = global (all 0 if empty)
+    tree: tuple = ()  # draft tree over the T new tokens: parent of each (-1: the prefix)
 
     def window(self, layer: int) -> int:
         return self.windows[layer] if self.windows else 0
+
+    def tree_mask(self) -> Optional[np.ndarray]:
+        """uint64 [B,T] mask rows of the draft tree (bit j of row t: new token
+        t's ancestor j), the same tree for every sequence; None without a tree."""
+        if not self.tree:
+            return None
+        rows = np.zeros(self.T, np.uint64)
+        for t, a in enumerate(self.tree):
+            while a >= 0:
+                rows[t] |= np.uint64(1) << np.uint64(a)
+                a = self.tree[a]
+        return np.tile(rows, (self.B, 1))
 
     @property
     def G(self) -> int:
@@ -107,7 +120,7 @@ def build(name: str, B: int, T: int, N: int, K: int, H: int, dtype: str,
           ctx: np.ndarray, *, seed: int, layers: int = 1, shuffle: bool = True,
           append: bool = True, spare_blocks: int = 1, block_size: int = BLOCK_SIZE,
           max_blocks: Optional[int] = None, device="cpu", vocab: int = 0,
-          desc: str = "", windows: tuple = ()) -> Workload:
+          desc: str = "", windows: tuple = (), tree: tuple = ()) -> Workload:
     """Lay out a paged block pool for the given context lengths and fill it.
 
     Physical blocks: sum_b ceil(ctx_b / bs) in use plus `spare_blocks` never
@@ -166,7 +179,7 @@ def build(name: str, B: int, T: int, N: int, K: int, H: int, dtype: str,
                  context_lens=torch.as_tensor(ctx.astype(np.int32), device=device),
                  block_tables=torch.as_tensor(tables.astype(np.int32), device=device),
                  q=qs, k_cache=kcs, v_cache=vcs, k_new=kns, v_new=vns,
-                 appended=append, desc=desc, windows=tuple(windows))
+                 appended=append, desc=desc, windows=tuple(windows), tree=tuple(tree))
     if vocab:
         logits = torch.randn((B, T, vocab), generator=gen, dtype=torch.float32,
                              device=device)
@@ -225,6 +238,15 @@ SPECS = {
              "context 8192 (8191 cached + 1 appended), shuffled blocks",
         B=32, T=1, N=32, K=8, H=128, dtype="bf16", layers=6, shuffle=True,
         append=True, ctx=("fixed", 8192), seed=106, windows=(1024,) * 5 + (0,)),
+    # Not one of the five: tree verification of a 26-node draft tree (a root,
+    # then 3, 6, 8 and 8 candidates per level) on the verify geometry.
+    "tree": dict(
+        desc="tree verify, B=16, T=26 (draft tree: 1 root, 3, 6, 8, 8 nodes per level), "
+             "N=64, K=8, H=128, bf16, context U[512,4096], custom mask among the new tokens",
+        B=16, T=26, N=64, K=8, H=128, dtype="bf16", layers=1, shuffle=True,
+        append=True, ctx=("uniform", 512, 4096), seed=107,
+        tree=(-1, 0, 0, 0, 1, 1, 2, 2, 3, 3) + tuple(4 + i // 2 for i in range(8))
+        + tuple(10 + i for i in range(8))),
 }
 
 

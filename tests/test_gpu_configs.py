@@ -40,8 +40,11 @@ def check_workload(name, dev, sample=None, layers=None, fused=False):
         else:
             okc, ovc = kc, vc
         win = w.window(layer)
+        tm = w.tree_mask()
+        extra = {} if tm is None else {
+            "tree_mask": torch.from_numpy(tm.view(np.int64)).to(dev)}
         ref, err = oracle.attention(w.q[layer], okc, ovc, w.block_tables, w.context_lens,
-                                    w.dtype, b_list=bl, window=win)
+                                    w.dtype, b_list=bl, window=win, tree_mask=tm)
         assert (err == 0).all()
         kd, vd = kc.to(dev), vc.to(dev)
         bt, cl = w.block_tables.to(dev), w.context_lens.to(dev)
@@ -50,7 +53,7 @@ def check_workload(name, dev, sample=None, layers=None, fused=False):
         if w.appended and fused:  # the append inside the attention launch (the bench's call)
             ffn = gq.append_decode_attention if w.T == 1 else gq.append_verify_attention
             out = ffn(w.q[layer].to(dev), w.k_new[layer].to(dev), w.v_new[layer].to(dev), kd, vd,
-                      bt, cl, status=st, pdl=True, early_kv=True, window=win)
+                      bt, cl, status=st, pdl=True, early_kv=True, window=win, **extra)
         elif w.appended:
             gq.kv_append(w.k_new[layer].to(dev), w.v_new[layer].to(dev), kd, vd, bt, cl,
                          status=st)
@@ -64,7 +67,7 @@ def check_workload(name, dev, sample=None, layers=None, fused=False):
                                           ovc[blocks].view(torch.int16).numpy())
         if out is None:
             fn = gq.decode_attention if w.T == 1 else gq.verify_attention
-            out = fn(w.q[layer].to(dev), kd, vd, bt, cl, status=st, window=win)
+            out = fn(w.q[layer].to(dev), kd, vd, bt, cl, status=st, window=win, **extra)
         torch.cuda.synchronize()
         assert int(st.item()) == 0
         got = out.cpu()[torch.as_tensor(bl).long()].double().numpy()
@@ -114,3 +117,11 @@ def test_hybrid_local_global_layers(gpu, fused):
     on the long-context geometry, through the bench's calls."""
     w, _ = check_workload("hybrid", gpu, sample=8, fused=fused)
     assert w.windows == (1024,) * 5 + (0,)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_tree_verify_workload(gpu, fused):
+    """The 26-node draft tree on the verify geometry (208 query rows per KV
+    head, five row chunks), through the bench's calls."""
+    w, _ = check_workload("tree", gpu, fused=fused)
+    assert w.T == 26 and len(w.tree) == 26
