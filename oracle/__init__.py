@@ -1,5 +1,5 @@
 """fp64 CPU oracle for paged GQA decode/verify attention, KV append, greedy
-prefix acceptance and speculative sampling.
+prefix acceptance, speculative sampling and the one-byte (int8 / e4m3) KV cache.
 
 TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the bench's CPU
 baseline leg may import this package; the product path never does.  It shares no
@@ -10,6 +10,10 @@ from .oracle import (  # noqa: F401
     f16_to_f64,
     bf16_to_f64,
     kv_append,
+    kv_append_quant,
+    quantize_row,
+    e4m3_to_f64,
+    e4m3_from_float,
     attention,
     accept_prefix,
     accept_sampled,

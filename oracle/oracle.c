@@ -105,6 +105,135 @@ int oracle_kv_append(int B, int T, int K, int H, int block_size, int num_blocks,
     return any;
 }
 
+/* ---- quantized KV cache ----------------------------------------------------
+ * [KV-AR], quantization section: symmetric absolute-maximum quantization --
+ * qmax = 2^(bits-1) - 1, scale = max|W| / qmax, codes round(W / scale) clamped
+ * to [-qmax-1, qmax], reconstruction codes * scale -- and fewer bytes per
+ * element make every memory-bound decode step faster.  [CS336-RU]
+ * §"Квантование": fp8 (e4m3) and int8 are the one-byte formats.
+ *
+ * Readings:
+ *   - The rule is applied to every cached vector (one key or value row of one
+ *     KV head, H elements), its fp32 scale stored per block as
+ *     scale[block][kv head][row]: the append writes one token at a time, and a
+ *     scale over a whole block would change as the block fills.
+ *   - int8: qmax = 127.  e4m3 (OCP FP8 E4M3, finite max 448 -- the page's
+ *     "[-240, 240]" is the range of another e4m3 variant): scale = max|W| / 448
+ *     and the code is x / scale rounded to the nearest e4m3 value, ties to
+ *     even, saturating at +-448.
+ *   - The codes are integers decided in floating point, so they are computed in
+ *     fp32 as the kernel does: max|W| of the widened elements, then scale =
+ *     max / qmax and x / scale as IEEE fp32 divisions, ties to even.  A row of
+ *     zeros has scale 0 and all codes 0. */
+#define ORACLE_KV_INT8 1
+#define ORACLE_KV_E4M3 2
+
+/* e4m3 code (sign | 4-bit exponent, bias 7 | 3-bit mantissa) nearest to x,
+ * ties to even, saturating at +-448 (no infinities; 0x7f / 0xff are NaN). */
+static uint8_t e4m3_encode(float xf) {
+    double x = (double)xf;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x)) return 0x7f;
+    double v = fabs(x);
+    if (v >= 448.0) return sign | 0x7e; /* saturate (448 itself is 0x7e) */
+    if (v == 0.0) return sign;
+    int e;
+    (void)frexp(v, &e); /* v = f * 2^e, f in [0.5, 1) */
+    int E = e - 1;      /* v in [2^E, 2^(E+1)) */
+    if (E < -6) E = -6; /* subnormals: spacing 2^-9, like the lowest binade */
+    double m = ldexp(v, 3 - E); /* v / 2^(E-3), exact */
+    int mi = (int)nearbyint(m); /* ties to even under the default rounding */
+    if (mi >= 16) {             /* rounded up into the next binade */
+        mi = 8;
+        E += 1;
+    }
+    if (mi < 8) return sign | (uint8_t)mi; /* subnormal (E == -6) */
+    int field = E + 7;
+    if (field > 15 || (field == 15 && mi - 8 > 6)) return sign | 0x7e;
+    return sign | (uint8_t)(field << 3) | (uint8_t)(mi - 8);
+}
+
+/* value of an e4m3 code (NaN for 0x7f / 0xff) */
+double oracle_e4m3_to_f64(uint8_t c) {
+    int field = (c >> 3) & 15, m = c & 7;
+    double s = (c & 0x80) ? -1.0 : 1.0;
+    if (field == 15 && m == 7) return NAN;
+    if (field == 0) return s * ldexp((double)m, -9);
+    return s * ldexp(8.0 + m, field - 10);
+}
+
+uint8_t oracle_e4m3_from_float(float x) { return e4m3_encode(x); }
+
+/* Quantize one row of n elements (fp16/bf16 bits) to one-byte codes. */
+void oracle_quantize_row(const uint16_t *x, int n, int dtype, int kind, uint8_t *codes,
+                         float *scale_out) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf((float)widen(x[i], dtype));
+        if (a > amax) amax = a;
+    }
+    const float qmax = kind == ORACLE_KV_INT8 ? 127.0f : 448.0f;
+    volatile float scale = amax / qmax; /* one fp32 division */
+    *scale_out = scale;
+    for (int i = 0; i < n; ++i) {
+        if (scale == 0.0f) {
+            codes[i] = 0;
+            continue;
+        }
+        volatile float y = (float)widen(x[i], dtype) / scale; /* one fp32 division */
+        if (kind == ORACLE_KV_INT8) {
+            float r = nearbyintf(y);
+            if (r > 127.0f) r = 127.0f;
+            if (r < -128.0f) r = -128.0f;
+            codes[i] = (uint8_t)(int8_t)(int)r;
+        } else {
+            codes[i] = e4m3_encode(y);
+        }
+    }
+}
+
+static double code_value(uint8_t c, int kind) {
+    return kind == ORACLE_KV_INT8 ? (double)(int8_t)c : oracle_e4m3_to_f64(c);
+}
+
+/* Quantized append: as oracle_kv_append, but each new key / value row of each
+ * KV head is quantized on its way into the one-byte caches [NB][bs][K][H]; its
+ * scale goes to k_scale / v_scale [NB][K][bs]. */
+int oracle_kv_append_quant(int B, int T, int K, int H, int block_size, int num_blocks,
+                           int max_blocks, int dtype, int kind, const uint16_t *k_new,
+                           const uint16_t *v_new, uint8_t *k_cache, uint8_t *v_cache,
+                           float *k_scale, float *v_scale, const int32_t *block_tables,
+                           const int32_t *context_lens, int32_t *seq_err) {
+    int any = 0;
+    for (int b = 0; b < B; ++b) {
+        int ctx = context_lens[b];
+        if (seq_err) seq_err[b] = 0;
+        if (ctx < T || ctx > (long long)max_blocks * block_size) {
+            if (seq_err) seq_err[b] = ORACLE_ERR_CONTEXT;
+            any = 1;
+            continue;
+        }
+        for (int t = 0; t < T; ++t) {
+            int pos = ctx - T + t;
+            int blk = block_tables[(size_t)b * max_blocks + pos / block_size];
+            if (blk < 0 || blk >= num_blocks) {
+                if (seq_err && !seq_err[b]) seq_err[b] = ORACLE_ERR_BLOCK_ID;
+                any = 1;
+                continue;
+            }
+            int row = pos % block_size;
+            for (int k = 0; k < K; ++k) {
+                size_t src = (((size_t)b * T + t) * K + k) * H;
+                size_t dst = (((size_t)blk * block_size + row) * K + k) * H;
+                size_t sc = ((size_t)blk * K + k) * block_size + row;
+                oracle_quantize_row(k_new + src, H, dtype, kind, k_cache + dst, &k_scale[sc]);
+                oracle_quantize_row(v_new + src, H, dtype, kind, v_cache + dst, &v_scale[sc]);
+            }
+        }
+    }
+    return any;
+}
+
 /* ---- attention -------------------------------------------------------------
  * [CS336-RU] §"Арифметическая интенсивность инференса" (attention layer: scores
  * A = Q K^T, Y = softmax(A) V) and §"Уменьшаем KV-кэш" (GQA: N query heads, K
@@ -137,8 +266,9 @@ int oracle_kv_append(int B, int T, int K, int H, int block_size, int num_blocks,
  * block id gets an all-zero output and a nonzero seq_err[i]. */
 int oracle_attention(int B, int T, int N, int K, int H, int block_size,
                      int num_blocks, int max_blocks, int dtype, double scale,
-                     int window, const uint64_t *tree_mask, const uint16_t *q, const uint16_t *k_cache,
-                     const uint16_t *v_cache, const int32_t *block_tables,
+                     int window, const uint64_t *tree_mask, int kv_kind,
+                     const float *k_scale, const float *v_scale, const uint16_t *q,
+                     const void *k_cache, const void *v_cache, const int32_t *block_tables,
                      const int32_t *context_lens, const int32_t *b_list, int nb,
                      double *out, int32_t *seq_err, int nthreads) {
     if (K <= 0 || N % K != 0 || window < 0 || (window > 0 && tree_mask)) return -1;
@@ -207,10 +337,16 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
         for (int j = first; j <= last; ++j) {
             if (!VISIBLE(j)) continue;
             int blk = block_tables[(size_t)b * max_blocks + j / block_size];
-            const uint16_t *kr =
-                k_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;
+            const size_t off = (((size_t)blk * block_size + j % block_size) * K + kh) * H;
             double acc = 0.0;
-            for (int h = 0; h < H; ++h) acc += qd[h] * widen(kr[h], dtype);
+            if (kv_kind) { /* one-byte codes times the row's scale */
+                const uint8_t *kr = (const uint8_t *)k_cache + off;
+                const double sc = k_scale[((size_t)blk * K + kh) * block_size + j % block_size];
+                for (int h = 0; h < H; ++h) acc += qd[h] * (code_value(kr[h], kv_kind) * sc);
+            } else {
+                const uint16_t *kr = (const uint16_t *)k_cache + off;
+                for (int h = 0; h < H; ++h) acc += qd[h] * widen(kr[h], dtype);
+            }
             s[j] = scale * acc;
             if (s[j] > smax) smax = s[j];
         }
@@ -225,10 +361,16 @@ int oracle_attention(int B, int T, int N, int K, int H, int block_size,
         for (int j = first; j <= last; ++j) {
             if (!VISIBLE(j)) continue;
             int blk = block_tables[(size_t)b * max_blocks + j / block_size];
-            const uint16_t *vr =
-                v_cache + (((size_t)blk * block_size + j % block_size) * K + kh) * H;
+            const size_t off = (((size_t)blk * block_size + j % block_size) * K + kh) * H;
             double p = s[j] / denom;
-            for (int h = 0; h < H; ++h) o[h] += p * widen(vr[h], dtype);
+            if (kv_kind) {
+                const uint8_t *vr = (const uint8_t *)v_cache + off;
+                const double sc = v_scale[((size_t)blk * K + kh) * block_size + j % block_size];
+                for (int h = 0; h < H; ++h) o[h] += p * (code_value(vr[h], kv_kind) * sc);
+            } else {
+                const uint16_t *vr = (const uint16_t *)v_cache + off;
+                for (int h = 0; h < H; ++h) o[h] += p * widen(vr[h], dtype);
+            }
         }
         free(qd);
         free(s);

@@ -51,7 +51,16 @@ def _get():
             lib.oracle_kv_append.restype = i
             lib.oracle_kv_append.argtypes = [i] * 7 + [P] * 7
             lib.oracle_attention.restype = i
-            lib.oracle_attention.argtypes = [i] * 9 + [ctypes.c_double, i] + [P] * 7 + [i, P, P, i]
+            lib.oracle_attention.argtypes = ([i] * 9 + [ctypes.c_double, i, P, i] + [P] * 8
+                                             + [i, P, P, i])
+            lib.oracle_quantize_row.restype = None
+            lib.oracle_quantize_row.argtypes = [P, i, i, i, P, P]
+            lib.oracle_kv_append_quant.restype = i
+            lib.oracle_kv_append_quant.argtypes = [i] * 9 + [P] * 8 + [P]
+            lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+            lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
             lib.oracle_accept_prefix.restype = None
             lib.oracle_accept_prefix.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_accept_sampled.restype = None
@@ -116,13 +125,27 @@ def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens):
     return kc, vc, err
 
 
+KV_KINDS = {"int8": 1, "e4m3": 2}
+
+
 def attention(q, k_cache, v_cache, block_tables, context_lens, dtype, scale=0.0,
-              b_list=None, nthreads=0, window=0, tree_mask=None):
+              b_list=None, nthreads=0, window=0, tree_mask=None, kv=None, k_scale=None,
+              v_scale=None):
     """fp64 paged GQA attention.  q [B,T,N,H]; caches [NB,bs,K,H]; window > 0
     limits query position i to positions i-window+1 .. i; tree_mask [B,T]
     (uint64) lets new token t see new token j < t only if bit j is set.
+    kv = "int8" / "e4m3": the caches hold one-byte codes (uint8 [NB,bs,K,H]) and
+    k_scale / v_scale fp32 [NB,K,bs] their row scales.
     Returns (out [nb,T,N,H] float64, seq_err [nb]) for the listed sequences."""
-    qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+    qb = _bits(q)
+    if kv is None:
+        kc, vc = _bits(k_cache), _bits(v_cache)
+        ks = vs = None
+    else:
+        kc = np.ascontiguousarray(_u8(k_cache))
+        vc = np.ascontiguousarray(_u8(v_cache))
+        ks = np.ascontiguousarray(_f32(k_scale))
+        vs = np.ascontiguousarray(_f32(v_scale))
     bt, cl = _i32(block_tables), _i32(context_lens)
     B, T, N, H = qb.shape
     NB, bs, K, H2 = kc.shape
@@ -135,8 +158,9 @@ def attention(q, k_cache, v_cache, block_tables, context_lens, dtype, scale=0.0,
     if tree_mask is not None:
         tm = np.ascontiguousarray(np.asarray(tree_mask).astype(np.uint64)).reshape(B, T)
     rc = _get().oracle_attention(B, T, N, K, H, bs, NB, bt.shape[1], _DT[dtype],
-                                 float(scale), int(window), _p(tm), _p(qb), _p(kc), _p(vc),
-                                 _p(bt), _p(cl),
+                                 float(scale), int(window), _p(tm),
+                                 0 if kv is None else KV_KINDS[kv], _p(ks), _p(vs), _p(qb),
+                                 _p(kc), _p(vc), _p(bt), _p(cl),
                                  _p(bl), nb, _p(out), _p(err), int(nthreads))
     if rc < 0:
         raise ValueError("oracle_attention: N must be a multiple of K, window >= 0, and a "
@@ -157,6 +181,54 @@ def accept_prefix(logits, draft, context_lens=None):
     cl = None if context_lens is None else _i32(context_lens).copy()
     _get().oracle_accept_prefix(B, T, V, _p(lg), _p(dr), _p(acc), _p(nxt), _p(cl))
     return acc, nxt, cl
+
+
+def _u8(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.asarray(a).view(np.uint8) if np.asarray(a).dtype == np.int8 else np.asarray(
+        a, dtype=np.uint8)
+
+
+def _f32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.asarray(a, dtype=np.float32)
+
+
+def quantize_row(x, dtype, kv):
+    """One-byte codes (uint8) and the fp32 scale of one fp16/bf16 row."""
+    xb = np.ascontiguousarray(_bits(x)).reshape(-1)
+    codes = np.zeros(xb.size, np.uint8)
+    sc = np.zeros(1, np.float32)
+    _get().oracle_quantize_row(_p(xb), xb.size, _DT[dtype], KV_KINDS[kv], _p(codes), _p(sc))
+    return codes, float(sc[0])
+
+
+def e4m3_to_f64(code: int) -> float:
+    return _get().oracle_e4m3_to_f64(int(code))
+
+
+def e4m3_from_float(x: float) -> int:
+    return int(_get().oracle_e4m3_from_float(float(x)))
+
+
+def kv_append_quant(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+                    context_lens, dtype, kv):
+    """Quantized append into copies of the one-byte caches uint8 [NB,bs,K,H] and
+    their scales fp32 [NB,K,bs].  Returns (k_cache', v_cache', k_scale',
+    v_scale', seq_err)."""
+    kn, vn = _bits(k_new), _bits(v_new)
+    kc, vc = _u8(k_cache).copy(), _u8(v_cache).copy()
+    ks, vs = _f32(k_scale).copy(), _f32(v_scale).copy()
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    B, T, K, H = kn.shape
+    NB, bs = kc.shape[0], kc.shape[1]
+    err = np.zeros(max(B, 1), np.int32)
+    _get().oracle_kv_append_quant(B, T, K, H, bs, NB, bt.shape[1], _DT[dtype], KV_KINDS[kv],
+                                  _p(kn), _p(vn), _p(kc), _p(vc), _p(ks), _p(vs), _p(bt),
+                                  _p(cl), _p(err))
+    return kc, vc, ks, vs, err[:B]
 
 
 def accept_sampled(q, p, draft, u, context_lens=None):
