@@ -10,6 +10,8 @@ CUDA kernels; calling any op without the built library raises.
     append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens)
     append_verify_attention(...)  (kv_append fused into the attention launch)
     (every attention call takes window=W > 0 for local attention)
+    kv_append_quant / decode_attention_quant / verify_attention_quant: the same
+    over a one-byte (int8 or e4m3) cache with per-row fp32 scales
     accept_prefix(target_logits, draft_ids, context_lens=None) -> (accepted, next)
     accept_sampled(target_probs, draft_probs, draft_ids, uniforms,
                    context_lens=None) -> (accepted, next)
@@ -23,7 +25,8 @@ import torch
 from . import _lib
 from ._lib import GqaError, Shape, Status, status_string  # noqa: F401
 
-__all__ = ["kv_append", "decode_attention", "verify_attention", "append_decode_attention",
+__all__ = ["kv_append", "kv_append_quant", "decode_attention", "verify_attention",
+           "decode_attention_quant", "verify_attention_quant", "append_decode_attention",
            "append_verify_attention", "accept_prefix", "accept_sampled",
            "attention_workspace_size", "GqaError", "Status", "Shape"]
 
@@ -51,6 +54,40 @@ def kv_append(k_new, v_new, k_cache, v_cache, block_tables, context_lens, *, sta
                                   _lib._ptr(block_tables), _lib._ptr(context_lens),
                                   _status_arg(status), _lib._stream(stream))
     _lib._check("gqa_kv_append", rc)
+
+
+_BYTE_DTYPES = (torch.uint8, torch.int8, torch.float8_e4m3fn)
+
+
+def _need_quant_cache(cache, scale, name):
+    if not isinstance(cache, torch.Tensor) or cache.dtype not in _BYTE_DTYPES:
+        raise ValueError(f"{name} must be a one-byte tensor (uint8 / int8 / float8_e4m3fn)")
+    _lib._need(cache, name, ndim=4)
+    _lib._need(scale, name + " scale", torch.float32, 3)
+    NB, bs, K, _ = cache.shape
+    if tuple(scale.shape) != (NB, K, bs):
+        raise ValueError(f"{name} scale must be [{NB},{K},{bs}], got {tuple(scale.shape)}")
+
+
+def kv_append_quant(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+                    context_lens, *, kv="int8", status=None, stream=None, pdl=False):
+    """gqa_kv_append_quant: quantize k_new / v_new [B,T,K,H] (fp16 / bf16) row
+    by row into one-byte caches [NB,16,K,H] and their scales fp32 [NB,K,16]."""
+    _lib._need(k_new, "k_new", ndim=4)
+    _lib._need(v_new, "v_new", k_new.dtype, 4)
+    _need_quant_cache(k_cache, k_scale, "k_cache")
+    _need_quant_cache(v_cache, v_scale, "v_cache")
+    _lib._need(block_tables, "block_tables", torch.int32, 2)
+    _lib._need(context_lens, "context_lens", torch.int32, 1)
+    shape = _lib.make_shape(k_new, k_cache, block_tables, None, heads_dim=3,
+                            flags=_lib.FLAG_PDL if pdl else 0, kv=kv)
+    rc = _lib.lib().gqa_kv_append_quant(ctypes.byref(shape), _lib._ptr(k_new),
+                                        _lib._ptr(v_new), _lib._ptr(k_cache),
+                                        _lib._ptr(v_cache), _lib._ptr(k_scale),
+                                        _lib._ptr(v_scale), _lib._ptr(block_tables),
+                                        _lib._ptr(context_lens), _status_arg(status),
+                                        _lib._stream(stream))
+    _lib._check("gqa_kv_append_quant", rc)
 
 
 def attention_workspace_size(q, k_cache, block_tables, scale=None, window=0) -> int:
@@ -137,6 +174,52 @@ def append_verify_attention(q, k_new, v_new, k_cache, v_cache, block_tables, con
     return _attention("gqa_append_verify_attention", q, k_cache, v_cache, block_tables,
                       context_lens, out, scale, workspace, status, stream, pdl, early_kv,
                       k_new=k_new, v_new=v_new, window=window, tree_mask=tree_mask)
+
+
+def _attention_quant(fn_name, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                     context_lens, out, scale, workspace, status, stream, pdl, early_kv, kv):
+    _lib._need(q, "q", ndim=4)
+    _need_quant_cache(k_cache, k_scale, "k_cache")
+    _need_quant_cache(v_cache, v_scale, "v_cache")
+    _lib._need(block_tables, "block_tables", torch.int32, 2)
+    _lib._need(context_lens, "context_lens", torch.int32, 1)
+    flags = (_lib.FLAG_PDL if pdl else 0) | (_lib.FLAG_EARLY_KV if early_kv else 0)
+    shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags, kv=kv)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _lib._need(out, "out", q.dtype, 4)
+    nbytes = _lib.workspace_size(shape)
+    if workspace is None:
+        workspace = _lib.get_workspace(nbytes, q.device)
+    else:
+        _lib._need(workspace, "workspace", torch.uint8)
+    rc = getattr(_lib.lib(), fn_name)(ctypes.byref(shape), _lib._ptr(q), _lib._ptr(k_cache),
+                                      _lib._ptr(v_cache), _lib._ptr(k_scale),
+                                      _lib._ptr(v_scale), _lib._ptr(block_tables),
+                                      _lib._ptr(context_lens), _lib._ptr(out),
+                                      _lib._ptr(workspace), workspace.numel(),
+                                      _status_arg(status), _lib._stream(stream))
+    _lib._check(fn_name, rc)
+    return out
+
+
+def decode_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                           *, kv="int8", out=None, scale=None, workspace=None, status=None,
+                           stream=None, pdl=False, early_kv=False):
+    """gqa_decode_attention_quant over a one-byte cache (kv = "int8" / "e4m3")."""
+    return _attention_quant("gqa_decode_attention_quant", q, k_cache, v_cache, k_scale, v_scale,
+                            block_tables, context_lens, out, scale, workspace, status, stream,
+                            pdl, early_kv, kv)
+
+
+def verify_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                           *, kv="int8", out=None, scale=None, workspace=None, status=None,
+                           stream=None, pdl=False, early_kv=False):
+    """gqa_verify_attention_quant over a one-byte cache (kv = "int8" / "e4m3")."""
+    return _attention_quant("gqa_verify_attention_quant", q, k_cache, v_cache, k_scale, v_scale,
+                            block_tables, context_lens, out, scale, workspace, status, stream,
+                            pdl, early_kv, kv)
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,

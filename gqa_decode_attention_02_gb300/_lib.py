@@ -34,6 +34,9 @@ class Status(enum.IntEnum):
     ERR_PROBS = 10
 
 
+KV_DTYPES = {"same": 0, "int8": 1, "e4m3": 2}
+
+
 class GqaError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = Status(status) if status in Status._value2member_map_ else status
@@ -46,7 +49,8 @@ class Shape(ctypes.Structure):
                 ("K", ctypes.c_int), ("H", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("num_blocks", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("scale", ctypes.c_float),
-                ("flags", ctypes.c_uint), ("window", ctypes.c_int)]
+                ("flags", ctypes.c_uint), ("window", ctypes.c_int),
+                ("kv_dtype", ctypes.c_int)]
 
 
 FLAG_PDL = 1
@@ -57,7 +61,8 @@ EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_attention_workspace_size", "gqa_workspace_clear", "gqa_decode_attention",
            "gqa_verify_attention", "gqa_append_decode_attention", "gqa_append_verify_attention",
            "gqa_accept_prefix", "gqa_accept_sampled", "gqa_tree_verify_attention",
-           "gqa_append_tree_verify_attention")
+           "gqa_append_tree_verify_attention", "gqa_kv_append_quant",
+           "gqa_decode_attention_quant", "gqa_verify_attention_quant")
 
 
 def lib() -> ctypes.CDLL:
@@ -94,6 +99,12 @@ def lib() -> ctypes.CDLL:
         L.gqa_tree_verify_attention.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
         L.gqa_append_tree_verify_attention.restype = I
         L.gqa_append_tree_verify_attention.argtypes = [S] + [P] * 10 + [ctypes.c_size_t, P, P]
+        L.gqa_kv_append_quant.restype = I
+        L.gqa_kv_append_quant.argtypes = [S] + [P] * 10
+        for name in ("gqa_decode_attention_quant", "gqa_verify_attention_quant"):
+            f = getattr(L, name)
+            f.restype = I
+            f.argtypes = [S] + [P] * 9 + [ctypes.c_size_t, P, P]
         L.gqa_accept_prefix.restype = I
         L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, P]
         L.gqa_accept_sampled.restype = I
@@ -139,7 +150,7 @@ def _need(t, name, dtype=None, ndim=None):
 
 def make_shape(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
                scale: float | None, heads_dim: int = 2, flags: int = 0,
-               window: int = 0) -> Shape:
+               window: int = 0, kv: str = "same") -> Shape:
     B, T, X, H = q_or_new.shape
     NB, bs, K, H2 = k_cache.shape
     if H2 != H:
@@ -149,7 +160,7 @@ def make_shape(q_or_new: torch.Tensor, k_cache: torch.Tensor, block_tables: torc
     return Shape(B=B, T=T, N=X if heads_dim == 2 else K, K=K, H=H, block_size=bs,
                  num_blocks=NB, max_blocks_per_seq=block_tables.shape[1],
                  dtype=_DTYPES[q_or_new.dtype], scale=float(scale or 0.0), flags=int(flags),
-                 window=int(window))
+                 window=int(window), kv_dtype=KV_DTYPES[kv])
 
 
 _ws_cache: dict = {}

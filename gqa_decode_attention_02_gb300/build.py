@@ -20,7 +20,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libgqa_decode.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "attention.cu", "kv_append.cu", "accept_prefix.cu", "accept_sampled.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "attention.cu", "kv_append.cu", "accept_prefix.cu", "accept_sampled.cu", "noalloc.cu",
+           "kv_quant.cu"]
 
 
 def nvcc() -> str:

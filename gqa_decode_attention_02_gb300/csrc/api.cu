@@ -20,6 +20,7 @@ gqa_status check_common(const gqa_shape* s) {
     if ((long long)s->max_blocks_per_seq * 16 > (1ll << 30)) return GQA_ERR_SHAPE;
     if ((long long)s->B * s->K * s->max_blocks_per_seq > (1ll << 31) - 1) return GQA_ERR_SHAPE;
     if (s->window < 0) return GQA_ERR_SHAPE;
+    if (s->kv_dtype < GQA_KV_SAME || s->kv_dtype > GQA_KV_E4M3) return GQA_ERR_DTYPE;
     return GQA_OK;
 }
 
@@ -28,10 +29,15 @@ gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, con
                            const void* v_cache, const int32_t* block_tables,
                            const int32_t* context_lens, const uint64_t* tree_mask, void* out,
                            void* workspace, size_t ws_bytes, int32_t* dev_status,
-                           void* stream) {
+                           void* stream, const float* k_scale = nullptr,
+                           const float* v_scale = nullptr) {
     gqa_status st = check_common(s);
     if (st != GQA_OK) return st;
     if (decode_only && s->T != 1) return GQA_ERR_SHAPE;
+    // one-byte caches come with their row scales (the _quant calls), others without
+    if ((s->kv_dtype != GQA_KV_SAME) != (k_scale != nullptr)) return GQA_ERR_DTYPE;
+    if (k_scale && (!v_scale || fused)) return GQA_ERR_NULL;
+    if (k_scale && (!aligned16(k_scale) || !aligned16(v_scale))) return GQA_ERR_ALIGN;
     if (s->B == 0) return GQA_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
         return GQA_ERR_NULL;
@@ -47,8 +53,9 @@ gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, con
     if (!workspace || ws_bytes < plan.workspace) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_ALIGN;
     return gqa::launch_attention(*s, plan, q, fused ? k_new : nullptr, fused ? v_new : nullptr,
-                                 k_cache, v_cache, block_tables, context_lens, tree_mask, out,
-                                 workspace, dev_status, static_cast<cudaStream_t>(stream));
+                                 k_cache, v_cache, block_tables, context_lens, tree_mask,
+                                 k_scale, v_scale, out, workspace, dev_status,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -79,6 +86,7 @@ gqa_status gqa_kv_append(const gqa_shape* shape, const void* k_new, const void* 
                          const int32_t* context_lens, int32_t* dev_status, void* stream) {
     gqa_status st = check_common(shape);
     if (st != GQA_OK) return st;
+    if (shape->kv_dtype != GQA_KV_SAME) return GQA_ERR_DTYPE;  // use gqa_kv_append_quant
     if (shape->B == 0) return GQA_OK;
     if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens)
         return GQA_ERR_NULL;
@@ -88,11 +96,31 @@ gqa_status gqa_kv_append(const gqa_shape* shape, const void* k_new, const void* 
                                  context_lens, dev_status, static_cast<cudaStream_t>(stream));
 }
 
+gqa_status gqa_kv_append_quant(const gqa_shape* shape, const void* k_new, const void* v_new,
+                               void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int32_t* dev_status, void* stream) {
+    gqa_status st = check_common(shape);
+    if (st != GQA_OK) return st;
+    if (shape->kv_dtype != GQA_KV_INT8 && shape->kv_dtype != GQA_KV_E4M3) return GQA_ERR_DTYPE;
+    if (shape->B == 0) return GQA_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !k_scale || !v_scale || !block_tables ||
+        !context_lens)
+        return GQA_ERR_NULL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(k_scale) || !aligned16(v_scale))
+        return GQA_ERR_ALIGN;
+    return gqa::launch_kv_append_quant(*shape, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                       block_tables, context_lens, dev_status,
+                                       static_cast<cudaStream_t>(stream));
+}
+
 size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     if (check_common(shape) != GQA_OK) return 0;
     // the larger of the two kernel variants' needs (they normally agree)
     gqa::AttnPlan plain, general;
     if (gqa::attention_plan(*shape, false, &plain) != GQA_OK) return 0;
+    if (shape->kv_dtype != GQA_KV_SAME) return plain.workspace;  // no general variant
     if (gqa::attention_plan(*shape, true, &general) != GQA_OK) return 0;
     return plain.workspace > general.workspace ? plain.workspace : general.workspace;
 }
@@ -168,6 +196,32 @@ gqa_status gqa_append_tree_verify_attention(const gqa_shape* shape, const void* 
     return attention_entry(shape, false, true, q, k_new, v_new, k_cache, v_cache, block_tables,
                            context_lens, tree_mask, out, workspace, workspace_bytes, dev_status,
                            stream);
+}
+
+gqa_status gqa_decode_attention_quant(const gqa_shape* shape, const void* q,
+                                      const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* block_tables,
+                                      const int32_t* context_lens, void* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream) {
+    if (!k_scale || !v_scale) return GQA_ERR_NULL;
+    return attention_entry(shape, true, false, q, nullptr, nullptr, k_cache, v_cache,
+                           block_tables, context_lens, nullptr, out, workspace,
+                           workspace_bytes, dev_status, stream, k_scale, v_scale);
+}
+
+gqa_status gqa_verify_attention_quant(const gqa_shape* shape, const void* q,
+                                      const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale,
+                                      const int32_t* block_tables,
+                                      const int32_t* context_lens, void* out, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status,
+                                      void* stream) {
+    if (!k_scale || !v_scale) return GQA_ERR_NULL;
+    return attention_entry(shape, false, false, q, nullptr, nullptr, k_cache, v_cache,
+                           block_tables, context_lens, nullptr, out, workspace,
+                           workspace_bytes, dev_status, stream, k_scale, v_scale);
 }
 
 gqa_status gqa_accept_prefix(int B, int T, int V, const float* target_logits,

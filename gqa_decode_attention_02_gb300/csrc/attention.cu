@@ -96,6 +96,9 @@ struct AttnParams {
     // Tree verification: new token t sees new token j < t only if bit j of
     // tree_mask[b * T + t] is set (nullptr: the chain, all j < t).
     const uint64_t* tree_mask;
+    // One-byte caches: fp32 scale of every cached row, [num_blocks][K][16].
+    const float* k_scale;
+    const float* v_scale;
     // Fused append (k_new != nullptr): the T newest positions are taken from
     // k_new / v_new [B][T][K][H] and written into the caches by this kernel.
     const void* k_new;
@@ -112,14 +115,20 @@ struct StageMeta {
     int blk[kTilesPerStage];  // physical block of each tile
 };
 
-template <int H>
+// KVQ: cache element kind -- 0: the dtype of q (2 bytes), GQA_KV_INT8 /
+// GQA_KV_E4M3: one-byte codes with an fp32 scale per cached row.
+template <int H, int KVQ = 0>
 struct Cfg {
-    static constexpr int kTileBytes = 16 * H * 2;  // 16 tokens x H elements
-    static constexpr int kStageBytes = 2 * kTilesPerStage * kTileBytes;  // K tiles, V tiles
-    // Default ring depth (two CTAs per SM fit); a CTA alone on its SM (the
-    // host decides) gets as many stages as the opt-in shared memory holds.
-    static constexpr int kStages = (H == 128) ? 3 : 6;
-    static constexpr int kHalves = H / 64;  // 64-element (128-byte) swizzle spans
+    static constexpr int kElemBytes = KVQ ? 1 : 2;
+    static constexpr int kTileBytes = 16 * H * kElemBytes;  // 16 tokens x H elements
+    static constexpr int kScaleBytes = KVQ ? 16 * 4 : 0;      // the tile's row scales
+    // K tiles, V tiles (then K scales, V scales), rounded to the 1 KB alignment
+    // of a 128-byte-swizzled TMA destination
+    static constexpr int kStageBytes =
+        (2 * kTilesPerStage * (kTileBytes + kScaleBytes) + 1023) / 1024 * 1024;
+    // Default ring depth (two CTAs per SM fit).
+    static constexpr int kStages = KVQ ? 6 : (H == 128) ? 3 : 6;
+    static constexpr int kHalves = KVQ ? 1 : H / 64;  // 128-byte swizzle spans per row
     static constexpr int kSteps = H / 16;  // k16 steps of QK^T == m16 tiles of PV
     static constexpr int kAccFloats = H / 4;  // accumulator floats per lane
     static constexpr int kHeaderFloats = 32;  // m[8], l[8], flag, pad
@@ -196,11 +205,11 @@ __device__ __forceinline__ void prefetch_q(const AttnParams& p, int b, int k) {
 }
 
 // ---------------------------------------------------------------------------
-template <int H, bool GENERAL>
+template <int H, bool GENERAL, int KVQ>
 __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
                          uint8_t* stages, const Bars& bar, StageMeta* meta,
                          volatile int* abort_flag) {
-    using C = Cfg<H>;
+    using C = Cfg<H, KVQ>;
     const int win = GENERAL ? p.window : 0;  // compile-time 0 for the plain kernel
     const int nC = GENERAL ? p.C : 1;        // row chunks (1 in the plain kernel)
     const int nKC = GENERAL ? p.KC : p.K;    // virtual heads
@@ -358,8 +367,22 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                         report(p.status, GQA_ERR_BLOCK_ID);
                         mbar_arrive(fb_);
                     } else {
-                        mbar_arrive_expect_tx(fb_, (uint32_t)(run * 2 * C::kTileBytes));
+                        mbar_arrive_expect_tx(
+                            fb_, (uint32_t)(run * 2 * (C::kTileBytes + C::kScaleBytes)));
                         const uint32_t dst = smem_addr(stages + (size_t)s * C::kStageBytes);
+                        if constexpr (KVQ != 0) {  // the tiles' row scales, 64 B each
+                            const uint32_t sdst = dst + 2 * kTilesPerStage * C::kTileBytes;
+#pragma unroll
+                            for (int j = 0; j < kTilesPerStage; ++j) {
+                                if (j < run) {
+                                    const size_t so =
+                                        ((size_t)blk[j] * p.K + (GENERAL ? kv : k)) * 16;
+                                    bulk_load(sdst + j * 64, p.k_scale + so, 64, fb_);
+                                    bulk_load(sdst + (kTilesPerStage + j) * 64, p.v_scale + so,
+                                              64, fb_);
+                                }
+                            }
+                        }
 #pragma unroll
                         for (int j = 0; j < kTilesPerStage; ++j) {
                             if (j < run) {
@@ -447,10 +470,11 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
 // rows 8*(w*NW + u) .. +7 (rows r = t*G + g).  Every K / V fragment it reads
 // from shared memory feeds NW mma, so more rows per warp means fewer warps
 // re-reading the same stage.
-template <int H, bool BF16, int NW, bool GENERAL>
+template <int H, bool BF16, int NW, bool GENERAL, int KVQ>
 struct Consumer {
-    using C = Cfg<H>;
-    using E = Elt<BF16>;
+    using C = Cfg<H, KVQ>;
+    using E = Elt<BF16 && !KVQ>;  // the mma type: f16 over one-byte codes
+    using EO = Elt<BF16>;         // the output type
     static constexpr unsigned FULL = 0xffffffffu;
 
     const AttnParams& p;
@@ -513,10 +537,31 @@ struct Consumer {
                 const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
                     static_cast<const uint16_t*>(p.q) +
                     (((size_t)cb * p.T + t) * p.N + (size_t)ck * p.G + gg) * H);
+                if constexpr (KVQ != 0) {
+                    // permuted dims: lane q4 takes dims 32*q4 .. +31, four per
+                    // k-step (see stage_q); f16 for the mma (bf16 -> f16 is
+                    // exact in f16's normal range)
+                    const uint4* q16 = reinterpret_cast<const uint4*>(qrow) + 4 * q4;
+                    uint32_t w[16];
 #pragma unroll
-                for (int kk = 0; kk < C::kSteps; ++kk) {
-                    qf[u][kk][0] = __ldg(qrow + kk * 8 + q4);
-                    qf[u][kk][1] = __ldg(qrow + kk * 8 + 4 + q4);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint4 v = __ldg(q16 + i);
+                        w[4 * i] = v.x;
+                        w[4 * i + 1] = v.y;
+                        w[4 * i + 2] = v.z;
+                        w[4 * i + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < C::kSteps; ++kk) {
+                        qf[u][kk][0] = to_f16x2(w[2 * kk]);
+                        qf[u][kk][1] = to_f16x2(w[2 * kk + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < C::kSteps; ++kk) {
+                        qf[u][kk][0] = __ldg(qrow + kk * 8 + q4);
+                        qf[u][kk][1] = __ldg(qrow + kk * 8 + 4 + q4);
+                    }
                 }
             } else {
 #pragma unroll
@@ -567,40 +612,23 @@ struct Consumer {
         return any;
     }
 
-    // One stage: md.ntiles tiles of 16 tokens starting at tile md.blk_i.
-    __device__ void stage(uint32_t kbase, const StageMeta& md) {
-        const int win = GENERAL ? p.window : 0;  // compile-time 0 for the plain kernel
-        if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
-        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
+    // Two q elements (the dtype of q) -> f16x2.
+    static __device__ __forceinline__ uint32_t to_f16x2(uint32_t x) {
+        if constexpr (BF16)
+            return Elt<false>::pack(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+        else
+            return x;
+    }
+
+    // Scores of one stage -> masked (unused tiles, causal bound, window, tree
+    // mask, slots past the context) and scaled into the log2 domain by tsc
+    // (per tile, for tokens g and g+8); running max with lazy rescale; ref*
+    // get the exponent references of the stage.
+    __device__ void mask_and_max(float (&sc)[NW][kTilesPerStage][4], const StageMeta& md,
+                                 const float (&tsc)[kTilesPerStage][2], float (&ref0)[NW],
+                                 float (&ref1)[NW]) {
+        const int win = GENERAL ? p.window : 0;
         const int ntl = md.ntiles;
-        // ---- S^T = K_tile . Q^T for every tile and row tile (independent chains)
-        float sc[NW][kTilesPerStage][4];
-#pragma unroll
-        for (int u = 0; u < NW; ++u)
-#pragma unroll
-            for (int j = 0; j < kTilesPerStage; ++j)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sc[u][j][e] = 0.f;
-        {
-            const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
-            const int chk = lane >> 4;
-#pragma unroll
-            for (int kk = 0; kk < C::kSteps; ++kk) {
-                const int hh = kk >> 2;
-                const int chunk = ((kk & 3) << 1) + chk;
-                const uint32_t off = hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4);
-#pragma unroll
-                for (int j = 0; j < kTilesPerStage; ++j) {
-                    uint32_t a[4];
-                    ldsm_x4(kbase + j * C::kTileBytes + off, a);
-#pragma unroll
-                    for (int u = 0; u < NW; ++u) E::mma(sc[u][j], a, qf[u][kk][0], qf[u][kk][1]);
-                }
-            }
-        }
-        // ---- scale, mask (unused tiles, causal bound, slots past the context),
-        //      running max in the log2 domain, lazy rescale ----------------------
-        float ref0[NW], ref1[NW];
 #pragma unroll
         for (int u = 0; u < NW; ++u) {
             float x0 = -INFINITY, x1 = -INFINITY;
@@ -608,7 +636,7 @@ struct Consumer {
             for (int j = 0; j < kTilesPerStage; ++j) {
                 const int tb = (md.blk_i + j) * 16;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[u][j][e] *= p.scale_log2;
+                for (int e = 0; e < 4; ++e) sc[u][j][e] *= tsc[j][e >> 1];
                 if (j >= ntl) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[u][j][e] = -INFINITY;
@@ -671,6 +699,148 @@ struct Consumer {
             ref0[u] = (m0[u] == -INFINITY) ? 0.f : m0[u];
             ref1[u] = (m1[u] == -INFINITY) ? 0.f : m1[u];
         }
+    }
+
+    // One stage: md.ntiles tiles of 16 tokens starting at tile md.blk_i.
+    // One stage over one-byte codes (H = 128, one 8-row tile per warp).  The
+    // head dimension is permuted so that each lane's fragment elements are
+    // contiguous bytes of shared memory (the dot products and the output are
+    // unchanged by a permutation applied to q, K and V alike):
+    //   QK^T, k-step kk: fragment column c <-> dim 32*(c%8/2) + 4*kk + c%2 + 2*(c/8),
+    //     so lane q4 reads dims 32*q4 .. +31 of its two token rows (32 bytes each);
+    //   PV, m-tile mt: fragment row m <-> dim 16*(m%8) + 2*mt + m/8,
+    //     so lane g reads dims 16*g .. +15 of its four tokens (16 bytes each)
+    //     and holds output dims 16*g .. +15 of its two query rows.
+    // Codes become f16 exactly; the K row scales multiply the scores, the V row
+    // scales the probabilities (the row sums use the unscaled ones).
+    __device__ void stage_q(uint32_t kbase, const StageMeta& md) {
+        static_assert(H == 128 && NW == 1, "one-byte caches: H = 128, one tile per warp");
+        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
+        const uint32_t ksb = vbase + kTilesPerStage * C::kTileBytes;  // K row scales
+        const uint32_t vsb = ksb + kTilesPerStage * 64;                // V row scales
+        const int ntl = md.ntiles;
+        float sc[NW][kTilesPerStage][4];
+        float tsc[kTilesPerStage][2];
+#pragma unroll
+        for (int j = 0; j < kTilesPerStage; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[0][j][e] = 0.f;
+            const uint32_t kt = kbase + j * C::kTileBytes;
+            const uint32_t c0 = (uint32_t)(((2 * q4) ^ g) << 4);
+            const uint32_t c1 = (uint32_t)(((2 * q4 + 1) ^ g) << 4);
+            const uint4 ra = ld_shared_v4(kt + g * 128 + c0);
+            const uint4 rb = ld_shared_v4(kt + g * 128 + c1);
+            const uint4 sa = ld_shared_v4(kt + (g + 8) * 128 + c0);
+            const uint4 sb = ld_shared_v4(kt + (g + 8) * 128 + c1);
+            const uint32_t w0[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+            const uint32_t w1[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+            for (int kk = 0; kk < C::kSteps; ++kk) {
+                uint32_t a[4];
+                a[0] = code2_to_f16x2<KVQ, false>(w0[kk]);  // token g, dims +0, +1
+                a[1] = code2_to_f16x2<KVQ, false>(w1[kk]);  // token g+8
+                a[2] = code2_to_f16x2<KVQ, true>(w0[kk]);   // token g, dims +2, +3
+                a[3] = code2_to_f16x2<KVQ, true>(w1[kk]);
+                E::mma(sc[0][j], a, qf[0][kk][0], qf[0][kk][1]);
+            }
+            tsc[j][0] = p.scale_log2 * ld_shared_f32(ksb + j * 64 + g * 4);
+            tsc[j][1] = p.scale_log2 * ld_shared_f32(ksb + j * 64 + (g + 8) * 4);
+        }
+        float ref0[NW], ref1[NW];
+        mask_and_max(sc, md, tsc, ref0, ref1);
+        // ---- O^T += V^T . (P * v_scale)^T, tile by tile -----------------------
+#pragma unroll
+        for (int j = 0; j < kTilesPerStage; ++j) {
+            if (j >= ntl) break;  // warp-uniform
+            const int tb = (md.blk_i + j) * 16;
+            const bool tail = tb + 16 > md.ctx;
+            float svg = ld_shared_f32(vsb + j * 64 + g * 4);
+            float sv8 = ld_shared_f32(vsb + j * 64 + (g + 8) * 4);
+            if (tail) {  // slots past the context may hold anything
+                if (tb + g >= md.ctx) svg = 0.f;
+                if (tb + g + 8 >= md.ctx) sv8 = 0.f;
+            }
+            const float e0 = fast_exp2(sc[0][j][0] - ref0[0]);
+            const float e1 = fast_exp2(sc[0][j][1] - ref1[0]);
+            const float e2 = fast_exp2(sc[0][j][2] - ref0[0]);
+            const float e3 = fast_exp2(sc[0][j][3] - ref1[0]);
+            const uint32_t u0 = E::pack(e0, e1), u1 = E::pack(e2, e3);
+            l0[0] += E::lo(u0) + E::lo(u1);
+            l1[0] += E::hi(u0) + E::hi(u1);
+            const uint32_t pb0 = movm_t(E::pack(e0 * svg, e1 * svg));  // tokens 2q4, +1
+            const uint32_t pb1 = movm_t(E::pack(e2 * sv8, e3 * sv8));  // tokens 2q4+8, +9
+            uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
+            if (tail) {
+                const int pb = tb + 2 * q4;
+                v01 = (pb < md.ctx ? 0x0000ffffu : 0u) | (pb + 1 < md.ctx ? 0xffff0000u : 0u);
+                v89 = (pb + 8 < md.ctx ? 0x0000ffffu : 0u) | (pb + 9 < md.ctx ? 0xffff0000u : 0u);
+            }
+            const uint32_t vt = vbase + j * C::kTileBytes;
+            const int t0_ = 2 * q4, t1_ = t0_ + 1, t2_ = t0_ + 8, t3_ = t0_ + 9;
+            const uint4 x0 = ld_shared_v4(vt + t0_ * 128 + ((g ^ (t0_ & 7)) << 4));
+            const uint4 x1 = ld_shared_v4(vt + t1_ * 128 + ((g ^ (t1_ & 7)) << 4));
+            const uint4 x2 = ld_shared_v4(vt + t2_ * 128 + ((g ^ (t2_ & 7)) << 4));
+            const uint4 x3 = ld_shared_v4(vt + t3_ * 128 + ((g ^ (t3_ & 7)) << 4));
+            const uint32_t y0[4] = {x0.x, x0.y, x0.z, x0.w}, y1[4] = {x1.x, x1.y, x1.z, x1.w};
+            const uint32_t y2[4] = {x2.x, x2.y, x2.z, x2.w}, y3[4] = {x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt) {
+                // dims 16g + 2mt (+1): byte 2*(mt&1) (+1) of word mt/2; interleave
+                // the two tokens of each pair, then two bytes -> f16x2
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t p01 = prmt(y0[mt >> 1], y1[mt >> 1], sel);
+                const uint32_t p23 = prmt(y2[mt >> 1], y3[mt >> 1], sel);
+                uint32_t a[4];
+                a[0] = code2_to_f16x2<KVQ, false>(p01) & v01;  // dim +0, tokens 2q4, +1
+                a[1] = code2_to_f16x2<KVQ, true>(p01) & v01;   // dim +1
+                a[2] = code2_to_f16x2<KVQ, false>(p23) & v89;  // dim +0, tokens +8, +9
+                a[3] = code2_to_f16x2<KVQ, true>(p23) & v89;
+                E::mma(acc[0][mt], a, pb0, pb1);
+            }
+        }
+    }
+
+    __device__ void stage(uint32_t kbase, const StageMeta& md) {
+        if constexpr (KVQ != 0) {
+            stage_q(kbase, md);
+            return;
+        }
+        const int win = GENERAL ? p.window : 0;  // compile-time 0 for the plain kernel
+        if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
+        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
+        const int ntl = md.ntiles;
+        // ---- S^T = K_tile . Q^T for every tile and row tile (independent chains)
+        float sc[NW][kTilesPerStage][4];
+#pragma unroll
+        for (int u = 0; u < NW; ++u)
+#pragma unroll
+            for (int j = 0; j < kTilesPerStage; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[u][j][e] = 0.f;
+        {
+            const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int chk = lane >> 4;
+#pragma unroll
+            for (int kk = 0; kk < C::kSteps; ++kk) {
+                const int hh = kk >> 2;
+                const int chunk = ((kk & 3) << 1) + chk;
+                const uint32_t off = hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+#pragma unroll
+                for (int j = 0; j < kTilesPerStage; ++j) {
+                    uint32_t a[4];
+                    ldsm_x4(kbase + j * C::kTileBytes + off, a);
+#pragma unroll
+                    for (int u = 0; u < NW; ++u) E::mma(sc[u][j], a, qf[u][kk][0], qf[u][kk][1]);
+                }
+            }
+        }
+        float ref0[NW], ref1[NW];
+        {
+            float tsc[kTilesPerStage][2];
+#pragma unroll
+            for (int j = 0; j < kTilesPerStage; ++j) tsc[j][0] = tsc[j][1] = p.scale_log2;
+            mask_and_max(sc, md, tsc, ref0, ref1);
+        }
         // ---- O^T += V_tile^T . P^T, tile by tile ------------------------------------
         const int tok = (lane & 7) + (lane >> 4) * 8;
         const int dof = ((lane >> 3) & 1) * 8;
@@ -724,7 +894,34 @@ struct Consumer {
     }
 
     // Normalise and store the rows of tile u of segment (cb, ck).
+    // One-byte caches: lane g holds output dims 16g .. +15 of query rows 2q4
+    // (acc[mt][0], acc[mt][2]) and 2q4+1 (acc[mt][1], acc[mt][3]).
+    __device__ void store_q(int u, float L0, float L1, bool is_bad) {
+        const float i0 = (!is_bad && L0 > 0.f) ? 1.f / L0 : 0.f;
+        const float i1 = (!is_bad && L1 > 0.f) ? 1.f / L1 : 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = row0(u) + 2 * q4 + half;
+            if (r >= row_end()) continue;
+            const float iv = half ? i1 : i0;
+            const int t = r / p.G, gg = r % p.G;
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<uint16_t*>(p.out) +
+                (((size_t)cb * p.T + t) * p.N + (size_t)ck * p.G + gg) * H + 16 * g);
+            uint32_t w[8];
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt)
+                w[mt] = is_bad ? 0u : EO::pack(acc[u][mt][half] * iv, acc[u][mt][2 + half] * iv);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+
     __device__ void store(int u, float L0, float L1, bool is_bad) {
+        if constexpr (KVQ != 0) {
+            store_q(u, L0, L1, is_bad);
+            return;
+        }
         const float i0 = (!is_bad && L0 > 0.f) ? 1.f / L0 : 0.f;
         const float i1 = (!is_bad && L1 > 0.f) ? 1.f / L1 : 0.f;
         const int r = row0(u) + g;
@@ -906,12 +1103,12 @@ struct Consumer {
 // 8*(w % nt) .. +7.  Every warp reads every stage's description, so all groups
 // agree on segment boundaries; at each boundary the groups' partial states
 // meet in shared memory and group 0 finishes the segment.
-template <int H, bool BF16, int NW, bool GENERAL>
+template <int H, bool BF16, int NW, bool GENERAL, int KVQ>
 __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
                          const StageMeta* meta, float* scratch, volatile int* abort_flag,
                          int w) {
-    using C = Cfg<H>;
-    using CS = Consumer<H, BF16, NW, GENERAL>;
+    using C = Cfg<H, KVQ>;
+    using CS = Consumer<H, BF16, NW, GENERAL, KVQ>;
     const int gi = w / p.nt, wr = w % p.nt;
     CS cs(p, wr);
     const int lane = threadIdx.x & 31;
@@ -980,11 +1177,11 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
 // many query rows) up to 3, with the register budget of the smaller CTA.
 // GENERAL: local attention, a tree mask or row chunks (all compiled out of the
 // plain kernel, which then runs with no window, the chain mask and one chunk).
-template <int H, bool BF16, int NW, bool GENERAL>
+template <int H, bool BF16, int NW, bool GENERAL, int KVQ>
 __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRowWarps / 2 + 1))
     attention_kernel(const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
-    using C = Cfg<H>;
+    using C = Cfg<H, KVQ>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1014,25 +1211,33 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
     }
     __syncthreads();
     if (warp == consumers)
-        producer<H, GENERAL>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
+        producer<H, GENERAL, KVQ>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
     else
-        consumer<H, BF16, NW, GENERAL>(p, stages, bar, meta, scratch, abort_flag, warp);
+        consumer<H, BF16, NW, GENERAL, KVQ>(p, stages, bar, meta, scratch, abort_flag, warp);
 }
 
 // ---------------------------------------------------------------------------
 // Host side
-// The instantiated variants: (nw, general) in {(1, no), (1, yes), (2, no)} for
-// each head size and dtype.
+// The instantiated variants, for each head size and dtype: (nw, general) in
+// {(1, no), (1, yes), (2, no)} over a cache in q's dtype, and for H = 128 the
+// plain kernel over int8 and e4m3 caches.
 template <int H, bool BF16>
-const void* kernel_ptr(int nw, bool general) {
-    if (nw == 2) return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 2, false>);
-    return general ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true>)
-               : reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false>);
+const void* kernel_ptr(int nw, bool general, int kvq) {
+    if constexpr (H == 128) {
+        if (kvq == GQA_KV_INT8)
+            return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false, GQA_KV_INT8>);
+        if (kvq == GQA_KV_E4M3)
+            return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false, GQA_KV_E4M3>);
+    }
+    if (nw == 2) return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 2, false, 0>);
+    return general ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true, 0>)
+                   : reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false, 0>);
 }
 
-const void* pick_kernel(int H, bool bf16, int nw, bool general) {
-    if (H == 64) return bf16 ? kernel_ptr<64, true>(nw, general) : kernel_ptr<64, false>(nw, general);
-    return bf16 ? kernel_ptr<128, true>(nw, general) : kernel_ptr<128, false>(nw, general);
+const void* pick_kernel(int H, bool bf16, int nw, bool general, int kvq) {
+    if (H == 64)
+        return bf16 ? kernel_ptr<64, true>(nw, general, kvq) : kernel_ptr<64, false>(nw, general, kvq);
+    return bf16 ? kernel_ptr<128, true>(nw, general, kvq) : kernel_ptr<128, false>(nw, general, kvq);
 }
 
 // Consumer groups for nt row warps.  (A third group was measured slower on
@@ -1044,16 +1249,20 @@ int max_row_warps(int nw) { return nw == 1 ? kMaxRowWarps : kMaxRowWarps / 2; }
 
 // Dynamic shared memory of one CTA: nt row warps (nw tiles each) per consumer
 // group and a ring of `stages` stages.
-template <int H>
+template <int H, int KVQ>
 size_t smem_of(int nt, int nw, int stages) {
-    using C = Cfg<H>;
+    using C = Cfg<H, KVQ>;
     return C::kFixed + (size_t)stages * (C::kStageBytes + C::kStageOverhead) +
            (size_t)(groups_for(nt) - 1) * nt * nw * C::kScratchBytesPerRowWarp;
 }
-size_t smem_for(int H, int nt, int nw, int stages) {
-    return H == 64 ? smem_of<64>(nt, nw, stages) : smem_of<128>(nt, nw, stages);
+size_t smem_for(int H, int nt, int nw, int stages, int kvq) {
+    if (kvq) return smem_of<128, 1>(nt, nw, stages);  // both one-byte kinds: H = 128
+    return H == 64 ? smem_of<64, 0>(nt, nw, stages) : smem_of<128, 0>(nt, nw, stages);
 }
-int default_stages(int H) { return H == 64 ? Cfg<64>::kStages : Cfg<128>::kStages; }
+int default_stages(int H, int kvq) {
+    if (kvq) return Cfg<128, 1>::kStages;
+    return H == 64 ? Cfg<64>::kStages : Cfg<128>::kStages;
+}
 
 size_t section_floats(int H) {
     return H == 64 ? Cfg<64>::kSectionFloats : Cfg<128>::kSectionFloats;
@@ -1073,17 +1282,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D view of a cache [num_blocks][16][K][H]: (h, kv head, block*16 + row);
-// one box = 16 rows x 64 elements of one KV head, 128-byte swizzled.
+// one box = 16 rows x 128 bytes of one KV head (64 two-byte elements, or 128
+// one-byte codes), 128-byte swizzled.
 bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const bool q8 = s.kv_dtype != GQA_KV_SAME;
+    const cuuint64_t eb = q8 ? 1 : 2;
     const cuuint64_t dims[3] = {(cuuint64_t)s.H, (cuuint64_t)s.K,
                                 (cuuint64_t)s.num_blocks * 16};
-    const cuuint64_t strides[2] = {(cuuint64_t)s.H * 2, (cuuint64_t)s.K * s.H * 2};
-    const cuuint32_t box[3] = {64, 1, 16};
+    const cuuint64_t strides[2] = {(cuuint64_t)s.H * eb, (cuuint64_t)s.K * s.H * eb};
+    const cuuint32_t box[3] = {q8 ? 128u : 64u, 1, 16};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(m, s.dtype == GQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+    const CUresult r = fn(m, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                             : s.dtype == GQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                           3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1094,20 +1307,21 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
 // CTAs of one variant resident per SM, queried once per (device, variant) so
 // that later calls -- including calls being captured into a CUDA graph -- make
 // no attribute or occupancy API calls.
-int resident_ctas(int H, bool bf16, int nt, int nw, bool general, size_t smem) {
+int resident_ctas(int H, bool bf16, int nt, int nw, bool general, int kvq, size_t smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key = std::make_tuple(dev, H, (int)bf16, nt, nw * 2 + (int)general);
+    const auto key = std::make_tuple(dev, H, (int)bf16, nt, (nw * 2 + (int)general) * 4 + kvq);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const void* kern = pick_kernel(H, bf16, nw, general);
+    const void* kern = pick_kernel(H, bf16, nw, general, kvq);
     // The attribute belongs to the kernel, whatever the row-warp count: set it
     // to the largest launch any shape makes.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_for(H, max_row_warps(nw), nw, default_stages(H))) !=
+                             (int)smem_for(H, max_row_warps(nw), nw, default_stages(H, kvq),
+                                           kvq)) !=
         cudaSuccess)
         return 0;
     int occ = 0;
@@ -1154,10 +1368,13 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     const int nt = (rows_per_chunk + 8 * nw - 1) / (8 * nw);
     const int groups = groups_for(nt);
     const int threads = 32 * (groups * nt + 1);
-    int stages = default_stages(s.H);
-    size_t smem = smem_for(s.H, nt, nw, stages);
+    const int kvq = s.kv_dtype;
+    int stages = default_stages(s.H, kvq);
+    size_t smem = smem_for(s.H, nt, nw, stages, kvq);
     const bool general = masked || s.window > 0 || chunks > 1;
-    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, general, smem);
+    // the one-byte caches have the plain kernel for H = 128 only
+    if (kvq != GQA_KV_SAME && (s.H != 128 || general)) return GQA_ERR_SHAPE;
+    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, general, kvq, smem);
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
@@ -1196,7 +1413,8 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
 gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
                             const void* k_new, const void* v_new, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables,
-                            const int32_t* context_lens, const uint64_t* tree_mask, void* out,
+                            const int32_t* context_lens, const uint64_t* tree_mask,
+                            const float* k_scale, const float* v_scale, void* out,
                             void* workspace, int32_t* dev_status, cudaStream_t stream) {
     if (s.B == 0) return GQA_OK;
     CUtensorMap tmk, tmv;
@@ -1229,6 +1447,9 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     p.early_kv = (s.flags & GQA_FLAG_EARLY_KV) ? 1 : 0;
     p.window = s.window;
     p.tree_mask = tree_mask;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    if ((s.kv_dtype != GQA_KV_SAME) != (k_scale != nullptr)) return GQA_ERR_NULL;
     p.k_new = k_new;
     p.v_new = v_new;
     p.k_cache = const_cast<void*>(k_cache);
@@ -1248,7 +1469,7 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     const int nw = plan.tiles_per_warp;
     if ((tree_mask || s.window > 0 || plan.chunks > 1) && !plan.general)
         return GQA_ERR_SHAPE;  // plan made for another call
-    const void* kern = pick_kernel(s.H, bf16, nw, plan.general);
+    const void* kern = pick_kernel(s.H, bf16, nw, plan.general, s.kv_dtype);
     void* args[] = {&tmk, &tmv, &p};
     const cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;

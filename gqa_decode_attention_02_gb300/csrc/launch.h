@@ -37,7 +37,8 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan);
 gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void* q,
                             const void* k_new, const void* v_new, const void* k_cache,
                             const void* v_cache, const int32_t* block_tables,
-                            const int32_t* context_lens, const uint64_t* tree_mask, void* out,
+                            const int32_t* context_lens, const uint64_t* tree_mask,
+                            const float* k_scale, const float* v_scale, void* out,
                             void* workspace, int32_t* dev_status, cudaStream_t stream);
 
 gqa_status launch_kv_append(const gqa_shape& s, const void* k_new, const void* v_new,
@@ -54,6 +55,11 @@ gqa_status launch_accept_sampled(int B, int T, int V, const float* q, const floa
                                  const int32_t* draft, const double* u, int32_t* accepted,
                                  int32_t* next_token, int32_t* ctx_io, int32_t* dev_status,
                                  cudaStream_t stream);
+
+gqa_status launch_kv_append_quant(const gqa_shape& s, const void* k_new, const void* v_new,
+                                  void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                  const int32_t* block_tables, const int32_t* context_lens,
+                                  int32_t* dev_status, cudaStream_t stream);
 
 // Cached per-device SM count (0 on failure).
 int device_sm_count();

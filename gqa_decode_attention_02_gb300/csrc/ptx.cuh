@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "gqa_decode.h"
@@ -185,6 +186,60 @@ struct Elt<false> {
     }
     static constexpr CUtensorMapDataType kTmaType = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
 };
+
+// ---- one-byte cache codes --------------------------------------------------
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+// bytes of the pair (a: 0-3, b: 4-7) picked by the four selector nibbles
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+// Untiled bulk copy global -> shared, completing on an mbarrier (16-byte
+// aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+// Two signed int8 codes (bytes 0-1 of x, or 2-3 with HI) -> f16x2, exact:
+// f16 1024 + (c + 128) has the code's bits in its mantissa; subtract 1152.
+template <bool HI>
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t x) {
+    const uint32_t u = x ^ 0x80808080u;  // c + 128, as unsigned bytes
+    const uint32_t h = prmt(u, 0x64646464u, HI ? 0x4342u : 0x4140u);
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    return r;
+}
+// Two e4m3 codes (bytes 0-1 of x, or 2-3 with HI) -> f16x2 (exact: every e4m3
+// value is an f16 value).
+template <bool HI>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(HI ? (x >> 16) : (x & 0xffffu)), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+template <int KIND, bool HI>
+__device__ __forceinline__ uint32_t code2_to_f16x2(uint32_t x) {
+    if constexpr (KIND == GQA_KV_INT8)
+        return i8x2_to_f16x2<HI>(x);
+    else
+        return e4m3x2_to_f16x2<HI>(x);
+}
 
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

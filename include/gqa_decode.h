@@ -8,6 +8,8 @@
  *   gqa_verify_attention the same for T >= 1 new tokens, causal among them
  *   gqa_tree_verify_attention  the same with a tree mask among the new tokens
  *   gqa_accept_prefix    greedy longest-prefix acceptance of draft tokens
+ *   gqa_kv_append_quant  the append into a one-byte (int8 / e4m3) cache, and
+ *   gqa_decode_attention_quant / gqa_verify_attention_quant  attention over it
  *   gqa_accept_sampled   stochastic acceptance of draft tokens (speculative
  *                        sampling: modified rejection sampling)
  *
@@ -78,6 +80,10 @@ typedef enum {
 
 typedef enum { GQA_F16 = 0, GQA_BF16 = 1 } gqa_dtype;
 
+/* Element type of the KV cache: the dtype of q (2 bytes), or one-byte codes
+ * with an fp32 scale per cached row (see gqa_kv_append_quant). */
+typedef enum { GQA_KV_SAME = 0, GQA_KV_INT8 = 1, GQA_KV_E4M3 = 2 } gqa_kv_dtype;
+
 /* Problem sizes, in the pages' notation (CS336 lecture 10, §"Напоминание:
  * трансформер"): B sequences, T new query tokens per sequence, N query heads,
  * K key/value heads (G = N/K), head size H. */
@@ -95,6 +101,8 @@ typedef struct {
     unsigned int flags;     /* GQA_FLAG_* bits, 0 for plain stream order */
     int window;             /* local attention: > 0 limits each query to the last
                                `window` positions up to itself; 0 = all */
+    int kv_dtype;           /* gqa_kv_dtype of the caches; GQA_KV_SAME except for
+                               the _quant calls */
 } gqa_shape;
 
 /* Local (sliding-window) attention, for the attention calls: CS336 lecture 10
@@ -272,6 +280,47 @@ gqa_status gqa_append_tree_verify_attention(const gqa_shape *shape, const void *
                                             const uint64_t *tree_mask, void *out,
                                             void *workspace, size_t workspace_bytes,
                                             int32_t *dev_status, void *stream);
+
+/* One-byte KV cache.  Quantization section of "جعل inference رخيصًا: KV cache
+ * وbatching والتكميم" (symmetric absolute-maximum quantization: scale =
+ * max|x| / qmax, codes round(x / scale) clamped; decode being bandwidth bound,
+ * fewer bytes per element make each step faster) and CS336 lecture 10
+ * §"Квантование" (fp8 e4m3 and int8 as one-byte formats).
+ *   caches    int8 or e4m3 codes [num_blocks][16][K][H] (shape->kv_dtype)
+ *   k_scale, v_scale  fp32 [num_blocks][K][16]: the scale of each cached row
+ * Every appended key / value row of one KV head (H elements) is quantized on
+ * its own: scale = max|x| / qmax (qmax = 127 for int8, 448 -- the largest
+ * finite e4m3 value -- for e4m3) and code = x / scale rounded to nearest even
+ * (int8: clamped to [-128, 127]; e4m3: saturating), both divisions in IEEE
+ * fp32.  A row of zeros gets scale 0 and codes 0.  Attention reads
+ * code * scale.  The append needs k_new / v_new in the dtype of the shape,
+ * H in {64, 128}; other requirements and device errors as gqa_kv_append. */
+gqa_status gqa_kv_append_quant(const gqa_shape *shape, const void *k_new, const void *v_new,
+                               void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int32_t *dev_status, void *stream);
+
+/* Decode / verify attention over a one-byte cache written by
+ * gqa_kv_append_quant: as gqa_decode_attention / gqa_verify_attention, with
+ * K_b[j] = code * k_scale[block][k][row] (likewise V).  shape->kv_dtype is
+ * GQA_KV_INT8 or GQA_KV_E4M3; requires H == 128, window == 0 and
+ * T * (N/K) <= 48; k_scale / v_scale 16-byte aligned.  The products run on f16
+ * tensor-core operands: q is rounded to f16 (exact for |q| in f16's normal
+ * range), the codes convert exactly; fp32 accumulation. */
+gqa_status gqa_decode_attention_quant(const gqa_shape *shape, const void *q,
+                                      const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables,
+                                      const int32_t *context_lens, void *out, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status,
+                                      void *stream);
+gqa_status gqa_verify_attention_quant(const gqa_shape *shape, const void *q,
+                                      const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_tables,
+                                      const int32_t *context_lens, void *out, void *workspace,
+                                      size_t workspace_bytes, int32_t *dev_status,
+                                      void *stream);
 
 /* Greedy prefix acceptance.  Speculative-decoding section of "جعل inference
  * رخيصًا" (a drafted token is kept only if the target would produce it) and

@@ -12,6 +12,7 @@ from .oracle import (  # noqa: F401
     kv_append,
     kv_append_quant,
     quantize_row,
+    quantize_cache,
     e4m3_to_f64,
     e4m3_from_float,
     attention,

@@ -182,6 +182,10 @@ void oracle_quantize_row(const uint16_t *x, int n, int dtype, int kind, uint8_t 
         }
         volatile float y = (float)widen(x[i], dtype) / scale; /* one fp32 division */
         if (kind == ORACLE_KV_INT8) {
+            if (y != y) { /* a NaN element: code 0 */
+                codes[i] = 0;
+                continue;
+            }
             float r = nearbyintf(y);
             if (r > 127.0f) r = 127.0f;
             if (r < -128.0f) r = -128.0f;
@@ -190,6 +194,13 @@ void oracle_quantize_row(const uint16_t *x, int n, int dtype, int kind, uint8_t 
             codes[i] = e4m3_encode(y);
         }
     }
+}
+
+/* Every row of an array [nrows][n] (a whole cache, for tests). */
+void oracle_quantize_rows(const uint16_t *x, int nrows, int n, int dtype, int kind,
+                          uint8_t *codes, float *scales) {
+    for (int r = 0; r < nrows; ++r)
+        oracle_quantize_row(x + (size_t)r * n, n, dtype, kind, codes + (size_t)r * n, &scales[r]);
 }
 
 static double code_value(uint8_t c, int kind) {

@@ -57,6 +57,8 @@ def _get():
             lib.oracle_quantize_row.argtypes = [P, i, i, i, P, P]
             lib.oracle_kv_append_quant.restype = i
             lib.oracle_kv_append_quant.argtypes = [i] * 9 + [P] * 8 + [P]
+            lib.oracle_quantize_rows.restype = None
+            lib.oracle_quantize_rows.argtypes = [P, i, i, i, i, P, P]
             lib.oracle_e4m3_to_f64.restype = ctypes.c_double
             lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
@@ -203,6 +205,20 @@ def quantize_row(x, dtype, kv):
     sc = np.zeros(1, np.float32)
     _get().oracle_quantize_row(_p(xb), xb.size, _DT[dtype], KV_KINDS[kv], _p(codes), _p(sc))
     return codes, float(sc[0])
+
+
+def quantize_cache(cache, dtype, kv):
+    """Quantize every row of a cache [NB,bs,K,H] (fp16/bf16): codes uint8
+    [NB,bs,K,H] and scales fp32 [NB,K,bs]."""
+    cb = _bits(cache)
+    NB, bs, K, H = cb.shape
+    flat = np.ascontiguousarray(cb.reshape(-1, H))
+    codes = np.zeros(flat.shape, np.uint8)
+    scales = np.zeros(flat.shape[0], np.float32)
+    _get().oracle_quantize_rows(_p(flat), flat.shape[0], H, _DT[dtype], KV_KINDS[kv],
+                                _p(codes), _p(scales))
+    return (codes.reshape(NB, bs, K, H),
+            np.ascontiguousarray(scales.reshape(NB, bs, K).transpose(0, 2, 1)))
 
 
 def e4m3_to_f64(code: int) -> float:

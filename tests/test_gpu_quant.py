@@ -1,0 +1,134 @@
+"""GPU one-byte KV cache: the quantized append bit-exact against the oracle
+(codes and scales), and attention over the quantized cache against the
+oracle's attention over the same codes and scales."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_attention_02_gb300 as gq
+import oracle
+from helpers import small, to
+
+pytestmark = pytest.mark.gpu
+
+
+def empty_quant(w, dev, fill=0):
+    NB, bs, K, H = w.k_cache[0].shape
+    kc = torch.full((NB, bs, K, H), fill, dtype=torch.uint8, device=dev)
+    vc = torch.full_like(kc, fill)
+    ks = torch.full((NB, K, bs), -1.0, dtype=torch.float32, device=dev)
+    vs = torch.full_like(ks, -1.0)
+    return kc, vc, ks, vs
+
+
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+@pytest.mark.parametrize("dtype,H", [("bf16", 128), ("f16", 128), ("bf16", 64), ("f16", 64)])
+@pytest.mark.parametrize("T", [1, 3])
+def test_quant_append_bit_exact(gpu, kv, dtype, H, T):
+    ctx = tuple(max(c, T) for c in (1, 3, 16, 17, 31, 32, 33, 500))
+    w = small(B=len(ctx), T=T, N=8, K=4, H=H, dtype=dtype, ctx=ctx, seed=T + H, append=True)
+    # rows with exact ties: scale 1 (max |x| = qmax), halves / e4m3 midpoints
+    qmax = 127.0 if kv == "int8" else 448.0
+    ties = [2.5, -2.5, 3.5, 0.5, -0.5, 17.0, 19.0, 0.01953125, 100.0, -1.5]
+    row = torch.zeros(H)
+    row[0] = qmax
+    row[1:1 + len(ties)] = torch.tensor(ties)
+    w.k_new[0][0, 0, 0] = row.to(w.torch_dtype)
+    w.v_new[0][-1, T - 1, 3] = (-row).to(w.torch_dtype)
+    w.k_new[0][1, 0, 1] = 0.0  # a row of zeros
+    kc0, vc0, ks0, vs0 = empty_quant(w, "cpu", fill=0x5A)
+    rk, rv, rks, rvs, err = oracle.kv_append_quant(w.k_new[0], w.v_new[0], kc0, vc0, ks0, vs0,
+                                                   w.block_tables, w.context_lens, dtype, kv)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    kc, vc, ks, vs = empty_quant(w, gpu, fill=0x5A)
+    gq.kv_append_quant(wd.k_new[0], wd.v_new[0], kc, vc, ks, vs, wd.block_tables,
+                       wd.context_lens, kv=kv)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(kc.cpu().numpy(), rk)
+    np.testing.assert_array_equal(vc.cpu().numpy(), rv)
+    np.testing.assert_array_equal(ks.cpu().numpy().view(np.uint32), rks.view(np.uint32))
+    np.testing.assert_array_equal(vs.cpu().numpy().view(np.uint32), rvs.view(np.uint32))
+
+
+def test_quant_append_reports_bad_context(gpu):
+    w = small(B=2, T=2, N=8, K=2, H=128, dtype="bf16", ctx=(5, 40), seed=3, append=True)
+    wd = to(w, gpu)
+    wd.context_lens[0] = 1  # < T
+    kc, vc, ks, vs = empty_quant(w, gpu)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    gq.kv_append_quant(wd.k_new[0], wd.v_new[0], kc, vc, ks, vs, wd.block_tables,
+                       wd.context_lens, kv="int8", status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 7
+
+
+def quant_inputs(w, kv):
+    kc, ks = oracle.quantize_cache(w.k_cache[0], w.dtype, kv)
+    vc, vs = oracle.quantize_cache(w.v_cache[0], w.dtype, kv)
+    return kc, vc, ks, vs
+
+
+def run_quant(w, kv, kc, vc, ks, vs, dev, status=None):
+    wd = to(w, dev)
+    fn = gq.decode_attention_quant if w.T == 1 else gq.verify_attention_quant
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    out = fn(wd.q[0], t(kc), t(vc), t(ks), t(vs), wd.block_tables, wd.context_lens, kv=kv,
+             status=status)
+    torch.cuda.synchronize()
+    return out.float().cpu().double().numpy()
+
+
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+@pytest.mark.parametrize("T,N,K,dtype", [(1, 32, 8, "bf16"), (1, 8, 8, "f16"), (1, 64, 8, "bf16"),
+                                         (5, 64, 8, "bf16"), (3, 16, 2, "f16"), (2, 8, 1, "bf16")])
+def test_quant_attention_matches_oracle(gpu, kv, T, N, K, dtype):
+    ctx = tuple(max(c, T) for c in (1, 2, 15, 16, 17, 31, 295, 1029, 4097))
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype=dtype, ctx=ctx, seed=N + T + K)
+    kc, vc, ks, vs = quant_inputs(w, kv)
+    ref, err = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, dtype, kv=kv,
+                                k_scale=ks, v_scale=vs)
+    assert (err == 0).all()
+    got = run_quant(w, kv, kc, vc, ks, vs, gpu)
+    from helpers import assert_close
+    assert_close(got, ref, dtype, f"{kv} T={T} N={N} K={K}")
+
+
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+def test_quant_append_then_attention(gpu, kv):
+    """The decode step on a one-byte cache: the GPU's own quantized append of
+    the new token, then attention, against the oracle doing both."""
+    T = 1
+    ctx = (1, 17, 300, 2000)
+    w = small(B=len(ctx), T=T, N=32, K=8, H=128, dtype="bf16", ctx=ctx, seed=71, append=True)
+    kc, vc, ks, vs = quant_inputs(w, kv)  # the cached part (new slots hold NaN -> zeros)
+    rk, rv, rks, rvs, err = oracle.kv_append_quant(w.k_new[0], w.v_new[0], kc, vc, ks, vs,
+                                                   w.block_tables, w.context_lens, "bf16", kv)
+    assert (err == 0).all()
+    ref, _ = oracle.attention(w.q[0], rk, rv, w.block_tables, w.context_lens, "bf16", kv=kv,
+                              k_scale=rks, v_scale=rvs)
+    wd = to(w, gpu)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(gpu)  # noqa: E731
+    dkc, dvc, dks, dvs = t(kc), t(vc), t(ks), t(vs)
+    gq.kv_append_quant(wd.k_new[0], wd.v_new[0], dkc, dvc, dks, dvs, wd.block_tables,
+                       wd.context_lens, kv=kv, pdl=True)
+    out = gq.decode_attention_quant(wd.q[0], dkc, dvc, dks, dvs, wd.block_tables,
+                                    wd.context_lens, kv=kv, pdl=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(dkc.cpu().numpy(), rk)
+    from helpers import assert_close
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", f"{kv} append+attend")
+
+
+def test_quant_attention_bad_block_and_shapes(gpu):
+    w = small(B=2, T=1, N=8, K=2, H=128, dtype="bf16", ctx=(5, 40), seed=72)
+    kc, vc, ks, vs = quant_inputs(w, "int8")
+    w.block_tables[1, 1] = 10**6
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    got = run_quant(w, "int8", kc, vc, ks, vs, gpu, status=st)
+    assert int(st.item()) == 8 and (got[1] == 0).all()
+    # H = 64 has no one-byte attention kernel
+    w64 = small(B=1, T=1, N=8, K=2, H=64, dtype="bf16", ctx=(5,), seed=73)
+    kc, vc, ks, vs = quant_inputs(w64, "int8")
+    with pytest.raises(gq.GqaError):
+        run_quant(w64, "int8", kc, vc, ks, vs, gpu)
