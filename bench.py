@@ -58,6 +58,9 @@ def parse_args():
                     help="acceptance step of a verify workload: greedy longest prefix over "
                          "logits, or stochastic acceptance (speculative sampling) over "
                          "probabilities")
+    ap.add_argument("--kv", default="same", choices=["same", "int8", "e4m3"],
+                    help="KV cache element type: q's dtype, or one-byte int8 / e4m3 codes with "
+                         "a per-row fp32 scale (quantized append + attention, H = 128)")
     ap.add_argument("--unfused", action="store_true",
                     help="separate kv_append launches instead of the append fused into "
                          "the attention launch")
@@ -72,15 +75,21 @@ def dist_env():
 
 
 # ---- accounting ------------------------------------------------------------------
-def step_bytes(w):
+def step_bytes(w, kv="same"):
     from gqa_decode_attention_02_gb300 import analytic as A
 
     e = 2
+    q8 = {} if kv == "same" else {"kv_elem_bytes": 1, "row_scale_bytes": 4}
     ctx = w.context_lens.cpu().numpy()
     # mean over the layers (they differ only in their local-attention window)
-    attn = sum(A.attention_algorithmic_bytes(ctx, w.T, w.N, w.K, w.H, e, window=w.window(l))
+    attn = sum(A.attention_algorithmic_bytes(ctx, w.T, w.N, w.K, w.H, e, window=w.window(l), **q8)
                for l in range(w.layers)) // w.layers
-    app = A.kv_append_bytes(w.B, w.T, w.K, w.H, e) if w.appended else 0
+    if not w.appended:
+        app = 0
+    elif kv == "same":
+        app = A.kv_append_bytes(w.B, w.T, w.K, w.H, e)
+    else:
+        app = A.kv_append_quant_bytes(w.B, w.T, w.K, w.H, e)
     acc = A.accept_bytes(w.B, w.T, w.logits.shape[-1]) if w.logits is not None else 0
     return attn, app, acc
 
@@ -192,15 +201,23 @@ def gpu_index_for_smi(local_rank):
 
 
 # ---- CPU oracle timing --------------------------------------------------------------
-def _oracle_layer_inputs(w, layer):
+def _oracle_layer_inputs(w, layer, quant=None):
     """CPU copies of one layer's inputs with the new tokens already appended by
-    the oracle (untimed: the timed part is the oracle's attention)."""
+    the oracle (untimed: the timed part is the oracle's attention).  quant =
+    (kv, k codes, v codes, k scales, v scales) per layer (CPU): a one-byte
+    cache, returned as (q, codes_k, codes_v, scales_k, scales_v)."""
     import numpy as np
     import torch
 
     import oracle
 
     q = w.q[layer].cpu()
+    if quant is not None:
+        kv, ck, cv, sk, sv = quant
+        out = oracle.kv_append_quant(w.k_new[layer].cpu(), w.v_new[layer].cpu(), ck[layer],
+                                     cv[layer], sk[layer], sv[layer], w.block_tables.cpu(),
+                                     w.context_lens.cpu(), w.dtype, kv)
+        return (q,) + tuple(out[:4])
     kc, vc = w.k_cache[layer].cpu(), w.v_cache[layer].cpu()
     if w.appended:
         kb, vb, _ = oracle.kv_append(w.k_new[layer].cpu(), w.v_new[layer].cpu(), kc, vc,
@@ -210,7 +227,7 @@ def _oracle_layer_inputs(w, layer):
     return q, kc, vc
 
 
-def oracle_sample(w, budget_s):
+def oracle_sample(w, budget_s, quant=None):
     """Time the oracle's attention (as it stands, all host threads) on a bounded
     sample of the workload: (layer, 8-sequence chunk) units in order until the
     budget is spent.  Returns (GB/s of algorithmic attention bytes, seconds,
@@ -224,16 +241,19 @@ def oracle_sample(w, budget_s):
     ctx = w.context_lens.cpu().numpy()
     tables, lens = w.block_tables.cpu(), w.context_lens.cpu()
     done_bytes, spent, units, seqs = 0, 0.0, 0, 0
+    q8 = {} if quant is None else {"kv_elem_bytes": 1, "row_scale_bytes": 4}
     for layer in range(w.layers):
-        q, kc, vc = _oracle_layer_inputs(w, layer)
+        ins = _oracle_layer_inputs(w, layer, quant)
+        q, kc, vc = ins[:3]
+        qa = {} if quant is None else {"kv": quant[0], "k_scale": ins[3], "v_scale": ins[4]}
         for s0 in range(0, w.B, 8):
             bl = np.arange(s0, min(w.B, s0 + 8), dtype=np.int32)
             t0 = time.perf_counter()
             oracle.attention(q, kc, vc, tables, lens, w.dtype, b_list=bl, window=w.window(layer),
-                             tree_mask=w.tree_mask())
+                             tree_mask=w.tree_mask(), **qa)
             spent += time.perf_counter() - t0
             done_bytes += A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2,
-                                                        window=w.window(layer))
+                                                        window=w.window(layer), **q8)
             units += 1
             seqs += len(bl)
             if spent >= budget_s:
@@ -273,8 +293,36 @@ def run_ours(args, world, rank, local):
     L = w.layers
     attn_fn = gq.decode_attention if w.T == 1 else gq.verify_attention
     fused_fn = gq.append_decode_attention if w.T == 1 else gq.append_verify_attention
-    fused = w.appended and not args.unfused
-    ws_bytes = gq.attention_workspace_size(w.q[0], w.k_cache[0], w.block_tables)
+    q8 = args.kv != "same"
+    fused = w.appended and not args.unfused and not q8  # no fused one-byte append
+    if q8:
+        # Input preparation (outside the timed region): the cached part of each
+        # layer's cache as one-byte codes with per-row scales, quantized here
+        # with plain torch ops (absmax rule); the step's own append writes the
+        # new tokens with the library.
+        qk, qv, sk, sv = [], [], [], []
+        for l in range(L):
+            for src, codes, scales in ((w.k_cache[l], qk, sk), (w.v_cache[l], qv, sv)):
+                x = torch.nan_to_num(src.float(), nan=0.0)
+                amax = x.abs().amax(-1)  # [NB, 16, K]
+                sc = amax / (127.0 if args.kv == "int8" else 448.0)
+                y = x / sc.clamp_min(1e-30)[..., None]
+                if args.kv == "int8":
+                    c = y.round().clamp(-128, 127).to(torch.int8).view(torch.uint8)
+                else:
+                    c = y.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+                codes.append(c.contiguous())
+                scales.append(sc.permute(0, 2, 1).contiguous())
+                del x, y
+            w.k_cache[l] = w.v_cache[l] = None  # the 2-byte caches are not used
+        torch.cuda.empty_cache()
+        quant_cpu = None
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            quant_cpu = (args.kv, [c.cpu() for c in qk], [c.cpu() for c in qv],
+                         [c.cpu() for c in sk], [c.cpu() for c in sv])
+        attn_q8 = gq.decode_attention_quant if w.T == 1 else gq.verify_attention_quant
+    ws_bytes = gq.attention_workspace_size(w.q[0], qk[0] if q8 else w.k_cache[0],
+                                           w.block_tables)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     outs = [torch.empty_like(q) for q in w.q]
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -296,15 +344,24 @@ def run_ours(args, world, rank, local):
     def do_append():
         if w.appended and not fused:
             for l in range(L):
-                gq.kv_append(w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
-                             w.block_tables, w.context_lens, status=st, pdl=True)
+                if q8:
+                    gq.kv_append_quant(w.k_new[l], w.v_new[l], qk[l], qv[l], sk[l], sv[l],
+                                       w.block_tables, w.context_lens, kv=args.kv, status=st,
+                                       pdl=True)
+                else:
+                    gq.kv_append(w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
+                                 w.block_tables, w.context_lens, status=st, pdl=True)
 
     def do_attn():
         for l in range(L):
             # early_kv: the previous kernel here is the previous layer's attention
             # (or, across the graph boundary, fully ordered), which writes neither
             # the tables, the lengths nor any cache position below ctx - T.
-            if fused:
+            if q8:
+                attn_q8(w.q[l], qk[l], qv[l], sk[l], sv[l], w.block_tables, w.context_lens,
+                        kv=args.kv, out=outs[l], workspace=ws, status=st, pdl=True,
+                        early_kv=True)
+            elif fused:
                 fused_fn(w.q[l], w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
                          w.block_tables, w.context_lens, out=outs[l], workspace=ws, status=st,
                          pdl=True, early_kv=True, window=w.window(l), **extra)
@@ -414,7 +471,7 @@ def run_ours(args, world, rank, local):
             attn_ms * 1e3 / L, 3), "chain_attention_us": round(chain_ms * 1e3 / L, 3),
             "tree_over_chain": round(attn_ms / chain_ms, 4)}
 
-    attn_b, app_b, acc_b = step_bytes(w)
+    attn_b, app_b, acc_b = step_bytes(w, args.kv)
     if sampled:
         from gqa_decode_attention_02_gb300 import analytic as A
 
@@ -425,7 +482,7 @@ def run_ours(args, world, rank, local):
     attn_launch_ms = attn_ms / L
     kernel_b = attn_b + (app_b if fused else 0)  # the fused launch also does the append
     achieved = kernel_b / (attn_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload)
+    traffic = profiled_traffic(args.workload if not q8 else f"{args.workload}_{args.kv}")
 
     # e2e: host buffers -> device, the captured API calls, results -> host
     e2e = None
@@ -491,7 +548,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, spent, desc, thr = oracle_sample(w, args.cpu_seconds)
+        v, spent, desc, thr = oracle_sample(w, args.cpu_seconds, quant_cpu if q8 else None)
         cpu = {"value": v, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
                "seconds": round(spent, 2)}
 
@@ -523,6 +580,9 @@ def run_ours(args, world, rank, local):
                        "separate kv_append launches" if w.appended else "none"),
             "parallelism": f"replicas x{world}",
             "windows": list(w.windows) if w.windows else None,
+            "kv_cache": ("dtype of q" if not q8 else
+                         f"{args.kv} codes + fp32 scale per cached row (quantized append, "
+                         f"then attention)"),
         },
         "pct_of_peak": round(100 * value / world / peak, 2),
         "attention_tokens_per_s": round(world * w.B * w.T * L / (step_ms_max * 1e-3), 1),
@@ -530,7 +590,8 @@ def run_ours(args, world, rank, local):
         "breakdown_ms": {"append": round(app_ms, 5), "attention": round(attn_ms, 5),
                          "accept": round(acc_ms, 5)},
         "roofline": {"bound": "hbm",
-                     "kernel": "attention_kernel" + (" (kv_append fused)" if fused else ""),
+                     "kernel": "attention_kernel" + (" (kv_append fused)" if fused else "") + (
+                         f" (one-byte {args.kv} cache)" if q8 else ""),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic,
@@ -572,21 +633,30 @@ def run_reference(args, world, rank, local):
     units = [(l, s) for l in range(w.layers) for s in range(0, w.B, chunk)]
     K, W = args.steps, args.warmup
     times, nbytes, cache = [], [], {}
+    quant = None
+    if args.kv != "same":  # the oracle's own one-byte caches
+        codes = [oracle.quantize_cache(c, w.dtype, args.kv) for c in w.k_cache]
+        vcodes = [oracle.quantize_cache(c, w.dtype, args.kv) for c in w.v_cache]
+        quant = (args.kv, [c for c, _ in codes], [c for c, _ in vcodes],
+                 [s_ for _, s_ in codes], [s_ for _, s_ in vcodes])
+    q8 = {} if quant is None else {"kv_elem_bytes": 1, "row_scale_bytes": 4}
     for i in range(W + K):
         l, s0 = units[i % len(units)]
         if l not in cache:
             cache.clear()
-            cache[l] = _oracle_layer_inputs(w, l)
-        q, kc, vc = cache[l]
+            cache[l] = _oracle_layer_inputs(w, l, quant)
+        q, kc, vc = cache[l][:3]
+        qa = {} if quant is None else {"kv": args.kv, "k_scale": cache[l][3],
+                                       "v_scale": cache[l][4]}
         bl = np.arange(s0, min(w.B, s0 + chunk), dtype=np.int32)
         t0 = time.perf_counter()
         oracle.attention(q, kc, vc, w.block_tables, w.context_lens, w.dtype, b_list=bl,
-                         window=w.window(l), tree_mask=w.tree_mask())
+                         window=w.window(l), tree_mask=w.tree_mask(), **qa)
         dt = time.perf_counter() - t0
         if i >= W:
             times.append(dt)
             nbytes.append(A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2,
-                                                        window=w.window(l)))
+                                                        window=w.window(l), **q8))
     value = sum(nbytes) / sum(times) / 1e9
     ms = 1e3 * sum(times) / K
     desc = (f"each step: the fp64 oracle's attention over one layer x {chunk} sequences of "

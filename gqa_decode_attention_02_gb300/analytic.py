@@ -62,16 +62,19 @@ def score_matrix_bytes(n: int, cached: bool, elem_bytes: int = 4) -> int:
 
 
 def attention_algorithmic_bytes(ctx_lens: Iterable[int], T: int, N: int, K: int, H: int,
-                                elem_bytes: int, block_size: int = 16, window: int = 0) -> int:
+                                elem_bytes: int, block_size: int = 16, window: int = 0,
+                                kv_elem_bytes: int = 0, row_scale_bytes: int = 0) -> int:
     """Bytes one decode/verify attention launch must move at minimum: every
     visible cached key and value once, q in and out back, the block ids in use
     and the context lengths.  With a window W > 0 the visible positions of a
     sequence are ctx - T - W + 1 .. ctx - 1 (clipped at 0): min(ctx, W + T - 1)
-    tokens, in the blocks from the one holding the first of them."""
+    tokens, in the blocks from the one holding the first of them.  A one-byte
+    cache: kv_elem_bytes = 1 and row_scale_bytes = 4 (the fp32 scale of each
+    cached key / value row)."""
     ctx = np.asarray(list(ctx_lens), np.int64)
     B = ctx.size
     first = np.maximum(0, ctx - T - window + 1) if window > 0 else np.zeros_like(ctx)
-    kv = int((ctx - first).sum()) * 2 * K * H * elem_bytes
+    kv = int((ctx - first).sum()) * 2 * K * (H * (kv_elem_bytes or elem_bytes) + row_scale_bytes)
     qo = 2 * B * T * N * H * elem_bytes
     ids = 4 * int(((ctx + block_size - 1) // block_size - first // block_size).sum())
     return kv + qo + ids + 4 * B
@@ -88,6 +91,11 @@ def attention_flops(ctx_lens: Iterable[int], T: int, N: int, H: int, window: int
 def kv_append_bytes(B: int, T: int, K: int, H: int, elem_bytes: int) -> int:
     """Read k_new/v_new, write them into the cache, plus B lengths and B*T ids."""
     return 2 * 2 * B * T * K * H * elem_bytes + 4 * B + 4 * B * T
+
+
+def kv_append_quant_bytes(B: int, T: int, K: int, H: int, elem_bytes: int) -> int:
+    """Read k_new / v_new, write one-byte codes and a 4-byte scale per row."""
+    return 2 * B * T * K * (H * elem_bytes + H + 4) + 4 * B + 4 * B * T
 
 
 def accept_bytes(B: int, T: int, V: int) -> int:

@@ -69,7 +69,8 @@ constexpr long long kMaxRows = 8192;       // T*G: above 48 the rows go in chunk
 constexpr int kGroups = 2;                 // stage-parallel consumer groups (default)
 constexpr int kMaxThreads = 32 * (kGroups * kMaxRowWarps + 1);
 constexpr int kEnd = 1, kBad = 2;
-constexpr int kTilesPerStage = 4;          // cache blocks per pipeline stage
+constexpr int kTilesPerStage = 4;          // cache blocks per pipeline stage (2-byte cache)
+constexpr int kMaxTilesPerStage = 8;       // ... and over one-byte codes
 constexpr int kQuotaMin = 4 * kTilesPerStage;  // tiles per CTA at least: fewer split pieces
 constexpr float kRescaleGap = 8.0f;        // log2-domain slack before rescaling
 constexpr long long kMaxFlags = 65536;     // CTAs * row warps per launch
@@ -108,11 +109,12 @@ struct AttnParams {
 };
 
 // Description of one pipeline stage, written by the producer.
-struct StageMeta {
+template <int NT>
+struct StageMetaT {
     int b, k, blk_i, ntiles;  // segment (b, k); its tiles blk_i .. blk_i+ntiles-1
     int ctx, seg_start, nblk, quota;
     int cta_start, flags, pad0, pad1;
-    int blk[kTilesPerStage];  // physical block of each tile
+    int blk[NT];  // physical block of each tile
 };
 
 // KVQ: cache element kind -- 0: the dtype of q (2 bytes), GQA_KV_INT8 /
@@ -122,12 +124,15 @@ struct Cfg {
     static constexpr int kElemBytes = KVQ ? 1 : 2;
     static constexpr int kTileBytes = 16 * H * kElemBytes;  // 16 tokens x H elements
     static constexpr int kScaleBytes = KVQ ? 16 * 4 : 0;      // the tile's row scales
+    // tiles per stage (one-byte stages with eight tiles were measured slower:
+    // twice the shared memory per CTA)
+    static constexpr int kTiles = kTilesPerStage;
     // K tiles, V tiles (then K scales, V scales), rounded to the 1 KB alignment
     // of a 128-byte-swizzled TMA destination
     static constexpr int kStageBytes =
-        (2 * kTilesPerStage * (kTileBytes + kScaleBytes) + 1023) / 1024 * 1024;
+        (2 * kTiles * (kTileBytes + kScaleBytes) + 1023) / 1024 * 1024;
     // Default ring depth (two CTAs per SM fit).
-    static constexpr int kStages = KVQ ? 6 : (H == 128) ? 3 : 6;
+    static constexpr int kStages = KVQ ? 4 : (H == 128) ? 3 : 6;
     static constexpr int kHalves = KVQ ? 1 : H / 64;  // 128-byte swizzle spans per row
     static constexpr int kSteps = H / 16;  // k16 steps of QK^T == m16 tiles of PV
     static constexpr int kAccFloats = H / 4;  // accumulator floats per lane
@@ -135,7 +140,8 @@ struct Cfg {
     static constexpr int kSectionFloats = kHeaderFloats + 32 * kAccFloats;
     // stages, barriers (full/meta/empty per stage + combine), stage
     // descriptions, abort flag; the combine scratch is added per launch
-    static constexpr size_t kStageOverhead = 24 + sizeof(StageMeta);  // barriers + meta
+    using Meta = StageMetaT<kTiles>;  // one stage's description
+    static constexpr size_t kStageOverhead = 24 + sizeof(Meta);  // barriers + meta
     static constexpr size_t kFixed = 1024 + 8 + 64;  // alignment, combine barrier, flag
     static constexpr size_t kScratchBytesPerRowWarp =
         2 * 32 * (4 + kAccFloats) * sizeof(float);  // per row warp of each extra group
@@ -207,7 +213,7 @@ __device__ __forceinline__ void prefetch_q(const AttnParams& p, int b, int k) {
 // ---------------------------------------------------------------------------
 template <int H, bool GENERAL, int KVQ>
 __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const AttnParams& p,
-                         uint8_t* stages, const Bars& bar, StageMeta* meta,
+                         uint8_t* stages, const Bars& bar, typename Cfg<H, KVQ>::Meta* meta,
                          volatile int* abort_flag) {
     using C = Cfg<H, KVQ>;
     const int win = GENERAL ? p.window : 0;  // compile-time 0 for the plain kernel
@@ -318,17 +324,17 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         // 3. Stream the range, one stage (up to four tiles of a segment) at a time.
         long long x = c0;
         while (x < c1) {
-            const int run = (int)min((long long)min(kTilesPerStage, nblk - i), c1 - x);
+            const int run = (int)min((long long)min(C::kTiles, nblk - i), c1 - x);
             if (i < ids_base || i + run > ids_base + 32) {  // warp-uniform refill
                 ids_base = i;
                 ids = (i + lane < nblk)
                           ? __ldg(p.block_tables + (size_t)b * p.max_blocks + f0 + i + lane)
                           : 0;
             }
-            int blk[kTilesPerStage];
+            int blk[C::kTiles];
             bool bad = false;
 #pragma unroll
-            for (int j = 0; j < kTilesPerStage; ++j) {
+            for (int j = 0; j < C::kTiles; ++j) {
                 blk[j] = __shfl_sync(FULL, ids, min(i - ids_base + j, 31));
                 if (j < run) bad |= (blk[j] < 0 || blk[j] >= p.num_blocks);
             }
@@ -348,7 +354,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                     *abort_flag = 1;
                     aborted = true;
                 } else {
-                    StageMeta& m = meta[s];
+                    auto& m = meta[s];
                     m.b = b;
                     m.k = k;
                     m.blk_i = f0 + i;  // logical block index
@@ -360,37 +366,23 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                     m.cta_start = (int)c0;
                     m.flags = bad ? kBad : 0;
 #pragma unroll
-                    for (int j = 0; j < kTilesPerStage; ++j) m.blk[j] = blk[j];
+                    for (int j = 0; j < C::kTiles; ++j) m.blk[j] = blk[j];
                     mbar_arrive(smem_addr(&bar.meta[s]));
                     const uint32_t fb_ = smem_addr(&bar.full[s]);
                     if (bad) {
                         report(p.status, GQA_ERR_BLOCK_ID);
                         mbar_arrive(fb_);
                     } else {
-                        mbar_arrive_expect_tx(
-                            fb_, (uint32_t)(run * 2 * (C::kTileBytes + C::kScaleBytes)));
+                        mbar_arrive_expect_tx(fb_, (uint32_t)(run * 2 * C::kTileBytes));
                         const uint32_t dst = smem_addr(stages + (size_t)s * C::kStageBytes);
-                        if constexpr (KVQ != 0) {  // the tiles' row scales, 64 B each
-                            const uint32_t sdst = dst + 2 * kTilesPerStage * C::kTileBytes;
 #pragma unroll
-                            for (int j = 0; j < kTilesPerStage; ++j) {
-                                if (j < run) {
-                                    const size_t so =
-                                        ((size_t)blk[j] * p.K + (GENERAL ? kv : k)) * 16;
-                                    bulk_load(sdst + j * 64, p.k_scale + so, 64, fb_);
-                                    bulk_load(sdst + (kTilesPerStage + j) * 64, p.v_scale + so,
-                                              64, fb_);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < kTilesPerStage; ++j) {
+                        for (int j = 0; j < C::kTiles; ++j) {
                             if (j < run) {
 #pragma unroll
                                 for (int hh = 0; hh < C::kHalves; ++hh) {
                                     tma_load_3d(dst + j * C::kTileBytes + hh * 2048, tmk, fb_,
                                                 hh * 64, GENERAL ? kv : k, blk[j] * 16, pol);
-                                    tma_load_3d(dst + (kTilesPerStage + j) * C::kTileBytes +
+                                    tma_load_3d(dst + (C::kTiles + j) * C::kTileBytes +
                                                     hh * 2048,
                                                 tmv, fb_, hh * 64, GENERAL ? kv : k, blk[j] * 16,
                                                 pol);
@@ -402,6 +394,26 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             }
             aborted = __shfl_sync(FULL, aborted, 0);
             if (aborted) break;
+            if constexpr (KVQ != 0) {
+                // The stage's row scales (K and V, 64 B per tile: 512 B) with one
+                // 16-byte cp.async per lane -- a bulk copy per tile was measured
+                // to cost a quarter of the launch.  Lane 0 has waited for the slot
+                // (the warp barrier below orders the other lanes after it); each lane's
+                // copy completes as one of the full barrier's 32 extra arrivals.
+                static_assert(C::kTiles * 2 * 4 == 32, "one 16-byte piece per lane");
+                __syncwarp();  // orders every lane after lane 0's wait for the slot
+                const int s = it % p.stages;
+                const int j = lane >> 3, part = (lane >> 2) & 1, ch = lane & 3;
+                if (!bad && j < run) {
+                    const float* src = (part ? p.v_scale : p.k_scale) +
+                                       ((size_t)blk[j] * p.K + (GENERAL ? kv : k)) * 16 + ch * 4;
+                    cp_async_16(smem_addr(stages + (size_t)s * C::kStageBytes) +
+                                    2 * C::kTiles * C::kTileBytes + (part * C::kTiles + j) * 64 +
+                                    ch * 16,
+                                src);
+                }
+                cp_async_mbar_arrive_noinc(smem_addr(&bar.full[s]));
+            }
             ++it;
             x += run;
             i += run;
@@ -443,6 +455,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     }
     // 4. End marker (a stage with no data), then, after an abort, let every
     //    copy already issued land before the CTA exits.
+    bool end_sent = false;
     if (lane == 0) {
         if (!aborted) {
             const int s = it % p.stages;
@@ -452,12 +465,19 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                 meta[s].flags = kEnd;
                 mbar_arrive(smem_addr(&bar.meta[s]));
                 mbar_arrive(smem_addr(&bar.full[s]));
+                end_sent = true;
             } else {
                 report(p.status, GQA_ERR_TIMEOUT);
                 *abort_flag = 1;
                 aborted = true;
             }
         }
+    }
+    if constexpr (KVQ != 0) {  // the full barrier's 32 extra arrivals
+        end_sent = __shfl_sync(FULL, end_sent, 0);
+        if (end_sent) mbar_arrive(smem_addr(&bar.full[it % p.stages]));
+    }
+    if (lane == 0) {
         if (aborted) {
             for (int j = max(0, it - p.stages); j < it; ++j)
                 mbar_wait(smem_addr(&bar.full[j % p.stages]), (j / p.stages) & 1);
@@ -486,6 +506,9 @@ struct Consumer {
     bool bad;
     int cb, ck, cstart, cnblk, cquota, ccta0;
     int rbase, rend;  // query rows [rbase, rend) of the current chunk
+    // int8 codes enter the QK^T mma as c + 1152 (no subtraction per pair):
+    // 1152 * sum_h q_h is taken off every score of query rows 2q4 / 2q4+1
+    float qbias0[NW], qbias1[NW];
 
     __device__ int row0(int u) const { return (GENERAL ? rbase : 0) + 8 * (w * NW + u); }
     __device__ int row_end() const { return GENERAL ? rend : p.R; }
@@ -508,7 +531,7 @@ struct Consumer {
     // Start segment (b, k): reset the running state and fetch the B fragments
     // of Q^T (k = head dim, n = query row): row row0(u)+g, dims kk*16 + 2*q4 +
     // {0,1} and the same + 8.  The loads complete while the stage's tiles land.
-    __device__ void begin(const StageMeta& md) {
+    __device__ void begin(const typename C::Meta& md) {
         cb = md.b;
         if (GENERAL) {  // md.k is the virtual head (KV head, row chunk)
             ck = md.k / p.C;
@@ -532,6 +555,7 @@ struct Consumer {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[u][mt][e] = 0.f;
             const int r = row0(u) + g;
+            float qsum_row = 0.f;
             if (r < row_end()) {
                 const int t = r / p.G, gg = r % p.G;
                 const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
@@ -551,11 +575,15 @@ struct Consumer {
                         w[4 * i + 2] = v.z;
                         w[4 * i + 3] = v.w;
                     }
+                    float qs = 0.f;  // sum of this lane's 32 dims, as the mma sees them
 #pragma unroll
                     for (int kk = 0; kk < C::kSteps; ++kk) {
                         qf[u][kk][0] = to_f16x2(w[2 * kk]);
                         qf[u][kk][1] = to_f16x2(w[2 * kk + 1]);
+                        qs += Elt<false>::lo(qf[u][kk][0]) + Elt<false>::hi(qf[u][kk][0]) +
+                              Elt<false>::lo(qf[u][kk][1]) + Elt<false>::hi(qf[u][kk][1]);
                     }
+                    qsum_row = qs;
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < C::kSteps; ++kk) {
@@ -567,6 +595,14 @@ struct Consumer {
 #pragma unroll
                 for (int kk = 0; kk < C::kSteps; ++kk) qf[u][kk][0] = qf[u][kk][1] = 0u;
             }
+            if constexpr (KVQ == GQA_KV_INT8) {
+                // row g's sum over the four lanes that hold it, then the sums of
+                // query rows 2q4 and 2q4+1 (lanes 8*q4 and 8*q4+4 hold them)
+                qsum_row += __shfl_xor_sync(FULL, qsum_row, 1);
+                qsum_row += __shfl_xor_sync(FULL, qsum_row, 2);
+                qbias0[u] = 1152.f * __shfl_sync(FULL, qsum_row, 8 * q4);
+                qbias1[u] = 1152.f * __shfl_sync(FULL, qsum_row, 8 * q4 + 4);
+            }
         }
     }
 
@@ -576,9 +612,9 @@ struct Consumer {
     // warp 0 write them into the caches (each new position of KV head k lies in
     // exactly one tile, handled by exactly one CTA).  Every row warp of the
     // group patches its own copy of the same bytes before reading them.
-    __device__ bool patch_new_rows(uint32_t kbase, const StageMeta& md) {
+    __device__ bool patch_new_rows(uint32_t kbase, const typename C::Meta& md) {
         constexpr int kChunks = H / 8;  // 16-byte chunks per row
-        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
+        const uint32_t vbase = kbase + C::kTiles * C::kTileBytes;
         const int first_new = md.ctx - p.T;
         bool any = false;
         for (int j = 0; j < md.ntiles; ++j) {  // warp-uniform
@@ -624,8 +660,10 @@ struct Consumer {
     // mask, slots past the context) and scaled into the log2 domain by tsc
     // (per tile, for tokens g and g+8); running max with lazy rescale; ref*
     // get the exponent references of the stage.
-    __device__ void mask_and_max(float (&sc)[NW][kTilesPerStage][4], const StageMeta& md,
-                                 const float (&tsc)[kTilesPerStage][2], float (&ref0)[NW],
+    // NJ tiles starting at tile j0 of the stage.
+    template <int NJ>
+    __device__ void mask_and_max(float (&sc)[NW][NJ][4], const typename C::Meta& md, int j0,
+                                 const float (&tsc)[NJ][2], float (&ref0)[NW],
                                  float (&ref1)[NW]) {
         const int win = GENERAL ? p.window : 0;
         const int ntl = md.ntiles;
@@ -633,11 +671,11 @@ struct Consumer {
         for (int u = 0; u < NW; ++u) {
             float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < kTilesPerStage; ++j) {
-                const int tb = (md.blk_i + j) * 16;
+            for (int j = 0; j < NJ; ++j) {
+                const int tb = (md.blk_i + j0 + j) * 16;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[u][j][e] *= tsc[j][e >> 1];
-                if (j >= ntl) {
+                if (j0 + j >= ntl) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) sc[u][j][e] = -INFINITY;
                 } else if (tb + 15 > md.ctx - p.T - (GENERAL && p.tree_mask ? 1 : 0) ||
@@ -711,20 +749,36 @@ struct Consumer {
     //   PV, m-tile mt: fragment row m <-> dim 16*(m%8) + 2*mt + m/8,
     //     so lane g reads dims 16*g .. +15 of its four tokens (16 bytes each)
     //     and holds output dims 16*g .. +15 of its two query rows.
-    // Codes become f16 exactly; the K row scales multiply the scores, the V row
-    // scales the probabilities (the row sums use the unscaled ones).
-    __device__ void stage_q(uint32_t kbase, const StageMeta& md) {
+    // Codes become f16 with integer ops only, exactly: int8 codes as c + 1152 on
+    // the K side (1152 * sum(q) is taken off each score) and as c on the V
+    // side; e4m3 codes as their values times 2^-8 (the row scales carry the
+    // 256).  The K row scales multiply the scores, the V row scales the
+    // probabilities (the row sums use the unscaled ones).
+    __device__ void stage_q(uint32_t kbase, const typename C::Meta& md) {
         static_assert(H == 128 && NW == 1, "one-byte caches: H = 128, one tile per warp");
-        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
-        const uint32_t ksb = vbase + kTilesPerStage * C::kTileBytes;  // K row scales
-        const uint32_t vsb = ksb + kTilesPerStage * 64;                // V row scales
+        // the stage's tiles in runs of four (the online softmax takes any split)
+#pragma unroll 1
+        for (int j0 = 0; j0 < C::kTiles && j0 < md.ntiles; j0 += 4) stage_q4(kbase, md, j0);
+    }
+
+    // The factor between a code's value and the f16 it becomes (e4m3 codes turn
+    // into their values times 2^-8).
+    static constexpr float kCodeScale = KVQ == GQA_KV_E4M3 ? 256.f : 1.f;
+
+    // Tiles j0 .. j0+3 of a one-byte stage.
+    __device__ void stage_q4(uint32_t kbase, const typename C::Meta& md, int j0) {
+        constexpr int NJ = 4;
+        const uint32_t vbase = kbase + C::kTiles * C::kTileBytes;
+        const uint32_t ksb = vbase + C::kTiles * C::kTileBytes;  // K row scales
+        const uint32_t vsb = ksb + C::kTiles * 64;                // V row scales
         const int ntl = md.ntiles;
-        float sc[NW][kTilesPerStage][4];
-        float tsc[kTilesPerStage][2];
+        float sc[NW][NJ][4];
+        float tsc[NJ][2];
 #pragma unroll
-        for (int j = 0; j < kTilesPerStage; ++j) {
+        for (int jj = 0; jj < NJ; ++jj) {
+            const int j = j0 + jj;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[0][j][e] = 0.f;
+            for (int e = 0; e < 4; ++e) sc[0][jj][e] = 0.f;
             const uint32_t kt = kbase + j * C::kTileBytes;
             const uint32_t c0 = (uint32_t)(((2 * q4) ^ g) << 4);
             const uint32_t c1 = (uint32_t)(((2 * q4 + 1) ^ g) << 4);
@@ -737,33 +791,48 @@ struct Consumer {
 #pragma unroll
             for (int kk = 0; kk < C::kSteps; ++kk) {
                 uint32_t a[4];
-                a[0] = code2_to_f16x2<KVQ, false>(w0[kk]);  // token g, dims +0, +1
-                a[1] = code2_to_f16x2<KVQ, false>(w1[kk]);  // token g+8
-                a[2] = code2_to_f16x2<KVQ, true>(w0[kk]);   // token g, dims +2, +3
-                a[3] = code2_to_f16x2<KVQ, true>(w1[kk]);
-                E::mma(sc[0][j], a, qf[0][kk][0], qf[0][kk][1]);
+                if constexpr (KVQ == GQA_KV_INT8) {  // codes + 1152 (see qbias)
+                    const uint32_t x0 = w0[kk] ^ 0x80808080u, x1 = w1[kk] ^ 0x80808080u;
+                    a[0] = u8x2_to_f16x2_biased<false>(x0);  // token g, dims +0, +1
+                    a[1] = u8x2_to_f16x2_biased<false>(x1);  // token g+8
+                    a[2] = u8x2_to_f16x2_biased<true>(x0);   // token g, dims +2, +3
+                    a[3] = u8x2_to_f16x2_biased<true>(x1);
+                } else {  // e4m3 values times 2^-8 (see kCodeScale)
+                    a[0] = e4m3x2_to_f16x2_scaled<false>(w0[kk]);
+                    a[1] = e4m3x2_to_f16x2_scaled<false>(w1[kk]);
+                    a[2] = e4m3x2_to_f16x2_scaled<true>(w0[kk]);
+                    a[3] = e4m3x2_to_f16x2_scaled<true>(w1[kk]);
+                }
+                E::mma(sc[0][jj], a, qf[0][kk][0], qf[0][kk][1]);
             }
-            tsc[j][0] = p.scale_log2 * ld_shared_f32(ksb + j * 64 + g * 4);
-            tsc[j][1] = p.scale_log2 * ld_shared_f32(ksb + j * 64 + (g + 8) * 4);
+            if constexpr (KVQ == GQA_KV_INT8) {
+                sc[0][jj][0] -= qbias0[0];
+                sc[0][jj][1] -= qbias1[0];
+                sc[0][jj][2] -= qbias0[0];
+                sc[0][jj][3] -= qbias1[0];
+            }
+            tsc[jj][0] = p.scale_log2 * kCodeScale * ld_shared_f32(ksb + j * 64 + g * 4);
+            tsc[jj][1] = p.scale_log2 * kCodeScale * ld_shared_f32(ksb + j * 64 + (g + 8) * 4);
         }
         float ref0[NW], ref1[NW];
-        mask_and_max(sc, md, tsc, ref0, ref1);
+        mask_and_max(sc, md, j0, tsc, ref0, ref1);
         // ---- O^T += V^T . (P * v_scale)^T, tile by tile -----------------------
 #pragma unroll
-        for (int j = 0; j < kTilesPerStage; ++j) {
+        for (int jj = 0; jj < NJ; ++jj) {
+            const int j = j0 + jj;
             if (j >= ntl) break;  // warp-uniform
             const int tb = (md.blk_i + j) * 16;
             const bool tail = tb + 16 > md.ctx;
-            float svg = ld_shared_f32(vsb + j * 64 + g * 4);
-            float sv8 = ld_shared_f32(vsb + j * 64 + (g + 8) * 4);
+            float svg = kCodeScale * ld_shared_f32(vsb + j * 64 + g * 4);
+            float sv8 = kCodeScale * ld_shared_f32(vsb + j * 64 + (g + 8) * 4);
             if (tail) {  // slots past the context may hold anything
                 if (tb + g >= md.ctx) svg = 0.f;
                 if (tb + g + 8 >= md.ctx) sv8 = 0.f;
             }
-            const float e0 = fast_exp2(sc[0][j][0] - ref0[0]);
-            const float e1 = fast_exp2(sc[0][j][1] - ref1[0]);
-            const float e2 = fast_exp2(sc[0][j][2] - ref0[0]);
-            const float e3 = fast_exp2(sc[0][j][3] - ref1[0]);
+            const float e0 = fast_exp2(sc[0][jj][0] - ref0[0]);
+            const float e1 = fast_exp2(sc[0][jj][1] - ref1[0]);
+            const float e2 = fast_exp2(sc[0][jj][2] - ref0[0]);
+            const float e3 = fast_exp2(sc[0][jj][3] - ref1[0]);
             const uint32_t u0 = E::pack(e0, e1), u1 = E::pack(e2, e3);
             l0[0] += E::lo(u0) + E::lo(u1);
             l1[0] += E::hi(u0) + E::hi(u1);
@@ -781,8 +850,17 @@ struct Consumer {
             const uint4 x1 = ld_shared_v4(vt + t1_ * 128 + ((g ^ (t1_ & 7)) << 4));
             const uint4 x2 = ld_shared_v4(vt + t2_ * 128 + ((g ^ (t2_ & 7)) << 4));
             const uint4 x3 = ld_shared_v4(vt + t3_ * 128 + ((g ^ (t3_ & 7)) << 4));
-            const uint32_t y0[4] = {x0.x, x0.y, x0.z, x0.w}, y1[4] = {x1.x, x1.y, x1.z, x1.w};
-            const uint32_t y2[4] = {x2.x, x2.y, x2.z, x2.w}, y3[4] = {x3.x, x3.y, x3.z, x3.w};
+            uint32_t y0[4] = {x0.x, x0.y, x0.z, x0.w}, y1[4] = {x1.x, x1.y, x1.z, x1.w};
+            uint32_t y2[4] = {x2.x, x2.y, x2.z, x2.w}, y3[4] = {x3.x, x3.y, x3.z, x3.w};
+            if constexpr (KVQ == GQA_KV_INT8) {  // offset the codes by 128 once per word
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    y0[i] ^= 0x80808080u;
+                    y1[i] ^= 0x80808080u;
+                    y2[i] ^= 0x80808080u;
+                    y3[i] ^= 0x80808080u;
+                }
+            }
 #pragma unroll
             for (int mt = 0; mt < C::kSteps; ++mt) {
                 // dims 16g + 2mt (+1): byte 2*(mt&1) (+1) of word mt/2; interleave
@@ -791,30 +869,37 @@ struct Consumer {
                 const uint32_t p01 = prmt(y0[mt >> 1], y1[mt >> 1], sel);
                 const uint32_t p23 = prmt(y2[mt >> 1], y3[mt >> 1], sel);
                 uint32_t a[4];
-                a[0] = code2_to_f16x2<KVQ, false>(p01) & v01;  // dim +0, tokens 2q4, +1
-                a[1] = code2_to_f16x2<KVQ, true>(p01) & v01;   // dim +1
-                a[2] = code2_to_f16x2<KVQ, false>(p23) & v89;  // dim +0, tokens +8, +9
-                a[3] = code2_to_f16x2<KVQ, true>(p23) & v89;
+                if constexpr (KVQ == GQA_KV_INT8) {
+                    a[0] = u8x2_to_f16x2<false>(p01) & v01;  // dim +0, tokens 2q4, +1
+                    a[1] = u8x2_to_f16x2<true>(p01) & v01;   // dim +1
+                    a[2] = u8x2_to_f16x2<false>(p23) & v89;  // dim +0, tokens +8, +9
+                    a[3] = u8x2_to_f16x2<true>(p23) & v89;
+                } else {
+                    a[0] = e4m3x2_to_f16x2_scaled<false>(p01) & v01;
+                    a[1] = e4m3x2_to_f16x2_scaled<true>(p01) & v01;
+                    a[2] = e4m3x2_to_f16x2_scaled<false>(p23) & v89;
+                    a[3] = e4m3x2_to_f16x2_scaled<true>(p23) & v89;
+                }
                 E::mma(acc[0][mt], a, pb0, pb1);
             }
         }
     }
 
-    __device__ void stage(uint32_t kbase, const StageMeta& md) {
+    __device__ void stage(uint32_t kbase, const typename C::Meta& md) {
         if constexpr (KVQ != 0) {
             stage_q(kbase, md);
             return;
         }
         const int win = GENERAL ? p.window : 0;  // compile-time 0 for the plain kernel
         if (p.k_new && (md.blk_i + md.ntiles) * 16 > md.ctx - p.T) patch_new_rows(kbase, md);
-        const uint32_t vbase = kbase + kTilesPerStage * C::kTileBytes;
+        const uint32_t vbase = kbase + C::kTiles * C::kTileBytes;
         const int ntl = md.ntiles;
         // ---- S^T = K_tile . Q^T for every tile and row tile (independent chains)
-        float sc[NW][kTilesPerStage][4];
+        float sc[NW][C::kTiles][4];
 #pragma unroll
         for (int u = 0; u < NW; ++u)
 #pragma unroll
-            for (int j = 0; j < kTilesPerStage; ++j)
+            for (int j = 0; j < C::kTiles; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[u][j][e] = 0.f;
         {
@@ -826,7 +911,7 @@ struct Consumer {
                 const int chunk = ((kk & 3) << 1) + chk;
                 const uint32_t off = hh * 2048 + tok * 128 + ((chunk ^ (tok & 7)) << 4);
 #pragma unroll
-                for (int j = 0; j < kTilesPerStage; ++j) {
+                for (int j = 0; j < C::kTiles; ++j) {
                     uint32_t a[4];
                     ldsm_x4(kbase + j * C::kTileBytes + off, a);
 #pragma unroll
@@ -836,16 +921,16 @@ struct Consumer {
         }
         float ref0[NW], ref1[NW];
         {
-            float tsc[kTilesPerStage][2];
+            float tsc[C::kTiles][2];
 #pragma unroll
-            for (int j = 0; j < kTilesPerStage; ++j) tsc[j][0] = tsc[j][1] = p.scale_log2;
-            mask_and_max(sc, md, tsc, ref0, ref1);
+            for (int j = 0; j < C::kTiles; ++j) tsc[j][0] = tsc[j][1] = p.scale_log2;
+            mask_and_max(sc, md, 0, tsc, ref0, ref1);
         }
         // ---- O^T += V_tile^T . P^T, tile by tile ------------------------------------
         const int tok = (lane & 7) + (lane >> 4) * 8;
         const int dof = ((lane >> 3) & 1) * 8;
 #pragma unroll
-        for (int j = 0; j < kTilesPerStage; ++j) {
+        for (int j = 0; j < C::kTiles; ++j) {
             if (j >= ntl) break;  // warp-uniform
             uint32_t pb0[NW], pb1[NW];
 #pragma unroll
@@ -1105,7 +1190,8 @@ struct Consumer {
 // meet in shared memory and group 0 finishes the segment.
 template <int H, bool BF16, int NW, bool GENERAL, int KVQ>
 __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
-                         const StageMeta* meta, float* scratch, volatile int* abort_flag,
+                         const typename Cfg<H, KVQ>::Meta* meta, float* scratch,
+                         volatile int* abort_flag,
                          int w) {
     using C = Cfg<H, KVQ>;
     using CS = Consumer<H, BF16, NW, GENERAL, KVQ>;
@@ -1147,7 +1233,7 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
             *abort_flag = 1;
             return;
         }
-        const StageMeta md = meta[s];
+        const auto md = meta[s];
         if (md.flags & kEnd) {
             if (cur >= 0) close();
             return;
@@ -1191,7 +1277,7 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
     bar.meta = bar.full + p.stages;
     bar.empty = bar.meta + p.stages;
     bar.cbar = bar.empty + p.stages;
-    StageMeta* meta = reinterpret_cast<StageMeta*>(bar.cbar + 1);
+    auto* meta = reinterpret_cast<typename C::Meta*>(bar.cbar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + p.stages);
     float* scratch = reinterpret_cast<float*>(
         (reinterpret_cast<uintptr_t>(abort_flag + 1) + 15) & ~uintptr_t(15));
@@ -1201,7 +1287,8 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
     griddep_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
-            mbar_init(smem_addr(&bar.full[s]), 1);
+            // one-byte caches: the producer warp's 32 scale copies arrive too
+            mbar_init(smem_addr(&bar.full[s]), KVQ ? 33 : 1);
             mbar_init(smem_addr(&bar.meta[s]), 1);
             mbar_init(smem_addr(&bar.empty[s]), consumers);
         }
@@ -1241,8 +1328,13 @@ const void* pick_kernel(int H, bool bf16, int nw, bool general, int kvq) {
 }
 
 // Consumer groups for nt row warps.  (A third group was measured slower on
-// the 40-row verify workload: stages then contend for shared memory.)
-int groups_for(int /*nt*/) { return kGroups; }
+// the 40-row verify workload: stages then contend for shared memory.)  Over a
+// one-byte cache every warp spends most of its issue slots turning codes
+// into mma fragments, so few-row shapes get more groups (more warps per SM).
+int groups_for(int nt, int kvq) {
+    if (kvq) return std::max(kGroups, std::min(4, (kGroups * kMaxRowWarps) / nt));
+    return kGroups;
+}
 
 // Row warps a group may have with nw 8-row tiles per warp (48 rows at most).
 int max_row_warps(int nw) { return nw == 1 ? kMaxRowWarps : kMaxRowWarps / 2; }
@@ -1253,7 +1345,7 @@ template <int H, int KVQ>
 size_t smem_of(int nt, int nw, int stages) {
     using C = Cfg<H, KVQ>;
     return C::kFixed + (size_t)stages * (C::kStageBytes + C::kStageOverhead) +
-           (size_t)(groups_for(nt) - 1) * nt * nw * C::kScratchBytesPerRowWarp;
+           (size_t)(groups_for(nt, KVQ) - 1) * nt * nw * C::kScratchBytesPerRowWarp;
 }
 size_t smem_for(int H, int nt, int nw, int stages, int kvq) {
     if (kvq) return smem_of<128, 1>(nt, nw, stages);  // both one-byte kinds: H = 128
@@ -1262,6 +1354,13 @@ size_t smem_for(int H, int nt, int nw, int stages, int kvq) {
 int default_stages(int H, int kvq) {
     if (kvq) return Cfg<128, 1>::kStages;
     return H == 64 ? Cfg<64>::kStages : Cfg<128>::kStages;
+}
+// The largest dynamic shared memory any launch of a variant asks for.
+size_t max_smem(int H, int nw, int kvq) {
+    size_t m = 0;
+    for (int nt = 1; nt <= max_row_warps(nw); ++nt)
+        m = std::max(m, smem_for(H, nt, nw, default_stages(H, kvq), kvq));
+    return m;
 }
 
 size_t section_floats(int H) {
@@ -1299,7 +1398,10 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                           3, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          // a one-byte row of a KV head is 128 B: promoting to
+                          // 256 B would fetch the next head's row as well
+                          q8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                             : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1320,12 +1422,12 @@ int resident_ctas(int H, bool bf16, int nt, int nw, bool general, int kvq, size_
     // The attribute belongs to the kernel, whatever the row-warp count: set it
     // to the largest launch any shape makes.
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_for(H, max_row_warps(nw), nw, default_stages(H, kvq),
-                                           kvq)) !=
+                             (int)max_smem(H, nw, kvq)) !=
         cudaSuccess)
         return 0;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * (groups_for(nt) * nt + 1),
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern,
+                                                      32 * (groups_for(nt, kvq) * nt + 1),
                                                       smem) !=
         cudaSuccess)
         return 0;
@@ -1366,7 +1468,7 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     // workload: fewer warps hide less latency.  The kernel keeps both forms.)
     const int nw = 1;
     const int nt = (rows_per_chunk + 8 * nw - 1) / (8 * nw);
-    const int groups = groups_for(nt);
+    const int groups = groups_for(nt, s.kv_dtype);
     const int threads = 32 * (groups * nt + 1);
     const int kvq = s.kv_dtype;
     int stages = default_stages(s.H, kvq);

@@ -5,7 +5,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "gqa_decode.h"
@@ -206,39 +205,39 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
     return d;
 }
-// Untiled bulk copy global -> shared, completing on an mbarrier (16-byte
-// aligned addresses, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
+// 16-byte asynchronous copy global -> shared (cp.async); its completion is
+// reported to an mbarrier by cp_async_mbar_arrive_noinc, as one arrival (the
+// barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// Two signed int8 codes (bytes 0-1 of x, or 2-3 with HI) -> f16x2, exact:
-// f16 1024 + (c + 128) has the code's bits in its mantissa; subtract 1152.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Two int8 codes, already offset by 128 (bytes 0-1 of u, or 2-3 with HI) ->
+// f16x2 holding 1024 + (c + 128) = c + 1152: the caller removes the 1152.
 template <bool HI>
-__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t x) {
-    const uint32_t u = x ^ 0x80808080u;  // c + 128, as unsigned bytes
-    const uint32_t h = prmt(u, 0x64646464u, HI ? 0x4342u : 0x4140u);
+__device__ __forceinline__ uint32_t u8x2_to_f16x2_biased(uint32_t u) {
+    return prmt(u, 0x64646464u, HI ? 0x4342u : 0x4140u);
+}
+// ... and with the 1152 removed: exact int8 values.
+template <bool HI>
+__device__ __forceinline__ uint32_t u8x2_to_f16x2(uint32_t u) {
     uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(u8x2_to_f16x2_biased<HI>(u)), "r"(0x64806480u));
     return r;
 }
-// Two e4m3 codes (bytes 0-1 of x, or 2-3 with HI) -> f16x2 (exact: every e4m3
-// value is an f16 value).
+// Two e4m3 codes (bytes 0-1 of x, or 2-3 with HI) -> f16x2 holding the values
+// times 2^-8, exactly, with integer ops only: each code, sign-extended to 16
+// bits by prmt, shifted left by 7 puts e4m3's exponent and mantissa bits in
+// f16's (exponent bias 7 versus 15: a factor 2^-8, subnormals included) and
+// its sign in bit 15; the mask clears bit 14 (a copy of the sign) and the low
+// code's sign copies that the shift moved into the high half.  The caller
+// multiplies the row scales by 256.
 template <bool HI>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(HI ? (x >> 16) : (x & 0xffffu)), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-template <int KIND, bool HI>
-__device__ __forceinline__ uint32_t code2_to_f16x2(uint32_t x) {
-    if constexpr (KIND == GQA_KV_INT8)
-        return i8x2_to_f16x2<HI>(x);
-    else
-        return e4m3x2_to_f16x2<HI>(x);
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t x) {
+    const uint32_t t = prmt(x, 0u, HI ? 0xB3A2u : 0x9180u);  // sign-extended code pair
+    return (t << 7) & 0xBF80BF80u;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -118,3 +118,12 @@ def test_windowed_bytes_by_hand():
     # T=3, W=20, ctx 100: positions 78..99 (22 tokens) from block 4
     b3 = A.attention_algorithmic_bytes([100], T=3, N=4, K=2, H=64, elem_bytes=2, window=20)
     assert b3 == 22 * 2 * 2 * 64 * 2 + 2 * 3 * 4 * 64 * 2 + 4 * (7 - 4) + 4
+
+
+def test_one_byte_cache_bytes_by_hand():
+    # ctx 100, T=1, K=2, H=128: 100 tokens x 2 (K, V) x 2 heads x (128 + 4) bytes,
+    # q and out in bf16, 7 block ids, one length
+    b = A.attention_algorithmic_bytes([100], T=1, N=8, K=2, H=128, elem_bytes=2,
+                                      kv_elem_bytes=1, row_scale_bytes=4)
+    assert b == 100 * 2 * 2 * 132 + 2 * 1 * 8 * 128 * 2 + 4 * 7 + 4
+    assert A.kv_append_quant_bytes(3, 1, 2, 128, 2) == 2 * 3 * 2 * (256 + 128 + 4) + 12 + 12
