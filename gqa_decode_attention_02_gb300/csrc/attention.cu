@@ -509,6 +509,10 @@ struct Consumer {
     // int8 codes enter the QK^T mma as c + 1152 (no subtraction per pair):
     // 1152 * sum_h q_h is taken off every score of query rows 2q4 / 2q4+1
     float qbias0[NW], qbias1[NW];
+    // ... and V codes as c + 1152 too: pv* sum the scaled probabilities fed to
+    // the PV mma per row; 1152 * pv comes off the accumulator when the segment
+    // closes (before any combine or merge, which are linear in it)
+    float pv0[NW], pv1[NW];
 
     __device__ int row0(int u) const { return (GENERAL ? rbase : 0) + 8 * (w * NW + u); }
     __device__ int row_end() const { return GENERAL ? rend : p.R; }
@@ -550,6 +554,7 @@ struct Consumer {
         for (int u = 0; u < NW; ++u) {
             m0[u] = m1[u] = -INFINITY;
             l0[u] = l1[u] = 0.f;
+            pv0[u] = pv1[u] = 0.f;
 #pragma unroll
             for (int mt = 0; mt < C::kSteps; ++mt)
 #pragma unroll
@@ -724,6 +729,10 @@ struct Consumer {
                 const float f1 = need1 ? fast_exp2(m1[u] - n1) : 1.f;
                 l0[u] *= f0;
                 l1[u] *= f1;
+                if constexpr (KVQ == GQA_KV_INT8) {
+                    pv0[u] *= f0;
+                    pv1[u] *= f1;
+                }
 #pragma unroll
                 for (int mt = 0; mt < C::kSteps; ++mt) {
                     acc[u][mt][0] *= f0;
@@ -836,8 +845,13 @@ struct Consumer {
             const uint32_t u0 = E::pack(e0, e1), u1 = E::pack(e2, e3);
             l0[0] += E::lo(u0) + E::lo(u1);
             l1[0] += E::hi(u0) + E::hi(u1);
-            const uint32_t pb0 = movm_t(E::pack(e0 * svg, e1 * svg));  // tokens 2q4, +1
-            const uint32_t pb1 = movm_t(E::pack(e2 * sv8, e3 * sv8));  // tokens 2q4+8, +9
+            const uint32_t w0p = E::pack(e0 * svg, e1 * svg), w1p = E::pack(e2 * sv8, e3 * sv8);
+            if constexpr (KVQ == GQA_KV_INT8) {
+                pv0[0] += E::lo(w0p) + E::lo(w1p);
+                pv1[0] += E::hi(w0p) + E::hi(w1p);
+            }
+            const uint32_t pb0 = movm_t(w0p);  // tokens 2q4, +1
+            const uint32_t pb1 = movm_t(w1p);  // tokens 2q4+8, +9
             uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
             if (tail) {
                 const int pb = tb + 2 * q4;
@@ -869,11 +883,11 @@ struct Consumer {
                 const uint32_t p01 = prmt(y0[mt >> 1], y1[mt >> 1], sel);
                 const uint32_t p23 = prmt(y2[mt >> 1], y3[mt >> 1], sel);
                 uint32_t a[4];
-                if constexpr (KVQ == GQA_KV_INT8) {
-                    a[0] = u8x2_to_f16x2<false>(p01) & v01;  // dim +0, tokens 2q4, +1
-                    a[1] = u8x2_to_f16x2<true>(p01) & v01;   // dim +1
-                    a[2] = u8x2_to_f16x2<false>(p23) & v89;  // dim +0, tokens +8, +9
-                    a[3] = u8x2_to_f16x2<true>(p23) & v89;
+                if constexpr (KVQ == GQA_KV_INT8) {  // c + 1152 (see pv0 / pv1)
+                    a[0] = u8x2_to_f16x2_biased<false>(p01) & v01;  // dim +0, tokens 2q4, +1
+                    a[1] = u8x2_to_f16x2_biased<true>(p01) & v01;   // dim +1
+                    a[2] = u8x2_to_f16x2_biased<false>(p23) & v89;  // dim +0, tokens +8, +9
+                    a[3] = u8x2_to_f16x2_biased<true>(p23) & v89;
                 } else {
                     a[0] = e4m3x2_to_f16x2_scaled<false>(p01) & v01;
                     a[1] = e4m3x2_to_f16x2_scaled<true>(p01) & v01;
@@ -1046,6 +1060,24 @@ struct Consumer {
             for (int o = 4; o < 32; o <<= 1) {
                 l0[u] += __shfl_xor_sync(FULL, l0[u], o);
                 l1[u] += __shfl_xor_sync(FULL, l1[u], o);
+            }
+        }
+        if constexpr (KVQ == GQA_KV_INT8) {  // remove the V codes' offset
+#pragma unroll
+            for (int u = 0; u < NW; ++u) {
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    pv0[u] += __shfl_xor_sync(FULL, pv0[u], o);
+                    pv1[u] += __shfl_xor_sync(FULL, pv1[u], o);
+                }
+                const float b0 = 1152.f * pv0[u], b1 = 1152.f * pv1[u];
+#pragma unroll
+                for (int mt = 0; mt < C::kSteps; ++mt) {
+                    acc[u][mt][0] -= b0;
+                    acc[u][mt][1] -= b1;
+                    acc[u][mt][2] -= b0;
+                    acc[u][mt][3] -= b1;
+                }
             }
         }
     }

@@ -215,17 +215,11 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 // Two int8 codes, already offset by 128 (bytes 0-1 of u, or 2-3 with HI) ->
-// f16x2 holding 1024 + (c + 128) = c + 1152: the caller removes the 1152.
+// f16x2 holding 1024 + (c + 128) = c + 1152, exactly: the caller accounts
+// for the 1152.
 template <bool HI>
 __device__ __forceinline__ uint32_t u8x2_to_f16x2_biased(uint32_t u) {
     return prmt(u, 0x64646464u, HI ? 0x4342u : 0x4140u);
-}
-// ... and with the 1152 removed: exact int8 values.
-template <bool HI>
-__device__ __forceinline__ uint32_t u8x2_to_f16x2(uint32_t u) {
-    uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(u8x2_to_f16x2_biased<HI>(u)), "r"(0x64806480u));
-    return r;
 }
 // Two e4m3 codes (bytes 0-1 of x, or 2-3 with HI) -> f16x2 holding the values
 // times 2^-8, exactly, with integer ops only: each code, sign-extended to 16
