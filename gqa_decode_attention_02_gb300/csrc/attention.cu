@@ -852,12 +852,6 @@ struct Consumer {
             }
             const uint32_t pb0 = movm_t(w0p);  // tokens 2q4, +1
             const uint32_t pb1 = movm_t(w1p);  // tokens 2q4+8, +9
-            uint32_t v01 = 0xffffffffu, v89 = 0xffffffffu;
-            if (tail) {
-                const int pb = tb + 2 * q4;
-                v01 = (pb < md.ctx ? 0x0000ffffu : 0u) | (pb + 1 < md.ctx ? 0xffff0000u : 0u);
-                v89 = (pb + 8 < md.ctx ? 0x0000ffffu : 0u) | (pb + 9 < md.ctx ? 0xffff0000u : 0u);
-            }
             const uint32_t vt = vbase + j * C::kTileBytes;
             const int t0_ = 2 * q4, t1_ = t0_ + 1, t2_ = t0_ + 8, t3_ = t0_ + 9;
             const uint4 x0 = ld_shared_v4(vt + t0_ * 128 + ((g ^ (t0_ & 7)) << 4));
@@ -883,16 +877,18 @@ struct Consumer {
                 const uint32_t p01 = prmt(y0[mt >> 1], y1[mt >> 1], sel);
                 const uint32_t p23 = prmt(y2[mt >> 1], y3[mt >> 1], sel);
                 uint32_t a[4];
+                // (no masking of slots past the context: every code becomes a
+                // finite f16, and those slots' probabilities are exactly 0)
                 if constexpr (KVQ == GQA_KV_INT8) {  // c + 1152 (see pv0 / pv1)
-                    a[0] = u8x2_to_f16x2_biased<false>(p01) & v01;  // dim +0, tokens 2q4, +1
-                    a[1] = u8x2_to_f16x2_biased<true>(p01) & v01;   // dim +1
-                    a[2] = u8x2_to_f16x2_biased<false>(p23) & v89;  // dim +0, tokens +8, +9
-                    a[3] = u8x2_to_f16x2_biased<true>(p23) & v89;
+                    a[0] = u8x2_to_f16x2_biased<false>(p01);  // dim +0, tokens 2q4, +1
+                    a[1] = u8x2_to_f16x2_biased<true>(p01);   // dim +1
+                    a[2] = u8x2_to_f16x2_biased<false>(p23);  // dim +0, tokens +8, +9
+                    a[3] = u8x2_to_f16x2_biased<true>(p23);
                 } else {
-                    a[0] = e4m3x2_to_f16x2_scaled<false>(p01) & v01;
-                    a[1] = e4m3x2_to_f16x2_scaled<true>(p01) & v01;
-                    a[2] = e4m3x2_to_f16x2_scaled<false>(p23) & v89;
-                    a[3] = e4m3x2_to_f16x2_scaled<true>(p23) & v89;
+                    a[0] = e4m3x2_to_f16x2_scaled<false>(p01);
+                    a[1] = e4m3x2_to_f16x2_scaled<true>(p01);
+                    a[2] = e4m3x2_to_f16x2_scaled<false>(p23);
+                    a[3] = e4m3x2_to_f16x2_scaled<true>(p23);
                 }
                 E::mma(acc[0][mt], a, pb0, pb1);
             }
