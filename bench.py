@@ -50,6 +50,9 @@ def parse_args():
     ap.add_argument("--workload", default="cfg4",
                     choices=["cfg1", "cfg2", "cfg3", "cfg4", "cfg5", "hybrid", "tree"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=None,
+                    help="a batch of B sequences drawn by the same workload recipe, for "
+                         "small profiling captures")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -289,7 +292,7 @@ def run_ours(args, world, rank, local):
 
             dist.barrier()
 
-    w = workloads.make(args.workload, device=dev)
+    w = workloads.make(args.workload, device=dev, B=args.batch)
     L = w.layers
     attn_fn = gq.decode_attention if w.T == 1 else gq.verify_attention
     fused_fn = gq.append_decode_attention if w.T == 1 else gq.append_verify_attention
@@ -627,7 +630,7 @@ def run_reference(args, world, rank, local):
     from gqa_decode_attention_02_gb300 import workloads
 
     oracle.build()
-    w = workloads.make(args.workload)  # CPU tensors
+    w = workloads.make(args.workload, B=args.batch)  # CPU tensors
     ctx = w.context_lens.numpy()
     chunk = 8
     units = [(l, s) for l in range(w.layers) for s in range(0, w.B, chunk)]

@@ -125,3 +125,41 @@ def test_tree_verify_workload(gpu, fused):
     head, five row chunks), through the bench's calls."""
     w, _ = check_workload("tree", gpu, fused=fused)
     assert w.T == 26 and len(w.tree) == 26
+
+
+@pytest.mark.parametrize("name,kv,sample", [("cfg4", "int8", 16), ("cfg3", "e4m3", 6),
+                                            ("cfg5", "int8", None)])
+def test_one_byte_cache_at_full_size(gpu, name, kv, sample):
+    """The named workloads with a one-byte cache: the cached part quantized by
+    the oracle, the new tokens appended by the library's quantized append
+    (bit-exact on the checked sequences' blocks), then attention, against the
+    oracle on a seeded sample of sequences."""
+    w = workloads.make(name)
+    ctx = w.context_lens.numpy()
+    bl = sample_sequences(ctx, sample, 2) if sample else np.arange(w.B, dtype=np.int32)
+    kc, ks = oracle.quantize_cache(w.k_cache[0], w.dtype, kv)
+    vc, vs = oracle.quantize_cache(w.v_cache[0], w.dtype, kv)
+    rk, rv, rks, rvs, err = oracle.kv_append_quant(w.k_new[0], w.v_new[0], kc, vc, ks, vs,
+                                                   w.block_tables, w.context_lens, w.dtype, kv)
+    assert (err == 0).all()
+    ref, err = oracle.attention(w.q[0], rk, rv, w.block_tables, w.context_lens, w.dtype,
+                                b_list=bl, kv=kv, k_scale=rks, v_scale=rvs)
+    assert (err == 0).all()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(gpu)  # noqa: E731
+    dkc, dvc, dks, dvs = t(kc), t(vc), t(ks), t(vs)
+    del kc, vc
+    bt, cl = w.block_tables.to(gpu), w.context_lens.to(gpu)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    gq.kv_append_quant(w.k_new[0].to(gpu), w.v_new[0].to(gpu), dkc, dvc, dks, dvs, bt, cl, kv=kv,
+                       status=st, pdl=True)
+    fn = gq.decode_attention_quant if w.T == 1 else gq.verify_attention_quant
+    out = fn(w.q[0].to(gpu), dkc, dvc, dks, dvs, bt, cl, kv=kv, status=st, pdl=True,
+             early_kv=True)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    tb = w.block_tables[torch.as_tensor(bl).long()]
+    blocks = torch.unique(tb[tb != workloads.INT32_MAX]).long()
+    np.testing.assert_array_equal(dkc[blocks.to(gpu)].cpu().numpy(), rk[blocks.numpy()])
+    np.testing.assert_array_equal(dvs[blocks.to(gpu)].cpu().numpy(), rvs[blocks.numpy()])
+    got = out.cpu()[torch.as_tensor(bl).long()].double().numpy()
+    assert_close(got, ref, w.dtype, f"{name} {kv} cache")
