@@ -98,8 +98,10 @@ def attention_workspace_size(q, k_cache, block_tables, scale=None, window=0) -> 
 
 def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, scale,
                workspace, status, stream, pdl, early_kv, k_new=None, v_new=None, window=0,
-               tree_mask=None):
+               tree_mask=None, engine="auto"):
     _lib._need(q, "q", ndim=4)
+    if engine not in _lib.ENGINES:
+        raise ValueError(f"engine must be one of {sorted(_lib.ENGINES)}, got {engine!r}")
     if tree_mask is not None:
         _lib._need(tree_mask, "tree_mask", torch.int64, 2)  # uint64 bits, held as int64
         if tuple(tree_mask.shape) != tuple(q.shape[:2]):
@@ -112,7 +114,8 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
     _lib._need(v_cache, "v_cache", q.dtype, 4)
     _lib._need(block_tables, "block_tables", torch.int32, 2)
     _lib._need(context_lens, "context_lens", torch.int32, 1)
-    flags = (_lib.FLAG_PDL if pdl else 0) | (_lib.FLAG_EARLY_KV if early_kv else 0)
+    flags = ((_lib.FLAG_PDL if pdl else 0) | (_lib.FLAG_EARLY_KV if early_kv else 0)
+             | _lib.ENGINES[engine])
     shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags, window=window)
     if out is None:
         out = torch.empty_like(q)
@@ -137,43 +140,49 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
 
 def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
                      workspace=None, status=None, stream=None, pdl=False, early_kv=False,
-                     window=0):
+                     window=0, engine="auto"):
     """gqa_decode_attention (T == 1).  q [B,1,N,H] -> out [B,1,N,H].
     pdl / early_kv select GQA_FLAG_PDL / GQA_FLAG_EARLY_KV (see the C header);
-    window > 0 is local attention over each query's last `window` positions."""
+    window > 0 is local attention over each query's last `window` positions;
+    engine "warp" / "tmem" forces the mma.sync / tcgen05 kernel ("auto": by
+    shape, GQA_FLAG_WARP_MMA / GQA_FLAG_TENSOR_MEMORY)."""
     return _attention("gqa_decode_attention", q, k_cache, v_cache, block_tables, context_lens,
-                      out, scale, workspace, status, stream, pdl, early_kv, window=window)
+                      out, scale, workspace, status, stream, pdl, early_kv, window=window,
+                      engine=engine)
 
 
 def verify_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=None, scale=None,
                      workspace=None, status=None, stream=None, pdl=False, early_kv=False,
-                     window=0, tree_mask=None):
+                     window=0, tree_mask=None, engine="auto"):
     """gqa_verify_attention (T >= 1, causal among the T new tokens), or with
     tree_mask (int64 [B,T] holding the uint64 mask rows)
     gqa_tree_verify_attention."""
     return _attention("gqa_verify_attention", q, k_cache, v_cache, block_tables, context_lens,
                       out, scale, workspace, status, stream, pdl, early_kv, window=window,
-                      tree_mask=tree_mask)
+                      tree_mask=tree_mask, engine=engine)
 
 
 def append_decode_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
                             out=None, scale=None, workspace=None, status=None, stream=None,
-                            pdl=False, early_kv=False, window=0):
+                            pdl=False, early_kv=False, window=0, engine="auto"):
     """gqa_append_decode_attention: kv_append + decode_attention in one launch
     (T == 1).  Writes k_new/v_new into the caches and returns out."""
     return _attention("gqa_append_decode_attention", q, k_cache, v_cache, block_tables,
                       context_lens, out, scale, workspace, status, stream, pdl, early_kv,
-                      k_new=k_new, v_new=v_new, window=window)
+                      k_new=k_new, v_new=v_new, window=window, engine=engine)
 
 
 def append_verify_attention(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, *,
                             out=None, scale=None, workspace=None, status=None, stream=None,
-                            pdl=False, early_kv=False, window=0, tree_mask=None):
+                            pdl=False, early_kv=False, window=0, tree_mask=None,
+                            engine="auto"):
     """gqa_append_verify_attention: kv_append + verify_attention in one launch
-    (gqa_append_tree_verify_attention with tree_mask)."""
+    (gqa_append_tree_verify_attention with tree_mask; with the tensor-memory
+    kernel the append is a launch of its own just before)."""
     return _attention("gqa_append_verify_attention", q, k_cache, v_cache, block_tables,
                       context_lens, out, scale, workspace, status, stream, pdl, early_kv,
-                      k_new=k_new, v_new=v_new, window=window, tree_mask=tree_mask)
+                      k_new=k_new, v_new=v_new, window=window, tree_mask=tree_mask,
+                      engine=engine)
 
 
 def _attention_quant(fn_name, q, k_cache, v_cache, k_scale, v_scale, block_tables,

@@ -55,6 +55,9 @@ class Shape(ctypes.Structure):
 
 FLAG_PDL = 1
 FLAG_EARLY_KV = 2
+FLAG_WARP_MMA = 4
+FLAG_TENSOR_MEMORY = 8
+ENGINES = {"auto": 0, "warp": FLAG_WARP_MMA, "tmem": FLAG_TENSOR_MEMORY}
 
 
 EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",

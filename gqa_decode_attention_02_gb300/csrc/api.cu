@@ -46,12 +46,30 @@ gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, con
         return GQA_ERR_ALIGN;
     if (fused && (!aligned16(k_new) || !aligned16(v_new))) return GQA_ERR_ALIGN;
     if (tree_mask && s->window > 0) return GQA_ERR_SHAPE;  // not combined
+    if (tree_mask && s->T > 64) return GQA_ERR_SHAPE;      // one 64-bit row per new token
     if (tree_mask && (reinterpret_cast<uintptr_t>(tree_mask) & 7u) != 0) return GQA_ERR_ALIGN;
+    const bool force_warp = (s->flags & GQA_FLAG_WARP_MMA) != 0;
+    const bool force_tc = (s->flags & GQA_FLAG_TENSOR_MEMORY) != 0;
+    if (force_warp && force_tc) return GQA_ERR_SHAPE;
+    if (force_tc && !gqa::tc_attention_supported(*s)) return GQA_ERR_SHAPE;
     gqa::AttnPlan plan;
     st = gqa::attention_plan(*s, tree_mask != nullptr, &plan);
     if (st != GQA_OK) return st;
     if (!workspace || ws_bytes < plan.workspace) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_ALIGN;
+    if (force_tc || (!force_warp && gqa::tc_attention_preferred(*s))) {
+        if (ws_bytes < gqa::tc_workspace_bytes(*s, plan.flags_bytes)) return GQA_ERR_WORKSPACE;
+        cudaStream_t cs = static_cast<cudaStream_t>(stream);
+        if (fused) {
+            st = gqa::launch_kv_append(*s, k_new, v_new, const_cast<void*>(k_cache),
+                                       const_cast<void*>(v_cache), block_tables, context_lens,
+                                       dev_status, cs);
+            if (st != GQA_OK) return st;
+        }
+        return gqa::launch_tc_attention(*s, q, k_cache, v_cache, block_tables, context_lens,
+                                        tree_mask, out, workspace, plan.flags_bytes, dev_status,
+                                        cs);
+    }
     return gqa::launch_attention(*s, plan, q, fused ? k_new : nullptr, fused ? v_new : nullptr,
                                  k_cache, v_cache, block_tables, context_lens, tree_mask,
                                  k_scale, v_scale, out, workspace, dev_status,
@@ -117,12 +135,14 @@ gqa_status gqa_kv_append_quant(const gqa_shape* shape, const void* k_new, const 
 
 size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     if (check_common(shape) != GQA_OK) return 0;
-    // the larger of the two kernel variants' needs (they normally agree)
+    // the largest need of the kernels that may serve the shape
     gqa::AttnPlan plain, general;
     if (gqa::attention_plan(*shape, false, &plain) != GQA_OK) return 0;
     if (shape->kv_dtype != GQA_KV_SAME) return plain.workspace;  // no general variant
     if (gqa::attention_plan(*shape, true, &general) != GQA_OK) return 0;
-    return plain.workspace > general.workspace ? plain.workspace : general.workspace;
+    size_t w = plain.workspace > general.workspace ? plain.workspace : general.workspace;
+    const size_t tc = gqa::tc_workspace_bytes(*shape, plain.flags_bytes);  // 0: not served
+    return tc > w ? tc : w;
 }
 
 gqa_status gqa_workspace_clear(void* workspace, size_t bytes, void* stream) {

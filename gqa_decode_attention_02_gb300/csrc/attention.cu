@@ -1465,6 +1465,10 @@ int resident_ctas(int H, bool bf16, int nt, int nw, bool general, int kvq, size_
 
 }  // namespace
 
+bool make_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
+    return encode_cache_map(m, base, s);
+}
+
 int device_sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;

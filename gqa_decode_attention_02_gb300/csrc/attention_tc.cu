@@ -1,0 +1,794 @@
+// attention_tc.cu -- decode / verify / tree-verify attention on the fifth-
+// generation tensor cores: tcgen05.mma with its accumulators in tensor memory.
+//
+// Same computation as attention.cu (CS336 lecture 10 §"Арифметическая
+// интенсивность инференса": Y = softmax(Q K^T) V of the new tokens over the
+// cached keys and values, GQA from §"Уменьшаем KV-кэш", paged reads from
+// §"PagedAttention"; the tree mask of "Болжау арқылы Sonar модельдерін
+// жылдамдату" §"EAGLE").  It serves the shapes where the contraction is dense:
+// many query rows per KV head (long drafts, draft trees, MQA with many query
+// heads), where the warp-level mma of attention.cu runs out of issue slots.
+//
+// Work order.  As in attention.cu: segments (sequence b, virtual head v) in
+// b-major order, a virtual head being a KV head and a chunk of at most 128 of
+// its T*G query rows; each segment is ceil(ctx_b / 16) tiles (cache blocks).
+// CTA c takes tiles [c*quota, (c+1)*quota) of that order (one CTA per SM), so
+// every SM streams the same number of bytes however ragged the batch.  A
+// segment cut by a range boundary leaves per-piece partial results (O
+// unnormalized, running max, sum) in the workspace; the piece that finishes
+// last merges them in piece order (a deterministic result) with log-sum-exp
+// weights -- the context split of FlashDecoding named in §"PagedAttention".
+//
+// One CTA: warp 0 MMA issuer and tensor-memory owner, warps 1..2 producers
+// (TMA), warps 3..10 softmax (two threads per query row, each on 32 of a
+// stage's 64 columns; tensor-memory lane = row).
+// A stage is up to 64 tokens (four 16-token cache blocks of one piece):
+//   S[128 x 64]   = Q[128 x 128] . K^T   8 MMAs, Q from tensor memory, K K-major
+//   rows: mask (causal, tree, past the context) as one 64-bit word, running
+//         max with a lazy rescale of O, P = exp2(S*scale - max) in q's dtype
+//   O[128 x 128] += P[128 x 64] . V       4 MMAs, P from tensor memory, V MN-major
+// Tensor memory (512 columns, lane = query row) holds O, S, P and the piece's
+// Q.  The MMA issuer starts QK^T of stage n + 1 as soon as S(n) has been
+// read, so it overlaps the softmax of stage n.  Shared memory is a ring of
+// six stages (K and V, each two 64-dim halves of 64 token rows x 128 B,
+// 128-byte swizzled): 192 KB in flight per SM.  V rows of a stage that hold
+// no data (past the context, or unused tiles) are zeroed before the PV
+// product: their probabilities are 0, but stale bytes could be NaN.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "launch.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace gqa {
+namespace {
+
+constexpr int kRowsTc = 128;                     // query rows per segment (MMA M)
+constexpr int kStagesTc = 6;
+constexpr int kProducerWarps = 2;                // TMA issuers (each takes blocks of a stage)
+constexpr int kSoftmaxWarp0 = 1 + kProducerWarps; // warp 0 issues the MMAs
+constexpr int kSoftmaxThreads = 256;             // eight softmax warps
+constexpr int kThreadsTc = 32 * kSoftmaxWarp0 + kSoftmaxThreads;
+constexpr int kHalfBytes = 64 * 128;             // 64 rows of one 64-dim half: 8 KB
+constexpr int kStageBytesTc = 4 * kHalfBytes;    // K then V, two halves each: 32 KB
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns (32 bits each; lane = query row): O fp32, S fp32,
+// P two 16-bit values per column, Q two 16-bit values per column
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 192, kColQ = 256;
+constexpr float kGapTc = 8.0f;                   // log2-domain slack before rescaling O
+constexpr int kQuotaMinTc = 16;                  // tiles per CTA at least: fewer split pieces
+constexpr int kPartFloats = 130 * kRowsTc;       // a partial: O^T [128][128], max, sum
+constexpr int kTcMinRows = 64;                   // rows per KV head from which it is picked
+constexpr unsigned FULLM = 0xffffffffu;
+
+struct TcParams {
+    const void* q;
+    void* out;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const uint64_t* tree_mask;  // nullptr: causal chain among the new tokens
+    int32_t* status;
+    int32_t* flags;             // per CTA: pieces of the split segment it starts, done
+    float* partials;            // [2 * grid][kPartFloats]
+    int B, T, N, K, G, R;
+    int C, Rc, KC;              // row chunks per KV head, rows per chunk, virtual heads
+    int max_blocks, num_blocks;
+    float scale_log2;
+};
+
+struct TcSmem {
+    uint64_t full[kStagesTc];   // stage data landed (TMA transaction bytes)
+    uint64_t empty[kStagesTc];  // the PV product of the stage completed
+    uint64_t q_ready;           // softmax threads wrote the piece's Q rows (tensor memory)
+    uint64_t s_ready;           // QK^T of a stage completed
+    uint64_t s_free;            // softmax threads read S
+    uint64_t p_ready;           // softmax threads wrote P (and zeroed stale V rows)
+    uint64_t o_ready;           // PV of a stage completed
+    uint64_t done;              // every MMA completed (before freeing tensor memory)
+    long long c0, c1, base;     // the CTA's tile range; first tile of segment (b0, 0)
+    int b0, quota;
+    int merge;                  // this CTA merges the split segment just finished
+    uint32_t tmem_base;
+    int bad[kStagesTc];         // the stage's blocks include an invalid id
+    volatile int abort_flag;
+    float xmax[2][2 * kRowsTc]; // per stage parity: the two halves' maxima of each row
+    float xl[2 * kRowsTc];      // the two halves' sums of each row
+};
+
+__device__ __forceinline__ int tc_nblk(const TcParams& p, int b) {
+    const int ctx = __ldg(p.context_lens + b);
+    return (ctx >= p.T && ctx >= 1 && ctx <= p.max_blocks * 16) ? (ctx + 15) >> 4 : 0;
+}
+
+__device__ __forceinline__ void tc_abort(TcSmem& sm, const TcParams& p) {
+    report(p.status, GQA_ERR_TIMEOUT);
+    sm.abort_flag = 1;
+}
+
+// Waits until stage n has landed.
+__device__ __forceinline__ bool stage_landed(TcSmem& sm, int n) {
+    return mbar_wait(smem_addr(&sm.full[n % kStagesTc]), (n / kStagesTc) & 1);
+}
+
+// All softmax threads (named barrier 1); the two warps of one lane quarter
+// (barriers 2..5).
+__device__ __forceinline__ void softmax_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+}
+__device__ __forceinline__ void pair_sync(int quarter) {
+    asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
+}
+
+// One piece: tiles [t0, t1) of segment (b, v), whose first tile is number
+// `first` of the whole order and which has nb tiles.
+struct TcPiece {
+    int b, v, nb, t0, t1;
+    long long first;
+};
+
+// Walks the pieces of the CTA's range in order (every role walks the same).
+struct TcWalker {
+    long long pos, c1, base;
+    int b, v, nb;
+    __device__ void init(const TcSmem& sm, const TcParams& p) {
+        pos = sm.c0;
+        c1 = sm.c1;
+        base = sm.base;
+        b = sm.b0;
+        v = 0;
+        nb = (pos < c1) ? tc_nblk(p, b) : 0;
+    }
+    __device__ bool next(const TcParams& p, TcPiece& pc) {
+        while (pos < c1) {
+            const long long first = base + (long long)v * nb;
+            if (nb > 0 && pos < first + nb) {
+                const long long e = min(c1, first + nb);
+                pc.b = b;
+                pc.v = v;
+                pc.nb = nb;
+                pc.t0 = (int)(pos - first);
+                pc.t1 = (int)(e - first);
+                pc.first = first;
+                pos = e;
+                return true;
+            }
+            if (nb > 0 && ++v < p.KC) continue;
+            base += (long long)p.KC * nb;
+            v = 0;
+            if (++b >= p.B) break;
+            nb = tc_nblk(p, b);
+        }
+        pos = c1;
+        return false;
+    }
+};
+
+// Warp 0, all lanes: tiles per sequence, their prefix sum, this CTA's range
+// and the sequence it starts in.
+__device__ void tc_plan(const TcParams& p, TcSmem& sm) {
+    const int lane = threadIdx.x & 31;
+    const int per = (p.B + 31) / 32;
+    const int lo = min(p.B, lane * per), hi = min(p.B, lo + per);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) local += tc_nblk(p, b);
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(FULLM, incl, o);
+        if (lane >= o) incl += x;
+    }
+    const int excl = incl - local;
+    const long long total = (long long)p.KC * __shfl_sync(FULLM, incl, 31);
+    const int quota = (int)max((total + gridDim.x - 1) / gridDim.x, (long long)kQuotaMinTc);
+    const long long c0 = (long long)blockIdx.x * quota;
+    const long long c1 = min(total, c0 + quota);
+    const bool mine = c0 < c1 && (long long)p.KC * excl <= c0 && c0 < (long long)p.KC * incl;
+    const unsigned owners = __ballot_sync(FULLM, mine);
+    if (lane == 0) {
+        sm.c0 = c0;
+        sm.c1 = c0 < c1 ? c1 : c0;
+        sm.quota = quota;
+        sm.b0 = 0;
+        sm.base = 0;
+    }
+    __syncwarp();
+    if (owners != 0 && lane == __ffs(owners) - 1) {
+        long long acc = (long long)p.KC * excl;
+        for (int b = lo; b < hi; ++b) {
+            const long long n = (long long)p.KC * tc_nblk(p, b);
+            if (c0 < acc + n) {
+                sm.b0 = b;
+                sm.base = acc;
+                break;
+            }
+            acc += n;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// kProducerWarps warps share each stage: warp pw loads the blocks j of the
+// stage with j % kProducerWarps == pw (K and V, two 64-dim halves each, one
+// box per lane) and arrives on the stage's barrier with its own byte count.
+// Block ids are read 32 at a time (a window of eight stages, one id per lane),
+// the next window while the current one is in use.
+__device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const TcParams& p,
+                            uint8_t* stages, TcSmem& sm, int pw) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0 && pw == 0) {
+        tma_prefetch_desc(tmk);
+        tma_prefetch_desc(tmv);
+    }
+    // row chunks read a block once per chunk: keep it in L2 for them
+    const uint64_t pol = p.C > 1 ? policy_evict_normal() : policy_evict_first();
+    // this lane's box: block bj of the stage, K (kvsel 0) or V, half bh
+    constexpr int kBlocksPerWarp = 4 / kProducerWarps;
+    const int bj = pw + kProducerWarps * (lane >> 2), kvsel = (lane >> 1) & 1, bh = lane & 1;
+    const bool boxer = lane < 4 * kBlocksPerWarp;
+    const CUtensorMap* tm = kvsel ? tmv : tmk;
+    TcWalker wk;
+    wk.init(sm, p);
+    TcPiece pc;
+    int it = 0;
+    bool aborted = false;
+    while (!aborted && wk.next(p, pc)) {
+        const int kv = pc.v / p.C;
+        const int32_t* table = p.block_tables + (size_t)pc.b * p.max_blocks;
+        int win = pc.t0;  // first tile of the current window
+        int ids = (win + lane < pc.t1) ? __ldg(table + win + lane) : 0;
+        int nxt = (win + 32 + lane < pc.t1) ? __ldg(table + win + 32 + lane) : 0;
+        for (int blk0 = pc.t0; blk0 < pc.t1; blk0 += 4) {
+            if (blk0 - win == 32) {  // next window; fetch the one after it
+                win = blk0;
+                ids = nxt;
+                nxt = (win + 32 + lane < pc.t1) ? __ldg(table + win + 32 + lane) : 0;
+            }
+            const int tiles = min(4, pc.t1 - blk0);
+            const int w0 = blk0 - win;
+            const int id = __shfl_sync(FULLM, ids, (w0 + (lane & 3)) & 31);
+            const bool bad =
+                __any_sync(FULLM, lane < tiles && (id < 0 || id >= p.num_blocks));
+            const int my_id = __shfl_sync(FULLM, ids, (w0 + (bj & 3)) & 31);
+            const int s = it % kStagesTc;
+            if (lane == 0) {
+                bool ok = true;
+                if (it >= kStagesTc)
+                    ok = mbar_wait(smem_addr(&sm.empty[s]), ((it / kStagesTc) - 1) & 1);
+                if (!ok) tc_abort(sm, p);
+                aborted = !ok || sm.abort_flag;
+                if (!aborted) {
+                    if (pw == 0) sm.bad[s] = bad ? 1 : 0;
+                    if (bad && pw == 0) report(p.status, GQA_ERR_BLOCK_ID);
+                    // each producer warp arrives once, expecting its own boxes' bytes
+                    const int mine =
+                        tiles > pw ? (tiles - pw + kProducerWarps - 1) / kProducerWarps : 0;
+                    if (bad || mine == 0)
+                        mbar_arrive(smem_addr(&sm.full[s]));
+                    else
+                        mbar_arrive_expect_tx(smem_addr(&sm.full[s]), (uint32_t)(mine * 4 * 2048));
+                }
+            }
+            aborted = __shfl_sync(FULLM, aborted, 0);
+            if (aborted) break;
+            // the stage's barrier expects this warp's bytes before its boxes are issued
+            if (!bad && boxer && bj < tiles) {
+                const uint32_t dst = smem_addr(stages + (size_t)s * kStageBytesTc) +
+                                     (2 * kvsel + bh) * kHalfBytes + bj * 2048;
+                tma_load_3d(dst, tm, smem_addr(&sm.full[s]), bh * 64, kv, my_id * 16, pol);
+            }
+            ++it;
+        }
+    }
+    if (lane == 0 && aborted) {  // let copies already issued land before the CTA exits
+        for (int j = max(0, it - kStagesTc); j < it; ++j)
+            stage_landed(sm, j);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// One elected thread issues every MMA.  Within a piece the QK^T of stage
+// n + 1 is issued as soon as the softmax threads have read S(n), so that it
+// runs while they work on stage n; PV(n) follows once P(n) is written.
+__device__ void tc_mma(const TcParams& p, bool bf16, uint8_t* stages, TcSmem& sm,
+                       uint32_t tmem) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+        const uint32_t id_s = umma_idesc(bf16, kRowsTc, 64, false);   // S = Q . K^T
+        const uint32_t id_o = umma_idesc(bf16, kRowsTc, 128, true);   // O += P . V
+        // S(n) = Q . K(n)^T once stage n has landed and S(n - 1) has been read
+        auto issue_qk = [&](int n) -> bool {
+            const int s = n % kStagesTc;
+            if (!stage_landed(sm, n)) return false;
+            if (n >= 1 && !mbar_wait(smem_addr(&sm.s_free), (n - 1) & 1)) return false;
+            tc_fence_after();
+            const uint32_t kb = smem_addr(stages + (size_t)s * kStageBytesTc);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {  // 16 head dims per MMA
+                const uint32_t off = (kk & 3) * 32u;  // 32 B along the 128-B row
+                const uint64_t bk = umma_desc_sw128(kb + (kk >> 2) * kHalfBytes + off, 16, 1024);
+                umma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bk, id_s, kk > 0);
+            }
+            umma_commit(smem_addr(&sm.s_ready));
+            return true;
+        };
+        TcWalker wk;
+        wk.init(sm, p);
+        TcPiece pc;
+        int n = 0, qs = 0;
+        bool ok = true;
+        while (ok && wk.next(p, pc)) {
+            const int nst = (pc.t1 - pc.t0 + 3) / 4;
+            ok = mbar_wait(smem_addr(&sm.q_ready), qs & 1);
+            ++qs;
+            ok = ok && !sm.abort_flag && issue_qk(n);
+            for (int st = 0; st < nst && ok; ++st, ++n) {
+                if (st + 1 < nst) ok = issue_qk(n + 1);
+                ok = ok && mbar_wait(smem_addr(&sm.p_ready), n & 1);
+                if (!ok || sm.abort_flag) break;
+                tc_fence_after();
+                const uint32_t vb = smem_addr(stages + (size_t)(n % kStagesTc) * kStageBytesTc) +
+                                    2 * kHalfBytes;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per MMA
+                    const uint64_t bv = umma_desc_sw128(vb + ks * 2048, kHalfBytes, 1024);
+                    umma_ts(tmem + kColO, tmem + kColP + ks * 8, bv, id_o, st > 0 || ks > 0);
+                }
+                umma_commit(smem_addr(&sm.o_ready));
+                umma_commit(smem_addr(&sm.empty[n % kStagesTc]));
+            }
+            if (!ok) tc_abort(sm, p);
+            if (sm.abort_flag) ok = false;
+        }
+        // every MMA issued so far has completed before tensor memory is freed
+        umma_commit(smem_addr(&sm.done));
+        if (!mbar_wait(smem_addr(&sm.done), 0)) tc_abort(sm, p);
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// Pairwise reductions: a dependency depth of log2(N) instead of N.
+template <int N>
+__device__ __forceinline__ float max_tree(const float (&v)[N]) {
+    float a[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) a[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+    if constexpr (N / 2 == 1) {
+        return a[0];
+    } else {
+        return max_tree<N / 2>(a);
+    }
+}
+template <int N>
+__device__ __forceinline__ float sum_tree(const float (&v)[N]) {
+    float a[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) a[i] = v[2 * i] + v[2 * i + 1];
+    if constexpr (N / 2 == 1) {
+        return a[0];
+    } else {
+        return sum_tree<N / 2>(a);
+    }
+}
+
+// 32 output elements of this thread's row: fp32 values times inv, rounded to
+// q's dtype.
+template <bool BF16>
+__device__ __forceinline__ void store_row32(uint4* dst, const uint32_t (&o)[32], float inv) {
+    using E = Elt<BF16>;
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        w[k] = E::pack(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+// Eight softmax warps: warps w and w + 4 share tensor-memory lane quarter
+// w % 4 (the same 32 rows); `half` 0 takes S columns 0..31 (tokens 0..31 of
+// the stage), O columns 0..63 and Q dims 0..63, half 1 the rest.  The two
+// threads of a row swap their stage maxima through shared memory (one pair
+// barrier per stage) so that both use the same reference.
+template <bool BF16>
+__device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t tmem) {
+    using E = Elt<BF16>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int quarter = warp & 3;  // a warp reaches tensor-memory lanes 32*(warp%4) .. +31
+    const int half = (warp - kSoftmaxWarp0) >> 2;
+    const int row = 32 * quarter + lane;
+    const int tsm = threadIdx.x - 32 * kSoftmaxWarp0;  // 0..255 among the softmax threads
+    const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
+    const uint32_t tS = trow + kColS + 32 * half, tP = trow + kColP + 16 * half;
+    const uint32_t tO = trow + kColO + 64 * half, tQ = trow + kColQ + 32 * half;
+    // sequences with an invalid length: zero outputs (CTA 0), status
+    if (blockIdx.x == 0) {
+        for (int b = tsm; b < p.B; b += kSoftmaxThreads) {
+            if (tc_nblk(p, b) != 0) continue;
+            report(p.status, GQA_ERR_CONTEXT);
+            uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                (size_t)b * p.T * p.N * 128);
+            for (int i = 0; i < p.T * p.N * 16; ++i) o[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    TcWalker wk;
+    wk.init(sm, p);
+    TcPiece pc;
+    int n = 0;
+    bool ok = true;
+    while (ok && wk.next(p, pc)) {
+        const int b = pc.b, kv = pc.v / p.C, chunk = pc.v % p.C;
+        const int r = chunk * p.Rc + row;
+        const bool active = row < p.Rc && r < p.R;
+        const int t = active ? r / p.G : 0, gg = active ? r % p.G : 0;
+        const int ctx = __ldg(p.context_lens + b);
+        const int nst = (pc.t1 - pc.t0 + 3) / 4;
+        // ---- this row's half of Q into tensor memory ----------------------------
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const uint16_t*>(p.q) +
+                (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128 + 64 * half);
+            uint32_t qw[32];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint4 x = active ? __ldg(src + cc) : make_uint4(0, 0, 0, 0);
+                qw[4 * cc] = x.x;
+                qw[4 * cc + 1] = x.y;
+                qw[4 * cc + 2] = x.z;
+                qw[4 * cc + 3] = x.w;
+            }
+            tmem_st32(tQ, qw);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&sm.q_ready));
+        }
+        const int fn = ctx - p.T;  // position of the first new token
+        const int lim = fn + t;    // last position this row sees
+        // tree rows: the new positions this row sees (its ancestors and itself)
+        const uint64_t tmk = (p.tree_mask && active)
+                                 ? (__ldg(p.tree_mask + (size_t)b * p.T + t) | (1ull << t))
+                                 : 0ull;
+        float m = -INFINITY, l = 0.f;  // l: this half's columns
+        bool bad = false;
+        for (int st = 0; st < nst && ok; ++st, ++n) {
+            const int s = n % kStagesTc;
+            // stage n has landed (its bad-block flag and V rows are read below)
+            ok = stage_landed(sm, n) && mbar_wait(smem_addr(&sm.s_ready), n & 1);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[32];
+            tmem_ld32(tS, sr);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&sm.s_free));
+            bad |= sm.bad[s] != 0;
+            const int blk0 = pc.t0 + 4 * st;
+            const int tok0 = blk0 * 16;
+            const int tiles = min(4, pc.t1 - blk0);
+            // visible columns of the stage as one word: loaded and causal ...
+            const int vis_end = min(tiles * 16, lim + 1 - tok0);
+            uint64_t vm = vis_end >= 64 ? ~0ull : vis_end <= 0 ? 0ull : (1ull << vis_end) - 1;
+            if (p.tree_mask) {  // ... and, among the new positions, on the row's tree path
+                const int d = fn - tok0;  // stage column of the first new token
+                if (d < 64) {
+                    const uint64_t nbits = d >= 0 ? tmk << d : (-d < 64 ? tmk >> -d : 0ull);
+                    const uint64_t nmask = d >= 0 ? ~0ull << d : ~0ull;
+                    vm &= ~nmask | nbits;
+                }
+            }
+            const uint32_t vh = half ? (uint32_t)(vm >> 32) : (uint32_t)vm;
+            float sv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sv[j] = (vh >> j) & 1u ? __uint_as_float(sr[j]) : -INFINITY;
+            const float xh = max_tree(sv);
+            float* xm = sm.xmax[n & 1];
+            xm[half * kRowsTc + row] = xh;
+            pair_sync(quarter);
+            const float x = fmaxf(xh, xm[(half ^ 1) * kRowsTc + row]) * p.scale_log2;
+            // running max; O is rescaled (lazily) in tensor memory, warp by warp
+            const bool need = x > m + kGapTc;
+            if (__any_sync(FULLM, need)) {
+                const float f = (need && m != -INFINITY) ? fast_exp2(m - x) : 1.f;
+                if (st > 0) {
+                    ok = mbar_wait(smem_addr(&sm.o_ready), (n - 1) & 1);  // PV(n-1) done
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + 32 * c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+                        tmem_st32(tO + 32 * c, o);
+                    }
+                    tmem_wait_st();
+                }
+                if (need) {
+                    l *= f;
+                    m = x;
+                }
+            }
+            const float nref = (m == -INFINITY) ? 0.f : -m;
+            uint32_t pw[16];
+            float ps[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                pw[k] = E::pack(fast_exp2(fmaf(sv[2 * k], p.scale_log2, nref)),
+                                fast_exp2(fmaf(sv[2 * k + 1], p.scale_log2, nref)));
+                ps[k] = E::lo(pw[k]) + E::hi(pw[k]);
+            }
+            l += sum_tree(ps);
+            if (n >= 1) {  // the previous stage's PV has read P
+                ok = mbar_wait(smem_addr(&sm.o_ready), (n - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st16(tP, pw);
+            tmem_wait_st();
+            // V rows without data in this stage: zero them (NaN-safe products)
+            const int valid_rows = max(0, min(tiles * 16, ctx - tok0));
+            if (valid_rows < 64) {
+                const uint32_t vb = smem_addr(stages + (size_t)s * kStageBytesTc) + 2 * kHalfBytes;
+                for (int i = tsm; i < (64 - valid_rows) * 16; i += kSoftmaxThreads) {
+                    const int rr = valid_rows + (i >> 4), c = i & 15, h = c >> 3, cc = c & 7;
+                    st_shared_v4(vb + h * kHalfBytes + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                                     ((cc ^ (rr & 7)) << 4),
+                                 make_uint4(0, 0, 0, 0));
+                }
+                fence_proxy_async_shared();
+            }
+            tc_fence_before();
+            mbar_arrive(smem_addr(&sm.p_ready));
+        }
+        // ---- the piece's rows ----------------------------------------------------
+        if (ok) {
+            ok = mbar_wait(smem_addr(&sm.o_ready), (n - 1) & 1);
+            tc_fence_after();
+        }
+        if (!ok) {
+            tc_abort(sm, p);
+            break;
+        }
+        // the row's sum over both halves
+        sm.xl[half * kRowsTc + row] = l;
+        pair_sync(quarter);
+        const float lt = l + sm.xl[(half ^ 1) * kRowsTc + row];
+        uint4* dst = reinterpret_cast<uint4*>(
+                         static_cast<uint16_t*>(p.out) +
+                         (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128) +
+                     8 * half;
+        const int first_cta = (int)(pc.first / sm.quota);
+        const int last_cta = (int)((pc.first + pc.nb - 1) / sm.quota);
+        if (first_cta == last_cta) {  // the whole segment: O / l in q's dtype
+            const bool zero = bad || !(lt > 0.f);  // an invalid block id: zeros
+            const float inv = zero ? 0.f : 1.f / lt;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * c, o);
+                tmem_wait_ld();
+                if (zero) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = 0u;
+                }
+                if (active) store_row32<BF16>(dst + 4 * c, o, inv);
+            }
+            tc_fence_before();
+            continue;
+        }
+        // ---- a piece of a split segment: publish; the last piece merges ----------
+        float* part = p.partials + (size_t)(2 * blockIdx.x + (pc.t0 == 0 ? 1 : 0)) * kPartFloats;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                __stcg(part + (64 * half + 32 * c + k) * kRowsTc + row, __uint_as_float(o[k]));
+        }
+        tc_fence_before();
+        if (half == 0) {
+            __stcg(part + 128 * kRowsTc + row, m);
+            __stcg(part + 129 * kRowsTc + row, bad ? -1.f : lt);  // -1: the piece saw a bad block
+        }
+        __threadfence();
+        softmax_sync();
+        if (tsm == 0) {
+            const int old = atomicAdd(p.flags + first_cta, 1);
+            sm.merge = old == last_cta - first_cta;
+        }
+        softmax_sync();
+        const bool merge = sm.merge != 0;
+        softmax_sync();  // every thread has read the decision before it is rewritten
+        if (!merge) continue;
+        __threadfence();
+        if (tsm == 0) p.flags[first_cta] = 0;  // back to zero for the next call
+        // the piece in first_cta starts the segment (slot 1), the others do not (slot 0)
+        auto piece_part = [&](int cta) -> const float* {
+            return p.partials + (size_t)(2 * cta + (cta == first_cta ? 1 : 0)) * kPartFloats;
+        };
+        float M = -INFINITY;
+        bool any_bad = false;
+        for (int cta = first_cta; cta <= last_cta; ++cta) {
+            const float* pp = piece_part(cta);
+            M = fmaxf(M, __ldcg(pp + 128 * kRowsTc + row));
+            any_bad |= __ldcg(pp + 129 * kRowsTc + row) < 0.f;
+        }
+        float L = 0.f;
+        for (int cta = first_cta; cta <= last_cta; ++cta) {
+            const float* pp = piece_part(cta);
+            const float mi = __ldcg(pp + 128 * kRowsTc + row);
+            L += (mi == -INFINITY ? 0.f : fast_exp2(mi - M)) * __ldcg(pp + 129 * kRowsTc + row);
+        }
+        const bool zero = any_bad || !(L > 0.f);
+        const float inv = zero ? 0.f : 1.f / L;
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+            float acc[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+            for (int cta = first_cta; cta <= last_cta; ++cta) {
+                const float* pp = piece_part(cta);
+                const float mi = __ldcg(pp + 128 * kRowsTc + row);
+                const float w = (zero || mi == -INFINITY) ? 0.f : fast_exp2(mi - M);
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    acc[k] += w * __ldcg(pp + (64 * half + 32 * c + k) * kRowsTc + row);
+            }
+            uint32_t o[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(acc[k]);
+            if (active) store_row32<BF16>(dst + 4 * c, o, inv);
+        }
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    tc_attention_kernel(const __grid_constant__ CUtensorMap tmk,
+                        const __grid_constant__ CUtensorMap tmv, const TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stages = base;
+    TcSmem& sm = *reinterpret_cast<TcSmem*>(stages + (size_t)kStagesTc * kStageBytesTc);
+    const int warp = threadIdx.x >> 5;
+    griddep_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStagesTc; ++s) {
+            mbar_init(smem_addr(&sm.full[s]), kProducerWarps);
+            mbar_init(smem_addr(&sm.empty[s]), 1);
+            sm.bad[s] = 0;
+        }
+        mbar_init(smem_addr(&sm.q_ready), kSoftmaxThreads);
+        mbar_init(smem_addr(&sm.s_ready), 1);
+        mbar_init(smem_addr(&sm.s_free), kSoftmaxThreads);
+        mbar_init(smem_addr(&sm.p_ready), kSoftmaxThreads);
+        mbar_init(smem_addr(&sm.o_ready), 1);
+        mbar_init(smem_addr(&sm.done), 1);
+        sm.abort_flag = 0;
+        sm.merge = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
+    griddep_wait();  // q, the caches, the lengths, the workspace and out follow earlier kernels
+    if (warp == 0) tc_plan(p, sm);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    if (warp == 0)
+        tc_mma(p, BF16, stages, sm, tmem);
+    else if (warp < kSoftmaxWarp0)
+        tc_producer(&tmk, &tmv, p, stages, sm, warp - 1);
+    else
+        tc_softmax<BF16>(p, stages, sm, tmem);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+constexpr size_t kSmemTc = 1024 + (size_t)kStagesTc * kStageBytesTc + sizeof(TcSmem);
+static_assert(kSmemTc <= 227 * 1024, "shared memory per CTA");
+
+}  // namespace
+
+bool tc_attention_supported(const gqa_shape& s) {
+    return s.H == 128 && s.kv_dtype == GQA_KV_SAME && s.window == 0 && s.block_size == 16 &&
+           (long long)s.T * (s.N / s.K) <= 8192;
+}
+
+bool tc_attention_preferred(const gqa_shape& s) {
+    return tc_attention_supported(s) && (long long)s.T * (s.N / s.K) >= kTcMinRows;
+}
+
+size_t tc_workspace_bytes(const gqa_shape& s, size_t flags_bytes) {
+    if (!tc_attention_supported(s)) return 0;
+    const int sms = device_sm_count();
+    if (sms < 1) return 0;
+    return flags_bytes + (size_t)2 * sms * kPartFloats * sizeof(float);
+}
+
+gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, const uint64_t* tree_mask, void* out,
+                               void* workspace, size_t flags_bytes, int32_t* dev_status,
+                               cudaStream_t stream) {
+    if (!tc_attention_supported(s)) return GQA_ERR_SHAPE;
+    if (s.B == 0) return GQA_OK;
+    // the shared-memory opt-in, once per device (no attribute calls later, so
+    // that launches can be captured into CUDA graphs)
+    {
+        static std::mutex mu;
+        static bool done[64] = {};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GQA_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!done[dev]) {
+            if (cudaFuncSetAttribute(tc_attention_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemTc) != cudaSuccess ||
+                cudaFuncSetAttribute(tc_attention_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemTc) != cudaSuccess)
+                return GQA_ERR_CUDA;
+            done[dev] = true;
+        }
+    }
+    CUtensorMap tmk, tmv;
+    if (!make_cache_map(&tmk, k_cache, s) || !make_cache_map(&tmv, v_cache, s)) return GQA_ERR_CUDA;
+    TcParams p;
+    p.q = q;
+    p.out = out;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.tree_mask = tree_mask;
+    p.status = dev_status;
+    p.flags = static_cast<int32_t*>(workspace);
+    p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + flags_bytes);
+    p.B = s.B;
+    p.T = s.T;
+    p.N = s.N;
+    p.K = s.K;
+    p.G = s.N / s.K;
+    p.R = s.T * p.G;
+    p.C = (p.R + kRowsTc - 1) / kRowsTc;
+    p.Rc = (p.R + p.C - 1) / p.C;
+    p.KC = s.K * p.C;
+    p.max_blocks = s.max_blocks_per_seq;
+    p.num_blocks = s.num_blocks;
+    const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
+    p.scale_log2 = (float)(scale * 1.4426950408889634);
+    const int sms = device_sm_count();
+    if (sms < 1) return GQA_ERR_CUDA;
+    // at most one CTA per SM, and no more than the tiles allow at the minimum
+    // quota (upper bound: every sequence at full capacity)
+    const long long tiles_max = (long long)s.B * p.KC * s.max_blocks_per_seq;
+    const long long grid = std::min<long long>(
+        sms, std::max<long long>(1, (tiles_max + kQuotaMinTc - 1) / kQuotaMinTc));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreadsTc);
+    cfg.dynamicSmemBytes = kSmemTc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (s.flags & (GQA_FLAG_PDL | GQA_FLAG_EARLY_KV)) ? 1 : 0;
+    const cudaError_t e =
+        s.dtype == GQA_BF16 ? cudaLaunchKernelEx(&cfg, tc_attention_kernel<true>, tmk, tmv, p)
+                            : cudaLaunchKernelEx(&cfg, tc_attention_kernel<false>, tmk, tmv, p);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
+}
+
+}  // namespace gqa

@@ -1,6 +1,7 @@
 // launch.h -- host-side launchers shared between the kernel files and api.cu.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -60,6 +61,23 @@ gqa_status launch_kv_append_quant(const gqa_shape& s, const void* k_new, const v
                                   void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                                   const int32_t* block_tables, const int32_t* context_lens,
                                   int32_t* dev_status, cudaStream_t stream);
+
+// TMA view (h, kv head, block*16 + row) of a cache, 128-byte boxes of 16 rows.
+bool make_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s);
+
+// Tensor-memory attention (tcgen05): decode / verify / tree verify with H = 128
+// over a cache in q's dtype, no window, no fused append (the caller appends
+// first).  `preferred`: the shapes where it is the faster of the two kernels.
+// The workspace holds the publication flags (flags_bytes, as the warp-level
+// kernel's plan lays them out) and then the partial results of split segments.
+bool tc_attention_supported(const gqa_shape& s);
+bool tc_attention_preferred(const gqa_shape& s);
+size_t tc_workspace_bytes(const gqa_shape& s, size_t flags_bytes);
+gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, const uint64_t* tree_mask, void* out,
+                               void* workspace, size_t flags_bytes, int32_t* dev_status,
+                               cudaStream_t stream);
 
 // Cached per-device SM count (0 on failure).
 int device_sm_count();

@@ -128,6 +128,16 @@ typedef struct {
  * finished; q, the T newest positions, the workspace and `out` are still
  * touched only after it has. */
 #define GQA_FLAG_EARLY_KV 2u
+/* Attention only: which kernel computes the call.  By default the library
+ * picks by shape: the tensor-memory kernel (tcgen05.mma, accumulators in
+ * tensor memory, 128 query rows of one KV head per tile) where a KV head has
+ * many query rows (T * N / K >= 64), the warp-level mma.sync kernel otherwise.
+ * GQA_FLAG_WARP_MMA forces the warp-level kernel; GQA_FLAG_TENSOR_MEMORY
+ * forces the tensor-memory one, which serves H = 128 with a cache in q's dtype
+ * and no window (GQA_ERR_SHAPE otherwise, or with both flags).  Both compute
+ * the same function; results differ only by rounding order. */
+#define GQA_FLAG_WARP_MMA 4u
+#define GQA_FLAG_TENSOR_MEMORY 8u
 
 /* Library version (major*10000 + minor*100 + patch). */
 int gqa_version(void);
@@ -151,8 +161,9 @@ gqa_status gqa_kv_append(const gqa_shape *shape, const void *k_new, const void *
 
 /* Bytes of device workspace gqa_decode_attention / gqa_verify_attention need
  * for this shape on the CURRENT device: a fixed 256 KiB region of int32
- * publication flags (one per thread block and group of 8 query rows) followed
- * by the split-context partial results.  Returns 0 if the shape is invalid.
+ * publication flags (one per thread block, or per thread block and group of 8
+ * query rows) followed by the split-context partial results of whichever
+ * kernel may serve the shape (see GQA_FLAG_TENSOR_MEMORY).  Returns 0 if the shape is invalid.
  * The workspace must be zero-filled before its first use (for example with
  * gqa_workspace_clear); every call whose kernels finish without
  * GQA_ERR_TIMEOUT leaves the flag region zero-filled again (the
@@ -264,7 +275,7 @@ gqa_status gqa_append_verify_attention(const gqa_shape *shape, const void *q,
  *              in topological order, its ancestors.  Bits j >= t are ignored;
  *              the chain mask (bits 0..t-1 set) gives gqa_verify_attention.
  * Requirements, layouts, workspace and device errors as gqa_verify_attention;
- * shape->window must be 0.  The _append_ form fuses gqa_kv_append as
+ * shape->window must be 0 and T <= 64.  The _append_ form fuses gqa_kv_append as
  * gqa_append_verify_attention does. */
 gqa_status gqa_tree_verify_attention(const gqa_shape *shape, const void *q,
                                      const void *k_cache, const void *v_cache,
