@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--kv", default="same", choices=["same", "int8", "e4m3"],
                     help="KV cache element type: q's dtype, or one-byte int8 / e4m3 codes with "
                          "a per-row fp32 scale (quantized append + attention, H = 128)")
+    ap.add_argument("--engine", default="auto", choices=["auto", "warp", "tmem"],
+                    help="attention kernel: picked by shape (auto), the warp-level mma.sync "
+                         "kernel, or the tensor-memory (tcgen05) kernel")
     ap.add_argument("--unfused", action="store_true",
                     help="separate kv_append launches instead of the append fused into "
                          "the attention launch")
@@ -106,17 +109,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
 
 
-def kernel_source_hash():
+def kernel_source_hash(engine="warp"):
     h = hashlib.sha256()
-    for f in ("attention.cu", "ptx.cuh"):
+    files = ("attention.cu", "ptx.cuh") if engine == "warp" else (
+        "attention_tc.cu", "tcgen05.cuh", "ptx.cuh")
+    for f in files:
         h.update(open(os.path.join(ROOT, "gqa_decode_attention_02_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(workload, engine="warp"):
     """dram bytes per attention launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", f"attention_{workload}_traffic.txt")
+    name = f"attention_{workload}" if engine == "warp" else f"tc_attention_{workload}"
+    p = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
     if not os.path.exists(p):
         return None
     kv = {}
@@ -124,7 +130,7 @@ def profiled_traffic(workload):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash(engine):
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -367,11 +373,12 @@ def run_ours(args, world, rank, local):
             elif fused:
                 fused_fn(w.q[l], w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
                          w.block_tables, w.context_lens, out=outs[l], workspace=ws, status=st,
-                         pdl=True, early_kv=True, window=w.window(l), **extra)
+                         pdl=True, early_kv=True, window=w.window(l), engine=args.engine,
+                         **extra)
             else:
                 attn_fn(w.q[l], w.k_cache[l], w.v_cache[l], w.block_tables, w.context_lens,
                         out=outs[l], workspace=ws, status=st, pdl=True, early_kv=True,
-                        window=w.window(l), **extra)
+                        window=w.window(l), engine=args.engine, **extra)
 
     def do_acc():
         if sampled:
@@ -485,7 +492,15 @@ def run_ours(args, world, rank, local):
     attn_launch_ms = attn_ms / L
     kernel_b = attn_b + (app_b if fused else 0)  # the fused launch also does the append
     achieved = kernel_b / (attn_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(args.workload if not q8 else f"{args.workload}_{args.kv}")
+    # which kernel served the attention calls: the library's rule for "auto"
+    # (tensor memory when a KV head has >= 64 query rows, H = 128, a cache in
+    # q's dtype and no window)
+    if args.engine != "auto":
+        engine = args.engine
+    else:
+        engine = "tmem" if (not q8 and w.H == 128 and w.T * (w.N // w.K) >= 64
+                            and not any(w.window(l) for l in range(L))) else "warp"
+    traffic = profiled_traffic(args.workload if not q8 else f"{args.workload}_{args.kv}", engine)
 
     # e2e: host buffers -> device, the captured API calls, results -> host
     e2e = None
@@ -582,6 +597,7 @@ def run_ours(args, world, rank, local):
             "append": ("fused into the attention launch" if fused else
                        "separate kv_append launches" if w.appended else "none"),
             "parallelism": f"replicas x{world}",
+            "engine": engine,
             "windows": list(w.windows) if w.windows else None,
             "kv_cache": ("dtype of q" if not q8 else
                          f"{args.kv} codes + fp32 scale per cached row (quantized append, "
@@ -593,7 +609,9 @@ def run_ours(args, world, rank, local):
         "breakdown_ms": {"append": round(app_ms, 5), "attention": round(attn_ms, 5),
                          "accept": round(acc_ms, 5)},
         "roofline": {"bound": "hbm",
-                     "kernel": "attention_kernel" + (" (kv_append fused)" if fused else "") + (
+                     "kernel": ("attention_kernel" if engine == "warp" else
+                                "tc_attention_kernel (tcgen05)") + (
+                                    " (kv_append fused)" if fused else "") + (
                          f" (one-byte {args.kv} cache)" if q8 else ""),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,

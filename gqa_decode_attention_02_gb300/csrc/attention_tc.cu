@@ -20,20 +20,24 @@
 // weights -- the context split of FlashDecoding named in §"PagedAttention".
 //
 // One CTA: warp 0 MMA issuer and tensor-memory owner, warps 1..2 producers
-// (TMA), warps 3..10 softmax (two threads per query row, each on 32 of a
-// stage's 64 columns; tensor-memory lane = row).
+// (TMA), warps 3..10 softmax in two groups of four warps (one thread per query
+// row each; tensor-memory lane = row).  Group g takes the stages st = g, g + 2,
+// ... of every piece with its own S, P and O in tensor memory, so the two
+// groups' online softmaxes run side by side and meet once per piece (a
+// log-sum-exp merge of two partial results, like the context split).
 // A stage is up to 64 tokens (four 16-token cache blocks of one piece):
-//   S[128 x 64]   = Q[128 x 128] . K^T   8 MMAs, Q from tensor memory, K K-major
+//   S_g[128 x 64]   = Q[128 x 128] . K^T   8 MMAs, Q from tensor memory, K K-major
 //   rows: mask (causal, tree, past the context) as one 64-bit word, running
-//         max with a lazy rescale of O, P = exp2(S*scale - max) in q's dtype
-//   O[128 x 128] += P[128 x 64] . V       4 MMAs, P from tensor memory, V MN-major
-// Tensor memory (512 columns, lane = query row) holds O, S, P and the piece's
-// Q.  The MMA issuer starts QK^T of stage n + 1 as soon as S(n) has been
-// read, so it overlaps the softmax of stage n.  Shared memory is a ring of
-// six stages (K and V, each two 64-dim halves of 64 token rows x 128 B,
-// 128-byte swizzled): 192 KB in flight per SM.  V rows of a stage that hold
-// no data (past the context, or unused tiles) are zeroed before the PV
-// product: their probabilities are 0, but stale bytes could be NaN.
+//         max with a lazy rescale of O_g, P = exp2(S*scale - max) in q's dtype
+//   O_g[128 x 128] += P_g[128 x 64] . V    4 MMAs, P from tensor memory, V MN-major
+// Tensor memory (512 columns, lane = query row) holds O_0, O_1, S_0, S_1,
+// P_0, P_1 and the piece's Q.  The MMA issuer starts PV(n) as soon as P(n) is
+// written and QK^T(n + 2) right after it (S_g is free once P_g is written), so
+// the tensor pipe and both groups stay busy.  Shared memory is a ring of six
+// stages (K and V, each two 64-dim halves of 64 token rows x 128 B, 128-byte
+// swizzled): 192 KB in flight per SM.  V rows of a stage that hold no data
+// (past the context, or unused tiles) are zeroed before the PV product: their
+// probabilities are 0, but stale bytes could be NaN.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -52,14 +56,17 @@ constexpr int kRowsTc = 128;                     // query rows per segment (MMA 
 constexpr int kStagesTc = 6;
 constexpr int kProducerWarps = 2;                // TMA issuers (each takes blocks of a stage)
 constexpr int kSoftmaxWarp0 = 1 + kProducerWarps; // warp 0 issues the MMAs
-constexpr int kSoftmaxThreads = 256;             // eight softmax warps
+constexpr int kSoftmaxThreads = 256;             // eight softmax warps, two groups
+constexpr int kGroupThreads = 128;               // one softmax group: a thread per row
 constexpr int kThreadsTc = 32 * kSoftmaxWarp0 + kSoftmaxThreads;
 constexpr int kHalfBytes = 64 * 128;             // 64 rows of one 64-dim half: 8 KB
 constexpr int kStageBytesTc = 4 * kHalfBytes;    // K then V, two halves each: 32 KB
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns (32 bits each; lane = query row): O fp32, S fp32,
-// P two 16-bit values per column, Q two 16-bit values per column
-constexpr uint32_t kColO = 0, kColS = 128, kColP = 192, kColQ = 256;
+// tensor-memory columns (32 bits each; lane = query row), per softmax group g:
+// O_g fp32 [128], S_g fp32 [64], P_g two 16-bit values per column [32]; Q two
+// 16-bit values per column [64], shared
+constexpr uint32_t kColO = 0, kColS = 256, kColP = 384, kColQ = 448;
+constexpr uint32_t kColOStep = 128, kColSStep = 64, kColPStep = 32;
 constexpr float kGapTc = 8.0f;                   // log2-domain slack before rescaling O
 constexpr int kQuotaMinTc = 16;                  // tiles per CTA at least: fewer split pieces
 constexpr int kPartFloats = 130 * kRowsTc;       // a partial: O^T [128][128], max, sum
@@ -85,19 +92,21 @@ struct TcSmem {
     uint64_t full[kStagesTc];   // stage data landed (TMA transaction bytes)
     uint64_t empty[kStagesTc];  // the PV product of the stage completed
     uint64_t q_ready;           // softmax threads wrote the piece's Q rows (tensor memory)
-    uint64_t s_ready;           // QK^T of a stage completed
-    uint64_t s_free;            // softmax threads read S
-    uint64_t p_ready;           // softmax threads wrote P (and zeroed stale V rows)
-    uint64_t o_ready;           // PV of a stage completed
+    uint64_t s_ready[2];        // QK^T of a stage of group g completed
+    uint64_t p_ready[2];        // group g wrote P_g (and zeroed stale V rows)
+    uint64_t o_ready[2];        // PV of a stage of group g completed
     uint64_t done;              // every MMA completed (before freeing tensor memory)
+    uint64_t pair[4];           // the two threads of each row of a lane quarter (64)
+    uint64_t all;               // every softmax thread (256)
     long long c0, c1, base;     // the CTA's tile range; first tile of segment (b0, 0)
     int b0, quota;
     int merge;                  // this CTA merges the split segment just finished
     uint32_t tmem_base;
     int bad[kStagesTc];         // the stage's blocks include an invalid id
     volatile int abort_flag;
-    float xmax[2][2 * kRowsTc]; // per stage parity: the two halves' maxima of each row
-    float xl[2 * kRowsTc];      // the two halves' sums of each row
+    float xm[2][kRowsTc];       // per group: running max of each row at the piece's end
+    float xl[2][kRowsTc];       // per group: sum of each row
+    int xb[2][kRowsTc];         // per group: a stage held an invalid block id
 };
 
 __device__ __forceinline__ int tc_nblk(const TcParams& p, int b) {
@@ -115,13 +124,15 @@ __device__ __forceinline__ bool stage_landed(TcSmem& sm, int n) {
     return mbar_wait(smem_addr(&sm.full[n % kStagesTc]), (n / kStagesTc) & 1);
 }
 
-// All softmax threads (named barrier 1); the two warps of one lane quarter
-// (barriers 2..5).
-__device__ __forceinline__ void softmax_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
-}
-__device__ __forceinline__ void pair_sync(int quarter) {
-    asm volatile("bar.sync %0, 64;" ::"r"(2 + quarter) : "memory");
+// All softmax threads meet on an mbarrier (arrive, then a bounded wait for
+// the phase): a thread that gave up on an earlier wait cannot leave the
+// others waiting without limit, as a named barrier would.  `ph` counts this
+// thread's uses.
+__device__ __forceinline__ bool softmax_bar(TcSmem& sm, int& ph) {
+    mbar_arrive(smem_addr(&sm.all));
+    const bool ok = mbar_wait(smem_addr(&sm.all), ph & 1);
+    ++ph;
+    return ok;
 }
 
 // One piece: tiles [t0, t1) of segment (b, v), whose first tile is number
@@ -291,55 +302,67 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
 }
 
 // ---------------------------------------------------------------------------
-// One elected thread issues every MMA.  Within a piece the QK^T of stage
-// n + 1 is issued as soon as the softmax threads have read S(n), so that it
-// runs while they work on stage n; PV(n) follows once P(n) is written.
-__device__ void tc_mma(const TcParams& p, bool bf16, uint8_t* stages, TcSmem& sm,
-                       uint32_t tmem) {
+// One elected thread issues every MMA.  Stage st of a piece belongs to
+// softmax group g = st % 2.  QK^T of the first two stages is issued when the
+// piece's Q is in tensor memory; then, per stage, PV(st) as soon as group g
+// has written P_g(st), and right after it QK^T(st + 2) into S_g, which group
+// g has finished reading (it wrote P_g from it).  Operand descriptors are
+// built once; per stage and per instruction only constants are added (the
+// 14-bit address field cannot carry: shared memory ends below 256 KB), which
+// keeps the issue rate at the tensor pipe's.
+template <bool BF16>
+__device__ void tc_mma(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t tmem) {
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
-        const uint32_t id_s = umma_idesc(bf16, kRowsTc, 64, false);   // S = Q . K^T
-        const uint32_t id_o = umma_idesc(bf16, kRowsTc, 128, true);   // O += P . V
-        // S(n) = Q . K(n)^T once stage n has landed and S(n - 1) has been read
-        auto issue_qk = [&](int n) -> bool {
-            const int s = n % kStagesTc;
+        constexpr uint32_t id_s = umma_idesc_ct(BF16, kRowsTc, 64, false);  // S = Q . K^T
+        constexpr uint32_t id_o = umma_idesc_ct(BF16, kRowsTc, 128, true);  // O += P . V
+        const uint32_t st0 = smem_addr(stages);
+        const uint64_t dk0 = umma_desc_sw128(st0, 16, 1024);                        // K, K-major
+        const uint64_t dv0 = umma_desc_sw128(st0 + 2 * kHalfBytes, kHalfBytes, 1024); // V, MN-major
+        const uint32_t tQ = tmem + kColQ;
+        // S_g = Q . K(n)^T once stage n has landed
+        auto issue_qk = [&](int n, int g) -> bool {
             if (!stage_landed(sm, n)) return false;
-            if (n >= 1 && !mbar_wait(smem_addr(&sm.s_free), (n - 1) & 1)) return false;
             tc_fence_after();
-            const uint32_t kb = smem_addr(stages + (size_t)s * kStageBytesTc);
+            const uint32_t tS = tmem + kColS + g * kColSStep;
+            const uint64_t dk = dk0 + (uint64_t)((n % kStagesTc) * (kStageBytesTc >> 4));
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {  // 16 head dims per MMA
-                const uint32_t off = (kk & 3) * 32u;  // 32 B along the 128-B row
-                const uint64_t bk = umma_desc_sw128(kb + (kk >> 2) * kHalfBytes + off, 16, 1024);
-                umma_ts(tmem + kColS, tmem + kColQ + 8 * kk, bk, id_s, kk > 0);
-            }
-            umma_commit(smem_addr(&sm.s_ready));
+            for (int kk = 0; kk < 8; ++kk)  // 16 head dims per MMA, 32 B along the 128-B row
+                umma_ts(tS, tQ + 8 * kk, dk + (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4),
+                        id_s, kk > 0);
+            umma_commit(smem_addr(&sm.s_ready[g]));
             return true;
         };
         TcWalker wk;
         wk.init(sm, p);
         TcPiece pc;
         int n = 0, qs = 0;
+        int kp0 = 0, kp1 = 0;  // P_0 / P_1 writes consumed so far (barrier phases)
         bool ok = true;
         while (ok && wk.next(p, pc)) {
             const int nst = (pc.t1 - pc.t0 + 3) / 4;
             ok = mbar_wait(smem_addr(&sm.q_ready), qs & 1);
             ++qs;
-            ok = ok && !sm.abort_flag && issue_qk(n);
+            ok = ok && !sm.abort_flag && issue_qk(n, 0);
+            if (ok && nst > 1) ok = issue_qk(n + 1, 1);
             for (int st = 0; st < nst && ok; ++st, ++n) {
-                if (st + 1 < nst) ok = issue_qk(n + 1);
-                ok = ok && mbar_wait(smem_addr(&sm.p_ready), n & 1);
+                const int g = st & 1;
+                ok = mbar_wait(smem_addr(&sm.p_ready[g]), (g ? kp1 : kp0) & 1);
+                if (g)
+                    ++kp1;
+                else
+                    ++kp0;
                 if (!ok || sm.abort_flag) break;
                 tc_fence_after();
-                const uint32_t vb = smem_addr(stages + (size_t)(n % kStagesTc) * kStageBytesTc) +
-                                    2 * kHalfBytes;
+                const uint32_t tO = tmem + kColO + g * kColOStep, tP = tmem + kColP + g * kColPStep;
+                const uint64_t dv = dv0 + (uint64_t)((n % kStagesTc) * (kStageBytesTc >> 4));
+                umma_ts(tO, tP, dv, id_o, st >= 2);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per MMA
-                    const uint64_t bv = umma_desc_sw128(vb + ks * 2048, kHalfBytes, 1024);
-                    umma_ts(tmem + kColO, tmem + kColP + ks * 8, bv, id_o, st > 0 || ks > 0);
-                }
-                umma_commit(smem_addr(&sm.o_ready));
+                for (int ks = 1; ks < 4; ++ks)  // 16 tokens per MMA
+                    umma_ts(tO, tP + ks * 8, dv + (uint64_t)((ks * 2048) >> 4), id_o, true);
+                umma_commit(smem_addr(&sm.o_ready[g]));
                 umma_commit(smem_addr(&sm.empty[n % kStagesTc]));
+                if (st + 2 < nst) ok = issue_qk(n + 2, g);
             }
             if (!ok) tc_abort(sm, p);
             if (sm.abort_flag) ok = false;
@@ -390,22 +413,27 @@ __device__ __forceinline__ void store_row32(uint4* dst, const uint32_t (&o)[32],
         dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-// Eight softmax warps: warps w and w + 4 share tensor-memory lane quarter
-// w % 4 (the same 32 rows); `half` 0 takes S columns 0..31 (tokens 0..31 of
-// the stage), O columns 0..63 and Q dims 0..63, half 1 the rest.  The two
-// threads of a row swap their stage maxima through shared memory (one pair
-// barrier per stage) so that both use the same reference.
+// Softmax group g = (warp - 3) / 4: its warps reach tensor-memory lane
+// quarters 3, 0, 1, 2 (a warp reaches lanes 32 * (warp % 4) .. + 31), one
+// thread per query row.  The group runs the online softmax of the stages
+// st = g, g + 2, ... of each piece into its own O_g.  At the piece's end the
+// two threads of a row (one per group) exchange running max, sum and
+// invalid-block flag through shared memory and each combines both groups'
+// O over its half of the head dimension (g = 0: dims 0..63, g = 1: 64..127),
+// with log-sum-exp weights, into the row's output or a split-segment partial.
 template <bool BF16>
 __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t tmem) {
     using E = Elt<BF16>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int quarter = warp & 3;  // a warp reaches tensor-memory lanes 32*(warp%4) .. +31
-    const int half = (warp - kSoftmaxWarp0) >> 2;
+    const int quarter = warp & 3;
+    const int g = (warp - kSoftmaxWarp0) >> 2;  // softmax group; also the half of the dims
     const int row = 32 * quarter + lane;
     const int tsm = threadIdx.x - 32 * kSoftmaxWarp0;  // 0..255 among the softmax threads
+    const int tg = tsm & (kGroupThreads - 1);         // 0..127 within the group
     const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
-    const uint32_t tS = trow + kColS + 32 * half, tP = trow + kColP + 16 * half;
-    const uint32_t tO = trow + kColO + 64 * half, tQ = trow + kColQ + 32 * half;
+    const uint32_t tS = trow + kColS + g * kColSStep, tP = trow + kColP + g * kColPStep;
+    const uint32_t tOg = trow + kColO + g * kColOStep;  // this group's accumulator
+    const uint32_t tQ = trow + kColQ + 32 * g;
     // sequences with an invalid length: zero outputs (CTA 0), status
     if (blockIdx.x == 0) {
         for (int b = tsm; b < p.B; b += kSoftmaxThreads) {
@@ -419,7 +447,9 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
     TcWalker wk;
     wk.init(sm, p);
     TcPiece pc;
-    int n = 0;
+    int n0 = 0;  // stages of earlier pieces
+    int kg = 0;  // stages of this group so far (barrier phases of s_ready[g], o_ready[g])
+    int pp = 0, ap = 0;  // phases of this thread's pair barrier and of the softmax barrier
     bool ok = true;
     while (ok && wk.next(p, pc)) {
         const int b = pc.b, kv = pc.v / p.C, chunk = pc.v % p.C;
@@ -432,7 +462,7 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
         {
             const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const uint16_t*>(p.q) +
-                (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128 + 64 * half);
+                (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128 + 64 * g);
             uint32_t qw[32];
 #pragma unroll
             for (int cc = 0; cc < 8; ++cc) {
@@ -453,19 +483,20 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
         const uint64_t tmk = (p.tree_mask && active)
                                  ? (__ldg(p.tree_mask + (size_t)b * p.T + t) | (1ull << t))
                                  : 0ull;
-        float m = -INFINITY, l = 0.f;  // l: this half's columns
+        float m = -INFINITY, l = 0.f;
         bool bad = false;
-        for (int st = 0; st < nst && ok; ++st, ++n) {
-            const int s = n % kStagesTc;
+        int mine = 0;  // this group's stages in this piece
+        for (int st = g; st < nst && ok; st += 2, ++kg, ++mine) {
+            const int n = n0 + st, s = n % kStagesTc;
             // stage n has landed (its bad-block flag and V rows are read below)
-            ok = stage_landed(sm, n) && mbar_wait(smem_addr(&sm.s_ready), n & 1);
+            ok = stage_landed(sm, n) && mbar_wait(smem_addr(&sm.s_ready[g]), kg & 1);
+            ok = __all_sync(FULLM, ok);  // warp-collective tensor-memory accesses follow
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[32];
-            tmem_ld32(tS, sr);
+            uint32_t sa[32], sb[32];
+            tmem_ld32(tS, sa);
+            tmem_ld32(tS + 32, sb);
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&sm.s_free));
             bad |= sm.bad[s] != 0;
             const int blk0 = pc.t0 + 4 * st;
             const int tok0 = blk0 * 16;
@@ -481,32 +512,28 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
                     vm &= ~nmask | nbits;
                 }
             }
-            const uint32_t vh = half ? (uint32_t)(vm >> 32) : (uint32_t)vm;
-            float sv[32];
+            float sv[64];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sv[j] = (vh >> j) & 1u ? __uint_as_float(sr[j]) : -INFINITY;
-            const float xh = max_tree(sv);
-            float* xm = sm.xmax[n & 1];
-            xm[half * kRowsTc + row] = xh;
-            pair_sync(quarter);
-            const float x = fmaxf(xh, xm[(half ^ 1) * kRowsTc + row]) * p.scale_log2;
-            // running max; O is rescaled (lazily) in tensor memory, warp by warp
+            for (int j = 0; j < 64; ++j)
+                sv[j] = (vm >> j) & 1ull ? __uint_as_float(j < 32 ? sa[j] : sb[j - 32]) : -INFINITY;
+            const float x = max_tree(sv) * p.scale_log2;
+            // running max; O_g is rescaled (lazily) in tensor memory, warp by warp
             const bool need = x > m + kGapTc;
             if (__any_sync(FULLM, need)) {
                 const float f = (need && m != -INFINITY) ? fast_exp2(m - x) : 1.f;
-                if (st > 0) {
-                    ok = mbar_wait(smem_addr(&sm.o_ready), (n - 1) & 1);  // PV(n-1) done
+                if (mine > 0) {  // PV of this group's previous stage has completed
+                    ok = __all_sync(FULLM, mbar_wait(smem_addr(&sm.o_ready[g]), (kg - 1) & 1));
                     if (!ok) break;
                     tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
                         uint32_t o[32];
-                        tmem_ld32(tO + 32 * c, o);
+                        tmem_ld32(tOg + 32 * c, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
                             o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-                        tmem_st32(tO + 32 * c, o);
+                        tmem_st32(tOg + 32 * c, o);
                     }
                     tmem_wait_st();
                 }
@@ -516,27 +543,27 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
                 }
             }
             const float nref = (m == -INFINITY) ? 0.f : -m;
-            uint32_t pw[16];
-            float ps[16];
+            uint32_t pw[32];
+            float ps[32];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
+            for (int k = 0; k < 32; ++k) {
                 pw[k] = E::pack(fast_exp2(fmaf(sv[2 * k], p.scale_log2, nref)),
-                                fast_exp2(fmaf(sv[2 * k + 1], p.scale_log2, nref)));
+                                     fast_exp2(fmaf(sv[2 * k + 1], p.scale_log2, nref)));
                 ps[k] = E::lo(pw[k]) + E::hi(pw[k]);
             }
             l += sum_tree(ps);
-            if (n >= 1) {  // the previous stage's PV has read P
-                ok = mbar_wait(smem_addr(&sm.o_ready), (n - 1) & 1);
+            if (mine > 0) {  // the previous PV of this group has read P_g
+                ok = __all_sync(FULLM, mbar_wait(smem_addr(&sm.o_ready[g]), (kg - 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
             }
-            tmem_st16(tP, pw);
+            tmem_st32(tP, pw);
             tmem_wait_st();
             // V rows without data in this stage: zero them (NaN-safe products)
             const int valid_rows = max(0, min(tiles * 16, ctx - tok0));
             if (valid_rows < 64) {
                 const uint32_t vb = smem_addr(stages + (size_t)s * kStageBytesTc) + 2 * kHalfBytes;
-                for (int i = tsm; i < (64 - valid_rows) * 16; i += kSoftmaxThreads) {
+                for (int i = tg; i < (64 - valid_rows) * 16; i += kGroupThreads) {
                     const int rr = valid_rows + (i >> 4), c = i & 15, h = c >> 3, cc = c & 7;
                     st_shared_v4(vb + h * kHalfBytes + (rr >> 3) * 1024 + (rr & 7) * 128 +
                                      ((cc ^ (rr & 7)) << 4),
@@ -545,35 +572,58 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
                 fence_proxy_async_shared();
             }
             tc_fence_before();
-            mbar_arrive(smem_addr(&sm.p_ready));
+            mbar_arrive(smem_addr(&sm.p_ready[g]));
         }
-        // ---- the piece's rows ----------------------------------------------------
-        if (ok) {
-            ok = mbar_wait(smem_addr(&sm.o_ready), (n - 1) & 1);
+        n0 += nst;
+        // ---- the piece's rows: the two groups' results meet ------------------------
+        if (ok && mine > 0) {  // this group's last PV has completed
+            ok = mbar_wait(smem_addr(&sm.o_ready[g]), (kg - 1) & 1);
             tc_fence_after();
         }
+        ok = __all_sync(FULLM, ok);
+        sm.xm[g][row] = m;
+        sm.xl[g][row] = l;
+        sm.xb[g][row] = bad ? 1 : 0;
+        tc_fence_before();
+        mbar_arrive(smem_addr(&sm.pair[quarter]));
+        ok = __all_sync(FULLM, ok && mbar_wait(smem_addr(&sm.pair[quarter]), pp & 1));
+        ++pp;
         if (!ok) {
             tc_abort(sm, p);
             break;
         }
-        // the row's sum over both halves
-        sm.xl[half * kRowsTc + row] = l;
-        pair_sync(quarter);
-        const float lt = l + sm.xl[(half ^ 1) * kRowsTc + row];
+        tc_fence_after();  // both groups' last PVs (and so every MMA of the piece) completed
+        const float m0 = sm.xm[0][row], m1 = sm.xm[1][row];
+        const float M = fmaxf(m0, m1);
+        const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
+        const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+        const float lt = w0 * sm.xl[0][row] + w1 * sm.xl[1][row];
+        bad = (sm.xb[0][row] | sm.xb[1][row]) != 0;
+        // columns 32c .. 32c+31 of this thread's half of the dims: w0 O_0 + w1 O_1
+        // (a group without stages in this piece has weight 0 and is not read)
+        auto combined = [&](int c, uint32_t (&o)[32]) {
+            uint32_t a0[32], a1[32];
+            tmem_ld32(trow + kColO + 64 * g + 32 * c, a0);
+            tmem_ld32(trow + kColO + kColOStep + 64 * g + 32 * c, a1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                o[k] = __float_as_uint((w0 != 0.f ? w0 * __uint_as_float(a0[k]) : 0.f) +
+                                       (w1 != 0.f ? w1 * __uint_as_float(a1[k]) : 0.f));
+        };
         uint4* dst = reinterpret_cast<uint4*>(
                          static_cast<uint16_t*>(p.out) +
                          (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128) +
-                     8 * half;
+                     8 * g;
         const int first_cta = (int)(pc.first / sm.quota);
         const int last_cta = (int)((pc.first + pc.nb - 1) / sm.quota);
         if (first_cta == last_cta) {  // the whole segment: O / l in q's dtype
             const bool zero = bad || !(lt > 0.f);  // an invalid block id: zeros
             const float inv = zero ? 0.f : 1.f / lt;
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tO + 32 * c, o);
-                tmem_wait_ld();
+                combined(c, o);
                 if (zero) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) o[k] = 0u;
@@ -585,29 +635,33 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
         }
         // ---- a piece of a split segment: publish; the last piece merges ----------
         float* part = p.partials + (size_t)(2 * blockIdx.x + (pc.t0 == 0 ? 1 : 0)) * kPartFloats;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_wait_ld();
+            combined(c, o);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-                __stcg(part + (64 * half + 32 * c + k) * kRowsTc + row, __uint_as_float(o[k]));
+                __stcg(part + (64 * g + 32 * c + k) * kRowsTc + row, __uint_as_float(o[k]));
         }
         tc_fence_before();
-        if (half == 0) {
-            __stcg(part + 128 * kRowsTc + row, m);
+        if (g == 0) {
+            __stcg(part + 128 * kRowsTc + row, M);
             __stcg(part + 129 * kRowsTc + row, bad ? -1.f : lt);  // -1: the piece saw a bad block
         }
         __threadfence();
-        softmax_sync();
-        if (tsm == 0) {
+        ok = softmax_bar(sm, ap);
+        if (ok && tsm == 0) {
             const int old = atomicAdd(p.flags + first_cta, 1);
             sm.merge = old == last_cta - first_cta;
         }
-        softmax_sync();
+        ok = ok && softmax_bar(sm, ap);
         const bool merge = sm.merge != 0;
-        softmax_sync();  // every thread has read the decision before it is rewritten
+        ok = ok && softmax_bar(sm, ap);  // every thread has read the decision before it is rewritten
+        ok = __all_sync(FULLM, ok);
+        if (!ok) {
+            tc_abort(sm, p);
+            break;
+        }
         if (!merge) continue;
         __threadfence();
         if (tsm == 0) p.flags[first_cta] = 0;  // back to zero for the next call
@@ -615,18 +669,18 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
         auto piece_part = [&](int cta) -> const float* {
             return p.partials + (size_t)(2 * cta + (cta == first_cta ? 1 : 0)) * kPartFloats;
         };
-        float M = -INFINITY;
+        float MM = -INFINITY;
         bool any_bad = false;
         for (int cta = first_cta; cta <= last_cta; ++cta) {
-            const float* pp = piece_part(cta);
-            M = fmaxf(M, __ldcg(pp + 128 * kRowsTc + row));
-            any_bad |= __ldcg(pp + 129 * kRowsTc + row) < 0.f;
+            const float* pp_ = piece_part(cta);
+            MM = fmaxf(MM, __ldcg(pp_ + 128 * kRowsTc + row));
+            any_bad |= __ldcg(pp_ + 129 * kRowsTc + row) < 0.f;
         }
         float L = 0.f;
         for (int cta = first_cta; cta <= last_cta; ++cta) {
-            const float* pp = piece_part(cta);
-            const float mi = __ldcg(pp + 128 * kRowsTc + row);
-            L += (mi == -INFINITY ? 0.f : fast_exp2(mi - M)) * __ldcg(pp + 129 * kRowsTc + row);
+            const float* pp_ = piece_part(cta);
+            const float mi = __ldcg(pp_ + 128 * kRowsTc + row);
+            L += (mi == -INFINITY ? 0.f : fast_exp2(mi - MM)) * __ldcg(pp_ + 129 * kRowsTc + row);
         }
         const bool zero = any_bad || !(L > 0.f);
         const float inv = zero ? 0.f : 1.f / L;
@@ -636,12 +690,12 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
 #pragma unroll
             for (int k = 0; k < 32; ++k) acc[k] = 0.f;
             for (int cta = first_cta; cta <= last_cta; ++cta) {
-                const float* pp = piece_part(cta);
-                const float mi = __ldcg(pp + 128 * kRowsTc + row);
-                const float w = (zero || mi == -INFINITY) ? 0.f : fast_exp2(mi - M);
+                const float* pp_ = piece_part(cta);
+                const float mi = __ldcg(pp_ + 128 * kRowsTc + row);
+                const float w = (zero || mi == -INFINITY) ? 0.f : fast_exp2(mi - MM);
 #pragma unroll
                 for (int k = 0; k < 32; ++k)
-                    acc[k] += w * __ldcg(pp + (64 * half + 32 * c + k) * kRowsTc + row);
+                    acc[k] += w * __ldcg(pp_ + (64 * g + 32 * c + k) * kRowsTc + row);
             }
             uint32_t o[32];
 #pragma unroll
@@ -669,10 +723,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             sm.bad[s] = 0;
         }
         mbar_init(smem_addr(&sm.q_ready), kSoftmaxThreads);
-        mbar_init(smem_addr(&sm.s_ready), 1);
-        mbar_init(smem_addr(&sm.s_free), kSoftmaxThreads);
-        mbar_init(smem_addr(&sm.p_ready), kSoftmaxThreads);
-        mbar_init(smem_addr(&sm.o_ready), 1);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(smem_addr(&sm.s_ready[g]), 1);
+            mbar_init(smem_addr(&sm.p_ready[g]), kGroupThreads);
+            mbar_init(smem_addr(&sm.o_ready[g]), 1);
+        }
+        for (int q = 0; q < 4; ++q) mbar_init(smem_addr(&sm.pair[q]), 2 * 32);
+        mbar_init(smem_addr(&sm.all), kSoftmaxThreads);
         mbar_init(smem_addr(&sm.done), 1);
         sm.abort_flag = 0;
         sm.merge = 0;
@@ -686,7 +743,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     if (warp == 0)
-        tc_mma(p, BF16, stages, sm, tmem);
+        tc_mma<BF16>(p, stages, sm, tmem);
     else if (warp < kSoftmaxWarp0)
         tc_producer(&tmk, &tmv, p, stages, sm, warp - 1);
     else
