@@ -1469,6 +1469,23 @@ bool make_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
     return encode_cache_map(m, base, s);
 }
 
+bool make_rows_map(CUtensorMap* m, const void* base, const gqa_shape& s, int hpc, int tpc) {
+    auto fn = encode_fn();
+    if (!fn || s.H != 128 || hpc < 1 || hpc > 256 || tpc < 1 || tpc > 256) return false;
+    const cuuint64_t G = (cuuint64_t)(s.N / s.K), H = 128, e = 2;
+    const cuuint64_t dims[5] = {H, G, (cuuint64_t)s.K, (cuuint64_t)s.T, (cuuint64_t)s.B};
+    const cuuint64_t strides[4] = {H * e, G * H * e, (cuuint64_t)s.N * H * e,
+                                   (cuuint64_t)s.T * s.N * H * e};
+    const cuuint32_t box[5] = {64, (cuuint32_t)hpc, 1, (cuuint32_t)tpc, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(m, s.dtype == GQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          5, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;

@@ -53,24 +53,28 @@ namespace gqa {
 namespace {
 
 constexpr int kRowsTc = 128;                     // query rows per segment (MMA M)
-constexpr int kStagesTc = 6;
-constexpr int kProducerWarps = 2;                // TMA issuers (each takes blocks of a stage)
-constexpr int kSoftmaxWarp0 = 1 + kProducerWarps; // warp 0 issues the MMAs
+constexpr int kStagesTc = 4;                     // (6 measured no faster: the pipeline, not memory, bounds it)
+constexpr int kProducerWarps = 1;                // TMA issuer of the K / V stages
+constexpr int kQWarp = 1 + kProducerWarps;       // TMA loads of Q (warp 0 issues the MMAs)
+constexpr int kSoftmaxWarp0 = kQWarp + 1;
 constexpr int kSoftmaxThreads = 256;             // eight softmax warps, two groups
 constexpr int kGroupThreads = 128;               // one softmax group: a thread per row
 constexpr int kThreadsTc = 32 * kSoftmaxWarp0 + kSoftmaxThreads;
 constexpr int kHalfBytes = 64 * 128;             // 64 rows of one 64-dim half: 8 KB
 constexpr int kStageBytesTc = 4 * kHalfBytes;    // K then V, two halves each: 32 KB
+constexpr int kRowHalfBytes = kRowsTc * 128;     // 128 rows x 64 dims of Q or of the output: 16 KB
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns (32 bits each; lane = query row), per softmax group g:
-// O_g fp32 [128], S_g fp32 [64], P_g two 16-bit values per column [32]; Q two
-// 16-bit values per column [64], shared
+// O_g fp32 [128], S_g fp32 [64], P_g two 16-bit values per column [32]; the
+// piece's Q two 16-bit values per column [64]
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 384, kColQ = 448;
 constexpr uint32_t kColOStep = 128, kColSStep = 64, kColPStep = 32;
 constexpr float kGapTc = 8.0f;                   // log2-domain slack before rescaling O
 constexpr int kQuotaMinTc = 16;                  // tiles per CTA at least: fewer split pieces
 constexpr int kPartFloats = 130 * kRowsTc;       // a partial: O^T [128][128], max, sum
-constexpr int kTcMinRows = 64;                   // rows per KV head from which it is picked
+constexpr int kTcMinRows = 32;                   // rows per KV head from which it is picked
+                                                 // (measured faster than mma.sync from 32 rows)
+constexpr int kCtxCache = 128;                   // context lengths cached from the CTA's first sequence
 constexpr unsigned FULLM = 0xffffffffu;
 
 struct TcParams {
@@ -82,8 +86,12 @@ struct TcParams {
     int32_t* status;
     int32_t* flags;             // per CTA: pieces of the split segment it starts, done
     float* partials;            // [2 * grid][kPartFloats]
-    int B, T, N, K, G, R;
-    int C, Rc, KC;              // row chunks per KV head, rows per chunk, virtual heads
+    int B, T, N, K, G;
+    // A row chunk (virtual head) is a box of tpc new tokens x hpc query heads of
+    // one KV head, Rc = tpc * hpc <= 128 rows (row = token-in-box * hpc +
+    // head-in-box); a KV head has C chunks: cpt per token block (G > 128)
+    // times ceil(T / tpc) token blocks.
+    int tpc, hpc, cpt, C, Rc, KC;
     int max_blocks, num_blocks;
     float scale_log2;
 };
@@ -91,7 +99,9 @@ struct TcParams {
 struct TcSmem {
     uint64_t full[kStagesTc];   // stage data landed (TMA transaction bytes)
     uint64_t empty[kStagesTc];  // the PV product of the stage completed
-    uint64_t q_ready;           // softmax threads wrote the piece's Q rows (tensor memory)
+    uint64_t q_full;            // the piece's Q box landed in shared memory (TMA bytes)
+    uint64_t q_free;            // every QK^T of the previous piece completed
+    uint64_t o_free;            // the softmax threads read O_0 / O_1 of the previous piece (256)
     uint64_t s_ready[2];        // QK^T of a stage of group g completed
     uint64_t p_ready[2];        // group g wrote P_g (and zeroed stale V rows)
     uint64_t o_ready[2];        // PV of a stage of group g completed
@@ -107,11 +117,19 @@ struct TcSmem {
     float xm[2][kRowsTc];       // per group: running max of each row at the piece's end
     float xl[2][kRowsTc];       // per group: sum of each row
     int xb[2][kRowsTc];         // per group: a stage held an invalid block id
+    int ctxc[kCtxCache];        // context_lens[b0 + i]: no dependent global load at a piece change
 };
 
-__device__ __forceinline__ int tc_nblk(const TcParams& p, int b) {
-    const int ctx = __ldg(p.context_lens + b);
+__device__ __forceinline__ int tc_nblk_of(const TcParams& p, int ctx) {
     return (ctx >= p.T && ctx >= 1 && ctx <= p.max_blocks * 16) ? (ctx + 15) >> 4 : 0;
+}
+__device__ __forceinline__ int tc_nblk(const TcParams& p, int b) {
+    return tc_nblk_of(p, __ldg(p.context_lens + b));
+}
+// context_lens[b] from the shared-memory copy where it holds b
+__device__ __forceinline__ int tc_ctx(const TcSmem& sm, const TcParams& p, int b) {
+    const int i = b - sm.b0;
+    return (i >= 0 && i < kCtxCache) ? sm.ctxc[i] : __ldg(p.context_lens + b);
 }
 
 __device__ __forceinline__ void tc_abort(TcSmem& sm, const TcParams& p) {
@@ -146,13 +164,15 @@ struct TcPiece {
 struct TcWalker {
     long long pos, c1, base;
     int b, v, nb;
-    __device__ void init(const TcSmem& sm, const TcParams& p) {
-        pos = sm.c0;
-        c1 = sm.c1;
-        base = sm.base;
-        b = sm.b0;
+    const TcSmem* sm;
+    __device__ void init(const TcSmem& s, const TcParams& p) {
+        sm = &s;
+        pos = s.c0;
+        c1 = s.c1;
+        base = s.base;
+        b = s.b0;
         v = 0;
-        nb = (pos < c1) ? tc_nblk(p, b) : 0;
+        nb = (pos < c1) ? tc_nblk_of(p, tc_ctx(s, p, b)) : 0;
     }
     __device__ bool next(const TcParams& p, TcPiece& pc) {
         while (pos < c1) {
@@ -172,7 +192,7 @@ struct TcWalker {
             base += (long long)p.KC * nb;
             v = 0;
             if (++b >= p.B) break;
-            nb = tc_nblk(p, b);
+            nb = tc_nblk_of(p, tc_ctx(*sm, p, b));
         }
         pos = c1;
         return false;
@@ -220,6 +240,10 @@ __device__ void tc_plan(const TcParams& p, TcSmem& sm) {
             acc += n;
         }
     }
+    __syncwarp();
+    const int b0 = sm.b0;
+    for (int i = lane; i < kCtxCache; i += 32)
+        sm.ctxc[i] = (b0 + i < p.B) ? __ldg(p.context_lens + b0 + i) : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -302,16 +326,71 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
 }
 
 // ---------------------------------------------------------------------------
+// Box of a row chunk in the 5-D view (dim, head in group, KV head, token,
+// sequence) of q and out.
+struct TcBox {
+    int h0, t0;  // first query head (within the group) and first new token of the chunk
+};
+__device__ __forceinline__ TcBox tc_box(const TcParams& p, int chunk) {
+    TcBox x;
+    x.h0 = (chunk % p.cpt) * p.hpc;
+    x.t0 = (chunk / p.cpt) * p.tpc;
+    return x;
+}
+
+// Lane 0 of warp kQWarp: the Q box of every piece, two 64-dim halves by TMA
+// into the shared Q buffer (128-byte swizzled, as an MMA operand; rows past
+// the box keep stale bytes: their S, P and O rows are never read).  The box
+// of piece k is loaded once the MMA issuer's copy of box k - 1 into tensor
+// memory has completed.
+__device__ void tc_qloader(const CUtensorMap* tmq, const TcParams& p, uint8_t* qbuf, TcSmem& sm) {
+    if ((threadIdx.x & 31) != 0) return;
+    tma_prefetch_desc(tmq);
+    TcWalker wk;
+    wk.init(sm, p);
+    TcPiece pc;
+    int k = 0;
+    const uint32_t bytes = 2u * 128u * (uint32_t)p.Rc;
+    bool aborted = false;
+    while (!aborted && wk.next(p, pc)) {
+        if (k >= 1 && !mbar_wait(smem_addr(&sm.q_free), (k - 1) & 1)) tc_abort(sm, p);
+        aborted = sm.abort_flag != 0;
+        if (aborted) break;
+        const TcBox x = tc_box(p, pc.v % p.C);
+        const int kv = pc.v / p.C;
+        mbar_arrive_expect_tx(smem_addr(&sm.q_full), bytes);
+        for (int h = 0; h < 2; ++h)
+            tma_load_5d(smem_addr(qbuf) + h * kRowHalfBytes, tmq, smem_addr(&sm.q_full), 64 * h, x.h0,
+                        kv, x.t0, pc.b);
+        ++k;
+    }
+    if (aborted && k >= 1) mbar_wait(smem_addr(&sm.q_full), (k - 1) & 1);  // the last box landed
+}
+
+// ---------------------------------------------------------------------------
 // One elected thread issues every MMA.  Stage st of a piece belongs to
-// softmax group g = st % 2.  QK^T of the first two stages is issued when the
-// piece's Q is in tensor memory; then, per stage, PV(st) as soon as group g
-// has written P_g(st), and right after it QK^T(st + 2) into S_g, which group
-// g has finished reading (it wrote P_g from it).  Operand descriptors are
-// built once; per stage and per instruction only constants are added (the
-// 14-bit address field cannot carry: shared memory ends below 256 KB), which
-// keeps the issue rate at the tensor pipe's.
+// softmax group g = st % 2.  When the piece's Q box has landed -- typically
+// long before, right after the previous piece's last PVs have been issued --
+// the issuer copies it into tensor memory (tcgen05.cp, in issue order after
+// the previous piece's QK^T products that read the old Q; a commit then frees
+// the shared buffer for the next box) and issues QK^T of the first two
+// stages, which run while the softmax threads finish the previous piece; then,
+// per stage, PV(st) as soon as group g has written P_g(st), and right after
+// it QK^T(st + 2) into S_g, which group g has finished reading (it wrote P_g
+// from it) once stage st + 2 has landed.  PV(st) goes first because its
+// completion frees the ring slot of stage st for the producer (waiting for
+// stage st + 2 before it would make the ring two stages shallower).  The first
+// PV of a piece overwrites O_g and so also waits until the softmax threads
+// have read the previous piece's O.  (Q is read from
+// tensor memory, not shared memory, which keeps the A operand off the shared
+// memory port that the ring's TMA writes also use.)  Operand descriptors are
+// built once and only constants are added per instruction: an MMA whose
+// descriptors were rebuilt in the issuing loop measured 130-200 cycles of
+// issue each, and the issuer's queue holds only a few MMAs (the 14-bit address
+// field cannot carry: shared memory ends below 256 KB).
 template <bool BF16>
-__device__ void tc_mma(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t tmem) {
+__device__ void tc_mma(const TcParams& p, uint8_t* stages, uint8_t* qbuf, TcSmem& sm,
+                       uint32_t tmem) {
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
         constexpr uint32_t id_s = umma_idesc_ct(BF16, kRowsTc, 64, false);  // S = Q . K^T
@@ -319,11 +398,10 @@ __device__ void tc_mma(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t 
         const uint32_t st0 = smem_addr(stages);
         const uint64_t dk0 = umma_desc_sw128(st0, 16, 1024);                        // K, K-major
         const uint64_t dv0 = umma_desc_sw128(st0 + 2 * kHalfBytes, kHalfBytes, 1024); // V, MN-major
+        const uint64_t dq = umma_desc_sw128(smem_addr(qbuf), 16, 1024);             // Q, K-major
         const uint32_t tQ = tmem + kColQ;
-        // S_g = Q . K(n)^T once stage n has landed
-        auto issue_qk = [&](int n, int g) -> bool {
-            if (!stage_landed(sm, n)) return false;
-            tc_fence_after();
+        // S_g = Q . K(n)^T (stage n came by TMA; Q is in tensor memory)
+        auto issue_qk = [&](int n, int g) {
             const uint32_t tS = tmem + kColS + g * kColSStep;
             const uint64_t dk = dk0 + (uint64_t)((n % kStagesTc) * (kStageBytesTc >> 4));
 #pragma unroll
@@ -331,29 +409,39 @@ __device__ void tc_mma(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t 
                 umma_ts(tS, tQ + 8 * kk, dk + (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4),
                         id_s, kk > 0);
             umma_commit(smem_addr(&sm.s_ready[g]));
-            return true;
         };
         TcWalker wk;
         wk.init(sm, p);
         TcPiece pc;
-        int n = 0, qs = 0;
+        int n = 0, k = 0;
         int kp0 = 0, kp1 = 0;  // P_0 / P_1 writes consumed so far (barrier phases)
         bool ok = true;
         while (ok && wk.next(p, pc)) {
             const int nst = (pc.t1 - pc.t0 + 3) / 4;
-            ok = mbar_wait(smem_addr(&sm.q_ready), qs & 1);
-            ++qs;
-            ok = ok && !sm.abort_flag && issue_qk(n, 0);
-            if (ok && nst > 1) ok = issue_qk(n + 1, 1);
+            ok = mbar_wait(smem_addr(&sm.q_full), k & 1) && !sm.abort_flag && stage_landed(sm, n);
+            if (ok) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // the Q box into tensor memory, 32 B of each row at a time
+                    tmem_cp_128x256b(tQ + 8 * kk,
+                                     dq + (uint64_t)(((kk >> 2) * kRowHalfBytes + (kk & 3) * 32) >> 4));
+                umma_commit(smem_addr(&sm.q_free));
+                issue_qk(n, 0);
+            }
+            if (ok && nst > 1) {
+                ok = stage_landed(sm, n + 1);
+                if (ok) issue_qk(n + 1, 1);
+            }
             for (int st = 0; st < nst && ok; ++st, ++n) {
                 const int g = st & 1;
-                ok = mbar_wait(smem_addr(&sm.p_ready[g]), (g ? kp1 : kp0) & 1);
+                const bool more = st + 2 < nst;
+                ok = mbar_wait(smem_addr(&sm.p_ready[g]), (g ? kp1 : kp0) & 1) &&
+                     (st >= 2 || k == 0 || mbar_wait(smem_addr(&sm.o_free), (k - 1) & 1));
                 if (g)
                     ++kp1;
                 else
                     ++kp0;
                 if (!ok || sm.abort_flag) break;
-                tc_fence_after();
+                tc_fence_after();  // P_g was written by the softmax threads
                 const uint32_t tO = tmem + kColO + g * kColOStep, tP = tmem + kColP + g * kColPStep;
                 const uint64_t dv = dv0 + (uint64_t)((n % kStagesTc) * (kStageBytesTc >> 4));
                 umma_ts(tO, tP, dv, id_o, st >= 2);
@@ -362,8 +450,12 @@ __device__ void tc_mma(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t 
                     umma_ts(tO, tP + ks * 8, dv + (uint64_t)((ks * 2048) >> 4), id_o, true);
                 umma_commit(smem_addr(&sm.o_ready[g]));
                 umma_commit(smem_addr(&sm.empty[n % kStagesTc]));
-                if (st + 2 < nst) ok = issue_qk(n + 2, g);
+                if (more) {
+                    ok = stage_landed(sm, n + 2);
+                    if (ok) issue_qk(n + 2, g);
+                }
             }
+            ++k;
             if (!ok) tc_abort(sm, p);
             if (sm.abort_flag) ok = false;
         }
@@ -413,16 +505,19 @@ __device__ __forceinline__ void store_row32(uint4* dst, const uint32_t (&o)[32],
         dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-// Softmax group g = (warp - 3) / 4: its warps reach tensor-memory lane
-// quarters 3, 0, 1, 2 (a warp reaches lanes 32 * (warp % 4) .. + 31), one
-// thread per query row.  The group runs the online softmax of the stages
+// Softmax group g = (warp - kSoftmaxWarp0) / 4: its warps reach tensor-memory
+// lane quarters 3, 0, 1, 2 (a warp reaches lanes 32 * (warp % 4) .. + 31),
+// one thread per query row.  The group runs the online softmax of the stages
 // st = g, g + 2, ... of each piece into its own O_g.  At the piece's end the
 // two threads of a row (one per group) exchange running max, sum and
-// invalid-block flag through shared memory and each combines both groups'
-// O over its half of the head dimension (g = 0: dims 0..63, g = 1: 64..127),
-// with log-sum-exp weights, into the row's output or a split-segment partial.
+// invalid-block flag through shared memory, each reads both groups' O over
+// its half of the head dimension (g = 0: dims 0..63, g = 1: 64..127), frees
+// O for the next piece's PV products, and combines them with log-sum-exp
+// weights into the row's output -- staged in shared memory and written by
+// one TMA store per half -- or into a split-segment partial.
 template <bool BF16>
-__device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint32_t tmem) {
+__device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* stages,
+                           uint8_t* obuf, TcSmem& sm, uint32_t tmem) {
     using E = Elt<BF16>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int quarter = warp & 3;
@@ -433,7 +528,9 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
     const uint32_t trow = tmem + ((uint32_t)(32 * quarter) << 16);
     const uint32_t tS = trow + kColS + g * kColSStep, tP = trow + kColP + g * kColPStep;
     const uint32_t tOg = trow + kColO + g * kColOStep;  // this group's accumulator
-    const uint32_t tQ = trow + kColQ + 32 * g;
+    // this thread's 128 bytes of the staged output (row, half g; 128-byte swizzle)
+    const uint32_t ostage = smem_addr(obuf) + g * kRowHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
+    if (tsm == 0) tma_prefetch_desc(tmo);
     // sequences with an invalid length: zero outputs (CTA 0), status
     if (blockIdx.x == 0) {
         for (int b = tsm; b < p.B; b += kSoftmaxThreads) {
@@ -451,34 +548,41 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
     int kg = 0;  // stages of this group so far (barrier phases of s_ready[g], o_ready[g])
     int pp = 0, ap = 0;  // phases of this thread's pair barrier and of the softmax barrier
     bool ok = true;
-    while (ok && wk.next(p, pc)) {
-        const int b = pc.b, kv = pc.v / p.C, chunk = pc.v % p.C;
-        const int r = chunk * p.Rc + row;
-        const bool active = row < p.Rc && r < p.R;
-        const int t = active ? r / p.G : 0, gg = active ? r % p.G : 0;
-        const int ctx = __ldg(p.context_lens + b);
-        const int nst = (pc.t1 - pc.t0 + 3) / 4;
-        // ---- this row's half of Q into tensor memory ----------------------------
-        {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(p.q) +
-                (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128 + 64 * g);
-            uint32_t qw[32];
+    // The staged rows (64 values of this thread's half, fp32 bit patterns)
+    // times inv, in q's dtype, into the staging buffer; then, once every
+    // softmax thread has written (and the store before has finished reading
+    // the buffer), one thread stores the box by TMA.
+    auto stage_row = [&](const uint32_t (&o)[64], float inv) {
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const uint4 x = active ? __ldg(src + cc) : make_uint4(0, 0, 0, 0);
-                qw[4 * cc] = x.x;
-                qw[4 * cc + 1] = x.y;
-                qw[4 * cc + 2] = x.z;
-                qw[4 * cc + 3] = x.w;
-            }
-            tmem_st32(tQ, qw);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_addr(&sm.q_ready));
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t w0 = E::pack(__uint_as_float(o[8 * j]) * inv, __uint_as_float(o[8 * j + 1]) * inv);
+            const uint32_t w1 = E::pack(__uint_as_float(o[8 * j + 2]) * inv, __uint_as_float(o[8 * j + 3]) * inv);
+            const uint32_t w2 = E::pack(__uint_as_float(o[8 * j + 4]) * inv, __uint_as_float(o[8 * j + 5]) * inv);
+            const uint32_t w3 = E::pack(__uint_as_float(o[8 * j + 6]) * inv, __uint_as_float(o[8 * j + 7]) * inv);
+            st_shared_v4(ostage + ((j ^ (row & 7)) << 4), make_uint4(w0, w1, w2, w3));
         }
-        const int fn = ctx - p.T;  // position of the first new token
-        const int lim = fn + t;    // last position this row sees
+        fence_proxy_async_shared();
+    };
+    auto store_box = [&](int b, int kv, const TcBox& x) {
+        if (tsm == 0) {
+            for (int h = 0; h < 2; ++h)
+                tma_store_5d(tmo, smem_addr(obuf) + h * kRowHalfBytes, 64 * h, x.h0, kv, x.t0, b);
+            bulk_commit();
+        }
+    };
+    while (ok && wk.next(p, pc)) {
+        __syncwarp();
+        const int b = pc.b, kv = pc.v / p.C;
+        const TcBox box = tc_box(p, pc.v % p.C);
+        const int t = box.t0 + row / p.hpc, gg = box.h0 + row % p.hpc;
+        const bool active = row < p.Rc && t < p.T && gg < p.G;
+        // a warp whose rows are all padding skips the softmax arithmetic: the
+        // lanes of its rows in S, P and O are never read out
+        const bool warp_active = __any_sync(FULLM, active);
+        const int ctx = tc_ctx(sm, p, b);
+        const int nst = (pc.t1 - pc.t0 + 3) / 4;
+        const int fn = ctx - p.T;             // position of the first new token
+        const int lim = fn + (active ? t : 0);  // last position this row sees
         // tree rows: the new positions this row sees (its ancestors and itself)
         const uint64_t tmk = (p.tree_mask && active)
                                  ? (__ldg(p.tree_mask + (size_t)b * p.T + t) | (1ull << t))
@@ -492,73 +596,80 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
             ok = stage_landed(sm, n) && mbar_wait(smem_addr(&sm.s_ready[g]), kg & 1);
             ok = __all_sync(FULLM, ok);  // warp-collective tensor-memory accesses follow
             if (!ok) break;
-            tc_fence_after();
-            uint32_t sa[32], sb[32];
-            tmem_ld32(tS, sa);
-            tmem_ld32(tS + 32, sb);
-            tmem_wait_ld();
-            bad |= sm.bad[s] != 0;
             const int blk0 = pc.t0 + 4 * st;
             const int tok0 = blk0 * 16;
             const int tiles = min(4, pc.t1 - blk0);
-            // visible columns of the stage as one word: loaded and causal ...
-            const int vis_end = min(tiles * 16, lim + 1 - tok0);
-            uint64_t vm = vis_end >= 64 ? ~0ull : vis_end <= 0 ? 0ull : (1ull << vis_end) - 1;
-            if (p.tree_mask) {  // ... and, among the new positions, on the row's tree path
-                const int d = fn - tok0;  // stage column of the first new token
-                if (d < 64) {
-                    const uint64_t nbits = d >= 0 ? tmk << d : (-d < 64 ? tmk >> -d : 0ull);
-                    const uint64_t nmask = d >= 0 ? ~0ull << d : ~0ull;
-                    vm &= ~nmask | nbits;
+            bad |= sm.bad[s] != 0;
+            if (warp_active) {
+                tc_fence_after();
+                uint32_t sa[32], sb[32];
+                tmem_ld32(tS, sa);
+                tmem_ld32(tS + 32, sb);
+                tmem_wait_ld();
+                // visible columns of the stage as one word: loaded and causal ...
+                const int vis_end = min(tiles * 16, lim + 1 - tok0);
+                uint64_t vm = vis_end >= 64 ? ~0ull : vis_end <= 0 ? 0ull : (1ull << vis_end) - 1;
+                if (p.tree_mask) {  // ... and, among the new positions, on the row's tree path
+                    const int d = fn - tok0;  // stage column of the first new token
+                    if (d < 64) {
+                        const uint64_t nbits = d >= 0 ? tmk << d : (-d < 64 ? tmk >> -d : 0ull);
+                        const uint64_t nmask = d >= 0 ? ~0ull << d : ~0ull;
+                        vm &= ~nmask | nbits;
+                    }
                 }
-            }
-            float sv[64];
+                float sv[64];
+                if (__all_sync(FULLM, vm == ~0ull)) {  // a stage inside every row's context
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                sv[j] = (vm >> j) & 1ull ? __uint_as_float(j < 32 ? sa[j] : sb[j - 32]) : -INFINITY;
-            const float x = max_tree(sv) * p.scale_log2;
-            // running max; O_g is rescaled (lazily) in tensor memory, warp by warp
-            const bool need = x > m + kGapTc;
-            if (__any_sync(FULLM, need)) {
-                const float f = (need && m != -INFINITY) ? fast_exp2(m - x) : 1.f;
-                if (mine > 0) {  // PV of this group's previous stage has completed
+                    for (int j = 0; j < 64; ++j) sv[j] = __uint_as_float(j < 32 ? sa[j] : sb[j - 32]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        sv[j] = (vm >> j) & 1ull ? __uint_as_float(j < 32 ? sa[j] : sb[j - 32]) : -INFINITY;
+                }
+                const float x = max_tree(sv) * p.scale_log2;
+                // running max; O_g is rescaled (lazily) in tensor memory, warp by warp
+                const bool need = x > m + kGapTc;
+                if (__any_sync(FULLM, need)) {
+                    const float f = (need && m != -INFINITY) ? fast_exp2(m - x) : 1.f;
+                    if (mine > 0) {  // PV of this group's previous stage has completed
+                        ok = __all_sync(FULLM, mbar_wait(smem_addr(&sm.o_ready[g]), (kg - 1) & 1));
+                        if (!ok) break;
+                        tc_fence_after();
+    #pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tOg + 32 * c, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k)
+                                o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+                            tmem_st32(tOg + 32 * c, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    if (need) {
+                        l *= f;
+                        m = x;
+                    }
+                }
+                const float nref = (m == -INFINITY) ? 0.f : -m;
+                uint32_t pw[32];
+                float ps[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    pw[k] = E::pack(fast_exp2(fmaf(sv[2 * k], p.scale_log2, nref)),
+                                         fast_exp2(fmaf(sv[2 * k + 1], p.scale_log2, nref)));
+                    ps[k] = E::lo(pw[k]) + E::hi(pw[k]);
+                }
+                l += sum_tree(ps);
+                if (mine > 0) {  // the previous PV of this group has read P_g
                     ok = __all_sync(FULLM, mbar_wait(smem_addr(&sm.o_ready[g]), (kg - 1) & 1));
                     if (!ok) break;
                     tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(tOg + 32 * c, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-                        tmem_st32(tOg + 32 * c, o);
-                    }
-                    tmem_wait_st();
                 }
-                if (need) {
-                    l *= f;
-                    m = x;
-                }
-            }
-            const float nref = (m == -INFINITY) ? 0.f : -m;
-            uint32_t pw[32];
-            float ps[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                pw[k] = E::pack(fast_exp2(fmaf(sv[2 * k], p.scale_log2, nref)),
-                                     fast_exp2(fmaf(sv[2 * k + 1], p.scale_log2, nref)));
-                ps[k] = E::lo(pw[k]) + E::hi(pw[k]);
-            }
-            l += sum_tree(ps);
-            if (mine > 0) {  // the previous PV of this group has read P_g
-                ok = __all_sync(FULLM, mbar_wait(smem_addr(&sm.o_ready[g]), (kg - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
-            }
-            tmem_st32(tP, pw);
-            tmem_wait_st();
+                tmem_st32(tP, pw);
+                tmem_wait_st();
+            }  // warp_active
             // V rows without data in this stage: zero them (NaN-safe products)
             const int valid_rows = max(0, min(tiles * 16, ctx - tok0));
             if (valid_rows < 64) {
@@ -599,56 +710,55 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
         const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
         const float lt = w0 * sm.xl[0][row] + w1 * sm.xl[1][row];
         bad = (sm.xb[0][row] | sm.xb[1][row]) != 0;
-        // columns 32c .. 32c+31 of this thread's half of the dims: w0 O_0 + w1 O_1
-        // (a group without stages in this piece has weight 0 and is not read)
-        auto combined = [&](int c, uint32_t (&o)[32]) {
+        // this thread's half of the dims: w0 O_0 + w1 O_1 (a group without
+        // stages in this piece has weight 0 and is not read); then O is free
+        uint32_t o[64];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
             uint32_t a0[32], a1[32];
             tmem_ld32(trow + kColO + 64 * g + 32 * c, a0);
             tmem_ld32(trow + kColO + kColOStep + 64 * g + 32 * c, a1);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k)
-                o[k] = __float_as_uint((w0 != 0.f ? w0 * __uint_as_float(a0[k]) : 0.f) +
-                                       (w1 != 0.f ? w1 * __uint_as_float(a1[k]) : 0.f));
-        };
-        uint4* dst = reinterpret_cast<uint4*>(
-                         static_cast<uint16_t*>(p.out) +
-                         (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128) +
-                     8 * g;
+                o[32 * c + k] = __float_as_uint((w0 != 0.f ? w0 * __uint_as_float(a0[k]) : 0.f) +
+                                                (w1 != 0.f ? w1 * __uint_as_float(a1[k]) : 0.f));
+        }
+        tc_fence_before();
+        mbar_arrive(smem_addr(&sm.o_free));
         const int first_cta = (int)(pc.first / sm.quota);
         const int last_cta = (int)((pc.first + pc.nb - 1) / sm.quota);
         if (first_cta == last_cta) {  // the whole segment: O / l in q's dtype
             const bool zero = bad || !(lt > 0.f);  // an invalid block id: zeros
-            const float inv = zero ? 0.f : 1.f / lt;
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                uint32_t o[32];
-                combined(c, o);
-                if (zero) {
+            if (zero) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = 0u;
-                }
-                if (active) store_row32<BF16>(dst + 4 * c, o, inv);
+                for (int k = 0; k < 64; ++k) o[k] = 0u;
             }
-            tc_fence_before();
+            if (tsm == 0) bulk_wait_read();  // the previous box has left the staging buffer
+            ok = softmax_bar(sm, ap);
+            if (active) stage_row(o, zero ? 0.f : 1.f / lt);
+            ok = __all_sync(FULLM, ok && softmax_bar(sm, ap));
+            if (!ok) {
+                tc_abort(sm, p);
+                break;
+            }
+            store_box(b, kv, box);
             continue;
         }
         // ---- a piece of a split segment: publish; the last piece merges ----------
+        // (rows of real queries only: padding rows are neither written nor read)
         float* part = p.partials + (size_t)(2 * blockIdx.x + (pc.t0 == 0 ? 1 : 0)) * kPartFloats;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            combined(c, o);
+        if (active) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k)
-                __stcg(part + (64 * g + 32 * c + k) * kRowsTc + row, __uint_as_float(o[k]));
-        }
-        tc_fence_before();
-        if (g == 0) {
-            __stcg(part + 128 * kRowsTc + row, M);
-            __stcg(part + 129 * kRowsTc + row, bad ? -1.f : lt);  // -1: the piece saw a bad block
+            for (int k = 0; k < 64; ++k)
+                __stcg(part + (64 * g + k) * kRowsTc + row, __uint_as_float(o[k]));
+            if (g == 0) {
+                __stcg(part + 128 * kRowsTc + row, M);
+                __stcg(part + 129 * kRowsTc + row, bad ? -1.f : lt);  // -1: the piece saw a bad block
+            }
         }
         __threadfence();
+        if (tsm == 0) bulk_wait_read();  // the previous box has left the staging buffer
         ok = softmax_bar(sm, ap);
         if (ok && tsm == 0) {
             const int old = atomicAdd(p.flags + first_cta, 1);
@@ -665,55 +775,62 @@ __device__ void tc_softmax(const TcParams& p, uint8_t* stages, TcSmem& sm, uint3
         if (!merge) continue;
         __threadfence();
         if (tsm == 0) p.flags[first_cta] = 0;  // back to zero for the next call
-        // the piece in first_cta starts the segment (slot 1), the others do not (slot 0)
-        auto piece_part = [&](int cta) -> const float* {
-            return p.partials + (size_t)(2 * cta + (cta == first_cta ? 1 : 0)) * kPartFloats;
-        };
-        float MM = -INFINITY;
-        bool any_bad = false;
-        for (int cta = first_cta; cta <= last_cta; ++cta) {
-            const float* pp_ = piece_part(cta);
-            MM = fmaxf(MM, __ldcg(pp_ + 128 * kRowsTc + row));
-            any_bad |= __ldcg(pp_ + 129 * kRowsTc + row) < 0.f;
-        }
-        float L = 0.f;
-        for (int cta = first_cta; cta <= last_cta; ++cta) {
-            const float* pp_ = piece_part(cta);
-            const float mi = __ldcg(pp_ + 128 * kRowsTc + row);
-            L += (mi == -INFINITY ? 0.f : fast_exp2(mi - MM)) * __ldcg(pp_ + 129 * kRowsTc + row);
-        }
-        const bool zero = any_bad || !(L > 0.f);
-        const float inv = zero ? 0.f : 1.f / L;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-            float acc[32];
+        if (active) {  // per-thread loads and arithmetic only
+            // the piece in first_cta starts the segment (slot 1), the others do not (slot 0)
+            auto piece_part = [&](int cta) -> const float* {
+                return p.partials + (size_t)(2 * cta + (cta == first_cta ? 1 : 0)) * kPartFloats;
+            };
+            // two rounds of independent loads: every piece's (max, sum), then every
+            // piece's 64 values, folded in piece order
+            float MM = -INFINITY;
+            bool any_bad = false;
+            for (int cta = first_cta; cta <= last_cta; ++cta) {
+                const float* pp_ = piece_part(cta);
+                MM = fmaxf(MM, __ldcg(pp_ + 128 * kRowsTc + row));
+                any_bad |= __ldcg(pp_ + 129 * kRowsTc + row) < 0.f;
+            }
+            float L = 0.f, acc[64];
 #pragma unroll
-            for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
             for (int cta = first_cta; cta <= last_cta; ++cta) {
                 const float* pp_ = piece_part(cta);
                 const float mi = __ldcg(pp_ + 128 * kRowsTc + row);
-                const float w = (zero || mi == -INFINITY) ? 0.f : fast_exp2(mi - MM);
+                const float w = (any_bad || mi == -INFINITY) ? 0.f : fast_exp2(mi - MM);
+                L += w * __ldcg(pp_ + 129 * kRowsTc + row);
+                const float* src = pp_ + (64 * g) * kRowsTc + row;
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    acc[k] += w * __ldcg(pp_ + (64 * g + 32 * c + k) * kRowsTc + row);
+                for (int k = 0; k < 64; ++k) acc[k] += w * __ldcg(src + k * kRowsTc);
             }
-            uint32_t o[32];
+            const bool zero = any_bad || !(L > 0.f);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(acc[k]);
-            if (active) store_row32<BF16>(dst + 4 * c, o, inv);
+            for (int k = 0; k < 64; ++k) o[k] = zero ? 0u : __float_as_uint(acc[k]);
+            stage_row(o, zero ? 0.f : 1.f / L);
         }
+        ok = __all_sync(FULLM, softmax_bar(sm, ap));
+        if (!ok) {
+            tc_abort(sm, p);
+            break;
+        }
+        store_box(b, kv, box);
     }
+    if (tsm == 0) bulk_wait_all();  // the boxes stored before the CTA leaves
 }
 
 template <bool BF16>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_attention_kernel(const __grid_constant__ CUtensorMap tmk,
-                        const __grid_constant__ CUtensorMap tmv, const TcParams p) {
+                        const __grid_constant__ CUtensorMap tmv,
+                        const __grid_constant__ CUtensorMap tmq,
+                        const __grid_constant__ CUtensorMap tmo, const TcParams p) {
+    // shared memory (1024-byte aligned): the K / V ring, the Q box (A operand
+    // of QK^T), the output staging box, the barriers and scratch
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stages = base;
-    TcSmem& sm = *reinterpret_cast<TcSmem*>(stages + (size_t)kStagesTc * kStageBytesTc);
+    uint8_t* qbuf = stages + (size_t)kStagesTc * kStageBytesTc;
+    uint8_t* obuf = qbuf + 2 * kRowHalfBytes;
+    TcSmem& sm = *reinterpret_cast<TcSmem*>(obuf + 2 * kRowHalfBytes);
     const int warp = threadIdx.x >> 5;
     griddep_launch_dependents();
     if (threadIdx.x == 0) {
@@ -722,7 +839,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             mbar_init(smem_addr(&sm.empty[s]), 1);
             sm.bad[s] = 0;
         }
-        mbar_init(smem_addr(&sm.q_ready), kSoftmaxThreads);
+        mbar_init(smem_addr(&sm.q_full), 1);
+        mbar_init(smem_addr(&sm.q_free), 1);
+        mbar_init(smem_addr(&sm.o_free), kSoftmaxThreads);
         for (int g = 0; g < 2; ++g) {
             mbar_init(smem_addr(&sm.s_ready[g]), 1);
             mbar_init(smem_addr(&sm.p_ready[g]), kGroupThreads);
@@ -743,18 +862,21 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     if (warp == 0)
-        tc_mma<BF16>(p, stages, sm, tmem);
-    else if (warp < kSoftmaxWarp0)
+        tc_mma<BF16>(p, stages, qbuf, sm, tmem);
+    else if (warp < kQWarp)
         tc_producer(&tmk, &tmv, p, stages, sm, warp - 1);
+    else if (warp == kQWarp)
+        tc_qloader(&tmq, p, qbuf, sm);
     else
-        tc_softmax<BF16>(p, stages, sm, tmem);
+        tc_softmax<BF16>(&tmo, p, stages, obuf, sm, tmem);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-constexpr size_t kSmemTc = 1024 + (size_t)kStagesTc * kStageBytesTc + sizeof(TcSmem);
+constexpr size_t kSmemTc =
+    1024 + (size_t)kStagesTc * kStageBytesTc + 4 * (size_t)kRowHalfBytes + sizeof(TcSmem);
 static_assert(kSmemTc <= 227 * 1024, "shared memory per CTA");
 
 }  // namespace
@@ -801,8 +923,22 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
             done[dev] = true;
         }
     }
-    CUtensorMap tmk, tmv;
-    if (!make_cache_map(&tmk, k_cache, s) || !make_cache_map(&tmv, v_cache, s)) return GQA_ERR_CUDA;
+    // row chunks: boxes of tpc new tokens x hpc query heads of one KV head
+    const int G = s.N / s.K;
+    int tpc, hpc, cpt;
+    if (G <= kRowsTc) {
+        hpc = G;
+        cpt = 1;
+        tpc = std::min(s.T, kRowsTc / G);
+    } else {
+        cpt = (G + kRowsTc - 1) / kRowsTc;
+        hpc = (G + cpt - 1) / cpt;
+        tpc = 1;
+    }
+    CUtensorMap tmk, tmv, tmq, tmo;
+    if (!make_cache_map(&tmk, k_cache, s) || !make_cache_map(&tmv, v_cache, s) ||
+        !make_rows_map(&tmq, q, s, hpc, tpc) || !make_rows_map(&tmo, out, s, hpc, tpc))
+        return GQA_ERR_CUDA;
     TcParams p;
     p.q = q;
     p.out = out;
@@ -816,10 +952,12 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
     p.T = s.T;
     p.N = s.N;
     p.K = s.K;
-    p.G = s.N / s.K;
-    p.R = s.T * p.G;
-    p.C = (p.R + kRowsTc - 1) / kRowsTc;
-    p.Rc = (p.R + p.C - 1) / p.C;
+    p.G = G;
+    p.tpc = tpc;
+    p.hpc = hpc;
+    p.cpt = cpt;
+    p.C = cpt * ((s.T + tpc - 1) / tpc);
+    p.Rc = tpc * hpc;
     p.KC = s.K * p.C;
     p.max_blocks = s.max_blocks_per_seq;
     p.num_blocks = s.num_blocks;
@@ -843,8 +981,9 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
     cfg.attrs = attr;
     cfg.numAttrs = (s.flags & (GQA_FLAG_PDL | GQA_FLAG_EARLY_KV)) ? 1 : 0;
     const cudaError_t e =
-        s.dtype == GQA_BF16 ? cudaLaunchKernelEx(&cfg, tc_attention_kernel<true>, tmk, tmv, p)
-                            : cudaLaunchKernelEx(&cfg, tc_attention_kernel<false>, tmk, tmv, p);
+        s.dtype == GQA_BF16
+            ? cudaLaunchKernelEx(&cfg, tc_attention_kernel<true>, tmk, tmv, tmq, tmo, p)
+            : cudaLaunchKernelEx(&cfg, tc_attention_kernel<false>, tmk, tmv, tmq, tmo, p);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 

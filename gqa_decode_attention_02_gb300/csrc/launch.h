@@ -64,6 +64,11 @@ gqa_status launch_kv_append_quant(const gqa_shape& s, const void* k_new, const v
 
 // TMA view (h, kv head, block*16 + row) of a cache, 128-byte boxes of 16 rows.
 bool make_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s);
+// 5-D TMA view (dim, query head within its group, KV head, new token,
+// sequence) of a [B][T][N][H = 128] tensor of q's dtype (q or out); one box =
+// 64 dims x hpc heads x tpc tokens of one KV head, 128-byte swizzled.
+// Elements outside the tensor read as zero and are not written.
+bool make_rows_map(CUtensorMap* m, const void* base, const gqa_shape& s, int hpc, int tpc);
 
 // Tensor-memory attention (tcgen05): decode / verify / tree verify with H = 128
 // over a cache in q's dtype, no window, no fused append (the caller appends

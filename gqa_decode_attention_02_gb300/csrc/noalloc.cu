@@ -58,12 +58,17 @@ extern "C" gqa_status gqa_decode_attention_noalloc(const gqa_shape* shape, const
                                                    int32_t* dev_status, void* stream) {
     if (!shape) return GQA_ERR_NULL;
     if (shape->T != 1) return GQA_ERR_SHAPE;  // decode: one new token per sequence
-    const size_t need = gqa_attention_workspace_size(shape);
-    if (need == 0) return GQA_ERR_SHAPE;
-    if (need > kScratchBytes) return GQA_ERR_WORKSPACE;  // beyond the fixed 8 MiB
+    if (gqa_attention_workspace_size(shape) == 0) return GQA_ERR_SHAPE;
     gqa::AttnPlan plan;
     const gqa_status st = gqa::attention_plan(*shape, false, &plan);
     if (st != GQA_OK) return st;
+    // the scratch of the kernel that serves the call (no engine is forced here)
+    const bool tc = (shape->flags & GQA_FLAG_WARP_MMA) == 0 &&
+                    ((shape->flags & GQA_FLAG_TENSOR_MEMORY) != 0 ||
+                     gqa::tc_attention_preferred(*shape));
+    const size_t need = tc ? gqa::tc_workspace_bytes(*shape, plan.flags_bytes) : plan.workspace;
+    if (need == 0) return GQA_ERR_SHAPE;
+    if (need > kScratchBytes) return GQA_ERR_WORKSPACE;  // beyond the fixed 8 MiB
     void* scratch = nullptr;
     const gqa_status ss = scratch_on_current_device(&scratch);
     if (ss != GQA_OK) return ss;

@@ -57,6 +57,13 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u));
 }
+// Tensor memory (128 lanes x 8 columns at taddr) <- 128 rows x 32 bytes of a
+// shared-memory matrix described like an MMA operand.  Asynchronous, and in
+// issue order with this thread's tcgen05.mma operations.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {

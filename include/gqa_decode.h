@@ -131,7 +131,7 @@ typedef struct {
 /* Attention only: which kernel computes the call.  By default the library
  * picks by shape: the tensor-memory kernel (tcgen05.mma, accumulators in
  * tensor memory, 128 query rows of one KV head per tile) where a KV head has
- * many query rows (T * N / K >= 64), the warp-level mma.sync kernel otherwise.
+ * many query rows (T * N / K >= 32), the warp-level mma.sync kernel otherwise.
  * GQA_FLAG_WARP_MMA forces the warp-level kernel; GQA_FLAG_TENSOR_MEMORY
  * forces the tensor-memory one, which serves H = 128 with a cache in q's dtype
  * and no window (GQA_ERR_SHAPE otherwise, or with both flags).  Both compute
@@ -209,8 +209,13 @@ gqa_status gqa_decode_attention(const gqa_shape *shape, const void *q,
  * gqa_decode_attention computes, with the same requirements, but takes no
  * workspace: its scratch is a static 8 MiB device array inside the library,
  * held on every GPU that loads the library until the process exits.
- *  - Shapes whose gqa_attention_workspace_size exceeds 8 MiB are rejected
- *    with GQA_ERR_WORKSPACE.
+ *  - Shapes whose scratch exceeds 8 MiB are rejected with GQA_ERR_WORKSPACE.
+ *    The scratch is what the kernel that serves the call needs: the
+ *    warp-level kernel's workspace, or the tensor-memory kernel's where the
+ *    shape picks that one (T * N / K >= 32, H = 128; its split-context
+ *    partials take ~133 KB per SM, more than 8 MiB on a full GPU, so such
+ *    shapes are rejected).  gqa_attention_workspace_size may report more: it
+ *    also covers a kernel forced by a flag.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
  *  - Each call first clears, on `stream`, the part of the array that must

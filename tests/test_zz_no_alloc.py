@@ -65,3 +65,8 @@ def test_noalloc_rejects_bad_shapes_before_touching_the_gpu(gpu):
     fake = ctypes.c_void_p(16)
     assert f(ctypes.byref(shape), fake, fake, fake, fake, fake, fake, None, None) == 2  # T != 1
     assert f(None, fake, fake, fake, fake, fake, fake, None, None) == 1
+    # 64 query rows per KV head pick the tensor-memory kernel, whose split
+    # partials exceed the fixed 8 MiB on a full GPU: rejected before any launch
+    mqa = _lib.Shape(B=2, T=1, N=64, K=1, H=128, block_size=16, num_blocks=4,
+                     max_blocks_per_seq=2, dtype=1, scale=0.0, flags=0)
+    assert f(ctypes.byref(mqa), fake, fake, fake, fake, fake, fake, None, None) == 5
