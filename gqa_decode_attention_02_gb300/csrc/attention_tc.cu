@@ -14,10 +14,12 @@
 // its T*G query rows; each segment is ceil(ctx_b / 16) tiles (cache blocks).
 // CTA c takes tiles [c*quota, (c+1)*quota) of that order (one CTA per SM), so
 // every SM streams the same number of bytes however ragged the batch.  A
-// segment cut by a range boundary leaves per-piece partial results (O
-// unnormalized, running max, sum) in the workspace; the piece that finishes
-// last merges them in piece order (a deterministic result) with log-sum-exp
-// weights -- the context split of FlashDecoding named in §"PagedAttention".
+// segment cut by range boundaries is split into pieces: every piece but the
+// first starts its CTA's range and publishes its partial result (O
+// unnormalized, running max, sum) in the workspace behind a release flag; the
+// first piece ends its CTA's range and folds the others into its own in piece
+// order (a deterministic result) with log-sum-exp weights -- the context split
+// of FlashDecoding named in §"PagedAttention".
 //
 // One CTA: warp 0 MMA issuer and tensor-memory owner, warps 1..2 producers
 // (TMA), warps 3..10 softmax in two groups of four warps (one thread per query
@@ -71,7 +73,7 @@ constexpr uint32_t kColO = 0, kColS = 256, kColP = 384, kColQ = 448;
 constexpr uint32_t kColOStep = 128, kColSStep = 64, kColPStep = 32;
 constexpr float kGapTc = 8.0f;                   // log2-domain slack before rescaling O
 constexpr int kQuotaMinTc = 16;                  // tiles per CTA at least: fewer split pieces
-constexpr int kPartFloats = 130 * kRowsTc;       // a partial: O^T [128][128], max, sum
+constexpr int kPartFloats = 132 * kRowsTc;       // a partial: O^T [128][128], (max, sum) per half
 constexpr int kTcMinRows = 32;                   // rows per KV head from which it is picked
                                                  // (measured faster than mma.sync from 32 rows)
 constexpr int kCtxCache = 128;                   // context lengths cached from the CTA's first sequence
@@ -85,7 +87,7 @@ struct TcParams {
     const uint64_t* tree_mask;  // nullptr: causal chain among the new tokens
     int32_t* status;
     int32_t* flags;             // per CTA: pieces of the split segment it starts, done
-    float* partials;            // [2 * grid][kPartFloats]
+    float* partials;            // [grid][kPartFloats]: the continuation piece of each CTA
     int B, T, N, K, G;
     // A row chunk (virtual head) is a box of tpc new tokens x hpc query heads of
     // one KV head, Rc = tpc * hpc <= 128 rows (row = token-in-box * hpc +
@@ -110,7 +112,6 @@ struct TcSmem {
     uint64_t all;               // every softmax thread (256)
     long long c0, c1, base;     // the CTA's tile range; first tile of segment (b0, 0)
     int b0, quota;
-    int merge;                  // this CTA merges the split segment just finished
     uint32_t tmem_base;
     int bad[kStagesTc];         // the stage's blocks include an invalid id
     volatile int abort_flag;
@@ -135,6 +136,26 @@ __device__ __forceinline__ int tc_ctx(const TcSmem& sm, const TcParams& p, int b
 __device__ __forceinline__ void tc_abort(TcSmem& sm, const TcParams& p) {
     report(p.status, GQA_ERR_TIMEOUT);
     sm.abort_flag = 1;
+}
+
+// Publication flags of split pieces (GPU scope): release store after the
+// partial's stores, acquire load before reading it; a bounded wait.
+__device__ __forceinline__ void flag_release(int32_t* f, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ int flag_acquire(const int32_t* f) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+__device__ __forceinline__ bool flag_wait(const int32_t* f) {
+    if (flag_acquire(f)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        __nanosleep(100);
+        if (flag_acquire(f)) return true;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // Waits until stage n has landed.
@@ -708,7 +729,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
         const float M = fmaxf(m0, m1);
         const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
         const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
-        const float lt = w0 * sm.xl[0][row] + w1 * sm.xl[1][row];
+        float lt = w0 * sm.xl[0][row] + w1 * sm.xl[1][row];
         bad = (sm.xb[0][row] | sm.xb[1][row]) != 0;
         // this thread's half of the dims: w0 O_0 + w1 O_1 (a group without
         // stages in this piece has weight 0 and is not read); then O is free
@@ -745,75 +766,84 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             store_box(b, kv, box);
             continue;
         }
-        // ---- a piece of a split segment: publish; the last piece merges ----------
-        // (rows of real queries only: padding rows are neither written nor read)
-        float* part = p.partials + (size_t)(2 * blockIdx.x + (pc.t0 == 0 ? 1 : 0)) * kPartFloats;
-        if (active) {
+        // ---- a piece of a split segment -------------------------------------------
+        // Every piece but the segment's first is the first piece of its CTA's
+        // range: it publishes its rows (partial O, max, sum -- each warp its 32
+        // rows x 64 dims) and goes on, each warp ending with a release store of
+        // its own flag.  The first piece ends its CTA's range: it waits for the
+        // flags of the other pieces' warps in the same position (bounded; a
+        // publisher never waits for anything of the merger, and the grid is one
+        // wave), folds their partials into its own registers in CTA order
+        // (deterministic), clears the flags for the next call and stores.
+        const int me = blockIdx.x;
+        const int wi = warp - kSoftmaxWarp0;  // this warp's flag among the CTA's eight
+        if (pc.t0 != 0) {
+            if (active) {
+                float* part = p.partials + (size_t)me * kPartFloats;
 #pragma unroll
-            for (int k = 0; k < 64; ++k)
-                __stcg(part + (64 * g + k) * kRowsTc + row, __uint_as_float(o[k]));
-            if (g == 0) {
-                __stcg(part + 128 * kRowsTc + row, M);
-                __stcg(part + 129 * kRowsTc + row, bad ? -1.f : lt);  // -1: the piece saw a bad block
+                for (int k = 0; k < 64; ++k)
+                    __stcg(part + (64 * g + k) * kRowsTc + row, __uint_as_float(o[k]));
+                __stcg(part + (128 + 2 * g) * kRowsTc + row, M);
+                __stcg(part + (129 + 2 * g) * kRowsTc + row, bad ? -1.f : lt);  // -1: a bad block
             }
+            __syncwarp();  // the lanes' stores before lane 0's release
+            if (lane == 0) flag_release(p.flags + 8 * me + wi, 1);
+            continue;
         }
-        __threadfence();
-        if (tsm == 0) bulk_wait_read();  // the previous box has left the staging buffer
-        ok = softmax_bar(sm, ap);
-        if (ok && tsm == 0) {
-            const int old = atomicAdd(p.flags + first_cta, 1);
-            sm.merge = old == last_cta - first_cta;
-        }
-        ok = ok && softmax_bar(sm, ap);
-        const bool merge = sm.merge != 0;
-        ok = ok && softmax_bar(sm, ap);  // every thread has read the decision before it is rewritten
-        ok = __all_sync(FULLM, ok);
-        if (!ok) {
-            tc_abort(sm, p);
-            break;
-        }
-        if (!merge) continue;
-        __threadfence();
-        if (tsm == 0) p.flags[first_cta] = 0;  // back to zero for the next call
-        if (active) {  // per-thread loads and arithmetic only
-            // the piece in first_cta starts the segment (slot 1), the others do not (slot 0)
-            auto piece_part = [&](int cta) -> const float* {
-                return p.partials + (size_t)(2 * cta + (cta == first_cta ? 1 : 0)) * kPartFloats;
-            };
-            // two rounds of independent loads: every piece's (max, sum), then every
-            // piece's 64 values, folded in piece order
-            float MM = -INFINITY;
-            bool any_bad = false;
-            for (int cta = first_cta; cta <= last_cta; ++cta) {
-                const float* pp_ = piece_part(cta);
-                MM = fmaxf(MM, __ldcg(pp_ + 128 * kRowsTc + row));
-                any_bad |= __ldcg(pp_ + 129 * kRowsTc + row) < 0.f;
-            }
-            float L = 0.f, acc[64];
+        bool got = true;
+        if (lane == 0)
+            for (int c = first_cta + 1; c <= last_cta; ++c) got &= flag_wait(p.flags + 8 * c + wi);
+        got = __shfl_sync(FULLM, got ? 1 : 0, 0) != 0;
+        __syncwarp();  // lane 0's acquire loads before every lane's reads of the partials
+        if (!got) tc_abort(sm, p);  // a piece never arrived (only after an aborted CTA)
+        if (active && got) {
+            // online fold: running max MM, sum L, unnormalized values o
+            float MM = M, L = bad ? -1.f : lt;
+            bool any_bad = bad;
+            for (int c = first_cta + 1; c <= last_cta; ++c) {
+                const float* pp_ = p.partials + (size_t)c * kPartFloats;
+                const float mc = __ldcg(pp_ + (128 + 2 * g) * kRowsTc + row);
+                const float lc = __ldcg(pp_ + (129 + 2 * g) * kRowsTc + row);
+                float v[64];
 #pragma unroll
-            for (int k = 0; k < 64; ++k) acc[k] = 0.f;
-            for (int cta = first_cta; cta <= last_cta; ++cta) {
-                const float* pp_ = piece_part(cta);
-                const float mi = __ldcg(pp_ + 128 * kRowsTc + row);
-                const float w = (any_bad || mi == -INFINITY) ? 0.f : fast_exp2(mi - MM);
-                L += w * __ldcg(pp_ + 129 * kRowsTc + row);
-                const float* src = pp_ + (64 * g) * kRowsTc + row;
+                for (int k = 0; k < 64; ++k) v[k] = __ldcg(pp_ + (64 * g + k) * kRowsTc + row);
+                any_bad |= lc < 0.f;
+                const float mn = fmaxf(MM, mc);
+                const float a = MM == -INFINITY ? 0.f : fast_exp2(MM - mn);
+                const float bw = mc == -INFINITY ? 0.f : fast_exp2(mc - mn);
 #pragma unroll
-                for (int k = 0; k < 64; ++k) acc[k] += w * __ldcg(src + k * kRowsTc);
+                for (int k = 0; k < 64; ++k)
+                    o[k] = __float_as_uint((a != 0.f ? a * __uint_as_float(o[k]) : 0.f) +
+                                           (bw != 0.f ? bw * v[k] : 0.f));
+                L = (a != 0.f ? a * L : 0.f) + (bw != 0.f ? bw * lc : 0.f);
+                MM = mn;
             }
             const bool zero = any_bad || !(L > 0.f);
+            if (zero) {
 #pragma unroll
-            for (int k = 0; k < 64; ++k) o[k] = zero ? 0u : __float_as_uint(acc[k]);
-            stage_row(o, zero ? 0.f : 1.f / L);
+                for (int k = 0; k < 64; ++k) o[k] = 0u;
+            }
+            lt = zero ? 0.f : L;
         }
-        ok = __all_sync(FULLM, softmax_bar(sm, ap));
+        __syncwarp();
+        if (lane == 0)
+            for (int c = first_cta + 1; c <= last_cta; ++c) p.flags[8 * c + wi] = 0;  // next call
+        if (!got) {
+#pragma unroll
+            for (int k = 0; k < 64; ++k) o[k] = 0u;
+            lt = 0.f;
+        }
+        if (tsm == 0) bulk_wait_read();  // the previous box has left the staging buffer
+        ok = softmax_bar(sm, ap);
+        if (active) stage_row(o, lt > 0.f ? 1.f / lt : 0.f);
+        ok = __all_sync(FULLM, ok && softmax_bar(sm, ap) && got);
         if (!ok) {
             tc_abort(sm, p);
             break;
         }
         store_box(b, kv, box);
     }
-    if (tsm == 0) bulk_wait_all();  // the boxes stored before the CTA leaves
+    if (tsm == 0) bulk_wait_read();  // the staging buffer is read before the CTA leaves
 }
 
 template <bool BF16>
@@ -851,7 +881,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         mbar_init(smem_addr(&sm.all), kSoftmaxThreads);
         mbar_init(smem_addr(&sm.done), 1);
         sm.abort_flag = 0;
-        sm.merge = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
@@ -894,7 +923,7 @@ size_t tc_workspace_bytes(const gqa_shape& s, size_t flags_bytes) {
     if (!tc_attention_supported(s)) return 0;
     const int sms = device_sm_count();
     if (sms < 1) return 0;
-    return flags_bytes + (size_t)2 * sms * kPartFloats * sizeof(float);
+    return flags_bytes + (size_t)sms * kPartFloats * sizeof(float);
 }
 
 gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_cache,
