@@ -12,8 +12,10 @@
 // Work order.  As in attention.cu: segments (sequence b, virtual head v) in
 // b-major order, a virtual head being a KV head and a chunk of at most 128 of
 // its T*G query rows; each segment is ceil(ctx_b / 16) tiles (cache blocks).
-// CTA c takes tiles [c*quota, (c+1)*quota) of that order (one CTA per SM), so
-// every SM streams the same number of bytes however ragged the batch.  A
+// CTA c takes units [c*quota, (c+1)*quota) of that order (one CTA per SM),
+// a segment being its tiles plus a few units for its start-up, so every SM
+// streams about the same bytes and pays about the same per-segment costs
+// however ragged the batch.  A
 // segment cut by range boundaries is split into pieces: every piece but the
 // first starts its CTA's range and publishes its partial result (O
 // unnormalized, running max, sum) in the workspace behind a release flag; the
@@ -73,6 +75,10 @@ constexpr uint32_t kColO = 0, kColS = 256, kColP = 384, kColQ = 448;
 constexpr uint32_t kColOStep = 128, kColSStep = 64, kColPStep = 32;
 constexpr float kGapTc = 8.0f;                   // log2-domain slack before rescaling O
 constexpr int kQuotaMinTc = 16;                  // tiles per CTA at least: fewer split pieces
+// Start-up cost of a segment in the partition, in tiles: every segment
+// occupies its tiles plus kSegCost units at its start, so a CTA that starts
+// many segments (each with its own epilogue, ~2 us) streams fewer tiles.
+constexpr int kSegCost = 6;
 constexpr int kPartFloats = 132 * kRowsTc;       // a partial: O^T [128][128], (max, sum) per half
 constexpr int kTcMinRows = 32;                   // rows per KV head from which it is picked
                                                  // (measured faster than mma.sync from 32 rows)
@@ -195,22 +201,28 @@ struct TcWalker {
         v = 0;
         nb = (pos < c1) ? tc_nblk_of(p, tc_ctx(s, p, b)) : 0;
     }
+    // segment (b, v) occupies units [first, first + nb + kSegCost); its tiles
+    // are the units from first + kSegCost on
     __device__ bool next(const TcParams& p, TcPiece& pc) {
         while (pos < c1) {
-            const long long first = base + (long long)v * nb;
-            if (nb > 0 && pos < first + nb) {
-                const long long e = min(c1, first + nb);
+            const long long units = nb > 0 ? nb + kSegCost : 0;
+            const long long first = base + (long long)v * units;
+            if (nb > 0 && pos < first + units) {
+                const long long e = min(c1, first + units);
+                const long long tile0 = first + kSegCost;
+                const long long s0 = max(pos, tile0);
+                pos = e;
+                if (e <= s0) continue;  // only start-up units in this range (pos is c1 now)
                 pc.b = b;
                 pc.v = v;
                 pc.nb = nb;
-                pc.t0 = (int)(pos - first);
-                pc.t1 = (int)(e - first);
-                pc.first = first;
-                pos = e;
+                pc.t0 = (int)(s0 - tile0);
+                pc.t1 = (int)(e - tile0);
+                pc.first = tile0;
                 return true;
             }
             if (nb > 0 && ++v < p.KC) continue;
-            base += (long long)p.KC * nb;
+            base += (long long)p.KC * units;
             v = 0;
             if (++b >= p.B) break;
             nb = tc_nblk_of(p, tc_ctx(*sm, p, b));
@@ -226,8 +238,11 @@ __device__ void tc_plan(const TcParams& p, TcSmem& sm) {
     const int lane = threadIdx.x & 31;
     const int per = (p.B + 31) / 32;
     const int lo = min(p.B, lane * per), hi = min(p.B, lo + per);
-    int local = 0;
-    for (int b = lo; b < hi; ++b) local += tc_nblk(p, b);
+    int local = 0;  // units of this lane's sequences (per virtual head)
+    for (int b = lo; b < hi; ++b) {
+        const int nb = tc_nblk(p, b);
+        local += nb > 0 ? nb + kSegCost : 0;
+    }
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -252,7 +267,8 @@ __device__ void tc_plan(const TcParams& p, TcSmem& sm) {
     if (owners != 0 && lane == __ffs(owners) - 1) {
         long long acc = (long long)p.KC * excl;
         for (int b = lo; b < hi; ++b) {
-            const long long n = (long long)p.KC * tc_nblk(p, b);
+            const int nb = tc_nblk(p, b);
+            const long long n = (long long)p.KC * (nb > 0 ? nb + kSegCost : 0);
             if (c0 < acc + n) {
                 sm.b0 = b;
                 sm.base = acc;
@@ -996,7 +1012,7 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
     if (sms < 1) return GQA_ERR_CUDA;
     // at most one CTA per SM, and no more than the tiles allow at the minimum
     // quota (upper bound: every sequence at full capacity)
-    const long long tiles_max = (long long)s.B * p.KC * s.max_blocks_per_seq;
+    const long long tiles_max = (long long)s.B * p.KC * (s.max_blocks_per_seq + kSegCost);
     const long long grid = std::min<long long>(
         sms, std::max<long long>(1, (tiles_max + kQuotaMinTc - 1) / kQuotaMinTc));
     cudaLaunchConfig_t cfg = {};
