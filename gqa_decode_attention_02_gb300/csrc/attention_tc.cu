@@ -101,6 +101,7 @@ struct TcParams {
     // times ceil(T / tpc) token blocks.
     int tpc, hpc, cpt, C, Rc, KC;
     int max_blocks, num_blocks;
+    int early;                  // GQA_FLAG_EARLY_KV: plan and stream older positions before the wait
     float scale_log2;
 };
 
@@ -308,9 +309,11 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
     TcPiece pc;
     int it = 0;
     bool aborted = false;
+    bool waited = !p.early;  // with early KV: only positions below ctx - T before the wait
     while (!aborted && wk.next(p, pc)) {
         const int kv = pc.v / p.C;
         const int32_t* table = p.block_tables + (size_t)pc.b * p.max_blocks;
+        const int newpos = tc_ctx(sm, p, pc.b) - p.T;  // the first of the T newest positions
         int win = pc.t0;  // first tile of the current window
         int ids = (win + lane < pc.t1) ? __ldg(table + win + lane) : 0;
         int nxt = (win + 32 + lane < pc.t1) ? __ldg(table + win + 32 + lane) : 0;
@@ -321,6 +324,10 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
                 nxt = (win + 32 + lane < pc.t1) ? __ldg(table + win + 32 + lane) : 0;
             }
             const int tiles = min(4, pc.t1 - blk0);
+            if (!waited && (blk0 + tiles) * 16 > newpos) {  // the stage holds a new position
+                griddep_wait();
+                waited = true;
+            }
             const int w0 = blk0 - win;
             const int id = __shfl_sync(FULLM, ids, (w0 + (lane & 3)) & 31);
             const bool bad =
@@ -383,6 +390,7 @@ __device__ __forceinline__ TcBox tc_box(const TcParams& p, int chunk) {
 __device__ void tc_qloader(const CUtensorMap* tmq, const TcParams& p, uint8_t* qbuf, TcSmem& sm) {
     if ((threadIdx.x & 31) != 0) return;
     tma_prefetch_desc(tmq);
+    if (p.early) griddep_wait();  // q follows earlier kernels
     TcWalker wk;
     wk.init(sm, p);
     TcPiece pc;
@@ -568,6 +576,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
     // this thread's 128 bytes of the staged output (row, half g; 128-byte swizzle)
     const uint32_t ostage = smem_addr(obuf) + g * kRowHalfBytes + (row >> 3) * 1024 + (row & 7) * 128;
     if (tsm == 0) tma_prefetch_desc(tmo);
+    if (p.early) griddep_wait();  // out, the workspace and the tree mask follow earlier kernels
     // sequences with an invalid length: zero outputs (CTA 0), status
     if (blockIdx.x == 0) {
         for (int b = tsm; b < p.B; b += kSoftmaxThreads) {
@@ -900,7 +909,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(smem_addr(&sm.tmem_base), kTmemCols);
-    griddep_wait();  // q, the caches, the lengths, the workspace and out follow earlier kernels
+    // q, the caches, the lengths, the workspace and out follow earlier kernels;
+    // with early KV the lengths and tables may be read now and the roles wait
+    // before their first access to anything else (the MMA issuer touches no
+    // global memory)
+    if (!p.early) griddep_wait();
     if (warp == 0) tc_plan(p, sm);
     tc_fence_before();
     __syncthreads();
@@ -1006,6 +1019,7 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
     p.KC = s.K * p.C;
     p.max_blocks = s.max_blocks_per_seq;
     p.num_blocks = s.num_blocks;
+    p.early = (s.flags & GQA_FLAG_EARLY_KV) ? 1 : 0;
     const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
     p.scale_log2 = (float)(scale * 1.4426950408889634);
     const int sms = device_sm_count();

@@ -166,6 +166,50 @@ def test_tmem_fused_append_matches_oracle(gpu, tree):
                                   vc)
 
 
+@pytest.mark.parametrize("tree", [False, True])
+def test_tmem_early_kv_after_append_is_bit_identical(gpu, tree):
+    """The fused append with PDL and early KV streaming (older positions read
+    while the append kernel may still run), eager and replayed from a CUDA
+    graph, equals the plain append followed by plain attention bit for bit."""
+    T = 5
+    ctx = (T, 17, 300, 2049, 4096)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=67, append=True)
+    m = random_trees(len(ctx), T, seed=5) if tree else None
+    kw = {} if m is None else {"tree_mask": as_i64(m).to(gpu)}
+    wp = to(w, gpu)
+    gq.kv_append(wp.k_new[0], wp.v_new[0], wp.k_cache[0], wp.v_cache[0], wp.block_tables,
+                 wp.context_lens)
+    plain = gq.verify_attention(wp.q[0], wp.k_cache[0], wp.v_cache[0], wp.block_tables,
+                                wp.context_lens, engine="tmem", **kw)
+    for use_graph in (False, True):
+        we = to(w, gpu)
+        args = (we.q[0], we.k_new[0], we.v_new[0], we.k_cache[0], we.v_cache[0],
+                we.block_tables, we.context_lens)
+        out = torch.empty_like(we.q[0])
+        if not use_graph:
+            gq.append_verify_attention(*args, out=out, engine="tmem", pdl=True, early_kv=True,
+                                       **kw)
+        else:
+            gq.append_verify_attention(*args, out=out, engine="tmem", **kw)  # outside capture
+            torch.cuda.synchronize()
+            we = to(w, gpu)  # fresh caches: the graph appends again
+            args = (we.q[0], we.k_new[0], we.v_new[0], we.k_cache[0], we.v_cache[0],
+                    we.block_tables, we.context_lens)
+            g = torch.cuda.CUDAGraph()
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                with torch.cuda.graph(g, stream=st):
+                    gq.append_verify_attention(*args, out=out, engine="tmem", pdl=True,
+                                               early_kv=True, **kw)
+            out.zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, plain), use_graph
+        # bit patterns: unused cache slots hold NaN sentinels
+        for a, b in ((we.k_cache[0], wp.k_cache[0]), (we.v_cache[0], wp.v_cache[0])):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), use_graph
+
+
 def test_engine_choice_by_shape(gpu):
     """auto = tensor memory from 32 rows per KV head, warp-level below:
     bit-identical to the forced engine in each case."""
