@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(kThreads)
                   int T, int V, int cs) {
     __shared__ unsigned long long table[kMaxT * kMaxCluster];  // used in rank 0
     __shared__ unsigned long long red[kThreads / 32][kRowsPerPass];
+    __shared__ int sdraft[kMaxT];  // the drafts, fetched while the logits stream
     griddep_launch_dependents();
     griddep_wait();  // logits and lengths follow the previous kernels
     const uint32_t rank = cluster_rank();
@@ -86,6 +87,7 @@ __global__ void __launch_bounds__(kThreads)
     const int S = (((V + cs - 1) / cs) + 3) & ~3;
     const int c_lo = min(V, (int)rank * S), c_hi = min(V, c_lo + S);
     const float* row0 = logits + (size_t)b * T * V;
+    if (rank == 0 && tid < T - 1) sdraft[tid] = __ldg(draft + (size_t)b * (T - 1) + tid);
     // Block 0's shared memory may be written only once block 0 is running:
     // arrive now, wait before the first remote store.
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -95,22 +97,33 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int i = 0; i < kRowsPerPass; ++i) key[i] = 0ull;  // below every real key
         if (kVec) {
-            // columns c_lo + 4*(tid + k*kThreads), all rows of the pass
-            for (int c = c_lo + 4 * tid; c < c_hi; c += 4 * kThreads) {
-                float4 v[kRowsPerPass];
+            // columns c_lo + 4*(tid + k*kThreads), all rows of the pass; the
+            // next column chunk's loads are issued before this one is reduced,
+            // so two chunks are in flight (one DRAM round trip for two)
+            const int step = 4 * kThreads;
+            int c = c_lo + 4 * tid;
+            float4 cur[kRowsPerPass], nxt[kRowsPerPass];
+#pragma unroll
+            for (int i = 0; i < kRowsPerPass; ++i)
+                if (t0 + i < T && c < c_hi)
+                    cur[i] = __ldg(reinterpret_cast<const float4*>(row0 + (size_t)(t0 + i) * V + c));
+            for (; c < c_hi; c += step) {
+                const int cn = c + step;
 #pragma unroll
                 for (int i = 0; i < kRowsPerPass; ++i)
-                    if (t0 + i < T)
-                        v[i] = __ldg(reinterpret_cast<const float4*>(row0 + (size_t)(t0 + i) * V + c));
+                    if (t0 + i < T && cn < c_hi)
+                        nxt[i] = __ldg(reinterpret_cast<const float4*>(row0 + (size_t)(t0 + i) * V + cn));
 #pragma unroll
                 for (int i = 0; i < kRowsPerPass; ++i) {
                     if (t0 + i < T) {
-                        key[i] = umax64(key[i], argmax_key(v[i].x, (uint32_t)c));
-                        key[i] = umax64(key[i], argmax_key(v[i].y, (uint32_t)c + 1));
-                        key[i] = umax64(key[i], argmax_key(v[i].z, (uint32_t)c + 2));
-                        key[i] = umax64(key[i], argmax_key(v[i].w, (uint32_t)c + 3));
+                        key[i] = umax64(key[i], argmax_key(cur[i].x, (uint32_t)c));
+                        key[i] = umax64(key[i], argmax_key(cur[i].y, (uint32_t)c + 1));
+                        key[i] = umax64(key[i], argmax_key(cur[i].z, (uint32_t)c + 2));
+                        key[i] = umax64(key[i], argmax_key(cur[i].w, (uint32_t)c + 3));
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < kRowsPerPass; ++i) cur[i] = nxt[i];
             }
         } else {
             for (int c = c_lo + tid; c < c_hi; c += kThreads) {
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(kThreads)
         g[t] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
     }
     int a = 0;
-    while (a < T - 1 && draft[(size_t)b * (T - 1) + a] == g[a]) ++a;
+    while (a < T - 1 && sdraft[a] == g[a]) ++a;
     accepted[b] = a;
     next_token[b] = g[a];
     if (ctx_io) {
