@@ -161,9 +161,9 @@ gqa_status gqa_kv_append(const gqa_shape *shape, const void *k_new, const void *
 
 /* Bytes of device workspace gqa_decode_attention / gqa_verify_attention need
  * for this shape on the CURRENT device: a fixed 256 KiB region of int32
- * publication flags (one per thread block, or per thread block and group of 8
- * query rows) followed by the split-context partial results of whichever
- * kernel may serve the shape (see GQA_FLAG_TENSOR_MEMORY).  Returns 0 if the shape is invalid.
+ * publication flags (one per thread block and warp of query rows) followed by
+ * the split-context partial results of whichever kernel may serve the shape
+ * (see GQA_FLAG_TENSOR_MEMORY).  Returns 0 if the shape is invalid.
  * The workspace must be zero-filled before its first use (for example with
  * gqa_workspace_clear); every call whose kernels finish without
  * GQA_ERR_TIMEOUT leaves the flag region zero-filled again (the
