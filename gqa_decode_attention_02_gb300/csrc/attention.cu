@@ -1529,15 +1529,15 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
-    // Small problems (at most ~256 tiles per SM even if every sequence were
-    // full) run one CTA per SM: fewer CTAs split fewer sequences, and the SM
-    // keeps room for the next launch on the stream, whose producer can then
-    // start streaming (programmatic dependent launch) while this one finishes.
+    // As many CTAs as fit on the GPU, also for small problems: one CTA per SM
+    // there (fewer split sequences, room for the next launch's CTAs under
+    // programmatic dependent launch) measured slower -- 24 layers of 14 MB
+    // 396 vs 371 us, the local/global layer mix 382 vs 317 us -- than
+    // shorter per-CTA chains on more CTAs.
     long long blocks_max = s.max_blocks_per_seq;  // per sequence, window included
     if (s.window > 0)
         blocks_max = std::min<long long>(blocks_max, ((long long)s.window + s.T + 14) / 16 + 1);
     const long long tiles_max = (long long)s.B * s.K * chunks * blocks_max;
-    if (tiles_max <= 256ll * sms) occ = 1;
     long long grid = (long long)sms * occ;
     grid = std::min<long long>(grid, std::max<long long>(1, (tiles_max + kQuotaMin - 1) / kQuotaMin));
     plan->grid = (int)grid;
