@@ -492,14 +492,14 @@ def run_ours(args, world, rank, local):
     attn_launch_ms = attn_ms / L
     kernel_b = attn_b + (app_b if fused else 0)  # the fused launch also does the append
     achieved = kernel_b / (attn_launch_ms * 1e-3) / 1e9
-    # which kernel served the attention calls: the library's rule for "auto"
-    # (tensor memory when a KV head has >= 32 query rows, H = 128, a cache in
-    # q's dtype and no window)
-    if args.engine != "auto":
-        engine = args.engine
+    # which kernel served the attention calls (the library's own choice; the
+    # one-byte cache always runs on the warp-level kernel)
+    if q8:
+        engine = "warp"
     else:
-        engine = "tmem" if (not q8 and w.H == 128 and w.T * (w.N // w.K) >= 32
-                            and not any(w.window(l) for l in range(L))) else "warp"
+        picks = {gq.attention_engine(w.q[l], w.k_cache[l], w.block_tables, window=w.window(l),
+                                     engine=args.engine) for l in range(L)}
+        engine = picks.pop() if len(picks) == 1 else "mixed"
     traffic = profiled_traffic(args.workload if not q8 else f"{args.workload}_{args.kv}", engine)
 
     # e2e: host buffers -> device, the captured API calls, results -> host

@@ -90,6 +90,20 @@ def kv_append_quant(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tabl
     _lib._check("gqa_kv_append_quant", rc)
 
 
+def attention_engine(q, k_cache, block_tables, window=0, engine="auto") -> str:
+    """Which kernel serves an attention call of this shape: "warp" (mma.sync)
+    or "tmem" (tcgen05 with tensor-memory accumulators); gqa_attention_engine.
+    Host logic only.  A tree mask does not change the choice."""
+    if engine not in _lib.ENGINES:
+        raise ValueError(f"engine must be one of {sorted(_lib.ENGINES)}, got {engine!r}")
+    shape = _lib.make_shape(q, k_cache, block_tables, None, window=window,
+                            flags=_lib.ENGINES[engine])
+    e = _lib.lib().gqa_attention_engine(ctypes.byref(shape))
+    if e == 0:
+        raise _lib.GqaError("gqa_attention_engine", _lib.Status.ERR_SHAPE)
+    return "warp" if e == 1 else "tmem"
+
+
 def attention_workspace_size(q, k_cache, block_tables, scale=None, window=0) -> int:
     """Workspace bytes of one attention call (a window never needs more than
     full attention of the same shape)."""

@@ -65,7 +65,7 @@ EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_verify_attention", "gqa_append_decode_attention", "gqa_append_verify_attention",
            "gqa_accept_prefix", "gqa_accept_sampled", "gqa_tree_verify_attention",
            "gqa_append_tree_verify_attention", "gqa_kv_append_quant",
-           "gqa_decode_attention_quant", "gqa_verify_attention_quant")
+           "gqa_decode_attention_quant", "gqa_verify_attention_quant", "gqa_attention_engine")
 
 
 def lib() -> ctypes.CDLL:

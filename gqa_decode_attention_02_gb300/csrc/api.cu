@@ -133,6 +133,16 @@ gqa_status gqa_kv_append_quant(const gqa_shape* shape, const void* k_new, const 
                                        static_cast<cudaStream_t>(stream));
 }
 
+int gqa_attention_engine(const gqa_shape* shape) {
+    if (check_common(shape) != GQA_OK) return 0;
+    const bool force_warp = (shape->flags & GQA_FLAG_WARP_MMA) != 0;
+    const bool force_tc = (shape->flags & GQA_FLAG_TENSOR_MEMORY) != 0;
+    if (force_warp && force_tc) return 0;
+    if (force_tc) return gqa::tc_attention_supported(*shape) ? GQA_ENGINE_TENSOR_MEMORY : 0;
+    if (force_warp) return GQA_ENGINE_WARP_MMA;
+    return gqa::tc_attention_preferred(*shape) ? GQA_ENGINE_TENSOR_MEMORY : GQA_ENGINE_WARP_MMA;
+}
+
 size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     if (check_common(shape) != GQA_OK) return 0;
     // the largest need of the kernels that may serve the shape

@@ -139,6 +139,15 @@ typedef struct {
 #define GQA_FLAG_WARP_MMA 4u
 #define GQA_FLAG_TENSOR_MEMORY 8u
 
+/* Which attention kernel serves a call with this shape and these flags (host
+ * logic only; no device work): GQA_ENGINE_WARP_MMA, GQA_ENGINE_TENSOR_MEMORY,
+ * or 0 if the shape fails the common checks or a forced kernel cannot serve
+ * it.  The call itself may still reject the shape for a reason of its own (a
+ * window with a one-byte cache, a tree mask with T > 64). */
+#define GQA_ENGINE_WARP_MMA 1
+#define GQA_ENGINE_TENSOR_MEMORY 2
+int gqa_attention_engine(const gqa_shape *shape);
+
 /* Library version (major*10000 + minor*100 + patch). */
 int gqa_version(void);
 

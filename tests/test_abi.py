@@ -89,3 +89,39 @@ def test_empty_batch_is_a_no_op(cuda_lib):
     assert rc == 0
     rc = cuda_lib.gqa_accept_prefix(0, 3, 10, None, None, None, None, None, None, None)
     assert rc == 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(T=1, N=32, K=8), 1),                 # 4 query rows per KV head: warp-level mma
+    (dict(T=5, N=64, K=8), 2),                 # 40 rows: tensor memory
+    (dict(T=4, N=64, K=8), 2),                 # 32 rows: tensor memory (threshold)
+    (dict(T=3, N=64, K=8), 1),                 # 24 rows: warp-level
+    (dict(T=5, N=64, K=8, H=64), 1),           # H = 64: only the warp-level kernel
+    (dict(T=5, N=64, K=8, window=128), 1),     # windows: only the warp-level kernel
+    (dict(T=5, N=64, K=8, flags=4), 1),        # GQA_FLAG_WARP_MMA
+    (dict(T=1, N=8, K=8, flags=8), 2),         # GQA_FLAG_TENSOR_MEMORY
+    (dict(T=1, N=8, K=8, H=64, flags=8), 0),   # forced, but not served
+    (dict(T=5, N=64, K=8, flags=12), 0),       # both forced
+    (dict(N=7), 0),                            # invalid shape
+])
+def test_attention_engine_choice(cuda_lib, kw, want):
+    """The kernel choice is host logic, checked without a GPU."""
+    assert cuda_lib.gqa_attention_engine(ctypes.byref(_shape(**kw))) == want
+
+
+def test_attention_engine_python_binding(cuda_lib):
+    import torch
+
+    import gqa_decode_attention_02_gb300 as gq
+
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    kc = torch.zeros(10, 16, 8, 128, dtype=torch.bfloat16)
+    verify = torch.zeros(2, 5, 64, 128, dtype=torch.bfloat16)   # 40 rows per KV head
+    decode = torch.zeros(2, 1, 32, 128, dtype=torch.bfloat16)   # 4 rows per KV head
+    assert gq.attention_engine(verify, kc, bt) == "tmem"
+    assert gq.attention_engine(decode, kc, bt) == "warp"
+    assert gq.attention_engine(verify, kc, bt, engine="warp") == "warp"
+    assert gq.attention_engine(verify, kc, bt, window=64) == "warp"
+    with pytest.raises(gq.GqaError):  # H = 64 cannot be forced onto tensor memory
+        gq.attention_engine(torch.zeros(2, 1, 32, 64, dtype=torch.bfloat16),
+                            torch.zeros(10, 16, 8, 64, dtype=torch.bfloat16), bt, engine="tmem")
