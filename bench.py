@@ -110,11 +110,18 @@ def measured_peak():
 
 
 def kernel_source_hash(engine="warp"):
+    """Hash of a kernel's source code with comments and whitespace removed, so
+    that a comment edit does not invalidate counters taken on the same code."""
+    import re
+
     h = hashlib.sha256()
     files = ("attention.cu", "ptx.cuh") if engine == "warp" else (
         "attention_tc.cu", "tcgen05.cuh", "ptx.cuh")
     for f in files:
-        h.update(open(os.path.join(ROOT, "gqa_decode_attention_02_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "gqa_decode_attention_02_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -37,9 +37,10 @@
 // Tensor memory (512 columns, lane = query row) holds O_0, O_1, S_0, S_1,
 // P_0, P_1 and the piece's Q.  The MMA issuer starts PV(n) as soon as P(n) is
 // written and QK^T(n + 2) right after it (S_g is free once P_g is written), so
-// the tensor pipe and both groups stay busy.  Shared memory is a ring of six
-// stages (K and V, each two 64-dim halves of 64 token rows x 128 B, 128-byte
-// swizzled): 192 KB in flight per SM.  V rows of a stage that hold no data
+// the tensor pipe and both groups stay busy.  Shared memory holds a ring of
+// four stages (K and V, each two 64-dim halves of 64 token rows x 128 B,
+// 128-byte swizzled: 128 KB), the piece's Q box (TMA, then copied into tensor
+// memory) and the output staging box (TMA store).  V rows of a stage that hold no data
 // (past the context, or unused tiles) are zeroed before the PV product: their
 // probabilities are 0, but stale bytes could be NaN.
 #include <cuda.h>
@@ -285,9 +286,9 @@ __device__ void tc_plan(const TcParams& p, TcSmem& sm) {
 }
 
 // ---------------------------------------------------------------------------
-// kProducerWarps warps share each stage: warp pw loads the blocks j of the
-// stage with j % kProducerWarps == pw (K and V, two 64-dim halves each, one
-// box per lane) and arrives on the stage's barrier with its own byte count.
+// kProducerWarps warps (one) share each stage: warp pw loads the blocks j of
+// the stage with j % kProducerWarps == pw (K and V, two 64-dim halves each,
+// one box per lane) and arrives on the stage's barrier with its own byte count.
 // Block ids are read 32 at a time (a window of eight stages, one id per lane),
 // the next window while the current one is in use.
 __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const TcParams& p,
@@ -566,7 +567,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
     using E = Elt<BF16>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int quarter = warp & 3;
-    const int g = (warp - kSoftmaxWarp0) >> 2;  // softmax group; also the half of the dims
+    const int g = (warp - kSoftmaxWarp0) >> 2;  // softmax group; also its half of the output dims
     const int row = 32 * quarter + lane;
     const int tsm = threadIdx.x - 32 * kSoftmaxWarp0;  // 0..255 among the softmax threads
     const int tg = tsm & (kGroupThreads - 1);         // 0..127 within the group
