@@ -18,8 +18,10 @@ library calls are captured once into CUDA graphs and replayed, so launch overhea
 bracketed by its own events, which gives the attention kernel's average launch
 duration live inside the timed region.
 
-Multi-GPU (torchrun): every rank runs its own replica of the workload (the path
-has no exchange step); value = all ranks' bytes / the slowest rank's time.
+Multi-GPU: every rank runs its own replica of the workload (the path has no
+exchange step); value = all ranks' bytes / the slowest rank's time.  Ranks come
+from torchrun, or, with --gpus N and no torchrun environment, from N processes
+this script spawns itself.
 """
 from __future__ import annotations
 
@@ -40,7 +42,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -56,6 +58,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the oracle check of the timed step's outputs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--accept", default="greedy", choices=["greedy", "sampled"],
                     help="acceptance step of a verify workload: greedy longest prefix over "
@@ -70,7 +74,7 @@ def parse_args():
     ap.add_argument("--unfused", action="store_true",
                     help="separate kv_append launches instead of the append fused into "
                          "the attention launch")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -243,11 +247,36 @@ def _oracle_layer_inputs(w, layer, quant=None):
     return q, kc, vc
 
 
-def oracle_sample(w, budget_s, quant=None):
-    """Time the oracle's attention (as it stands, all host threads) on a bounded
-    sample of the workload: (layer, 8-sequence chunk) units in order until the
-    budget is spent.  Returns (GB/s of algorithmic attention bytes, seconds,
-    description, threads)."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                name = line.split(":", 1)[1].strip()
+                if name and not name.isdigit():
+                    vendor = [l.split(":", 1)[1].strip() for l in out.splitlines()
+                              if l.startswith("Vendor ID")]
+                    return f"{vendor[0]} {name}" if vendor else name
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def oracle_sample(w, budget_s, quant=None, nthreads=0, inputs=None):
+    """Time the oracle's attention (as it stands; nthreads=0: all host threads)
+    on a bounded sample of the workload: (layer, 8-sequence chunk) units in
+    order until the budget is spent.  `inputs` caches each layer's oracle
+    inputs across calls.  Returns (GB/s of algorithmic attention bytes,
+    seconds, description, threads)."""
     import numpy as np
 
     import oracle
@@ -258,15 +287,19 @@ def oracle_sample(w, budget_s, quant=None):
     tables, lens = w.block_tables.cpu(), w.context_lens.cpu()
     done_bytes, spent, units, seqs = 0, 0.0, 0, 0
     q8 = {} if quant is None else {"kv_elem_bytes": 1, "row_scale_bytes": 4}
+    inputs = {} if inputs is None else inputs
     for layer in range(w.layers):
-        ins = _oracle_layer_inputs(w, layer, quant)
+        if layer not in inputs:
+            inputs.clear()
+            inputs[layer] = _oracle_layer_inputs(w, layer, quant)
+        ins = inputs[layer]
         q, kc, vc = ins[:3]
         qa = {} if quant is None else {"kv": quant[0], "k_scale": ins[3], "v_scale": ins[4]}
         for s0 in range(0, w.B, 8):
             bl = np.arange(s0, min(w.B, s0 + 8), dtype=np.int32)
             t0 = time.perf_counter()
             oracle.attention(q, kc, vc, tables, lens, w.dtype, b_list=bl, window=w.window(layer),
-                             tree_mask=w.tree_mask(), **qa)
+                             tree_mask=w.tree_mask(), nthreads=nthreads, **qa)
             spent += time.perf_counter() - t0
             done_bytes += A.attention_algorithmic_bytes(ctx[bl], w.T, w.N, w.K, w.H, 2,
                                                         window=w.window(layer), **q8)
@@ -276,9 +309,69 @@ def oracle_sample(w, budget_s, quant=None):
                 break
         if spent >= budget_s:
             break
+    thr = nthreads if nthreads > 0 else oracle.num_threads()
     desc = (f"oracle attention over {seqs} of the {w.layers * w.B} (layer, sequence) pairs "
-            f"({units} chunks of <= 8 sequences); fp64 C with OpenMP")
-    return done_bytes / spent / 1e9, spent, desc, oracle.num_threads()
+            f"({units} chunks of <= 8 sequences); fp64 C, {thr} thread(s)")
+    return done_bytes / spent / 1e9, spent, desc, thr
+
+
+def parity_sample(w, outs, quant=None, inputs=None, n_seq=8, seed=1234):
+    """Check the timed step's attention outputs against the oracle on a seeded
+    sample of sequences (the shortest and the longest always included) of the
+    first and last layer, outside the timed region.  Returns the record."""
+    import numpy as np
+
+    import oracle
+
+    ctx = w.context_lens.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    pick = {int(np.argmin(ctx)), int(np.argmax(ctx))}
+    rest = [b for b in range(w.B) if b not in pick]
+    pick |= set(int(b) for b in rng.choice(rest, size=min(len(rest), n_seq - len(pick)),
+                                            replace=False)) if rest else set()
+    bl = np.array(sorted(pick), np.int32)
+    tol = {"f16": 2e-3, "bf16": 1e-2}[w.dtype]
+    mant = 10 if w.dtype == "f16" else 7
+    worst, ok = 0.0, True
+    inputs = {} if inputs is None else inputs
+    layers = sorted({0, w.layers - 1})
+    for layer in layers:
+        if layer not in inputs:
+            inputs.clear()
+            inputs[layer] = _oracle_layer_inputs(w, layer, quant)
+        ins = inputs[layer]
+        qa = {} if quant is None else {"kv": quant[0], "k_scale": ins[3], "v_scale": ins[4]}
+        ref, err = oracle.attention(ins[0], ins[1], ins[2], w.block_tables.cpu(),
+                                    w.context_lens.cpu(), w.dtype, b_list=bl,
+                                    window=w.window(layer), tree_mask=w.tree_mask(), **qa)
+        got = outs[layer][torch_index(bl, outs[layer].device)].double().cpu().numpy()
+        d = np.abs(got - ref)
+        a = np.abs(ref)
+        half_ulp = 0.5 * np.exp2(np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))),
+                                            -14 if w.dtype == "f16" else -126) - mant)
+        ok &= bool(np.isfinite(got).all() and (d <= np.maximum(tol, half_ulp)).all()
+                   and (err == 0).all())
+        worst = max(worst, float(d.max()) if d.size else 0.0)
+    return {"max_abs_err": worst, "parity_pass": ok, "tol": tol,
+            "rule": "|gpu - oracle| <= max(tol, half an ulp of the oracle value in the dtype)",
+            "sample": f"sequences {bl.tolist()} (shortest and longest included) of layers "
+                      f"{layers}, the timed step's outputs vs the fp64 oracle"}
+
+
+def torch_index(bl, device):
+    import torch
+
+    return torch.as_tensor(bl, dtype=torch.long, device=device)
+
+
+def hold_gpu(steps: int) -> None:
+    """Keep the GPU busy (a spin kernel, before the first step's events) while
+    the host enqueues the timed steps, so that every step's events measure
+    GPU time only: a short step (tens of microseconds) would otherwise also
+    count the host's launch latency whenever the host falls behind."""
+    import torch
+
+    torch.cuda._sleep(int(2.0e9 * max(2e-3, steps * 3e-4)))  # ~cycles at ~2 GHz
 
 
 # ---- our arm -----------------------------------------------------------------------------
@@ -346,6 +439,8 @@ def run_ours(args, world, rank, local):
     sampled = has_acc and args.accept == "sampled"
     if has_acc:
         ctx_scratch = w.context_lens.clone()
+        acc_ws = torch.zeros(gq._lib.lib().gqa_accept_workspace_size(w.B, w.T),
+                             dtype=torch.uint8, device=dev)
         acc_out = torch.empty(w.B, dtype=torch.int32, device=dev)
         nxt_out = torch.empty(w.B, dtype=torch.int32, device=dev)
         V = w.logits.shape[-1]
@@ -393,7 +488,7 @@ def run_ours(args, world, rank, local):
                               accepted=acc_out, next_token=nxt_out, status=st)
         elif has_acc:
             gq.accept_prefix(w.logits, w.draft, ctx_scratch, accepted=acc_out,
-                             next_token=nxt_out, status=st)
+                             next_token=nxt_out, status=st, workspace=acc_ws)
 
     # eager warm-up (also builds the launch plans), then capture
     side = torch.cuda.Stream(device=dev)
@@ -440,6 +535,7 @@ def run_ours(args, world, rank, local):
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    hold_gpu(K)
     for i in range(K):
         refresh()
         e = evs[i]
@@ -477,6 +573,7 @@ def run_ours(args, world, rank, local):
         for _ in range(args.warmup):
             refresh()
             g_chain.replay()
+        hold_gpu(K)
         for i in range(K):
             refresh()
             ev[i][0].record()
@@ -571,11 +668,40 @@ def run_ours(args, world, rank, local):
                 rec["how"] = "as e2e but every library call made from Python each step"
                 e2e_eager = rec
 
+    # Parity of the timed step's outputs (outside the timed region): attention
+    # on a seeded sample of sequences, acceptance on the whole batch.
+    oracle_inputs = {}
+    parity = None
+    if rank == 0 and not args.no_parity:
+        import oracle
+
+        oracle.build()
+        parity = parity_sample(w, outs, quant_cpu if q8 else None, oracle_inputs)
+        if has_acc:
+            ctx0 = w.context_lens.cpu().numpy()
+            if sampled:
+                ra, rn, rc, _ = oracle.accept_sampled(
+                    sin.q.cpu().numpy(), sin.p.cpu().numpy(), sin.draft.cpu().numpy(),
+                    sin.uniforms.cpu().numpy(), ctx0)
+            else:
+                ra, rn, rc = oracle.accept_prefix(w.logits.cpu(), w.draft.cpu(), ctx0)
+            acc_ok = (np.array_equal(acc_out.cpu().numpy(), ra)
+                      and np.array_equal(nxt_out.cpu().numpy(), rn)
+                      and np.array_equal(ctx_scratch.cpu().numpy(), rc))
+            parity["accept_bit_exact"] = bool(acc_ok)
+            parity["parity_pass"] = bool(parity["parity_pass"] and acc_ok)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, spent, desc, thr = oracle_sample(w, args.cpu_seconds, quant_cpu if q8 else None)
+        v, spent, desc, thr = oracle_sample(w, args.cpu_seconds, quant_cpu if q8 else None,
+                                            inputs=oracle_inputs)
+        v1, spent1, desc1, _ = oracle_sample(w, args.cpu_seconds / 3,
+                                             quant_cpu if q8 else None, nthreads=1,
+                                             inputs=oracle_inputs)
         cpu = {"value": v, "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
-               "seconds": round(spent, 2)}
+               "seconds": round(spent, 2), "cpu_model": cpu_model(),
+               "single_thread": {"value": v1, "unit": "GB/s", "cores": 1, "sample": desc1,
+                                 "seconds": round(spent1, 2)}}
 
     ctx = w.context_lens.cpu().numpy()
     line = {
@@ -627,6 +753,7 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes_per_launch": kernel_b,
                      "avg_launch_us": round(attn_launch_ms * 1e3, 3)},
         "tree_verify": tree_rec,
+        "parity": parity,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "e2e_eager": e2e_eager,
@@ -707,9 +834,39 @@ def run_reference(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
-def main():
-    args = parse_args()
-    world, rank, local = dist_env()
+def _free_port() -> int:
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _replica(local, n, port, fn, argv):
+    """Child process of launch_replicas: the environment torchrun would give
+    rank `local` of `n` on this node, then fn(argv)."""
+    os.environ.update(RANK=str(local), LOCAL_RANK=str(local), WORLD_SIZE=str(n),
+                      LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    fn(argv)
+
+
+def launch_replicas(n: int, fn, argv) -> None:
+    """Run fn(argv) in n spawned processes, one rank each (RANK / LOCAL_RANK /
+    WORLD_SIZE / MASTER_ADDR=127.0.0.1 / MASTER_PORT set as torchrun sets
+    them); raises if any rank fails."""
+    import torch.multiprocessing as mp
+
+    mp.start_processes(_replica, args=(n, _free_port(), fn, argv), nprocs=n, join=True,
+                       start_method="spawn")
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # launched directly with --gpus N: start the N ranks here
+        launch_replicas(args.gpus, main, sys.argv[1:] if argv is None else argv)
+        return
+    world, rank, local = dist_env()  # a launcher's world size wins over --gpus
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     else:

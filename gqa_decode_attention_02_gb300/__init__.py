@@ -28,7 +28,13 @@ from ._lib import GqaError, Shape, Status, status_string  # noqa: F401
 __all__ = ["kv_append", "kv_append_quant", "decode_attention", "verify_attention",
            "decode_attention_quant", "verify_attention_quant", "append_decode_attention",
            "append_verify_attention", "accept_prefix", "accept_sampled",
-           "attention_workspace_size", "GqaError", "Status", "Shape"]
+           "attention_workspace_size", "reset_workspaces", "GqaError", "Status", "Shape"]
+
+
+def reset_workspaces():
+    """Drop the workspaces the binding caches per (device, stream); see
+    _lib.reset_workspaces."""
+    _lib.reset_workspaces()
 
 
 def _status_arg(status):
@@ -137,7 +143,7 @@ def _attention(fn_name, q, k_cache, v_cache, block_tables, context_lens, out, sc
         _lib._need(out, "out", q.dtype, 4)
     nbytes = _lib.workspace_size(shape)
     if workspace is None:
-        workspace = _lib.get_workspace(nbytes, q.device)
+        workspace = _lib.get_workspace(nbytes, q.device, stream)
     else:
         _lib._need(workspace, "workspace", torch.uint8)
     L = _lib.lib()
@@ -214,7 +220,7 @@ def _attention_quant(fn_name, q, k_cache, v_cache, k_scale, v_scale, block_table
         _lib._need(out, "out", q.dtype, 4)
     nbytes = _lib.workspace_size(shape)
     if workspace is None:
-        workspace = _lib.get_workspace(nbytes, q.device)
+        workspace = _lib.get_workspace(nbytes, q.device, stream)
     else:
         _lib._need(workspace, "workspace", torch.uint8)
     rc = getattr(_lib.lib(), fn_name)(ctypes.byref(shape), _lib._ptr(q), _lib._ptr(k_cache),
@@ -246,9 +252,12 @@ def verify_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,
-                  next_token=None, status=None, stream=None):
+                  next_token=None, status=None, stream=None, workspace=None, cluster=False):
     """gqa_accept_prefix.  target_logits fp32 [B,T,V], draft_ids int32 [B,T-1].
-    Returns (accepted [B], next_token [B]); updates context_lens in place if given."""
+    Returns (accepted [B], next_token [B]); updates context_lens in place if given.
+    workspace: uint8 device tensor of at least gqa_accept_workspace_size(B, T)
+    bytes (default: one cached per stream); cluster=True passes no workspace
+    (one thread-block cluster per sequence)."""
     _lib._need(target_logits, "target_logits", torch.float32, 3)
     B, T, V = target_logits.shape
     if T > 1:
@@ -260,11 +269,20 @@ def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,
         accepted = torch.empty(B, dtype=torch.int32, device=dev)
     if next_token is None:
         next_token = torch.empty(B, dtype=torch.int32, device=dev)
-    rc = _lib.lib().gqa_accept_prefix(B, T, V, _lib._ptr(target_logits),
-                                      _lib._ptr(draft_ids) if T > 1 else None,
-                                      _lib._ptr(accepted), _lib._ptr(next_token),
-                                      _lib._ptr(context_lens), _status_arg(status),
-                                      _lib._stream(stream))
+    L = _lib.lib()
+    if cluster:
+        workspace = None
+    elif workspace is None:
+        workspace = _lib.get_workspace(L.gqa_accept_workspace_size(B, T), dev, stream,
+                                       kind="accept")
+    else:
+        _lib._need(workspace, "workspace", torch.uint8)
+    rc = L.gqa_accept_prefix(B, T, V, _lib._ptr(target_logits),
+                             _lib._ptr(draft_ids) if T > 1 else None,
+                             _lib._ptr(accepted), _lib._ptr(next_token),
+                             _lib._ptr(context_lens), _lib._ptr(workspace),
+                             0 if workspace is None else workspace.numel(),
+                             _status_arg(status), _lib._stream(stream))
     _lib._check("gqa_accept_prefix", rc)
     return accepted, next_token
 

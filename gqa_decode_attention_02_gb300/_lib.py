@@ -63,7 +63,7 @@ ENGINES = {"auto": 0, "warp": FLAG_WARP_MMA, "tmem": FLAG_TENSOR_MEMORY}
 EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_attention_workspace_size", "gqa_workspace_clear", "gqa_decode_attention",
            "gqa_verify_attention", "gqa_append_decode_attention", "gqa_append_verify_attention",
-           "gqa_accept_prefix", "gqa_accept_sampled", "gqa_tree_verify_attention",
+           "gqa_accept_workspace_size", "gqa_accept_prefix", "gqa_accept_sampled", "gqa_tree_verify_attention",
            "gqa_append_tree_verify_attention", "gqa_kv_append_quant",
            "gqa_decode_attention_quant", "gqa_verify_attention_quant", "gqa_attention_engine")
 
@@ -108,8 +108,10 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = I
             f.argtypes = [S] + [P] * 9 + [ctypes.c_size_t, P, P]
+        L.gqa_accept_workspace_size.restype = ctypes.c_size_t
+        L.gqa_accept_workspace_size.argtypes = [I, I]
         L.gqa_accept_prefix.restype = I
-        L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, P]
+        L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, ctypes.c_size_t, P, P]
         L.gqa_accept_sampled.restype = I
         L.gqa_accept_sampled.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P]
         _lib = L
@@ -176,13 +178,32 @@ def workspace_size(shape: Shape) -> int:
     return n
 
 
-def get_workspace(nbytes: int, device) -> torch.Tensor:
-    """A zero-filled workspace of at least nbytes, kept per device and reused
-    (the library returns it zero-filled after every call)."""
+def get_workspace(nbytes: int, device, stream=None, kind: str = "attention") -> torch.Tensor:
+    """A zero-filled workspace of at least nbytes for calls on `stream`
+    (default: the current stream of `device`), cached per (device, stream,
+    kind) and reused: the library returns a workspace zero-filled after every
+    call, and calls on one stream never overlap, so one buffer per stream is
+    race-free.  The buffer is allocated and zero-filled on that stream, so the
+    caching allocator hands its memory back only in that stream's order when
+    a larger one replaces it."""
     dev = torch.device(device)
-    key = dev.index if dev.index is not None else torch.cuda.current_device()
-    ws = _ws_cache.get(key)
-    if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
-        _ws_cache[key] = ws
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    key = (dev.index, int(stream.cuda_stream), kind)
+    with _lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            with torch.cuda.stream(stream):
+                ws = torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=dev)
+            _ws_cache[key] = ws
     return ws
+
+
+def reset_workspaces() -> None:
+    """Drop every cached workspace (the next call allocates a fresh, zeroed
+    one).  Needed only after a call reported GQA_ERR_TIMEOUT through its
+    status word, which may leave a workspace's flags set."""
+    with _lock:
+        _ws_cache.clear()

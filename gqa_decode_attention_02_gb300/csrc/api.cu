@@ -254,17 +254,25 @@ gqa_status gqa_verify_attention_quant(const gqa_shape* shape, const void* q,
                            workspace_bytes, dev_status, stream, k_scale, v_scale);
 }
 
+size_t gqa_accept_workspace_size(int B, int T) { return gqa::accept_workspace_bytes(B, T); }
+
 gqa_status gqa_accept_prefix(int B, int T, int V, const float* target_logits,
                              const int32_t* draft_ids, int32_t* accepted, int32_t* next_token,
-                             int32_t* context_lens_inout, int32_t* dev_status, void* stream) {
-    if (B < 0 || T < 1 || T > 64 || V < 1 || B > 65535) return GQA_ERR_SHAPE;
+                             int32_t* context_lens_inout, void* workspace,
+                             size_t workspace_bytes, int32_t* dev_status, void* stream) {
+    if (B < 0 || T < 1 || T > 64 || V < 1) return GQA_ERR_SHAPE;
+    if (!workspace && B > 65535) return GQA_ERR_SHAPE;  // one cluster per sequence (grid y)
     if (B == 0) return GQA_OK;
     if (!target_logits || !accepted || !next_token || (T > 1 && !draft_ids))
         return GQA_ERR_NULL;
     if (!aligned16(target_logits)) return GQA_ERR_ALIGN;
     if ((long long)T * V > (1ll << 31) - 1) return GQA_ERR_SHAPE;
+    if (workspace) {
+        if (workspace_bytes < gqa::accept_workspace_bytes(B, T)) return GQA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return GQA_ERR_ALIGN;
+    }
     return gqa::launch_accept_prefix(B, T, V, target_logits, draft_ids, accepted, next_token,
-                                     context_lens_inout, dev_status,
+                                     context_lens_inout, workspace, dev_status,
                                      static_cast<cudaStream_t>(stream));
 }
 

@@ -44,11 +44,12 @@
 //    is g modulo the group count; at a segment boundary the groups' states
 //    meet in shared memory and group 0 finishes the segment.
 //  * A finished segment is written directly when the CTA owns all of it.  Of
-//    a split segment, the CTA holding the first piece meets it last in its
-//    range and merges; every other piece is the first segment of its CTA,
-//    which publishes it (partial result, then a release flag) early and goes
-//    on, so no merge ever stalls the middle of a range and no CTA waits for a
-//    piece that is still being computed behind it.
+//    a split segment, every piece's row warp publishes its partial result and
+//    takes a ticket (an acq_rel atomicAdd on the segment's counter); the warp
+//    that draws the last ticket folds all pieces in piece order (the same
+//    arithmetic whichever CTA it runs in: a deterministic result), stores the
+//    rows and resets the counter.  No CTA ever waits for another, so the
+//    result does not depend on which CTAs are resident at the same time.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -81,7 +82,7 @@ struct AttnParams {
     const int32_t* block_tables;
     const int32_t* context_lens;
     float* partials;
-    int32_t* flags;  // one per (CTA, row warp): piece published
+    int32_t* flags;  // tickets: per (CTA holding a split segment's first piece, row warp)
     int32_t* status;
     int B, T, N, K, G, R, nt;  // nt: row warps per consumer group
     // Row chunks: the R = T*G query rows of a KV head are split into C chunks
@@ -168,28 +169,17 @@ __device__ void zero_sequence(const AttnParams& p, int b) {
     for (size_t i = 0; i < n16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
 }
 
-// Publication flags of split pieces (GPU scope): the publisher's release
-// store follows its partial-result stores (made visible to it by __syncwarp);
-// the merger's acquire load precedes its reads of them.
-__device__ __forceinline__ void st_release_gpu(int32_t* f, int v) {
-    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t* f) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+// Tickets of split segments (GPU scope): every piece's warp stores its
+// partial result, then (after __syncwarp, which orders its lanes' stores
+// before lane 0) takes a ticket with an acq_rel atomic; the warp that draws
+// the last ticket has acquired every earlier piece's stores.
+__device__ __forceinline__ unsigned ticket_acq_rel(int32_t* t) {
+    unsigned v;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(v)
+                 : "l"(t)
+                 : "memory");
     return v;
-}
-// Bounded wait for a flag.  Every CTA of the grid is resident (the grid is
-// sized to one wave) and a publisher never waits for its merger, so the flag
-// is set in bounded time; the limit only guards against an aborted CTA.
-__device__ __forceinline__ bool wait_flag(const int32_t* f) {
-    if (ld_acquire_gpu(f)) return true;
-    const unsigned long long t0 = global_ns();
-    while (true) {
-        __nanosleep(100);
-        if (ld_acquire_gpu(f)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
 }
 
 // Barriers of one CTA.
@@ -1040,12 +1030,18 @@ struct Consumer {
         }
     }
 
-    // Partial-result section of tile u in CTA `cta`.  One per CTA is enough:
-    // the only segment a CTA hands to another for merging is its first.
-    __device__ float* section(int cta, int u) const {
-        return p.partials + (((size_t)cta * p.nt + w) * NW + u) * C::kSectionFloats;
+    // Partial-result section of tile u in CTA `cta`, slot 0 for the CTA's
+    // first segment (a piece other than a segment's first) and slot 1 for its
+    // last (the first piece of a segment): a CTA holds at most one of each.
+    __device__ float* section(int cta, int slot, int u) const {
+        return p.partials +
+               ((((size_t)cta * 2 + slot) * p.nt + w) * NW + u) * C::kSectionFloats;
     }
-    __device__ int32_t* flag(int cta) const { return p.flags + (size_t)cta * p.nt + w; }
+    // Ticket of a split segment for this row warp, indexed by the CTA that
+    // holds the segment's first piece.
+    __device__ int32_t* ticket(int first_cta) const {
+        return p.flags + (size_t)first_cta * p.nt + w;
+    }
 
     // Row sums: each lane holds the sum over its own tokens; add up the 8 lanes
     // that share a row pair.
@@ -1126,11 +1122,11 @@ struct Consumer {
     }
 
     // Finish the segment (row sums already reduced).  A split segment's pieces
-    // sit in CTAs first..last.  CTA `first` meets the segment last in its own
-    // range, so it is the merger; every other piece is the first segment of
-    // its CTA, which publishes it (partial result, then a release flag) and
-    // goes on.  The merger folds the published pieces into its own in CTA
-    // order (deterministic) and clears their flags for the next call.
+    // sit in CTAs first..last.  Each piece's warp publishes its partial (max,
+    // sum, accumulator, invalid-block flag) and takes a ticket; the warp that
+    // draws the last one folds the pieces in CTA order -- starting from the
+    // first piece's state, exactly as stored -- stores the rows and resets the
+    // ticket for the next call.  Nothing waits.
     __device__ void finalize() {
         const int first = cstart / cquota;
         const int last = (cstart + cnblk - 1) / cquota;
@@ -1140,44 +1136,55 @@ struct Consumer {
             for (int u = 0; u < NW; ++u) store(u, l0[u], l1[u], bad);
             return;
         }
-        if (me != first) {
-#pragma unroll
-            for (int u = 0; u < NW; ++u) {
-                float* sec = section(me, u);
-                if (g == 0) {
-                    sec[2 * q4] = m0[u];
-                    sec[2 * q4 + 1] = m1[u];
-                    sec[8 + 2 * q4] = l0[u];
-                    sec[8 + 2 * q4 + 1] = l1[u];
-                }
-                if (lane == 0) sec[16] = bad ? 1.f : 0.f;
-                float4* a4 = reinterpret_cast<float4*>(sec + C::kHeaderFloats) + lane * C::kSteps;
-#pragma unroll
-                for (int mt = 0; mt < C::kSteps; ++mt)
-                    a4[mt] = make_float4(acc[u][mt][0], acc[u][mt][1], acc[u][mt][2],
-                                         acc[u][mt][3]);
-            }
-            __syncwarp();  // orders the lanes' stores before lane 0's release
-            if (lane == 0) st_release_gpu(flag(me), 1);
-            return;
-        }
-        // ---- merger: wait for every published piece, then fold them in, in
-        //      batches whose loads are all in flight before any is used -----
-        int ok = 1;
-        if (lane == 0)
-            for (int c = first + 1; c <= last; ++c) ok &= wait_flag(flag(c)) ? 1 : 0;
-        ok = __shfl_sync(FULL, ok, 0);
-        if (!ok) {  // a piece never arrived (cannot happen unless a CTA aborted)
-            if (lane == 0) report(p.status, GQA_ERR_TIMEOUT);
-#pragma unroll
-            for (int u = 0; u < NW; ++u) store(u, 0.f, 0.f, true);
-            return;
-        }
-        __syncwarp();  // orders lane 0's acquires before every lane's loads
-        constexpr int kBatch = (H == 64) ? 4 : 2;
-        bool any_bad = bad;
+        auto slot_of = [&](int c) { return c == first ? 1 : 0; };
 #pragma unroll
         for (int u = 0; u < NW; ++u) {
+            float* sec = section(me, slot_of(me), u);
+            if (g == 0) {
+                sec[2 * q4] = m0[u];
+                sec[2 * q4 + 1] = m1[u];
+                sec[8 + 2 * q4] = l0[u];
+                sec[8 + 2 * q4 + 1] = l1[u];
+            }
+            if (lane == 0) sec[16] = bad ? 1.f : 0.f;
+            float4* a4 = reinterpret_cast<float4*>(sec + C::kHeaderFloats) + lane * C::kSteps;
+#pragma unroll
+            for (int mt = 0; mt < C::kSteps; ++mt)
+                a4[mt] = make_float4(acc[u][mt][0], acc[u][mt][1], acc[u][mt][2], acc[u][mt][3]);
+        }
+        __syncwarp();  // orders the lanes' stores before lane 0's ticket
+        unsigned drawn = 0;
+        if (lane == 0) drawn = ticket_acq_rel(ticket(first));
+        drawn = __shfl_sync(FULL, drawn, 0);
+        if (drawn != (unsigned)(last - first)) return;  // another piece's warp merges
+        __syncwarp();  // orders lane 0's acquire before every lane's loads
+        // ---- the last piece to finish: fold all pieces in CTA order, in
+        //      batches whose loads are all in flight before any is used -----
+        constexpr int kBatch = (H == 64) ? 4 : 2;
+        bool any_bad = false;
+#pragma unroll
+        for (int u = 0; u < NW; ++u) {
+            // start from the first piece's state (registers if this is it)
+            if (me != first) {
+                const float* sc = section(first, 1, u);
+                m0[u] = __ldcg(sc + 2 * q4);
+                m1[u] = __ldcg(sc + 2 * q4 + 1);
+                l0[u] = __ldcg(sc + 8 + 2 * q4);
+                l1[u] = __ldcg(sc + 8 + 2 * q4 + 1);
+                any_bad |= __ldcg(sc + 16) != 0.f;
+                const float4* b4 =
+                    reinterpret_cast<const float4*>(sc + C::kHeaderFloats) + lane * C::kSteps;
+#pragma unroll
+                for (int mt = 0; mt < C::kSteps; ++mt) {
+                    const float4 v = __ldcg(b4 + mt);
+                    acc[u][mt][0] = v.x;
+                    acc[u][mt][1] = v.y;
+                    acc[u][mt][2] = v.z;
+                    acc[u][mt][3] = v.w;
+                }
+            } else {
+                any_bad |= bad;
+            }
             for (int c0 = first + 1; c0 <= last; c0 += kBatch) {
                 float mc[kBatch][2], lc[kBatch][2], fl[kBatch];
                 float4 v[kBatch][C::kSteps];
@@ -1185,7 +1192,7 @@ struct Consumer {
                 // and then gives it no weight).
 #pragma unroll
                 for (int j = 0; j < kBatch; ++j) {
-                    const float* sc = section(min(c0 + j, last), u);
+                    const float* sc = section(min(c0 + j, last), 0, u);
                     mc[j][0] = __ldcg(sc + 2 * q4);
                     mc[j][1] = __ldcg(sc + 2 * q4 + 1);
                     lc[j][0] = __ldcg(sc + 8 + 2 * q4);
@@ -1204,8 +1211,7 @@ struct Consumer {
                 }
             }
         }
-        if (lane == 0)
-            for (int c = first + 1; c <= last; ++c) *flag(c) = 0;  // ready for the next call
+        if (lane == 0) *ticket(first) = 0;  // ready for the next call
 #pragma unroll
         for (int u = 0; u < NW; ++u) store(u, l0[u], l1[u], any_bad);
     }
@@ -1550,13 +1556,13 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     plan->general = general;
     plan->chunks = chunks;
     plan->rows_per_chunk = rows_per_chunk;
-    // The publication flags live in a fixed region at the start of every
-    // workspace, whatever the shape, and partial results always start after
-    // it: partial data of one call can then never sit where a later call of
-    // another shape expects zeroed flags.
+    // The tickets of split segments live in a fixed region at the start of
+    // every workspace, whatever the shape, and partial results always start
+    // after it: partial data of one call can then never sit where a later
+    // call of another shape expects zeroed tickets.
     if (grid * nt > kMaxFlags) return GQA_ERR_SHAPE;
     plan->flags_bytes = (size_t)kMaxFlags * 4;
-    plan->partial_floats_per_cta = section_floats(s.H) * nt * nw;
+    plan->partial_floats_per_cta = 2 * section_floats(s.H) * nt * nw;  // two slots
     plan->workspace = plan->flags_bytes + (size_t)grid * plan->partial_floats_per_cta * 4;
     return GQA_OK;
 }

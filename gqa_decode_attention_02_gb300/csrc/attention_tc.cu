@@ -16,12 +16,13 @@
 // a segment being its tiles plus a few units for its start-up, so every SM
 // streams about the same bytes and pays about the same per-segment costs
 // however ragged the batch.  A
-// segment cut by range boundaries is split into pieces: every piece but the
-// first starts its CTA's range and publishes its partial result (O
-// unnormalized, running max, sum) in the workspace behind a release flag; the
-// first piece ends its CTA's range and folds the others into its own in piece
-// order (a deterministic result) with log-sum-exp weights -- the context split
-// of FlashDecoding named in §"PagedAttention".
+// segment cut by range boundaries is split into pieces: every piece's softmax
+// warps publish their partial result (O unnormalized, running max, sum) in the
+// workspace and take a ticket (an acq_rel atomicAdd); the warp that draws the
+// last ticket folds the pieces in piece order (the same arithmetic in
+// whichever CTA it runs: a deterministic result) with log-sum-exp weights --
+// the context split of FlashDecoding named in §"PagedAttention" -- and stores
+// its rows.  No CTA waits for another.
 //
 // One CTA: warp 0 MMA issuer and tensor-memory owner, warps 1..2 producers
 // (TMA), warps 3..10 softmax in two groups of four warps (one thread per query
@@ -93,8 +94,9 @@ struct TcParams {
     const int32_t* context_lens;
     const uint64_t* tree_mask;  // nullptr: causal chain among the new tokens
     int32_t* status;
-    int32_t* flags;             // per CTA: pieces of the split segment it starts, done
-    float* partials;            // [grid][kPartFloats]: the continuation piece of each CTA
+    int32_t* flags;             // tickets: per (CTA holding a first piece, softmax warp)
+    float* partials;            // [grid][2][kPartFloats]: per CTA, slot 0 its first
+                                // segment (a later piece), slot 1 its last (a first piece)
     int B, T, N, K, G;
     // A row chunk (virtual head) is a box of tpc new tokens x hpc query heads of
     // one KV head, Rc = tpc * hpc <= 128 rows (row = token-in-box * hpc +
@@ -146,24 +148,16 @@ __device__ __forceinline__ void tc_abort(TcSmem& sm, const TcParams& p) {
     sm.abort_flag = 1;
 }
 
-// Publication flags of split pieces (GPU scope): release store after the
-// partial's stores, acquire load before reading it; a bounded wait.
-__device__ __forceinline__ void flag_release(int32_t* f, int v) {
-    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
-}
-__device__ __forceinline__ int flag_acquire(const int32_t* f) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+// Ticket of a split segment (GPU scope): a warp stores its partial, then
+// (after __syncwarp) lane 0 takes a ticket with an acq_rel atomic; the warp
+// that draws the last ticket has acquired every earlier piece's stores.
+__device__ __forceinline__ unsigned tc_ticket(int32_t* t) {
+    unsigned v;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(v)
+                 : "l"(t)
+                 : "memory");
     return v;
-}
-__device__ __forceinline__ bool flag_wait(const int32_t* f) {
-    if (flag_acquire(f)) return true;
-    const unsigned long long t0 = global_ns();
-    while (true) {
-        __nanosleep(100);
-        if (flag_acquire(f)) return true;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
 }
 
 // Waits until stage n has landed.
@@ -793,41 +787,45 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             continue;
         }
         // ---- a piece of a split segment -------------------------------------------
-        // Every piece but the segment's first is the first piece of its CTA's
-        // range: it publishes its rows (partial O, max, sum -- each warp its 32
-        // rows x 64 dims) and goes on, each warp ending with a release store of
-        // its own flag.  The first piece ends its CTA's range: it waits for the
-        // flags of the other pieces' warps in the same position (bounded; a
-        // publisher never waits for anything of the merger, and the grid is one
-        // wave), folds their partials into its own registers in CTA order
-        // (deterministic), clears the flags for the next call and stores.
+        // Each warp publishes its rows of the piece (partial O over its 64
+        // dims, max, sum; slot 1 for the segment's first piece, which ends its
+        // CTA's range, slot 0 for the others, which start theirs) and takes a
+        // ticket.  The warp that draws the last one folds the pieces' partials
+        // in CTA order, starting from the first piece's, and stores its 32
+        // rows x 64 dims with plain stores; it resets the ticket for the next
+        // call.  No warp waits for another CTA.
         const int me = blockIdx.x;
-        const int wi = warp - kSoftmaxWarp0;  // this warp's flag among the CTA's eight
-        if (pc.t0 != 0) {
-            if (active) {
-                float* part = p.partials + (size_t)me * kPartFloats;
+        const int wi = warp - kSoftmaxWarp0;  // this warp's ticket among the CTA's eight
+        const int npieces = last_cta - first_cta + 1;
+        if (active) {
+            float* part = p.partials + ((size_t)me * 2 + (me == first_cta ? 1 : 0)) * kPartFloats;
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+                __stcg(part + (64 * g + k) * kRowsTc + row, __uint_as_float(o[k]));
+            __stcg(part + (128 + 2 * g) * kRowsTc + row, M);
+            __stcg(part + (129 + 2 * g) * kRowsTc + row, bad ? -1.f : lt);  // -1: a bad block
+        }
+        __syncwarp();  // the lanes' stores before lane 0's ticket
+        unsigned drawn = 0;
+        if (lane == 0) drawn = tc_ticket(p.flags + 8 * first_cta + wi);
+        drawn = __shfl_sync(FULLM, drawn, 0);
+        if (drawn != (unsigned)(npieces - 1)) continue;  // another piece's warp merges
+        __syncwarp();  // lane 0's acquire before every lane's reads of the partials
+        if (active) {
+            // online fold over the pieces in CTA order: running max MM, sum L
+            // (< 0 marks a piece with an invalid block), unnormalized values o
+            float MM = M, L = bad ? -1.f : lt;
+            if (me != first_cta) {  // start from the first piece's stored state
+                const float* pf = p.partials + ((size_t)first_cta * 2 + 1) * kPartFloats;
+                MM = __ldcg(pf + (128 + 2 * g) * kRowsTc + row);
+                L = __ldcg(pf + (129 + 2 * g) * kRowsTc + row);
 #pragma unroll
                 for (int k = 0; k < 64; ++k)
-                    __stcg(part + (64 * g + k) * kRowsTc + row, __uint_as_float(o[k]));
-                __stcg(part + (128 + 2 * g) * kRowsTc + row, M);
-                __stcg(part + (129 + 2 * g) * kRowsTc + row, bad ? -1.f : lt);  // -1: a bad block
+                    o[k] = __float_as_uint(__ldcg(pf + (64 * g + k) * kRowsTc + row));
             }
-            __syncwarp();  // the lanes' stores before lane 0's release
-            if (lane == 0) flag_release(p.flags + 8 * me + wi, 1);
-            continue;
-        }
-        bool got = true;
-        if (lane == 0)
-            for (int c = first_cta + 1; c <= last_cta; ++c) got &= flag_wait(p.flags + 8 * c + wi);
-        got = __shfl_sync(FULLM, got ? 1 : 0, 0) != 0;
-        __syncwarp();  // lane 0's acquire loads before every lane's reads of the partials
-        if (!got) tc_abort(sm, p);  // a piece never arrived (only after an aborted CTA)
-        if (active && got) {
-            // online fold: running max MM, sum L, unnormalized values o
-            float MM = M, L = bad ? -1.f : lt;
-            bool any_bad = bad;
+            bool any_bad = L < 0.f;
             for (int c = first_cta + 1; c <= last_cta; ++c) {
-                const float* pp_ = p.partials + (size_t)c * kPartFloats;
+                const float* pp_ = p.partials + (size_t)c * 2 * kPartFloats;  // slot 0
                 const float mc = __ldcg(pp_ + (128 + 2 * g) * kRowsTc + row);
                 const float lc = __ldcg(pp_ + (129 + 2 * g) * kRowsTc + row);
                 float v[64];
@@ -845,29 +843,24 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
                 MM = mn;
             }
             const bool zero = any_bad || !(L > 0.f);
-            if (zero) {
+            // this row's 64 dims of half g, in q's dtype
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<uint16_t*>(p.out) +
+                (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128 + 64 * g);
+            const float inv = zero ? 0.f : 1.f / L;
 #pragma unroll
-                for (int k = 0; k < 64; ++k) o[k] = 0u;
+            for (int j = 0; j < 8; ++j) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w4[e] = zero ? 0u
+                                 : E::pack(__uint_as_float(o[8 * j + 2 * e]) * inv,
+                                           __uint_as_float(o[8 * j + 2 * e + 1]) * inv);
+                dst[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            lt = zero ? 0.f : L;
         }
         __syncwarp();
-        if (lane == 0)
-            for (int c = first_cta + 1; c <= last_cta; ++c) p.flags[8 * c + wi] = 0;  // next call
-        if (!got) {
-#pragma unroll
-            for (int k = 0; k < 64; ++k) o[k] = 0u;
-            lt = 0.f;
-        }
-        if (tsm == 0) bulk_wait_read();  // the previous box has left the staging buffer
-        ok = softmax_bar(sm, ap);
-        if (active) stage_row(o, lt > 0.f ? 1.f / lt : 0.f);
-        ok = __all_sync(FULLM, ok && softmax_bar(sm, ap) && got);
-        if (!ok) {
-            tc_abort(sm, p);
-            break;
-        }
-        store_box(b, kv, box);
+        if (lane == 0) p.flags[8 * first_cta + wi] = 0;  // ready for the next call
     }
     if (tsm == 0) bulk_wait_read();  // the staging buffer is read before the CTA leaves
 }
@@ -953,7 +946,7 @@ size_t tc_workspace_bytes(const gqa_shape& s, size_t flags_bytes) {
     if (!tc_attention_supported(s)) return 0;
     const int sms = device_sm_count();
     if (sms < 1) return 0;
-    return flags_bytes + (size_t)sms * kPartFloats * sizeof(float);
+    return flags_bytes + (size_t)sms * 2 * kPartFloats * sizeof(float);  // two slots per CTA
 }
 
 gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_cache,

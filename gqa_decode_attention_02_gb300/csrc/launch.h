@@ -47,10 +47,13 @@ gqa_status launch_kv_append(const gqa_shape& s, const void* k_new, const void* v
                             const int32_t* context_lens, int32_t* dev_status,
                             cudaStream_t stream);
 
+// workspace == nullptr: one thread-block cluster per sequence; otherwise many
+// blocks per sequence whose keys meet in the workspace (accept_workspace_bytes).
+size_t accept_workspace_bytes(int B, int T);
 gqa_status launch_accept_prefix(int B, int T, int V, const float* logits,
                                 const int32_t* draft, int32_t* accepted,
-                                int32_t* next_token, int32_t* ctx_io, int32_t* dev_status,
-                                cudaStream_t stream);
+                                int32_t* next_token, int32_t* ctx_io, void* workspace,
+                                int32_t* dev_status, cudaStream_t stream);
 
 gqa_status launch_accept_sampled(int B, int T, int V, const float* q, const float* p,
                                  const int32_t* draft, const double* u, int32_t* accepted,

@@ -7,8 +7,8 @@
 // latency-critical decode path, where cudaMalloc / cudaFree can synchronise
 // the device; or a plain C caller with no allocator of its own at hand.  For
 // them gqa_decode_attention_noalloc runs the same split-context decode kernel
-// as gqa_decode_attention, but with its scratch (publication flags and partial
-// results) in a file-scope device array of fixed size, so the caller passes
+// as gqa_decode_attention, but with its scratch (split-segment tickets and
+// partial results) in a file-scope device array of fixed size, so the caller passes
 // only inputs and outputs.
 //
 // The array costs every GPU that loads the library kScratchBytes of device
@@ -58,7 +58,6 @@ extern "C" gqa_status gqa_decode_attention_noalloc(const gqa_shape* shape, const
                                                    int32_t* dev_status, void* stream) {
     if (!shape) return GQA_ERR_NULL;
     if (shape->T != 1) return GQA_ERR_SHAPE;  // decode: one new token per sequence
-    if (gqa_attention_workspace_size(shape) == 0) return GQA_ERR_SHAPE;
     gqa::AttnPlan plan;
     const gqa_status st = gqa::attention_plan(*shape, false, &plan);
     if (st != GQA_OK) return st;
@@ -72,7 +71,8 @@ extern "C" gqa_status gqa_decode_attention_noalloc(const gqa_shape* shape, const
     void* scratch = nullptr;
     const gqa_status ss = scratch_on_current_device(&scratch);
     if (ss != GQA_OK) return ss;
-    // The publication flags must read zero when the kernel starts.
+    // The tickets must read zero when the kernel starts.  A call that ended
+    // normally left them zero, but one that timed out may not have.
     if (cudaMemsetAsync(scratch, 0, plan.flags_bytes, static_cast<cudaStream_t>(stream)) !=
         cudaSuccess)
         return GQA_ERR_CUDA;

@@ -221,14 +221,18 @@ gqa_status gqa_decode_attention(const gqa_shape *shape, const void *q,
  *  - Shapes whose scratch exceeds 8 MiB are rejected with GQA_ERR_WORKSPACE.
  *    The scratch is what the kernel that serves the call needs: the
  *    warp-level kernel's workspace, or the tensor-memory kernel's where the
- *    shape picks that one (T * N / K >= 32, H = 128; its split-context
- *    partials take ~133 KB per SM, more than 8 MiB on a full GPU, so such
- *    shapes are rejected).  gqa_attention_workspace_size may report more: it
- *    also covers a kernel forced by a flag.
+ *    shape picks that one (T * N / K >= 32, H = 128).  The latter is 256 KiB
+ *    plus 132 KiB of split-context partials per SM, so it exceeds 8 MiB, and
+ *    such shapes are rejected, on every GPU with more than 60 SMs (GB300 has
+ *    152).  gqa_attention_workspace_size may report more: it also covers a
+ *    kernel forced by a flag.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
  *  - Each call first clears, on `stream`, the part of the array that must
  *    start at zero (one cudaMemsetAsync; nothing is allocated or freed).
+ *    That memset sits between the previous kernel on the stream and the
+ *    attention launch, so GQA_FLAG_PDL / GQA_FLAG_EARLY_KV give no launch
+ *    overlap through this entry point (the results are the same).
  *  - All calls share the one array: calls whose work overlaps on the GPU (on
  *    different streams or from different host threads) race on it. */
 gqa_status gqa_decode_attention_noalloc(const gqa_shape *shape, const void *q,
@@ -360,10 +364,23 @@ gqa_status gqa_verify_attention_quant(const gqa_shape *shape, const void *q,
  *                                    rejected drafts, on the device)
  * Requires B >= 0, 1 <= T <= 64, V >= 1.  target_logits must be 16-byte
  * aligned.  Device errors: a context length that would drop below zero is
- * left unchanged (GQA_ERR_CONTEXT). */
+ * left unchanged (GQA_ERR_CONTEXT).
+ * workspace: device memory of at least gqa_accept_workspace_size(B, T) bytes,
+ * 16-byte aligned and zero-filled before its first use; every call leaves it
+ * zero-filled again, so one buffer serves later calls of any size that fits.
+ * With it, each sequence's columns are split over many thread blocks (about
+ * four per SM over the batch) that store their per-row maxima in the
+ * workspace; the block that finishes last (an atomic ticket) combines them
+ * and walks the drafts.  No block waits for another.  Calls that share a workspace must not
+ * overlap on the GPU.  workspace == NULL (workspace_bytes ignored) runs one
+ * thread-block cluster of up to 8 blocks per sequence instead (B <= 65535),
+ * which needs no scratch but fills the GPU only for large batches.  Both give
+ * the same results. */
+size_t gqa_accept_workspace_size(int B, int T);
 gqa_status gqa_accept_prefix(int B, int T, int V, const float *target_logits,
                              const int32_t *draft_ids, int32_t *accepted,
                              int32_t *next_token, int32_t *context_lens_inout,
+                             void *workspace, size_t workspace_bytes,
                              int32_t *dev_status, void *stream);
 
 /* Stochastic acceptance (speculative sampling).  CS336 lecture 10

@@ -76,10 +76,25 @@ def test_validation_rejects_null_and_misaligned(cuda_lib):
     assert rc == 2  # decode is T == 1 only
     rc = cuda_lib.gqa_kv_append(ctypes.byref(s), None, fake, fake, fake, fake, fake, None, None)
     assert rc == 1
-    rc = cuda_lib.gqa_accept_prefix(2, 0, 10, fake, fake, fake, fake, None, None, None)
+    rc = cuda_lib.gqa_accept_prefix(2, 0, 10, fake, fake, fake, fake, None, None, 0, None,
+                                    None)
     assert rc == 2
-    rc = cuda_lib.gqa_accept_prefix(2, 3, 10, odd, fake, fake, fake, None, None, None)
+    rc = cuda_lib.gqa_accept_prefix(2, 3, 10, odd, fake, fake, fake, None, None, 0, None, None)
     assert rc == 4
+    # a workspace smaller than the size query, or misaligned
+    need = cuda_lib.gqa_accept_workspace_size(2, 3)
+    assert need >= 8 * 2 * 3 + 4 * 2 and need % 16 == 0
+    rc = cuda_lib.gqa_accept_prefix(2, 3, 10, fake, fake, fake, fake, None, fake, need - 1,
+                                    None, None)
+    assert rc == 5
+    rc = cuda_lib.gqa_accept_prefix(2, 3, 10, fake, fake, fake, fake, None, odd, need, None,
+                                    None)
+    assert rc == 4
+    assert cuda_lib.gqa_accept_workspace_size(2, 65) == 0  # T > 64
+    # more sequences than one cluster per sequence can take need the workspace
+    rc = cuda_lib.gqa_accept_prefix(70000, 1, 10, fake, None, fake, fake, None, None, 0, None,
+                                    None)
+    assert rc == 2
 
 
 def test_empty_batch_is_a_no_op(cuda_lib):
@@ -87,7 +102,8 @@ def test_empty_batch_is_a_no_op(cuda_lib):
     rc = cuda_lib.gqa_kv_append(ctypes.byref(s), None, None, None, None, None, None, None,
                                 None)
     assert rc == 0
-    rc = cuda_lib.gqa_accept_prefix(0, 3, 10, None, None, None, None, None, None, None)
+    rc = cuda_lib.gqa_accept_prefix(0, 3, 10, None, None, None, None, None, None, 0, None,
+                                    None)
     assert rc == 0
 
 

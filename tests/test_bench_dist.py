@@ -1,6 +1,7 @@
 """The bench's multi-rank path on CPU: two gloo ranks run replicas with
 different step times; the whole-job figure uses the slowest rank's time and
-all ranks' bytes.  The reference arm prints from rank 0 only."""
+all ranks' bytes.  The reference arm prints from rank 0 only.  --gpus N
+without a torchrun environment spawns the N ranks itself."""
 import os
 import socket
 import subprocess
@@ -64,3 +65,31 @@ def test_reference_arm_prints_only_on_rank_zero():
                        text=True, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def _rank_job(argv):
+    """A replica as bench.launch_replicas starts it: joins the gloo group from
+    the environment it was given and reports its rank's view."""
+    import torch.distributed as dist
+
+    out_dir = argv[0]
+    dist.init_process_group("gloo")
+    rank, world = dist.get_rank(), dist.get_world_size()
+    ms, gbs = __import__("bench").combine_ranks([3.0, 7.0][rank], 1_000_000, world,
+                                                torch.device("cpu"))
+    with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+        f.write(f"{os.environ['RANK']} {os.environ['LOCAL_RANK']} {os.environ['WORLD_SIZE']} "
+                f"{os.environ['MASTER_ADDR']} {ms} {gbs}")
+    dist.destroy_process_group()
+
+
+def test_launch_replicas_spawns_ranks_with_torchrun_environment(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    bench.launch_replicas(2, _rank_job, [str(tmp_path)])
+    for r in (0, 1):
+        rank, local, world, addr, ms, gbs = open(tmp_path / f"rank{r}.txt").read().split()
+        assert (rank, local, world, addr) == (str(r), str(r), "2", "127.0.0.1")
+        assert float(ms) == 7.0
+        assert abs(float(gbs) - 2 * 1_000_000 / 7e-3 / 1e9) < 1e-9
