@@ -17,10 +17,11 @@
 //
 // Structure of one CTA (persistent; grid = SMs x resident CTAs):
 //  * Work order.  The tiles of the whole batch are laid out as segments
-//    (b, k) in b-major order, each segment being ceil(ctx_b/16) tiles of 16
-//    tokens (one cache block of one KV head).  CTA c takes the contiguous
-//    range [c*quota, (c+1)*quota) of that order, so every CTA streams the same
-//    number of bytes however ragged the context lengths are.  A segment cut by
+//    (b, k) in b-major order, each segment being a few start-up units and
+//    then ceil(ctx_b/16) tiles of 16 tokens (one cache block of one KV head).
+//    CTA c takes the contiguous range [c*quota, (c+1)*quota) of those units,
+//    so every CTA streams about the same bytes and pays about the same
+//    per-segment costs however ragged the context lengths are.  A segment cut by
 //    a range boundary is finished by merging its pieces with log-sum-exp
 //    weights -- the context split of FlashDecoding (named in §"PagedAttention"),
 //    balanced over the whole batch.  Every CTA derives the plan from
@@ -72,7 +73,12 @@ constexpr int kMaxThreads = 32 * (kGroups * kMaxRowWarps + 1);
 constexpr int kEnd = 1, kBad = 2;
 constexpr int kTilesPerStage = 4;          // cache blocks per pipeline stage (2-byte cache)
 constexpr int kMaxTilesPerStage = 8;       // ... and over one-byte codes
-constexpr int kQuotaMin = 4 * kTilesPerStage;  // tiles per CTA at least: fewer split pieces
+constexpr int kQuotaMin = 4 * kTilesPerStage;  // units per CTA at least: fewer split pieces
+// Start-up cost of a segment in the work partition, in tiles: a segment
+// occupies kSegUnits units and then its tiles, so a CTA that starts many
+// (short) segments -- each with its q rows, new rows and epilogue -- streams
+// fewer tiles.
+constexpr int kSegUnits = 6;
 constexpr float kRescaleGap = 8.0f;        // log2-domain slack before rescaling
 constexpr long long kMaxFlags = 65536;     // CTAs * row warps per launch
 
@@ -113,7 +119,7 @@ struct AttnParams {
 template <int NT>
 struct StageMetaT {
     int b, k, blk_i, ntiles;  // segment (b, k); its tiles blk_i .. blk_i+ntiles-1
-    int ctx, seg_start, nblk, quota;
+    int ctx, seg_start, nblk, quota;  // seg_start: partition unit of the segment's first tile
     int cta_start, flags, pad0, pad1;
     int blk[NT];  // physical block of each tile
 };
@@ -160,6 +166,8 @@ __device__ __forceinline__ int seq_blocks(int ctx, int T, int max_blocks, int wi
                ? ((ctx + 15) >> 4) - first_block(ctx, T, window)
                : 0;
 }
+// Partition units of a segment of nblk tiles: its start-up units, then its tiles.
+__device__ __forceinline__ int seg_units(int nblk) { return nblk > 0 ? nblk + kSegUnits : 0; }
 
 // Zero the outputs of one sequence (T x N x H elements of 2 bytes).
 template <int H>
@@ -179,6 +187,12 @@ __device__ __forceinline__ unsigned ticket_acq_rel(int32_t* t) {
                  : "=r"(v)
                  : "l"(t)
                  : "memory");
+    return v;
+}
+// Tickets drawn so far (acquire: the pieces that drew them are visible).
+__device__ __forceinline__ unsigned ticket_seen(const int32_t* t) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(t) : "memory");
     return v;
 }
 
@@ -225,14 +239,14 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         griddep_wait();
         waited = true;
     }
-    // 1. Blocks per sequence and their prefix sum (lane l owns a run of b).
+    // 1. Partition units per sequence and their prefix sum (lane l owns a run of b).
     const int per = (p.B + 31) / 32;
     const int lo = min(p.B, lane * per), hi = min(p.B, lo + per);
     int local = 0;
     bool invalid = false;
     for (int b = lo; b < hi; ++b) {
         const int n = seq_blocks(p.context_lens[b], p.T, p.max_blocks, win);
-        local += n;
+        local += seg_units(n);
         invalid |= (n == 0);
     }
     if (blockIdx.x == 0 && __any_sync(FULL, invalid)) {
@@ -264,7 +278,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
     int it = 0;  // stages issued
     bool aborted = false;
     if (c0 < c1) {
-        // 2. Locate tile c0: the lane whose run of sequences contains it.
+        // 2. Locate unit c0: the lane whose run of sequences contains it.
         const bool mine = (long long)nKC * excl <= c0 && c0 < (long long)nKC * incl;
         const unsigned owners = __ballot_sync(FULL, mine);
         const int owner = __ffs(owners) - 1;
@@ -273,8 +287,8 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         if (lane == owner) {
             long long acc = (long long)nKC * excl;
             for (int b = lo; b < hi; ++b) {
-                const long long n =
-                    (long long)nKC * seq_blocks(p.context_lens[b], p.T, p.max_blocks, win);
+                const long long n = (long long)nKC *
+                                    seg_units(seq_blocks(p.context_lens[b], p.T, p.max_blocks, win));
                 if (c0 < acc + n) {
                     fb = b;
                     fbase = acc;
@@ -284,7 +298,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             }
         }
         int b = __shfl_sync(FULL, fb, owner);
-        long long base = __shfl_sync(FULL, fbase, owner);  // first tile of segment (b, 0)
+        long long base = __shfl_sync(FULL, fbase, owner);  // first unit of segment (b, 0)
         // Lane-distributed look-ahead windows: context lengths of sequences
         // b .. b+31, and the first 32 block ids of sequence b+1, fetched before
         // they are needed so that moving to the next sequence costs no
@@ -294,8 +308,11 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         int ctx = __shfl_sync(FULL, ctxw, 0);
         int nblk = seq_blocks(ctx, p.T, p.max_blocks, win);
         int f0 = first_block(ctx, p.T, win);  // tile i is logical block f0 + i
+        // the range starts in segment k, at unit u of it (its first tile is
+        // unit kSegUnits): the first tile of the range is i
         const int rel = (int)(c0 - base);
-        int k = rel / nblk, i = rel % nblk;
+        int k = rel / seg_units(nblk);
+        int i = max(0, rel - k * seg_units(nblk) - kSegUnits);
         // KV head of virtual head k, kept incrementally (the issue path of
         // this warp is on the critical path: no division per stage)
         int kv = k / nC, kc = k - kv * nC;
@@ -312,7 +329,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         bool next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);  // ids_next is b+1's
 
         // 3. Stream the range, one stage (up to four tiles of a segment) at a time.
-        long long x = c0;
+        long long x = base + (long long)k * seg_units(nblk) + kSegUnits + i;  // unit of tile i
         while (x < c1) {
             const int run = (int)min((long long)min(C::kTiles, nblk - i), c1 - x);
             if (i < ids_base || i + run > ids_base + 32) {  // warp-uniform refill
@@ -350,7 +367,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                     m.blk_i = f0 + i;  // logical block index
                     m.ntiles = run;
                     m.ctx = ctx;
-                    m.seg_start = (int)(base + (long long)k * nblk);
+                    m.seg_start = (int)(base + (long long)k * seg_units(nblk) + kSegUnits);
                     m.nblk = nblk;
                     m.quota = quota;
                     m.cta_start = (int)c0;
@@ -409,6 +426,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
             i += run;
             if (i == nblk) {
                 i = 0;
+                x += kSegUnits;  // the next segment's start-up units
                 const bool more = x < c1;
                 if (GENERAL && ++kc == nC) {
                     kc = 0;
@@ -417,7 +435,7 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                 if (++k == nKC) {
                     k = 0;
                     kv = 0;
-                    base += (long long)nKC * nblk;
+                    base += (long long)nKC * seg_units(nblk);
                     ids_base = -(1 << 30);
                     if (x < c1) {
                         const int b_prev = b;
@@ -495,6 +513,11 @@ struct Consumer {
     float m0[NW], m1[NW], l0[NW], l1[NW];
     bool bad;
     int cb, ck, cstart, cnblk, cquota, ccta0;
+    unsigned seen;  // lane 0: tickets of the current split segment read before its close
+    // Fused append with one new token: this lane's 16-byte chunk of the new
+    // key (lanes < H/8) or value (the next H/8 lanes) row, loaded when the
+    // segment starts so that it has landed by the stage that holds it.
+    uint4 newrow;
     int rbase, rend;  // query rows [rbase, rend) of the current chunk
     // int8 codes enter the QK^T mma as c + 1152 (no subtraction per pair):
     // 1152 * sum_h q_h is taken off every score of query rows 2q4 / 2q4+1
@@ -540,6 +563,18 @@ struct Consumer {
         cquota = md.quota;
         ccta0 = md.cta_start;
         bad = false;
+        if constexpr (KVQ == 0 && !GENERAL) {
+            // the segment's piece in this CTA holds the new token iff this CTA
+            // holds the segment's last tile
+            constexpr int kChunks = H / 8;
+            if (p.k_new && p.T == 1 && (cstart + cnblk - 1) / cquota == (int)blockIdx.x &&
+                lane < 2 * kChunks) {
+                const bool is_v = lane >= kChunks;
+                const size_t row = ((size_t)cb * p.K + ck) * kChunks;
+                newrow = __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row +
+                               (is_v ? lane - kChunks : lane));
+            }
+        }
 #pragma unroll
         for (int u = 0; u < NW; ++u) {
             m0[u] = m1[u] = -INFINITY;
@@ -623,7 +658,9 @@ struct Consumer {
                     const int c = is_v ? lane - kChunks : lane;
                     const size_t row = (((size_t)cb * p.T + t) * p.K + ck) * kChunks;
                     const uint4 val =
-                        __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row + c);
+                        (!GENERAL && p.T == 1) ? newrow  // loaded when the segment started
+                                 : __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) +
+                                         row + c);
                     const uint32_t dst = (is_v ? vbase : kbase) + j * C::kTileBytes +
                                          (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
                     st_shared_v4(dst, val);
@@ -1121,12 +1158,25 @@ struct Consumer {
         }
     }
 
+    // The first piece of a split segment ends its CTA's range, so the other
+    // pieces have usually drawn their tickets by then: read the count early
+    // (lane 0, before the groups meet), so that finalize can merge at once.
+    __device__ void peek_ticket() {
+        const int first = cstart / cquota;
+        const int last = (cstart + cnblk - 1) / cquota;
+        seen = 0u;
+        if (lane == 0 && first != last && (int)blockIdx.x == first) seen = ticket_seen(ticket(first));
+    }
+
     // Finish the segment (row sums already reduced).  A split segment's pieces
-    // sit in CTAs first..last.  Each piece's warp publishes its partial (max,
-    // sum, accumulator, invalid-block flag) and takes a ticket; the warp that
-    // draws the last one folds the pieces in CTA order -- starting from the
-    // first piece's state, exactly as stored -- stores the rows and resets the
-    // ticket for the next call.  Nothing waits.
+    // sit in CTAs first..last.  If the others have all drawn tickets when the
+    // first piece closes (the usual case: it ends its CTA's range), it folds
+    // them into its own state right away.  Otherwise each piece's warp
+    // publishes its partial (max, sum, accumulator, invalid-block flag) and
+    // takes a ticket, and the warp that draws the last one folds the pieces.
+    // Either way the fold runs in CTA order from the first piece's state,
+    // exactly as stored -- a deterministic result -- and the merger stores
+    // the rows and resets the ticket for the next call.  Nothing waits.
     __device__ void finalize() {
         const int first = cstart / cquota;
         const int last = (cstart + cnblk - 1) / cquota;
@@ -1134,6 +1184,11 @@ struct Consumer {
         if (first == last) {
 #pragma unroll
             for (int u = 0; u < NW; ++u) store(u, l0[u], l1[u], bad);
+            return;
+        }
+        if (me == first && __shfl_sync(FULL, seen, 0) == (unsigned)(last - first)) {
+            __syncwarp();  // lane 0's acquire before every lane's loads
+            merge_others(first, last);
             return;
         }
         auto slot_of = [&](int c) { return c == first ? 1 : 0; };
@@ -1158,9 +1213,16 @@ struct Consumer {
         drawn = __shfl_sync(FULL, drawn, 0);
         if (drawn != (unsigned)(last - first)) return;  // another piece's warp merges
         __syncwarp();  // orders lane 0's acquire before every lane's loads
-        // ---- the last piece to finish: fold all pieces in CTA order, in
-        //      batches whose loads are all in flight before any is used -----
-        constexpr int kBatch = (H == 64) ? 4 : 2;
+        merge_others(first, last);
+    }
+
+    // Fold every piece of the split segment in CTA order -- starting from the
+    // first piece's state (this warp's registers if it holds it) -- in batches
+    // whose loads are all in flight before any is used; store the rows and
+    // reset the ticket.
+    __device__ void merge_others(int first, int last) {
+        const int me = blockIdx.x;
+        constexpr int kBatch = 2;
         bool any_bad = false;
 #pragma unroll
         for (int u = 0; u < NW; ++u) {
@@ -1240,6 +1302,7 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
     };
     int nseg = 0;  // segments closed so far (phase of the combine barrier)
     auto close = [&]() -> bool {
+        if (gi == 0) cs.peek_ticket();  // its latency overlaps the groups' meeting
         cs.reduce_l();
         const int buf = nseg & 1;  // double buffer: group 0 may still read the other
         if (gi != 0) cs.save_state(slot(buf, gi));
@@ -1362,9 +1425,11 @@ const void* pick_kernel(int H, bool bf16, int nw, bool general, int kvq) {
 }
 
 // Consumer groups for nt row warps.  (A third group was measured slower on
-// the 40-row verify workload: stages then contend for shared memory.)  Over a
-// one-byte cache every warp spends most of its issue slots turning codes
-// into mma fragments, so few-row shapes get more groups (more warps per SM).
+// the 40-row verify workload: stages then contend for shared memory; four
+// groups for one row warp were measured slower on the 24-layer batch of
+// short contexts, 313 vs 285 us per step.)  Over a one-byte cache every warp
+// spends most of its issue slots turning codes into mma fragments, so
+// few-row shapes get more groups (more warps per SM).
 int groups_for(int nt, int kvq) {
     if (kvq) return std::max(kGroups, std::min(4, (kGroups * kMaxRowWarps) / nt));
     return kGroups;
@@ -1376,14 +1441,15 @@ int max_row_warps(int nw) { return nw == 1 ? kMaxRowWarps : kMaxRowWarps / 2; }
 // Dynamic shared memory of one CTA: nt row warps (nw tiles each) per consumer
 // group and a ring of `stages` stages.
 template <int H, int KVQ>
-size_t smem_of(int nt, int nw, int stages) {
+size_t smem_of(int nt, int nw, int stages, int groups) {
     using C = Cfg<H, KVQ>;
     return C::kFixed + (size_t)stages * (C::kStageBytes + C::kStageOverhead) +
-           (size_t)(groups_for(nt, KVQ) - 1) * nt * nw * C::kScratchBytesPerRowWarp;
+           (size_t)(groups - 1) * nt * nw * C::kScratchBytesPerRowWarp;
 }
-size_t smem_for(int H, int nt, int nw, int stages, int kvq) {
-    if (kvq) return smem_of<128, 1>(nt, nw, stages);  // both one-byte kinds: H = 128
-    return H == 64 ? smem_of<64, 0>(nt, nw, stages) : smem_of<128, 0>(nt, nw, stages);
+size_t smem_for(int H, int nt, int nw, int stages, int kvq, int groups) {
+    if (kvq) return smem_of<128, 1>(nt, nw, stages, groups);  // both one-byte kinds: H = 128
+    return H == 64 ? smem_of<64, 0>(nt, nw, stages, groups)
+                   : smem_of<128, 0>(nt, nw, stages, groups);
 }
 int default_stages(int H, int kvq) {
     if (kvq) return Cfg<128, 1>::kStages;
@@ -1393,7 +1459,7 @@ int default_stages(int H, int kvq) {
 size_t max_smem(int H, int nw, int kvq) {
     size_t m = 0;
     for (int nt = 1; nt <= max_row_warps(nw); ++nt)
-        m = std::max(m, smem_for(H, nt, nw, default_stages(H, kvq), kvq));
+        m = std::max(m, smem_for(H, nt, nw, default_stages(H, kvq), kvq, groups_for(nt, kvq)));
     return m;
 }
 
@@ -1443,12 +1509,14 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
 // CTAs of one variant resident per SM, queried once per (device, variant) so
 // that later calls -- including calls being captured into a CUDA graph -- make
 // no attribute or occupancy API calls.
-int resident_ctas(int H, bool bf16, int nt, int nw, bool general, int kvq, size_t smem) {
+int resident_ctas(int H, bool bf16, int nt, int nw, bool general, int kvq, int groups,
+                  size_t smem) {
     static std::mutex mu;
     static std::map<std::tuple<int, int, int, int, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key = std::make_tuple(dev, H, (int)bf16, nt, (nw * 2 + (int)general) * 4 + kvq);
+    const auto key =
+        std::make_tuple(dev, H, (int)bf16, nt, ((nw * 2 + (int)general) * 4 + kvq) * 8 + groups);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
@@ -1461,7 +1529,7 @@ int resident_ctas(int H, bool bf16, int nt, int nw, bool general, int kvq, size_
         return 0;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern,
-                                                      32 * (groups_for(nt, kvq) * nt + 1),
+                                                      32 * (groups * nt + 1),
                                                       smem) !=
         cudaSuccess)
         return 0;
@@ -1523,15 +1591,15 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     // workload: fewer warps hide less latency.  The kernel keeps both forms.)
     const int nw = 1;
     const int nt = (rows_per_chunk + 8 * nw - 1) / (8 * nw);
-    const int groups = groups_for(nt, s.kv_dtype);
-    const int threads = 32 * (groups * nt + 1);
     const int kvq = s.kv_dtype;
+    const int groups = groups_for(nt, kvq);
     int stages = default_stages(s.H, kvq);
-    size_t smem = smem_for(s.H, nt, nw, stages, kvq);
+    size_t smem = smem_for(s.H, nt, nw, stages, kvq, groups);
     const bool general = masked || s.window > 0 || chunks > 1;
     // the one-byte caches have the plain kernel for H = 128 only
     if (kvq != GQA_KV_SAME && (s.H != 128 || general)) return GQA_ERR_SHAPE;
-    int occ = resident_ctas(s.H, s.dtype == GQA_BF16, nt, nw, general, kvq, smem);
+    const bool bf16 = s.dtype == GQA_BF16;
+    const int occ = resident_ctas(s.H, bf16, nt, nw, general, kvq, groups, smem);
     if (occ < 1) return GQA_ERR_CUDA;
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
@@ -1543,7 +1611,8 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     long long blocks_max = s.max_blocks_per_seq;  // per sequence, window included
     if (s.window > 0)
         blocks_max = std::min<long long>(blocks_max, ((long long)s.window + s.T + 14) / 16 + 1);
-    const long long tiles_max = (long long)s.B * s.K * chunks * blocks_max;
+    const long long tiles_max = (long long)s.B * s.K * chunks * (blocks_max + kSegUnits);
+    const int threads = 32 * (groups * nt + 1);
     long long grid = (long long)sms * occ;
     grid = std::min<long long>(grid, std::max<long long>(1, (tiles_max + kQuotaMin - 1) / kQuotaMin));
     plan->grid = (int)grid;

@@ -159,6 +159,12 @@ __device__ __forceinline__ unsigned tc_ticket(int32_t* t) {
                  : "memory");
     return v;
 }
+// Tickets drawn so far (acquire: the pieces that drew them are visible).
+__device__ __forceinline__ unsigned tc_ticket_seen(const int32_t* t) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(t) : "memory");
+    return v;
+}
 
 // Waits until stage n has landed.
 __device__ __forceinline__ bool stage_landed(TcSmem& sm, int n) {
@@ -728,6 +734,15 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
         }
         n0 += nst;
         // ---- the piece's rows: the two groups' results meet ------------------------
+        // The first piece of a split segment ends its CTA's range, so the
+        // other pieces have usually drawn their tickets by now: read the
+        // count (its latency overlaps the meeting below).
+        const int first_cta = (int)(pc.first / sm.quota);
+        const int last_cta = (int)((pc.first + pc.nb - 1) / sm.quota);
+        const int wi = warp - kSoftmaxWarp0;  // this warp's ticket among the CTA's eight
+        unsigned seen = 0u;
+        if (lane == 0 && first_cta != last_cta && (int)blockIdx.x == first_cta)
+            seen = tc_ticket_seen(p.flags + 8 * first_cta + wi);
         if (ok && mine > 0) {  // this group's last PV has completed
             ok = mbar_wait(smem_addr(&sm.o_ready[g]), (kg - 1) & 1);
             tc_fence_after();
@@ -767,8 +782,6 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
         }
         tc_fence_before();
         mbar_arrive(smem_addr(&sm.o_free));
-        const int first_cta = (int)(pc.first / sm.quota);
-        const int last_cta = (int)((pc.first + pc.nb - 1) / sm.quota);
         if (first_cta == last_cta) {  // the whole segment: O / l in q's dtype
             const bool zero = bad || !(lt > 0.f);  // an invalid block id: zeros
             if (zero) {
@@ -787,17 +800,19 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             continue;
         }
         // ---- a piece of a split segment -------------------------------------------
-        // Each warp publishes its rows of the piece (partial O over its 64
-        // dims, max, sum; slot 1 for the segment's first piece, which ends its
-        // CTA's range, slot 0 for the others, which start theirs) and takes a
-        // ticket.  The warp that draws the last one folds the pieces' partials
-        // in CTA order, starting from the first piece's, and stores its 32
-        // rows x 64 dims with plain stores; it resets the ticket for the next
+        // If this is the first piece and every other piece's warp has drawn
+        // its ticket, fold them in now.  Otherwise each warp publishes its
+        // rows of the piece (partial O over its 64 dims, max, sum; slot 1 for
+        // the segment's first piece, which ends its CTA's range, slot 0 for
+        // the others, which start theirs) and takes a ticket, and the warp
+        // that draws the last one folds.  The fold runs over the pieces in CTA
+        // order from the first piece's state; the merging warp stores its 32
+        // rows x 64 dims with plain stores and resets the ticket for the next
         // call.  No warp waits for another CTA.
         const int me = blockIdx.x;
-        const int wi = warp - kSoftmaxWarp0;  // this warp's ticket among the CTA's eight
         const int npieces = last_cta - first_cta + 1;
-        if (active) {
+        const bool early = me == first_cta && __shfl_sync(FULLM, seen, 0) == (unsigned)(npieces - 1);
+        if (active && !early) {
             float* part = p.partials + ((size_t)me * 2 + (me == first_cta ? 1 : 0)) * kPartFloats;
 #pragma unroll
             for (int k = 0; k < 64; ++k)
@@ -806,10 +821,12 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             __stcg(part + (129 + 2 * g) * kRowsTc + row, bad ? -1.f : lt);  // -1: a bad block
         }
         __syncwarp();  // the lanes' stores before lane 0's ticket
-        unsigned drawn = 0;
-        if (lane == 0) drawn = tc_ticket(p.flags + 8 * first_cta + wi);
-        drawn = __shfl_sync(FULLM, drawn, 0);
-        if (drawn != (unsigned)(npieces - 1)) continue;  // another piece's warp merges
+        if (!early) {
+            unsigned drawn = 0;
+            if (lane == 0) drawn = tc_ticket(p.flags + 8 * first_cta + wi);
+            drawn = __shfl_sync(FULLM, drawn, 0);
+            if (drawn != (unsigned)(npieces - 1)) continue;  // another piece's warp merges
+        }
         __syncwarp();  // lane 0's acquire before every lane's reads of the partials
         if (active) {
             // online fold over the pieces in CTA order: running max MM, sum L

@@ -6,11 +6,11 @@ of its tiles, and hands CTA c the units [c*quota, (c+1)*quota).  Its split-
 segment protocol relies on three properties, checked here over random ragged
 batches with the kernel's own constants read from the source:
   - every tile of every segment lands in exactly one piece;
-  - a split segment's first piece (tile 0) is the last piece of its CTA (it
-    merges at the end of the CTA's range);
-  - every other piece of a split segment is the first piece of its CTA, and
-    every CTA between the first and the last holds one (it publishes early and
-    the merger waits for exactly those CTAs).
+  - a split segment's first piece (tile 0) is the last piece of its CTA, so
+    it can use the CTA's second partial slot;
+  - every other piece of a split segment is the first piece of its CTA (the
+    first slot), and every CTA between the first and the last holds one (the
+    ticket counts exactly those pieces).
 The GPU tests exercise the kernel itself; this pins the arithmetic it uses."""
 import os
 import random
@@ -86,10 +86,10 @@ def check(nblks, kc, grid):
             if fc == lc:
                 continue
             if t0 == 0:
-                assert c == fc and i == len(ps) - 1  # merger: ends its CTA's range
+                assert c == fc and i == len(ps) - 1  # first piece: ends its CTA's range
                 for cc in range(fc + 1, lc + 1):
                     head = pieces[cc][0]
-                    assert head[:2] == (b, v) and head[3] > 0  # publisher, first in range
+                    assert head[:2] == (b, v) and head[3] > 0  # later piece, first in range
             else:
                 assert fc < c <= lc and i == 0
     assert set(cover) == {(b, v, t) for b, nb in enumerate(nblks) for v in range(kc)
