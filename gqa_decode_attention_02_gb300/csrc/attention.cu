@@ -73,7 +73,7 @@ constexpr int kMaxThreads = 32 * (kGroups * kMaxRowWarps + 1);
 constexpr int kEnd = 1, kBad = 2;
 constexpr int kTilesPerStage = 4;          // cache blocks per pipeline stage (2-byte cache)
 constexpr int kMaxTilesPerStage = 8;       // ... and over one-byte codes
-constexpr int kQuotaMin = 4 * kTilesPerStage;  // units per CTA at least: fewer split pieces
+constexpr int kQuotaMin = 2 * kTilesPerStage;  // units per CTA at least: fewer split pieces
 // Start-up cost of a segment in the work partition, in tiles: a segment
 // occupies kSegUnits units and then its tiles, so a CTA that starts many
 // (short) segments -- each with its q rows, new rows and epilogue -- streams
@@ -1216,18 +1216,19 @@ struct Consumer {
         merge_others(first, last);
     }
 
-    // Fold every piece of the split segment in CTA order -- starting from the
-    // first piece's state (this warp's registers if it holds it) -- in batches
-    // whose loads are all in flight before any is used; store the rows and
-    // reset the ticket.
+    // Combine every piece of the split segment, in two passes whose loads are
+    // all in flight together: the rows' maxima M over the pieces, then the
+    // sums of the pieces' (sum, accumulator) with weights 2^(m_c - M), in CTA
+    // order from the first piece (this warp's registers if it holds it).  The
+    // result does not depend on which warp merges.  Store the rows and reset
+    // the ticket.
     __device__ void merge_others(int first, int last) {
         const int me = blockIdx.x;
-        constexpr int kBatch = 2;
+        constexpr int kUnroll = (H == 64) ? 4 : 1;  // pieces whose loads are in flight at once
         bool any_bad = false;
 #pragma unroll
         for (int u = 0; u < NW; ++u) {
-            // start from the first piece's state (registers if this is it)
-            if (me != first) {
+            if (me != first) {  // the first piece's state
                 const float* sc = section(first, 1, u);
                 m0[u] = __ldcg(sc + 2 * q4);
                 m1[u] = __ldcg(sc + 2 * q4 + 1);
@@ -1247,31 +1248,53 @@ struct Consumer {
             } else {
                 any_bad |= bad;
             }
-            for (int c0 = first + 1; c0 <= last; c0 += kBatch) {
-                float mc[kBatch][2], lc[kBatch][2], fl[kBatch];
-                float4 v[kBatch][C::kSteps];
-                // Unconditional loads (past the last piece the batch re-reads it
-                // and then gives it no weight).
+            // pass 1: the maxima of the two rows this lane holds
+            float M0 = m0[u], M1 = m1[u];
+#pragma unroll kUnroll
+            for (int c = first + 1; c <= last; ++c) {
+                const float* sc = section(c, 0, u);
+                M0 = fmaxf(M0, __ldcg(sc + 2 * q4));
+                M1 = fmaxf(M1, __ldcg(sc + 2 * q4 + 1));
+            }
+            // pass 2: the first piece scaled, then the others added in order
+            {
+                const float a0 = (m0[u] == -INFINITY) ? 0.f : fast_exp2(m0[u] - M0);
+                const float a1 = (m1[u] == -INFINITY) ? 0.f : fast_exp2(m1[u] - M1);
+                l0[u] *= a0;
+                l1[u] *= a1;
 #pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    const float* sc = section(min(c0 + j, last), 0, u);
-                    mc[j][0] = __ldcg(sc + 2 * q4);
-                    mc[j][1] = __ldcg(sc + 2 * q4 + 1);
-                    lc[j][0] = __ldcg(sc + 8 + 2 * q4);
-                    lc[j][1] = __ldcg(sc + 8 + 2 * q4 + 1);
-                    fl[j] = __ldcg(sc + 16);
-                    const float4* b4 =
-                        reinterpret_cast<const float4*>(sc + C::kHeaderFloats) + lane * C::kSteps;
-#pragma unroll
-                    for (int mt = 0; mt < C::kSteps; ++mt) v[j][mt] = __ldcg(b4 + mt);
-                }
-#pragma unroll
-                for (int j = 0; j < kBatch; ++j) {
-                    if (c0 + j > last) continue;
-                    any_bad |= fl[j] != 0.f;
-                    fold(u, mc[j][0], mc[j][1], lc[j][0], lc[j][1], v[j]);
+                for (int mt = 0; mt < C::kSteps; ++mt) {
+                    acc[u][mt][0] *= a0;
+                    acc[u][mt][1] *= a1;
+                    acc[u][mt][2] *= a0;
+                    acc[u][mt][3] *= a1;
                 }
             }
+#pragma unroll kUnroll
+            for (int c = first + 1; c <= last; ++c) {
+                const float* sc = section(c, 0, u);
+                const float mc0 = __ldcg(sc + 2 * q4), mc1 = __ldcg(sc + 2 * q4 + 1);
+                const float lc0 = __ldcg(sc + 8 + 2 * q4), lc1 = __ldcg(sc + 8 + 2 * q4 + 1);
+                any_bad |= __ldcg(sc + 16) != 0.f;
+                const float4* b4 =
+                    reinterpret_cast<const float4*>(sc + C::kHeaderFloats) + lane * C::kSteps;
+                float4 v[C::kSteps];
+#pragma unroll
+                for (int mt = 0; mt < C::kSteps; ++mt) v[mt] = __ldcg(b4 + mt);
+                const float a0 = (mc0 == -INFINITY) ? 0.f : fast_exp2(mc0 - M0);
+                const float a1 = (mc1 == -INFINITY) ? 0.f : fast_exp2(mc1 - M1);
+                l0[u] += lc0 * a0;
+                l1[u] += lc1 * a1;
+#pragma unroll
+                for (int mt = 0; mt < C::kSteps; ++mt) {
+                    acc[u][mt][0] += v[mt].x * a0;
+                    acc[u][mt][1] += v[mt].y * a1;
+                    acc[u][mt][2] += v[mt].z * a0;
+                    acc[u][mt][3] += v[mt].w * a1;
+                }
+            }
+            m0[u] = M0;
+            m1[u] = M1;
         }
         if (lane == 0) *ticket(first) = 0;  // ready for the next call
 #pragma unroll
