@@ -557,6 +557,30 @@ def run_ours(args, world, rank, local):
     if int(st.item()) != 0:
         raise RuntimeError(f"device status {int(st.item())} in the timed region")
 
+    # Parity of the timed step's outputs (outside the timed region, before any
+    # other launch writes `outs`): attention on a seeded sample of sequences,
+    # acceptance on the whole batch.
+    oracle_inputs = {}
+    parity = None
+    if rank == 0 and not args.no_parity:
+        import oracle
+
+        oracle.build()
+        parity = parity_sample(w, outs, quant_cpu if q8 else None, oracle_inputs)
+        if has_acc:
+            ctx0 = w.context_lens.cpu().numpy()
+            if sampled:
+                ra, rn, rc, _ = oracle.accept_sampled(
+                    sin.q.cpu().numpy(), sin.p.cpu().numpy(), sin.draft.cpu().numpy(),
+                    sin.uniforms.cpu().numpy(), ctx0)
+            else:
+                ra, rn, rc = oracle.accept_prefix(w.logits.cpu(), w.draft.cpu(), ctx0)
+            acc_ok = (np.array_equal(acc_out.cpu().numpy(), ra)
+                      and np.array_equal(nxt_out.cpu().numpy(), rn)
+                      and np.array_equal(ctx_scratch.cpu().numpy(), rc))
+            parity["accept_bit_exact"] = bool(acc_ok)
+            parity["parity_pass"] = bool(parity["parity_pass"] and acc_ok)
+
     # Tree verification: the same launches with the plain chain mask, for the
     # cost of the custom mask (the speculation blog reports up to 50 % for a
     # mask over the whole sequence).
@@ -667,29 +691,6 @@ def run_ours(args, world, rank, local):
             else:
                 rec["how"] = "as e2e but every library call made from Python each step"
                 e2e_eager = rec
-
-    # Parity of the timed step's outputs (outside the timed region): attention
-    # on a seeded sample of sequences, acceptance on the whole batch.
-    oracle_inputs = {}
-    parity = None
-    if rank == 0 and not args.no_parity:
-        import oracle
-
-        oracle.build()
-        parity = parity_sample(w, outs, quant_cpu if q8 else None, oracle_inputs)
-        if has_acc:
-            ctx0 = w.context_lens.cpu().numpy()
-            if sampled:
-                ra, rn, rc, _ = oracle.accept_sampled(
-                    sin.q.cpu().numpy(), sin.p.cpu().numpy(), sin.draft.cpu().numpy(),
-                    sin.uniforms.cpu().numpy(), ctx0)
-            else:
-                ra, rn, rc = oracle.accept_prefix(w.logits.cpu(), w.draft.cpu(), ctx0)
-            acc_ok = (np.array_equal(acc_out.cpu().numpy(), ra)
-                      and np.array_equal(nxt_out.cpu().numpy(), rn)
-                      and np.array_equal(ctx_scratch.cpu().numpy(), rc))
-            parity["accept_bit_exact"] = bool(acc_ok)
-            parity["parity_pass"] = bool(parity["parity_pass"] and acc_ok)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
