@@ -125,6 +125,28 @@ def test_zero_row(kv):
     assert sc == 0.0 and (codes == 0).all()
 
 
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+def test_nan_element_leaves_the_rest_of_the_row_as_if_it_were_zero(kv):
+    """A NaN element (outside the contract: the pages quantize finite values)
+    does not enter max|x| -- the row's scale and every other code are those of
+    the same row with that element at zero -- and gets code 0 for int8 and
+    e4m3's NaN code 0x7f, the code torch.float8_e4m3fn gives a NaN."""
+    x = torch.randn(128, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    x[17] = float("nan")
+    zeroed = x.clone()
+    zeroed[17] = 0.0
+    codes, sc = oracle.quantize_row(x, "bf16", kv)
+    codes0, sc0 = oracle.quantize_row(zeroed, "bf16", kv)
+    assert sc == sc0 and sc > 0
+    keep = np.arange(128) != 17
+    np.testing.assert_array_equal(codes[keep], codes0[keep])
+    if kv == "int8":
+        assert codes[17] == 0
+    else:
+        want = torch.tensor([float("nan")]).to(torch.float8_e4m3fn).view(torch.uint8).item()
+        assert codes[17] == want == 0x7F
+
+
 # ---- quantized append and attention --------------------------------------------------
 def empty_quant_cache(w):
     NB, bs, K, H = w.k_cache[0].shape
