@@ -425,8 +425,8 @@ def run_ours(args, world, rank, local):
                 del x, y
             w.k_cache[l] = w.v_cache[l] = None  # the 2-byte caches are not used
         torch.cuda.empty_cache()
-        quant_cpu = None
-        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        quant_cpu = None  # CPU copies for the oracle: parity and the CPU baseline
+        if rank == 0 and (not args.no_parity or (world == 1 and not args.no_cpu_baseline)):
             quant_cpu = (args.kv, [c.cpu() for c in qk], [c.cpu() for c in qv],
                          [c.cpu() for c in sk], [c.cpu() for c in sv])
         attn_q8 = gq.decode_attention_quant if w.T == 1 else gq.verify_attention_quant
@@ -471,7 +471,7 @@ def run_ours(args, world, rank, local):
             if q8:
                 attn_q8(w.q[l], qk[l], qv[l], sk[l], sv[l], w.block_tables, w.context_lens,
                         kv=args.kv, out=outs[l], workspace=ws, status=st, pdl=True,
-                        early_kv=True)
+                        early_kv=True, window=w.window(l))
             elif fused:
                 fused_fn(w.q[l], w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
                          w.block_tables, w.context_lens, out=outs[l], workspace=ws, status=st,

@@ -206,14 +206,15 @@ def append_verify_attention(q, k_new, v_new, k_cache, v_cache, block_tables, con
 
 
 def _attention_quant(fn_name, q, k_cache, v_cache, k_scale, v_scale, block_tables,
-                     context_lens, out, scale, workspace, status, stream, pdl, early_kv, kv):
+                     context_lens, out, scale, workspace, status, stream, pdl, early_kv, kv,
+                     window=0):
     _lib._need(q, "q", ndim=4)
     _need_quant_cache(k_cache, k_scale, "k_cache")
     _need_quant_cache(v_cache, v_scale, "v_cache")
     _lib._need(block_tables, "block_tables", torch.int32, 2)
     _lib._need(context_lens, "context_lens", torch.int32, 1)
     flags = (_lib.FLAG_PDL if pdl else 0) | (_lib.FLAG_EARLY_KV if early_kv else 0)
-    shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags, kv=kv)
+    shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags, window=window, kv=kv)
     if out is None:
         out = torch.empty_like(q)
     else:
@@ -235,20 +236,22 @@ def _attention_quant(fn_name, q, k_cache, v_cache, k_scale, v_scale, block_table
 
 def decode_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                            *, kv="int8", out=None, scale=None, workspace=None, status=None,
-                           stream=None, pdl=False, early_kv=False):
-    """gqa_decode_attention_quant over a one-byte cache (kv = "int8" / "e4m3")."""
+                           stream=None, pdl=False, early_kv=False, window=0):
+    """gqa_decode_attention_quant over a one-byte cache (kv = "int8" / "e4m3");
+    window > 0 is local attention as in decode_attention."""
     return _attention_quant("gqa_decode_attention_quant", q, k_cache, v_cache, k_scale, v_scale,
                             block_tables, context_lens, out, scale, workspace, status, stream,
-                            pdl, early_kv, kv)
+                            pdl, early_kv, kv, window)
 
 
 def verify_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                            *, kv="int8", out=None, scale=None, workspace=None, status=None,
-                           stream=None, pdl=False, early_kv=False):
-    """gqa_verify_attention_quant over a one-byte cache (kv = "int8" / "e4m3")."""
+                           stream=None, pdl=False, early_kv=False, window=0):
+    """gqa_verify_attention_quant over a one-byte cache (kv = "int8" / "e4m3");
+    window > 0 is local attention as in verify_attention."""
     return _attention_quant("gqa_verify_attention_quant", q, k_cache, v_cache, k_scale, v_scale,
                             block_tables, context_lens, out, scale, workspace, status, stream,
-                            pdl, early_kv, kv)
+                            pdl, early_kv, kv, window)
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,

@@ -148,7 +148,7 @@ size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     // the largest need of the kernels that may serve the shape
     gqa::AttnPlan plain, general;
     if (gqa::attention_plan(*shape, false, &plain) != GQA_OK) return 0;
-    if (shape->kv_dtype != GQA_KV_SAME) return plain.workspace;  // no general variant
+    if (shape->kv_dtype != GQA_KV_SAME) return plain.workspace;  // no tree mask, no tcgen05
     if (gqa::attention_plan(*shape, true, &general) != GQA_OK) return 0;
     size_t w = plain.workspace > general.workspace ? plain.workspace : general.workspace;
     const size_t tc = gqa::tc_workspace_bytes(*shape, plain.flags_bytes);  // 0: not served

@@ -138,8 +138,11 @@ struct Cfg {
     // of a 128-byte-swizzled TMA destination
     static constexpr int kStageBytes =
         (2 * kTiles * (kTileBytes + kScaleBytes) + 1023) / 1024 * 1024;
-    // Default ring depth (two CTAs per SM fit).
-    static constexpr int kStages = KVQ ? 4 : (H == 128) ? 3 : 6;
+    // Ring depth: two CTAs per SM fit at H = 128; at H = 64 four stages let
+    // three fit (the 24-layer batch of short contexts ran 272 us per step,
+    // against 283 with six stages and two CTAs).  One-byte caches: the deepest
+    // ring tried (the launch takes the depth that fits the most CTAs per SM).
+    static constexpr int kStages = KVQ ? 4 : (H == 128) ? 3 : 4;
     static constexpr int kHalves = KVQ ? 1 : H / 64;  // 128-byte swizzle spans per row
     static constexpr int kSteps = H / 16;  // k16 steps of QK^T == m16 tiles of PV
     static constexpr int kAccFloats = H / 4;  // accumulator floats per lane
@@ -789,7 +792,9 @@ struct Consumer {
     // the K side (1152 * sum(q) is taken off each score) and as c on the V
     // side; e4m3 codes as their values times 2^-8 (the row scales carry the
     // 256).  The K row scales multiply the scores, the V row scales the
-    // probabilities (the row sums use the unscaled ones).
+    // probabilities.  The row sums add the fp32 probabilities: the PV operand
+    // (probability x scale, rounded to f16) has no unscaled counterpart, so
+    // rounding the sums as well would only add a second error of 2^-12 relative.
     __device__ void stage_q(uint32_t kbase, const typename C::Meta& md) {
         static_assert(H == 128 && NW == 1, "one-byte caches: H = 128, one tile per warp");
         // the stage's tiles in runs of four (the online softmax takes any split)
@@ -858,27 +863,44 @@ struct Consumer {
             const int j = j0 + jj;
             if (j >= ntl) break;  // warp-uniform
             const int tb = (md.blk_i + j) * 16;
-            const bool tail = tb + 16 > md.ctx;
+            // slots past the context, and (local attention) positions below
+            // every new token's window, may hold anything, NaN scales included
+            const int lo_min = (GENERAL && p.window > 0) ? md.ctx - p.T - p.window + 1 : 0;
+            const bool tail = tb + 16 > md.ctx || tb < lo_min;
             float svg = kCodeScale * ld_shared_f32(vsb + j * 64 + g * 4);
             float sv8 = kCodeScale * ld_shared_f32(vsb + j * 64 + (g + 8) * 4);
-            if (tail) {  // slots past the context may hold anything
-                if (tb + g >= md.ctx) svg = 0.f;
-                if (tb + g + 8 >= md.ctx) sv8 = 0.f;
+            if (tail) {
+                if (tb + g >= md.ctx || tb + g < lo_min) svg = 0.f;
+                if (tb + g + 8 >= md.ctx || tb + g + 8 < lo_min) sv8 = 0.f;
             }
             const float e0 = fast_exp2(sc[0][jj][0] - ref0[0]);
             const float e1 = fast_exp2(sc[0][jj][1] - ref1[0]);
             const float e2 = fast_exp2(sc[0][jj][2] - ref0[0]);
             const float e3 = fast_exp2(sc[0][jj][3] - ref1[0]);
-            const uint32_t u0 = E::pack(e0, e1), u1 = E::pack(e2, e3);
-            l0[0] += E::lo(u0) + E::lo(u1);
-            l1[0] += E::hi(u0) + E::hi(u1);
-            const uint32_t w0p = E::pack(e0 * svg, e1 * svg), w1p = E::pack(e2 * sv8, e3 * sv8);
+            l0[0] += e0 + e2;
+            l1[0] += e1 + e3;
+            const float f0 = e0 * svg, f1 = e1 * svg, f2 = e2 * sv8, f3 = e3 * sv8;
+            const uint32_t w0p = E::pack(f0, f1), w1p = E::pack(f2, f3);
             if constexpr (KVQ == GQA_KV_INT8) {
                 pv0[0] += E::lo(w0p) + E::lo(w1p);
                 pv1[0] += E::hi(w0p) + E::hi(w1p);
             }
             const uint32_t pb0 = movm_t(w0p);  // tokens 2q4, +1
             const uint32_t pb1 = movm_t(w1p);  // tokens 2q4+8, +9
+            // f16 outputs: each operand's rounding error enters as a second f16
+            // term (a half ulp of f16 relative to |V| would take half of the
+            // output's own error budget; bf16 outputs round far more coarsely)
+            uint32_t lb0 = 0u, lb1 = 0u;
+            if constexpr (!BF16) {
+                const uint32_t w0l = E::pack(f0 - E::lo(w0p), f1 - E::hi(w0p));
+                const uint32_t w1l = E::pack(f2 - E::lo(w1p), f3 - E::hi(w1p));
+                if constexpr (KVQ == GQA_KV_INT8) {
+                    pv0[0] += E::lo(w0l) + E::lo(w1l);
+                    pv1[0] += E::hi(w0l) + E::hi(w1l);
+                }
+                lb0 = movm_t(w0l);
+                lb1 = movm_t(w1l);
+            }
             const uint32_t vt = vbase + j * C::kTileBytes;
             const int t0_ = 2 * q4, t1_ = t0_ + 1, t2_ = t0_ + 8, t3_ = t0_ + 9;
             const uint4 x0 = ld_shared_v4(vt + t0_ * 128 + ((g ^ (t0_ & 7)) << 4));
@@ -918,6 +940,7 @@ struct Consumer {
                     a[3] = e4m3x2_to_f16x2_scaled<true>(p23);
                 }
                 E::mma(acc[0][mt], a, pb0, pb1);
+                if constexpr (!BF16) E::mma(acc[0][mt], a, lb0, lb1);
             }
         }
     }
@@ -1426,15 +1449,21 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
 // ---------------------------------------------------------------------------
 // Host side
 // The instantiated variants, for each head size and dtype: (nw, general) in
-// {(1, no), (1, yes), (2, no)} over a cache in q's dtype, and for H = 128 the
-// plain kernel over int8 and e4m3 caches.
+// {(1, no), (1, yes), (2, no)} over a cache in q's dtype, and for H = 128
+// (1, no) and (1, yes) over int8 and e4m3 caches.
 template <int H, bool BF16>
 const void* kernel_ptr(int nw, bool general, int kvq) {
     if constexpr (H == 128) {
         if (kvq == GQA_KV_INT8)
-            return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false, GQA_KV_INT8>);
+            return general ? reinterpret_cast<const void*>(
+                                 &attention_kernel<H, BF16, 1, true, GQA_KV_INT8>)
+                           : reinterpret_cast<const void*>(
+                                 &attention_kernel<H, BF16, 1, false, GQA_KV_INT8>);
         if (kvq == GQA_KV_E4M3)
-            return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, false, GQA_KV_E4M3>);
+            return general ? reinterpret_cast<const void*>(
+                                 &attention_kernel<H, BF16, 1, true, GQA_KV_E4M3>)
+                           : reinterpret_cast<const void*>(
+                                 &attention_kernel<H, BF16, 1, false, GQA_KV_E4M3>);
     }
     if (nw == 2) return reinterpret_cast<const void*>(&attention_kernel<H, BF16, 2, false, 0>);
     return general ? reinterpret_cast<const void*>(&attention_kernel<H, BF16, 1, true, 0>)
@@ -1447,16 +1476,15 @@ const void* pick_kernel(int H, bool bf16, int nw, bool general, int kvq) {
     return bf16 ? kernel_ptr<128, true>(nw, general, kvq) : kernel_ptr<128, false>(nw, general, kvq);
 }
 
-// Consumer groups for nt row warps.  (A third group was measured slower on
-// the 40-row verify workload: stages then contend for shared memory; four
-// groups for one row warp were measured slower on the 24-layer batch of
-// short contexts, 313 vs 285 us per step.)  Over a one-byte cache every warp
-// spends most of its issue slots turning codes into mma fragments, so
-// few-row shapes get more groups (more warps per SM).
-int groups_for(int nt, int kvq) {
-    if (kvq) return std::max(kGroups, std::min(4, (kGroups * kMaxRowWarps) / nt));
-    return kGroups;
-}
+// Consumer groups for nt row warps: two.  (A third group was measured slower
+// on the 40-row verify workload: stages then contend for shared memory; four
+// groups for one row warp were measured slower on the 24-layer batch of short
+// contexts, 313 vs 285 us per step.  Over a one-byte cache, the 256-sequence
+// ragged batch ran 365 us with two groups and two stages -- five CTAs per SM --
+// against 423 with three groups and 490 with four groups and four stages: what
+// bounds it is each CTA's one-stage-at-a-time producer, so CTAs per SM count
+// for more than warps per CTA.)
+int groups_for(int, int) { return kGroups; }
 
 // Row warps a group may have with nw 8-row tiles per warp (48 rows at most).
 int max_row_warps(int nw) { return nw == 1 ? kMaxRowWarps : kMaxRowWarps / 2; }
@@ -1529,17 +1557,18 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
     return r == CUDA_SUCCESS;
 }
 
-// CTAs of one variant resident per SM, queried once per (device, variant) so
+// CTAs of one variant resident per SM, queried once per (device, variant,
+// shared memory) so
 // that later calls -- including calls being captured into a CUDA graph -- make
 // no attribute or occupancy API calls.
 int resident_ctas(int H, bool bf16, int nt, int nw, bool general, int kvq, int groups,
                   size_t smem) {
     static std::mutex mu;
-    static std::map<std::tuple<int, int, int, int, int>, int> cache;
+    static std::map<std::tuple<int, int, int, int, int, size_t>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    const auto key =
-        std::make_tuple(dev, H, (int)bf16, nt, ((nw * 2 + (int)general) * 4 + kvq) * 8 + groups);
+    const auto key = std::make_tuple(dev, H, (int)bf16, nt,
+                                     ((nw * 2 + (int)general) * 4 + kvq) * 8 + groups, smem);
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
@@ -1619,11 +1648,24 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     int stages = default_stages(s.H, kvq);
     size_t smem = smem_for(s.H, nt, nw, stages, kvq, groups);
     const bool general = masked || s.window > 0 || chunks > 1;
-    // the one-byte caches have the plain kernel for H = 128 only
-    if (kvq != GQA_KV_SAME && (s.H != 128 || general)) return GQA_ERR_SHAPE;
+    // the one-byte caches have kernels for H = 128 only, and no tree mask entry
+    if (kvq != GQA_KV_SAME && (s.H != 128 || masked)) return GQA_ERR_SHAPE;
     const bool bf16 = s.dtype == GQA_BF16;
-    const int occ = resident_ctas(s.H, bf16, nt, nw, general, kvq, groups, smem);
+    int occ = resident_ctas(s.H, bf16, nt, nw, general, kvq, groups, smem);
     if (occ < 1) return GQA_ERR_CUDA;
+    if (kvq != GQA_KV_SAME) {
+        // the shallower ring where it fits more CTAs per SM (each CTA issues
+        // its stages one at a time, so more CTAs keep more stages in flight)
+        for (int st = stages - 1; st >= 2; --st) {
+            const size_t sm = smem_for(s.H, nt, nw, st, kvq, groups);
+            const int o = resident_ctas(s.H, bf16, nt, nw, general, kvq, groups, sm);
+            if (o > occ) {
+                occ = o;
+                stages = st;
+                smem = sm;
+            }
+        }
+    }
     const int sms = device_sm_count();
     if (sms < 1) return GQA_ERR_CUDA;
     // As many CTAs as fit on the GPU, also for small problems: one CTA per SM

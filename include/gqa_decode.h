@@ -142,8 +142,8 @@ typedef struct {
 /* Which attention kernel serves a call with this shape and these flags (host
  * logic only; no device work): GQA_ENGINE_WARP_MMA, GQA_ENGINE_TENSOR_MEMORY,
  * or 0 if the shape fails the common checks or a forced kernel cannot serve
- * it.  The call itself may still reject the shape for a reason of its own (a
- * window with a one-byte cache, a tree mask with T > 64). */
+ * it.  The call itself may still reject the shape for a reason of its own (H =
+ * 64 with a one-byte cache, a tree mask with T > 64). */
 #define GQA_ENGINE_WARP_MMA 1
 #define GQA_ENGINE_TENSOR_MEMORY 2
 int gqa_attention_engine(const gqa_shape *shape);
@@ -332,10 +332,14 @@ gqa_status gqa_kv_append_quant(const gqa_shape *shape, const void *k_new, const 
 /* Decode / verify attention over a one-byte cache written by
  * gqa_kv_append_quant: as gqa_decode_attention / gqa_verify_attention, with
  * K_b[j] = code * k_scale[block][k][row] (likewise V).  shape->kv_dtype is
- * GQA_KV_INT8 or GQA_KV_E4M3; requires H == 128, window == 0 and
- * T * (N/K) <= 48; k_scale / v_scale 16-byte aligned.  The products run on f16
- * tensor-core operands: q is rounded to f16 (exact for |q| in f16's normal
- * range), the codes convert exactly; fp32 accumulation. */
+ * GQA_KV_INT8 or GQA_KV_E4M3; requires H == 128 (GQA_ERR_SHAPE otherwise);
+ * k_scale / v_scale 16-byte aligned.  shape->window works as for the other
+ * attention calls (rows and scales below every new token's window are never
+ * used), and more than 48 query rows per KV head run in row chunks, each
+ * reading the KV head's blocks once.  Served by the warp-level kernel
+ * (GQA_FLAG_TENSOR_MEMORY: GQA_ERR_SHAPE).  The products run on f16 tensor-core operands: q is
+ * rounded to f16 (exact for |q| in f16's normal range), the codes convert
+ * exactly; fp32 accumulation. */
 gqa_status gqa_decode_attention_quant(const gqa_shape *shape, const void *q,
                                       const void *k_cache, const void *v_cache,
                                       const float *k_scale, const float *v_scale,

@@ -7,7 +7,7 @@ import torch
 
 import gqa_decode_attention_02_gb300 as gq
 import oracle
-from helpers import small, to
+from helpers import assert_close, small, to
 
 pytestmark = pytest.mark.gpu
 
@@ -69,12 +69,13 @@ def quant_inputs(w, kv):
     return kc, vc, ks, vs
 
 
-def run_quant(w, kv, kc, vc, ks, vs, dev, status=None):
+def run_quant(w, kv, kc, vc, ks, vs, dev, status=None, window=0, tables=None):
     wd = to(w, dev)
     fn = gq.decode_attention_quant if w.T == 1 else gq.verify_attention_quant
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
-    out = fn(wd.q[0], t(kc), t(vc), t(ks), t(vs), wd.block_tables, wd.context_lens, kv=kv,
-             status=status)
+    bt = wd.block_tables if tables is None else t(tables)
+    out = fn(wd.q[0], t(kc), t(vc), t(ks), t(vs), bt, wd.context_lens, kv=kv,
+             status=status, window=window)
     torch.cuda.synchronize()
     return out.float().cpu().double().numpy()
 
@@ -132,3 +133,68 @@ def test_quant_attention_bad_block_and_shapes(gpu):
     kc, vc, ks, vs = quant_inputs(w64, "int8")
     with pytest.raises(gq.GqaError):
         run_quant(w64, "int8", kc, vc, ks, vs, gpu)
+
+
+# ---- local attention and row chunks over a one-byte cache ---------------------------
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+@pytest.mark.parametrize("T,N,K,dtype", [(1, 32, 8, "bf16"), (5, 64, 8, "bf16"), (3, 16, 2, "f16")])
+@pytest.mark.parametrize("W", [1, 15, 17, 100, 1024])
+def test_quant_window_matches_oracle(gpu, kv, T, N, K, dtype, W):
+    ctx = tuple(max(c, T) for c in (1, 2, 15, 16, 17, 31, 295, 1029, 4097))
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype=dtype, ctx=ctx, seed=W + 7 * T + N)
+    kc, vc, ks, vs = quant_inputs(w, kv)
+    ref, err = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, dtype,
+                                window=W, kv=kv, k_scale=ks, v_scale=vs)
+    assert (err == 0).all()
+    got = run_quant(w, kv, kc, vc, ks, vs, gpu, window=W)
+    assert_close(got, ref, dtype, f"{kv} window {W} T={T}")
+
+
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+@pytest.mark.parametrize("T", [1, 4])
+def test_quant_window_ignores_poisoned_rows_and_freed_blocks(gpu, kv, T):
+    """Below the earliest window: codes of every value (e4m3 NaN codes too),
+    NaN row scales, and INT32_MAX table entries for whole blocks.  Same
+    result as the clean cache, no error."""
+    W = 40
+    ctx = (T, 45, 64, 300, 1000)
+    w = small(B=len(ctx), T=T, N=8, K=2, H=128, dtype="bf16", ctx=ctx, seed=177 + T)
+    kc, vc, ks, vs = quant_inputs(w, kv)
+    ref, _ = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, "bf16",
+                              window=W, kv=kv, k_scale=ks, v_scale=vs)
+    kc, vc, ks, vs = kc.copy(), vc.copy(), ks.copy(), vs.copy()
+    tables = w.block_tables.numpy().copy()
+    rng = np.random.default_rng(T)
+    for b, c in enumerate(ctx):
+        first = max(0, c - T - W + 1)
+        for pos in range(first):
+            blk, row = tables[b, pos // 16], pos % 16
+            kc[blk, row] = rng.integers(0, 256, size=kc[blk, row].shape)
+            vc[blk, row] = 0x7F  # the e4m3 NaN code; an ordinary code for int8
+            ks[blk, :, row] = np.nan
+            vs[blk, :, row] = np.nan
+        tables[b, : first // 16] = 2**31 - 1
+    ref2, err = oracle.attention(w.q[0], kc, vc, tables, w.context_lens, "bf16", window=W,
+                                 kv=kv, k_scale=ks, v_scale=vs)
+    assert (err == 0).all()
+    np.testing.assert_array_equal(ref2, ref)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    got = run_quant(w, kv, kc, vc, ks, vs, gpu, status=st, window=W, tables=tables)
+    assert int(st.item()) == 0
+    assert np.isfinite(got).all()
+    assert_close(got, ref, "bf16", f"{kv} poisoned window")
+
+
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+@pytest.mark.parametrize("T,N,K,W", [(4, 64, 4, 0), (7, 64, 8, 0), (5, 64, 2, 0), (4, 64, 4, 33)])
+def test_quant_row_chunks_match_oracle(gpu, kv, T, N, K, W):
+    """More than 48 query rows per KV head (T * N / K = 64, 56, 160): row
+    chunks, each reading the KV head's blocks; with and without a window."""
+    ctx = tuple(max(c, T) for c in (1, 16, 17, 300, 2049))
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype="bf16", ctx=ctx, seed=T * N + K + W)
+    kc, vc, ks, vs = quant_inputs(w, kv)
+    ref, err = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, "bf16",
+                                window=W, kv=kv, k_scale=ks, v_scale=vs)
+    assert (err == 0).all()
+    got = run_quant(w, kv, kc, vc, ks, vs, gpu, window=W)
+    assert_close(got, ref, "bf16", f"{kv} chunks T={T} N={N} K={K} W={W}")
