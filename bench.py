@@ -68,9 +68,10 @@ def parse_args(argv=None):
     ap.add_argument("--kv", default="same", choices=["same", "int8", "e4m3"],
                     help="KV cache element type: q's dtype, or one-byte int8 / e4m3 codes with "
                          "a per-row fp32 scale (quantized append + attention, H = 128)")
-    ap.add_argument("--engine", default="auto", choices=["auto", "warp", "tmem"],
-                    help="attention kernel: picked by shape (auto), the warp-level mma.sync "
-                         "kernel, or the tensor-memory (tcgen05) kernel")
+    ap.add_argument("--engine", default="auto", choices=["auto", "warp", "direct", "tmem"],
+                    help="attention kernel: picked by shape (auto), the persistent warp-level "
+                         "mma.sync kernel, the direct one (one CTA per sequence and KV head), "
+                         "or the tensor-memory (tcgen05) kernel")
     ap.add_argument("--unfused", action="store_true",
                     help="separate kv_append launches instead of the append fused into "
                          "the attention launch")
@@ -119,7 +120,7 @@ def kernel_source_hash(engine="warp"):
     import re
 
     h = hashlib.sha256()
-    files = ("attention.cu", "ptx.cuh") if engine == "warp" else (
+    files = ("attention.cu", "ptx.cuh") if engine in ("warp", "direct") else (
         "attention_tc.cu", "tcgen05.cuh", "ptx.cuh")
     for f in files:
         src = open(os.path.join(ROOT, "gqa_decode_attention_02_gb300", "csrc", f)).read()
@@ -132,7 +133,8 @@ def kernel_source_hash(engine="warp"):
 def profiled_traffic(workload, engine="warp"):
     """dram bytes per attention launch from the committed ncu summary, if it was
     taken on the current kernel source; else None."""
-    name = f"attention_{workload}" if engine == "warp" else f"tc_attention_{workload}"
+    name = {"warp": f"attention_{workload}", "direct": f"direct_attention_{workload}"}.get(
+        engine, f"tc_attention_{workload}")
     p = os.path.join(ROOT, "profiles", f"{name}_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -743,9 +745,10 @@ def run_ours(args, world, rank, local):
         "breakdown_ms": {"append": round(app_ms, 5), "attention": round(attn_ms, 5),
                          "accept": round(acc_ms, 5)},
         "roofline": {"bound": "hbm",
-                     "kernel": ("attention_kernel" if engine == "warp" else
-                                "tc_attention_kernel (tcgen05)") + (
-                                    "" if not fused else " (kv_append fused)" if engine == "warp"
+                     "kernel": {"warp": "attention_kernel", "direct": "direct_kernel"}.get(
+                                    engine, "tc_attention_kernel (tcgen05)") + (
+                                    "" if not fused else " (kv_append fused)"
+                                    if engine in ("warp", "direct")
                                     else " (with the kv_append launch of the same call)") + (
                          f" (one-byte {args.kv} cache)" if q8 else ""),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",

@@ -97,9 +97,11 @@ def kv_append_quant(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tabl
 
 
 def attention_engine(q, k_cache, block_tables, window=0, engine="auto") -> str:
-    """Which kernel serves an attention call of this shape: "warp" (mma.sync)
-    or "tmem" (tcgen05 with tensor-memory accumulators); gqa_attention_engine.
-    Host logic only.  A tree mask does not change the choice."""
+    """Which kernel serves an attention call of this shape: "warp" (the
+    persistent mma.sync kernel), "direct" (mma.sync, one CTA per sequence and
+    KV head) or "tmem" (tcgen05 with tensor-memory accumulators);
+    gqa_attention_engine.  Host logic only, for a call without a tree mask (a
+    tree mask rules "direct" out)."""
     if engine not in _lib.ENGINES:
         raise ValueError(f"engine must be one of {sorted(_lib.ENGINES)}, got {engine!r}")
     shape = _lib.make_shape(q, k_cache, block_tables, None, window=window,
@@ -107,7 +109,7 @@ def attention_engine(q, k_cache, block_tables, window=0, engine="auto") -> str:
     e = _lib.lib().gqa_attention_engine(ctypes.byref(shape))
     if e == 0:
         raise _lib.GqaError("gqa_attention_engine", _lib.Status.ERR_SHAPE)
-    return "warp" if e == 1 else "tmem"
+    return _lib.ENGINE_NAMES[e]
 
 
 def attention_workspace_size(q, k_cache, block_tables, scale=None, window=0) -> int:
@@ -164,8 +166,9 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, *, out=Non
     """gqa_decode_attention (T == 1).  q [B,1,N,H] -> out [B,1,N,H].
     pdl / early_kv select GQA_FLAG_PDL / GQA_FLAG_EARLY_KV (see the C header);
     window > 0 is local attention over each query's last `window` positions;
-    engine "warp" / "tmem" forces the mma.sync / tcgen05 kernel ("auto": by
-    shape, GQA_FLAG_WARP_MMA / GQA_FLAG_TENSOR_MEMORY)."""
+    engine "warp" / "direct" / "tmem" forces the persistent mma.sync, the
+    direct mma.sync or the tcgen05 kernel ("auto": by shape; GQA_FLAG_WARP_MMA
+    / GQA_FLAG_DIRECT / GQA_FLAG_TENSOR_MEMORY)."""
     return _attention("gqa_decode_attention", q, k_cache, v_cache, block_tables, context_lens,
                       out, scale, workspace, status, stream, pdl, early_kv, window=window,
                       engine=engine)

@@ -57,7 +57,9 @@ FLAG_PDL = 1
 FLAG_EARLY_KV = 2
 FLAG_WARP_MMA = 4
 FLAG_TENSOR_MEMORY = 8
-ENGINES = {"auto": 0, "warp": FLAG_WARP_MMA, "tmem": FLAG_TENSOR_MEMORY}
+FLAG_DIRECT = 16
+ENGINES = {"auto": 0, "warp": FLAG_WARP_MMA, "tmem": FLAG_TENSOR_MEMORY, "direct": FLAG_DIRECT}
+ENGINE_NAMES = {1: "warp", 2: "tmem", 3: "direct"}
 
 
 EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",

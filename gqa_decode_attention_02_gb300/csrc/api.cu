@@ -50,14 +50,15 @@ gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, con
     if (tree_mask && (reinterpret_cast<uintptr_t>(tree_mask) & 7u) != 0) return GQA_ERR_ALIGN;
     const bool force_warp = (s->flags & GQA_FLAG_WARP_MMA) != 0;
     const bool force_tc = (s->flags & GQA_FLAG_TENSOR_MEMORY) != 0;
-    if (force_warp && force_tc) return GQA_ERR_SHAPE;
+    const bool force_direct = (s->flags & GQA_FLAG_DIRECT) != 0;
+    if ((int)force_warp + (int)force_tc + (int)force_direct > 1) return GQA_ERR_SHAPE;
     if (force_tc && !gqa::tc_attention_supported(*s)) return GQA_ERR_SHAPE;
     gqa::AttnPlan plan;
     st = gqa::attention_plan(*s, tree_mask != nullptr, &plan);
     if (st != GQA_OK) return st;
     if (!workspace || ws_bytes < plan.workspace) return GQA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GQA_ERR_ALIGN;
-    if (force_tc || (!force_warp && gqa::tc_attention_preferred(*s))) {
+    if (force_tc || (!force_warp && !force_direct && gqa::tc_attention_preferred(*s))) {
         if (ws_bytes < gqa::tc_workspace_bytes(*s, plan.flags_bytes)) return GQA_ERR_WORKSPACE;
         cudaStream_t cs = static_cast<cudaStream_t>(stream);
         if (fused) {
@@ -137,19 +138,26 @@ int gqa_attention_engine(const gqa_shape* shape) {
     if (check_common(shape) != GQA_OK) return 0;
     const bool force_warp = (shape->flags & GQA_FLAG_WARP_MMA) != 0;
     const bool force_tc = (shape->flags & GQA_FLAG_TENSOR_MEMORY) != 0;
-    if (force_warp && force_tc) return 0;
+    const bool force_direct = (shape->flags & GQA_FLAG_DIRECT) != 0;
+    if ((int)force_warp + (int)force_tc + (int)force_direct > 1) return 0;
     if (force_tc) return gqa::tc_attention_supported(*shape) ? GQA_ENGINE_TENSOR_MEMORY : 0;
+    if (force_direct) return gqa::direct_attention_supported(*shape, false) ? GQA_ENGINE_DIRECT : 0;
     if (force_warp) return GQA_ENGINE_WARP_MMA;
-    return gqa::tc_attention_preferred(*shape) ? GQA_ENGINE_TENSOR_MEMORY : GQA_ENGINE_WARP_MMA;
+    if (gqa::tc_attention_preferred(*shape)) return GQA_ENGINE_TENSOR_MEMORY;
+    return gqa::direct_attention_preferred(*shape, false) ? GQA_ENGINE_DIRECT
+                                                          : GQA_ENGINE_WARP_MMA;
 }
 
 size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     if (check_common(shape) != GQA_OK) return 0;
-    // the largest need of the kernels that may serve the shape
+    // the largest need of the kernels that may serve the shape (the direct
+    // kernel uses none, so its flag does not change the size)
+    gqa_shape sh = *shape;
+    sh.flags &= ~GQA_FLAG_DIRECT;
     gqa::AttnPlan plain, general;
-    if (gqa::attention_plan(*shape, false, &plain) != GQA_OK) return 0;
-    if (shape->kv_dtype != GQA_KV_SAME) return plain.workspace;  // no tree mask, no tcgen05
-    if (gqa::attention_plan(*shape, true, &general) != GQA_OK) return 0;
+    if (gqa::attention_plan(sh, false, &plain) != GQA_OK) return 0;
+    if (sh.kv_dtype != GQA_KV_SAME) return plain.workspace;  // no tree mask, no tcgen05
+    if (gqa::attention_plan(sh, true, &general) != GQA_OK) return 0;
     size_t w = plain.workspace > general.workspace ? plain.workspace : general.workspace;
     const size_t tc = gqa::tc_workspace_bytes(*shape, plain.flags_bytes);  // 0: not served
     return tc > w ? tc : w;

@@ -320,6 +320,16 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         // this warp is on the critical path: no division per stage)
         int kv = k / nC, kc = k - kv * nC;
         int ids = 0, ids_base = -(1 << 30);
+        // Block ids held besides the current window: the first window of
+        // sequence ids0_b (every head's segment of a sequence starts there) and
+        // the window at pf_base of sequence pf_b, loaded eight stages before
+        // its first use -- a load on the issue path stalls every stage behind it.
+        int ids0 = 0, ids0_b = -1, ids_pf = 0, pf_base = -1, pf_b = -1;
+        auto load_ids = [&](int from) {
+            return (from + lane < nblk)
+                       ? __ldg(p.block_tables + (size_t)b * p.max_blocks + f0 + from + lane)
+                       : 0;
+        };
         auto next_ids = [&](int bn) {
             const int cn = (bn < p.B) ? __shfl_sync(FULL, ctxw, min(bn - cbase, 31)) : 0;
             const int nn =
@@ -336,10 +346,17 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
         while (x < c1) {
             const int run = (int)min((long long)min(C::kTiles, nblk - i), c1 - x);
             if (i < ids_base || i + run > ids_base + 32) {  // warp-uniform refill
+                ids = (i == pf_base && b == pf_b) ? ids_pf
+                      : (i == 0 && b == ids0_b)   ? ids0
+                                                  : load_ids(i);
                 ids_base = i;
-                ids = (i + lane < nblk)
-                          ? __ldg(p.block_tables + (size_t)b * p.max_blocks + f0 + i + lane)
-                          : 0;
+                if (i == 0) {
+                    ids0 = ids;
+                    ids0_b = b;
+                }
+                pf_base = i + 32;
+                pf_b = b;
+                ids_pf = load_ids(pf_base);
             }
             int blk[C::kTiles];
             bool bad = false;
@@ -453,8 +470,8 @@ __device__ void producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const A
                         } while (nblk == 0);
                         f0 = first_block(ctx, p.T, win);
                         if (b == b_prev + 1 && next_ok) {  // prefetched ids are b's
-                            ids = ids_next;
-                            ids_base = 0;
+                            ids0 = ids_next;
+                            ids0_b = b;
                         }
                         ids_next = next_ids(b + 1);
                         next_ok = (b + 1 < p.B) && (b + 1 - cbase < 32);
@@ -551,7 +568,9 @@ struct Consumer {
     // Start segment (b, k): reset the running state and fetch the B fragments
     // of Q^T (k = head dim, n = query row): row row0(u)+g, dims kk*16 + 2*q4 +
     // {0,1} and the same + 8.  The loads complete while the stage's tiles land.
-    __device__ void begin(const typename C::Meta& md) {
+    // holds_last: this warp will process the segment's last tile (the one that
+    // holds the new token of a fused append).
+    __device__ void begin(const typename C::Meta& md, bool holds_last) {
         cb = md.b;
         if (GENERAL) {  // md.k is the virtual head (KV head, row chunk)
             ck = md.k / p.C;
@@ -567,11 +586,8 @@ struct Consumer {
         ccta0 = md.cta_start;
         bad = false;
         if constexpr (KVQ == 0 && !GENERAL) {
-            // the segment's piece in this CTA holds the new token iff this CTA
-            // holds the segment's last tile
             constexpr int kChunks = H / 8;
-            if (p.k_new && p.T == 1 && (cstart + cnblk - 1) / cquota == (int)blockIdx.x &&
-                lane < 2 * kChunks) {
+            if (p.k_new && p.T == 1 && holds_last && lane < 2 * kChunks) {
                 const bool is_v = lane >= kChunks;
                 const size_t row = ((size_t)cb * p.K + ck) * kChunks;
                 newrow = __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) + row +
@@ -1384,7 +1400,9 @@ __device__ void consumer(const AttnParams& p, uint8_t* stages, const Bars& bar,
         const int seg = md.b * (GENERAL ? p.KC : p.K) + md.k;
         if (seg != cur) {
             if (cur >= 0 && !close()) return;
-            cs.begin(md);
+            // the segment's piece in this CTA holds the new token iff this CTA
+            // holds the segment's last tile
+            cs.begin(md, (md.seg_start + md.nblk - 1) / md.quota == (int)blockIdx.x);
             cur = seg;
         }
         if (md.flags & kBad) {
@@ -1444,6 +1462,155 @@ __global__ void __launch_bounds__(NW == 1 ? kMaxThreads : 32 * (kGroups * kMaxRo
         producer<H, GENERAL, KVQ>(&tmk, &tmv, p, stages, bar, meta, abort_flag);
     else
         consumer<H, BF16, NW, GENERAL, KVQ>(p, stages, bar, meta, scratch, abort_flag, warp);
+}
+
+// ---------------------------------------------------------------------------
+// Direct kernel, for small problems: one CTA per (b, k) segment and no split.
+// Every warp loads its own stages (four tiles each: stages w, w + W, ...) with
+// cp.async into a buffer of its own, in the layout the TMA writes (128-byte
+// swizzle), and runs the consumer's stage code on it; the warps' states are
+// combined in shared memory and warp 0 stores the rows.  The critical path is
+// one round trip for the context length and the block ids, one for the tiles
+// of every warp at once, the stages, and one combine in shared memory.  (The
+// persistent kernel's producer issues the stages one after another, and its
+// split segments meet through global memory: round trips that dominate when
+// the whole call is a few microseconds of HBM traffic.)
+template <int H>
+struct Direct {
+    static constexpr int kWarps = H == 64 ? 8 : 6;  // one 16 / 32 KB stage buffer each
+    static constexpr int kMaxStagesPerWarp = 2;     // longer segments: the persistent kernel
+};
+
+// Copy tiles 0 .. run-1 (cache blocks blk[j]) of KV head k into a stage buffer,
+// K tiles then V tiles, each row's 16-byte chunk c at chunk c ^ (row & 7) of its
+// 128-byte span; one group of cp.async per call.
+template <int H>
+__device__ void direct_load(uint32_t buf, const AttnParams& p, int k,
+                            const int (&blk)[kTilesPerStage], int run, int lane) {
+    using C = Cfg<H, 0>;
+    constexpr int kChunks = H / 8;          // 16-byte chunks per row
+    constexpr int kPerTile = 16 * kChunks;  // chunks per tile
+    const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
+    const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
+#pragma unroll
+    for (int j = 0; j < kTilesPerStage; ++j) {
+        if (j < run) {  // warp-uniform
+#pragma unroll
+            for (int x = lane; x < kPerTile; x += 32) {
+                const int r = x / kChunks, c = x % kChunks;
+                const size_t src = (((size_t)blk[j] * 16 + r) * p.K + k) * (H * 2) + c * 16;
+                const uint32_t off = (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+                cp_async_16(buf + j * C::kTileBytes + off, kc + src);
+                cp_async_16(buf + (C::kTiles + j) * C::kTileBytes + off, vc + src);
+            }
+        }
+    }
+    cp_async_commit();
+}
+
+template <int H, bool BF16>
+__global__ void __launch_bounds__(32 * Direct<H>::kWarps)
+    direct_kernel(const AttnParams p) {
+    using C = Cfg<H, 0>;
+    using CS = Consumer<H, BF16, 1, false, 0>;
+    static_assert(C::kTiles == kTilesPerStage, "stage layout of the two-byte cache");
+    constexpr int W = Direct<H>::kWarps;
+    constexpr unsigned FULL = 0xffffffffu;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_bad[W];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* scratch = reinterpret_cast<float*>(smem + (size_t)W * C::kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.x / p.K, k = blockIdx.x - b * p.K;
+    griddep_launch_dependents();
+    // Without the early-KV promise every global access waits for the grids
+    // this launch depends on; with it, the length, the block ids and the
+    // cache below position ctx - T may be read first.
+    bool waited = false;
+    if (!p.early_kv) {
+        griddep_wait();
+        waited = true;
+    }
+    const int ctx = __ldg(p.context_lens + b);
+    const int nblk = seq_blocks(ctx, p.T, p.max_blocks, 0);
+    if (nblk == 0) {  // invalid length: this KV head's rows are zeros
+        griddep_wait();
+        if (threadIdx.x == 0) report(p.status, GQA_ERR_CONTEXT);
+        constexpr int kRow16 = H * 2 / 16;
+        for (int x = threadIdx.x; x < p.T * p.G * kRow16; x += blockDim.x) {
+            const int row = x / kRow16, t = row / p.G, gg = row - t * p.G;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                                  (((size_t)b * p.T + t) * p.N +
+                                                   (size_t)k * p.G + gg) * H);
+            dst[x - row * kRow16] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    const int nst = (nblk + C::kTiles - 1) / C::kTiles;  // stages of the segment
+    const uint32_t buf = smem_addr(smem + (size_t)warp * C::kStageBytes);
+    CS cs(p, 0);  // every warp holds all (at most 8) query rows
+    typename C::Meta md;
+    md.b = b;
+    md.k = k;
+    md.ctx = ctx;
+    md.nblk = nblk;
+    md.seg_start = 0;
+    md.quota = 1 << 30;
+    md.cta_start = 0;
+    md.flags = 0;
+    bool bad = false, began = false;
+    for (int st = warp; st < nst; st += W) {  // warp-uniform
+        const int i = st * C::kTiles;
+        const int run = min(C::kTiles, nblk - i);
+        const int id = (lane < run) ? __ldg(p.block_tables + (size_t)b * p.max_blocks + i + lane)
+                                    : 0;
+        bool sbad = false;
+#pragma unroll
+        for (int j = 0; j < C::kTiles; ++j) {
+            md.blk[j] = __shfl_sync(FULL, id, j);
+            if (j < run) sbad |= (md.blk[j] < 0 || md.blk[j] >= p.num_blocks);
+        }
+        md.blk_i = i;
+        md.ntiles = run;
+        // a stage holding new positions that an earlier kernel wrote waits for it
+        if (!waited && (sbad || (!p.k_new && (i + run) * 16 > ctx - p.T))) {
+            griddep_wait();
+            waited = true;
+        }
+        if (!sbad) direct_load<H>(buf, p, k, md.blk, run, lane);
+        if (!began) {  // q (and k_new / v_new) follow the previous kernels
+            if (!waited) {
+                griddep_wait();
+                waited = true;
+            }
+            cs.begin(md, (nst - 1) % W == warp);
+            began = true;
+        }
+        if (sbad) {
+            if (lane == 0) report(p.status, GQA_ERR_BLOCK_ID);
+            bad = true;
+            continue;
+        }
+        cp_async_wait_all();
+        __syncwarp();  // every lane's copies landed before any lane reads them
+        cs.stage(buf, md);
+        __syncwarp();  // every lane done with the buffer before the next copies
+    }
+    // combine: warps 1 .. active-1 hand their states to warp 0, in warp order
+    const int active = min(W, nst);
+    if (began) cs.reduce_l();
+    if (warp > 0 && warp < active)
+        cs.save_state(scratch + ((size_t)(warp - 1) * 32 + lane) * CS::kScratchFloats);
+    if (lane == 0) s_bad[warp] = bad ? 1 : 0;
+    __syncthreads();
+    if (warp == 0) {
+        bool any_bad = false;
+        for (int w = 0; w < active; ++w) any_bad |= s_bad[w] != 0;
+        for (int w = 1; w < active; ++w)
+            cs.absorb(scratch + ((size_t)(w - 1) * 32 + lane) * CS::kScratchFloats);
+        cs.store(0, cs.l0[0], cs.l1[0], any_bad);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1623,6 +1790,66 @@ int device_sm_count() {
     return n;
 }
 
+namespace {
+
+// Dynamic shared memory of the direct kernel: a stage buffer per warp and the
+// combine scratch of every warp but the first.
+template <int H>
+size_t direct_smem_of() {
+    using C = Cfg<H, 0>;
+    constexpr int W = Direct<H>::kWarps;
+    return 1024 + (size_t)W * C::kStageBytes +
+           (size_t)(W - 1) * 32 * (4 + C::kAccFloats) * sizeof(float);
+}
+
+const void* direct_ptr(int H, bool bf16) {
+    if (H == 64)
+        return bf16 ? reinterpret_cast<const void*>(&direct_kernel<64, true>)
+                    : reinterpret_cast<const void*>(&direct_kernel<64, false>);
+    return bf16 ? reinterpret_cast<const void*>(&direct_kernel<128, true>)
+                : reinterpret_cast<const void*>(&direct_kernel<128, false>);
+}
+
+// The direct kernel's shared-memory attribute, set once per (device, variant).
+bool direct_ready(int H, bool bf16) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, bool> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const auto key = std::make_tuple(dev, H, (int)bf16);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = done.find(key);
+    if (it != done.end()) return it->second;
+    const size_t smem = H == 64 ? direct_smem_of<64>() : direct_smem_of<128>();
+    const bool ok = cudaFuncSetAttribute(direct_ptr(H, bf16),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem) == cudaSuccess;
+    done[key] = ok;
+    return ok;
+}
+
+// Segments (sequence, KV head) the direct kernel takes by default: one wave of
+// one CTA per SM on a GB300 (152 SMs).
+constexpr long long kDirectMaxSegments = 152;
+
+}  // namespace
+
+bool direct_attention_supported(const gqa_shape& s, bool masked) {
+    return s.kv_dtype == GQA_KV_SAME && !masked && s.window == 0 && s.block_size == 16 &&
+           (s.H == 64 || s.H == 128) && s.K >= 1 && s.N % s.K == 0 &&
+           (long long)s.T * (s.N / s.K) <= 8;
+}
+
+bool direct_attention_preferred(const gqa_shape& s, bool masked) {
+    if ((s.flags & (GQA_FLAG_WARP_MMA | GQA_FLAG_TENSOR_MEMORY)) != 0) return false;
+    if ((s.flags & GQA_FLAG_DIRECT) != 0) return direct_attention_supported(s, masked);
+    const long long max_tiles =
+        4LL * (s.H == 64 ? Direct<64>::kWarps * Direct<64>::kMaxStagesPerWarp
+                         : Direct<128>::kWarps * Direct<128>::kMaxStagesPerWarp);
+    return direct_attention_supported(s, masked) &&
+           (long long)s.B * s.K <= kDirectMaxSegments && s.max_blocks_per_seq <= max_tiles;
+}
+
 gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     // masked: a tree mask will be passed (the general kernel variant)
     if (s.B < 0 || s.T < 1 || s.N < 1 || s.K < 1 || s.N % s.K != 0) return GQA_ERR_SHAPE;
@@ -1698,6 +1925,16 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     plan->flags_bytes = (size_t)kMaxFlags * 4;
     plan->partial_floats_per_cta = 2 * section_floats(s.H) * nt * nw;  // two slots
     plan->workspace = plan->flags_bytes + (size_t)grid * plan->partial_floats_per_cta * 4;
+    // The direct kernel, where it serves the call (the workspace stays sized
+    // for the persistent kernel: one size for every kernel a shape may take).
+    plan->direct = direct_attention_preferred(s, masked);
+    if ((s.flags & GQA_FLAG_DIRECT) != 0 && !plan->direct) return GQA_ERR_SHAPE;
+    if (plan->direct) {
+        if (!direct_ready(s.H, bf16)) return GQA_ERR_CUDA;
+        plan->grid = s.B * s.K;
+        plan->threads = 32 * (s.H == 64 ? Direct<64>::kWarps : Direct<128>::kWarps);
+        plan->smem = s.H == 64 ? direct_smem_of<64>() : direct_smem_of<128>();
+    }
     return GQA_OK;
 }
 
@@ -1708,8 +1945,9 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
                             const float* k_scale, const float* v_scale, void* out,
                             void* workspace, int32_t* dev_status, cudaStream_t stream) {
     if (s.B == 0) return GQA_OK;
-    CUtensorMap tmk, tmv;
-    if (!encode_cache_map(&tmk, k_cache, s) || !encode_cache_map(&tmv, v_cache, s))
+    CUtensorMap tmk, tmv;  // (the direct kernel copies with cp.async: no tensor maps)
+    if (!plan.direct &&
+        (!encode_cache_map(&tmk, k_cache, s) || !encode_cache_map(&tmv, v_cache, s)))
         return GQA_ERR_CUDA;
     AttnParams p;
     p.q = q;
@@ -1757,6 +1995,13 @@ gqa_status launch_attention(const gqa_shape& s, const AttnPlan& plan, const void
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if (plan.direct) {
+        if (tree_mask || s.window > 0 || s.kv_dtype != GQA_KV_SAME)
+            return GQA_ERR_SHAPE;  // plan made for another call
+        void* dargs[] = {&p};
+        const cudaError_t e = cudaLaunchKernelExC(&cfg, direct_ptr(s.H, bf16), dargs);
+        return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
+    }
     const int nw = plan.tiles_per_warp;
     if ((tree_mask || s.window > 0 || plan.chunks > 1) && !plan.general)
         return GQA_ERR_SHAPE;  // plan made for another call

@@ -25,6 +25,9 @@ struct AttnPlan {
     size_t flags_bytes;             // fixed region of publication flags
     size_t partial_floats_per_cta;
     size_t workspace;    // total bytes
+    // The direct kernel serves the call instead (one CTA per segment, no
+    // workspace use; grid, threads and smem above are then its own).
+    bool direct;
 };
 
 // Fills `plan`; `masked`: a tree mask will be passed.  The plan picks the plain
@@ -78,6 +81,10 @@ bool make_rows_map(CUtensorMap* m, const void* base, const gqa_shape& s, int hpc
 // first).  `preferred`: the shapes where it is the faster of the two kernels.
 // The workspace holds the publication flags (flags_bytes, as the warp-level
 // kernel's plan lays them out) and then the partial results of split segments.
+// The direct warp-level kernel (one CTA per (sequence, KV head)): which
+// shapes it can serve, and which it serves by default.  Host logic only.
+bool direct_attention_supported(const gqa_shape& s, bool masked);
+bool direct_attention_preferred(const gqa_shape& s, bool masked);
 bool tc_attention_supported(const gqa_shape& s);
 bool tc_attention_preferred(const gqa_shape& s);
 size_t tc_workspace_bytes(const gqa_shape& s, size_t flags_bytes);

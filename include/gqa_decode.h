@@ -131,21 +131,34 @@ typedef struct {
 /* Attention only: which kernel computes the call.  By default the library
  * picks by shape: the tensor-memory kernel (tcgen05.mma, accumulators in
  * tensor memory, 128 query rows of one KV head per tile) where a KV head has
- * many query rows (T * N / K >= 32), the warp-level mma.sync kernel otherwise.
- * GQA_FLAG_WARP_MMA forces the warp-level kernel; GQA_FLAG_TENSOR_MEMORY
- * forces the tensor-memory one, which serves H = 128 with a cache in q's dtype
- * and no window (GQA_ERR_SHAPE otherwise, or with both flags).  Both compute
- * the same function; results differ only by rounding order. */
+ * many query rows (T * N / K >= 32); for small calls -- a cache in q's dtype,
+ * T * N / K <= 8, no window, no tree mask, B * K <= 152 and max_blocks_per_seq
+ * <= 64 (H = 64) or 48 (H = 128) -- the direct warp-level kernel (one CTA per
+ * (sequence, KV head), every warp loading its own cache blocks, no split of a
+ * context over CTAs); the persistent warp-level mma.sync kernel (contexts split
+ * evenly over all SMs, pieces merged through the workspace) otherwise.
+ * GQA_FLAG_WARP_MMA forces the persistent warp-level kernel;
+ * GQA_FLAG_TENSOR_MEMORY forces the tensor-memory one, which serves H = 128
+ * with a cache in q's dtype and no window; GQA_FLAG_DIRECT forces the direct
+ * one, which serves a cache in q's dtype with T * N / K <= 8, no window and no
+ * tree mask, at any context length (GQA_ERR_SHAPE where the forced kernel
+ * cannot serve the call, or with more than one of the flags).  All compute the
+ * same function; results differ only by rounding order.  The workspace size
+ * does not depend on the kernel. */
 #define GQA_FLAG_WARP_MMA 4u
 #define GQA_FLAG_TENSOR_MEMORY 8u
+#define GQA_FLAG_DIRECT 16u
 
 /* Which attention kernel serves a call with this shape and these flags (host
- * logic only; no device work): GQA_ENGINE_WARP_MMA, GQA_ENGINE_TENSOR_MEMORY,
- * or 0 if the shape fails the common checks or a forced kernel cannot serve
- * it.  The call itself may still reject the shape for a reason of its own (H =
- * 64 with a one-byte cache, a tree mask with T > 64). */
+ * logic only; no device work), for a call without a tree mask (a tree mask
+ * rules the direct kernel out): GQA_ENGINE_WARP_MMA (persistent warp-level),
+ * GQA_ENGINE_TENSOR_MEMORY, GQA_ENGINE_DIRECT, or 0 if the shape fails the
+ * common checks or a forced kernel cannot serve it.  The call itself may still
+ * reject the shape for a reason of its own (H = 64 with a one-byte cache, a
+ * tree mask with T > 64). */
 #define GQA_ENGINE_WARP_MMA 1
 #define GQA_ENGINE_TENSOR_MEMORY 2
+#define GQA_ENGINE_DIRECT 3
 int gqa_attention_engine(const gqa_shape *shape);
 
 /* Library version (major*10000 + minor*100 + patch). */

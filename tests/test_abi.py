@@ -108,7 +108,21 @@ def test_empty_batch_is_a_no_op(cuda_lib):
 
 
 @pytest.mark.parametrize("kw,want", [
-    (dict(T=1, N=32, K=8), 1),                 # 4 query rows per KV head: warp-level mma
+    (dict(T=1, N=32, K=8), 3),                 # 4 rows per KV head, a small call: direct
+    (dict(T=2, N=32, K=8), 3),                 # 8 rows: direct
+    (dict(T=3, N=32, K=8), 1),                 # 12 rows: persistent warp-level
+    (dict(T=1, N=32, K=8, B=19), 3),           # 152 segments: direct
+    (dict(T=1, N=32, K=8, B=20), 1),           # 160 segments: persistent
+    (dict(T=1, N=32, K=8, max_blocks_per_seq=48), 3),  # H = 128 up to 48 blocks
+    (dict(T=1, N=32, K=8, max_blocks_per_seq=49), 1),
+    (dict(T=1, N=32, K=8, H=64, max_blocks_per_seq=64), 3),  # H = 64 up to 64 blocks
+    (dict(T=1, N=32, K=8, H=64, max_blocks_per_seq=65), 1),
+    (dict(T=1, N=32, K=8, window=8), 1),       # a window: persistent
+    (dict(T=1, N=32, K=8, kv_dtype=1), 1),     # one-byte cache: persistent
+    (dict(T=1, N=32, K=8, flags=4), 1),        # GQA_FLAG_WARP_MMA: persistent
+    (dict(T=1, N=32, K=8, B=500, max_blocks_per_seq=1000, flags=16), 3),  # GQA_FLAG_DIRECT
+    (dict(T=5, N=64, K=8, flags=16), 0),       # forced direct, 40 rows: not served
+    (dict(T=1, N=32, K=8, flags=20), 0),       # two forced
     (dict(T=5, N=64, K=8), 2),                 # 40 rows: tensor memory
     (dict(T=4, N=64, K=8), 2),                 # 32 rows: tensor memory (threshold)
     (dict(T=3, N=64, K=8), 1),                 # 24 rows: warp-level
@@ -135,7 +149,8 @@ def test_attention_engine_python_binding(cuda_lib):
     verify = torch.zeros(2, 5, 64, 128, dtype=torch.bfloat16)   # 40 rows per KV head
     decode = torch.zeros(2, 1, 32, 128, dtype=torch.bfloat16)   # 4 rows per KV head
     assert gq.attention_engine(verify, kc, bt) == "tmem"
-    assert gq.attention_engine(decode, kc, bt) == "warp"
+    assert gq.attention_engine(decode, kc, bt) == "direct"
+    assert gq.attention_engine(decode, kc, bt, engine="warp") == "warp"
     assert gq.attention_engine(verify, kc, bt, engine="warp") == "warp"
     assert gq.attention_engine(verify, kc, bt, window=64) == "warp"
     with pytest.raises(gq.GqaError):  # H = 64 cannot be forced onto tensor memory

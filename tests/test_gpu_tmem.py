@@ -211,13 +211,14 @@ def test_tmem_early_kv_after_append_is_bit_identical(gpu, tree):
 
 
 def test_engine_choice_by_shape(gpu):
-    """auto = tensor memory from 32 rows per KV head, warp-level below:
-    bit-identical to the forced engine in each case."""
+    """auto = tensor memory from 32 rows per KV head, a warp-level kernel
+    below: bit-identical to the forced engine in each case."""
     for T, N, K in ((1, 32, 8), (3, 64, 8), (4, 64, 8), (5, 64, 8), (1, 64, 1), (26, 64, 8)):
         ctx = tuple(max(c, T) for c in (1, 100, 2000))
         w = small(B=3, T=T, N=N, K=K, H=128, dtype="bf16", ctx=ctx, seed=T + N)
         auto = run(w, gpu, engine="auto")
-        pick = "tmem" if T * (N // K) >= 32 else "warp"
+        pick = gq.attention_engine(w.q[0], w.k_cache[0], w.block_tables)
+        assert (pick == "tmem") == (T * (N // K) >= 32), (T, N, K, pick)
         assert torch.equal(auto, run(w, gpu, engine=pick)), (T, N, K)
 
 
