@@ -132,7 +132,7 @@ typedef struct {
  * picks by shape: the tensor-memory kernel (tcgen05.mma, accumulators in
  * tensor memory, 128 query rows of one KV head per tile) where a KV head has
  * many query rows (T * N / K >= 32); for small calls -- a cache in q's dtype,
- * T * N / K <= 8, no window, no tree mask, B * K <= 152 and max_blocks_per_seq
+ * T * N / K <= 8, no window, no tree mask, B * K <= 304 and max_blocks_per_seq
  * <= 64 (H = 64) or 48 (H = 128) -- the direct warp-level kernel (one CTA per
  * (sequence, KV head), every warp loading its own cache blocks, no split of a
  * context over CTAs); the persistent warp-level mma.sync kernel (contexts split

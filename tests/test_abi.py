@@ -111,8 +111,8 @@ def test_empty_batch_is_a_no_op(cuda_lib):
     (dict(T=1, N=32, K=8), 3),                 # 4 rows per KV head, a small call: direct
     (dict(T=2, N=32, K=8), 3),                 # 8 rows: direct
     (dict(T=3, N=32, K=8), 1),                 # 12 rows: persistent warp-level
-    (dict(T=1, N=32, K=8, B=19), 3),           # 152 segments: direct
-    (dict(T=1, N=32, K=8, B=20), 1),           # 160 segments: persistent
+    (dict(T=1, N=32, K=8, B=38), 3),           # 304 segments: direct
+    (dict(T=1, N=32, K=8, B=39), 1),           # 312 segments: persistent
     (dict(T=1, N=32, K=8, max_blocks_per_seq=48), 3),  # H = 128 up to 48 blocks
     (dict(T=1, N=32, K=8, max_blocks_per_seq=49), 1),
     (dict(T=1, N=32, K=8, H=64, max_blocks_per_seq=64), 3),  # H = 64 up to 64 blocks
