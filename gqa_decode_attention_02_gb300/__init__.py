@@ -26,7 +26,8 @@ from . import _lib
 from ._lib import GqaError, Shape, Status, status_string  # noqa: F401
 
 __all__ = ["kv_append", "kv_append_quant", "decode_attention", "verify_attention",
-           "decode_attention_quant", "verify_attention_quant", "append_decode_attention",
+           "decode_attention_quant", "verify_attention_quant", "append_decode_attention_quant",
+           "append_verify_attention_quant", "append_decode_attention",
            "append_verify_attention", "accept_prefix", "accept_sampled",
            "attention_workspace_size", "reset_workspaces", "GqaError", "Status", "Shape"]
 
@@ -255,6 +256,62 @@ def verify_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
     return _attention_quant("gqa_verify_attention_quant", q, k_cache, v_cache, k_scale, v_scale,
                             block_tables, context_lens, out, scale, workspace, status, stream,
                             pdl, early_kv, kv, window)
+
+
+def _append_attention_quant(fn_name, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                            block_tables, context_lens, out, scale, workspace, status, stream,
+                            pdl, early_kv, kv, window):
+    _lib._need(q, "q", ndim=4)
+    _lib._need(k_new, "k_new", q.dtype, 4)
+    _lib._need(v_new, "v_new", q.dtype, 4)
+    _need_quant_cache(k_cache, k_scale, "k_cache")
+    _need_quant_cache(v_cache, v_scale, "v_cache")
+    _lib._need(block_tables, "block_tables", torch.int32, 2)
+    _lib._need(context_lens, "context_lens", torch.int32, 1)
+    flags = (_lib.FLAG_PDL if pdl else 0) | (_lib.FLAG_EARLY_KV if early_kv else 0)
+    shape = _lib.make_shape(q, k_cache, block_tables, scale, flags=flags, window=window, kv=kv)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _lib._need(out, "out", q.dtype, 4)
+    nbytes = _lib.workspace_size(shape)
+    if workspace is None:
+        workspace = _lib.get_workspace(nbytes, q.device, stream)
+    else:
+        _lib._need(workspace, "workspace", torch.uint8)
+    P = _lib._ptr
+    rc = getattr(_lib.lib(), fn_name)(ctypes.byref(shape), P(q), P(k_new), P(v_new),
+                                      P(k_cache), P(v_cache), P(k_scale), P(v_scale),
+                                      P(block_tables), P(context_lens), P(out), P(workspace),
+                                      workspace.numel(), _status_arg(status),
+                                      _lib._stream(stream))
+    _lib._check(fn_name, rc)
+    return out
+
+
+def append_decode_attention_quant(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                  block_tables, context_lens, *, kv="int8", out=None,
+                                  scale=None, workspace=None, status=None, stream=None,
+                                  pdl=False, early_kv=False, window=0):
+    """gqa_append_decode_attention_quant: kv_append_quant of the new token and
+    decode attention over the one-byte cache in one call (two launches; the
+    caches and their scales are written)."""
+    return _append_attention_quant("gqa_append_decode_attention_quant", q, k_new, v_new,
+                                   k_cache, v_cache, k_scale, v_scale, block_tables,
+                                   context_lens, out, scale, workspace, status, stream, pdl,
+                                   early_kv, kv, window)
+
+
+def append_verify_attention_quant(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                                  block_tables, context_lens, *, kv="int8", out=None,
+                                  scale=None, workspace=None, status=None, stream=None,
+                                  pdl=False, early_kv=False, window=0):
+    """gqa_append_verify_attention_quant: the T new tokens appended to the
+    one-byte cache and verify attention over it, in one call (two launches)."""
+    return _append_attention_quant("gqa_append_verify_attention_quant", q, k_new, v_new,
+                                   k_cache, v_cache, k_scale, v_scale, block_tables,
+                                   context_lens, out, scale, workspace, status, stream, pdl,
+                                   early_kv, kv, window)
 
 
 def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,

@@ -67,7 +67,9 @@ EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_verify_attention", "gqa_append_decode_attention", "gqa_append_verify_attention",
            "gqa_accept_workspace_size", "gqa_accept_prefix", "gqa_accept_sampled", "gqa_tree_verify_attention",
            "gqa_append_tree_verify_attention", "gqa_kv_append_quant",
-           "gqa_decode_attention_quant", "gqa_verify_attention_quant", "gqa_attention_engine")
+           "gqa_decode_attention_quant", "gqa_verify_attention_quant",
+           "gqa_append_decode_attention_quant", "gqa_append_verify_attention_quant",
+           "gqa_attention_engine")
 
 
 def lib() -> ctypes.CDLL:
@@ -110,6 +112,10 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = I
             f.argtypes = [S] + [P] * 9 + [ctypes.c_size_t, P, P]
+        for name in ("gqa_append_decode_attention_quant", "gqa_append_verify_attention_quant"):
+            f = getattr(L, name)
+            f.restype = I
+            f.argtypes = [S] + [P] * 11 + [ctypes.c_size_t, P, P]
         L.gqa_accept_workspace_size.restype = ctypes.c_size_t
         L.gqa_accept_workspace_size.argtypes = [I, I]
         L.gqa_accept_prefix.restype = I

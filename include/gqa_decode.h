@@ -10,6 +10,8 @@
  *   gqa_accept_prefix    greedy longest-prefix acceptance of draft tokens
  *   gqa_kv_append_quant  the append into a one-byte (int8 / e4m3) cache, and
  *   gqa_decode_attention_quant / gqa_verify_attention_quant  attention over it
+ *   gqa_append_decode_attention_quant / gqa_append_verify_attention_quant  both
+ *                        in one call
  *   gqa_accept_sampled   stochastic acceptance of draft tokens (speculative
  *                        sampling: modified rejection sampling)
  *
@@ -367,6 +369,30 @@ gqa_status gqa_verify_attention_quant(const gqa_shape *shape, const void *q,
                                       const int32_t *context_lens, void *out, void *workspace,
                                       size_t workspace_bytes, int32_t *dev_status,
                                       void *stream);
+
+/* The append and the one-byte attention in one call: gqa_kv_append_quant
+ * followed by gqa_decode_attention_quant / gqa_verify_attention_quant on the
+ * same stream, as two launches (the attention launch chained to the append by
+ * programmatic dependent launch when the flags ask for it).  k_new / v_new
+ * [B][T][K][H] in the dtype of the shape.  (A one-launch form, with the new
+ * rows quantized inside the attention kernel, measured slower than the two
+ * launches on a 256-sequence int8 batch: that kernel is bound by its producer
+ * warp's issue rate and its consumer warps' registers.)  Requirements, flags
+ * and device errors as the two calls. */
+gqa_status gqa_append_decode_attention_quant(const gqa_shape *shape, const void *q,
+                                             const void *k_new, const void *v_new,
+                                             void *k_cache, void *v_cache, float *k_scale,
+                                             float *v_scale, const int32_t *block_tables,
+                                             const int32_t *context_lens, void *out,
+                                             void *workspace, size_t workspace_bytes,
+                                             int32_t *dev_status, void *stream);
+gqa_status gqa_append_verify_attention_quant(const gqa_shape *shape, const void *q,
+                                             const void *k_new, const void *v_new,
+                                             void *k_cache, void *v_cache, float *k_scale,
+                                             float *v_scale, const int32_t *block_tables,
+                                             const int32_t *context_lens, void *out,
+                                             void *workspace, size_t workspace_bytes,
+                                             int32_t *dev_status, void *stream);
 
 /* Greedy prefix acceptance.  Speculative-decoding section of "جعل inference
  * رخيصًا" (a drafted token is kept only if the target would produce it) and

@@ -97,6 +97,20 @@ def test_validation_rejects_null_and_misaligned(cuda_lib):
     assert rc == 2
 
 
+def test_fused_quant_entry_points_check_their_arguments(cuda_lib):
+    fake = ctypes.c_void_p(16)
+    s = _shape(kv_dtype=1)
+    for name in ("gqa_append_decode_attention_quant", "gqa_append_verify_attention_quant"):
+        f = getattr(cuda_lib, name)
+        # missing scale arrays
+        assert f(ctypes.byref(s), fake, fake, fake, fake, fake, None, fake, fake, fake, fake,
+                 fake, 1 << 20, None, None) == 1
+        # a two-byte cache shape with scales: dtype mismatch
+        plain = _shape()
+        assert f(ctypes.byref(plain), fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                 fake, fake, 1 << 20, None, None) == 3
+
+
 def test_empty_batch_is_a_no_op(cuda_lib):
     s = _shape(B=0)
     rc = cuda_lib.gqa_kv_append(ctypes.byref(s), None, None, None, None, None, None, None,

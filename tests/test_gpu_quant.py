@@ -198,3 +198,52 @@ def test_quant_row_chunks_match_oracle(gpu, kv, T, N, K, W):
     assert (err == 0).all()
     got = run_quant(w, kv, kc, vc, ks, vs, gpu, window=W)
     assert_close(got, ref, "bf16", f"{kv} chunks T={T} N={N} K={K} W={W}")
+
+
+# ---- the append fused into the one-byte attention call --------------------------------
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+@pytest.mark.parametrize("T,N,K,dtype,W", [(1, 32, 8, "bf16", 0), (1, 8, 2, "f16", 0),
+                                           (5, 64, 8, "bf16", 0), (3, 16, 2, "bf16", 40),
+                                           (4, 64, 4, "bf16", 0)])
+def test_fused_quant_append_matches_oracle_and_the_pair(gpu, kv, T, N, K, dtype, W):
+    """One call (the append launch, then the attention launch): the new rows
+    quantized (codes and scales bit-exact with the oracle's append), attention
+    over them within tolerance of the oracle, and the same bits as the two
+    calls made separately.  Covers a window and row chunks (64 query rows per
+    KV head), with and without programmatic dependent launch."""
+    ctx = tuple(max(c, T) for c in (1, 16, 17, 33, 300, 2049))
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype=dtype, ctx=ctx, seed=T * N + K + W,
+              append=True)
+    kc, vc, ks, vs = quant_inputs(w, kv)  # the cached part (new slots hold NaN -> zeros)
+    rk, rv, rks, rvs, err = oracle.kv_append_quant(w.k_new[0], w.v_new[0], kc, vc, ks, vs,
+                                                   w.block_tables, w.context_lens, dtype, kv)
+    assert (err == 0).all()
+    ref, err = oracle.attention(w.q[0], rk, rv, w.block_tables, w.context_lens, dtype,
+                                window=W, kv=kv, k_scale=rks, v_scale=rvs)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(gpu)  # noqa: E731
+    fused = gq.append_decode_attention_quant if T == 1 else gq.append_verify_attention_quant
+    outs = []
+    for flags in (dict(), dict(pdl=True, early_kv=True)):
+        dkc, dvc, dks, dvs = t(kc), t(vc), t(ks), t(vs)
+        st = torch.zeros(1, dtype=torch.int32, device=gpu)
+        out = fused(wd.q[0], wd.k_new[0], wd.v_new[0], dkc, dvc, dks, dvs, wd.block_tables,
+                    wd.context_lens, kv=kv, status=st, window=W, **flags)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        np.testing.assert_array_equal(dkc.cpu().numpy(), rk)
+        np.testing.assert_array_equal(dvc.cpu().numpy(), rv)
+        np.testing.assert_array_equal(dks.cpu().numpy().view(np.uint32), rks.view(np.uint32))
+        np.testing.assert_array_equal(dvs.cpu().numpy().view(np.uint32), rvs.view(np.uint32))
+        assert_close(out.float().cpu().double().numpy(), ref, dtype, f"fused {kv} T={T} W={W}")
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    # the separate append, then attention: the same bits
+    dkc, dvc, dks, dvs = t(kc), t(vc), t(ks), t(vs)
+    gq.kv_append_quant(wd.k_new[0], wd.v_new[0], dkc, dvc, dks, dvs, wd.block_tables,
+                       wd.context_lens, kv=kv)
+    attn = gq.decode_attention_quant if T == 1 else gq.verify_attention_quant
+    pair = attn(wd.q[0], dkc, dvc, dks, dvs, wd.block_tables, wd.context_lens, kv=kv, window=W)
+    torch.cuda.synchronize()
+    assert torch.equal(pair.view(torch.int16), outs[0].view(torch.int16))
