@@ -91,6 +91,31 @@ def test_attention_next_to_a_gemm_that_holds_sms(gpu):
     assert_close(got_b.double().cpu().numpy(), _oracle(wb), "bf16", "next to a GEMM")
 
 
+def test_direct_kernel_next_to_a_split_one_on_two_streams(gpu):
+    """A small call (the direct kernel: one CTA per sequence and KV head) and
+    a large one (the persistent kernel, split segments) overlapping on two
+    streams, three times without syncing: every output equals the oracle's and
+    the same call run alone."""
+    small_w = small(B=3, T=1, N=14, K=2, H=64, dtype="f16", ctx=(1, 295, 1000), seed=93)
+    big_w, _ = _cases()
+    ds, db = to(small_w, gpu), to(big_w, gpu)
+    assert gq.attention_engine(small_w.q[0], small_w.k_cache[0], small_w.block_tables) == "direct"
+    sa, sb = torch.cuda.Stream(gpu), torch.cuda.Stream(gpu)
+    st = torch.zeros(2, dtype=torch.int32, device=gpu)
+    torch.cuda.synchronize()
+    outs = [(_call(ds, sa, status=st[0:1]), _call(db, sb, status=st[1:2])) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert st.tolist() == [0, 0]
+    rs, rb = _oracle(small_w), _oracle(big_w)
+    for os_, ob in outs:
+        assert_close(os_.double().cpu().numpy(), rs, "f16", "direct, stream A")
+        assert_close(ob.double().cpu().numpy(), rb, "bf16", "persistent, stream B")
+        assert torch.equal(os_, outs[0][0]) and torch.equal(ob, outs[0][1])
+    alone = _call(ds, torch.cuda.current_stream(gpu))
+    torch.cuda.synchronize()
+    assert torch.equal(alone, outs[0][0])
+
+
 def test_binding_keeps_one_workspace_per_stream(gpu):
     from gqa_decode_attention_02_gb300 import _lib
 

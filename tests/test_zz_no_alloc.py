@@ -1,7 +1,8 @@
 """gqa_decode_attention_noalloc: decode attention for callers that cannot
 allocate device memory (a host program whose memory is all in its own pool, a
 decode loop that must not let cudaMalloc synchronise the device).  Called
-through the C ABI on two calls in a row, of different shapes; each output must
+through the C ABI on three calls in a row, of different shapes (the last one
+small enough for the direct kernel); each output must
 match the fp64 oracle, and gqa_decode_attention's output, within the parity
 tolerance.  Collected last on purpose, so that a run stopping at the first
 failure has run every other test already."""
@@ -30,7 +31,7 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def test_noalloc_matches_oracle_and_workspace_entry_point_on_two_calls(gpu):
+def test_noalloc_matches_oracle_and_workspace_entry_point_on_calls_in_a_row(gpu):
     f = _entry()
     cases = [
         # ragged bf16 batch with long contexts: split sequences, merged pieces
@@ -38,6 +39,8 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_on_two_calls(gpu):
               seed=61),
         # then an fp16 H=64 batch of another shape, on the same static scratch
         small(B=5, T=1, N=14, K=2, H=64, dtype="f16", ctx=(1, 295, 1024, 17, 3000), seed=62),
+        # and a small call, served by the direct kernel (no scratch used)
+        small(B=2, T=1, N=14, K=2, H=64, dtype="f16", ctx=(295, 40), seed=63),
     ]
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for w in cases:
