@@ -349,13 +349,13 @@ def parity_sample(w, outs, quant=None, inputs=None, n_seq=8, seed=1234):
         got = outs[layer][torch_index(bl, outs[layer].device)].double().cpu().numpy()
         d = np.abs(got - ref)
         a = np.abs(ref)
-        half_ulp = 0.5 * np.exp2(np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))),
-                                            -14 if w.dtype == "f16" else -126) - mant)
-        ok &= bool(np.isfinite(got).all() and (d <= np.maximum(tol, half_ulp)).all()
+        one_ulp = np.exp2(np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))),
+                                     -14 if w.dtype == "f16" else -126) - mant)
+        ok &= bool(np.isfinite(got).all() and (d <= np.maximum(tol, one_ulp)).all()
                    and (err == 0).all())
         worst = max(worst, float(d.max()) if d.size else 0.0)
     return {"max_abs_err": worst, "parity_pass": ok, "tol": tol,
-            "rule": "|gpu - oracle| <= max(tol, half an ulp of the oracle value in the dtype)",
+            "rule": "|gpu - oracle| <= max(tol, one ulp of the oracle value in the dtype)",
             "sample": f"sequences {bl.tolist()} (shortest and longest included) of layers "
                       f"{layers}, the timed step's outputs vs the fp64 oracle"}
 

@@ -105,6 +105,7 @@ struct TcParams {
     int tpc, hpc, cpt, C, Rc, KC;
     int max_blocks, num_blocks;
     int early;                  // GQA_FLAG_EARLY_KV: plan and stream older positions before the wait
+    int window;                 // local attention: each query sees its last `window` positions (0: all)
     float scale_log2;
 };
 
@@ -131,8 +132,17 @@ struct TcSmem {
     int ctxc[kCtxCache];        // context_lens[b0 + i]: no dependent global load at a piece change
 };
 
+// First logical block a segment reads: the one holding the earliest position
+// any of its T new tokens sees (0 without a window).
+__device__ __forceinline__ int tc_first(const TcParams& p, int ctx) {
+    return p.window > 0 ? max(0, ctx - p.T - p.window + 1) >> 4 : 0;
+}
+// Tiles of a segment: logical blocks tc_first .. ceil(ctx / 16) - 1 (0 for an
+// invalid length).
 __device__ __forceinline__ int tc_nblk_of(const TcParams& p, int ctx) {
-    return (ctx >= p.T && ctx >= 1 && ctx <= p.max_blocks * 16) ? (ctx + 15) >> 4 : 0;
+    return (ctx >= p.T && ctx >= 1 && ctx <= p.max_blocks * 16)
+               ? ((ctx + 15) >> 4) - tc_first(p, ctx)
+               : 0;
 }
 __device__ __forceinline__ int tc_nblk(const TcParams& p, int b) {
     return tc_nblk_of(p, __ldg(p.context_lens + b));
@@ -186,6 +196,7 @@ __device__ __forceinline__ bool softmax_bar(TcSmem& sm, int& ph) {
 // `first` of the whole order and which has nb tiles.
 struct TcPiece {
     int b, v, nb, t0, t1;
+    int f0;  // logical block of the segment's tile 0 (the window's first block)
     long long first;
 };
 
@@ -220,6 +231,7 @@ struct TcWalker {
                 pc.nb = nb;
                 pc.t0 = (int)(s0 - tile0);
                 pc.t1 = (int)(e - tile0);
+                pc.f0 = p.window > 0 ? tc_first(p, tc_ctx(*sm, p, b)) : 0;
                 pc.first = tile0;
                 return true;
             }
@@ -313,7 +325,7 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
     bool waited = !p.early;  // with early KV: only positions below ctx - T before the wait
     while (!aborted && wk.next(p, pc)) {
         const int kv = pc.v / p.C;
-        const int32_t* table = p.block_tables + (size_t)pc.b * p.max_blocks;
+        const int32_t* table = p.block_tables + (size_t)pc.b * p.max_blocks + pc.f0;
         const int newpos = tc_ctx(sm, p, pc.b) - p.T;  // the first of the T newest positions
         int win = pc.t0;  // first tile of the current window
         int ids = (win + lane < pc.t1) ? __ldg(table + win + lane) : 0;
@@ -325,7 +337,7 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
                 nxt = (win + 32 + lane < pc.t1) ? __ldg(table + win + 32 + lane) : 0;
             }
             const int tiles = min(4, pc.t1 - blk0);
-            if (!waited && (blk0 + tiles) * 16 > newpos) {  // the stage holds a new position
+            if (!waited && (pc.f0 + blk0 + tiles) * 16 > newpos) {  // the stage holds a new position
                 griddep_wait();
                 waited = true;
             }
@@ -644,7 +656,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             ok = __all_sync(FULLM, ok);  // warp-collective tensor-memory accesses follow
             if (!ok) break;
             const int blk0 = pc.t0 + 4 * st;
-            const int tok0 = blk0 * 16;
+            const int tok0 = (pc.f0 + blk0) * 16;
             const int tiles = min(4, pc.t1 - blk0);
             bad |= sm.bad[s] != 0;
             if (warp_active) {
@@ -656,6 +668,10 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
                 // visible columns of the stage as one word: loaded and causal ...
                 const int vis_end = min(tiles * 16, lim + 1 - tok0);
                 uint64_t vm = vis_end >= 64 ? ~0ull : vis_end <= 0 ? 0ull : (1ull << vis_end) - 1;
+                if (p.window > 0) {  // ... above the row's window: lim - window < position
+                    const int vis_beg = lim - p.window + 1 - tok0;
+                    if (vis_beg > 0) vm &= vis_beg >= 64 ? 0ull : ~((1ull << vis_beg) - 1);
+                }
                 if (p.tree_mask) {  // ... and, among the new positions, on the row's tree path
                     const int d = fn - tok0;  // stage column of the first new token
                     if (d < 64) {
@@ -717,12 +733,19 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
                 tmem_st32(tP, pw);
                 tmem_wait_st();
             }  // warp_active
-            // V rows without data in this stage: zero them (NaN-safe products)
+            // V rows without data in this stage -- past the context, or below
+            // every new token's window (a block partly inside it may hold
+            // anything there): zero them (NaN-safe products)
             const int valid_rows = max(0, min(tiles * 16, ctx - tok0));
-            if (valid_rows < 64) {
+            const int low_rows =
+                p.window > 0 ? min(valid_rows, max(0, fn - p.window + 1 - tok0)) : 0;
+            if (valid_rows < 64 || low_rows > 0) {
                 const uint32_t vb = smem_addr(stages + (size_t)s * kStageBytesTc) + 2 * kHalfBytes;
-                for (int i = tg; i < (64 - valid_rows) * 16; i += kGroupThreads) {
-                    const int rr = valid_rows + (i >> 4), c = i & 15, h = c >> 3, cc = c & 7;
+                const int nz = 64 - valid_rows + low_rows;  // rows [0, low) and [valid, 64)
+                for (int i = tg; i < nz * 16; i += kGroupThreads) {
+                    const int k = i >> 4;
+                    const int rr = k < low_rows ? k : valid_rows + (k - low_rows);
+                    const int c = i & 15, h = c >> 3, cc = c & 7;
                     st_shared_v4(vb + h * kHalfBytes + (rr >> 3) * 1024 + (rr & 7) * 128 +
                                      ((cc ^ (rr & 7)) << 4),
                                  make_uint4(0, 0, 0, 0));
@@ -951,7 +974,7 @@ static_assert(kSmemTc <= 227 * 1024, "shared memory per CTA");
 }  // namespace
 
 bool tc_attention_supported(const gqa_shape& s) {
-    return s.H == 128 && s.kv_dtype == GQA_KV_SAME && s.window == 0 && s.block_size == 16 &&
+    return s.H == 128 && s.kv_dtype == GQA_KV_SAME && s.block_size == 16 &&
            (long long)s.T * (s.N / s.K) <= 8192;
 }
 
@@ -1031,6 +1054,7 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
     p.max_blocks = s.max_blocks_per_seq;
     p.num_blocks = s.num_blocks;
     p.early = (s.flags & GQA_FLAG_EARLY_KV) ? 1 : 0;
+    p.window = s.window;
     const double scale = s.scale > 0.f ? (double)s.scale : 1.0 / sqrt((double)s.H);
     p.scale_log2 = (float)(scale * 1.4426950408889634);
     const int sms = device_sm_count();

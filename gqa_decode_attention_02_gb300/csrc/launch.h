@@ -76,15 +76,16 @@ bool make_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s);
 // Elements outside the tensor read as zero and are not written.
 bool make_rows_map(CUtensorMap* m, const void* base, const gqa_shape& s, int hpc, int tpc);
 
-// Tensor-memory attention (tcgen05): decode / verify / tree verify with H = 128
-// over a cache in q's dtype, no window, no fused append (the caller appends
-// first).  `preferred`: the shapes where it is the faster of the two kernels.
-// The workspace holds the publication flags (flags_bytes, as the warp-level
-// kernel's plan lays them out) and then the partial results of split segments.
 // The direct warp-level kernel (one CTA per (sequence, KV head)): which
 // shapes it can serve, and which it serves by default.  Host logic only.
 bool direct_attention_supported(const gqa_shape& s, bool masked);
 bool direct_attention_preferred(const gqa_shape& s, bool masked);
+
+// Tensor-memory attention (tcgen05): decode / verify / tree verify and local
+// attention with H = 128 over a cache in q's dtype, no fused append (the caller
+// appends first).  `preferred`: the shapes where it is the faster kernel.  The
+// workspace holds the publication flags (flags_bytes, as the warp-level
+// kernel's plan lays them out) and then the partial results of split segments.
 bool tc_attention_supported(const gqa_shape& s);
 bool tc_attention_preferred(const gqa_shape& s);
 size_t tc_workspace_bytes(const gqa_shape& s, size_t flags_bytes);

@@ -133,7 +133,8 @@ typedef struct {
 /* Attention only: which kernel computes the call.  By default the library
  * picks by shape: the tensor-memory kernel (tcgen05.mma, accumulators in
  * tensor memory, 128 query rows of one KV head per tile) where a KV head has
- * many query rows (T * N / K >= 32); for small calls -- a cache in q's dtype,
+ * many query rows (T * N / K >= 32, H = 128, a cache in q's dtype, with or
+ * without a window); for small calls -- a cache in q's dtype,
  * T * N / K <= 8, no window, no tree mask, B * K <= 304 and max_blocks_per_seq
  * <= 64 (H = 64) or 48 (H = 128) -- the direct warp-level kernel (one CTA per
  * (sequence, KV head), every warp loading its own cache blocks, no split of a
@@ -141,7 +142,7 @@ typedef struct {
  * evenly over all SMs, pieces merged through the workspace) otherwise.
  * GQA_FLAG_WARP_MMA forces the persistent warp-level kernel;
  * GQA_FLAG_TENSOR_MEMORY forces the tensor-memory one, which serves H = 128
- * with a cache in q's dtype and no window; GQA_FLAG_DIRECT forces the direct
+ * with a cache in q's dtype; GQA_FLAG_DIRECT forces the direct
  * one, which serves a cache in q's dtype with T * N / K <= 8, no window and no
  * tree mask, at any context length (GQA_ERR_SHAPE where the forced kernel
  * cannot serve the call, or with more than one of the flags).  All compute the

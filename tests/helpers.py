@@ -55,20 +55,24 @@ def to(w, device):
     return w2
 
 
-def half_ulp(ref: np.ndarray, dtype: str) -> np.ndarray:
-    """Half a unit in the last place of |ref| in the output dtype."""
+def ulp(ref: np.ndarray, dtype: str) -> np.ndarray:
+    """One unit in the last place of |ref| in the output dtype.  The parity bar
+    is max(tol, one ulp): where the dtype's spacing is wider than the tolerance
+    (bf16 from |x| = 2, fp16 from 4) a result whose arithmetic is within the
+    tolerance can still round to the far neighbour of the exact value, so
+    there the bar is a faithfully rounded output."""
     mant = 10 if dtype == "f16" else 7
     a = np.abs(ref)
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     e = np.maximum(e, -14 if dtype == "f16" else -126)
-    return 0.5 * np.exp2(e - mant)
+    return np.exp2(e - mant)
 
 
 TOL = {"f16": 2e-3, "bf16": 1e-2}
 
 
 def assert_close(gpu: np.ndarray, ref: np.ndarray, dtype: str, what=""):
-    """|gpu - ref| <= max(tol, half an ulp of ref in the output dtype)."""
+    """|gpu - ref| <= max(tol, one ulp of ref in the output dtype)."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
@@ -76,7 +80,7 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, dtype: str, what=""):
     bad_nan = ~np.isfinite(gpu)
     assert not bad_nan.any(), f"{what}: {bad_nan.sum()} non-finite GPU outputs"
     err = np.abs(gpu - ref)
-    lim = np.maximum(TOL[dtype], half_ulp(ref, dtype))
+    lim = np.maximum(TOL[dtype], ulp(ref, dtype))
     worst = float(err.max()) if err.size else 0.0
     assert (err <= lim).all(), (
         f"{what}: max |err| {worst:.3g} > tol {TOL[dtype]} at "

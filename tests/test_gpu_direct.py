@@ -9,7 +9,7 @@ import torch
 
 import gqa_decode_attention_02_gb300 as gq
 import oracle
-from helpers import TOL, assert_close, half_ulp, small, to
+from helpers import TOL, assert_close, small, to, ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def close_to_each_other(a, b, dtype):
     a = a.float().cpu().double().numpy()
     b = b.float().cpu().double().numpy()
     assert np.isfinite(a).all()
-    lim = np.maximum(TOL[dtype], half_ulp(b, dtype))
+    lim = np.maximum(TOL[dtype], ulp(b, dtype))
     assert (np.abs(a - b) <= lim).all(), float(np.abs(a - b).max())
 
 

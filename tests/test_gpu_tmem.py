@@ -254,10 +254,6 @@ def test_tmem_empty_batch_and_rejected_shapes(gpu):
     w64 = small(B=1, T=1, N=8, K=2, H=64, dtype="bf16", ctx=(5,), seed=68)
     with pytest.raises(gq.GqaError):
         run(w64, gpu)  # H = 64 has no tensor-memory kernel
-    with pytest.raises(gq.GqaError):
-        wd2 = to(w, gpu)
-        gq.decode_attention(wd2.q[0], wd2.k_cache[0], wd2.v_cache[0], wd2.block_tables,
-                            wd2.context_lens, window=16, engine="tmem")
     with pytest.raises(ValueError):
         run(w, gpu, engine="both")
 
@@ -293,3 +289,79 @@ def test_tmem_bad_block_in_a_split_segment(gpu):
     assert int(st.item()) == 8
     assert (got[2] == 0).all()
     assert_close(got[:2], ref[:2], "bf16", "healthy sequences next to a split bad one")
+
+
+# ---- local attention on the tensor-memory kernel ---------------------------------
+@pytest.mark.parametrize("T,N,K", [(5, 64, 8), (1, 64, 1), (26, 64, 8)])
+@pytest.mark.parametrize("W", [1, 15, 16, 17, 100, 1024])
+def test_tmem_window_matches_oracle(gpu, T, N, K, W):
+    ctx = tuple(max(c, T) for c in (1, 2, 15, 16, 17, 31, 295, 1029, 4097))
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype="bf16", ctx=ctx, seed=W + T + N)
+    ref, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                                w.context_lens, "bf16", window=W)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    fn = gq.decode_attention if T == 1 else gq.verify_attention
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    out = fn(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables, wd.context_lens,
+             window=W, engine="tmem", status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", f"tmem window {W} T={T}")
+    # the warp-level kernel on the same call: the same function
+    warp = fn(wd.q[0], wd.k_cache[0], wd.v_cache[0], wd.block_tables, wd.context_lens,
+              window=W, engine="warp")
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().double().numpy(), warp.float().cpu().double().numpy(),
+                 "bf16", "tmem vs warp, window")
+
+
+def test_tmem_window_ignores_poisoned_rows_and_freed_blocks(gpu):
+    """NaN in every position below the earliest window (keys and values) and
+    INT32_MAX in the table entries of blocks no query sees: the same result as
+    the clean cache, no error, on the tensor-memory kernel."""
+    T, W = 5, 40
+    ctx = (T, 45, 64, 300, 1000)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=177)
+    ref, _ = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
+                              w.context_lens, "bf16", window=W)
+    tables = w.block_tables.clone()
+    for b, c in enumerate(ctx):
+        first = max(0, c - T - W + 1)
+        for pos in range(first):
+            set_token(w, b, pos, k=torch.full((8, 128), float("nan")),
+                      v=torch.full((8, 128), float("nan")))
+        tables[b, : first // 16] = 2**31 - 1
+    wd = to(w, gpu)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    out = gq.verify_attention(wd.q[0], wd.k_cache[0], wd.v_cache[0], tables.to(gpu),
+                              wd.context_lens, window=W, engine="tmem", status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.float().cpu().double().numpy()
+    assert np.isfinite(got).all()
+    assert_close(got, ref, "bf16", "tmem, poisoned window")
+
+
+def test_tmem_window_fused_append_pdl_early_matches_oracle(gpu):
+    """The append and windowed verify in one call, plain and with PDL and early
+    KV reads: the oracle's result, and the same bits either way."""
+    T, W = 5, 100
+    ctx = (T, 17, 300, 2000, 64)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=41, append=True)
+    kc, vc, err = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
+                                   w.block_tables, w.context_lens)
+    assert (err == 0).all()
+    ref, _ = oracle.attention(w.q[0], torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16),
+                              torch.from_numpy(vc.view(np.int16)).view(torch.bfloat16),
+                              w.block_tables, w.context_lens, "bf16", window=W)
+    outs = []
+    for flags in (dict(), dict(pdl=True, early_kv=True)):
+        wd = to(w, gpu)
+        out = gq.append_verify_attention(wd.q[0], wd.k_new[0], wd.v_new[0], wd.k_cache[0],
+                                         wd.v_cache[0], wd.block_tables, wd.context_lens,
+                                         window=W, engine="tmem", **flags)
+        torch.cuda.synchronize()
+        assert_close(out.float().cpu().double().numpy(), ref, "bf16", f"fused window {flags}")
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))

@@ -15,7 +15,7 @@ import torch
 import gqa_decode_attention_02_gb300 as gq
 import oracle
 from gqa_decode_attention_02_gb300 import _lib
-from helpers import TOL, assert_close, half_ulp, small, to
+from helpers import TOL, assert_close, small, to, ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,7 @@ def test_noalloc_matches_oracle_and_workspace_entry_point_on_calls_in_a_row(gpu)
         a = out.double().cpu().numpy()
         b = ref.double().cpu().numpy()
         assert np.isfinite(a).all()
-        lim = np.maximum(TOL[w.dtype], half_ulp(b, w.dtype))
+        lim = np.maximum(TOL[w.dtype], ulp(b, w.dtype))
         assert (np.abs(a - b) <= lim).all(), float(np.abs(a - b).max())
 
 
