@@ -75,7 +75,9 @@ def test_small_calls_pick_the_direct_kernel_by_default(gpu):
 @pytest.mark.parametrize("T,N,K,H,dtype", [(1, 14, 2, 64, "f16"), (1, 32, 8, 128, "bf16"),
                                            (2, 16, 4, 128, "bf16")])
 def test_direct_fused_append_writes_the_cache_and_matches_oracle(gpu, T, N, K, H, dtype):
-    ctx = tuple(max(c, T) for c in (1, 16, 17, 32, 33, 300, 1024))
+    # 65 and 129 with T = 2: the new positions straddle two stages, so two
+    # different warps patch and write them
+    ctx = tuple(max(c, T) for c in (1, 16, 17, 32, 33, 65, 129, 300, 1024))
     w = small(B=len(ctx), T=T, N=N, K=K, H=H, dtype=dtype, ctx=ctx, seed=T + 11 * K,
               append=True)
     kc, vc, err = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
