@@ -1771,8 +1771,9 @@ bool make_cache_map(CUtensorMap* m, const void* base, const gqa_shape& s) {
 
 bool make_rows_map(CUtensorMap* m, const void* base, const gqa_shape& s, int hpc, int tpc) {
     auto fn = encode_fn();
-    if (!fn || s.H != 128 || hpc < 1 || hpc > 256 || tpc < 1 || tpc > 256) return false;
-    const cuuint64_t G = (cuuint64_t)(s.N / s.K), H = 128, e = 2;
+    if (!fn || (s.H != 64 && s.H != 128) || hpc < 1 || hpc > 256 || tpc < 1 || tpc > 256)
+        return false;
+    const cuuint64_t G = (cuuint64_t)(s.N / s.K), H = (cuuint64_t)s.H, e = 2;
     const cuuint64_t dims[5] = {H, G, (cuuint64_t)s.K, (cuuint64_t)s.T, (cuuint64_t)s.B};
     const cuuint64_t strides[4] = {H * e, G * H * e, (cuuint64_t)s.N * H * e,
                                    (cuuint64_t)s.T * s.N * H * e};

@@ -1,7 +1,7 @@
 // attention_tc.cu -- decode / verify / tree-verify attention on the fifth-
 // generation tensor cores: tcgen05.mma with its accumulators in tensor memory.
 //
-// Same computation as attention.cu (CS336 lecture 10 §"Арифметическая
+// Head size 64 or 128.  Same computation as attention.cu (CS336 lecture 10 §"Арифметическая
 // интенсивность инференса": Y = softmax(Q K^T) V of the new tokens over the
 // cached keys and values, GQA from §"Уменьшаем KV-кэш", paged reads from
 // §"PagedAttention"; the tree mask of "Болжау арқылы Sonar модельдерін
@@ -83,7 +83,9 @@ constexpr int kQuotaMinTc = 16;                  // tiles per CTA at least: fewe
 constexpr int kSegCost = 6;
 constexpr int kPartFloats = 132 * kRowsTc;       // a partial: O^T [128][128], (max, sum) per half
 constexpr int kTcMinRows = 32;                   // rows per KV head from which it is picked
-                                                 // (measured faster than mma.sync from 32 rows)
+                                                 // (measured faster than mma.sync from 32 rows;
+                                                 // at H = 64 70.6 vs 82.1 us at 40 rows and
+                                                 // 77.0 vs 141.3 at 64, a 16-sequence verify)
 constexpr int kCtxCache = 128;                   // context lengths cached from the CTA's first sequence
 constexpr unsigned FULLM = 0xffffffffu;
 
@@ -303,6 +305,7 @@ __device__ void tc_plan(const TcParams& p, TcSmem& sm) {
 // one box per lane) and arrives on the stage's barrier with its own byte count.
 // Block ids are read 32 at a time (a window of eight stages, one id per lane),
 // the next window while the current one is in use.
+template <int H>
 __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, const TcParams& p,
                             uint8_t* stages, TcSmem& sm, int pw) {
     const int lane = threadIdx.x & 31;
@@ -315,7 +318,8 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
     // this lane's box: block bj of the stage, K (kvsel 0) or V, half bh
     constexpr int kBlocksPerWarp = 4 / kProducerWarps;
     const int bj = pw + kProducerWarps * (lane >> 2), kvsel = (lane >> 1) & 1, bh = lane & 1;
-    const bool boxer = lane < 4 * kBlocksPerWarp;
+    // (H = 64: one 64-dim half per block, K and V)
+    const bool boxer = lane < 4 * kBlocksPerWarp && (H == 128 || bh == 0);
     const CUtensorMap* tm = kvsel ? tmv : tmk;
     TcWalker wk;
     wk.init(sm, p);
@@ -362,7 +366,8 @@ __device__ void tc_producer(const CUtensorMap* tmk, const CUtensorMap* tmv, cons
                     if (bad || mine == 0)
                         mbar_arrive(smem_addr(&sm.full[s]));
                     else
-                        mbar_arrive_expect_tx(smem_addr(&sm.full[s]), (uint32_t)(mine * 4 * 2048));
+                        mbar_arrive_expect_tx(smem_addr(&sm.full[s]),
+                                              (uint32_t)(mine * 2 * (H / 64) * 2048));
                 }
             }
             aborted = __shfl_sync(FULLM, aborted, 0);
@@ -400,6 +405,7 @@ __device__ __forceinline__ TcBox tc_box(const TcParams& p, int chunk) {
 // the box keep stale bytes: their S, P and O rows are never read).  The box
 // of piece k is loaded once the MMA issuer's copy of box k - 1 into tensor
 // memory has completed.
+template <int H>
 __device__ void tc_qloader(const CUtensorMap* tmq, const TcParams& p, uint8_t* qbuf, TcSmem& sm) {
     if ((threadIdx.x & 31) != 0) return;
     tma_prefetch_desc(tmq);
@@ -408,7 +414,7 @@ __device__ void tc_qloader(const CUtensorMap* tmq, const TcParams& p, uint8_t* q
     wk.init(sm, p);
     TcPiece pc;
     int k = 0;
-    const uint32_t bytes = 2u * 128u * (uint32_t)p.Rc;
+    const uint32_t bytes = (uint32_t)(H / 64) * 128u * (uint32_t)p.Rc;
     bool aborted = false;
     while (!aborted && wk.next(p, pc)) {
         if (k >= 1 && !mbar_wait(smem_addr(&sm.q_free), (k - 1) & 1)) tc_abort(sm, p);
@@ -417,7 +423,7 @@ __device__ void tc_qloader(const CUtensorMap* tmq, const TcParams& p, uint8_t* q
         const TcBox x = tc_box(p, pc.v % p.C);
         const int kv = pc.v / p.C;
         mbar_arrive_expect_tx(smem_addr(&sm.q_full), bytes);
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < H / 64; ++h)
             tma_load_5d(smem_addr(qbuf) + h * kRowHalfBytes, tmq, smem_addr(&sm.q_full), 64 * h, x.h0,
                         kv, x.t0, pc.b);
         ++k;
@@ -446,13 +452,13 @@ __device__ void tc_qloader(const CUtensorMap* tmq, const TcParams& p, uint8_t* q
 // descriptors were rebuilt in the issuing loop measured 130-200 cycles of
 // issue each, and the issuer's queue holds only a few MMAs (the 14-bit address
 // field cannot carry: shared memory ends below 256 KB).
-template <bool BF16>
+template <bool BF16, int H>
 __device__ void tc_mma(const TcParams& p, uint8_t* stages, uint8_t* qbuf, TcSmem& sm,
                        uint32_t tmem) {
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
         constexpr uint32_t id_s = umma_idesc_ct(BF16, kRowsTc, 64, false);  // S = Q . K^T
-        constexpr uint32_t id_o = umma_idesc_ct(BF16, kRowsTc, 128, true);  // O += P . V
+        constexpr uint32_t id_o = umma_idesc_ct(BF16, kRowsTc, H, true);  // O += P . V
         const uint32_t st0 = smem_addr(stages);
         const uint64_t dk0 = umma_desc_sw128(st0, 16, 1024);                        // K, K-major
         const uint64_t dv0 = umma_desc_sw128(st0 + 2 * kHalfBytes, kHalfBytes, 1024); // V, MN-major
@@ -463,7 +469,7 @@ __device__ void tc_mma(const TcParams& p, uint8_t* stages, uint8_t* qbuf, TcSmem
             const uint32_t tS = tmem + kColS + g * kColSStep;
             const uint64_t dk = dk0 + (uint64_t)((n % kStagesTc) * (kStageBytesTc >> 4));
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // 16 head dims per MMA, 32 B along the 128-B row
+            for (int kk = 0; kk < H / 16; ++kk)  // 16 head dims per MMA, 32 B along the 128-B row
                 umma_ts(tS, tQ + 8 * kk, dk + (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4),
                         id_s, kk > 0);
             umma_commit(smem_addr(&sm.s_ready[g]));
@@ -479,7 +485,7 @@ __device__ void tc_mma(const TcParams& p, uint8_t* stages, uint8_t* qbuf, TcSmem
             ok = mbar_wait(smem_addr(&sm.q_full), k & 1) && !sm.abort_flag && stage_landed(sm, n);
             if (ok) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)  // the Q box into tensor memory, 32 B of each row at a time
+                for (int kk = 0; kk < H / 16; ++kk)  // the Q box into tensor memory, 32 B of each row at a time
                     tmem_cp_128x256b(tQ + 8 * kk,
                                      dq + (uint64_t)(((kk >> 2) * kRowHalfBytes + (kk & 3) * 32) >> 4));
                 umma_commit(smem_addr(&sm.q_free));
@@ -573,7 +579,7 @@ __device__ __forceinline__ void store_row32(uint4* dst, const uint32_t (&o)[32],
 // O for the next piece's PV products, and combines them with log-sum-exp
 // weights into the row's output -- staged in shared memory and written by
 // one TMA store per half -- or into a split-segment partial.
-template <bool BF16>
+template <bool BF16, int H>
 __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* stages,
                            uint8_t* obuf, TcSmem& sm, uint32_t tmem) {
     using E = Elt<BF16>;
@@ -596,8 +602,8 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             if (tc_nblk(p, b) != 0) continue;
             report(p.status, GQA_ERR_CONTEXT);
             uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                                (size_t)b * p.T * p.N * 128);
-            for (int i = 0; i < p.T * p.N * 16; ++i) o[i] = make_uint4(0, 0, 0, 0);
+                                                (size_t)b * p.T * p.N * H);
+            for (int i = 0; i < p.T * p.N * (H / 8); ++i) o[i] = make_uint4(0, 0, 0, 0);
         }
     }
     TcWalker wk;
@@ -624,7 +630,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
     };
     auto store_box = [&](int b, int kv, const TcBox& x) {
         if (tsm == 0) {
-            for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < H / 64; ++h)
                 tma_store_5d(tmo, smem_addr(obuf) + h * kRowHalfBytes, 64 * h, x.h0, kv, x.t0, b);
             bulk_commit();
         }
@@ -699,7 +705,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
                         if (!ok) break;
                         tc_fence_after();
     #pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < H / 32; ++c) {
                             uint32_t o[32];
                             tmem_ld32(tOg + 32 * c, o);
                             tmem_wait_ld();
@@ -742,10 +748,11 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             if (valid_rows < 64 || low_rows > 0) {
                 const uint32_t vb = smem_addr(stages + (size_t)s * kStageBytesTc) + 2 * kHalfBytes;
                 const int nz = 64 - valid_rows + low_rows;  // rows [0, low) and [valid, 64)
-                for (int i = tg; i < nz * 16; i += kGroupThreads) {
-                    const int k = i >> 4;
+                constexpr int kChunks = H / 8;  // 16-byte chunks per row
+                for (int i = tg; i < nz * kChunks; i += kGroupThreads) {
+                    const int k = i / kChunks;
                     const int rr = k < low_rows ? k : valid_rows + (k - low_rows);
-                    const int c = i & 15, h = c >> 3, cc = c & 7;
+                    const int c = i % kChunks, h = c >> 3, cc = c & 7;
                     st_shared_v4(vb + h * kHalfBytes + (rr >> 3) * 1024 + (rr & 7) * 128 +
                                      ((cc ^ (rr & 7)) << 4),
                                  make_uint4(0, 0, 0, 0));
@@ -805,6 +812,10 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
         }
         tc_fence_before();
         mbar_arrive(smem_addr(&sm.o_free));
+        // this thread's rows and dims of the output (H = 64: group 0 holds all
+        // the dims, group 1 none -- it still takes its part in the meetings and
+        // tickets below)
+        const bool mine_out = active && 64 * g < H;
         if (first_cta == last_cta) {  // the whole segment: O / l in q's dtype
             const bool zero = bad || !(lt > 0.f);  // an invalid block id: zeros
             if (zero) {
@@ -813,7 +824,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             }
             if (tsm == 0) bulk_wait_read();  // the previous box has left the staging buffer
             ok = softmax_bar(sm, ap);
-            if (active) stage_row(o, zero ? 0.f : 1.f / lt);
+            if (mine_out) stage_row(o, zero ? 0.f : 1.f / lt);
             ok = __all_sync(FULLM, ok && softmax_bar(sm, ap));
             if (!ok) {
                 tc_abort(sm, p);
@@ -835,7 +846,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
         const int me = blockIdx.x;
         const int npieces = last_cta - first_cta + 1;
         const bool early = me == first_cta && __shfl_sync(FULLM, seen, 0) == (unsigned)(npieces - 1);
-        if (active && !early) {
+        if (mine_out && !early) {
             float* part = p.partials + ((size_t)me * 2 + (me == first_cta ? 1 : 0)) * kPartFloats;
 #pragma unroll
             for (int k = 0; k < 64; ++k)
@@ -851,7 +862,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             if (drawn != (unsigned)(npieces - 1)) continue;  // another piece's warp merges
         }
         __syncwarp();  // lane 0's acquire before every lane's reads of the partials
-        if (active) {
+        if (mine_out) {
             // online fold over the pieces in CTA order: running max MM, sum L
             // (< 0 marks a piece with an invalid block), unnormalized values o
             float MM = M, L = bad ? -1.f : lt;
@@ -886,7 +897,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
             // this row's 64 dims of half g, in q's dtype
             uint4* dst = reinterpret_cast<uint4*>(
                 static_cast<uint16_t*>(p.out) +
-                (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * 128 + 64 * g);
+                (((size_t)b * p.T + t) * p.N + (size_t)kv * p.G + gg) * H + 64 * g);
             const float inv = zero ? 0.f : 1.f / L;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -905,7 +916,7 @@ __device__ void tc_softmax(const CUtensorMap* tmo, const TcParams& p, uint8_t* s
     if (tsm == 0) bulk_wait_read();  // the staging buffer is read before the CTA leaves
 }
 
-template <bool BF16>
+template <bool BF16, int H>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_attention_kernel(const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv,
@@ -954,13 +965,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     if (warp == 0)
-        tc_mma<BF16>(p, stages, qbuf, sm, tmem);
+        tc_mma<BF16, H>(p, stages, qbuf, sm, tmem);
     else if (warp < kQWarp)
-        tc_producer(&tmk, &tmv, p, stages, sm, warp - 1);
+        tc_producer<H>(&tmk, &tmv, p, stages, sm, warp - 1);
     else if (warp == kQWarp)
-        tc_qloader(&tmq, p, qbuf, sm);
+        tc_qloader<H>(&tmq, p, qbuf, sm);
     else
-        tc_softmax<BF16>(&tmo, p, stages, obuf, sm, tmem);
+        tc_softmax<BF16, H>(&tmo, p, stages, obuf, sm, tmem);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -974,7 +985,7 @@ static_assert(kSmemTc <= 227 * 1024, "shared memory per CTA");
 }  // namespace
 
 bool tc_attention_supported(const gqa_shape& s) {
-    return s.H == 128 && s.kv_dtype == GQA_KV_SAME && s.block_size == 16 &&
+    return (s.H == 64 || s.H == 128) && s.kv_dtype == GQA_KV_SAME && s.block_size == 16 &&
            (long long)s.T * (s.N / s.K) <= 8192;
 }
 
@@ -1005,13 +1016,14 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GQA_ERR_CUDA;
         std::lock_guard<std::mutex> lock(mu);
         if (!done[dev]) {
-            if (cudaFuncSetAttribute(tc_attention_kernel<true>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemTc) != cudaSuccess ||
-                cudaFuncSetAttribute(tc_attention_kernel<false>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemTc) != cudaSuccess)
-                return GQA_ERR_CUDA;
+            const void* kerns[4] = {reinterpret_cast<const void*>(&tc_attention_kernel<true, 128>),
+                                    reinterpret_cast<const void*>(&tc_attention_kernel<false, 128>),
+                                    reinterpret_cast<const void*>(&tc_attention_kernel<true, 64>),
+                                    reinterpret_cast<const void*>(&tc_attention_kernel<false, 64>)};
+            for (const void* k : kerns)
+                if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemTc) != cudaSuccess)
+                    return GQA_ERR_CUDA;
             done[dev] = true;
         }
     }
@@ -1076,8 +1088,10 @@ gqa_status launch_tc_attention(const gqa_shape& s, const void* q, const void* k_
     cfg.numAttrs = (s.flags & (GQA_FLAG_PDL | GQA_FLAG_EARLY_KV)) ? 1 : 0;
     const cudaError_t e =
         s.dtype == GQA_BF16
-            ? cudaLaunchKernelEx(&cfg, tc_attention_kernel<true>, tmk, tmv, tmq, tmo, p)
-            : cudaLaunchKernelEx(&cfg, tc_attention_kernel<false>, tmk, tmv, tmq, tmo, p);
+            ? (s.H == 64 ? cudaLaunchKernelEx(&cfg, tc_attention_kernel<true, 64>, tmk, tmv, tmq, tmo, p)
+                         : cudaLaunchKernelEx(&cfg, tc_attention_kernel<true, 128>, tmk, tmv, tmq, tmo, p))
+            : (s.H == 64 ? cudaLaunchKernelEx(&cfg, tc_attention_kernel<false, 64>, tmk, tmv, tmq, tmo, p)
+                         : cudaLaunchKernelEx(&cfg, tc_attention_kernel<false, 128>, tmk, tmv, tmq, tmo, p));
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -82,7 +82,7 @@ bool direct_attention_supported(const gqa_shape& s, bool masked);
 bool direct_attention_preferred(const gqa_shape& s, bool masked);
 
 // Tensor-memory attention (tcgen05): decode / verify / tree verify and local
-// attention with H = 128 over a cache in q's dtype, no fused append (the caller
+// attention with H = 64 or 128 over a cache in q's dtype, no fused append (the caller
 // appends first).  `preferred`: the shapes where it is the faster kernel.  The
 // workspace holds the publication flags (flags_bytes, as the warp-level
 // kernel's plan lays them out) and then the partial results of split segments.

@@ -133,16 +133,16 @@ typedef struct {
 /* Attention only: which kernel computes the call.  By default the library
  * picks by shape: the tensor-memory kernel (tcgen05.mma, accumulators in
  * tensor memory, 128 query rows of one KV head per tile) where a KV head has
- * many query rows (T * N / K >= 32, H = 128, a cache in q's dtype, with or
- * without a window); for small calls -- a cache in q's dtype,
+ * many query rows (T * N / K >= 32, a cache in q's dtype, with or without a
+ * window); for small calls -- a cache in q's dtype,
  * T * N / K <= 8, no window, no tree mask, B * K <= 304 and max_blocks_per_seq
  * <= 64 (H = 64) or 48 (H = 128) -- the direct warp-level kernel (one CTA per
  * (sequence, KV head), every warp loading its own cache blocks, no split of a
  * context over CTAs); the persistent warp-level mma.sync kernel (contexts split
  * evenly over all SMs, pieces merged through the workspace) otherwise.
  * GQA_FLAG_WARP_MMA forces the persistent warp-level kernel;
- * GQA_FLAG_TENSOR_MEMORY forces the tensor-memory one, which serves H = 128
- * with a cache in q's dtype; GQA_FLAG_DIRECT forces the direct
+ * GQA_FLAG_TENSOR_MEMORY forces the tensor-memory one, which serves a cache
+ * in q's dtype; GQA_FLAG_DIRECT forces the direct
  * one, which serves a cache in q's dtype with T * N / K <= 8, no window and no
  * tree mask, at any context length (GQA_ERR_SHAPE where the forced kernel
  * cannot serve the call, or with more than one of the flags).  All compute the
@@ -237,7 +237,7 @@ gqa_status gqa_decode_attention(const gqa_shape *shape, const void *q,
  *  - Shapes whose scratch exceeds 8 MiB are rejected with GQA_ERR_WORKSPACE.
  *    The scratch is what the kernel that serves the call needs: the
  *    warp-level kernel's workspace, or the tensor-memory kernel's where the
- *    shape picks that one (T * N / K >= 32, H = 128).  The latter is 256 KiB
+ *    shape picks that one (T * N / K >= 32).  The latter is 256 KiB
  *    plus 132 KiB of split-context partials per SM, so it exceeds 8 MiB, and
  *    such shapes are rejected, on every GPU with more than 60 SMs (GB300 has
  *    152).  gqa_attention_workspace_size may report more: it also covers a

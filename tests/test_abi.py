@@ -140,12 +140,14 @@ def test_empty_batch_is_a_no_op(cuda_lib):
     (dict(T=5, N=64, K=8), 2),                 # 40 rows: tensor memory
     (dict(T=4, N=64, K=8), 2),                 # 32 rows: tensor memory (threshold)
     (dict(T=3, N=64, K=8), 1),                 # 24 rows: warp-level
-    (dict(T=5, N=64, K=8, H=64), 1),           # H = 64: only the warp-level kernel
+    (dict(T=5, N=64, K=8, H=64), 2),           # H = 64, 40 rows: tensor memory too
     (dict(T=5, N=64, K=8, window=128), 2),     # a window, 40 rows: tensor memory
-    (dict(T=5, N=64, K=8, window=128, H=64), 1),  # ... but not at H = 64
+    (dict(T=5, N=64, K=8, window=128, H=64), 2),  # ... also at H = 64
+    (dict(T=3, N=64, K=8, H=64), 1),           # 24 rows: warp-level
     (dict(T=5, N=64, K=8, flags=4), 1),        # GQA_FLAG_WARP_MMA
     (dict(T=1, N=8, K=8, flags=8), 2),         # GQA_FLAG_TENSOR_MEMORY
-    (dict(T=1, N=8, K=8, H=64, flags=8), 0),   # forced, but not served
+    (dict(T=1, N=8, K=8, H=64, flags=8), 2),   # forced: served at H = 64 too
+    (dict(T=1, N=8, K=8, kv_dtype=1, flags=8), 0),  # forced, one-byte cache: not served
     (dict(T=5, N=64, K=8, flags=12), 0),       # both forced
     (dict(N=7), 0),                            # invalid shape
 ])
@@ -168,6 +170,6 @@ def test_attention_engine_python_binding(cuda_lib):
     assert gq.attention_engine(decode, kc, bt, engine="warp") == "warp"
     assert gq.attention_engine(verify, kc, bt, engine="warp") == "warp"
     assert gq.attention_engine(verify, kc, bt, window=64) == "tmem"
-    with pytest.raises(gq.GqaError):  # H = 64 cannot be forced onto tensor memory
-        gq.attention_engine(torch.zeros(2, 1, 32, 64, dtype=torch.bfloat16),
-                            torch.zeros(10, 16, 8, 64, dtype=torch.bfloat16), bt, engine="tmem")
+    assert gq.attention_engine(torch.zeros(2, 1, 32, 64, dtype=torch.bfloat16),  # H = 64, forced
+                               torch.zeros(10, 16, 8, 64, dtype=torch.bfloat16), bt,
+                               engine="tmem") == "tmem"

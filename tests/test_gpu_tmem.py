@@ -38,33 +38,36 @@ def as_np(out):
 CTX = (1, 2, 15, 16, 17, 63, 64, 65, 300, 4097)
 
 
+@pytest.mark.parametrize("H", [128, 64])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("N,K", [(8, 8), (32, 8), (64, 8), (8, 1), (128, 1), (129, 1),
                                  (256, 2)])
-def test_tmem_decode_matches_oracle(gpu, dtype, N, K):
-    w = small(B=len(CTX), T=1, N=N, K=K, H=128, dtype=dtype, ctx=CTX, seed=3 * N + K)
+def test_tmem_decode_matches_oracle(gpu, dtype, N, K, H):
+    w = small(B=len(CTX), T=1, N=N, K=K, H=H, dtype=dtype, ctx=CTX, seed=3 * N + K + H)
     ref, err = ref_of(w)
     assert (err == 0).all()
-    assert_close(as_np(run(w, gpu)), ref, dtype, f"tmem decode N={N} K={K}")
+    assert_close(as_np(run(w, gpu)), ref, dtype, f"tmem decode N={N} K={K} H={H}")
 
 
+@pytest.mark.parametrize("H", [128, 64])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("T,N,K", [(2, 8, 2), (5, 64, 8), (8, 64, 8), (26, 64, 8),
-                                   (64, 4, 4), (3, 16, 1), (17, 16, 2), (64, 8, 2)])
-def test_tmem_verify_matches_oracle(gpu, dtype, T, N, K):
+                                   (64, 4, 4), (3, 16, 1), (17, 16, 2), (64, 8, 2), (5, 56, 8)])
+def test_tmem_verify_matches_oracle(gpu, dtype, T, N, K, H):
     ctx = tuple(max(c, T) for c in (T, T + 1, 16, 17, 64, 65, 300, 2049))
-    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype=dtype, ctx=ctx, seed=T * 10 + N + K)
+    w = small(B=len(ctx), T=T, N=N, K=K, H=H, dtype=dtype, ctx=ctx, seed=T * 10 + N + K + H)
     ref, err = ref_of(w)
     assert (err == 0).all()
-    assert_close(as_np(run(w, gpu)), ref, dtype, f"tmem verify T={T} N={N} K={K}")
+    assert_close(as_np(run(w, gpu)), ref, dtype, f"tmem verify T={T} N={N} K={K} H={H}")
 
 
-@pytest.mark.parametrize("T,N,K,dtype", [(6, 64, 8, "bf16"), (26, 64, 8, "bf16"),
-                                         (64, 2, 1, "f16"), (33, 8, 2, "bf16"),
-                                         (4, 16, 2, "f16")])
-def test_tmem_tree_matches_oracle(gpu, T, N, K, dtype):
+@pytest.mark.parametrize("T,N,K,dtype,H", [(6, 64, 8, "bf16", 128), (26, 64, 8, "bf16", 128),
+                                           (64, 2, 1, "f16", 128), (33, 8, 2, "bf16", 128),
+                                           (4, 16, 2, "f16", 128), (6, 56, 8, "bf16", 64),
+                                           (26, 64, 8, "f16", 64)])
+def test_tmem_tree_matches_oracle(gpu, T, N, K, dtype, H):
     ctx = (T, T + 1, 16 + T, 300, 1029, 4100)
-    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype=dtype, ctx=ctx, seed=11 * T + N)
+    w = small(B=len(ctx), T=T, N=N, K=K, H=H, dtype=dtype, ctx=ctx, seed=11 * T + N + H)
     m = random_trees(len(ctx), T, seed=T + 1)
     ref, err = ref_of(w, tree=m)
     assert (err == 0).all()
@@ -140,11 +143,12 @@ def test_tmem_poisoned_slots_past_the_context_are_not_read(gpu):
     assert_close(as_np(run(w, gpu)), ref, "bf16", "tmem poisoned tail")
 
 
+@pytest.mark.parametrize("H", [128, 64])
 @pytest.mark.parametrize("tree", [False, True])
-def test_tmem_fused_append_matches_oracle(gpu, tree):
+def test_tmem_fused_append_matches_oracle(gpu, tree, H):
     T = 8
     ctx = (T, 70, 333, 2000)
-    w = small(B=len(ctx), T=T, N=64, K=8, H=128, dtype="bf16", ctx=ctx, seed=65, append=True)
+    w = small(B=len(ctx), T=T, N=64, K=8, H=H, dtype="bf16", ctx=ctx, seed=65 + H, append=True)
     m = random_trees(len(ctx), T, seed=3) if tree else None
     kc, vc, _ = oracle.kv_append(w.k_new[0], w.v_new[0], w.k_cache[0], w.v_cache[0],
                                  w.block_tables, w.context_lens)
@@ -244,26 +248,24 @@ def test_tmem_pdl_and_graph_match_plain(gpu):
     assert torch.equal(out, plain)
 
 
-def test_tmem_empty_batch_and_rejected_shapes(gpu):
+def test_tmem_empty_batch_and_unknown_engine(gpu):
     w = small(B=1, T=1, N=8, K=2, H=128, dtype="bf16", ctx=(5,), seed=67)
     wd = to(w, gpu)
     q0 = wd.q[0][:0]
     out = gq.decode_attention(q0, wd.k_cache[0], wd.v_cache[0], wd.block_tables[:0],
                               wd.context_lens[:0], engine="tmem")
     assert out.shape[0] == 0
-    w64 = small(B=1, T=1, N=8, K=2, H=64, dtype="bf16", ctx=(5,), seed=68)
-    with pytest.raises(gq.GqaError):
-        run(w64, gpu)  # H = 64 has no tensor-memory kernel
     with pytest.raises(ValueError):
         run(w, gpu, engine="both")
 
 
-def test_tmem_long_sequences_split_across_many_ctas(gpu):
+@pytest.mark.parametrize("H", [128, 64])
+def test_tmem_long_sequences_split_across_many_ctas(gpu, H):
     """Segments far longer than one CTA's share: pieces on many CTAs merged
     with log-sum-exp weights, next to short whole segments; a second call on
     the same workspace is bit-identical and leaves the flags at zero."""
     ctx = (30000, 5, 17000, 64, 1)
-    w = small(B=len(ctx), T=1, N=32, K=8, H=128, dtype="bf16", ctx=ctx, seed=69)
+    w = small(B=len(ctx), T=1, N=32, K=8, H=H, dtype="bf16", ctx=ctx, seed=69 + H)
     ref, err = ref_of(w)
     assert (err == 0).all()
     wd = to(w, gpu)
@@ -292,11 +294,12 @@ def test_tmem_bad_block_in_a_split_segment(gpu):
 
 
 # ---- local attention on the tensor-memory kernel ---------------------------------
-@pytest.mark.parametrize("T,N,K", [(5, 64, 8), (1, 64, 1), (26, 64, 8)])
+@pytest.mark.parametrize("T,N,K,H", [(5, 64, 8, 128), (1, 64, 1, 128), (26, 64, 8, 128),
+                                     (5, 56, 8, 64)])
 @pytest.mark.parametrize("W", [1, 15, 16, 17, 100, 1024])
-def test_tmem_window_matches_oracle(gpu, T, N, K, W):
+def test_tmem_window_matches_oracle(gpu, T, N, K, H, W):
     ctx = tuple(max(c, T) for c in (1, 2, 15, 16, 17, 31, 295, 1029, 4097))
-    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype="bf16", ctx=ctx, seed=W + T + N)
+    w = small(B=len(ctx), T=T, N=N, K=K, H=H, dtype="bf16", ctx=ctx, seed=W + T + N + H)
     ref, err = oracle.attention(w.q[0], w.k_cache[0], w.v_cache[0], w.block_tables,
                                 w.context_lens, "bf16", window=W)
     assert (err == 0).all()
