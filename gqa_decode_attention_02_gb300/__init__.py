@@ -211,8 +211,13 @@ def append_verify_attention(q, k_new, v_new, k_cache, v_cache, block_tables, con
 
 def _attention_quant(fn_name, q, k_cache, v_cache, k_scale, v_scale, block_tables,
                      context_lens, out, scale, workspace, status, stream, pdl, early_kv, kv,
-                     window=0):
+                     window=0, tree_mask=None):
     _lib._need(q, "q", ndim=4)
+    if tree_mask is not None:
+        _lib._need(tree_mask, "tree_mask", torch.int64, 2)  # uint64 bits, held as int64
+        if tuple(tree_mask.shape) != tuple(q.shape[:2]):
+            raise ValueError(f"tree_mask must be [B,T] = {tuple(q.shape[:2])}")
+        fn_name = "gqa_tree_verify_attention_quant"
     _need_quant_cache(k_cache, k_scale, "k_cache")
     _need_quant_cache(v_cache, v_scale, "v_cache")
     _lib._need(block_tables, "block_tables", torch.int32, 2)
@@ -228,10 +233,11 @@ def _attention_quant(fn_name, q, k_cache, v_cache, k_scale, v_scale, block_table
         workspace = _lib.get_workspace(nbytes, q.device, stream)
     else:
         _lib._need(workspace, "workspace", torch.uint8)
+    mask = () if tree_mask is None else (_lib._ptr(tree_mask),)
     rc = getattr(_lib.lib(), fn_name)(ctypes.byref(shape), _lib._ptr(q), _lib._ptr(k_cache),
                                       _lib._ptr(v_cache), _lib._ptr(k_scale),
                                       _lib._ptr(v_scale), _lib._ptr(block_tables),
-                                      _lib._ptr(context_lens), _lib._ptr(out),
+                                      _lib._ptr(context_lens), *mask, _lib._ptr(out),
                                       _lib._ptr(workspace), workspace.numel(),
                                       _status_arg(status), _lib._stream(stream))
     _lib._check(fn_name, rc)
@@ -250,12 +256,14 @@ def decode_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
 
 def verify_attention_quant(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
                            *, kv="int8", out=None, scale=None, workspace=None, status=None,
-                           stream=None, pdl=False, early_kv=False, window=0):
+                           stream=None, pdl=False, early_kv=False, window=0, tree_mask=None):
     """gqa_verify_attention_quant over a one-byte cache (kv = "int8" / "e4m3");
-    window > 0 is local attention as in verify_attention."""
+    window > 0 is local attention and tree_mask (int64 [B,T] holding the uint64
+    mask rows) tree verification, as in verify_attention
+    (gqa_tree_verify_attention_quant)."""
     return _attention_quant("gqa_verify_attention_quant", q, k_cache, v_cache, k_scale, v_scale,
                             block_tables, context_lens, out, scale, workspace, status, stream,
-                            pdl, early_kv, kv, window)
+                            pdl, early_kv, kv, window, tree_mask)
 
 
 def _append_attention_quant(fn_name, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,

@@ -69,6 +69,7 @@ EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_append_tree_verify_attention", "gqa_kv_append_quant",
            "gqa_decode_attention_quant", "gqa_verify_attention_quant",
            "gqa_append_decode_attention_quant", "gqa_append_verify_attention_quant",
+           "gqa_tree_verify_attention_quant",
            "gqa_attention_engine")
 
 
@@ -112,6 +113,8 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = I
             f.argtypes = [S] + [P] * 9 + [ctypes.c_size_t, P, P]
+        L.gqa_tree_verify_attention_quant.restype = I
+        L.gqa_tree_verify_attention_quant.argtypes = [S] + [P] * 10 + [ctypes.c_size_t, P, P]
         for name in ("gqa_append_decode_attention_quant", "gqa_append_verify_attention_quant"):
             f = getattr(L, name)
             f.restype = I

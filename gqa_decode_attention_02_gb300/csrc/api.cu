@@ -174,7 +174,6 @@ size_t gqa_attention_workspace_size(const gqa_shape* shape) {
     sh.flags &= ~GQA_FLAG_DIRECT;
     gqa::AttnPlan plain, general;
     if (gqa::attention_plan(sh, false, &plain) != GQA_OK) return 0;
-    if (sh.kv_dtype != GQA_KV_SAME) return plain.workspace;  // no tree mask, no tcgen05
     if (gqa::attention_plan(sh, true, &general) != GQA_OK) return 0;
     size_t w = plain.workspace > general.workspace ? plain.workspace : general.workspace;
     const size_t tc = gqa::tc_workspace_bytes(*shape, plain.flags_bytes);  // 0: not served
@@ -277,6 +276,20 @@ gqa_status gqa_verify_attention_quant(const gqa_shape* shape, const void* q,
     if (!k_scale || !v_scale) return GQA_ERR_NULL;
     return attention_entry(shape, false, false, q, nullptr, nullptr, k_cache, v_cache,
                            block_tables, context_lens, nullptr, out, workspace,
+                           workspace_bytes, dev_status, stream, k_scale, v_scale);
+}
+
+gqa_status gqa_tree_verify_attention_quant(const gqa_shape* shape, const void* q,
+                                          const void* k_cache, const void* v_cache,
+                                          const float* k_scale, const float* v_scale,
+                                          const int32_t* block_tables,
+                                          const int32_t* context_lens,
+                                          const uint64_t* tree_mask, void* out, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_status,
+                                          void* stream) {
+    if (!k_scale || !v_scale || !tree_mask) return GQA_ERR_NULL;
+    return attention_entry(shape, false, false, q, nullptr, nullptr, k_cache, v_cache,
+                           block_tables, context_lens, tree_mask, out, workspace,
                            workspace_bytes, dev_status, stream, k_scale, v_scale);
 }
 

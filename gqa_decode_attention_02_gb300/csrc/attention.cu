@@ -1885,8 +1885,8 @@ gqa_status attention_plan(const gqa_shape& s, bool masked, AttnPlan* plan) {
     int stages = default_stages(s.H, kvq);
     size_t smem = smem_for(s.H, nt, nw, stages, kvq, groups);
     const bool general = masked || s.window > 0 || chunks > 1;
-    // the one-byte caches have kernels for H = 128 only, and no tree mask entry
-    if (kvq != GQA_KV_SAME && (s.H != 128 || masked)) return GQA_ERR_SHAPE;
+    // the one-byte caches have kernels for H = 128 only
+    if (kvq != GQA_KV_SAME && s.H != 128) return GQA_ERR_SHAPE;
     const bool bf16 = s.dtype == GQA_BF16;
     int occ = resident_ctas(s.H, bf16, nt, nw, general, kvq, groups, smem);
     if (occ < 1) return GQA_ERR_CUDA;

@@ -11,7 +11,7 @@
  *   gqa_kv_append_quant  the append into a one-byte (int8 / e4m3) cache, and
  *   gqa_decode_attention_quant / gqa_verify_attention_quant  attention over it
  *   gqa_append_decode_attention_quant / gqa_append_verify_attention_quant  both
- *                        in one call
+ *                        in one call; gqa_tree_verify_attention_quant
  *   gqa_accept_sampled   stochastic acceptance of draft tokens (speculative
  *                        sampling: modified rejection sampling)
  *
@@ -370,6 +370,18 @@ gqa_status gqa_verify_attention_quant(const gqa_shape *shape, const void *q,
                                       const int32_t *context_lens, void *out, void *workspace,
                                       size_t workspace_bytes, int32_t *dev_status,
                                       void *stream);
+
+/* Tree verification over a one-byte cache: gqa_tree_verify_attention with the
+ * caches and row scales of gqa_verify_attention_quant (tree_mask as there:
+ * uint64 [B][T], T <= 64; no window). */
+gqa_status gqa_tree_verify_attention_quant(const gqa_shape *shape, const void *q,
+                                          const void *k_cache, const void *v_cache,
+                                          const float *k_scale, const float *v_scale,
+                                          const int32_t *block_tables,
+                                          const int32_t *context_lens,
+                                          const uint64_t *tree_mask, void *out, void *workspace,
+                                          size_t workspace_bytes, int32_t *dev_status,
+                                          void *stream);
 
 /* The append and the one-byte attention in one call: gqa_kv_append_quant
  * followed by gqa_decode_attention_quant / gqa_verify_attention_quant on the

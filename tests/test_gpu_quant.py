@@ -247,3 +247,42 @@ def test_fused_quant_append_matches_oracle_and_the_pair(gpu, kv, T, N, K, dtype,
     pair = attn(wd.q[0], dkc, dvc, dks, dvs, wd.block_tables, wd.context_lens, kv=kv, window=W)
     torch.cuda.synchronize()
     assert torch.equal(pair.view(torch.int16), outs[0].view(torch.int16))
+
+
+# ---- tree verification over a one-byte cache ---------------------------------------
+@pytest.mark.parametrize("kv", ["int8", "e4m3"])
+@pytest.mark.parametrize("T,N,K", [(6, 64, 8), (26, 64, 8), (4, 16, 2)])
+def test_quant_tree_verify_matches_oracle(gpu, kv, T, N, K):
+    """Draft trees (random ancestor masks, 24-208 query rows per KV head, row
+    chunks included) over one-byte codes, against the oracle over the same
+    codes and scales; the chain mask gives verify_attention_quant's bits."""
+    from test_gpu_attention import as_i64, random_trees
+
+    ctx = (T, T + 1, 16 + T, 300, 1029)
+    w = small(B=len(ctx), T=T, N=N, K=K, H=128, dtype="bf16", ctx=ctx, seed=11 * T + N)
+    kc, vc, ks, vs = quant_inputs(w, kv)
+    m = random_trees(len(ctx), T, seed=T + 2)
+    ref, err = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, "bf16",
+                                tree_mask=m, kv=kv, k_scale=ks, v_scale=vs)
+    assert (err == 0).all()
+    wd = to(w, gpu)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(gpu)  # noqa: E731
+    dkc, dvc, dks, dvs = t(kc), t(vc), t(ks), t(vs)
+    st = torch.zeros(1, dtype=torch.int32, device=gpu)
+    out = gq.verify_attention_quant(wd.q[0], dkc, dvc, dks, dvs, wd.block_tables,
+                                    wd.context_lens, kv=kv, status=st,
+                                    tree_mask=as_i64(m).to(gpu))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_close(out.float().cpu().double().numpy(), ref, "bf16", f"{kv} tree T={T}")
+    # the chain mask (every earlier new token) is plain causal verification
+    chain = np.array([[(1 << t) - 1 for t in range(T)]] * len(ctx), dtype=np.uint64)
+    a = gq.verify_attention_quant(wd.q[0], dkc, dvc, dks, dvs, wd.block_tables,
+                                  wd.context_lens, kv=kv, tree_mask=as_i64(chain).to(gpu))
+    b = gq.verify_attention_quant(wd.q[0], dkc, dvc, dks, dvs, wd.block_tables,
+                                  wd.context_lens, kv=kv)
+    torch.cuda.synchronize()
+    ref_c, _ = oracle.attention(w.q[0], kc, vc, w.block_tables, w.context_lens, "bf16",
+                                kv=kv, k_scale=ks, v_scale=vs)
+    assert_close(a.float().cpu().double().numpy(), ref_c, "bf16", f"{kv} chain mask")
+    assert_close(b.float().cpu().double().numpy(), ref_c, "bf16", f"{kv} verify")
