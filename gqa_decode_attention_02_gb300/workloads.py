@@ -60,7 +60,7 @@ class Workload:
     appended: bool  # True: the caches do NOT yet hold the T new tokens (NaN there)
     logits: Optional[torch.Tensor] = None  # fp32 [B,T,V] (verify workloads)
     draft: Optional[torch.Tensor] = None  # int32 [B,T-1]
-    draft_k: Optional[np.ndarray] = None  # planted accepted-prefix length per b
+    draft_k: Optional[np.ndarray] = None  # planted accepted-prefix length (tree: node) per b
     desc: str = ""
     windows: tuple = ()  # per layer: local-attention window, 0 = global (all 0 if empty)
     tree: tuple = ()  # draft tree over the T new tokens: parent of each (-1: the prefix)
@@ -79,6 +79,13 @@ class Workload:
                 rows[t] |= np.uint64(1) << np.uint64(a)
                 a = self.tree[a]
         return np.tile(rows, (self.B, 1))
+
+    def parents(self) -> Optional[np.ndarray]:
+        """int32 [B,T] parent of each new token in the draft tree (-1 for the
+        root), the same tree for every sequence; None without a tree."""
+        if not self.tree:
+            return None
+        return np.tile(np.asarray(self.tree, np.int32), (self.B, 1))
 
     @property
     def G(self) -> int:
@@ -186,13 +193,23 @@ def build(name: str, B: int, T: int, N: int, K: int, H: int, dtype: str,
         # Drafts: the first k_b positions carry the target's choice by construction
         # (a planted logit of 10.0, far above any N(0,1) draw of this size), the
         # rest are uniform random ids.  The oracle, not this recipe, decides the
-        # accepted length.
+        # accepted length.  With a draft tree, k_b is a node and its branch is
+        # planted the same way.
         kb = rng.integers(0, T, size=B)  # k uniform in 0..T-1
         draft = rng.integers(0, vocab, size=(B, max(T - 1, 0)))
         li = logits.cpu() if device != "cpu" else logits
         for b in range(B):
-            for t in range(int(kb[b])):
-                li[b, t, int(draft[b, t])] = 10.0
+            if tree:
+                # a draft tree: node kb[b]'s branch carries the target's choice
+                # at every edge (the logit of the child's token planted at its
+                # parent's row); draft[b, c-1] is node c's token
+                c = int(kb[b])
+                while c > 0:
+                    li[b, tree[c], int(draft[b, c - 1])] = 10.0
+                    c = tree[c]
+            else:
+                for t in range(int(kb[b])):
+                    li[b, t, int(draft[b, t])] = 10.0
         if device != "cpu":
             logits.copy_(li)
         w.logits = logits

@@ -1,5 +1,6 @@
 """fp64 CPU oracle for paged GQA decode/verify attention, KV append, greedy
-prefix acceptance, speculative sampling and the one-byte (int8 / e4m3) KV cache.
+prefix acceptance, speculative sampling, greedy acceptance over a draft tree and the
+cache compaction after it, and the one-byte (int8 / e4m3) KV cache.
 
 TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the bench's CPU
 baseline leg may import this package; the product path never does.  It shares no
@@ -18,6 +19,8 @@ from .oracle import (  # noqa: F401
     attention,
     accept_prefix,
     accept_sampled,
+    accept_tree,
+    kv_compact,
     argmax,
     num_threads,
 )

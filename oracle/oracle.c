@@ -1,7 +1,8 @@
 /*
  * oracle.c -- plain fp64 CPU oracle for paged grouped-query decode / verify
- * attention, the KV append that precedes it, greedy prefix acceptance and
- * stochastic acceptance (speculative sampling).
+ * attention, the KV append that precedes it, greedy prefix acceptance,
+ * stochastic acceptance (speculative sampling), greedy acceptance over a draft
+ * tree and the cache compaction that follows it.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
  * this file: only the tests, the package's smoke check and the bench's CPU
@@ -543,6 +544,185 @@ void oracle_accept_sampled(int B, int T, int V, const float *q, const float *p,
             }
         }
     }
+}
+
+/* ---- greedy acceptance over a draft tree ------------------------------------
+ * [SONAR-KK] §"EAGLE": instead of one chain the draft explores a tree (the top
+ * candidates at each node, to a fixed depth); the target scores every node in
+ * one pass, each node attending only to its ancestors (a custom attention
+ * mask), and the longest candidate sequence is kept for continuation, together
+ * with one more token from the target.  §"Спекулятивті кодтан шығару" gives the
+ * chain case of the same rule (longest accepted prefix, then one target token).
+ *
+ * Nodes 0..T-1 are the T new positions of sequence b.  Node 0 is the root (the
+ * token that follows the committed prefix; parents[b][0] is -1); node i >= 1
+ * has parent parents[b][i] < i and carries the drafted token draft[b][i-1].
+ * logits[b][i] is the target's prediction after the root-to-i path, and
+ * g_i = argmax logits[b][i] (argmax_row's reading).
+ *
+ * Readings (the page gives the rule in words only):
+ *   - with greedy decoding a node is acceptable iff the target would have
+ *     produced every token on its path: for every edge p -> c on the path from
+ *     the root to node i, draft[b][c-1] == g_p.  The root always is.
+ *   - "the longest" is the acceptable node of greatest depth (depth = edges
+ *     from the root); among several of the same depth (only possible when
+ *     siblings carry the same token) the lowest node index.
+ *   - outputs: accepted[b] = a = depth of that node m; path[b][0..a-1] = the
+ *     nodes of the root-to-m path below the root, by depth, and -1 in the
+ *     other T-1-a entries; next_token[b] = g_m; ctx_inout[b] -= T-1-a (the
+ *     cache keeps the root and the a accepted tokens once they are compacted,
+ *     see oracle_kv_compact).
+ *   - a malformed tree (parents[b][0] != -1, or parents[b][i] outside [0, i))
+ *     sets seq_err[b] = ORACLE_ERR_TREE; a node whose path to the root meets a
+ *     bad entry is not acceptable; everything else is decided as above.
+ *   - a context length that would drop below zero is left unchanged
+ *     (ORACLE_ERR_CONTEXT, unless the tree error was set first).
+ * With parents[b][i] = i-1 for every i this is exactly the chain rule of
+ * oracle_accept_prefix. */
+#define ORACLE_ERR_TREE 11 /* a draft tree's parent entry is out of range */
+
+/* Nodes of the path from the root to node i, root excluded, deepest first;
+ * returns their count (the depth of i), or -1 if the walk meets a parent entry
+ * outside [0, node). */
+static int tree_path_up(const int32_t *par, int i, int *nodes) {
+    int d = 0;
+    while (i != 0) {
+        const int p = par[i];
+        if (p < 0 || p >= i) return -1;
+        nodes[d++] = i;
+        i = p;
+    }
+    return d;
+}
+
+void oracle_accept_tree(int B, int T, int V, const float *logits, const int32_t *draft,
+                        const int32_t *parents, int32_t *accepted, int32_t *next_token,
+                        int32_t *path, int32_t *ctx_inout, int32_t *seq_err) {
+    for (int b = 0; b < B; ++b) {
+        const int32_t *par = parents + (size_t)b * T;
+        const int32_t *dr = draft + (size_t)b * (T > 1 ? T - 1 : 0);
+        const float *lg = logits + (size_t)b * T * V;
+        int err = par[0] == -1 ? 0 : ORACLE_ERR_TREE;
+        for (int i = 1; i < T; ++i)
+            if (par[i] < 0 || par[i] >= i) err = ORACLE_ERR_TREE;
+        int best = 0, best_depth = 0;
+        int up[64];
+        for (int i = 1; i < T; ++i) {
+            const int d = tree_path_up(par, i, up);
+            if (d < 0) continue;
+            int ok = 1;
+            for (int e = 0; e < d && ok; ++e) {
+                const int c = up[e], p = par[c];
+                if (dr[c - 1] != argmax_row(lg + (size_t)p * V, V)) ok = 0;
+            }
+            if (ok && d > best_depth) { /* strict: the lower index keeps a tie */
+                best = i;
+                best_depth = d;
+            }
+        }
+        const int a = tree_path_up(par, best, up);
+        for (int j = 0; j < T - 1; ++j) path[(size_t)b * (T - 1) + j] = j < a ? up[a - 1 - j] : -1;
+        accepted[b] = a;
+        next_token[b] = argmax_row(lg + (size_t)best * V, V);
+        if (ctx_inout) {
+            const int nc = ctx_inout[b] - (T - 1 - a);
+            if (nc < 0) {
+                if (!err) err = ORACLE_ERR_CONTEXT;
+            } else {
+                ctx_inout[b] = nc;
+            }
+        }
+        seq_err[b] = err;
+    }
+}
+
+/* ---- cache compaction after tree acceptance ---------------------------------
+ * [SONAR-KK] §"EAGLE" keeps the accepted branch of the tree and continues from
+ * it; [CS336-RU] §"PagedAttention" stores a sequence's tokens in its blocks in
+ * order.  The T tree nodes were appended at positions base .. base+T-1 (node i
+ * at base+i); after acceptance the sequence must read as the prefix, the root
+ * and the a accepted tokens in order, so position base+j (j = 1..a) takes the
+ * cached K and V rows (every KV head) of node path[b][j-1].
+ * context_lens[b] is the length AFTER acceptance (oracle_accept_tree's
+ * ctx_inout): base = context_lens[b] - 1 - a.
+ * Rows are moved as raw bytes (esize bytes per element: 2 for a cache in q's
+ * dtype, 1 for one-byte codes); with k_scale / v_scale ([NB][K][bs] fp32, the
+ * one-byte caches' row scales) the scales move with their rows.
+ * Checks (the sequence is left untouched and seq_err[b] set): a outside
+ * [0, T-1] or a path that is not strictly increasing within [1, T)
+ * (ORACLE_ERR_TREE); base < 0, or base+T-1 beyond the bs*max_blocks rows
+ * the table addresses (ORACLE_ERR_CONTEXT); a block holding one of the
+ * positions base .. base+T-1 whose id is outside [0, NB) (ORACLE_ERR_BLOCK_ID).
+ * Every source row is read before any destination row is written. */
+int oracle_kv_compact(int B, int T, int K, int H, int bs, int NB, int max_blocks, int esize,
+                      uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                      const int32_t *block_tables, const int32_t *context_lens,
+                      const int32_t *path, const int32_t *accepted, int32_t *seq_err) {
+    const size_t row = (size_t)H * esize;
+    uint8_t *tmp = (uint8_t *)malloc((size_t)(T > 1 ? T : 1) * K * row * 2 + 1);
+    float *tsc = (float *)malloc((size_t)(T > 1 ? T : 1) * K * 2 * sizeof(float) + 4);
+    if (!tmp || !tsc) {
+        free(tmp);
+        free(tsc);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int a = accepted[b];
+        const int32_t *pt = path + (size_t)b * (T > 1 ? T - 1 : 0);
+        const int32_t *tab = block_tables + (size_t)b * max_blocks;
+        seq_err[b] = 0;
+        int ok = a >= 0 && a <= T - 1;
+        for (int j = 0; ok && j < a; ++j)
+            if (pt[j] < 1 || pt[j] >= T || (j > 0 && pt[j] <= pt[j - 1])) ok = 0;
+        if (!ok) {
+            seq_err[b] = ORACLE_ERR_TREE;
+            continue;
+        }
+        const long long base = (long long)context_lens[b] - 1 - a;
+        if (base < 0 || base + T > (long long)bs * max_blocks) {
+            seq_err[b] = ORACLE_ERR_CONTEXT;
+            continue;
+        }
+        for (long long pos = base; pos < base + T; ++pos) {
+            const int id = tab[pos / bs];
+            if (id < 0 || id >= NB) ok = 0;
+        }
+        if (!ok) {
+            seq_err[b] = ORACLE_ERR_BLOCK_ID;
+            continue;
+        }
+        /* gather every source row first ... */
+        for (int j = 0; j < a; ++j) {
+            const long long pos = base + pt[j];
+            const size_t blk = (size_t)tab[pos / bs], r = (size_t)(pos % bs);
+            for (int k = 0; k < K; ++k) {
+                const size_t src = ((blk * bs + r) * K + k) * row;
+                memcpy(tmp + (((size_t)j * K + k) * 2 + 0) * row, k_cache + src, row);
+                memcpy(tmp + (((size_t)j * K + k) * 2 + 1) * row, v_cache + src, row);
+                if (k_scale) {
+                    tsc[((size_t)j * K + k) * 2 + 0] = k_scale[(blk * K + k) * bs + r];
+                    tsc[((size_t)j * K + k) * 2 + 1] = v_scale[(blk * K + k) * bs + r];
+                }
+            }
+        }
+        /* ... then write position base+1+j for the (j+1)-th accepted node */
+        for (int j = 0; j < a; ++j) {
+            const long long pos = base + 1 + j;
+            const size_t blk = (size_t)tab[pos / bs], r = (size_t)(pos % bs);
+            for (int k = 0; k < K; ++k) {
+                const size_t dst = ((blk * bs + r) * K + k) * row;
+                memcpy(k_cache + dst, tmp + (((size_t)j * K + k) * 2 + 0) * row, row);
+                memcpy(v_cache + dst, tmp + (((size_t)j * K + k) * 2 + 1) * row, row);
+                if (k_scale) {
+                    k_scale[(blk * K + k) * bs + r] = tsc[((size_t)j * K + k) * 2 + 0];
+                    v_scale[(blk * K + k) * bs + r] = tsc[((size_t)j * K + k) * 2 + 1];
+                }
+            }
+        }
+    }
+    free(tmp);
+    free(tsc);
+    return 0;
 }
 
 int oracle_num_threads(void) {

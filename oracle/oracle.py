@@ -67,6 +67,10 @@ def _get():
             lib.oracle_accept_prefix.argtypes = [i, i, i, P, P, P, P, P]
             lib.oracle_accept_sampled.restype = None
             lib.oracle_accept_sampled.argtypes = [i, i, i] + [P] * 8
+            lib.oracle_accept_tree.restype = None
+            lib.oracle_accept_tree.argtypes = [i, i, i] + [P] * 8
+            lib.oracle_kv_compact.restype = i
+            lib.oracle_kv_compact.argtypes = [i] * 8 + [P] * 9
             lib.oracle_argmax.restype = i
             lib.oracle_argmax.argtypes = [P, i]
             lib.oracle_num_threads.restype = i
@@ -266,6 +270,61 @@ def accept_sampled(q, p, draft, u, context_lens=None):
     _get().oracle_accept_sampled(B, T, V, _p(qa), _p(pa), _p(dr), _p(ua), _p(acc), _p(nxt),
                                  _p(cl), _p(err))
     return acc, nxt, cl, err[:B]
+
+
+def accept_tree(logits, draft, parents, context_lens=None):
+    """Greedy acceptance over a draft tree.  logits [B,T,V] float32 (row i: the
+    target's prediction after the root-to-node-i path), draft [B,T-1] int32
+    (node i's token at column i-1), parents [B,T] int32 (-1 for node 0, then a
+    parent index below the node's own).  Returns (accepted [B], next_token [B],
+    path [B,T-1] (accepted nodes by depth, then -1), context_lens' or None,
+    seq_err [B])."""
+    if hasattr(logits, "detach"):
+        logits = logits.detach().cpu().numpy()
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    B, T, V = lg.shape
+    if not 1 <= T <= 64:
+        raise ValueError("accept_tree: T must be in [1, 64]")
+    dr = np.ascontiguousarray(_i32(draft).reshape(B, T - 1))
+    par = np.ascontiguousarray(_i32(parents).reshape(B, T))
+    acc = np.zeros(B, np.int32)
+    nxt = np.zeros(B, np.int32)
+    path = np.full((B, max(T - 1, 0)), -1, np.int32)
+    err = np.zeros(max(B, 1), np.int32)
+    cl = None if context_lens is None else _i32(context_lens).copy()
+    _get().oracle_accept_tree(B, T, V, _p(lg), _p(dr), _p(par), _p(acc), _p(nxt), _p(path),
+                              _p(cl), _p(err))
+    return acc, nxt, path, cl, err[:B]
+
+
+def kv_compact(k_cache, v_cache, block_tables, context_lens, path, accepted, T,
+               k_scale=None, v_scale=None):
+    """Cache compaction after tree acceptance, on copies: position base+j
+    (j = 1..a, base = context_lens[b] - 1 - a) takes the rows of node
+    path[b][j-1].  Caches [NB,bs,K,H] of 16-bit elements (numpy uint16/float16
+    or torch fp16/bf16) or one-byte codes (uint8/int8, with k_scale / v_scale
+    fp32 [NB,K,bs]).  Returns (k_cache', v_cache', k_scale', v_scale', seq_err)."""
+    one_byte = k_scale is not None
+    if one_byte:
+        kc, vc = _u8(k_cache).copy(), _u8(v_cache).copy()
+        ks, vs = _f32(k_scale).copy(), _f32(v_scale).copy()
+        raw_k, raw_v = kc, vc
+    else:
+        kc, vc = _bits(k_cache).copy(), _bits(v_cache).copy()
+        ks = vs = None
+        raw_k, raw_v = kc.view(np.uint8), vc.view(np.uint8)
+    NB, bs, K, H = kc.shape
+    bt, cl = _i32(block_tables), _i32(context_lens)
+    B = bt.shape[0]
+    pt = np.ascontiguousarray(_i32(path).reshape(B, max(T - 1, 0)))
+    ac = _i32(accepted).reshape(B)
+    err = np.zeros(max(B, 1), np.int32)
+    rc = _get().oracle_kv_compact(B, T, K, H, bs, NB, bt.shape[1], 1 if one_byte else 2,
+                                  _p(raw_k), _p(raw_v), _p(ks), _p(vs), _p(bt), _p(cl), _p(pt),
+                                  _p(ac), _p(err))
+    if rc != 0:
+        raise MemoryError("oracle_kv_compact")
+    return kc, vc, ks, vs, err[:B]
 
 
 def argmax(row) -> int:
