@@ -15,6 +15,9 @@ CUDA kernels; calling any op without the built library raises.
     accept_prefix(target_logits, draft_ids, context_lens=None) -> (accepted, next)
     accept_sampled(target_probs, draft_probs, draft_ids, uniforms,
                    context_lens=None) -> (accepted, next)
+    accept_tree(target_logits, draft_ids, parents, context_lens=None)
+        -> (accepted, next, path); then kv_compact(k_cache, v_cache, block_tables,
+        context_lens, path, accepted) moves the accepted branch's cached rows
 """
 from __future__ import annotations
 
@@ -28,7 +31,8 @@ from ._lib import GqaError, Shape, Status, status_string  # noqa: F401
 __all__ = ["kv_append", "kv_append_quant", "decode_attention", "verify_attention",
            "decode_attention_quant", "verify_attention_quant", "append_decode_attention_quant",
            "append_verify_attention_quant", "append_decode_attention",
-           "append_verify_attention", "accept_prefix", "accept_sampled",
+           "append_verify_attention", "accept_prefix", "accept_sampled", "accept_tree",
+           "kv_compact",
            "attention_workspace_size", "reset_workspaces", "GqaError", "Status", "Shape"]
 
 
@@ -356,6 +360,95 @@ def accept_prefix(target_logits, draft_ids, context_lens=None, *, accepted=None,
                              _status_arg(status), _lib._stream(stream))
     _lib._check("gqa_accept_prefix", rc)
     return accepted, next_token
+
+
+def accept_tree(target_logits, draft_ids, parents, context_lens=None, *, accepted=None,
+                next_token=None, path=None, status=None, stream=None, workspace=None,
+                cluster=False):
+    """gqa_accept_tree: greedy acceptance over a draft tree.  target_logits fp32
+    [B,T,V] (row i: the target's prediction after node i's branch), draft_ids
+    int32 [B,T-1] (node i's token at column i-1), parents int32 [B,T] (-1 for
+    the root, then an index below the node's own).  Returns (accepted [B],
+    next_token [B], path [B,T-1]: the accepted branch's nodes by depth, then
+    -1); updates context_lens in place if given.  workspace / cluster as in
+    accept_prefix."""
+    _lib._need(target_logits, "target_logits", torch.float32, 3)
+    B, T, V = target_logits.shape
+    _lib._need(parents, "parents", torch.int32, 2)
+    if tuple(parents.shape) != (B, T):
+        raise ValueError(f"parents must be [{B},{T}], got {tuple(parents.shape)}")
+    if T > 1:
+        _lib._need(draft_ids, "draft_ids", torch.int32, 2)
+        if tuple(draft_ids.shape) != (B, T - 1):
+            raise ValueError(f"draft_ids must be [{B},{T - 1}], got {tuple(draft_ids.shape)}")
+    if context_lens is not None:
+        _lib._need(context_lens, "context_lens", torch.int32, 1)
+    dev = target_logits.device
+    if accepted is None:
+        accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=dev)
+    if path is None:
+        path = torch.empty((B, max(T - 1, 0)), dtype=torch.int32, device=dev)
+    else:
+        _lib._need(path, "path", torch.int32, 2)
+        if tuple(path.shape) != (B, max(T - 1, 0)):
+            raise ValueError(f"path must be [{B},{max(T - 1, 0)}], got {tuple(path.shape)}")
+    L = _lib.lib()
+    if cluster:
+        workspace = None
+    elif workspace is None:
+        workspace = _lib.get_workspace(L.gqa_accept_workspace_size(B, T), dev, stream,
+                                       kind="accept")
+    else:
+        _lib._need(workspace, "workspace", torch.uint8)
+    rc = L.gqa_accept_tree(B, T, V, _lib._ptr(target_logits),
+                           _lib._ptr(draft_ids) if T > 1 else None, _lib._ptr(parents),
+                           _lib._ptr(accepted), _lib._ptr(next_token),
+                           _lib._ptr(path) if T > 1 else None, _lib._ptr(context_lens),
+                           _lib._ptr(workspace), 0 if workspace is None else workspace.numel(),
+                           _status_arg(status), _lib._stream(stream))
+    _lib._check("gqa_accept_tree", rc)
+    return accepted, next_token, path
+
+
+def kv_compact(k_cache, v_cache, block_tables, context_lens, path, accepted, *, k_scale=None,
+               v_scale=None, kv="same", status=None, stream=None, pdl=False):
+    """gqa_kv_compact: after accept_tree, position base+j (j = 1..a, base =
+    context_lens[b] - 1 - a, context_lens as accept_tree left them) takes the
+    cached K and V rows of node path[b][j-1].  Caches [NB,16,K,H] in q's dtype
+    (kv="same"), or one-byte caches with their scales fp32 [NB,K,16]
+    (kv="int8" / "e4m3").  The tree size T is path.shape[1] + 1."""
+    if kv == "same":
+        _lib._need(k_cache, "k_cache", ndim=4)
+        _lib._need(v_cache, "v_cache", k_cache.dtype, 4)
+        if k_cache.dtype not in _lib._DTYPES:
+            raise ValueError(f"k_cache dtype {k_cache.dtype} unsupported (fp16 / bf16)")
+        dtype = _lib._DTYPES[k_cache.dtype]
+    else:
+        _need_quant_cache(k_cache, k_scale, "k_cache")
+        _need_quant_cache(v_cache, v_scale, "v_cache")
+        dtype = 0
+    _lib._need(block_tables, "block_tables", torch.int32, 2)
+    _lib._need(context_lens, "context_lens", torch.int32, 1)
+    _lib._need(path, "path", torch.int32, 2)
+    _lib._need(accepted, "accepted", torch.int32, 1)
+    NB, bs, K, H = k_cache.shape
+    B = block_tables.shape[0]
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must have the same shape")
+    if context_lens.shape[0] != B or accepted.shape[0] != B or path.shape[0] != B:
+        raise ValueError(f"context_lens, accepted and path must have {B} rows")
+    shape = _lib.Shape(B=B, T=path.shape[1] + 1, N=K, K=K, H=H, block_size=bs, num_blocks=NB,
+                       max_blocks_per_seq=block_tables.shape[1], dtype=dtype, scale=0.0,
+                       flags=_lib.FLAG_PDL if pdl else 0, window=0,
+                       kv_dtype=_lib.KV_DTYPES[kv])
+    rc = _lib.lib().gqa_kv_compact(ctypes.byref(shape), _lib._ptr(k_cache), _lib._ptr(v_cache),
+                                   _lib._ptr(k_scale), _lib._ptr(v_scale),
+                                   _lib._ptr(block_tables), _lib._ptr(context_lens),
+                                   _lib._ptr(path), _lib._ptr(accepted), _status_arg(status),
+                                   _lib._stream(stream))
+    _lib._check("gqa_kv_compact", rc)
 
 
 def accept_sampled(target_probs, draft_probs, draft_ids, uniforms, context_lens=None, *,

@@ -32,6 +32,7 @@ class Status(enum.IntEnum):
     ERR_BLOCK_ID = 8
     ERR_TIMEOUT = 9
     ERR_PROBS = 10
+    ERR_TREE = 11
 
 
 KV_DTYPES = {"same": 0, "int8": 1, "e4m3": 2}
@@ -69,7 +70,7 @@ EXPORTS = ("gqa_version", "gqa_status_string", "gqa_kv_append",
            "gqa_append_tree_verify_attention", "gqa_kv_append_quant",
            "gqa_decode_attention_quant", "gqa_verify_attention_quant",
            "gqa_append_decode_attention_quant", "gqa_append_verify_attention_quant",
-           "gqa_tree_verify_attention_quant",
+           "gqa_tree_verify_attention_quant", "gqa_accept_tree", "gqa_kv_compact",
            "gqa_attention_engine")
 
 
@@ -125,6 +126,10 @@ def lib() -> ctypes.CDLL:
         L.gqa_accept_prefix.argtypes = [I, I, I, P, P, P, P, P, P, ctypes.c_size_t, P, P]
         L.gqa_accept_sampled.restype = I
         L.gqa_accept_sampled.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P]
+        L.gqa_accept_tree.restype = I
+        L.gqa_accept_tree.argtypes = [I, I, I] + [P] * 8 + [ctypes.c_size_t, P, P]
+        L.gqa_kv_compact.restype = I
+        L.gqa_kv_compact.argtypes = [S] + [P] * 10
         _lib = L
         return L
 

@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libgqa_decode.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "attention.cu", "kv_append.cu", "accept_prefix.cu", "accept_sampled.cu", "noalloc.cu",
-           "kv_quant.cu", "attention_tc.cu"]
+           "kv_quant.cu", "attention_tc.cu", "kv_compact.cu"]
 
 
 def nvcc() -> str:

@@ -16,6 +16,11 @@
 // +0.  A max over keys does not depend on the order it is taken in, so any
 // split of the columns gives the same result.
 //
+// Greedy acceptance over a draft tree ("Болжау арқылы Sonar модельдерін
+// жылдамдату" §"EAGLE": the longest branch of candidates the target agrees
+// with is kept, plus one token from the target) shares the argmax pass and
+// differs only in the last step (finish_acceptance).
+//
 // Two kernels compute the same thing:
 //  * accept_grid_kernel (with a workspace): S thread blocks per sequence, S
 //    chosen so that the whole batch is ~4 blocks per SM; block r reduces
@@ -81,17 +86,78 @@ __device__ __forceinline__ void cluster_sync_all() {
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The last step, by one thread once every row's argmax is known (g_of(t));
+// depth: shared scratch of kMaxT ints.
+// Chain (tree == false): a = the longest run of drafts equal to the target's
+// choices, next = g_a.  Tree: node i >= 1 (parent spar[i] < i, token
+// sdraft[i-1]) is kept iff its parent is kept and its token is the target's
+// choice at the parent; a node with a parent entry outside [0, i) is never
+// kept (GQA_ERR_TREE, also for a root entry other than -1).  The kept node m
+// of greatest depth, the lowest index among equals, ends the accepted
+// branch: a = depth(m), path = the branch's nodes below the root by depth
+// (then -1), next = g_m.  Both: context_lens[b] -= T-1-a unless that drops
+// below zero (GQA_ERR_CONTEXT, the length unchanged).
+template <typename GOf>
+__device__ void finish_acceptance(int b, int T, bool tree, const int* sdraft, const int* spar,
+                                  int* depth, GOf g_of, int32_t* accepted, int32_t* next_token,
+                                  int32_t* path, int32_t* ctx_io, int32_t* status) {
+    int a = 0, m = 0;
+    if (!tree) {
+        while (a < T - 1 && sdraft[a] == g_of(a)) ++a;
+        m = a;
+    } else {
+        unsigned long long kept = 1ull;  // bit i: node i kept (the root always)
+        bool bad = spar[0] != -1;
+        depth[0] = 0;
+        for (int i = 1; i < T; ++i) {
+            const int p = spar[i];
+            depth[i] = 0;
+            if (p < 0 || p >= i) {
+                bad = true;
+                continue;
+            }
+            depth[i] = depth[p] + 1;
+            if (((kept >> p) & 1ull) && sdraft[i - 1] == g_of(p)) {
+                kept |= 1ull << i;
+                if (depth[i] > a) {  // strict: the lower index keeps a tie
+                    a = depth[i];
+                    m = i;
+                }
+            }
+        }
+        if (bad) report(status, GQA_ERR_TREE);
+        int32_t* pb = path + (size_t)b * (T - 1);
+        int cur = m;
+        for (int j = a - 1; j >= 0; --j) {
+            pb[j] = cur;
+            cur = spar[cur];
+        }
+        for (int j = a; j < T - 1; ++j) pb[j] = -1;
+    }
+    accepted[b] = a;
+    next_token[b] = g_of(m);
+    if (ctx_io) {
+        const int nc = ctx_io[b] - (T - 1 - a);
+        if (nc < 0)
+            report(status, GQA_ERR_CONTEXT);
+        else
+            ctx_io[b] = nc;
+    }
+}
+
 // Cluster rank r reduces columns [r*S, min(V, (r+1)*S)) of every row of its
 // sequence (S a multiple of 4): the T slices are loaded a few rows at a time
 // with 16-byte loads (vec) or scalar loads, all of a pass in flight together.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads)
     accept_kernel(const float* __restrict__ logits, const int32_t* __restrict__ draft,
-                  int32_t* accepted, int32_t* next_token, int32_t* ctx_io, int32_t* status,
-                  int T, int V, int cs) {
+                  const int32_t* __restrict__ parents, int32_t* accepted, int32_t* next_token,
+                  int32_t* path, int32_t* ctx_io, int32_t* status, int T, int V, int cs) {
     __shared__ unsigned long long table[kMaxT * kMaxCluster];  // used in rank 0
     __shared__ unsigned long long red[kThreads / 32][kRowsPerPass];
     __shared__ int sdraft[kMaxT];  // the drafts, fetched while the logits stream
+    __shared__ int spar[kMaxT];    // the tree's parent entries (tree acceptance)
+    __shared__ int sdepth[kMaxT];  // node depths (tree acceptance, thread 0 of rank 0)
     griddep_launch_dependents();
     griddep_wait();  // logits and lengths follow the previous kernels
     const uint32_t rank = cluster_rank();
@@ -101,6 +167,7 @@ __global__ void __launch_bounds__(kThreads)
     const int c_lo = min(V, (int)rank * S), c_hi = min(V, c_lo + S);
     const float* row0 = logits + (size_t)b * T * V;
     if (rank == 0 && tid < T - 1) sdraft[tid] = __ldg(draft + (size_t)b * (T - 1) + tid);
+    if (parents && rank == 0 && tid < T) spar[tid] = __ldg(parents + (size_t)b * T + tid);
     // Block 0's shared memory may be written only once block 0 is running:
     // arrive now, wait before the first remote store.
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
@@ -169,23 +236,13 @@ __global__ void __launch_bounds__(kThreads)
     }
     cluster_sync_all();
     if (rank != 0 || tid != 0) return;
-    int g[kMaxT];
-    for (int t = 0; t < T; ++t) {
+    auto g_of = [&](int t) {
         unsigned long long k = 0ull;
         for (int r = 0; r < cs; ++r) k = umax64(k, table[t * kMaxCluster + r]);
-        g[t] = (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
-    }
-    int a = 0;
-    while (a < T - 1 && sdraft[a] == g[a]) ++a;
-    accepted[b] = a;
-    next_token[b] = g[a];
-    if (ctx_io) {
-        const int nc = ctx_io[b] - (T - 1 - a);
-        if (nc < 0)
-            report(status, GQA_ERR_CONTEXT);
-        else
-            ctx_io[b] = nc;
-    }
+        return (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+    };
+    finish_acceptance(b, T, parents != nullptr, sdraft, spar, sdepth, g_of, accepted, next_token,
+                      path, ctx_io, status);
 }
 
 
@@ -229,11 +286,14 @@ __device__ __forceinline__ unsigned seq_ticket(unsigned* t) {
 template <bool kVec>
 __global__ void __launch_bounds__(kGridThreads)
     accept_grid_kernel(const float* __restrict__ logits, const int32_t* __restrict__ draft,
-                       int32_t* accepted, int32_t* next_token, int32_t* ctx_io, int32_t* status,
+                       const int32_t* __restrict__ parents, int32_t* accepted,
+                       int32_t* next_token, int32_t* path, int32_t* ctx_io, int32_t* status,
                        unsigned* tickets, unsigned long long* parts, int T, int V, int S, int W) {
     __shared__ unsigned long long red[kGridThreads / 32][kMaxT];
     __shared__ unsigned long long skey[kMaxT];
     __shared__ int sdraft[kMaxT];
+    __shared__ int spar[kMaxT];
+    __shared__ int sdepth[kMaxT];
     __shared__ int s_last;
     griddep_launch_dependents();
     griddep_wait();  // logits and lengths follow the previous kernels
@@ -247,6 +307,7 @@ __global__ void __launch_bounds__(kGridThreads)
     const float* row0 = logits + (size_t)b * T * V;
     // this thread's draft id (for the last block's walk), in flight with the logits
     const int my_draft = (tid < T - 1) ? __ldg(draft + (size_t)b * (T - 1) + tid) : 0;
+    const int my_parent = (parents && tid < T) ? __ldg(parents + (size_t)b * T + tid) : 0;
     // Per row, this thread's running argmax over its columns, which it visits
     // in increasing order: (bv, bi) is replaced by (x, c) iff bv is not NaN and
     // !(x <= bv) -- x larger, or x NaN -- so the first NaN wins, then the
@@ -316,6 +377,7 @@ __global__ void __launch_bounds__(kGridThreads)
         }
     }
     if (tid < T - 1) sdraft[tid] = my_draft;
+    if (tid < T) spar[tid] = my_parent;
     __syncthreads();
     // this block's key of each row into its own slot
     for (int t = tid; t < T; t += kGridThreads) {
@@ -352,17 +414,8 @@ __global__ void __launch_bounds__(kGridThreads)
     if (tid != 0) return;
     tickets[b] = 0u;  // ready for the next call
     auto g_of = [&](int t) { return (int)(0xffffffffu - (uint32_t)(skey[t] & 0xffffffffull)); };
-    int a = 0;
-    while (a < T - 1 && sdraft[a] == g_of(a)) ++a;
-    accepted[b] = a;
-    next_token[b] = g_of(a);
-    if (ctx_io) {
-        const int nc = ctx_io[b] - (T - 1 - a);
-        if (nc < 0)
-            report(status, GQA_ERR_CONTEXT);
-        else
-            ctx_io[b] = nc;
-    }
+    finish_acceptance(b, T, parents != nullptr, sdraft, spar, sdepth, g_of, accepted, next_token,
+                      path, ctx_io, status);
 }
 
 }  // namespace
@@ -375,8 +428,9 @@ size_t accept_workspace_bytes(int B, int T) {
 }
 
 gqa_status launch_accept_prefix(int B, int T, int V, const float* logits, const int32_t* draft,
-                                int32_t* accepted, int32_t* next_token, int32_t* ctx_io,
-                                void* workspace, int32_t* dev_status, cudaStream_t stream) {
+                                const int32_t* parents, int32_t* accepted, int32_t* next_token,
+                                int32_t* path, int32_t* ctx_io, void* workspace,
+                                int32_t* dev_status, cudaStream_t stream) {
     if (B == 0) return GQA_OK;
     // 16-byte loads need every row to start on a 16-byte boundary
     const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
@@ -397,10 +451,12 @@ gqa_status launch_accept_prefix(int B, int T, int V, const float* logits, const 
         cfg.attrs = nullptr;
         cfg.numAttrs = 0;
         const cudaError_t e =
-            vec ? cudaLaunchKernelEx(&cfg, accept_grid_kernel<true>, logits, draft, accepted,
-                                     next_token, ctx_io, dev_status, tickets, parts, T, V, S, W)
-                : cudaLaunchKernelEx(&cfg, accept_grid_kernel<false>, logits, draft, accepted,
-                                     next_token, ctx_io, dev_status, tickets, parts, T, V, S, W);
+            vec ? cudaLaunchKernelEx(&cfg, accept_grid_kernel<true>, logits, draft, parents,
+                                     accepted, next_token, path, ctx_io, dev_status, tickets,
+                                     parts, T, V, S, W)
+                : cudaLaunchKernelEx(&cfg, accept_grid_kernel<false>, logits, draft, parents,
+                                     accepted, next_token, path, ctx_io, dev_status, tickets,
+                                     parts, T, V, S, W);
         return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
     }
     // one cluster of up to 8 blocks per sequence; each block takes V/cs columns
@@ -420,10 +476,10 @@ gqa_status launch_accept_prefix(int B, int T, int V, const float* logits, const 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e =
-        vec ? cudaLaunchKernelEx(&cfg, accept_kernel<true>, logits, draft, accepted, next_token,
-                                 ctx_io, dev_status, T, V, cs)
-            : cudaLaunchKernelEx(&cfg, accept_kernel<false>, logits, draft, accepted, next_token,
-                                 ctx_io, dev_status, T, V, cs);
+        vec ? cudaLaunchKernelEx(&cfg, accept_kernel<true>, logits, draft, parents, accepted,
+                                 next_token, path, ctx_io, dev_status, T, V, cs)
+            : cudaLaunchKernelEx(&cfg, accept_kernel<false>, logits, draft, parents, accepted,
+                                 next_token, path, ctx_io, dev_status, T, V, cs);
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -114,6 +114,7 @@ const char* gqa_status_string(int status) {
         case GQA_ERR_BLOCK_ID: return "block id out of range";
         case GQA_ERR_TIMEOUT: return "bounded wait inside a kernel timed out";
         case GQA_ERR_PROBS: return "invalid probability, uniform or empty distribution";
+        case GQA_ERR_TREE: return "draft tree parent or accepted path out of range";
         default: return "unknown status";
     }
 }
@@ -336,9 +337,50 @@ gqa_status gqa_accept_prefix(int B, int T, int V, const float* target_logits,
         if (workspace_bytes < gqa::accept_workspace_bytes(B, T)) return GQA_ERR_WORKSPACE;
         if (!aligned16(workspace)) return GQA_ERR_ALIGN;
     }
-    return gqa::launch_accept_prefix(B, T, V, target_logits, draft_ids, accepted, next_token,
-                                     context_lens_inout, workspace, dev_status,
-                                     static_cast<cudaStream_t>(stream));
+    return gqa::launch_accept_prefix(B, T, V, target_logits, draft_ids, nullptr, accepted,
+                                     next_token, nullptr, context_lens_inout, workspace,
+                                     dev_status, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status gqa_accept_tree(int B, int T, int V, const float* target_logits,
+                           const int32_t* draft_ids, const int32_t* parents, int32_t* accepted,
+                           int32_t* next_token, int32_t* path, int32_t* context_lens_inout,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+    if (B < 0 || T < 1 || T > 64 || V < 1) return GQA_ERR_SHAPE;
+    if (!workspace && B > 65535) return GQA_ERR_SHAPE;  // one cluster per sequence (grid y)
+    if (B == 0) return GQA_OK;
+    if (!target_logits || !parents || !accepted || !next_token ||
+        (T > 1 && (!draft_ids || !path)))
+        return GQA_ERR_NULL;
+    if (!aligned16(target_logits)) return GQA_ERR_ALIGN;
+    if ((long long)T * V > (1ll << 31) - 1) return GQA_ERR_SHAPE;
+    if (workspace) {
+        if (workspace_bytes < gqa::accept_workspace_bytes(B, T)) return GQA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return GQA_ERR_ALIGN;
+    }
+    return gqa::launch_accept_prefix(B, T, V, target_logits, draft_ids, parents, accepted,
+                                     next_token, path, context_lens_inout, workspace,
+                                     dev_status, static_cast<cudaStream_t>(stream));
+}
+
+gqa_status gqa_kv_compact(const gqa_shape* shape, void* k_cache, void* v_cache, float* k_scale,
+                          float* v_scale, const int32_t* block_tables,
+                          const int32_t* context_lens, const int32_t* path,
+                          const int32_t* accepted, int32_t* dev_status, void* stream) {
+    gqa_status st = check_common(shape);
+    if (st != GQA_OK) return st;
+    if (shape->T > 64) return GQA_ERR_SHAPE;
+    const bool one_byte = shape->kv_dtype != GQA_KV_SAME;
+    if (!one_byte && (k_scale || v_scale)) return GQA_ERR_DTYPE;  // scales: one-byte caches only
+    if (one_byte && (!k_scale || !v_scale)) return GQA_ERR_NULL;
+    if (shape->B == 0 || shape->T == 1) return GQA_OK;  // nothing can move
+    if (!k_cache || !v_cache || !block_tables || !context_lens || !path || !accepted)
+        return GQA_ERR_NULL;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return GQA_ERR_ALIGN;
+    return gqa::launch_kv_compact(*shape, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                  context_lens, path, accepted, dev_status,
+                                  static_cast<cudaStream_t>(stream));
 }
 
 gqa_status gqa_accept_sampled(int B, int T, int V, const float* target_probs,

@@ -52,11 +52,22 @@ gqa_status launch_kv_append(const gqa_shape& s, const void* k_new, const void* v
 
 // workspace == nullptr: one thread-block cluster per sequence; otherwise many
 // blocks per sequence whose keys meet in the workspace (accept_workspace_bytes).
+// parents == nullptr: prefix acceptance of a chain of drafts; otherwise
+// acceptance over the draft tree parents [B][T], the accepted branch's nodes
+// written to path [B][T-1].
 size_t accept_workspace_bytes(int B, int T);
 gqa_status launch_accept_prefix(int B, int T, int V, const float* logits,
-                                const int32_t* draft, int32_t* accepted,
-                                int32_t* next_token, int32_t* ctx_io, void* workspace,
-                                int32_t* dev_status, cudaStream_t stream);
+                                const int32_t* draft, const int32_t* parents,
+                                int32_t* accepted, int32_t* next_token, int32_t* path,
+                                int32_t* ctx_io, void* workspace, int32_t* dev_status,
+                                cudaStream_t stream);
+
+// Moves the cached rows of an accepted tree branch behind its root (see
+// gqa_kv_compact); k_scale / v_scale non-null for one-byte caches.
+gqa_status launch_kv_compact(const gqa_shape& s, void* k_cache, void* v_cache, float* k_scale,
+                             float* v_scale, const int32_t* block_tables,
+                             const int32_t* context_lens, const int32_t* path,
+                             const int32_t* accepted, int32_t* dev_status, cudaStream_t stream);
 
 gqa_status launch_accept_sampled(int B, int T, int V, const float* q, const float* p,
                                  const int32_t* draft, const double* u, int32_t* accepted,

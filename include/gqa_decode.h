@@ -76,8 +76,10 @@ typedef enum {
     GQA_ERR_CONTEXT = 7,   /* device: context_lens[b] < T, < 1 or > capacity */
     GQA_ERR_BLOCK_ID = 8,  /* device: a block-table entry in use not in [0,num_blocks) */
     GQA_ERR_TIMEOUT = 9,   /* device: a bounded wait inside a kernel gave up */
-    GQA_ERR_PROBS = 10     /* device: an entry read is not a probability in [0,1], a
+    GQA_ERR_PROBS = 10,    /* device: an entry read is not a probability in [0,1], a
                               uniform is not in [0,1), or a row has no weight */
+    GQA_ERR_TREE = 11      /* device: a draft tree's parent entry, or an accepted
+                              branch passed to gqa_kv_compact, is out of range */
 } gqa_status;
 
 typedef enum { GQA_F16 = 0, GQA_BF16 = 1 } gqa_dtype;
@@ -438,6 +440,68 @@ gqa_status gqa_accept_prefix(int B, int T, int V, const float *target_logits,
                              int32_t *next_token, int32_t *context_lens_inout,
                              void *workspace, size_t workspace_bytes,
                              int32_t *dev_status, void *stream);
+
+/* Greedy acceptance over a draft tree.  "Болжау арқылы Sonar модельдерін
+ * жылдамдату" §"EAGLE": the draft explores a tree of candidates, the target
+ * scores every node in one pass (gqa_tree_verify_attention), and the longest
+ * branch the target agrees with is kept, plus one token from the target.
+ * Nodes 0..T-1 are the T new positions of a sequence; node 0 is the root (the
+ * token after the committed prefix).
+ *   target_logits fp32 [B][T][V]   row i: the target's prediction after the
+ *                                  root-to-node-i branch; g_i = its argmax
+ *                                  (ties and NaN as in gqa_accept_prefix)
+ *   draft_ids     int32 [B][T-1]   draft_ids[b][i-1]: node i's token
+ *   parents       int32 [B][T]     parents[b][0] = -1; parents[b][i] < i
+ *   Node i >= 1 is kept iff its parent is kept and draft_ids[b][i-1] equals
+ *   g of its parent (the root is always kept).  The kept node m of greatest
+ *   depth ends the accepted branch; among nodes of equal depth (siblings with
+ *   the same token) the lowest index wins.
+ *   accepted[b]   = a = depth of m (edges from the root)
+ *   path[b][0..a-1] = the branch's nodes below the root, by depth; -1 in the
+ *                     other T-1-a entries
+ *   next_token[b] = g_m
+ *   context_lens_inout[b] -= T-1-a  (if not NULL); then gqa_kv_compact moves
+ *                     the branch's cached rows behind the root
+ * A chain (parents[b][i] = i-1) gives exactly gqa_accept_prefix's results.
+ * Requirements, workspace and the two kernels as gqa_accept_prefix;
+ * draft_ids and path may be NULL when T == 1.  Device errors: a parent entry
+ * outside [0, i) (or a root entry other than -1) is reported (GQA_ERR_TREE)
+ * and that node and its descendants are never kept; a context length that
+ * would drop below zero is left unchanged (GQA_ERR_CONTEXT). */
+gqa_status gqa_accept_tree(int B, int T, int V, const float *target_logits,
+                           const int32_t *draft_ids, const int32_t *parents,
+                           int32_t *accepted, int32_t *next_token, int32_t *path,
+                           int32_t *context_lens_inout, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* Cache compaction after tree acceptance.  §"EAGLE" (same page): decoding
+ * continues from the kept branch, and CS336 lecture 10 §"PagedAttention"
+ * stores a sequence's tokens in its blocks in order.  The T tree nodes were
+ * appended at positions base .. base+T-1 (node i at base+i, as
+ * gqa_append_verify_attention writes them); afterwards position base+j
+ * (j = 1..a) holds the K and V rows, every KV head, of node path[b][j-1],
+ * with base = context_lens[b] - 1 - a.
+ *   shape          T = tree nodes (<= 64), K, H, block_size, num_blocks,
+ *                  max_blocks_per_seq, kv_dtype (N, dtype as for the cache's
+ *                  attention calls; q-side fields are not used)
+ *   context_lens   int32 [B], the lengths AFTER acceptance (gqa_accept_tree's
+ *                  context_lens_inout)
+ *   path, accepted gqa_accept_tree's outputs ([B][T-1], [B])
+ *   k_scale, v_scale  fp32 [num_blocks][K][block_size] row scales of a
+ *                  one-byte cache (kv_dtype GQA_KV_INT8 / GQA_KV_E4M3; moved
+ *                  with their rows); NULL for a cache in q's dtype
+ * Rows move as raw bytes: the result is bit for bit the branch's rows.
+ * Caches 16-byte aligned.  The blocks holding positions base .. base+T-1
+ * must not be shared with another sequence.  Device errors (the sequence is
+ * left untouched): a outside [0, T-1] or a branch that is not strictly
+ * increasing within [1, T) (GQA_ERR_TREE); base < 0 or base+T beyond
+ * 16*max_blocks_per_seq (GQA_ERR_CONTEXT); a block holding one of positions
+ * base .. base+T-1 outside [0, num_blocks) (GQA_ERR_BLOCK_ID).
+ * GQA_FLAG_PDL in shape->flags chains the launch to the acceptance kernel. */
+gqa_status gqa_kv_compact(const gqa_shape *shape, void *k_cache, void *v_cache,
+                          float *k_scale, float *v_scale, const int32_t *block_tables,
+                          const int32_t *context_lens, const int32_t *path,
+                          const int32_t *accepted, int32_t *dev_status, void *stream);
 
 /* Stochastic acceptance (speculative sampling).  CS336 lecture 10
  * §"Спекулятивное сэмплирование": modified rejection sampling with the draft

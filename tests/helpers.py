@@ -86,3 +86,31 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, dtype: str, what=""):
         f"{what}: max |err| {worst:.3g} > tol {TOL[dtype]} at "
         f"{np.unravel_index(int(np.argmax(err - lim)), err.shape)}")
     return worst
+
+
+def planted_tree_inputs(B, T, V, parents, rng, p_match=0.6):
+    """Random logits and drafts where an edge agrees with the target with
+    probability p_match (the parent's planted choice is reused as the child's
+    token).  Returns logits [B,T,V] float32 and draft [B,T-1] int32."""
+    lg = rng.normal(size=(B, T, V)).astype(np.float32)
+    choice = rng.integers(0, V, size=(B, T))
+    for b in range(B):
+        for i in range(T):
+            lg[b, i, choice[b, i]] = 10.0
+    draft = rng.integers(0, V, size=(B, max(T - 1, 0))).astype(np.int32)
+    for b in range(B):
+        for c in range(1, T):
+            if rng.random() < p_match:
+                draft[b, c - 1] = choice[b, parents[b, c]]
+    return lg, draft
+
+
+def random_parents(B, T, rng, chain_bias=0.0):
+    """int32 [B,T] random draft trees in topological order (parents[0] = -1,
+    parents[i] < i); chain_bias: chance that a node continues the chain."""
+    par = np.zeros((B, T), np.int32)
+    par[:, 0] = -1
+    for b in range(B):
+        for i in range(1, T):
+            par[b, i] = i - 1 if rng.random() < chain_bias else rng.integers(0, i)
+    return par

@@ -111,6 +111,38 @@ def test_fused_quant_entry_points_check_their_arguments(cuda_lib):
                  fake, fake, 1 << 20, None, None) == 3
 
 
+def test_tree_acceptance_and_compaction_check_their_arguments(cuda_lib):
+    fake = ctypes.c_void_p(16)
+    odd = ctypes.c_void_p(18)
+    f = cuda_lib.gqa_accept_tree
+    # (B, T, V, logits, draft, parents, accepted, next, path, ctx, ws, ws_bytes, status, stream)
+    assert f(2, 65, 10, fake, fake, fake, fake, fake, fake, None, None, 0, None, None) == 2
+    assert f(2, 3, 10, fake, fake, None, fake, fake, fake, None, None, 0, None, None) == 1
+    assert f(2, 3, 10, fake, fake, fake, fake, fake, None, None, None, 0, None, None) == 1
+    assert f(2, 3, 10, odd, fake, fake, fake, fake, fake, None, None, 0, None, None) == 4
+    need = cuda_lib.gqa_accept_workspace_size(2, 3)
+    assert f(2, 3, 10, fake, fake, fake, fake, fake, fake, None, fake, need - 1, None,
+             None) == 5
+    assert f(0, 3, 10, None, None, None, None, None, None, None, None, 0, None, None) == 0
+    g = cuda_lib.gqa_kv_compact
+    # (shape, k_cache, v_cache, k_scale, v_scale, tables, ctx, path, accepted, status, stream)
+    assert g(ctypes.byref(_shape(T=65)), fake, fake, None, None, fake, fake, fake, fake, None,
+             None) == 2
+    assert g(ctypes.byref(_shape(T=4)), fake, fake, fake, fake, fake, fake, fake, fake, None,
+             None) == 3  # scales with a two-byte cache
+    assert g(ctypes.byref(_shape(T=4, kv_dtype=1)), fake, fake, None, None, fake, fake, fake,
+             fake, None, None) == 1  # a one-byte cache without its scales
+    assert g(ctypes.byref(_shape(T=4)), fake, fake, None, None, fake, fake, None, fake, None,
+             None) == 1
+    assert g(ctypes.byref(_shape(T=4)), odd, fake, None, None, fake, fake, fake, fake, None,
+             None) == 4
+    # nothing can move: an empty batch, or a tree of one node
+    assert g(ctypes.byref(_shape(B=0, T=4)), None, None, None, None, None, None, None, None,
+             None, None) == 0
+    assert g(ctypes.byref(_shape(T=1)), None, None, None, None, None, None, None, None, None,
+             None) == 0
+
+
 def test_empty_batch_is_a_no_op(cuda_lib):
     s = _shape(B=0)
     rc = cuda_lib.gqa_kv_append(ctypes.byref(s), None, None, None, None, None, None, None,

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import slot, small
+from helpers import planted_tree_inputs as planted, random_parents, slot, small
 
 
 def one_hot_logits(g, T, V):
@@ -66,32 +66,6 @@ def test_deeper_branch_wins_and_equal_depth_goes_to_the_lower_index():
     tok2 = np.array([[3, 3, 4, 6]], np.int32)
     acc, nxt, path, _, _ = oracle.accept_tree(one_hot_logits(g, 5, 8), tok2, par)
     assert acc[0] == 1 and path[0][0] == 1 and nxt[0] == 1
-
-
-def planted(B, T, V, parents, rng, p_match=0.6):
-    """Random logits and drafts where an edge agrees with the target with
-    probability p_match (the parent's planted choice is reused as the child's
-    token).  Returns logits [B,T,V] float32 and draft [B,T-1] int32."""
-    lg = rng.normal(size=(B, T, V)).astype(np.float32)
-    choice = rng.integers(0, V, size=(B, T))
-    for b in range(B):
-        for i in range(T):
-            lg[b, i, choice[b, i]] = 10.0
-    draft = rng.integers(0, V, size=(B, max(T - 1, 0))).astype(np.int32)
-    for b in range(B):
-        for c in range(1, T):
-            if rng.random() < p_match:
-                draft[b, c - 1] = choice[b, parents[b, c]]
-    return lg, draft
-
-
-def random_parents(B, T, rng, chain_bias=0.0):
-    par = np.zeros((B, T), np.int32)
-    par[:, 0] = -1
-    for b in range(B):
-        for i in range(1, T):
-            par[b, i] = i - 1 if rng.random() < chain_bias else rng.integers(0, i)
-    return par
 
 
 @pytest.mark.parametrize("T", [1, 2, 5, 16, 64])
