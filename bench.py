@@ -75,7 +75,10 @@ def parse_args(argv=None):
     ap.add_argument("--unfused", action="store_true",
                     help="separate kv_append launches instead of the append fused into "
                          "the attention launch")
-    return ap.parse_args(argv)
+    args = ap.parse_args(argv)
+    if args.workload == "tree" and args.accept == "sampled":
+        ap.error("stochastic acceptance over a draft tree is not built (--accept greedy)")
+    return args
 
 
 def dist_env():
@@ -453,6 +456,12 @@ def run_ours(args, world, rank, local):
     tm = w.tree_mask()
     tree_t = None if tm is None else torch.from_numpy(tm.view(np.int64)).to(dev)
     extra = {} if tree_t is None else {"tree_mask": tree_t}
+    # a draft tree: acceptance walks the tree and the kept branch's cache rows
+    # are compacted behind its root (every layer's caches)
+    tree_acc = has_acc and not sampled and tree_t is not None
+    if tree_acc:
+        parents_d = torch.as_tensor(w.parents()).to(dev)
+        path_out = torch.empty((w.B, w.T - 1), dtype=torch.int32, device=dev)
 
     def do_append():
         if w.appended and not fused:
@@ -473,7 +482,7 @@ def run_ours(args, world, rank, local):
             if q8:
                 attn_q8(w.q[l], qk[l], qv[l], sk[l], sv[l], w.block_tables, w.context_lens,
                         kv=args.kv, out=outs[l], workspace=ws, status=st, pdl=True,
-                        early_kv=True, window=w.window(l))
+                        early_kv=True, window=w.window(l), **extra)
             elif fused:
                 fused_fn(w.q[l], w.k_new[l], w.v_new[l], w.k_cache[l], w.v_cache[l],
                          w.block_tables, w.context_lens, out=outs[l], workspace=ws, status=st,
@@ -488,6 +497,16 @@ def run_ours(args, world, rank, local):
         if sampled:
             gq.accept_sampled(sin.q, sin.p, sin.draft, sin.uniforms, ctx_scratch,
                               accepted=acc_out, next_token=nxt_out, status=st)
+        elif tree_acc:
+            gq.accept_tree(w.logits, w.draft, parents_d, ctx_scratch, accepted=acc_out,
+                           next_token=nxt_out, path=path_out, status=st, workspace=acc_ws)
+            for l in range(L):
+                if q8:
+                    gq.kv_compact(qk[l], qv[l], w.block_tables, ctx_scratch, path_out, acc_out,
+                                  k_scale=sk[l], v_scale=sv[l], kv=args.kv, status=st, pdl=True)
+                else:
+                    gq.kv_compact(w.k_cache[l], w.v_cache[l], w.block_tables, ctx_scratch,
+                                  path_out, acc_out, status=st, pdl=True)
         elif has_acc:
             gq.accept_prefix(w.logits, w.draft, ctx_scratch, accepted=acc_out,
                              next_token=nxt_out, status=st, workspace=acc_ws)
@@ -574,15 +593,53 @@ def run_ours(args, world, rank, local):
         parity = parity_sample(w, outs, quant_cpu if q8 else None, oracle_inputs)
         if has_acc:
             ctx0 = w.context_lens.cpu().numpy()
+            rp = None
             if sampled:
                 ra, rn, rc, _ = oracle.accept_sampled(
                     sin.q.cpu().numpy(), sin.p.cpu().numpy(), sin.draft.cpu().numpy(),
                     sin.uniforms.cpu().numpy(), ctx0)
+            elif tree_acc:
+                ra, rn, rp, rc, _ = oracle.accept_tree(w.logits.cpu(), w.draft.cpu(), w.parents(),
+                                                       ctx0)
             else:
                 ra, rn, rc = oracle.accept_prefix(w.logits.cpu(), w.draft.cpu(), ctx0)
             acc_ok = (np.array_equal(acc_out.cpu().numpy(), ra)
                       and np.array_equal(nxt_out.cpu().numpy(), rn)
                       and np.array_equal(ctx_scratch.cpu().numpy(), rc))
+            if rp is not None:
+                acc_ok = acc_ok and np.array_equal(path_out.cpu().numpy(), rp)
+                # the compacted rows: after the step's append node i's rows are
+                # k_new / v_new[b, i] (one-byte caches: the oracle's codes and
+                # scale of that row); the oracle's branch says which node each
+                # position base+1+j must now hold (every layer)
+                comp_ok = True
+                bt_h = w.block_tables.cpu().numpy()
+                for l in range(L):
+                    news = (w.k_new[l].cpu(), w.v_new[l].cpu())
+                    if q8:
+                        caches = (qk[l].cpu(), qv[l].cpu())
+                        scales = (sk[l].cpu(), sv[l].cpu())
+                    else:
+                        caches = (w.k_cache[l].cpu(), w.v_cache[l].cpu())
+                    for b in range(w.B):
+                        base = int(rc[b]) - 1 - int(ra[b])
+                        for j in range(int(ra[b])):
+                            pos = base + 1 + j
+                            blk, row = int(bt_h[b, pos // 16]), pos % 16
+                            node = int(rp[b, j])
+                            for c, cache in enumerate(caches):
+                                src = news[c][b, node]  # [K, H]
+                                if not q8:
+                                    comp_ok &= torch.equal(cache[blk, row].view(torch.int16),
+                                                           src.view(torch.int16))
+                                    continue
+                                for kh in range(w.K):
+                                    codes, scale = oracle.quantize_row(src[kh], w.dtype, args.kv)
+                                    comp_ok &= bool(np.array_equal(
+                                        cache[blk, row, kh].numpy(), codes)
+                                        and float(scales[c][blk, kh, row]) == scale)
+                parity["compaction_bit_exact"] = bool(comp_ok)
+                acc_ok = acc_ok and comp_ok
             parity["accept_bit_exact"] = bool(acc_ok)
             parity["parity_pass"] = bool(parity["parity_pass"] and acc_ok)
 
@@ -619,6 +676,12 @@ def run_ours(args, world, rank, local):
         from gqa_decode_attention_02_gb300 import analytic as A
 
         acc_b = A.accept_sampled_bytes(acc_out.cpu().numpy(), w.T, V)
+    elif tree_acc:
+        from gqa_decode_attention_02_gb300 import analytic as A
+
+        acc_b = (A.accept_tree_bytes(w.B, w.T, V)
+                 + L * A.kv_compact_bytes(acc_out.cpu().numpy(), w.K, w.H, 1 if q8 else 2, w.T,
+                                          scale_bytes=4 if q8 else 0))
     bytes_step = L * (attn_b + app_b) + acc_b
     step_ms_max, value = combine_ranks(step_ms, bytes_step, world, dev)
     peak, peak_src = measured_peak()
@@ -649,13 +712,16 @@ def run_ours(args, world, rank, local):
                 h_in.append(t.cpu().pin_memory())
                 d_in.append(t)
         elif has_acc:
-            for t in (w.logits, w.draft):
+            for t in (w.logits, w.draft) + ((parents_d,) if tree_acc else ()):
                 h_in.append(t.cpu().pin_memory())
                 d_in.append(t)
         if has_acc:
             h_acc = [torch.empty(w.B, dtype=torch.int32).pin_memory() for _ in range(2)]
+            if tree_acc:
+                h_acc.append(torch.empty_like(path_out, device="cpu").pin_memory())
         h2d = sum(t.numel() * t.element_size() for t in h_in + h_meta)
-        d2h = sum(t.numel() * t.element_size() for t in h_out) + (8 * w.B if has_acc else 0)
+        d2h = (sum(t.numel() * t.element_size() for t in h_out)
+               + (sum(t.numel() * t.element_size() for t in h_acc) if has_acc else 0))
 
         def e2e_step(use_graph):
             for d, h in zip(d_in + d_meta, h_in + h_meta):
@@ -671,6 +737,8 @@ def run_ours(args, world, rank, local):
             if has_acc:
                 h_acc[0].copy_(acc_out, non_blocking=True)
                 h_acc[1].copy_(nxt_out, non_blocking=True)
+                if tree_acc:
+                    h_acc[2].copy_(path_out, non_blocking=True)
 
         for use_graph in (True, False):
             for _ in range(2):
@@ -732,6 +800,8 @@ def run_ours(args, world, rank, local):
             "accept": ("none" if not has_acc else
                        "stochastic (speculative sampling) over fp32 probabilities [B,T,V] and "
                        "[B,T-1,V], seeded Dirichlet rows" if sampled else
+                       "greedy over the draft tree (fp32 logits [B,T,V]), then compaction of "
+                       "the kept branch's cache rows" if tree_acc else
                        "greedy longest prefix over fp32 logits [B,T,V]"),
             "append": ("fused into the attention launch" if fused else
                        "separate kv_append launches" if w.appended else "none"),
@@ -766,7 +836,7 @@ def run_ours(args, world, rank, local):
         "e2e_eager": e2e_eager,
         # the tensor-memory kernel's fused form is a kv_append launch + the attention launch
         "gpu_launches": K * ((L if w.appended and (not fused or engine == "tmem") else 0) + L
-                             + (1 if has_acc else 0)),
+                             + (1 if has_acc else 0) + (L if tree_acc else 0)),
         "clocks": clk,
         "wall_s_timed": round(wall, 4),
     }

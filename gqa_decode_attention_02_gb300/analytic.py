@@ -103,6 +103,21 @@ def accept_bytes(B: int, T: int, V: int) -> int:
     return B * T * V * 4 + B * max(T - 1, 0) * 4 + 3 * 4 * B
 
 
+def accept_tree_bytes(B: int, T: int, V: int) -> int:
+    """Tree acceptance: read the fp32 logits, drafts and parent entries;
+    write accepted / next token / the branch and read-write the lengths."""
+    return B * T * V * 4 + B * max(T - 1, 0) * 4 + B * T * 4 + 4 * B * (T - 1 + 4)
+
+
+def kv_compact_bytes(accepted, K: int, H: int, elem_bytes: int = 2, T: int = 1,
+                     scale_bytes: int = 0) -> int:
+    """Compaction after tree acceptance: every kept node's K and V rows (and a
+    one-byte row's scale) read and written once, plus the branch, the count
+    and the length per sequence."""
+    rows = int(sum(int(a) for a in accepted))
+    return rows * 2 * 2 * K * (H * elem_bytes + scale_bytes) + len(accepted) * 4 * (T - 1 + 2)
+
+
 def accept_sampled_bytes(accepted, T: int, V: int) -> int:
     """Bytes stochastic acceptance must move, given the accepted counts: per
     sequence the T fp64 uniforms and T-1 draft ids, q(x) and p(x) of every draft

@@ -256,12 +256,15 @@ SPECS = {
         B=32, T=1, N=32, K=8, H=128, dtype="bf16", layers=6, shuffle=True,
         append=True, ctx=("fixed", 8192), seed=106, windows=(1024,) * 5 + (0,)),
     # Not one of the five: tree verification of a 26-node draft tree (a root,
-    # then 3, 6, 8 and 8 candidates per level) on the verify geometry.
+    # then 3, 6, 8 and 8 candidates per level) on the verify geometry, then
+    # greedy acceptance over the tree and compaction of the kept branch.
     "tree": dict(
         desc="tree verify, B=16, T=26 (draft tree: 1 root, 3, 6, 8, 8 nodes per level), "
-             "N=64, K=8, H=128, bf16, context U[512,4096], custom mask among the new tokens",
+             "N=64, K=8, H=128, bf16, context U[512,4096], custom mask among the new tokens; "
+             "greedy acceptance over the tree (fp32 logits [16,26,32000]) and compaction "
+             "of the kept branch's cache rows",
         B=16, T=26, N=64, K=8, H=128, dtype="bf16", layers=1, shuffle=True,
-        append=True, ctx=("uniform", 512, 4096), seed=107,
+        append=True, ctx=("uniform", 512, 4096), seed=107, vocab=32000,
         tree=(-1, 0, 0, 0, 1, 1, 2, 2, 3, 3) + tuple(4 + i // 2 for i in range(8))
         + tuple(10 + i for i in range(8))),
 }
