@@ -127,3 +127,17 @@ def test_one_byte_cache_bytes_by_hand():
                                       kv_elem_bytes=1, row_scale_bytes=4)
     assert b == 100 * 2 * 2 * 132 + 2 * 1 * 8 * 128 * 2 + 4 * 7 + 4
     assert A.kv_append_quant_bytes(3, 1, 2, 128, 2) == 2 * 3 * 2 * (256 + 128 + 4) + 12 + 12
+
+
+def test_tree_acceptance_and_compaction_bytes_by_hand():
+    # B=2 sequences of a 26-node tree over V=1000: logits, 25 drafts and 26
+    # parent entries each; accepted / next token / length read and written and
+    # a 25-entry branch out
+    assert A.accept_tree_bytes(2, 26, 1000) == (2 * 26 * 1000 * 4 + 2 * 25 * 4 + 2 * 26 * 4
+                                                + 2 * 4 * (25 + 4))
+    # compaction of 3 + 0 kept nodes, K=8, H=128: each row of K and V read and
+    # written once (bf16), plus the branch and two ints per sequence
+    assert A.kv_compact_bytes([3, 0], 8, 128, 2, 26) == (3 * 2 * 2 * 8 * 128 * 2
+                                                         + 2 * 4 * (25 + 2))
+    # one-byte rows carry their fp32 scale
+    assert A.kv_compact_bytes([1], 2, 128, 1, 4, scale_bytes=4) == 2 * 2 * 2 * 132 + 4 * 5
