@@ -262,3 +262,29 @@ def test_compaction_checks_leave_the_sequence_untouched():
     _, _, _, _, err = oracle.kv_compact(w.k_cache[0], w.v_cache[0], w.block_tables, ctx, path,
                                         np.array([8, 0, 2], np.int32), w.T)
     assert list(err) == [11, 0, 0]
+
+
+def test_tree_workload_keeps_at_least_its_planted_branch():
+    """The tree workload's recipe plants one branch per sequence whose every
+    edge carries the target's choice; the kept branch is at least that deep,
+    and a kept branch's edges all agree with the target (checked edge by edge
+    with numpy's first-max argmax; the rows hold no NaN)."""
+    from gqa_decode_attention_02_gb300 import workloads
+
+    w = workloads.make("tree", B=6)
+    par = w.parents()
+    acc, nxt, path, _, err = oracle.accept_tree(w.logits, w.draft, par)
+    assert (err == 0).all()
+    lg = w.logits.numpy()
+    dr = w.draft.numpy()
+    for b in range(w.B):
+        depth, node = 0, int(w.draft_k[b])
+        while node > 0:
+            depth, node = depth + 1, int(par[b, node])
+        assert acc[b] >= depth
+        prev = 0
+        for j in range(acc[b]):
+            c = int(path[b, j])
+            assert par[b, c] == prev and dr[b, c - 1] == int(np.argmax(lg[b, prev]))
+            prev = c
+        assert nxt[b] == int(np.argmax(lg[b, prev]))
