@@ -99,7 +99,7 @@ gqa_status attention_entry(const gqa_shape* s, bool decode_only, bool fused, con
 
 extern "C" {
 
-int gqa_version(void) { return 100; }
+int gqa_version(void) { return 200; }
 
 const char* gqa_status_string(int status) {
     switch (status) {
