@@ -2,7 +2,7 @@
  * gqa_decode.h -- C ABI of the paged grouped-query decode-attention library
  * (hand-written CUDA for sm_103a / GB300).
  *
- * Four operations on a paged KV cache, all asynchronous on the caller's stream:
+ * Operations on a paged KV cache, all asynchronous on the caller's stream:
  *   gqa_kv_append        write the T newest tokens' keys and values into the cache
  *   gqa_decode_attention attention of one new query token per sequence (T == 1)
  *   gqa_verify_attention the same for T >= 1 new tokens, causal among them
@@ -14,6 +14,8 @@
  *                        in one call; gqa_tree_verify_attention_quant
  *   gqa_accept_sampled   stochastic acceptance of draft tokens (speculative
  *                        sampling: modified rejection sampling)
+ *   gqa_accept_tree      greedy acceptance over a draft tree, and
+ *   gqa_kv_compact       the kept branch's cached rows moved behind its root
  *
  * Sources (web pages, cited by title and section):
  *   "CS336, лекции 10 и 12: инференс и оценка моделей" (CS336 lectures 10/12,
@@ -28,8 +30,10 @@
  *     and the speculative-decoding section (greedy acceptance).
  *   "Болжау арқылы Sonar модельдерін жылдамдату" (Accelerating Sonar through
  *     speculation): §"Спекулятивті кодтан шығару" (longest accepted prefix plus
- *     one target token) and §"Спекулятивті кодтан шығару арқылы инференс"
- *     (appending accepted tokens on the GPU, avoiding a GPU->CPU sync).
+ *     one target token), §"Спекулятивті кодтан шығару арқылы инференс"
+ *     (appending accepted tokens on the GPU, avoiding a GPU->CPU sync) and
+ *     §"EAGLE" (draft trees verified under a custom attention mask; the
+ *     longest agreeing branch kept).
  *
  * Conventions for every entry point
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except the
